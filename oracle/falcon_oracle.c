@@ -1,0 +1,235 @@
+/*
+ * falcon_oracle.c -- fp64 CPU oracle for the Falcon-1 / Falcon-1A fast-weight
+ * recurrences of "Fast Weight Attention for Continual Learning".
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, token-by-token
+ * definition of what the GPU library computes.  Only the tests, the smoke
+ * check and the benchmark's CPU-baseline leg may load it.  It shares no code,
+ * header, table or helper with the CUDA library, and it never calls it.
+ *
+ * Everything is double precision.  Inputs are the already-rounded values the
+ * GPU sees (bf16 or fp32 widened exactly to fp64 by the caller).
+ *
+ * Passages followed (page hyper.ai/fr/papers/2608.27763 unless noted):
+ *   - shifted write stream x_1 = 0, x_t = phi(k_{t-1}): Section 2.2, Eq. (2.3)
+ *     and the "Naming and formula summary" at the head of Section 4;
+ *   - boundary sentinel eta_1 = 0 (so alpha_1 = 0, gamma_1 = 1): Section 3,
+ *     "Indexing and causality conventions";
+ *   - NLMS step eta_t = beta_t / (||x_t||^2 + lambda_t + eps), eta := 0 when
+ *     the denominator is 0: Section 3.1, Eq. (3.4);
+ *   - Falcon-1 update S_t = (1 - eta lambda) S_{t-1} + eta x_t r_t^T with
+ *     r_t = v_t - S_{t-1}^T x_t: Section 3.1, Eq. (3.3) and Section 4 summary;
+ *   - Falcon-1A update S_t = (1 - eta lambda) S_{t-1} + eta x_t v_t^T with
+ *     E_t = ||x_t||^2: Section 4.3, Eq. (4.6) and (4.8);
+ *   - positive-decay clamp alpha = min(eta lambda, 1 - eps_gamma),
+ *     gamma = 1 - alpha: Section 4.3 "Decay positivity" and Section 4.4
+ *     (the clamped recurrence is the implemented one);
+ *   - read after write o_t = S_t^T phi(q_t): Section 4 summary;
+ *   - one-step pseudocode with the same order of operations: page
+ *     rcap.io/posts/fast-weight-attention-for-continual-learning-2026-08-27.
+ *
+ * Readings where the pages are silent:
+ *   - phi is either the identity or the l2 normalisation u / max(||u||, 1e-12)
+ *     ("QK-l2" in the experiment tables of page juhoplayground.github.io);
+ *   - a caller that carries state across calls passes x_prev = phi(k_T) of the
+ *     previous segment; then step 1 writes with x_1 = x_prev (no sentinel).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_FALCON1 1  /* regression rule, Eq. (3.3) */
+#define ORACLE_FALCON1A 2 /* inner-product rule, Eq. (4.6) */
+#define ORACLE_PHI_IDENTITY 0
+#define ORACLE_PHI_L2 1
+
+/* phi applied to one m-vector (Section 2.2 feature map; l2 variant). */
+static void feature_map(int phi, int m, const double *u, double *out) {
+  if (phi == ORACLE_PHI_L2) {
+    double ss = 0.0;
+    for (int i = 0; i < m; ++i) ss += u[i] * u[i];
+    double nrm = sqrt(ss);
+    if (nrm < 1e-12) nrm = 1e-12;
+    for (int i = 0; i < m; ++i) out[i] = u[i] / nrm;
+  } else {
+    for (int i = 0; i < m; ++i) out[i] = u[i];
+  }
+}
+
+/* eta_t and gamma_t of one step (Eq. (3.4) and the decay clamp). */
+static void step_scalars(int sentinel, int m, const double *x, double beta,
+                         double lambda, double eps, double eps_gamma,
+                         double *eta_out, double *gamma_out) {
+  double eta = 0.0;
+  if (!sentinel) {
+    double E = 0.0;
+    for (int i = 0; i < m; ++i) E += x[i] * x[i];
+    double den = E + lambda + eps;
+    eta = (den > 0.0) ? beta / den : 0.0;
+  }
+  double alpha = eta * lambda;
+  if (alpha > 1.0 - eps_gamma) alpha = 1.0 - eps_gamma;
+  *eta_out = eta;
+  *gamma_out = 1.0 - alpha;
+}
+
+/* One token of the recurrence on one head.  S is m x dv row-major, updated in
+ * place.  x is the write feature of this step; qf = phi(q_t).  Writes o_t. */
+static void one_token(int rule, int m, int dv, double *S, const double *x,
+                      const double *qf, const double *v, double eta,
+                      double gamma, double *r /* dv scratch */, double *o) {
+  if (rule == ORACLE_FALCON1) {
+    /* r_t = v_t - S_{t-1}^T x_t  (prediction from the pre-update state) */
+    for (int j = 0; j < dv; ++j) {
+      double pred = 0.0;
+      for (int i = 0; i < m; ++i) pred += S[(int64_t)i * dv + j] * x[i];
+      r[j] = v[j] - pred;
+    }
+  } else {
+    /* Falcon-1A writes the target itself */
+    for (int j = 0; j < dv; ++j) r[j] = v[j];
+  }
+  /* S_t = gamma S_{t-1} + eta x_t r_t^T */
+  for (int i = 0; i < m; ++i)
+    for (int j = 0; j < dv; ++j)
+      S[(int64_t)i * dv + j] = gamma * S[(int64_t)i * dv + j] + eta * x[i] * r[j];
+  /* o_t = S_t^T phi(q_t)  (read after write) */
+  for (int j = 0; j < dv; ++j) {
+    double acc = 0.0;
+    for (int i = 0; i < m; ++i) acc += S[(int64_t)i * dv + j] * qf[i];
+    o[j] = acc;
+  }
+}
+
+typedef struct {
+  int rule, m, dv, phi;
+  int64_t T;
+  double eps, eps_gamma;
+  const double *q, *k, *v, *beta, *lambda, *S0, *x_prev;
+  double *o, *S_out, *x_last, *S_traj;
+} fwd_args;
+
+/* The whole sequence of one head (b, h). */
+static void forward_head(const fwd_args *a, int64_t bh) {
+  const int m = a->m, dv = a->dv;
+  const int64_t T = a->T;
+  double *S = (double *)calloc((size_t)m * dv, sizeof(double));
+  double *x = (double *)calloc((size_t)m, sizeof(double));
+  double *qf = (double *)malloc(sizeof(double) * (size_t)m);
+  double *r = (double *)malloc(sizeof(double) * (size_t)dv);
+  if (a->S0) memcpy(S, a->S0 + bh * m * dv, sizeof(double) * (size_t)m * dv);
+  int sentinel = 1;
+  if (a->x_prev) {
+    memcpy(x, a->x_prev + bh * m, sizeof(double) * (size_t)m);
+    sentinel = 0;
+  }
+  for (int64_t t = 0; t < T; ++t) {
+    const int64_t row = bh * T + t;
+    double eta, gamma;
+    step_scalars(sentinel && t == 0, m, x, a->beta[row], a->lambda[row],
+                 a->eps, a->eps_gamma, &eta, &gamma);
+    feature_map(a->phi, m, a->q + row * m, qf);
+    one_token(a->rule, m, dv, S, x, qf, a->v + row * dv, eta, gamma, r,
+              a->o + row * dv);
+    if (a->S_traj)
+      memcpy(a->S_traj + row * m * dv, S, sizeof(double) * (size_t)m * dv);
+    /* the next step writes under phi(k_t) */
+    feature_map(a->phi, m, a->k + row * m, x);
+  }
+  if (a->S_out) memcpy(a->S_out + bh * m * dv, S, sizeof(double) * (size_t)m * dv);
+  if (a->x_last) memcpy(a->x_last + bh * m, x, sizeof(double) * (size_t)m);
+  free(S);
+  free(x);
+  free(qf);
+  free(r);
+}
+
+typedef struct {
+  const fwd_args *a;
+  int64_t begin, end;
+} fwd_slice;
+
+static void *forward_worker(void *p) {
+  const fwd_slice *s = (const fwd_slice *)p;
+  for (int64_t bh = s->begin; bh < s->end; ++bh) forward_head(s->a, bh);
+  return NULL;
+}
+
+/*
+ * Whole-sequence forward for all B*H heads.  Layouts (row-major):
+ *   q, k: [BH, T, m]   v, o: [BH, T, dv]   beta, lambda: [BH, T]
+ *   S0 (nullable => zeros), S_out: [BH, m, dv]
+ *   x_prev (nullable => sentinel), x_last (nullable): [BH, m]
+ *   S_traj (nullable): [BH, T, m, dv], the state after every token.
+ * Heads are independent; they are split over nthreads POSIX threads.
+ * Returns 0, or -1 on a bad argument.
+ */
+int falcon_oracle_forward(int rule, int64_t BH, int64_t T, int m, int dv,
+                          int phi, double eps, double eps_gamma,
+                          const double *q, const double *k, const double *v,
+                          const double *beta, const double *lambda,
+                          const double *S0, const double *x_prev, double *o,
+                          double *S_out, double *x_last, double *S_traj,
+                          int nthreads) {
+  if (rule != ORACLE_FALCON1 && rule != ORACLE_FALCON1A) return -1;
+  if (BH < 0 || T < 0 || m <= 0 || dv <= 0) return -1;
+  fwd_args a = {rule, m, dv, phi, T, eps, eps_gamma, q, k, v, beta, lambda,
+                S0, x_prev, o, S_out, x_last, S_traj};
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > BH) nthreads = (int)(BH > 0 ? BH : 1);
+  pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+  fwd_slice *sl = (fwd_slice *)malloc(sizeof(fwd_slice) * (size_t)nthreads);
+  for (int w = 0; w < nthreads; ++w) {
+    sl[w].a = &a;
+    sl[w].begin = BH * w / nthreads;
+    sl[w].end = BH * (w + 1) / nthreads;
+  }
+  for (int w = 1; w < nthreads; ++w) pthread_create(&tid[w], NULL, forward_worker, &sl[w]);
+  forward_worker(&sl[0]);
+  for (int w = 1; w < nthreads; ++w) pthread_join(tid[w], NULL);
+  free(tid);
+  free(sl);
+  return 0;
+}
+
+/*
+ * One recurrent decode step for N independent states (the same token update
+ * as above, applied once).  Layouts:
+ *   q, k: [N, m]   v, o: [N, dv]   beta, lambda: [N]
+ *   S: [N, m, dv], updated in place.
+ *   x_prev: [N, m], read as this step's write feature, then overwritten with
+ *           phi(k) for the next step.
+ *   fresh (nullable): [N] bytes; nonzero marks the first token of a sequence,
+ *           where the sentinel applies (x = 0, eta = 0).
+ */
+int falcon_oracle_decode_step(int rule, int64_t N, int m, int dv, int phi,
+                              double eps, double eps_gamma, const double *q,
+                              const double *k, const double *v,
+                              const double *beta, const double *lambda,
+                              double *S, double *x_prev,
+                              const unsigned char *fresh, double *o) {
+  if (rule != ORACLE_FALCON1 && rule != ORACLE_FALCON1A) return -1;
+  if (N < 0 || m <= 0 || dv <= 0) return -1;
+  double *x = (double *)malloc(sizeof(double) * (size_t)m);
+  double *qf = (double *)malloc(sizeof(double) * (size_t)m);
+  double *r = (double *)malloc(sizeof(double) * (size_t)dv);
+  for (int64_t n = 0; n < N; ++n) {
+    const int sentinel = fresh ? (fresh[n] != 0) : 0;
+    if (sentinel)
+      memset(x, 0, sizeof(double) * (size_t)m);
+    else
+      memcpy(x, x_prev + n * m, sizeof(double) * (size_t)m);
+    double eta, gamma;
+    step_scalars(sentinel, m, x, beta[n], lambda[n], eps, eps_gamma, &eta, &gamma);
+    feature_map(phi, m, q + n * m, qf);
+    one_token(rule, m, dv, S + n * m * dv, x, qf, v + n * dv, eta, gamma, r,
+              o + n * dv);
+    feature_map(phi, m, k + n * m, x_prev + n * m);
+  }
+  free(x);
+  free(qf);
+  free(r);
+  return 0;
+}
