@@ -1,0 +1,397 @@
+"""Benchmark: Falcon-1 chunked forward, B8 H12 T2048 d64 bf16 (tokens/s).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step is one pass of the whole hot path over one batch: the Falcon-1
+chunk-parallel forward on the B=8, H=12, T=2048, m=dv=64, bf16 workload
+(tokens = B*T per step), inputs resident in HBM.  Under torchrun every rank
+runs the same per-rank workload on its own GPU (independent problems, no
+data-path collective: weak scaling); the time is the max over ranks.
+
+The line also carries
+  e2e          the same metric through the public API from pinned host
+               buffers, with host->device inputs and device->host outputs
+               inside the timed region;
+  roofline     achieved algorithmic HBM bytes per launch / launch time of
+               the dominant kernel against the measured copy bandwidth;
+  cpu_baseline the fp64 oracle on this host's cores on a bounded sample;
+  also         the other workloads (Falcon-1A, long context, decode).
+
+`--impl reference` times the fp64 CPU oracle (the only reference this method
+has) on the same workload, a bounded sample per step.
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from delta_rule_attention_gb300 import workloads  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+METRIC = "Falcon-1 chunked fwd tokens/s (B8 H12 T2048 d64 bf16) and % of roofline"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"], "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+def algorithmic_bytes(w, with_S0=False):
+    """Bytes one chunked-forward call must move: q, k, v read, beta, lambda
+    read, o written, S_T (and x_last) written, S0 read if given."""
+    es = torch.finfo(w.dtype).bits // 8
+    BH = w.B * w.H
+    b = BH * w.T * (2 * w.m + w.dv) * es + BH * w.T * 8 + BH * w.T * w.dv * es
+    b += BH * w.m * w.dv * 4 + BH * w.m * 4
+    if with_S0:
+        b += BH * w.m * w.dv * 4
+    return b
+
+
+def algorithmic_flops(w):
+    """Triangle-aware flops of the chunk form per call (Falcon-1), per chunk
+    and head: C(C-1)m (X X^T) + C(C+1)m (Q X^T) + C^3/3 (solve) + C^2 (m+dv)
+    (T X, T V) + 6 C m dv (state products) + C(C+1) dv (P U)."""
+    C, m, dv = w.chunk, w.m, w.dv
+    per = C * (C - 1) * m + C * (C + 1) * m + C ** 3 / 3 + C * C * (m + dv) + 6 * C * m * dv \
+        + C * (C + 1) * dv
+    if w.rule == "falcon1a":
+        per = C * (C + 1) * (m + dv) + 4 * C * m * dv
+    return per * w.B * w.H * ((w.T + C - 1) // C)
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no_samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def barrier(ws):
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x, ws):
+    if ws > 1:
+        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+    return x
+
+
+def input_sets(w, n_sets, device):
+    """n_sets independent copies of the workload (different seeds) so that
+    consecutive timed steps never find their inputs in L2."""
+    sets = []
+    for s in range(n_sets):
+        sets.append(workloads.generate(dataclasses.replace(w, seed=w.seed + 1000 * s),
+                                       device=device))
+    return sets
+
+
+def time_device(fn, sets, steps, warmup, ws):
+    """Run fn(set) for warmup + steps steps; time exactly `steps` on the
+    device with events on the current stream, barrier + sync both sides."""
+    for i in range(warmup):
+        fn(sets[i % len(sets)])
+    torch.cuda.synchronize()
+    barrier(ws)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for i in range(steps):
+        fn(sets[i % len(sets)])
+    ev1.record()
+    torch.cuda.synchronize()
+    barrier(ws)
+    torch.cuda.synchronize()
+    return ev0.elapsed_time(ev1) / 1e3
+
+
+def run_ours(args):
+    import delta_rule_attention_gb300 as falcon
+    import numpy as np
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    w = workloads.LM
+    per_set = algorithmic_bytes(w)
+    n_sets = max(2, -(-2 * L2_BYTES // per_set) + 1)
+    sets = input_sets(w, n_sets, dev)
+    outs = [(torch.empty((w.B, w.H, w.T, w.dv), dtype=w.dtype, device=dev),
+             torch.empty((w.B, w.H, w.m, w.dv), dtype=torch.float32, device=dev),
+             torch.empty((w.B, w.H, w.m), dtype=torch.float32, device=dev))
+            for _ in range(n_sets)]
+    shape = falcon.make_shape(w.B, w.H, w.T, w.m, w.dv, w.chunk, w.dtype, w.phi, w.eps,
+                              w.eps_gamma)
+    ws_bytes = falcon.falcon_workspace_bytes(shape)
+    workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    launches_per_step = 2
+    counter = {"i": 0}
+
+    def step(x):
+        i = counter["i"] % n_sets
+        counter["i"] += 1
+        o, S, xl = outs[i]
+        falcon.falcon1_fwd_chunked(x["q"], x["k"], x["v"], x["beta"], x["lambda"],
+                                   chunk=w.chunk, phi=w.phi, eps=w.eps, eps_gamma=w.eps_gamma,
+                                   o=o, S_out=S, x_last=xl, workspace=workspace)
+
+    # Calibrate the step count so the timed region lasts ~3 s unless given.
+    for i in range(3):
+        step(sets[i % n_sets])
+    torch.cuda.synchronize()
+    steps = args.steps
+    if steps is None:
+        t = time_device(step, sets, 20, 0, 1)
+        steps = int(min(200000, max(100, 3.0 / max(t / 20, 1e-7))))
+    with ClockSampler(local) as clk:
+        secs = time_device(step, sets, steps, args.warmup, ws)
+    secs = max_over_ranks(secs, ws)
+    assert falcon.falcon_sync_check() == 0
+    ms = secs * 1e3 / steps
+    value = w.tokens * ws * steps / secs
+
+    # e2e: public API from pinned host buffers, H2D inputs + D2H outputs timed.
+    host = {n: t.cpu().pin_memory() for n, t in sets[0].items()}
+    o_h = torch.empty((w.B, w.H, w.T, w.dv), dtype=w.dtype).pin_memory()
+    S_h = torch.empty((w.B, w.H, w.m, w.dv), dtype=torch.float32).pin_memory()
+    dx = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
+
+    def e2e_step(_):
+        for n in dx:
+            dx[n].copy_(host[n], non_blocking=True)
+        o, S, xl = outs[0]
+        falcon.falcon1_fwd_chunked(dx["q"], dx["k"], dx["v"], dx["beta"], dx["lambda"],
+                                   chunk=w.chunk, phi=w.phi, eps=w.eps, eps_gamma=w.eps_gamma,
+                                   o=o, S_out=S, x_last=xl, workspace=workspace)
+        o_h.copy_(o, non_blocking=True)
+        S_h.copy_(S, non_blocking=True)
+
+    e2e_steps = max(10, min(steps, 200))
+    e2e_secs = max_over_ranks(time_device(e2e_step, [None], e2e_steps, 3, ws), ws)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = o_h.numel() * o_h.element_size() + S_h.numel() * S_h.element_size()
+
+    pk = peaks()
+    achieved = per_set / (secs / steps) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) q,k,v; "
+        "beta=2*sigmoid(n), lambda=softplus(n-3))",
+        "config": {"workload": w.name, "rule": w.rule, "B": w.B, "H": w.H, "T": w.T, "m": w.m,
+                   "dv": w.dv, "chunk": w.chunk, "phi": w.phi, "tokens_per_step": w.tokens,
+                   "l2": f"{n_sets} rotating input sets of {per_set / 1e6:.1f} MB (> L2)",
+                   "parallelism": f"replica x{ws} (independent batches, no collective)"},
+        "clocks": clk.summary(),
+        "e2e": {"value": w.tokens * ws * e2e_steps / e2e_secs, "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * (steps + 0),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": None,
+                     "peak_source": pk["source"],
+                     "kernel": "whole step (chunk_prep_kernel + chunk_scan_kernel)",
+                     "bytes_per_launch": per_set},
+        "flops_per_step": algorithmic_flops(w),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
+    if rank == 0 and not args.no_extra:
+        line["also"] = extra_workloads(falcon, dev)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line))
+
+
+def extra_workloads(falcon, dev):
+    """The other workloads, timed the same way (device-resident inputs)."""
+    out = []
+    pk = peaks()
+    for w, steps in ((workloads.LM_1A, 200), (workloads.LONG, 5)):
+        sets = input_sets(w, 2 if w is workloads.LM_1A else 1, dev)
+        fn = falcon.falcon1_fwd_chunked if w.rule == "falcon1" else falcon.falcon1a_fwd_chunked
+        o = torch.empty((w.B, w.H, w.T, w.dv), dtype=w.dtype, device=dev)
+        S = torch.empty((w.B, w.H, w.m, w.dv), dtype=torch.float32, device=dev)
+        shape = falcon.make_shape(w.B, w.H, w.T, w.m, w.dv, w.chunk, w.dtype, w.phi)
+        wsb = torch.empty(max(falcon.falcon_workspace_bytes(shape), 1), dtype=torch.uint8,
+                          device=dev)
+
+        def step(x):
+            fn(x["q"], x["k"], x["v"], x["beta"], x["lambda"], chunk=w.chunk, phi=w.phi,
+               o=o, S_out=S, workspace=wsb, want_x_last=False)
+        secs = time_device(step, sets, steps, 2, 1)
+        b = algorithmic_bytes(w)
+        out.append({"workload": w.name, "tokens_per_s": w.tokens * steps / secs,
+                    "ms_per_call": secs * 1e3 / steps,
+                    "hbm_frac": b / (secs / steps) / 1e9 / pk["hbm_gbs"]})
+        del sets
+    # decode: rotating per-step inputs, state resident
+    d = workloads.DECODE
+    stream = workloads.DecodeStream(d, device=dev)
+    S = stream.initial_state()
+    xp = torch.zeros((d.N, d.m), device=dev)
+    steps_in = [stream.step() for _ in range(8)]
+    o = torch.empty((d.N, d.dv), dtype=d.dtype, device=dev)
+
+    def dstep(x):
+        falcon.falcon1_decode_step(x["q"], x["k"], x["v"], x["beta"], x["lambda"], S, xp,
+                                   phi=d.phi, o=o)
+    n = 512
+    secs = time_device(dstep, steps_in, n, 4, 1)
+    state_bytes = 2 * d.N * d.m * d.dv * 4
+    step_bytes = state_bytes + d.N * ((2 * d.m + 2 * d.dv) * 2 + 8 + 2 * d.m * 4)
+    out.append({"workload": d.name, "tokens_per_s": d.N * n / secs,
+                "us_per_step": secs * 1e6 / n,
+                "hbm_frac": step_bytes / (secs / n) / 1e9 / pk["hbm_gbs"]})
+    return out
+
+
+def cpu_baseline(w, budget_s=12.0, reps_max=20):
+    """The fp64 oracle on this host's cores: whole LM workload per rep (all
+    heads), repeated until ~budget_s of CPU time."""
+    import oracle
+    x = workloads.generate(w, device="cpu")
+    cores = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.forward(w.rule, x["q"], x["k"], x["v"], x["beta"], x["lambda"], phi=w.phi,
+                       eps=w.eps, eps_gamma=w.eps_gamma, threads=cores)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el > budget_s or reps >= reps_max:
+            break
+    return {"value": w.tokens * reps / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{reps} x full {w.name} (all {w.B * w.H} heads, fp64, {cores} threads)"}
+
+
+def run_reference(args):
+    """The fp64 oracle timed on the host cores, one bounded sample per step
+    (batch element 0: all 12 heads, T = 2048), rank 0 only."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    w = workloads.LM
+    x = workloads.generate(w, device="cpu")
+    sub = {n: t[:1].contiguous() for n, t in x.items()}
+    cores = os.cpu_count() or 1
+    steps = args.steps if args.steps is not None else 20
+
+    def one():
+        oracle.forward(w.rule, sub["q"], sub["k"], sub["v"], sub["beta"], sub["lambda"],
+                       phi=w.phi, eps=w.eps, eps_gamma=w.eps_gamma, threads=cores)
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    secs = time.perf_counter() - t0
+    tokens = w.T * steps  # one batch element per step
+    value = tokens / secs
+    sample = f"batch element 0 of {w.name} (12 heads x 2048 tokens) per step, fp64"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": ws, "steps": steps, "warmup": args.warmup,
+            "ms_per_step": secs * 1e3 / steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "tokens_per_step": w.T},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

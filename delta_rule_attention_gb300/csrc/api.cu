@@ -1,0 +1,218 @@
+// C ABI of the library (declared in include/falcon.h): argument checks, the
+// zero-length cases, and dispatch to the kernels.  Nothing is launched when an
+// argument is rejected.
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace falcon {
+// Device error word: set by a kernel whose bounded wait gave up, read and
+// cleared by falcon_sync_check().
+static __device__ int g_device_error = 0;
+}  // namespace falcon
+
+namespace {
+
+using falcon::ChunkArgs;
+using falcon::DecodeArgs;
+
+bool misaligned(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+bool dim_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+
+// The kernels are built for sm_103a only.
+int check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FALCON_ERR_CUDA;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return FALCON_ERR_CUDA;
+  return (major == 10 && minor == 3) ? FALCON_OK : FALCON_ERR_DEVICE;
+}
+
+int check_common(int dtype, int phi, float eps, float eps_gamma) {
+  if (dtype != FALCON_BF16 && dtype != FALCON_F32) return FALCON_ERR_BAD_DTYPE;
+  if (phi != FALCON_PHI_IDENTITY && phi != FALCON_PHI_L2) return FALCON_ERR_BAD_DTYPE;
+  if (!(eps >= 0.f) || !(eps_gamma > 0.f) || !(eps_gamma < 1.f)) return FALCON_ERR_BAD_ARG;
+  return FALCON_OK;
+}
+
+int check_shape(const falcon_shape* s) {
+  if (!s) return FALCON_ERR_NULL_PTR;
+  if (s->B < 0 || s->H < 0 || s->T < 0) return FALCON_ERR_BAD_SHAPE;
+  if (!dim_ok(s->m) || !dim_ok(s->dv)) return FALCON_ERR_BAD_SHAPE;
+  if (s->chunk != 16 && s->chunk != 32 && s->chunk != 64) return FALCON_ERR_BAD_SHAPE;
+  // Grid limits: B*H CTAs along y of the prep grid, chunks along x.
+  if (s->B * s->H > 65535 || (s->T + s->chunk - 1) / s->chunk > 0x7fffffffLL)
+    return FALCON_ERR_BAD_SHAPE;
+  return check_common(s->dtype, s->phi, s->eps, s->eps_gamma);
+}
+
+int to_status(cudaError_t e) { return e == cudaSuccess ? FALCON_OK : FALCON_ERR_CUDA; }
+
+int fwd_chunked(int rule, const falcon_shape* s, const void* q, const void* k, const void* v,
+                const float* beta, const float* lambda, const float* S0, const float* x_prev,
+                void* o, float* S_out, float* x_last, void* workspace, size_t workspace_bytes,
+                cudaStream_t stream) {
+  int rc = check_shape(s);
+  if (rc) return rc;
+  const int64_t BH = s->B * s->H;
+  if (BH == 0) return FALCON_OK;
+  if (!S_out) return FALCON_ERR_NULL_PTR;
+  if (s->T > 0 && (!q || !k || !v || !beta || !lambda || !o)) return FALCON_ERR_NULL_PTR;
+  const void* ptrs[] = {q, k, v, beta, lambda, S0, x_prev, o, S_out, x_last};
+  for (const void* p : ptrs)
+    if (misaligned(p)) return FALCON_ERR_MISALIGNED;
+  const size_t need = falcon_workspace_bytes(s);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return FALCON_ERR_WORKSPACE;
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return FALCON_ERR_MISALIGNED;
+  rc = check_device();
+  if (rc) return rc;
+
+  const size_t state_bytes = sizeof(float) * (size_t)BH * s->m * s->dv;
+  if (s->T == 0) {  // nothing to run: S_T = S0, x_last = x_prev
+    cudaError_t e = cudaSuccess;
+    if (S0 && S0 != S_out)
+      e = cudaMemcpyAsync(S_out, S0, state_bytes, cudaMemcpyDeviceToDevice, stream);
+    else if (!S0)
+      e = cudaMemsetAsync(S_out, 0, state_bytes, stream);
+    if (e == cudaSuccess && x_last && x_prev && x_last != x_prev)
+      e = cudaMemcpyAsync(x_last, x_prev, sizeof(float) * (size_t)BH * s->m,
+                          cudaMemcpyDeviceToDevice, stream);
+    return to_status(e);
+  }
+  ChunkArgs a;
+  a.rule = rule;
+  a.BH = BH;
+  a.T = s->T;
+  a.m = s->m;
+  a.dv = s->dv;
+  a.C = s->chunk;
+  a.dtype = s->dtype;
+  a.phi = s->phi;
+  a.eps = s->eps;
+  a.eps_gamma = s->eps_gamma;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.beta = beta;
+  a.lambda = lambda;
+  a.S0 = S0;
+  a.x_prev = x_prev;
+  a.o = o;
+  a.S_out = S_out;
+  a.x_last = x_last;
+  a.workspace = workspace;
+  return to_status(falcon::launch_generic_chunked(a, stream));
+}
+
+int decode(int rule, int64_t N, int32_t m, int32_t dv, int32_t dtype, int32_t phi, float eps,
+           float eps_gamma, const void* q, const void* k, const void* v, const float* beta,
+           const float* lambda, float* S, float* x_prev, const uint8_t* fresh, void* o,
+           cudaStream_t stream) {
+  if (N < 0 || N > 0x7fffffffLL || !dim_ok(m) || !dim_ok(dv)) return FALCON_ERR_BAD_SHAPE;
+  int rc = check_common(dtype, phi, eps, eps_gamma);
+  if (rc) return rc;
+  if (N == 0) return FALCON_OK;
+  if (!q || !k || !v || !beta || !lambda || !S || !x_prev || !o) return FALCON_ERR_NULL_PTR;
+  const void* ptrs[] = {q, k, v, beta, lambda, S, x_prev, o};
+  for (const void* p : ptrs)
+    if (misaligned(p)) return FALCON_ERR_MISALIGNED;
+  rc = check_device();
+  if (rc) return rc;
+  DecodeArgs a;
+  a.rule = rule;
+  a.N = N;
+  a.m = m;
+  a.dv = dv;
+  a.dtype = dtype;
+  a.phi = phi;
+  a.eps = eps;
+  a.eps_gamma = eps_gamma;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.beta = beta;
+  a.lambda = lambda;
+  a.S = S;
+  a.x_prev = x_prev;
+  a.fresh = fresh;
+  a.o = o;
+  return to_status(falcon::launch_decode(a, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t falcon_workspace_bytes(const falcon_shape* s) {
+  if (check_shape(s) != FALCON_OK) return 0;
+  return falcon::generic_workspace_bytes(s->B * s->H, s->T, s->m, s->dv, s->chunk);
+}
+
+int falcon1_fwd_chunked(const falcon_shape* s, const void* q, const void* k, const void* v,
+                        const float* beta, const float* lambda, const float* S0,
+                        const float* x_prev, void* o, float* S_out, float* x_last,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return fwd_chunked(falcon::kFalcon1, s, q, k, v, beta, lambda, S0, x_prev, o, S_out, x_last,
+                     workspace, workspace_bytes, stream);
+}
+
+int falcon1a_fwd_chunked(const falcon_shape* s, const void* q, const void* k, const void* v,
+                         const float* beta, const float* lambda, const float* S0,
+                         const float* x_prev, void* o, float* S_out, float* x_last,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return fwd_chunked(falcon::kFalcon1A, s, q, k, v, beta, lambda, S0, x_prev, o, S_out, x_last,
+                     workspace, workspace_bytes, stream);
+}
+
+int falcon1_decode_step(int64_t N, int32_t m, int32_t dv, int32_t dtype, int32_t phi, float eps,
+                        float eps_gamma, const void* q, const void* k, const void* v,
+                        const float* beta, const float* lambda, float* S, float* x_prev,
+                        const uint8_t* fresh, void* o, cudaStream_t stream) {
+  return decode(falcon::kFalcon1, N, m, dv, dtype, phi, eps, eps_gamma, q, k, v, beta, lambda,
+                S, x_prev, fresh, o, stream);
+}
+
+int falcon1a_decode_step(int64_t N, int32_t m, int32_t dv, int32_t dtype, int32_t phi,
+                         float eps, float eps_gamma, const void* q, const void* k, const void* v,
+                         const float* beta, const float* lambda, float* S, float* x_prev,
+                         const uint8_t* fresh, void* o, cudaStream_t stream) {
+  return decode(falcon::kFalcon1A, N, m, dv, dtype, phi, eps, eps_gamma, q, k, v, beta, lambda,
+                S, x_prev, fresh, o, stream);
+}
+
+int falcon_sync_check(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FALCON_ERR_CUDA;
+  int flag = 0;
+  if (cudaMemcpyFromSymbol(&flag, falcon::g_device_error, sizeof(int)) != cudaSuccess)
+    return FALCON_ERR_CUDA;
+  if (flag) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(falcon::g_device_error, &zero, sizeof(int)) != cudaSuccess)
+      return FALCON_ERR_CUDA;
+    return FALCON_ERR_TIMEOUT;
+  }
+  return FALCON_OK;
+}
+
+const char* falcon_strerror(int code) {
+  switch (code) {
+    case FALCON_OK: return "ok";
+    case FALCON_ERR_NULL_PTR: return "a required pointer is NULL";
+    case FALCON_ERR_BAD_SHAPE: return "unsupported shape (m, dv in {16,32,64,128}; chunk in {16,32,64})";
+    case FALCON_ERR_BAD_DTYPE: return "dtype or phi code out of range";
+    case FALCON_ERR_MISALIGNED: return "pointer not 16-byte aligned (workspace: 256-byte)";
+    case FALCON_ERR_WORKSPACE: return "workspace missing or too small";
+    case FALCON_ERR_CUDA: return "CUDA launch or query failed";
+    case FALCON_ERR_TIMEOUT: return "a device-side wait hit its iteration limit";
+    case FALCON_ERR_BAD_ARG: return "eps must be >= 0 and eps_gamma in (0, 1)";
+    case FALCON_ERR_DEVICE: return "current device is not sm_103 (GB300)";
+  }
+  return "unknown error code";
+}
+
+int falcon_version(void) { return 100; }
+
+}  // extern "C"

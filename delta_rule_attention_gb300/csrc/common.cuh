@@ -1,0 +1,80 @@
+// Shared device helpers of the Falcon GB300 library (sm_103a only).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "falcon.h"
+
+namespace falcon {
+
+// Rule selector shared by kernels: Falcon-1 writes the residual
+// r_t = v_t - S_{t-1}^T x_t, Falcon-1A writes the target v_t.
+enum Rule : int { kFalcon1 = 1, kFalcon1A = 2 };
+
+__device__ __forceinline__ float load_elem(const void* p, int64_t i, int dtype) {
+  if (dtype == FALCON_BF16)
+    return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[i]);
+  return reinterpret_cast<const float*>(p)[i];
+}
+
+__device__ __forceinline__ void store_elem(void* p, int64_t i, float x, int dtype) {
+  if (dtype == FALCON_BF16)
+    reinterpret_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(x);
+  else
+    reinterpret_cast<float*>(p)[i] = x;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// Step size and log-decay of one token (Eq. (3.4) and the decay clamp).
+// Returns eta; writes log(gamma) = log1p(-min(eta*lambda, 1 - eps_gamma)).
+__device__ __forceinline__ float step_eta_loggamma(bool sentinel, float E, float beta,
+                                                   float lambda, float eps,
+                                                   float eps_gamma, float* log_gamma) {
+  float eta = 0.f;
+  if (!sentinel) {
+    const float den = E + lambda + eps;
+    eta = den > 0.f ? beta / den : 0.f;
+  }
+  const float alpha = fminf(eta * lambda, 1.f - eps_gamma);
+  *log_gamma = log1pf(-alpha);
+  return eta;
+}
+
+}  // namespace falcon
+
+// Host-side launchers (defined in the kernel translation units).
+namespace falcon {
+struct ChunkArgs {
+  int rule;
+  int64_t BH, T;
+  int m, dv, C, dtype, phi;
+  float eps, eps_gamma;
+  const void *q, *k, *v;
+  const float *beta, *lambda, *S0, *x_prev;
+  void* o;
+  float *S_out, *x_last;
+  void* workspace;
+};
+size_t generic_workspace_bytes(int64_t BH, int64_t T, int m, int dv, int C);
+cudaError_t launch_generic_chunked(const ChunkArgs& a, cudaStream_t stream);
+
+struct DecodeArgs {
+  int rule;
+  int64_t N;
+  int m, dv, dtype, phi;
+  float eps, eps_gamma;
+  const void *q, *k, *v;
+  const float *beta, *lambda;
+  float *S, *x_prev;
+  const uint8_t* fresh;
+  void* o;
+};
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+}  // namespace falcon

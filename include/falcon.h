@@ -1,0 +1,169 @@
+/*
+ * falcon.h -- C ABI of the GB300 (sm_103a) Falcon fast-weight attention
+ * library: chunk-parallel forward of Falcon-1 and Falcon-1A, and the
+ * single-token recurrent decode step.
+ *
+ * The operations are defined on the page hyper.ai/fr/papers/2608.27763
+ * ("Fast Weight Attention for Continual Learning"):
+ *   - causal write pair x_t = phi(k_{t-1}), y_t = v_t, boundary x_1 = 0 with
+ *     eta_1 = 0, and the read after write o_t = S_t^T phi(q_t): Section 4,
+ *     "Naming and formula summary", and Section 3 "Indexing and causality
+ *     conventions";
+ *   - Falcon-1: S_t = (1 - eta_t lambda_t) S_{t-1} + eta_t x_t r_t^T with
+ *     r_t = v_t - S_{t-1}^T x_t: Section 3.1, Eq. (3.3);
+ *   - Falcon-1A: S_t = (1 - eta_t lambda_t) S_{t-1} + eta_t x_t v_t^T:
+ *     Section 4.3, Eq. (4.6);
+ *   - step size eta_t = beta_t / (||x_t||^2 + lambda_t + eps), 0 when the
+ *     denominator is 0: Section 3.1, Eq. (3.4) and Section 4.3, Eq. (4.8);
+ *   - decay clamp alpha_t = min(eta_t lambda_t, 1 - eps_gamma),
+ *     gamma_t = 1 - alpha_t, evaluated in log space: Section 4.3, "Decay
+ *     positivity", and Section 4.4, Eq. (4.15)-(4.16).
+ * phi is the identity or the l2 map u / max(||u||_2, 1e-12) ("QK-l2" of the
+ * experiments).
+ *
+ * Conventions shared by every entry point
+ *   - All pointers are DEVICE pointers owned by the caller.  The library keeps
+ *     no pointer after a call returns and allocates no memory; scratch space,
+ *     where needed, is the caller's `workspace`.
+ *   - Every call is asynchronous on the caller's `stream` (0 = legacy default
+ *     stream) and returns before the GPU work ends.  A nonzero return means
+ *     nothing was launched (argument errors) or a launch failed (FALCON_ERR_CUDA).
+ *   - Tensors are dense, row-major, contiguous; [B,H,T,m] means element
+ *     (b,h,t,i) is at ((b*H + h)*T + t)*m + i.
+ *   - Every pointer must be 16-byte aligned (FALCON_ERR_MISALIGNED otherwise).
+ *   - The library never prints, exits or traps.
+ */
+#ifndef FALCON_GB300_H
+#define FALCON_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define FALCON_OK 0
+#define FALCON_ERR_NULL_PTR (-1)   /* a required pointer is NULL */
+#define FALCON_ERR_BAD_SHAPE (-2)  /* unsupported size (see each call) */
+#define FALCON_ERR_BAD_DTYPE (-3)  /* dtype or phi code out of range */
+#define FALCON_ERR_MISALIGNED (-4) /* a pointer is not 16-byte aligned */
+#define FALCON_ERR_WORKSPACE (-5)  /* workspace NULL or smaller than required */
+#define FALCON_ERR_CUDA (-6)       /* a CUDA launch or query failed */
+#define FALCON_ERR_TIMEOUT (-7)    /* a device-side wait hit its limit */
+#define FALCON_ERR_BAD_ARG (-8)    /* eps/eps_gamma out of range */
+#define FALCON_ERR_DEVICE (-9)     /* the current device is not sm_103 */
+
+/* Element type of q, k, v and o.  beta, lambda, states and features are
+ * always float32. */
+#define FALCON_BF16 0
+#define FALCON_F32 1
+
+/* Feature map phi applied to q and k. */
+#define FALCON_PHI_IDENTITY 0
+#define FALCON_PHI_L2 1
+
+/* Problem description for the chunked forward calls.
+ *   B, H   batch and heads; the B*H heads are independent.
+ *   T      tokens per head, T >= 0; T need not be a multiple of `chunk`
+ *          (the last chunk is partial).
+ *   m      feature dimension of q, k (and of the state's rows): 16, 32, 64
+ *          or 128.
+ *   dv     value dimension: 16, 32, 64 or 128.
+ *   chunk  chunk length C used by the chunk-parallel form: 16, 32 or 64.  It
+ *          changes only the rounding, never the result in exact arithmetic.
+ *   dtype  FALCON_BF16 or FALCON_F32 (q, k, v, o).
+ *   phi    FALCON_PHI_IDENTITY or FALCON_PHI_L2.
+ *   eps    >= 0, the step-size stabiliser of Eq. (3.4).
+ *   eps_gamma in (0, 1), the clamp margin: gamma_t >= eps_gamma. */
+typedef struct {
+  int64_t B, H, T;
+  int32_t m, dv, chunk;
+  int32_t dtype;
+  int32_t phi;
+  float eps;
+  float eps_gamma;
+} falcon_shape;
+
+/* Bytes of device workspace a chunked forward call with this shape needs
+ * (0 means the call accepts workspace = NULL).  Returns 0 for an invalid
+ * shape as well; the forward call then reports the shape error. */
+size_t falcon_workspace_bytes(const falcon_shape *shape);
+
+/* Falcon-1 chunk-parallel forward (Section 3.1 Eq. (3.3) with Eq. (3.4)).
+ *   q, k    [B,H,T,m]  dtype
+ *   v       [B,H,T,dv] dtype
+ *   beta    [B,H,T]    f32, the gain beta_t (the pages use beta in (0,2))
+ *   lambda  [B,H,T]    f32, the ridge coefficient lambda_t >= 0
+ *   S0      [B,H,m,dv] f32, state entering token 1; NULL means zeros
+ *   x_prev  [B,H,m]    f32, write feature of token 1 (phi(k) of the token
+ *           before this segment); NULL means a fresh sequence, where the
+ *           boundary sentinel applies (x_1 = 0, eta_1 = 0)
+ *   o       [B,H,T,dv] dtype, out: o_t = S_t^T phi(q_t)
+ *   S_out   [B,H,m,dv] f32, out: S_T.  May alias S0.
+ *   x_last  [B,H,m]    f32, out, nullable: phi(k_T) (x_prev of the next
+ *           segment; left untouched when T = 0 and x_prev is NULL, copied
+ *           from x_prev when T = 0 otherwise)
+ *   workspace, workspace_bytes: device scratch of at least
+ *           falcon_workspace_bytes(shape) bytes, 256-byte aligned; contents
+ *           are overwritten.  Concurrent calls need separate workspaces.
+ * Errors: FALCON_ERR_NULL_PTR, _BAD_SHAPE, _BAD_DTYPE, _MISALIGNED,
+ * _WORKSPACE, _BAD_ARG, _DEVICE (nothing launched); _CUDA (launch failed). */
+int falcon1_fwd_chunked(const falcon_shape *shape, const void *q, const void *k,
+                        const void *v, const float *beta, const float *lambda,
+                        const float *S0, const float *x_prev, void *o,
+                        float *S_out, float *x_last, void *workspace,
+                        size_t workspace_bytes, cudaStream_t stream);
+
+/* Falcon-1A chunk-parallel forward (Section 4.3 Eq. (4.6), step size
+ * Eq. (4.8) with E_t = ||x_t||^2).  Arguments, layouts, ownership and errors
+ * are those of falcon1_fwd_chunked. */
+int falcon1a_fwd_chunked(const falcon_shape *shape, const void *q,
+                         const void *k, const void *v, const float *beta,
+                         const float *lambda, const float *S0,
+                         const float *x_prev, void *o, float *S_out,
+                         float *x_last, void *workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
+
+/* One recurrent token (read after write) for N independent states: the
+ * Falcon-1 update of Section 3.1 Eq. (3.3), as in the one-step listing of page
+ * rcap.io/posts/fast-weight-attention-for-continual-learning-2026-08-27.
+ *   q, k    [N,m]  dtype;  v, o [N,dv] dtype;  beta, lambda [N] f32
+ *   S       [N,m,dv] f32, updated in place to S_t
+ *   x_prev  [N,m] f32: read as this token's write feature x_t, then
+ *           overwritten with phi(k_t) for the next token
+ *   fresh   [N] bytes, nullable: nonzero marks a state whose sequence starts
+ *           at this token (sentinel: x_t = 0, eta_t = 0, so S is not
+ *           decayed and o = S^T phi(q)); NULL means no state is fresh
+ * m, dv in {16, 32, 64, 128}.  N >= 0 (N = 0 launches nothing).
+ * Errors as for falcon1_fwd_chunked (no workspace). */
+int falcon1_decode_step(int64_t N, int32_t m, int32_t dv, int32_t dtype,
+                        int32_t phi, float eps, float eps_gamma, const void *q,
+                        const void *k, const void *v, const float *beta,
+                        const float *lambda, float *S, float *x_prev,
+                        const uint8_t *fresh, void *o, cudaStream_t stream);
+
+/* The same single-token step for Falcon-1A (Section 4.3 Eq. (4.6)). */
+int falcon1a_decode_step(int64_t N, int32_t m, int32_t dv, int32_t dtype,
+                         int32_t phi, float eps, float eps_gamma, const void *q,
+                         const void *k, const void *v, const float *beta,
+                         const float *lambda, float *S, float *x_prev,
+                         const uint8_t *fresh, void *o, cudaStream_t stream);
+
+/* Waits for `stream`, then reads and clears the library's device error word
+ * (set by a kernel whose bounded wait ran out).  Returns FALCON_OK,
+ * FALCON_ERR_TIMEOUT, or FALCON_ERR_CUDA if the stream itself failed. */
+int falcon_sync_check(cudaStream_t stream);
+
+/* Static description of a return code. */
+const char *falcon_strerror(int code);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int falcon_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FALCON_GB300_H */
