@@ -75,9 +75,12 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(ChunkArgs a, int n
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   extern __shared__ float sm[];
-  float* X = sm;               // (C+1) x m : row i = write feature of token t0+i
-  float* Qf = X + (C + 1) * m; // C x m     : phi(q)
-  float* V = Qf + C * m;       // C x dv
+  // X and Qf rows are padded to m + 1 floats so that the Gram loop below,
+  // where a warp walks down a column, hits 32 different banks.
+  const int ld = m + 1;
+  float* X = sm;               // (C+1) x ld : row i = write feature of token t0+i
+  float* Qf = X + (C + 1) * ld;  // C x ld  : phi(q)
+  float* V = Qf + C * ld;      // C x dv
   float* Am = V + C * dv;      // C x C     : strictly lower A of I + A
   float* P = Am + C * C;       // C x C     : masked, decayed Q X^T
   float* WU = P + C * C;       // C x (m+dv): [W | U~]
@@ -94,7 +97,7 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(ChunkArgs a, int n
     float e = 0.f;
     if (i <= n) {
       if (t >= 1) {
-        e = warp_feature(a.k, (rowbase + t - 1) * m, m, a.dtype, a.phi, X + i * m);
+        e = warp_feature(a.k, (rowbase + t - 1) * m, m, a.dtype, a.phi, X + i * ld);
       } else if (a.x_prev) {
         float ss = 0.f;
         for (int j = lane; j < m; j += 32) {
@@ -107,14 +110,14 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(ChunkArgs a, int n
         for (int j = lane; j < m; j += 32) X[j] = 0.f;
       }
     } else {
-      for (int j = lane; j < m; j += 32) X[i * m + j] = 0.f;
+      for (int j = lane; j < m; j += 32) X[i * ld + j] = 0.f;
     }
     if (lane == 0 && i < C) E[i] = e;
     if (i < C) {
       if (i < n)
-        warp_feature(a.q, (rowbase + t) * m, m, a.dtype, a.phi, Qf + i * m);
+        warp_feature(a.q, (rowbase + t) * m, m, a.dtype, a.phi, Qf + i * ld);
       else
-        for (int j = lane; j < m; j += 32) Qf[i * m + j] = 0.f;
+        for (int j = lane; j < m; j += 32) Qf[i * ld + j] = 0.f;
     }
   }
   for (int idx = threadIdx.x; idx < C * dv; idx += kThreads) {
@@ -123,16 +126,16 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(ChunkArgs a, int n
   }
   __syncthreads();
   if (a.x_last && c == nchunks - 1)
-    for (int j = threadIdx.x; j < m; j += kThreads) a.x_last[bh * m + j] = X[n * m + j];
+    for (int j = threadIdx.x; j < m; j += kThreads) a.x_last[bh * m + j] = X[n * ld + j];
 
   // Per-token step size and log-decay, then the chunk-local prefix sums.
   if (threadIdx.x < C) {
     const int i = threadIdx.x;
-    float lg = 0.f, e = 0.f;
+    float lg = 0.f, e = 0.f, gam;
     if (i < n) {
       const bool sentinel = (t0 + i == 0) && (a.x_prev == nullptr);
-      e = step_eta_loggamma(sentinel, E[i], a.beta[rowbase + t0 + i],
-                            a.lambda[rowbase + t0 + i], a.eps, a.eps_gamma, &lg);
+      e = step_eta_gamma(sentinel, E[i], a.beta[rowbase + t0 + i], a.lambda[rowbase + t0 + i],
+                         a.eps, a.eps_gamma, &gam, &lg);
     }
     eta[i] = e;
     g[i] = lg;  // prefix below
@@ -155,8 +158,8 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(ChunkArgs a, int n
     if (j <= i) {
       float dq = 0.f, dx = 0.f;
       for (int r = 0; r < m; ++r) {
-        dq += Qf[i * m + r] * X[j * m + r];
-        dx += X[i * m + r] * X[j * m + r];
+        dq += Qf[i * ld + r] * X[j * ld + r];
+        dx += X[i * ld + r] * X[j * ld + r];
       }
       pij = __expf(fminf(g[i] - g[j], 0.f)) * dq;
       if (j < i && a.rule == kFalcon1) aij = eta[i] * __expf(fminf(gx[i] - g[j], 0.f)) * dx;
@@ -169,7 +172,7 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(ChunkArgs a, int n
     const int i = idx / (m + dv), j = idx % (m + dv);
     float rhs;
     if (j < m)
-      rhs = (a.rule == kFalcon1) ? eta[i] * __expf(gx[i]) * X[i * m + j] : 0.f;
+      rhs = (a.rule == kFalcon1) ? eta[i] * __expf(gx[i]) * X[i * ld + j] : 0.f;
     else
       rhs = eta[i] * V[i * dv + (j - m)];
     WU[idx] = rhs;
@@ -197,12 +200,12 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(ChunkArgs a, int n
     float acc = 0.f;
     if (r < m) {  // Xt^T [W | U~] with Xt_j = e^{g_C - g_j} x_j
       for (int j = 0; j < C; ++j)
-        acc += __expf(fminf(gC - g[j], 0.f)) * X[j * m + r] * WU[j * (m + dv) + s];
+        acc += __expf(fminf(gC - g[j], 0.f)) * X[j * ld + r] * WU[j * (m + dv) + s];
       if (s < m) acc = ((r == s) ? __expf(gC) : 0.f) - acc;
     } else {  // P [W | U~]
       const int i = r - m;
       for (int j = 0; j <= i; ++j) acc += P[i * C + j] * WU[j * (m + dv) + s];
-      if (s < m) acc = __expf(g[i]) * Qf[i * m + s] - acc;
+      if (s < m) acc = __expf(g[i]) * Qf[i * ld + s] - acc;
     }
     if (s < m)
       Mc[(int64_t)r * m + s] = acc;
@@ -266,7 +269,7 @@ cudaError_t launch_generic_chunked(const ChunkArgs& a, cudaStream_t stream) {
   const int nchunks = (int)((a.T + a.C - 1) / a.C);
   const int m = a.m, dv = a.dv, C = a.C;
   const size_t prep_smem =
-      sizeof(float) * ((size_t)(C + 1) * m + (size_t)C * m + (size_t)C * dv + 2 * (size_t)C * C +
+      sizeof(float) * ((size_t)(C + 1) * (m + 1) + (size_t)C * (m + 1) + (size_t)C * dv + 2 * (size_t)C * C +
                        (size_t)C * (m + dv) + 4 * (size_t)C);
   cudaError_t err = cudaFuncSetAttribute(chunk_prep_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,

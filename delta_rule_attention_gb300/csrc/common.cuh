@@ -32,18 +32,26 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
-// Step size and log-decay of one token (Eq. (3.4) and the decay clamp).
-// Returns eta; writes log(gamma) = log1p(-min(eta*lambda, 1 - eps_gamma)).
-__device__ __forceinline__ float step_eta_loggamma(bool sentinel, float E, float beta,
-                                                   float lambda, float eps,
-                                                   float eps_gamma, float* log_gamma) {
+// Step size and decay of one token (Eq. (3.4) and the decay clamp).
+// Returns eta; writes gamma = 1 - min(eta*lambda, 1 - eps_gamma) and its log.
+// On the clamped branch gamma is exactly eps_gamma: forming 1 - (1 - eps_gamma)
+// in fp32 would cancel (9.54e-7 instead of 1e-6).
+__device__ __forceinline__ float step_eta_gamma(bool sentinel, float E, float beta,
+                                                float lambda, float eps, float eps_gamma,
+                                                float* gamma, float* log_gamma) {
   float eta = 0.f;
   if (!sentinel) {
     const float den = E + lambda + eps;
     eta = den > 0.f ? beta / den : 0.f;
   }
-  const float alpha = fminf(eta * lambda, 1.f - eps_gamma);
-  *log_gamma = log1pf(-alpha);
+  const float a = eta * lambda;
+  if (a >= 1.f - eps_gamma) {
+    *gamma = eps_gamma;
+    *log_gamma = logf(eps_gamma);
+  } else {
+    *gamma = 1.f - a;
+    *log_gamma = log1pf(-a);
+  }
   return eta;
 }
 

@@ -97,11 +97,11 @@ __global__ void __launch_bounds__(DecodeCfg<M, DV>::kThreads)
     }
     xq = warp_sum(xq);
     if (tid == 0) {
-      float lg;
-      const float eta = step_eta_loggamma(fresh, E, a.beta[n], a.lambda[n], a.eps,
-                                          a.eps_gamma, &lg);
+      float gamma, lg;
+      const float eta = step_eta_gamma(fresh, E, a.beta[n], a.lambda[n], a.eps, a.eps_gamma,
+                                       &gamma, &lg);
       scal[0] = eta;
-      scal[1] = 1.f - fminf(eta * a.lambda[n], 1.f - a.eps_gamma);
+      scal[1] = gamma;
       scal[2] = xq;
     }
   }
