@@ -31,8 +31,10 @@ _DTYPE = {torch.bfloat16: FALCON_BF16, torch.float32: FALCON_F32}
 EXPORTS = (
     "falcon_workspace_bytes", "falcon1_fwd_chunked", "falcon1a_fwd_chunked",
     "falcon1_decode_step", "falcon1a_decode_step", "falcon_sync_check",
-    "falcon_strerror", "falcon_version",
+    "falcon_strerror", "falcon_version", "falcon1_fwd_chunked_fixed_scratch",
 )
+FALCON_ERR_SCRATCH_LIMIT = -10
+FALCON_FIXED_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
 class FalconError(RuntimeError):
@@ -78,6 +80,9 @@ def load_library(path: str | None = None):
             fn.restype = ctypes.c_int
             fn.argtypes = [i64, i32, i32, i32, i32, ctypes.c_float, ctypes.c_float,
                            vp, vp, vp, f32p, f32p, f32p, f32p, vp, vp, vp]
+        lib.falcon1_fwd_chunked_fixed_scratch.restype = ctypes.c_int
+        lib.falcon1_fwd_chunked_fixed_scratch.argtypes = [shp, vp, vp, vp, f32p, f32p, f32p,
+                                                          f32p, vp, f32p, f32p, vp]
         lib.falcon_sync_check.restype = ctypes.c_int
         lib.falcon_sync_check.argtypes = [vp]
         lib.falcon_strerror.restype = ctypes.c_char_p
@@ -179,6 +184,43 @@ def falcon1_fwd_chunked(q, k, v, beta, lam, S0=None, x_prev=None, chunk=64, phi=
     fp32 or None (fresh sequence).  Returns (o, S_T, x_last)."""
     return _fwd("falcon1_fwd_chunked", q, k, v, beta, lam, S0, x_prev, chunk, phi, eps,
                 eps_gamma, **kw)
+
+
+def falcon1_fwd_chunked_fixed_scratch(q, k, v, beta, lam, S0=None, x_prev=None, chunk=64,
+                                      phi="l2", eps=1e-6, eps_gamma=1e-6, o=None, S_out=None,
+                                      x_last=None, stream=None):
+    """Falcon-1 chunked forward that needs no workspace: for callers that
+    cannot allocate device memory, the library uses a fixed scratch array of
+    FALCON_FIXED_SCRATCH_BYTES built into it.  Pass preallocated o, S_out,
+    x_last to keep the whole call free of allocation (otherwise this wrapper
+    allocates the outputs with torch, as the caller's own buffers).  Calls whose
+    GPU work overlaps share that array and race; the first call on a device
+    resolves its address and should precede any stream capture.  Returns
+    (o, S_T, x_last)."""
+    lib = load_library()
+    _need(q, "q")
+    B, H, T, m = q.shape
+    dv = v.shape[-1]
+    dt = q.dtype
+    if dt not in _DTYPE:
+        raise TypeError("q, k, v must be bfloat16 or float32")
+    dev = q.device
+    if o is None:
+        o = torch.empty((B, H, T, dv), dtype=dt, device=dev)
+    if S_out is None:
+        S_out = torch.empty((B, H, m, dv), dtype=torch.float32, device=dev)
+    if x_last is None:
+        x_last = torch.empty((B, H, m), dtype=torch.float32, device=dev)
+    for t, name in ((k, "k"), (v, "v"), (beta, "beta"), (lam, "lambda"), (o, "o"),
+                    (S_out, "S_out"), (x_last, "x_last"), (S0, "S0"), (x_prev, "x_prev")):
+        if t is not None:
+            _need(t, name)
+    shape = make_shape(B, H, T, m, dv, chunk, dt, phi, eps, eps_gamma)
+    rc = lib.falcon1_fwd_chunked_fixed_scratch(
+        ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(lam), _ptr(S0),
+        _ptr(x_prev), _ptr(o), _ptr(S_out), _ptr(x_last), _stream(stream))
+    _check(rc, "falcon1_fwd_chunked_fixed_scratch")
+    return o, S_out, x_last
 
 
 def falcon1a_fwd_chunked(q, k, v, beta, lam, S0=None, x_prev=None, chunk=64, phi="l2",

@@ -209,6 +209,8 @@ const char* falcon_strerror(int code) {
     case FALCON_ERR_TIMEOUT: return "a device-side wait hit its iteration limit";
     case FALCON_ERR_BAD_ARG: return "eps must be >= 0 and eps_gamma in (0, 1)";
     case FALCON_ERR_DEVICE: return "current device is not sm_103 (GB300)";
+    case FALCON_ERR_SCRATCH_LIMIT:
+      return "problem needs more scratch than the library's fixed array (FALCON_FIXED_SCRATCH_BYTES)";
   }
   return "unknown error code";
 }

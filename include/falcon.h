@@ -55,6 +55,11 @@ extern "C" {
 #define FALCON_ERR_TIMEOUT (-7)    /* a device-side wait hit its limit */
 #define FALCON_ERR_BAD_ARG (-8)    /* eps/eps_gamma out of range */
 #define FALCON_ERR_DEVICE (-9)     /* the current device is not sm_103 */
+#define FALCON_ERR_SCRATCH_LIMIT (-10) /* needs more than FALCON_FIXED_SCRATCH_BYTES */
+
+/* Size of the scratch array built into the library for
+ * falcon1_fwd_chunked_fixed_scratch (held on every GPU that loads it). */
+#define FALCON_FIXED_SCRATCH_BYTES (16u * 1024u * 1024u)
 
 /* Element type of q, k, v and o.  beta, lambda, states and features are
  * always float32. */
@@ -116,6 +121,32 @@ int falcon1_fwd_chunked(const falcon_shape *shape, const void *q, const void *k,
                         const float *S0, const float *x_prev, void *o,
                         float *S_out, float *x_last, void *workspace,
                         size_t workspace_bytes, cudaStream_t stream);
+
+/* falcon1_fwd_chunked for callers that cannot allocate device memory: the
+ * paper has no counterpart; this is a library convenience.  It computes
+ * exactly what falcon1_fwd_chunked computes, but takes no workspace: its
+ * scratch is a fixed array of FALCON_FIXED_SCRATCH_BYTES inside the library
+ * (held on every GPU that loads the library until the process exits), so the
+ * call allocates nothing.  It serves callers that are handed only input and
+ * output buffers (a C host program, a plugin interface), whose allocator is
+ * out of reach at the call site, or that forbid allocation after start-up.
+ *   - Shapes with falcon_workspace_bytes(shape) > FALCON_FIXED_SCRATCH_BYTES
+ *     are rejected with FALCON_ERR_SCRATCH_LIMIT (nothing launched).
+ *   - The first call on each device, with that device current, resolves the
+ *     array's device address (cudaGetSymbolAddress); make that first call
+ *     before any stream capture on the device.
+ *   - All calls on a device share the array, which keeps the previous call's
+ *     contents (nothing needs clearing: every scratch element read is written
+ *     first by the same call).  Calls whose GPU work overlaps race on it: issue
+ *     them on one stream.
+ * Other arguments, layouts, ownership and errors are those of
+ * falcon1_fwd_chunked. */
+int falcon1_fwd_chunked_fixed_scratch(const falcon_shape *shape, const void *q,
+                                      const void *k, const void *v,
+                                      const float *beta, const float *lambda,
+                                      const float *S0, const float *x_prev,
+                                      void *o, float *S_out, float *x_last,
+                                      cudaStream_t stream);
 
 /* Falcon-1A chunk-parallel forward (Section 4.3 Eq. (4.6), step size
  * Eq. (4.8) with E_t = ||x_t||^2).  Arguments, layouts, ownership and errors
