@@ -3,6 +3,8 @@
 // argument is rejected.
 #include <stdint.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace falcon {
@@ -50,6 +52,24 @@ int check_shape(const falcon_shape* s) {
 }
 
 int to_status(cudaError_t e) { return e == cudaSuccess ? FALCON_OK : FALCON_ERR_CUDA; }
+
+// Device address of g_device_error on the current device (kernels with
+// bounded waits set it); resolved once per device.
+constexpr int kMaxDevices = 64;
+std::mutex g_err_mu;
+int* g_err_ptr[kMaxDevices] = {};
+
+int* device_error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_err_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, falcon::g_device_error) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_err_ptr[dev];
+}
 
 int fwd_chunked(int rule, const falcon_shape* s, const void* q, const void* k, const void* v,
                 const float* beta, const float* lambda, const float* S0, const float* x_prev,
@@ -104,6 +124,11 @@ int fwd_chunked(int rule, const falcon_shape* s, const void* q, const void* k, c
   a.S_out = S_out;
   a.x_last = x_last;
   a.workspace = workspace;
+  if (falcon::tc_path_applies(s->dtype, s->m, s->dv, s->chunk)) {
+    int* err = device_error_word();
+    if (!err) return FALCON_ERR_CUDA;
+    return to_status(falcon::launch_tc_chunked(a, err, stream));
+  }
   return to_status(falcon::launch_generic_chunked(a, stream));
 }
 
@@ -148,6 +173,8 @@ extern "C" {
 
 size_t falcon_workspace_bytes(const falcon_shape* s) {
   if (check_shape(s) != FALCON_OK) return 0;
+  if (falcon::tc_path_applies(s->dtype, s->m, s->dv, s->chunk))
+    return falcon::tc_workspace_bytes(s->B * s->H, s->T);
   return falcon::generic_workspace_bytes(s->B * s->H, s->T, s->m, s->dv, s->chunk);
 }
 

@@ -60,6 +60,9 @@ CASES = [
     (1, 3, 257, 128, 128, 64, torch.bfloat16, "l2"),
     (1, 2, 40, 16, 64, 16, torch.float32, "identity"),
     (3, 2, 7, 64, 16, 64, torch.float32, "l2"),       # shorter than one chunk
+    (3, 2, 7, 64, 64, 64, torch.bfloat16, "l2"),      # tensor-core path, one partial chunk
+    (1, 2, 1, 64, 64, 64, torch.bfloat16, "l2"),      # a single token
+    (2, 2, 4 * 64, 64, 64, 64, torch.bfloat16, "identity"),
 ]
 
 
