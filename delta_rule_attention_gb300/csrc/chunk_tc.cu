@@ -13,17 +13,19 @@
 //        O   =             Mc_bot S + Nc_bot,   Mc_bot = Diag(e^g) Q - P W,  Nc_bot = P U~
 //
 //     with W = T Diag(eta e^{g_-}) X, U~ = T Diag(eta) V, T = (I + A)^{-1}.
-//     Three tcgen05 MMAs (bf16 operands from shared memory, fp32 accumulators
-//     in TMEM) do the contractions:
-//        MMA1  [X; Q] [X; Q]^T      -> G = X X^T and P^T (before masking)
-//        MMA2  [Xh^T; Vh^T] T^T     -> [W^T; U~^T]
-//        MMA3  [Xt^T; P] [W | U~]   -> [Xt^T W | Xt^T U~ ; P W | P U~]
-//     The triangular solve runs in fp32 on the CUDA cores.  Mc is written to
-//     the workspace as a ready-to-use swizzled bf16 operand tile, Nc in fp32.
+//     tcgen05 MMAs (bf16 operands in shared memory, fp32 accumulators in TMEM)
+//     do the contractions:
+//        MMA1   [X; Q] X^T                 -> G = X X^T (lanes 0..63), Q X^T (64..127)
+//        MMA2   [Xh^T; Vh^T] T^T           -> [W^T; U~^T]
+//        MMA3   [Xt^T; 0] [W|U~] + [0; P] [W|U~] -> [Xt^T W | Xt^T U~ ; P W | P U~]
+//     The unit-lower solve runs in fp32 (diagonal 16 x 16 blocks) with warp
+//     MMAs for the off-diagonal block products.  The map goes to the workspace
+//     as two ready-to-use bf16 tiles (Mc swizzled as an MMA operand, Nc with
+//     rows swizzled at 16-byte granularity) plus e^{g_C}.
 //     Falcon-1A takes the same path with T = I and W = 0.
 //
 //  2. tc_chunk_scan_kernel -- one CTA per head, sequential over chunks: one
-//     M=128 tcgen05 MMA per chunk, [Mc_top; Mc_bot] S, with the map of the
+//     M=128 tcgen05 MMA per chunk, [Mc_top; Mc_bot] S, with the maps of the
 //     next chunks prefetched by bulk copies.  The e^{g_C} S part of the state
 //     update stays in fp32 registers (only the correction goes through bf16
 //     operands), so an undecayed state does not drift over long sequences.
@@ -39,9 +41,12 @@ namespace {
 using namespace tc;
 
 constexpr int kC = 64;
-constexpr uint32_t kMcBytes = 128 * 128;     // 128 rows x 64 bf16 (swizzled image)
-constexpr uint32_t kNcBytes = 128 * 64 * 4;  // 128 rows x 64 fp32
+constexpr uint32_t kMcBytes = 128 * 128;  // 128 rows x 64 bf16 (swizzled operand image)
+constexpr uint32_t kNcBytes = 128 * 128;  // 128 rows x 64 bf16 (rows swizzled by 16 B)
 constexpr uint32_t kMapBytes = kMcBytes + kNcBytes + 128;  // + e^{g_C} (padded)
+// A chunk whose log-decay spans at most this much factors e^{a-b} as
+// e^{a-r} e^{r-b} (both factors stay within fp32 range).
+constexpr float kFactorSpan = 80.f;
 
 __device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
   return reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(p) + 1023) &
@@ -85,98 +90,146 @@ __device__ __forceinline__ float apply_phi(float* v, int phi) {
   return ss;
 }
 
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// 8 consecutive values (scaled) as one 16-byte bf16 chunk.
+__device__ __forceinline__ uint4 pack8(const float* v, float scale) {
+  uint4 pk;
+  pk.x = pack_bf16(scale * v[0], scale * v[1]);
+  pk.y = pack_bf16(scale * v[2], scale * v[3]);
+  pk.z = pack_bf16(scale * v[4], scale * v[5]);
+  pk.w = pack_bf16(scale * v[6], scale * v[7]);
+  return pk;
+}
+
+// Row r of a 64-wide bf16 tile with the 128-byte swizzle (chunk c -> c ^ (r & 7)).
 __device__ __forceinline__ void store_row_scaled(unsigned char* tile, int r, const float* v,
                                                  float scale) {
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    float w[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) w[e] = scale * v[8 * c + e];
-    uint4 pk;
-    __nv_bfloat162 h0 = __floats2bfloat162_rn(w[0], w[1]);
-    __nv_bfloat162 h1 = __floats2bfloat162_rn(w[2], w[3]);
-    __nv_bfloat162 h2 = __floats2bfloat162_rn(w[4], w[5]);
-    __nv_bfloat162 h3 = __floats2bfloat162_rn(w[6], w[7]);
-    pk.x = *reinterpret_cast<uint32_t*>(&h0);
-    pk.y = *reinterpret_cast<uint32_t*>(&h1);
-    pk.z = *reinterpret_cast<uint32_t*>(&h2);
-    pk.w = *reinterpret_cast<uint32_t*>(&h3);
-    *reinterpret_cast<uint4*>(tile + r * 128 + ((c ^ (r & 7)) << 4)) = pk;
-  }
+  for (int c = 0; c < 8; ++c)
+    *reinterpret_cast<uint4*>(tile + r * 128 + ((c ^ (r & 7)) << 4)) = pack8(v + 8 * c, scale);
 }
 
-// Shared memory of the map kernel.  Buffers with disjoint lifetimes share
-// space: R1 holds the MMA1 operand [X; Q], then A (fp32), then MMA3's B
-// operand; R2 holds the solve's fp32 scratch, then T as MMA2's B operand.
+// Warp-level bf16 MMA, 16 x 8 x 16, fp32 accumulate (used for the 16-row
+// blocks of the triangular solve, below the 64-row minimum of tcgen05).
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4],
+                                         const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// A fragment (rows r0..r0+15, cols k0..k0+15) of a row-major fp32 matrix.
+__device__ __forceinline__ void frag_a(uint32_t (&a)[4], const float* M, int ld, int r0, int k0) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const float* p0 = M + (r0 + g) * ld + k0 + 2 * t;
+  const float* p1 = p0 + 8 * ld;
+  a[0] = pack_bf16(p0[0], p0[1]);
+  a[1] = pack_bf16(p1[0], p1[1]);
+  a[2] = pack_bf16(p0[8], p0[9]);
+  a[3] = pack_bf16(p1[8], p1[9]);
+}
+
+// B fragment (K rows k0..k0+15, N cols n0..n0+7) of a row-major fp32 K x N matrix.
+__device__ __forceinline__ void frag_b(uint32_t (&b)[2], const float* M, int ld, int k0, int n0) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const float* p = M + (k0 + 2 * t) * ld + n0 + g;
+  b[0] = pack_bf16(p[0], p[ld]);
+  b[1] = pack_bf16(p[8 * ld], p[9 * ld]);
+}
+
+// Shared memory of the map kernel.  Buffers with disjoint lifetimes share space:
+//   R1: [X; Q] (MMA1 operand) -> A (fp32, for the solve) -> [W^T; U~^T] (MMA3 B)
+//   R2: solve scratch (T, right-hand sides, diagonal inverses) -> MMA2 operands
+//       (A = [Xh^T; Vh^T] at +0, B = T at +17408)
+//   A3: MMA3 A operands: Xt tile | zero tile | P tile
+constexpr int kR2Tt = 17408;
 struct MapSmem {
   union {
-    unsigned char xq[128 * 128];  // K-major: rows 0..63 X, 64..127 phi(Q) (MMA1 A and B)
-    float As[64 * 65];            // strictly lower A of I + A (fp32), padded rows
-    unsigned char b3[128 * 128];  // K-major B of MMA3: rows = [W^T; U~^T]
+    unsigned char xq[128 * 128];
+    float As[64 * 65];
+    unsigned char b3[128 * 128];
   } __align__(1024) r1;
-  unsigned char a2[2 * 8192] __align__(1024);  // MN-major A of MMA2: atom 0 = Xh rows, atom 1 = Vh rows
-  unsigned char a3[2 * 8192] __align__(1024);  // MN-major A of MMA3: atom 0 = Xt rows, atom 1 row j = P[:, j]
   union {
     struct {
-      float Ts[64 * 65];    // T = (I + A)^{-1} during the solve
+      float Ts[64 * 65];    // T = (I + A)^{-1}
       float Rs[16 * 49];    // block-row right-hand sides
-      float Dinv[64 * 17];  // inverses of the 16 x 16 diagonal blocks
+      float Dinv[64 * 17];  // inverses of the 16 x 16 diagonal blocks (row-wise)
     } sv;
-    unsigned char tt[64 * 128];  // K-major B of MMA2: row i = T[i][:]
+    unsigned char mma2[kR2Tt + 8192];  // a2 at +0 (MN-major, two 8 KB atoms), tt at +kR2Tt
   } __align__(1024) r2;
+  unsigned char a3[3 * 8192] __align__(1024);
   float eta[64], g[64], gx[64];
+  float fu[64], fv[64], fw[64];  // rank-1 decay factors (span <= kFactorSpan)
   float carry;
   int fail;
   uint64_t bar;
   uint32_t tmem_base;
 };
 
-// T = (I + A)^{-1} for the strictly lower 64 x 64 A in s.As (fp32, CUDA
-// cores).  16 x 16 diagonal blocks are inverted by forward substitution with
-// warp shuffles; block rows 1..3 follow T_b = Dinv_b (-A_b,<b T_<b).
+// T = (I + A)^{-1} for the strictly lower 64 x 64 A in s.r1.As.  Warp b
+// inverts diagonal block b in fp32 by forward substitution (two lanes per
+// row, eight columns each, rows broadcast by shuffles); block rows b = 1..3
+// then follow T_{b,<b} = Dinv_b (-A_{b,<b} T_{<b}) with warp MMAs.
 __device__ void solve_unit_lower(MapSmem& s) {
-  const int tid = threadIdx.x;
-  if (tid < 64) {
-    const int lane = tid & 31, r = tid & 15, b = tid >> 4;
-    float dinv[16];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  {
+    const int b = warp, r = lane >> 1, h = lane & 1, row = 16 * b + r;
+    float dinv[8];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) dinv[j] = (j == r) ? 1.f : 0.f;
+    for (int jj = 0; jj < 8; ++jj) dinv[jj] = (8 * h + jj == r) ? 1.f : 0.f;
 #pragma unroll
     for (int k = 0; k < 15; ++k) {
-      const float aik = s.r1.As[tid * 65 + 16 * b + k];
+      const float aik = s.r1.As[row * 65 + 16 * b + k];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float tkj = __shfl_sync(0xffffffffu, dinv[j], (lane & 16) | k);
-        if (r > k) dinv[j] -= aik * tkj;
+      for (int jj = 0; jj < 8; ++jj) {
+        const float tkj = __shfl_sync(0xffffffffu, dinv[jj], 2 * k + h);
+        if (r > k) dinv[jj] -= aik * tkj;
       }
     }
 #pragma unroll
-    for (int j = 0; j < 16; ++j) s.r2.sv.Dinv[tid * 17 + j] = dinv[j];
-    // T rows of block 0 are Dinv rows; every row is zero to the right of its
-    // diagonal block.
-    for (int j = 0; j < 64; ++j) {
-      const int rel = j - 16 * b;
-      s.r2.sv.Ts[tid * 65 + j] = (rel >= 0 && rel < 16) ? dinv[rel] : 0.f;
+    for (int jj = 0; jj < 8; ++jj) {
+      s.r2.sv.Dinv[row * 17 + 8 * h + jj] = dinv[jj];
+      s.r2.sv.Ts[row * 65 + 16 * b + 8 * h + jj] = dinv[jj];
     }
   }
   __syncthreads();
+  const int g = lane >> 2, t = lane & 3;
   for (int b = 1; b < 4; ++b) {
-    const int w = 16 * b;  // columns to the left of block b
-    for (int idx = tid; idx < 16 * w; idx += 128) {
-      const int ii = idx / w, cc = idx % w;
-      const float* arow = s.r1.As + (w + ii) * 65;
-      float acc = 0.f;
-      for (int k = cc; k < w; ++k) acc -= arow[k] * s.r2.sv.Ts[k * 65 + cc];  // T[k][cc] = 0 for k < cc
-      s.r2.sv.Rs[ii * 49 + cc] = acc;
+    const int w = 16 * b;  // columns to the left of block b: 2b n-tiles of 8
+    // R = -A[w:w+16, 0:w] T[0:w, 0:w]; T[k][n] = 0 for k < n, so those k-steps are skipped.
+    for (int nt = warp; nt < 2 * b; nt += 4) {
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int kb = nt >> 1; kb < b; ++kb) {
+        uint32_t fa[4], fb[2];
+        frag_a(fa, s.r1.As, 65, w, 16 * kb);
+        frag_b(fb, s.r2.sv.Ts, 65, 16 * kb, 8 * nt);
+        mma16816(d, fa, fb);
+      }
+      float* r0 = s.r2.sv.Rs + g * 49 + 8 * nt + 2 * t;
+      r0[0] = -d[0];
+      r0[1] = -d[1];
+      r0[8 * 49] = -d[2];
+      r0[8 * 49 + 1] = -d[3];
     }
     __syncthreads();
-    for (int idx = tid; idx < 16 * w; idx += 128) {
-      const int ii = idx / w, cc = idx % w;
-      const float* drow = s.r2.sv.Dinv + (w + ii) * 17;
-      float acc = 0.f;
-#pragma unroll
-      for (int r = 0; r < 16; ++r) acc += drow[r] * s.r2.sv.Rs[r * 49 + cc];
-      s.r2.sv.Ts[(w + ii) * 65 + cc] = acc;
+    // T[w:w+16, 0:w] = Dinv_b R
+    for (int nt = warp; nt < 2 * b; nt += 4) {
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t fa[4], fb[2];
+      frag_a(fa, s.r2.sv.Dinv, 17, w, 0);
+      frag_b(fb, s.r2.sv.Rs, 49, 0, 8 * nt);
+      mma16816(d, fa, fb);
+      float* t0 = s.r2.sv.Ts + (w + g) * 65 + 8 * nt + 2 * t;
+      t0[0] = d[0];
+      t0[1] = d[1];
+      t0[8 * 65] = d[2];
+      t0[8 * 65 + 1] = d[3];
     }
     __syncthreads();
   }
@@ -195,6 +248,11 @@ __global__ void __launch_bounds__(128) tc_chunk_map_kernel(ChunkArgs a, int nchu
   const __nv_bfloat16* kg = reinterpret_cast<const __nv_bfloat16*>(a.k);
   const __nv_bfloat16* vg = reinterpret_cast<const __nv_bfloat16*>(a.v);
   const int64_t rowbase = bh * a.T;
+  unsigned char* const xt_tile = s.a3;         // MN-major A of MMA3a, atom 0
+  unsigned char* const zero_tile = s.a3 + 8192;  // atom 1 of MMA3a, rows 0..63 of MMA3b
+  unsigned char* const p_tile = s.a3 + 16384;  // rows 64..127 of MMA3b (K-major)
+  unsigned char* const a2 = s.r2.mma2;
+  unsigned char* const tt = s.r2.mma2 + kR2Tt;
 
   if (warp == 0) tmem_alloc(&s.tmem_base, 128);
   if (tid == 0) {
@@ -202,6 +260,10 @@ __global__ void __launch_bounds__(128) tc_chunk_map_kernel(ChunkArgs a, int nchu
     fence_mbar_init();
     s.fail = 0;
   }
+  reinterpret_cast<uint4*>(zero_tile)[tid] = make_uint4(0, 0, 0, 0);
+  reinterpret_cast<uint4*>(zero_tile)[tid + 128] = make_uint4(0, 0, 0, 0);
+  reinterpret_cast<uint4*>(zero_tile)[tid + 256] = make_uint4(0, 0, 0, 0);
+  reinterpret_cast<uint4*>(zero_tile)[tid + 384] = make_uint4(0, 0, 0, 0);
 
   // ---- features: thread t < 64 builds the write feature x_t = phi(k_{t0+t-1});
   //      thread 64 + i builds phi(q_{t0+i}).  Rows past the sequence are zero.
@@ -240,7 +302,7 @@ __global__ void __launch_bounds__(128) tc_chunk_map_kernel(ChunkArgs a, int nchu
       for (int j = 0; j < 64; ++j) a.x_last[bh * 64 + j] = kl[j];
     }
   }
-  store_row_bf16(s.r1.xq, tid, x);
+  store_row_scaled(s.r1.xq, tid, x, 1.f);
 
   // ---- step sizes, log-decays, chunk-local inclusive prefix g ----
   float eta = 0.f, lg = 0.f;
@@ -257,7 +319,6 @@ __global__ void __launch_bounds__(128) tc_chunk_map_kernel(ChunkArgs a, int nchu
     if (lane >= o) incl += y;
   }
   if (tid == 31) s.carry = incl;
-  fence_async_smem();
   __syncthreads();
   if (warp == 1) incl += s.carry;
   if (tid < 64) {
@@ -265,75 +326,97 @@ __global__ void __launch_bounds__(128) tc_chunk_map_kernel(ChunkArgs a, int nchu
     s.g[tid] = incl;
     s.gx[tid] = incl - lg;
   }
+  fence_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
   const uint32_t tlane = tmem + ((uint32_t)(warp * 32) << 16);
+  const float gC = s.g[kC - 1];
+  const bool factored = -gC <= kFactorSpan;
 
-  // ---- MMA1: D[0:128) = [X; Q] [X; Q]^T ----
+  // ---- MMA1: D[0:64) = [X; Q] X^T ----
   if (tid == 0) {
     mma_k64(tmem, smem_addr(s.r1.xq), false, 16, smem_addr(s.r1.xq), false, 16,
-            idesc_bf16(128, 128, false, false), false);
+            idesc_bf16(128, 64, false, false), false);
     mma_commit(&s.bar);
   }
-  const float gC = s.g[kC - 1];
-  // Meanwhile: Xh = Diag(eta e^{g_-}) X, Xt = Diag(e^{g_C - g}) X, Vh = Diag(eta) V.
+  // Meanwhile: Xt = Diag(e^{g_C - g}) X (MMA3a operand) and the rank-1 decay
+  // factors around r = g_C / 2: fu_l = e^{r - g_l}, fv_j = eta_j e^{g_{j-1} - r},
+  // fw_i = e^{g_i - r}.
   if (tid < 64) {
-    store_row_scaled(s.a2, tid, x, f1 ? s.eta[tid] * __expf(s.gx[tid]) : 0.f);
-    store_row_scaled(s.a3, tid, x, __expf(gC - s.g[tid]));
+    store_row_scaled(xt_tile, tid, x, __expf(gC - s.g[tid]));
+    if (factored) {
+      const float r = 0.5f * gC;
+      s.fu[tid] = __expf(r - s.g[tid]);
+      s.fv[tid] = s.eta[tid] * __expf(s.gx[tid] - r);
+      s.fw[tid] = __expf(s.g[tid] - r);
+    }
+  }
+  if (!mbar_wait(&s.bar, 0)) s.fail = 1;
+  tc_fence_after();
+  __syncthreads();  // fu/fv/fw visible
+  {
+    float d[64];
+    tmem_ld32(tlane, d);
+    tmem_ld32(tlane + 32, d + 32);
+    if (tid < 64) {
+      // A row j: eta_j e^{g_{j-1} - g_l} G[j][l] for l < j
+      const int j = tid;
+      if (f1) {
+        if (factored) {
+          const float vj = s.fv[j];
+#pragma unroll
+          for (int l = 0; l < 64; ++l) s.r1.As[j * 65 + l] = (l < j) ? vj * s.fu[l] * d[l] : 0.f;
+        } else {
+          const float ej = s.eta[j], gxj = s.gx[j];
+#pragma unroll
+          for (int l = 0; l < 64; ++l)
+            s.r1.As[j * 65 + l] = (l < j) ? ej * __expf(fminf(gxj - s.g[l], 0.f)) * d[l] : 0.f;
+        }
+      }
+    } else {
+      // P row i: e^{g_i - g_j} (Q X^T)[i][j] for j <= i
+      const int i = tid - 64;
+      if (factored) {
+        const float wi = s.fw[i];
+#pragma unroll
+        for (int jj = 0; jj < 64; ++jj) d[jj] = (jj <= i) ? wi * s.fu[jj] * d[jj] : 0.f;
+      } else {
+        const float gi = s.g[i];
+#pragma unroll
+        for (int jj = 0; jj < 64; ++jj)
+          d[jj] = (jj <= i) ? __expf(fminf(gi - s.g[jj], 0.f)) * d[jj] : 0.f;
+      }
+      store_row_scaled(p_tile, i, d, 1.f);
+    }
+  }
+  __syncthreads();
+  if (__syncthreads_or(s.fail)) goto teardown;
+
+  // ---- T = (I + A)^{-1} (identity for Falcon-1A), then the MMA2 operands ----
+  if (f1) solve_unit_lower(s);
+  if (tid < 64) {
+    // T row tid as bf16: the solve result left of and in the diagonal block, zero beyond.
+    float trow[64];
+    const int end = (tid | 15) + 1;
+#pragma unroll
+    for (int j = 0; j < 64; ++j)
+      trow[j] = f1 ? ((j < end) ? s.r2.sv.Ts[tid * 65 + j] : 0.f) : ((j == tid) ? 1.f : 0.f);
+    store_row_scaled(tt, tid, trow, 1.f);
+  }
+  __syncthreads();  // the MMA2 A operand overwrites the solve scratch
+  if (tid < 64) {
+    store_row_scaled(a2, tid, x, f1 ? s.eta[tid] * __expf(s.gx[tid]) : 0.f);
   } else {
     const int i = tid - 64;
     float v[64];
     if (i < n)
       load_row_global(vg + (rowbase + t0 + i) * 64, v);
     else
+#pragma unroll
       for (int j = 0; j < 64; ++j) v[j] = 0.f;
-    store_row_scaled(s.a2 + 8192, i, v, s.eta[i]);
-  }
-  if (!mbar_wait(&s.bar, 0)) s.fail = 1;
-  tc_fence_after();
-  if (tid < 64) {
-    const int j = tid;  // row j of G, column j of P
-    const float gxj = s.gx[j], gj = s.g[j], ej = s.eta[j];
-    float d[32];
-    for (int h = 0; h < 2; ++h) {
-      tmem_ld32(tlane + 32 * h, d);
-#pragma unroll
-      for (int l = 0; l < 32; ++l) {
-        const int col = 32 * h + l;
-        s.r1.As[j * 65 + col] = (f1 && col < j) ? ej * __expf(gxj - s.g[col]) * d[l] : 0.f;
-      }
-    }
-    float p[64];
-    for (int h = 0; h < 2; ++h) {
-      tmem_ld32(tlane + 64 + 32 * h, d);
-#pragma unroll
-      for (int l = 0; l < 32; ++l) {
-        const int i = 32 * h + l;
-        p[i] = (i >= j) ? __expf(fminf(s.g[i] - gj, 0.f)) * d[l] : 0.f;
-      }
-    }
-    store_row_bf16(s.a3 + 8192, j, p);  // MN-major: row j holds P[:, j]
-  }
-  __syncthreads();
-  if (__syncthreads_or(s.fail)) goto teardown;
-
-  // ---- T = (I + A)^{-1} (identity for Falcon-1A) ----
-  if (f1) {
-    solve_unit_lower(s);
-    float trow[64];
-    if (tid < 64) {
-#pragma unroll
-      for (int j = 0; j < 64; ++j) trow[j] = s.r2.sv.Ts[tid * 65 + j];
-    }
-    __syncthreads();  // the bf16 T tile overwrites the fp32 scratch
-    if (tid < 64) store_row_bf16(s.r2.tt, tid, trow);
-  } else if (tid < 64) {
-    float trow[64];
-#pragma unroll
-    for (int j = 0; j < 64; ++j) trow[j] = (j == tid) ? 1.f : 0.f;
-    store_row_bf16(s.r2.tt, tid, trow);
+    store_row_scaled(a2 + 8192, i, v, s.eta[i]);
   }
   fence_async_smem();
   tc_fence_before();
@@ -342,7 +425,7 @@ __global__ void __launch_bounds__(128) tc_chunk_map_kernel(ChunkArgs a, int nchu
 
   // ---- MMA2: D[0:64) = [Xh^T; Vh^T] T^T = [W^T; U~^T] ----
   if (tid == 0) {
-    mma_k64(tmem, smem_addr(s.a2), true, 8192, smem_addr(s.r2.tt), false, 16,
+    mma_k64(tmem, smem_addr(a2), true, 8192, smem_addr(tt), false, 16,
             idesc_bf16(128, 64, true, false), false);
     mma_commit(&s.bar);
   }
@@ -352,7 +435,7 @@ __global__ void __launch_bounds__(128) tc_chunk_map_kernel(ChunkArgs a, int nchu
     float d[64];
     tmem_ld32(tlane, d);
     tmem_ld32(tlane + 32, d + 32);
-    store_row_bf16(s.r1.b3, tid, d);
+    store_row_scaled(s.r1.b3, tid, d, 1.f);
   }
   fence_async_smem();
   tc_fence_before();
@@ -360,10 +443,12 @@ __global__ void __launch_bounds__(128) tc_chunk_map_kernel(ChunkArgs a, int nchu
   tc_fence_after();
   if (__syncthreads_or(s.fail)) goto teardown;
 
-  // ---- MMA3: D[0:128) = [Xt^T; P] [W | U~] ----
+  // ---- MMA3: D[0:128) = [Xt^T; 0] [W | U~] + [0; P] [W | U~] ----
   if (tid == 0) {
-    mma_k64(tmem, smem_addr(s.a3), true, 8192, smem_addr(s.r1.b3), false, 16,
+    mma_k64(tmem, smem_addr(xt_tile), true, 8192, smem_addr(s.r1.b3), false, 16,
             idesc_bf16(128, 128, true, false), false);
+    mma_k64(tmem, smem_addr(zero_tile), false, 16, smem_addr(s.r1.b3), false, 16,
+            idesc_bf16(128, 128, false, false), true);
     mma_commit(&s.bar);
   }
   if (!mbar_wait(&s.bar, 0)) s.fail = 1;
@@ -378,27 +463,16 @@ __global__ void __launch_bounds__(128) tc_chunk_map_kernel(ChunkArgs a, int nchu
     const float eg = (tid >= 64) ? __expf(s.g[tid - 64]) : 0.f;
 #pragma unroll
     for (int j = 0; j < 64; ++j) d[j] = (tid < 64) ? -d[j] : eg * x[j] - d[j];
-    {
-      // swizzled image of the K-major operand tile, row tid
 #pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        uint4 pk;
-        __nv_bfloat162 h0 = __floats2bfloat162_rn(d[8 * cc + 0], d[8 * cc + 1]);
-        __nv_bfloat162 h1 = __floats2bfloat162_rn(d[8 * cc + 2], d[8 * cc + 3]);
-        __nv_bfloat162 h2 = __floats2bfloat162_rn(d[8 * cc + 4], d[8 * cc + 5]);
-        __nv_bfloat162 h3 = __floats2bfloat162_rn(d[8 * cc + 6], d[8 * cc + 7]);
-        pk.x = *reinterpret_cast<uint32_t*>(&h0);
-        pk.y = *reinterpret_cast<uint32_t*>(&h1);
-        pk.z = *reinterpret_cast<uint32_t*>(&h2);
-        pk.w = *reinterpret_cast<uint32_t*>(&h3);
-        *reinterpret_cast<uint4*>(map + tid * 128 + ((cc ^ (tid & 7)) << 4)) = pk;
-      }
-    }
+    for (int cc = 0; cc < 8; ++cc)
+      *reinterpret_cast<uint4*>(map + tid * 128 + ((cc ^ (tid & 7)) << 4)) = pack8(d + 8 * cc, 1.f);
     tmem_ld32(tlane + 64, d);
     tmem_ld32(tlane + 96, d + 32);
-    float4* nc = reinterpret_cast<float4*>(map + kMcBytes + tid * 256);
+    // Nc row: 16-byte chunk cc stored at chunk position cc ^ (tid & 7)
 #pragma unroll
-    for (int j = 0; j < 16; ++j) nc[j] = make_float4(d[4 * j], d[4 * j + 1], d[4 * j + 2], d[4 * j + 3]);
+    for (int cc = 0; cc < 8; ++cc)
+      *reinterpret_cast<uint4*>(map + kMcBytes + tid * 128 + ((cc ^ (tid & 7)) << 4)) =
+          pack8(d + 8 * cc, 1.f);
     if (tid == 0) *reinterpret_cast<float*>(map + kMcBytes + kNcBytes) = __expf(gC);
   }
 
@@ -410,18 +484,25 @@ teardown:
 }
 
 // ---------------------------------------------------------------------------
-constexpr int kStages = 2;
+constexpr int kStages = 3;
 
 struct ScanSmem {
   unsigned char mc[kStages][kMcBytes];  // A tiles of the state MMA (K-major)
+  unsigned char nc[kStages][kNcBytes];  // Nc rows (bf16, 16-byte chunks swizzled)
   unsigned char sop[8192];              // S as MN-major B operand (rows = m, 64 bf16 along d_v)
-  float nc[kStages][128 * 64];
   float gc[kStages][4];
   uint64_t full[kStages];
   uint64_t mbar;
   uint32_t tmem_base;
   int fail;
 };
+
+__device__ __forceinline__ void issue_map_load(ScanSmem& s, int st, const unsigned char* m) {
+  mbar_expect_tx(&s.full[st], kMcBytes + kNcBytes + 16);
+  bulk_g2s(s.mc[st], m, kMcBytes, &s.full[st]);
+  bulk_g2s(s.nc[st], m + kMcBytes, kNcBytes, &s.full[st]);
+  bulk_g2s(s.gc[st], m + kMcBytes + kNcBytes, 16, &s.full[st]);
+}
 
 __global__ void __launch_bounds__(128) tc_chunk_scan_kernel(ChunkArgs a, int nchunks, int* err) {
   extern __shared__ unsigned char smem_raw[];
@@ -436,20 +517,15 @@ __global__ void __launch_bounds__(128) tc_chunk_scan_kernel(ChunkArgs a, int nch
     mbar_init(&s.mbar, 1);
     fence_mbar_init();
     s.fail = 0;
-    for (int st = 0; st < kStages && st < nchunks; ++st) {
-      const unsigned char* m = ws + (size_t)st * kMapBytes;
-      mbar_expect_tx(&s.full[st], kMcBytes + kNcBytes + 16);
-      bulk_g2s(s.mc[st], m, kMcBytes, &s.full[st]);
-      bulk_g2s(s.nc[st], m + kMcBytes, kNcBytes, &s.full[st]);
-      bulk_g2s(s.gc[st], m + kMcBytes + kNcBytes, 16, &s.full[st]);
-    }
+    for (int st = 0; st < kStages && st < nchunks; ++st)
+      issue_map_load(s, st, ws + (size_t)st * kMapBytes);
   }
   // State: thread t < 64 keeps row t of S in fp32 registers.
   float S[64];
   if (tid < 64) {
 #pragma unroll
     for (int j = 0; j < 64; ++j) S[j] = a.S0 ? a.S0[(bh * 64 + tid) * 64 + j] : 0.f;
-    store_row_bf16(s.sop, tid, S);
+    store_row_scaled(s.sop, tid, S, 1.f);
   }
   fence_async_smem();
   tc_fence_before();
@@ -475,12 +551,26 @@ __global__ void __launch_bounds__(128) tc_chunk_scan_kernel(ChunkArgs a, int nch
     float d[64];
     tmem_ld32(tlane, d);
     tmem_ld32(tlane + 32, d + 32);
-    const float* nrow = s.nc[st] + tid * 64;
+    {
+      // + Nc row tid (16-byte chunk cc at chunk position cc ^ (tid & 7))
+      const unsigned char* nrow = s.nc[st] + tid * 128;
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        const uint4 pk = *reinterpret_cast<const uint4*>(nrow + ((cc ^ (tid & 7)) << 4));
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&pk);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(h[e]);
+          d[8 * cc + 2 * e] += f.x;
+          d[8 * cc + 2 * e + 1] += f.y;
+        }
+      }
+    }
     if (tid < 64) {
       const float gC = s.gc[st][0];
 #pragma unroll
-      for (int j = 0; j < 64; ++j) S[j] = gC * S[j] + d[j] + nrow[j];
-      store_row_bf16(s.sop, tid, S);  // the MMA of this chunk has completed
+      for (int j = 0; j < 64; ++j) S[j] = gC * S[j] + d[j];
+      store_row_scaled(s.sop, tid, S, 1.f);  // the MMA of this chunk has completed
     } else {
       // o row t0 + i straight from registers (16-byte stores; rows past T skipped)
       const int i = tid - 64;
@@ -488,33 +578,14 @@ __global__ void __launch_bounds__(128) tc_chunk_scan_kernel(ChunkArgs a, int nch
       if (t < a.T) {
         uint4* orow = reinterpret_cast<uint4*>(og + (bh * a.T + t) * 64);
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          uint4 pk;
-          __nv_bfloat162 h0 = __floats2bfloat162_rn(d[8 * cc + 0] + nrow[8 * cc + 0], d[8 * cc + 1] + nrow[8 * cc + 1]);
-          __nv_bfloat162 h1 = __floats2bfloat162_rn(d[8 * cc + 2] + nrow[8 * cc + 2], d[8 * cc + 3] + nrow[8 * cc + 3]);
-          __nv_bfloat162 h2 = __floats2bfloat162_rn(d[8 * cc + 4] + nrow[8 * cc + 4], d[8 * cc + 5] + nrow[8 * cc + 5]);
-          __nv_bfloat162 h3 = __floats2bfloat162_rn(d[8 * cc + 6] + nrow[8 * cc + 6], d[8 * cc + 7] + nrow[8 * cc + 7]);
-          pk.x = *reinterpret_cast<uint32_t*>(&h0);
-          pk.y = *reinterpret_cast<uint32_t*>(&h1);
-          pk.z = *reinterpret_cast<uint32_t*>(&h2);
-          pk.w = *reinterpret_cast<uint32_t*>(&h3);
-          orow[cc] = pk;
-        }
+        for (int cc = 0; cc < 8; ++cc) orow[cc] = pack8(d + 8 * cc, 1.f);
       }
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (tid == 0) {
-      const int nx = c + kStages;
-      if (nx < nchunks) {
-        const unsigned char* m = ws + (size_t)nx * kMapBytes;
-        mbar_expect_tx(&s.full[st], kMcBytes + kNcBytes + 16);
-        bulk_g2s(s.mc[st], m, kMcBytes, &s.full[st]);
-        bulk_g2s(s.nc[st], m + kMcBytes, kNcBytes, &s.full[st]);
-        bulk_g2s(s.gc[st], m + kMcBytes + kNcBytes, 16, &s.full[st]);
-      }
-    }
+    if (tid == 0 && c + kStages < nchunks)
+      issue_map_load(s, st, ws + (size_t)(c + kStages) * kMapBytes);
   }
   if (!s.fail && tid < 64)
 #pragma unroll
