@@ -48,29 +48,16 @@ constexpr uint32_t kMapBytes = kMcBytes + kNcBytes + 128;  // + e^{g_C} (padded)
 // e^{a-r} e^{r-b} (both factors stay within fp32 range).
 constexpr float kFactorSpan = 80.f;
 
+// 1024-byte aligned base inside the dynamic shared buffer.  The offset is added
+// to the __shared__ pointer itself (not via an integer round trip), so the
+// compiler keeps the shared address space and emits shared loads and stores.
 __device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
-  return reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(p) + 1023) &
-                                          ~static_cast<uintptr_t>(1023));
+  const uint32_t off = (1024u - (smem_addr(p) & 1023u)) & 1023u;
+  return p + off;
 }
 
 __device__ __forceinline__ void flag_error(int* err) {
   if (err) atomicExch(err, 1);
-}
-
-// Load one 64-element bf16 row from global memory (16-byte vector loads).
-__device__ __forceinline__ void load_row_global(const __nv_bfloat16* src, float* v) {
-  const uint4* p = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const uint4 pk = __ldg(p + c);
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&pk);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 f = __bfloat1622float2(h[e]);
-      v[8 * c + 2 * e] = f.x;
-      v[8 * c + 2 * e + 1] = f.y;
-    }
-  }
 }
 
 // phi in place; returns ||phi(u)||^2.
@@ -143,101 +130,127 @@ __device__ __forceinline__ void frag_b(uint32_t (&b)[2], const float* M, int ld,
   b[1] = pack_bf16(p[8 * ld], p[9 * ld]);
 }
 
-// Shared memory of the map kernel.  Buffers with disjoint lifetimes share space:
-//   R1: [X; Q] (MMA1 operand) -> A (fp32, for the solve) -> [W^T; U~^T] (MMA3 B)
-//   R2: solve scratch (T, right-hand sides, diagonal inverses) -> MMA2 operands
-//       (A = [Xh^T; Vh^T] at +0, B = T at +17408)
-//   A3: MMA3 A operands: Xt tile | zero tile | P tile
-constexpr int kR2Tt = 17408;
-struct MapSmem {
-  union {
-    unsigned char xq[128 * 128];
-    float As[64 * 65];
-    unsigned char b3[128 * 128];
-  } __align__(1024) r1;
-  union {
-    struct {
-      float Ts[64 * 65];    // T = (I + A)^{-1}
-      float Rs[16 * 49];    // block-row right-hand sides
-      float Dinv[64 * 17];  // inverses of the 16 x 16 diagonal blocks (row-wise)
-    } sv;
-    unsigned char mma2[kR2Tt + 8192];  // a2 at +0 (MN-major, two 8 KB atoms), tt at +kR2Tt
-  } __align__(1024) r2;
-  unsigned char a3[3 * 8192] __align__(1024);
+// ---------------------------------------------------------------------------
+// Map kernel.  Shared memory, in bytes from a 1024-aligned base (buffers with
+// disjoint lifetimes share space):
+//   R1  [0, 17408)      [X; Q] (MMA1 operand) -> A (fp32, rows of 68 floats)
+//                       -> T (bf16, MMA2 B) -> [W^T; U~^T] (MMA3 B)
+//   R2  [17408, 37888)  solve scratch (T in fp32 rows of 65, right-hand sides)
+//                       -> Xh rows (atom 0 of MMA2's MN-major A)
+//   VH  [37888, 46080)  v rows as copied in, then Vh rows in place (atom 1)
+//   A3  [46080, 70656)  raw k and q rows as copied in; then Xt | zero | P tiles
+//   SC  [70656, ...)    per-token scalars and barriers
+constexpr uint32_t kOffR1 = 0, kOffR2 = 17408, kOffVH = 37888, kOffA3 = 46080, kOffSC = 70656;
+constexpr uint32_t kLboA2 = kOffVH - kOffR2;  // Xh atom -> Vh atom of MMA2's A operand
+constexpr int kLdA = 68;  // fp32 row stride of A (16-byte aligned rows)
+constexpr int kLdT = 65;  // fp32 row stride of T during the solve
+constexpr int kLdR = 49;  // fp32 row stride of the block right-hand sides
+
+struct MapScalars {
   float eta[64], g[64], gx[64];
   float fu[64], fv[64], fw[64];  // rank-1 decay factors (span <= kFactorSpan)
   float carry;
   int fail;
-  uint64_t bar;
+  uint64_t bar_in, bar_mma;
   uint32_t tmem_base;
 };
+constexpr size_t kMapSmemBytes = kOffSC + sizeof(MapScalars);
 
-// T = (I + A)^{-1} for the strictly lower 64 x 64 A in s.r1.As.  Warp b
-// inverts diagonal block b in fp32 by forward substitution (two lanes per
-// row, eight columns each, rows broadcast by shuffles); block rows b = 1..3
-// then follow T_{b,<b} = Dinv_b (-A_{b,<b} T_{<b}) with warp MMAs.
-__device__ void solve_unit_lower(MapSmem& s) {
+// Read row r of a plain (unswizzled) bf16 tile with 128-byte rows.
+__device__ __forceinline__ void load_row_plain(const unsigned char* tile, int r, float* v) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint4 pk = *reinterpret_cast<const uint4*>(tile + r * 128 + 16 * c);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&pk);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(h[e]);
+      v[8 * c + 2 * e] = f.x;
+      v[8 * c + 2 * e + 1] = f.y;
+    }
+  }
+}
+
+// T = (I + A)^{-1} for the strictly lower 64 x 64 A (rows of kLdA floats).
+// Warp b inverts diagonal block b in fp32 by forward substitution (two lanes
+// per row, eight columns each, rows broadcast by shuffles) and leaves it as the
+// diagonal block of T; block rows b = 1..3 then follow
+// T_{b,<b} = T_bb (-A_{b,<b} T_{<b}) with warp MMAs.
+__device__ void solve_unit_lower(const float* As, float* Ts, float* Rs) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   {
     const int b = warp, r = lane >> 1, h = lane & 1, row = 16 * b + r;
+    float arow[15];
+#pragma unroll
+    for (int k = 0; k < 15; ++k) arow[k] = As[row * kLdA + 16 * b + k];
     float dinv[8];
 #pragma unroll
     for (int jj = 0; jj < 8; ++jj) dinv[jj] = (8 * h + jj == r) ? 1.f : 0.f;
 #pragma unroll
     for (int k = 0; k < 15; ++k) {
-      const float aik = s.r1.As[row * 65 + 16 * b + k];
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj) {
         const float tkj = __shfl_sync(0xffffffffu, dinv[jj], 2 * k + h);
-        if (r > k) dinv[jj] -= aik * tkj;
+        if (r > k) dinv[jj] -= arow[k] * tkj;
       }
     }
 #pragma unroll
-    for (int jj = 0; jj < 8; ++jj) {
-      s.r2.sv.Dinv[row * 17 + 8 * h + jj] = dinv[jj];
-      s.r2.sv.Ts[row * 65 + 16 * b + 8 * h + jj] = dinv[jj];
-    }
+    for (int jj = 0; jj < 8; ++jj) Ts[row * kLdT + 16 * b + 8 * h + jj] = dinv[jj];
   }
   __syncthreads();
   const int g = lane >> 2, t = lane & 3;
   for (int b = 1; b < 4; ++b) {
-    const int w = 16 * b;  // columns to the left of block b: 2b n-tiles of 8
+    const int w = 16 * b;  // columns left of block b: 2b n-tiles of 8
     // R = -A[w:w+16, 0:w] T[0:w, 0:w]; T[k][n] = 0 for k < n, so those k-steps are skipped.
     for (int nt = warp; nt < 2 * b; nt += 4) {
       float d[4] = {0.f, 0.f, 0.f, 0.f};
       for (int kb = nt >> 1; kb < b; ++kb) {
         uint32_t fa[4], fb[2];
-        frag_a(fa, s.r1.As, 65, w, 16 * kb);
-        frag_b(fb, s.r2.sv.Ts, 65, 16 * kb, 8 * nt);
+        frag_a(fa, As, kLdA, w, 16 * kb);
+        frag_b(fb, Ts, kLdT, 16 * kb, 8 * nt);
         mma16816(d, fa, fb);
       }
-      float* r0 = s.r2.sv.Rs + g * 49 + 8 * nt + 2 * t;
+      float* r0 = Rs + g * kLdR + 8 * nt + 2 * t;
       r0[0] = -d[0];
       r0[1] = -d[1];
-      r0[8 * 49] = -d[2];
-      r0[8 * 49 + 1] = -d[3];
+      r0[8 * kLdR] = -d[2];
+      r0[8 * kLdR + 1] = -d[3];
     }
     __syncthreads();
-    // T[w:w+16, 0:w] = Dinv_b R
+    // T[w:w+16, 0:w] = T_bb R  (T_bb: diagonal block b of T)
     for (int nt = warp; nt < 2 * b; nt += 4) {
       float d[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t fa[4], fb[2];
-      frag_a(fa, s.r2.sv.Dinv, 17, w, 0);
-      frag_b(fb, s.r2.sv.Rs, 49, 0, 8 * nt);
+      frag_a(fa, Ts, kLdT, w, w);
+      frag_b(fb, Rs, kLdR, 0, 8 * nt);
       mma16816(d, fa, fb);
-      float* t0 = s.r2.sv.Ts + (w + g) * 65 + 8 * nt + 2 * t;
+      float* t0 = Ts + (w + g) * kLdT + 8 * nt + 2 * t;
       t0[0] = d[0];
       t0[1] = d[1];
-      t0[8 * 65] = d[2];
-      t0[8 * 65 + 1] = d[3];
+      t0[8 * kLdT] = d[2];
+      t0[8 * kLdT + 1] = d[3];
     }
     __syncthreads();
   }
 }
 
-__global__ void __launch_bounds__(128) tc_chunk_map_kernel(ChunkArgs a, int nchunks, int* err) {
+__global__ void __launch_bounds__(128, 3) tc_chunk_map_kernel(ChunkArgs a, int nchunks, int* err) {
   extern __shared__ unsigned char smem_raw[];
-  MapSmem& s = *reinterpret_cast<MapSmem*>(align1024(smem_raw));
+  unsigned char* const base = align1024(smem_raw);
+  unsigned char* const r1 = base + kOffR1;
+  unsigned char* const r2 = base + kOffR2;
+  unsigned char* const vh = base + kOffVH;
+  unsigned char* const a3 = base + kOffA3;
+  MapScalars& sc = *reinterpret_cast<MapScalars*>(base + kOffSC);
+  float* const As = reinterpret_cast<float*>(r1);
+  float* const Ts = reinterpret_cast<float*>(r2);
+  float* const Rs = Ts + 64 * kLdT;
+  unsigned char* const kst = a3;            // raw k rows: row r = k_{t0-1+r}
+  unsigned char* const qst = a3 + 65 * 128;  // raw q rows
+  unsigned char* const xt_tile = a3;          // MN-major A of MMA3a, atom 0
+  unsigned char* const zero_tile = a3 + 8192;  // atom 1 of MMA3a; rows 0..63 of MMA3b
+  unsigned char* const p_tile = a3 + 16384;   // rows 64..127 of MMA3b (K-major)
+
   const int c = blockIdx.x;
   const int64_t bh = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -248,22 +261,29 @@ __global__ void __launch_bounds__(128) tc_chunk_map_kernel(ChunkArgs a, int nchu
   const __nv_bfloat16* kg = reinterpret_cast<const __nv_bfloat16*>(a.k);
   const __nv_bfloat16* vg = reinterpret_cast<const __nv_bfloat16*>(a.v);
   const int64_t rowbase = bh * a.T;
-  unsigned char* const xt_tile = s.a3;         // MN-major A of MMA3a, atom 0
-  unsigned char* const zero_tile = s.a3 + 8192;  // atom 1 of MMA3a, rows 0..63 of MMA3b
-  unsigned char* const p_tile = s.a3 + 16384;  // rows 64..127 of MMA3b (K-major)
-  unsigned char* const a2 = s.r2.mma2;
-  unsigned char* const tt = s.r2.mma2 + kR2Tt;
 
-  if (warp == 0) tmem_alloc(&s.tmem_base, 128);
+  if (warp == 0) tmem_alloc(&sc.tmem_base, 128);
   if (tid == 0) {
-    mbar_init(&s.bar, 1);
+    mbar_init(&sc.bar_in, 1);
+    mbar_init(&sc.bar_mma, 1);
     fence_mbar_init();
-    s.fail = 0;
+    sc.fail = 0;
+    // Every input row of the chunk in flight at once (k rows t0-1 .. t0+n-1).
+    const uint32_t kbytes = (uint32_t)(t0 > 0 ? n + 1 : n) * 128u;
+    const uint32_t rbytes = (uint32_t)n * 128u;
+    mbar_expect_tx(&sc.bar_in, kbytes + 2 * rbytes);
+    bulk_g2s(t0 > 0 ? kst : kst + 128, kg + (rowbase + (t0 > 0 ? t0 - 1 : 0)) * 64, kbytes,
+             &sc.bar_in);
+    bulk_g2s(qst, qg + (rowbase + t0) * 64, rbytes, &sc.bar_in);
+    bulk_g2s(vh, vg + (rowbase + t0) * 64, rbytes, &sc.bar_in);
   }
-  reinterpret_cast<uint4*>(zero_tile)[tid] = make_uint4(0, 0, 0, 0);
-  reinterpret_cast<uint4*>(zero_tile)[tid + 128] = make_uint4(0, 0, 0, 0);
-  reinterpret_cast<uint4*>(zero_tile)[tid + 256] = make_uint4(0, 0, 0, 0);
-  reinterpret_cast<uint4*>(zero_tile)[tid + 384] = make_uint4(0, 0, 0, 0);
+  float beta_t = 0.f, lam_t = 0.f;
+  if (tid < n) {
+    beta_t = a.beta[rowbase + t0 + tid];
+    lam_t = a.lambda[rowbase + t0 + tid];
+  }
+  __syncthreads();
+  if (!mbar_wait(&sc.bar_in, 0)) sc.fail = 1;
 
   // ---- features: thread t < 64 builds the write feature x_t = phi(k_{t0+t-1});
   //      thread 64 + i builds phi(q_{t0+i}).  Rows past the sequence are zero.
@@ -272,7 +292,7 @@ __global__ void __launch_bounds__(128) tc_chunk_map_kernel(ChunkArgs a, int nchu
   if (tid < 64) {
     const int64_t tk = t0 + tid - 1;
     if (tid <= n && tk >= 0) {
-      load_row_global(kg + (rowbase + tk) * 64, x);
+      load_row_plain(kst, tid, x);
       E = apply_phi(x, a.phi);
     } else if (tk < 0 && a.x_prev) {
 #pragma unroll
@@ -289,7 +309,7 @@ __global__ void __launch_bounds__(128) tc_chunk_map_kernel(ChunkArgs a, int nchu
   } else {
     const int i = tid - 64;
     if (i < n) {
-      load_row_global(qg + (rowbase + t0 + i) * 64, x);
+      load_row_plain(qst, i, x);
       apply_phi(x, a.phi);
     } else {
 #pragma unroll
@@ -297,20 +317,19 @@ __global__ void __launch_bounds__(128) tc_chunk_map_kernel(ChunkArgs a, int nchu
     }
     if (a.x_last && c == nchunks - 1 && n == kC && tid == 64) {
       float kl[64];
-      load_row_global(kg + (rowbase + a.T - 1) * 64, kl);
+      load_row_plain(kst, n, kl);  // row n = k_{t0+n-1} = k_{T-1}
       apply_phi(kl, a.phi);
       for (int j = 0; j < 64; ++j) a.x_last[bh * 64 + j] = kl[j];
     }
   }
-  store_row_scaled(s.r1.xq, tid, x, 1.f);
+  store_row_scaled(r1, tid, x, 1.f);  // [X; Q]
 
   // ---- step sizes, log-decays, chunk-local inclusive prefix g ----
   float eta = 0.f, lg = 0.f;
   if (tid < 64 && tid < n) {
     float gam;
     const bool sentinel = (t0 + tid == 0) && (a.x_prev == nullptr);
-    eta = step_eta_gamma(sentinel, E, a.beta[rowbase + t0 + tid], a.lambda[rowbase + t0 + tid],
-                         a.eps, a.eps_gamma, &gam, &lg);
+    eta = step_eta_gamma(sentinel, E, beta_t, lam_t, a.eps, a.eps_gamma, &gam, &lg);
   }
   float incl = lg;
 #pragma unroll
@@ -318,106 +337,113 @@ __global__ void __launch_bounds__(128) tc_chunk_map_kernel(ChunkArgs a, int nchu
     const float y = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += y;
   }
-  if (tid == 31) s.carry = incl;
-  __syncthreads();
-  if (warp == 1) incl += s.carry;
+  if (tid == 31) sc.carry = incl;
+  __syncthreads();  // (also: every raw k and q row has been read)
+  if (warp == 1) incl += sc.carry;
   if (tid < 64) {
-    s.eta[tid] = eta;
-    s.g[tid] = incl;
-    s.gx[tid] = incl - lg;
+    sc.eta[tid] = eta;
+    sc.g[tid] = incl;
+    sc.gx[tid] = incl - lg;
   }
   fence_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = s.tmem_base;
+  const uint32_t tmem = sc.tmem_base;
   const uint32_t tlane = tmem + ((uint32_t)(warp * 32) << 16);
-  const float gC = s.g[kC - 1];
+  const float gC = sc.g[kC - 1];
   const bool factored = -gC <= kFactorSpan;
 
   // ---- MMA1: D[0:64) = [X; Q] X^T ----
-  if (tid == 0) {
-    mma_k64(tmem, smem_addr(s.r1.xq), false, 16, smem_addr(s.r1.xq), false, 16,
+  if (tid == 0 && !sc.fail) {
+    mma_k64(tmem, smem_addr(r1), false, 16, smem_addr(r1), false, 16,
             idesc_bf16(128, 64, false, false), false);
-    mma_commit(&s.bar);
+    mma_commit(&sc.bar_mma);
   }
-  // Meanwhile: Xt = Diag(e^{g_C - g}) X (MMA3a operand) and the rank-1 decay
-  // factors around r = g_C / 2: fu_l = e^{r - g_l}, fv_j = eta_j e^{g_{j-1} - r},
-  // fw_i = e^{g_i - r}.
+  // Meanwhile: the zero tile, Xt = Diag(e^{g_C - g}) X, the rank-1 decay factors
+  // around r = g_C / 2 (fu_l = e^{r - g_l}, fv_j = eta_j e^{g_{j-1} - r},
+  // fw_i = e^{g_i - r}), and Vh = Diag(eta) V in place.
+#pragma unroll
+  for (int z = 0; z < 4; ++z)
+    reinterpret_cast<uint4*>(zero_tile)[tid + 128 * z] = make_uint4(0u, 0u, 0u, 0u);
   if (tid < 64) {
-    store_row_scaled(xt_tile, tid, x, __expf(gC - s.g[tid]));
+    store_row_scaled(xt_tile, tid, x, __expf(gC - sc.g[tid]));
     if (factored) {
       const float r = 0.5f * gC;
-      s.fu[tid] = __expf(r - s.g[tid]);
-      s.fv[tid] = s.eta[tid] * __expf(s.gx[tid] - r);
-      s.fw[tid] = __expf(s.g[tid] - r);
+      sc.fu[tid] = __expf(r - sc.g[tid]);
+      sc.fv[tid] = sc.eta[tid] * __expf(sc.gx[tid] - r);
+      sc.fw[tid] = __expf(sc.g[tid] - r);
     }
+  } else {
+    const int i = tid - 64;
+    float v[64];
+    if (i < n) {
+      load_row_plain(vh, i, v);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 64; ++j) v[j] = 0.f;
+    }
+    store_row_scaled(vh, i, v, sc.eta[i]);
   }
-  if (!mbar_wait(&s.bar, 0)) s.fail = 1;
+  if (!sc.fail && !mbar_wait(&sc.bar_mma, 0)) sc.fail = 1;
   tc_fence_after();
-  __syncthreads();  // fu/fv/fw visible
+  __syncthreads();  // fu/fv/fw visible; MMA1 has finished reading [X; Q]
   {
     float d[64];
     tmem_ld32(tlane, d);
     tmem_ld32(tlane + 32, d + 32);
     if (tid < 64) {
-      // A row j: eta_j e^{g_{j-1} - g_l} G[j][l] for l < j
+      // A row j: eta_j e^{g_{j-1} - g_l} G[j][l] for l < j (all loads, then the stores)
       const int j = tid;
       if (f1) {
         if (factored) {
-          const float vj = s.fv[j];
+          const float vj = sc.fv[j];
 #pragma unroll
-          for (int l = 0; l < 64; ++l) s.r1.As[j * 65 + l] = (l < j) ? vj * s.fu[l] * d[l] : 0.f;
+          for (int l = 0; l < 64; ++l) d[l] = (l < j) ? vj * sc.fu[l] * d[l] : 0.f;
         } else {
-          const float ej = s.eta[j], gxj = s.gx[j];
+          const float ej = sc.eta[j], gxj = sc.gx[j];
 #pragma unroll
           for (int l = 0; l < 64; ++l)
-            s.r1.As[j * 65 + l] = (l < j) ? ej * __expf(fminf(gxj - s.g[l], 0.f)) * d[l] : 0.f;
+            d[l] = (l < j) ? ej * __expf(fminf(gxj - sc.g[l], 0.f)) * d[l] : 0.f;
         }
+        float4* arow = reinterpret_cast<float4*>(As + j * kLdA);
+#pragma unroll
+        for (int l4 = 0; l4 < 16; ++l4)
+          arow[l4] = make_float4(d[4 * l4], d[4 * l4 + 1], d[4 * l4 + 2], d[4 * l4 + 3]);
       }
     } else {
       // P row i: e^{g_i - g_j} (Q X^T)[i][j] for j <= i
       const int i = tid - 64;
       if (factored) {
-        const float wi = s.fw[i];
+        const float wi = sc.fw[i];
 #pragma unroll
-        for (int jj = 0; jj < 64; ++jj) d[jj] = (jj <= i) ? wi * s.fu[jj] * d[jj] : 0.f;
+        for (int jj = 0; jj < 64; ++jj) d[jj] = (jj <= i) ? wi * sc.fu[jj] * d[jj] : 0.f;
       } else {
-        const float gi = s.g[i];
+        const float gi = sc.g[i];
 #pragma unroll
         for (int jj = 0; jj < 64; ++jj)
-          d[jj] = (jj <= i) ? __expf(fminf(gi - s.g[jj], 0.f)) * d[jj] : 0.f;
+          d[jj] = (jj <= i) ? __expf(fminf(gi - sc.g[jj], 0.f)) * d[jj] : 0.f;
       }
       store_row_scaled(p_tile, i, d, 1.f);
     }
   }
   __syncthreads();
-  if (__syncthreads_or(s.fail)) goto teardown;
+  if (__syncthreads_or(sc.fail)) goto teardown;
 
   // ---- T = (I + A)^{-1} (identity for Falcon-1A), then the MMA2 operands ----
-  if (f1) solve_unit_lower(s);
+  if (f1) solve_unit_lower(As, Ts, Rs);
   if (tid < 64) {
-    // T row tid as bf16: the solve result left of and in the diagonal block, zero beyond.
+    // T row tid as bf16 into R1 (A is dead): the solve result up to the end of
+    // the diagonal block, zero beyond.
     float trow[64];
     const int end = (tid | 15) + 1;
 #pragma unroll
     for (int j = 0; j < 64; ++j)
-      trow[j] = f1 ? ((j < end) ? s.r2.sv.Ts[tid * 65 + j] : 0.f) : ((j == tid) ? 1.f : 0.f);
-    store_row_scaled(tt, tid, trow, 1.f);
+      trow[j] = f1 ? ((j < end) ? Ts[tid * kLdT + j] : 0.f) : ((j == tid) ? 1.f : 0.f);
+    store_row_scaled(r1, tid, trow, 1.f);
   }
-  __syncthreads();  // the MMA2 A operand overwrites the solve scratch
-  if (tid < 64) {
-    store_row_scaled(a2, tid, x, f1 ? s.eta[tid] * __expf(s.gx[tid]) : 0.f);
-  } else {
-    const int i = tid - 64;
-    float v[64];
-    if (i < n)
-      load_row_global(vg + (rowbase + t0 + i) * 64, v);
-    else
-#pragma unroll
-      for (int j = 0; j < 64; ++j) v[j] = 0.f;
-    store_row_scaled(a2 + 8192, i, v, s.eta[i]);
-  }
+  __syncthreads();  // Xh overwrites the solve scratch
+  if (tid < 64) store_row_scaled(r2, tid, x, f1 ? sc.eta[tid] * __expf(sc.gx[tid]) : 0.f);
   fence_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -425,42 +451,42 @@ __global__ void __launch_bounds__(128) tc_chunk_map_kernel(ChunkArgs a, int nchu
 
   // ---- MMA2: D[0:64) = [Xh^T; Vh^T] T^T = [W^T; U~^T] ----
   if (tid == 0) {
-    mma_k64(tmem, smem_addr(a2), true, 8192, smem_addr(tt), false, 16,
+    mma_k64(tmem, smem_addr(r2), true, kLboA2, smem_addr(r1), false, 16,
             idesc_bf16(128, 64, true, false), false);
-    mma_commit(&s.bar);
+    mma_commit(&sc.bar_mma);
   }
-  if (!mbar_wait(&s.bar, 1)) s.fail = 1;
+  if (!mbar_wait(&sc.bar_mma, 1)) sc.fail = 1;
   tc_fence_after();
   {
     float d[64];
     tmem_ld32(tlane, d);
     tmem_ld32(tlane + 32, d + 32);
-    store_row_scaled(s.r1.b3, tid, d, 1.f);
+    store_row_scaled(r1, tid, d, 1.f);  // [W^T; U~^T] over T (MMA2 is complete)
   }
   fence_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (__syncthreads_or(s.fail)) goto teardown;
+  if (__syncthreads_or(sc.fail)) goto teardown;
 
   // ---- MMA3: D[0:128) = [Xt^T; 0] [W | U~] + [0; P] [W | U~] ----
   if (tid == 0) {
-    mma_k64(tmem, smem_addr(xt_tile), true, 8192, smem_addr(s.r1.b3), false, 16,
+    mma_k64(tmem, smem_addr(xt_tile), true, 8192, smem_addr(r1), false, 16,
             idesc_bf16(128, 128, true, false), false);
-    mma_k64(tmem, smem_addr(zero_tile), false, 16, smem_addr(s.r1.b3), false, 16,
+    mma_k64(tmem, smem_addr(zero_tile), false, 16, smem_addr(r1), false, 16,
             idesc_bf16(128, 128, false, false), true);
-    mma_commit(&s.bar);
+    mma_commit(&sc.bar_mma);
   }
-  if (!mbar_wait(&s.bar, 0)) s.fail = 1;
+  if (!mbar_wait(&sc.bar_mma, 0)) sc.fail = 1;
   tc_fence_after();
-  if (!__syncthreads_or(s.fail)) {
+  if (!__syncthreads_or(sc.fail)) {
     unsigned char* map = reinterpret_cast<unsigned char*>(a.workspace) +
                          (size_t)(bh * nchunks + c) * kMapBytes;
     float d[64];
     tmem_ld32(tlane, d);
     tmem_ld32(tlane + 32, d + 32);
     // Mc row: rows < 64 -> -Xt^T W ; rows >= 64 -> e^{g_i} q_i - P W
-    const float eg = (tid >= 64) ? __expf(s.g[tid - 64]) : 0.f;
+    const float eg = (tid >= 64) ? __expf(sc.g[tid - 64]) : 0.f;
 #pragma unroll
     for (int j = 0; j < 64; ++j) d[j] = (tid < 64) ? -d[j] : eg * x[j] - d[j];
 #pragma unroll
@@ -477,13 +503,18 @@ __global__ void __launch_bounds__(128) tc_chunk_map_kernel(ChunkArgs a, int nchu
   }
 
 teardown:
-  if (s.fail && tid == 0) flag_error(err);
+  if (sc.fail && tid == 0) flag_error(err);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
 // ---------------------------------------------------------------------------
+// Scan kernel.  Roles within the CTA: threads 0..63 own the state rows (the
+// critical path: MMA -> state update -> next B operand); threads 64..127 own
+// the output rows and refill the map pipeline.  mbarriers hand off between
+// the roles, the accumulator is double-buffered in TMEM, so the output rows
+// of chunk c are written while the MMA of chunk c+1 runs.
 constexpr int kStages = 3;
 
 struct ScanSmem {
@@ -491,8 +522,11 @@ struct ScanSmem {
   unsigned char nc[kStages][kNcBytes];  // Nc rows (bf16, 16-byte chunks swizzled)
   unsigned char sop[8192];              // S as MN-major B operand (rows = m, 64 bf16 along d_v)
   float gc[kStages][4];
-  uint64_t full[kStages];
-  uint64_t mbar;
+  uint64_t full[kStages];   // map of the stage has arrived
+  uint64_t empty[kStages];  // all 128 threads are done with the stage
+  uint64_t mma_done[2];     // MMA into accumulator buffer b has completed
+  uint64_t o_done[2];       // output rows have read accumulator buffer b
+  uint64_t s_ready;         // the next state operand is in sop
   uint32_t tmem_base;
   int fail;
 };
@@ -507,27 +541,27 @@ __device__ __forceinline__ void issue_map_load(ScanSmem& s, int st, const unsign
 __global__ void __launch_bounds__(128) tc_chunk_scan_kernel(ChunkArgs a, int nchunks, int* err) {
   extern __shared__ unsigned char smem_raw[];
   ScanSmem& s = *reinterpret_cast<ScanSmem*>(align1024(smem_raw));
+  volatile int* fail = &s.fail;
   const int64_t bh = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5;
   const unsigned char* ws = reinterpret_cast<const unsigned char*>(a.workspace) +
                             (size_t)bh * nchunks * kMapBytes;
-  if (warp == 0) tmem_alloc(&s.tmem_base, 64);
+  if (warp == 0) tmem_alloc(&s.tmem_base, 128);
   if (tid == 0) {
-    for (int st = 0; st < kStages; ++st) mbar_init(&s.full[st], 1);
-    mbar_init(&s.mbar, 1);
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(&s.full[st], 1);
+      mbar_init(&s.empty[st], 128);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s.mma_done[b], 1);
+      mbar_init(&s.o_done[b], 64);
+    }
+    mbar_init(&s.s_ready, 64);
     fence_mbar_init();
     s.fail = 0;
     for (int st = 0; st < kStages && st < nchunks; ++st)
       issue_map_load(s, st, ws + (size_t)st * kMapBytes);
   }
-  // State: thread t < 64 keeps row t of S in fp32 registers.
-  float S[64];
-  if (tid < 64) {
-#pragma unroll
-    for (int j = 0; j < 64; ++j) S[j] = a.S0 ? a.S0[(bh * 64 + tid) * 64 + j] : 0.f;
-    store_row_scaled(s.sop, tid, S, 1.f);
-  }
-  fence_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -535,22 +569,40 @@ __global__ void __launch_bounds__(128) tc_chunk_scan_kernel(ChunkArgs a, int nch
   const uint32_t tlane = tmem + ((uint32_t)(warp * 32) << 16);
   __nv_bfloat16* og = reinterpret_cast<__nv_bfloat16*>(a.o);
 
+  // State: thread t < 64 keeps row t of S in fp32 registers.
+  float S[64];
+  if (tid < 64) {
+#pragma unroll
+    for (int j = 0; j < 64; ++j) S[j] = a.S0 ? a.S0[(bh * 64 + tid) * 64 + j] : 0.f;
+    store_row_scaled(s.sop, tid, S, 1.f);
+    fence_async_smem();
+    mbar_arrive(&s.s_ready);
+  }
+
   for (int c = 0; c < nchunks; ++c) {
-    const int st = c % kStages;
-    const uint32_t par = (uint32_t)(c / kStages) & 1u;
-    if (!mbar_wait(&s.full[st], par)) s.fail = 1;
-    if (tid == 0 && !s.fail) {
-      tc_fence_after();
-      mma_k64(tmem, smem_addr(s.mc[st]), false, 16, smem_addr(s.sop), true, 8192,
-              idesc_bf16(128, 64, false, true), false);
-      mma_commit(&s.mbar);
+    if (*fail) break;
+    const int st = c % kStages, b = c & 1;
+    if (tid == 0) {
+      bool ok = mbar_wait(&s.full[st], (uint32_t)(c / kStages) & 1u);
+      ok = ok && mbar_wait(&s.s_ready, (uint32_t)c & 1u);
+      if (c >= 2) ok = ok && mbar_wait(&s.o_done[b], (uint32_t)((c - 2) >> 1) & 1u);
+      if (ok) {
+        tc_fence_after();
+        mma_k64(tmem + 64 * b, smem_addr(s.mc[st]), false, 16, smem_addr(s.sop), true, 8192,
+                idesc_bf16(128, 64, false, true), false);
+        mma_commit(&s.mma_done[b]);
+      } else {
+        *fail = 1;
+      }
     }
-    if (!s.fail && !mbar_wait(&s.mbar, (uint32_t)c & 1u)) s.fail = 1;
-    if (__syncthreads_or(s.fail)) break;
+    if (!mbar_wait(&s.mma_done[b], (uint32_t)(c >> 1) & 1u)) {
+      *fail = 1;
+      break;
+    }
     tc_fence_after();
     float d[64];
-    tmem_ld32(tlane, d);
-    tmem_ld32(tlane + 32, d + 32);
+    tmem_ld32(tlane + 64 * b, d);
+    tmem_ld32(tlane + 64 * b + 32, d + 32);
     {
       // + Nc row tid (16-byte chunk cc at chunk position cc ^ (tid & 7))
       const unsigned char* nrow = s.nc[st] + tid * 128;
@@ -566,12 +618,17 @@ __global__ void __launch_bounds__(128) tc_chunk_scan_kernel(ChunkArgs a, int nch
         }
       }
     }
+    const float gC = s.gc[st][0];
+    tc_fence_before();
+    mbar_arrive(&s.empty[st]);
     if (tid < 64) {
-      const float gC = s.gc[st][0];
 #pragma unroll
       for (int j = 0; j < 64; ++j) S[j] = gC * S[j] + d[j];
       store_row_scaled(s.sop, tid, S, 1.f);  // the MMA of this chunk has completed
+      fence_async_smem();
+      mbar_arrive(&s.s_ready);
     } else {
+      mbar_arrive(&s.o_done[b]);
       // o row t0 + i straight from registers (16-byte stores; rows past T skipped)
       const int i = tid - 64;
       const int64_t t = (int64_t)c * kC + i;
@@ -580,20 +637,22 @@ __global__ void __launch_bounds__(128) tc_chunk_scan_kernel(ChunkArgs a, int nch
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) orow[cc] = pack8(d + 8 * cc, 1.f);
       }
+      if (tid == 64 && c + kStages < nchunks) {
+        if (mbar_wait(&s.empty[st], (uint32_t)(c / kStages) & 1u))
+          issue_map_load(s, st, ws + (size_t)(c + kStages) * kMapBytes);
+        else
+          *fail = 1;
+      }
     }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0 && c + kStages < nchunks)
-      issue_map_load(s, st, ws + (size_t)(c + kStages) * kMapBytes);
   }
-  if (!s.fail && tid < 64)
+  if (!*fail && tid < 64)
 #pragma unroll
     for (int j = 0; j < 64; ++j) a.S_out[(bh * 64 + tid) * 64 + j] = S[j];
-  if (s.fail && tid == 0) flag_error(err);
+  __syncthreads();
+  if (*fail && tid == 0) flag_error(err);
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 64);
+  if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
 }  // namespace
@@ -609,7 +668,7 @@ size_t tc_workspace_bytes(int64_t BH, int64_t T) {
 
 cudaError_t launch_tc_chunked(const ChunkArgs& a, int* err, cudaStream_t stream) {
   const int nchunks = (int)((a.T + kC - 1) / kC);
-  const size_t map_smem = sizeof(MapSmem) + 1024;
+  const size_t map_smem = kMapSmemBytes + 1024;
   cudaError_t e = cudaFuncSetAttribute(tc_chunk_map_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)map_smem);
   if (e != cudaSuccess) return e;
