@@ -60,19 +60,17 @@ __device__ __forceinline__ void flag_error(int* err) {
   if (err) atomicExch(err, 1);
 }
 
-// phi in place; returns ||phi(u)||^2.
+// phi in place; returns ||phi(u)||^2 (eight independent partial sums).
 __device__ __forceinline__ float apply_phi(float* v, int phi) {
-  float ss = 0.f;
+  float p[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int j = 0; j < 64; ++j) ss += v[j] * v[j];
+  for (int j = 0; j < 64; ++j) p[j & 7] += v[j] * v[j];
+  float ss = ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
   if (phi == FALCON_PHI_L2) {
     const float inv = 1.f / fmaxf(sqrtf(ss), 1e-12f);
-    ss = 0.f;
 #pragma unroll
-    for (int j = 0; j < 64; ++j) {
-      v[j] *= inv;
-      ss += v[j] * v[j];
-    }
+    for (int j = 0; j < 64; ++j) v[j] *= inv;
+    ss *= inv * inv;
   }
   return ss;
 }
@@ -427,8 +425,7 @@ __global__ void __launch_bounds__(128, 3) tc_chunk_map_kernel(ChunkArgs a, int n
       store_row_scaled(p_tile, i, d, 1.f);
     }
   }
-  __syncthreads();
-  if (__syncthreads_or(sc.fail)) goto teardown;
+  if (__syncthreads_or(sc.fail)) goto teardown;  // A and P complete
 
   // ---- T = (I + A)^{-1} (identity for Falcon-1A), then the MMA2 operands ----
   if (f1) solve_unit_lower(As, Ts, Rs);
@@ -465,9 +462,8 @@ __global__ void __launch_bounds__(128, 3) tc_chunk_map_kernel(ChunkArgs a, int n
   }
   fence_async_smem();
   tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
   if (__syncthreads_or(sc.fail)) goto teardown;
+  tc_fence_after();
 
   // ---- MMA3: D[0:128) = [Xt^T; 0] [W | U~] + [0; P] [W | U~] ----
   if (tid == 0) {
@@ -503,6 +499,7 @@ __global__ void __launch_bounds__(128, 3) tc_chunk_map_kernel(ChunkArgs a, int n
   }
 
 teardown:
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (sc.fail && tid == 0) flag_error(err);
   tc_fence_before();
   __syncthreads();
@@ -510,12 +507,14 @@ teardown:
 }
 
 // ---------------------------------------------------------------------------
-// Scan kernel.  Roles within the CTA: threads 0..63 own the state rows (the
-// critical path: MMA -> state update -> next B operand); threads 64..127 own
-// the output rows and refill the map pipeline.  mbarriers hand off between
-// the roles, the accumulator is double-buffered in TMEM, so the output rows
-// of chunk c are written while the MMA of chunk c+1 runs.
+// Scan kernel, 256 threads per head.  TMEM lane rules give warps 0,1,4,5 the
+// state rows (lanes 0..63) and warps 2,3,6,7 the output rows (lanes 64..127);
+// warps 0..3 take columns 0..31 of their rows and warps 4..7 columns 32..63.
+// The state path (MMA -> state update -> next B operand) is the critical
+// chain; the output rows and the refills of the map pipeline run beside it,
+// handed off through mbarriers, with a double-buffered TMEM accumulator.
 constexpr int kStages = 3;
+constexpr int kScanThreads = 256;
 
 struct ScanSmem {
   unsigned char mc[kStages][kMcBytes];  // A tiles of the state MMA (K-major)
@@ -523,7 +522,7 @@ struct ScanSmem {
   unsigned char sop[8192];              // S as MN-major B operand (rows = m, 64 bf16 along d_v)
   float gc[kStages][4];
   uint64_t full[kStages];   // map of the stage has arrived
-  uint64_t empty[kStages];  // all 128 threads are done with the stage
+  uint64_t empty[kStages];  // every thread is done with the stage
   uint64_t mma_done[2];     // MMA into accumulator buffer b has completed
   uint64_t o_done[2];       // output rows have read accumulator buffer b
   uint64_t s_ready;         // the next state operand is in sop
@@ -538,43 +537,55 @@ __device__ __forceinline__ void issue_map_load(ScanSmem& s, int st, const unsign
   bulk_g2s(s.gc[st], m + kMcBytes + kNcBytes, 16, &s.full[st]);
 }
 
-__global__ void __launch_bounds__(128) tc_chunk_scan_kernel(ChunkArgs a, int nchunks, int* err) {
+__global__ void __launch_bounds__(kScanThreads) tc_chunk_scan_kernel(ChunkArgs a, int nchunks,
+                                                                     int* err) {
   extern __shared__ unsigned char smem_raw[];
   ScanSmem& s = *reinterpret_cast<ScanSmem*>(align1024(smem_raw));
   volatile int* fail = &s.fail;
   const int64_t bh = blockIdx.x;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row = 32 * (warp & 3) + lane;  // TMEM lane = row of [S'; O]
+  const int h = warp >> 2;                 // column half: 32h .. 32h+31
+  const bool srow = row < 64;
   const unsigned char* ws = reinterpret_cast<const unsigned char*>(a.workspace) +
                             (size_t)bh * nchunks * kMapBytes;
   if (warp == 0) tmem_alloc(&s.tmem_base, 128);
   if (tid == 0) {
     for (int st = 0; st < kStages; ++st) {
       mbar_init(&s.full[st], 1);
-      mbar_init(&s.empty[st], 128);
+      mbar_init(&s.empty[st], kScanThreads);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s.mma_done[b], 1);
-      mbar_init(&s.o_done[b], 64);
+      mbar_init(&s.o_done[b], kScanThreads / 2);
     }
-    mbar_init(&s.s_ready, 64);
+    mbar_init(&s.s_ready, kScanThreads / 2);
     fence_mbar_init();
     s.fail = 0;
-    for (int st = 0; st < kStages && st < nchunks; ++st)
-      issue_map_load(s, st, ws + (size_t)st * kMapBytes);
+  }
+  // State: each state thread keeps 32 columns of its row in fp32 registers.
+  float S[32];
+  if (srow) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) S[j] = a.S0 ? a.S0[(bh * 64 + row) * 64 + 32 * h + j] : 0.f;
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // The maps are written by the preceding launch: wait for it to complete.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (tid == 0)
+    for (int st = 0; st < kStages && st < nchunks; ++st)
+      issue_map_load(s, st, ws + (size_t)st * kMapBytes);
   const uint32_t tmem = s.tmem_base;
-  const uint32_t tlane = tmem + ((uint32_t)(warp * 32) << 16);
+  const uint32_t tlane = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 32 * h;
   __nv_bfloat16* og = reinterpret_cast<__nv_bfloat16*>(a.o);
 
-  // State: thread t < 64 keeps row t of S in fp32 registers.
-  float S[64];
-  if (tid < 64) {
+  if (srow) {
 #pragma unroll
-    for (int j = 0; j < 64; ++j) S[j] = a.S0 ? a.S0[(bh * 64 + tid) * 64 + j] : 0.f;
-    store_row_scaled(s.sop, tid, S, 1.f);
+    for (int q = 0; q < 4; ++q)
+      *reinterpret_cast<uint4*>(s.sop + row * 128 + (((4 * h + q) ^ (row & 7)) << 4)) =
+          pack8(S + 8 * q, 1.f);
     fence_async_smem();
     mbar_arrive(&s.s_ready);
   }
@@ -600,42 +611,43 @@ __global__ void __launch_bounds__(128) tc_chunk_scan_kernel(ChunkArgs a, int nch
       break;
     }
     tc_fence_after();
-    float d[64];
+    float d[32];
     tmem_ld32(tlane + 64 * b, d);
-    tmem_ld32(tlane + 64 * b + 32, d + 32);
     {
-      // + Nc row tid (16-byte chunk cc at chunk position cc ^ (tid & 7))
-      const unsigned char* nrow = s.nc[st] + tid * 128;
+      // + Nc row, columns 32h..32h+31 (16-byte chunk cc at position cc ^ (row & 7))
+      const unsigned char* nrow = s.nc[st] + row * 128;
 #pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        const uint4 pk = *reinterpret_cast<const uint4*>(nrow + ((cc ^ (tid & 7)) << 4));
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&pk);
+      for (int q = 0; q < 4; ++q) {
+        const uint4 pk = *reinterpret_cast<const uint4*>(nrow + (((4 * h + q) ^ (row & 7)) << 4));
+        const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&pk);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float2 f = __bfloat1622float2(h[e]);
-          d[8 * cc + 2 * e] += f.x;
-          d[8 * cc + 2 * e + 1] += f.y;
+          const float2 f = __bfloat1622float2(hv[e]);
+          d[8 * q + 2 * e] += f.x;
+          d[8 * q + 2 * e + 1] += f.y;
         }
       }
     }
     const float gC = s.gc[st][0];
     tc_fence_before();
     mbar_arrive(&s.empty[st]);
-    if (tid < 64) {
+    if (srow) {
 #pragma unroll
-      for (int j = 0; j < 64; ++j) S[j] = gC * S[j] + d[j];
-      store_row_scaled(s.sop, tid, S, 1.f);  // the MMA of this chunk has completed
+      for (int j = 0; j < 32; ++j) S[j] = gC * S[j] + d[j];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)  // the MMA of this chunk has completed
+        *reinterpret_cast<uint4*>(s.sop + row * 128 + (((4 * h + q) ^ (row & 7)) << 4)) =
+            pack8(S + 8 * q, 1.f);
       fence_async_smem();
       mbar_arrive(&s.s_ready);
     } else {
       mbar_arrive(&s.o_done[b]);
-      // o row t0 + i straight from registers (16-byte stores; rows past T skipped)
-      const int i = tid - 64;
-      const int64_t t = (int64_t)c * kC + i;
+      // o row t, columns 32h..32h+31 (rows past T skipped)
+      const int64_t t = (int64_t)c * kC + (row - 64);
       if (t < a.T) {
-        uint4* orow = reinterpret_cast<uint4*>(og + (bh * a.T + t) * 64);
+        uint4* orow = reinterpret_cast<uint4*>(og + (bh * a.T + t) * 64 + 32 * h);
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) orow[cc] = pack8(d + 8 * cc, 1.f);
+        for (int q = 0; q < 4; ++q) orow[q] = pack8(d + 8 * q, 1.f);
       }
       if (tid == 64 && c + kStages < nchunks) {
         if (mbar_wait(&s.empty[st], (uint32_t)(c / kStages) & 1u))
@@ -645,9 +657,9 @@ __global__ void __launch_bounds__(128) tc_chunk_scan_kernel(ChunkArgs a, int nch
       }
     }
   }
-  if (!*fail && tid < 64)
+  if (!*fail && srow)
 #pragma unroll
-    for (int j = 0; j < 64; ++j) a.S_out[(bh * 64 + tid) * 64 + j] = S[j];
+    for (int j = 0; j < 32; ++j) a.S_out[(bh * 64 + row) * 64 + 32 * h + j] = S[j];
   __syncthreads();
   if (*fail && tid == 0) flag_error(err);
   tc_fence_before();
@@ -679,8 +691,19 @@ cudaError_t launch_tc_chunked(const ChunkArgs& a, int* err, cudaStream_t stream)
   e = cudaFuncSetAttribute(tc_chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)scan_smem);
   if (e != cudaSuccess) return e;
-  tc_chunk_scan_kernel<<<(unsigned)a.BH, 128, scan_smem, stream>>>(a, nchunks, err);
-  return cudaGetLastError();
+  // Programmatic dependent launch: the scan grid may be scheduled while the map
+  // grid drains; griddepcontrol.wait in the scan orders it after every map write.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)a.BH);
+  cfg.blockDim = dim3(kScanThreads);
+  cfg.dynamicSmemBytes = scan_smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc_chunk_scan_kernel, a, nchunks, err);
 }
 
 }  // namespace falcon
