@@ -478,6 +478,11 @@ __global__ void __launch_bounds__(128, 3) tc_chunk_map_kernel(ChunkArgs a, int n
   if (!__syncthreads_or(sc.fail)) {
     unsigned char* map = reinterpret_cast<unsigned char*>(a.workspace) +
                          (size_t)(bh * nchunks + c) * kMapBytes;
+    // The map images are staged in shared memory (the MMA3 operands are dead)
+    // and leave in two bulk copies: row-scattered 16-byte global stores would
+    // touch a different 128-byte line per thread.
+    unsigned char* mc_stage = a3;  // 16 KB
+    unsigned char* nc_stage = r1;  // 16 KB
     float d[64];
     tmem_ld32(tlane, d);
     tmem_ld32(tlane + 32, d + 32);
@@ -487,15 +492,24 @@ __global__ void __launch_bounds__(128, 3) tc_chunk_map_kernel(ChunkArgs a, int n
     for (int j = 0; j < 64; ++j) d[j] = (tid < 64) ? -d[j] : eg * x[j] - d[j];
 #pragma unroll
     for (int cc = 0; cc < 8; ++cc)
-      *reinterpret_cast<uint4*>(map + tid * 128 + ((cc ^ (tid & 7)) << 4)) = pack8(d + 8 * cc, 1.f);
+      *reinterpret_cast<uint4*>(mc_stage + tid * 128 + ((cc ^ (tid & 7)) << 4)) =
+          pack8(d + 8 * cc, 1.f);
     tmem_ld32(tlane + 64, d);
     tmem_ld32(tlane + 96, d + 32);
     // Nc row: 16-byte chunk cc stored at chunk position cc ^ (tid & 7)
 #pragma unroll
     for (int cc = 0; cc < 8; ++cc)
-      *reinterpret_cast<uint4*>(map + kMcBytes + tid * 128 + ((cc ^ (tid & 7)) << 4)) =
+      *reinterpret_cast<uint4*>(nc_stage + tid * 128 + ((cc ^ (tid & 7)) << 4)) =
           pack8(d + 8 * cc, 1.f);
-    if (tid == 0) *reinterpret_cast<float*>(map + kMcBytes + kNcBytes) = __expf(gC);
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      *reinterpret_cast<float*>(map + kMcBytes + kNcBytes) = __expf(gC);
+      bulk_s2g(map, mc_stage, kMcBytes);
+      bulk_s2g(map + kMcBytes, nc_stage, kNcBytes);
+      bulk_commit();
+      bulk_wait<0>();  // the staging must outlive the copies; the map is complete
+    }
   }
 
 teardown:
