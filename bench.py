@@ -179,8 +179,10 @@ def barrier(ws):
 
 
 def max_over_ranks(x, ws):
+    """The slowest rank's time (NCCL on the GPU machine, gloo on a CPU host)."""
     if ws > 1:
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         return float(t.item())
     return x

@@ -32,6 +32,7 @@ EXPORTS = (
     "falcon_workspace_bytes", "falcon1_fwd_chunked", "falcon1a_fwd_chunked",
     "falcon1_decode_step", "falcon1a_decode_step", "falcon_sync_check",
     "falcon_strerror", "falcon_version", "falcon1_fwd_chunked_fixed_scratch",
+    "falcon_selftest_wait_timeout",
 )
 FALCON_ERR_SCRATCH_LIMIT = -10
 FALCON_FIXED_SCRATCH_BYTES = 16 * 1024 * 1024
@@ -83,6 +84,8 @@ def load_library(path: str | None = None):
         lib.falcon1_fwd_chunked_fixed_scratch.restype = ctypes.c_int
         lib.falcon1_fwd_chunked_fixed_scratch.argtypes = [shp, vp, vp, vp, f32p, f32p, f32p,
                                                           f32p, vp, f32p, f32p, vp]
+        lib.falcon_selftest_wait_timeout.restype = ctypes.c_int
+        lib.falcon_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
         lib.falcon_sync_check.restype = ctypes.c_int
         lib.falcon_sync_check.argtypes = [vp]
         lib.falcon_strerror.restype = ctypes.c_char_p
@@ -272,6 +275,14 @@ def falcon1a_decode_step(q, k, v, beta, lam, S, x_prev, fresh=None, phi="l2", ep
 def falcon_sync_check(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device error status."""
     return int(load_library().falcon_sync_check(_stream(stream)))
+
+
+def falcon_selftest_wait_timeout(limit_us: int = 20000, stream=None) -> None:
+    """Run the failure-path diagnostic: a kernel whose wait can never complete
+    gives up after limit_us and records the expiry in the device error word
+    (read it with falcon_sync_check, which then returns FALCON_ERR_TIMEOUT)."""
+    _check(load_library().falcon_selftest_wait_timeout(int(limit_us), _stream(stream)),
+           "falcon_selftest_wait_timeout")
 
 
 def falcon_version() -> int:

@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 namespace falcon {
 // Device error word: set by a kernel whose bounded wait gave up, read and
@@ -132,6 +133,21 @@ int fwd_chunked(int rule, const falcon_shape* s, const void* q, const void* k, c
   return to_status(falcon::launch_generic_chunked(a, stream));
 }
 
+// Failure-path diagnostic: every thread waits on an mbarrier that nothing
+// completes, gives up after limit_ns and records the expiry in the device
+// error word (the same path the tensor-core kernels take on a lost wait).
+__global__ void wait_timeout_kernel(uint64_t limit_ns, int* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    falcon::tc::mbar_init(&bar, 1);
+    falcon::tc::fence_mbar_init();
+  }
+  __syncthreads();
+  const bool ok = falcon::tc::mbar_wait(&bar, 0, limit_ns);
+  if (!__syncthreads_or(!ok)) return;
+  if (threadIdx.x == 0) atomicExch(err, 1);
+}
+
 int decode(int rule, int64_t N, int32_t m, int32_t dv, int32_t dtype, int32_t phi, float eps,
            float eps_gamma, const void* q, const void* k, const void* v, const float* beta,
            const float* lambda, float* S, float* x_prev, const uint8_t* fresh, void* o,
@@ -208,6 +224,16 @@ int falcon1a_decode_step(int64_t N, int32_t m, int32_t dv, int32_t dtype, int32_
                          const uint8_t* fresh, void* o, cudaStream_t stream) {
   return decode(falcon::kFalcon1A, N, m, dv, dtype, phi, eps, eps_gamma, q, k, v, beta, lambda,
                 S, x_prev, fresh, o, stream);
+}
+
+int falcon_selftest_wait_timeout(uint32_t limit_us, cudaStream_t stream) {
+  if (limit_us == 0 || limit_us > 10000000u) return FALCON_ERR_BAD_ARG;
+  int rc = check_device();
+  if (rc) return rc;
+  int* err = device_error_word();
+  if (!err) return FALCON_ERR_CUDA;
+  wait_timeout_kernel<<<1, 64, 0, stream>>>((uint64_t)limit_us * 1000ull, err);
+  return to_status(cudaGetLastError());
 }
 
 int falcon_sync_check(cudaStream_t stream) {

@@ -18,9 +18,9 @@
 namespace falcon {
 namespace tc {
 
-// Spin limit of every wait on an mbarrier (~seconds at most); on expiry the
-// caller records an error and leaves the loop.
-constexpr uint32_t kSpinLimit = 1u << 26;
+// Time limit of every wait on an mbarrier; on expiry the caller records an
+// error in the device error word and leaves the wait.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -56,12 +56,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity.  Returns false if the
-// spin limit ran out (the caller flags the error and stops waiting).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait for the phase with the given parity: gives up after limit_ns of
+// wall time (a try_wait may itself suspend the thread for a while, so the
+// bound is on time, not on iterations).  Returns false on expiry; the caller
+// flags the error and stops waiting.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > limit_ns) return false;
+  }
 }
 
 // ---- bulk async copies (global <-> shared, no tensor map) ----------------

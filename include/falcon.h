@@ -188,6 +188,15 @@ int falcon1a_decode_step(int64_t N, int32_t m, int32_t dv, int32_t dtype,
  * FALCON_ERR_TIMEOUT, or FALCON_ERR_CUDA if the stream itself failed. */
 int falcon_sync_check(cudaStream_t stream);
 
+/* Diagnostic of the failure path (no counterpart in the paper): launches a
+ * kernel whose threads wait on a barrier that nothing completes.  The wait
+ * gives up after limit_us microseconds (1 .. 10^7) and records the expiry in
+ * the device error word, exactly as the chunked kernels do when a wait is
+ * lost; nothing traps and the CUDA context stays usable.  A following
+ * falcon_sync_check(stream) returns FALCON_ERR_TIMEOUT (and clears the word).
+ * Returns FALCON_ERR_BAD_ARG for limit_us out of range. */
+int falcon_selftest_wait_timeout(uint32_t limit_us, cudaStream_t stream);
+
 /* Static description of a return code. */
 const char *falcon_strerror(int code);
 
