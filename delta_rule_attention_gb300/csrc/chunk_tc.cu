@@ -147,60 +147,80 @@ constexpr int kLdR = 49;  // fp32 row stride of the block right-hand sides
 struct MapScalars {
   float eta[64], g[64], gx[64];
   float fu[64], fv[64], fw[64];  // rank-1 decay factors (span <= kFactorSpan)
+  float ssp[2][128];             // half-row partial sums of squares
   float carry;
   int fail;
   uint64_t bar_in, bar_mma;
   uint32_t tmem_base;
 };
 constexpr size_t kMapSmemBytes = kOffSC + sizeof(MapScalars);
+constexpr int kMapThreads = 256;
 
-// Read row r of a plain (unswizzled) bf16 tile with 128-byte rows.
-__device__ __forceinline__ void load_row_plain(const unsigned char* tile, int r, float* v) {
+// Half-row helpers: a thread owns columns 32h .. 32h+31 of row r (four
+// 16-byte chunks).  "plain": unswizzled 128-byte rows; "sw": 128-byte swizzle.
+__device__ __forceinline__ void load_half_plain(const unsigned char* tile, int r, int h, float* v) {
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const uint4 pk = *reinterpret_cast<const uint4*>(tile + r * 128 + 16 * c);
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&pk);
+  for (int c = 0; c < 4; ++c) {
+    const uint4 pk = *reinterpret_cast<const uint4*>(tile + r * 128 + 16 * (4 * h + c));
+    const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&pk);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float2 f = __bfloat1622float2(h[e]);
+      const float2 f = __bfloat1622float2(hv[e]);
       v[8 * c + 2 * e] = f.x;
       v[8 * c + 2 * e + 1] = f.y;
     }
   }
 }
 
-// T = (I + A)^{-1} for the strictly lower 64 x 64 A (rows of kLdA floats).
-// Warp b inverts diagonal block b in fp32 by forward substitution (two lanes
-// per row, eight columns each, rows broadcast by shuffles) and leaves it as the
-// diagonal block of T; block rows b = 1..3 then follow
-// T_{b,<b} = T_bb (-A_{b,<b} T_{<b}) with warp MMAs.
+__device__ __forceinline__ void store_half_sw(unsigned char* tile, int r, int h, const float* v,
+                                              float scale) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    *reinterpret_cast<uint4*>(tile + r * 128 + (((4 * h + c) ^ (r & 7)) << 4)) =
+        pack8(v + 8 * c, scale);
+}
+
+__device__ __forceinline__ float sumsq32(const float* v) {
+  float p[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < 32; ++j) p[j & 7] += v[j] * v[j];
+  return ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
+}
+
+// T = (I + A)^{-1} for the strictly lower 64 x 64 A (rows of kLdA floats),
+// eight warps.  Diagonal block b = warp & 3 is inverted in fp32 by forward
+// substitution: warp w owns columns 8 (w >> 2) .. +7 of the block, two lanes
+// per row with four columns each, and broadcasts finished rows by shuffles;
+// the result stays as the diagonal block of T.  Block rows b = 1..3 then
+// follow T_{b,<b} = T_bb (-A_{b,<b} T_{<b}) with warp MMAs, one n-tile per warp.
 __device__ void solve_unit_lower(const float* As, float* Ts, float* Rs) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   {
-    const int b = warp, r = lane >> 1, h = lane & 1, row = 16 * b + r;
+    const int b = warp & 3, hh = warp >> 2, rr = lane >> 1, q = lane & 1, row = 16 * b + rr;
     float arow[15];
 #pragma unroll
     for (int k = 0; k < 15; ++k) arow[k] = As[row * kLdA + 16 * b + k];
-    float dinv[8];
+    float dv4[4];
 #pragma unroll
-    for (int jj = 0; jj < 8; ++jj) dinv[jj] = (8 * h + jj == r) ? 1.f : 0.f;
+    for (int jj = 0; jj < 4; ++jj) dv4[jj] = (8 * hh + 4 * q + jj == rr) ? 1.f : 0.f;
 #pragma unroll
     for (int k = 0; k < 15; ++k) {
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj) {
-        const float tkj = __shfl_sync(0xffffffffu, dinv[jj], 2 * k + h);
-        if (r > k) dinv[jj] -= arow[k] * tkj;
+      for (int jj = 0; jj < 4; ++jj) {
+        const float tkj = __shfl_sync(0xffffffffu, dv4[jj], 2 * k + q);
+        if (rr > k) dv4[jj] -= arow[k] * tkj;
       }
     }
 #pragma unroll
-    for (int jj = 0; jj < 8; ++jj) Ts[row * kLdT + 16 * b + 8 * h + jj] = dinv[jj];
+    for (int jj = 0; jj < 4; ++jj) Ts[row * kLdT + 16 * b + 8 * hh + 4 * q + jj] = dv4[jj];
   }
   __syncthreads();
   const int g = lane >> 2, t = lane & 3;
   for (int b = 1; b < 4; ++b) {
     const int w = 16 * b;  // columns left of block b: 2b n-tiles of 8
+    const int nt = warp;
     // R = -A[w:w+16, 0:w] T[0:w, 0:w]; T[k][n] = 0 for k < n, so those k-steps are skipped.
-    for (int nt = warp; nt < 2 * b; nt += 4) {
+    if (nt < 2 * b) {
       float d[4] = {0.f, 0.f, 0.f, 0.f};
       for (int kb = nt >> 1; kb < b; ++kb) {
         uint32_t fa[4], fb[2];
@@ -216,7 +236,7 @@ __device__ void solve_unit_lower(const float* As, float* Ts, float* Rs) {
     }
     __syncthreads();
     // T[w:w+16, 0:w] = T_bb R  (T_bb: diagonal block b of T)
-    for (int nt = warp; nt < 2 * b; nt += 4) {
+    if (nt < 2 * b) {
       float d[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t fa[4], fb[2];
       frag_a(fa, Ts, kLdT, w, w);
@@ -232,7 +252,10 @@ __device__ void solve_unit_lower(const float* As, float* Ts, float* Rs) {
   }
 }
 
-__global__ void __launch_bounds__(128, 3) tc_chunk_map_kernel(ChunkArgs a, int nchunks, int* err) {
+// 256 threads per chunk: thread t owns row r = t & 127 (its TMEM lane) and
+// columns 32h .. 32h+31 with h = t >> 7.
+__global__ void __launch_bounds__(kMapThreads, 3) tc_chunk_map_kernel(ChunkArgs a, int nchunks,
+                                                                      int* err) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* const base = align1024(smem_raw);
   unsigned char* const r1 = base + kOffR1;
@@ -243,8 +266,8 @@ __global__ void __launch_bounds__(128, 3) tc_chunk_map_kernel(ChunkArgs a, int n
   float* const As = reinterpret_cast<float*>(r1);
   float* const Ts = reinterpret_cast<float*>(r2);
   float* const Rs = Ts + 64 * kLdT;
-  unsigned char* const kst = a3;            // raw k rows: row r = k_{t0-1+r}
-  unsigned char* const qst = a3 + 65 * 128;  // raw q rows
+  unsigned char* const kst = a3;              // raw k rows: row r = k_{t0-1+r}
+  unsigned char* const qst = a3 + 65 * 128;   // raw q rows
   unsigned char* const xt_tile = a3;          // MN-major A of MMA3a, atom 0
   unsigned char* const zero_tile = a3 + 8192;  // atom 1 of MMA3a; rows 0..63 of MMA3b
   unsigned char* const p_tile = a3 + 16384;   // rows 64..127 of MMA3b (K-major)
@@ -252,9 +275,11 @@ __global__ void __launch_bounds__(128, 3) tc_chunk_map_kernel(ChunkArgs a, int n
   const int c = blockIdx.x;
   const int64_t bh = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r = tid & 127, h = tid >> 7;
   const int64_t t0 = (int64_t)c * kC;
   const int n = (int)min((int64_t)kC, a.T - t0);
   const bool f1 = a.rule == kFalcon1;
+  const bool last = c == nchunks - 1;
   const __nv_bfloat16* qg = reinterpret_cast<const __nv_bfloat16*>(a.q);
   const __nv_bfloat16* kg = reinterpret_cast<const __nv_bfloat16*>(a.k);
   const __nv_bfloat16* vg = reinterpret_cast<const __nv_bfloat16*>(a.v);
@@ -283,46 +308,55 @@ __global__ void __launch_bounds__(128, 3) tc_chunk_map_kernel(ChunkArgs a, int n
   __syncthreads();
   if (!mbar_wait(&sc.bar_in, 0)) sc.fail = 1;
 
-  // ---- features: thread t < 64 builds the write feature x_t = phi(k_{t0+t-1});
-  //      thread 64 + i builds phi(q_{t0+i}).  Rows past the sequence are zero.
-  float x[64];
-  float E = 0.f;
-  if (tid < 64) {
-    const int64_t tk = t0 + tid - 1;
-    if (tid <= n && tk >= 0) {
-      load_row_plain(kst, tid, x);
-      E = apply_phi(x, a.phi);
-    } else if (tk < 0 && a.x_prev) {
+  // ---- features: rows 0..63 are the write features x_r = phi(k_{t0+r-1}),
+  //      rows 64..127 are phi(q_{t0+r-64}); rows past the sequence are zero.
+  float x[32];
+  const bool carried_row = (r == 0 && t0 == 0);  // x_1: x_prev as given, or the sentinel zero
+  if (r < 64) {
+    if (!carried_row && r <= n) {
+      load_half_plain(kst, r, h, x);
+    } else if (carried_row && a.x_prev) {
 #pragma unroll
-      for (int j = 0; j < 64; ++j) x[j] = a.x_prev[bh * 64 + j];
-#pragma unroll
-      for (int j = 0; j < 64; ++j) E += x[j] * x[j];
+      for (int j = 0; j < 32; ++j) x[j] = a.x_prev[bh * 64 + 32 * h + j];
     } else {
 #pragma unroll
-      for (int j = 0; j < 64; ++j) x[j] = 0.f;
+      for (int j = 0; j < 32; ++j) x[j] = 0.f;
     }
-    // phi(k_{T-1}) is x_n when the last chunk is partial.
-    if (a.x_last && c == nchunks - 1 && n < kC && tid == n)
-      for (int j = 0; j < 64; ++j) a.x_last[bh * 64 + j] = x[j];
+  } else if (r - 64 < n) {
+    load_half_plain(qst, r - 64, h, x);
   } else {
-    const int i = tid - 64;
-    if (i < n) {
-      load_row_plain(qst, i, x);
-      apply_phi(x, a.phi);
-    } else {
 #pragma unroll
-      for (int j = 0; j < 64; ++j) x[j] = 0.f;
-    }
-    if (a.x_last && c == nchunks - 1 && n == kC && tid == 64) {
-      float kl[64];
-      load_row_plain(kst, n, kl);  // row n = k_{t0+n-1} = k_{T-1}
-      apply_phi(kl, a.phi);
-      for (int j = 0; j < 64; ++j) a.x_last[bh * 64 + j] = kl[j];
+    for (int j = 0; j < 32; ++j) x[j] = 0.f;
+  }
+  sc.ssp[h][r] = sumsq32(x);
+  __syncthreads();
+  float E = sc.ssp[0][r] + sc.ssp[1][r];  // ||x_r||^2 (rows < 64)
+  if (a.phi == FALCON_PHI_L2 && !carried_row) {
+    const float inv = rsqrtf(fmaxf(E, 1e-24f));  // 1 / max(||u||, 1e-12)
+#pragma unroll
+    for (int j = 0; j < 32; ++j) x[j] *= inv;
+    E *= inv * inv;
+  }
+  if (a.x_last && last) {
+    // phi(k_{T-1}): row n of the features when the last chunk is partial,
+    // otherwise raw k row n of the staging (normalised here).
+    if (n < kC && r == n) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) a.x_last[bh * 64 + 32 * h + j] = x[j];
+    } else if (n == kC && r == 64) {
+      float kl[32], kr[32];
+      load_half_plain(kst, n, 0, kl);
+      load_half_plain(kst, n, 1, kr);
+      const float s2 = sumsq32(kl) + sumsq32(kr);
+      const float inv = (a.phi == FALCON_PHI_L2) ? rsqrtf(fmaxf(s2, 1e-24f)) : 1.f;
+      const float* src = h ? kr : kl;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) a.x_last[bh * 64 + 32 * h + j] = src[j] * inv;
     }
   }
-  store_row_scaled(r1, tid, x, 1.f);  // [X; Q]
+  store_half_sw(r1, r, h, x, 1.f);  // [X; Q]
 
-  // ---- step sizes, log-decays, chunk-local inclusive prefix g ----
+  // ---- step sizes, log-decays, chunk-local inclusive prefix g (threads 0..63) ----
   float eta = 0.f, lg = 0.f;
   if (tid < 64 && tid < n) {
     float gam;
@@ -336,7 +370,7 @@ __global__ void __launch_bounds__(128, 3) tc_chunk_map_kernel(ChunkArgs a, int n
     if (lane >= o) incl += y;
   }
   if (tid == 31) sc.carry = incl;
-  __syncthreads();  // (also: every raw k and q row has been read)
+  __syncthreads();
   if (warp == 1) incl += sc.carry;
   if (tid < 64) {
     sc.eta[tid] = eta;
@@ -348,7 +382,7 @@ __global__ void __launch_bounds__(128, 3) tc_chunk_map_kernel(ChunkArgs a, int n
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sc.tmem_base;
-  const uint32_t tlane = tmem + ((uint32_t)(warp * 32) << 16);
+  const uint32_t tlane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
   const float gC = sc.g[kC - 1];
   const bool factored = -gC <= kFactorSpan;
 
@@ -358,89 +392,86 @@ __global__ void __launch_bounds__(128, 3) tc_chunk_map_kernel(ChunkArgs a, int n
             idesc_bf16(128, 64, false, false), false);
     mma_commit(&sc.bar_mma);
   }
-  // Meanwhile: the zero tile, Xt = Diag(e^{g_C - g}) X, the rank-1 decay factors
-  // around r = g_C / 2 (fu_l = e^{r - g_l}, fv_j = eta_j e^{g_{j-1} - r},
-  // fw_i = e^{g_i - r}), and Vh = Diag(eta) V in place.
-#pragma unroll
-  for (int z = 0; z < 4; ++z)
-    reinterpret_cast<uint4*>(zero_tile)[tid + 128 * z] = make_uint4(0u, 0u, 0u, 0u);
-  if (tid < 64) {
-    store_row_scaled(xt_tile, tid, x, __expf(gC - sc.g[tid]));
-    if (factored) {
-      const float r = 0.5f * gC;
-      sc.fu[tid] = __expf(r - sc.g[tid]);
-      sc.fv[tid] = sc.eta[tid] * __expf(sc.gx[tid] - r);
-      sc.fw[tid] = __expf(sc.g[tid] - r);
+  // Meanwhile: the zero tile, Xt = Diag(e^{g_C - g}) X, the rank-1 decay
+  // factors around rr = g_C / 2 (fu_l = e^{rr - g_l}, fv_j = eta_j e^{g_{j-1} - rr},
+  // fw_i = e^{g_i - rr}), and the raw v halves (Vh is written in place after
+  // the next barrier: a row's two halves swap chunks under the swizzle).
+  reinterpret_cast<uint4*>(zero_tile)[tid] = make_uint4(0u, 0u, 0u, 0u);
+  reinterpret_cast<uint4*>(zero_tile)[tid + 256] = make_uint4(0u, 0u, 0u, 0u);
+  float v[32];
+  if (r < 64) {
+    store_half_sw(xt_tile, r, h, x, __expf(gC - sc.g[r]));
+    if (h == 0 && factored) {
+      const float rr = 0.5f * gC;
+      sc.fu[r] = __expf(rr - sc.g[r]);
+      sc.fv[r] = sc.eta[r] * __expf(sc.gx[r] - rr);
+      sc.fw[r] = __expf(sc.g[r] - rr);
     }
+  } else if (r - 64 < n) {
+    load_half_plain(vh, r - 64, h, v);
   } else {
-    const int i = tid - 64;
-    float v[64];
-    if (i < n) {
-      load_row_plain(vh, i, v);
-    } else {
 #pragma unroll
-      for (int j = 0; j < 64; ++j) v[j] = 0.f;
-    }
-    store_row_scaled(vh, i, v, sc.eta[i]);
+    for (int j = 0; j < 32; ++j) v[j] = 0.f;
   }
   if (!sc.fail && !mbar_wait(&sc.bar_mma, 0)) sc.fail = 1;
   tc_fence_after();
-  __syncthreads();  // fu/fv/fw visible; MMA1 has finished reading [X; Q]
+  __syncthreads();  // fu/fv/fw visible; raw v read; MMA1 has finished reading [X; Q]
+  if (r >= 64) store_half_sw(vh, r - 64, h, v, sc.eta[r - 64]);
   {
-    float d[64];
-    tmem_ld32(tlane, d);
-    tmem_ld32(tlane + 32, d + 32);
-    if (tid < 64) {
-      // A row j: eta_j e^{g_{j-1} - g_l} G[j][l] for l < j (all loads, then the stores)
-      const int j = tid;
+    float d[32];
+    tmem_ld32(tlane + 32 * h, d);
+    if (r < 64) {
+      // A row r: eta_r e^{g_{r-1} - g_l} G[r][l] for l < r (computed, then stored)
       if (f1) {
         if (factored) {
-          const float vj = sc.fv[j];
+          const float vr = sc.fv[r];
 #pragma unroll
-          for (int l = 0; l < 64; ++l) d[l] = (l < j) ? vj * sc.fu[l] * d[l] : 0.f;
+          for (int l = 0; l < 32; ++l) d[l] = (32 * h + l < r) ? vr * sc.fu[32 * h + l] * d[l] : 0.f;
         } else {
-          const float ej = sc.eta[j], gxj = sc.gx[j];
+          const float er = sc.eta[r], gxr = sc.gx[r];
 #pragma unroll
-          for (int l = 0; l < 64; ++l)
-            d[l] = (l < j) ? ej * __expf(fminf(gxj - sc.g[l], 0.f)) * d[l] : 0.f;
+          for (int l = 0; l < 32; ++l)
+            d[l] = (32 * h + l < r) ? er * __expf(fminf(gxr - sc.g[32 * h + l], 0.f)) * d[l] : 0.f;
         }
-        float4* arow = reinterpret_cast<float4*>(As + j * kLdA);
+        float4* arow = reinterpret_cast<float4*>(As + r * kLdA + 32 * h);
 #pragma unroll
-        for (int l4 = 0; l4 < 16; ++l4)
+        for (int l4 = 0; l4 < 8; ++l4)
           arow[l4] = make_float4(d[4 * l4], d[4 * l4 + 1], d[4 * l4 + 2], d[4 * l4 + 3]);
       }
     } else {
       // P row i: e^{g_i - g_j} (Q X^T)[i][j] for j <= i
-      const int i = tid - 64;
+      const int i = r - 64;
       if (factored) {
         const float wi = sc.fw[i];
 #pragma unroll
-        for (int jj = 0; jj < 64; ++jj) d[jj] = (jj <= i) ? wi * sc.fu[jj] * d[jj] : 0.f;
+        for (int jj = 0; jj < 32; ++jj)
+          d[jj] = (32 * h + jj <= i) ? wi * sc.fu[32 * h + jj] * d[jj] : 0.f;
       } else {
         const float gi = sc.g[i];
 #pragma unroll
-        for (int jj = 0; jj < 64; ++jj)
-          d[jj] = (jj <= i) ? __expf(fminf(gi - sc.g[jj], 0.f)) * d[jj] : 0.f;
+        for (int jj = 0; jj < 32; ++jj)
+          d[jj] = (32 * h + jj <= i) ? __expf(fminf(gi - sc.g[32 * h + jj], 0.f)) * d[jj] : 0.f;
       }
-      store_row_scaled(p_tile, i, d, 1.f);
+      store_half_sw(p_tile, i, h, d, 1.f);
     }
   }
   if (__syncthreads_or(sc.fail)) goto teardown;  // A and P complete
 
   // ---- T = (I + A)^{-1} (identity for Falcon-1A), then the MMA2 operands ----
   if (f1) solve_unit_lower(As, Ts, Rs);
-  if (tid < 64) {
-    // T row tid as bf16 into R1 (A is dead): the solve result up to the end of
-    // the diagonal block, zero beyond.
-    float trow[64];
-    const int end = (tid | 15) + 1;
+  if (r < 64) {
+    // T row r as bf16 into R1 (A is dead): up to the end of the diagonal block, zero beyond.
+    float trow[32];
+    const int end = (r | 15) + 1;
 #pragma unroll
-    for (int j = 0; j < 64; ++j)
-      trow[j] = f1 ? ((j < end) ? Ts[tid * kLdT + j] : 0.f) : ((j == tid) ? 1.f : 0.f);
-    store_row_scaled(r1, tid, trow, 1.f);
+    for (int j = 0; j < 32; ++j) {
+      const int col = 32 * h + j;
+      trow[j] = f1 ? ((col < end) ? Ts[r * kLdT + col] : 0.f) : ((col == r) ? 1.f : 0.f);
+    }
+    store_half_sw(r1, r, h, trow, 1.f);
   }
   __syncthreads();  // Xh overwrites the solve scratch
-  if (tid < 64) store_row_scaled(r2, tid, x, f1 ? sc.eta[tid] * __expf(sc.gx[tid]) : 0.f);
+  if (r < 64) store_half_sw(r2, r, h, x, f1 ? sc.eta[r] * __expf(sc.gx[r]) : 0.f);
   fence_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -455,10 +486,9 @@ __global__ void __launch_bounds__(128, 3) tc_chunk_map_kernel(ChunkArgs a, int n
   if (!mbar_wait(&sc.bar_mma, 1)) sc.fail = 1;
   tc_fence_after();
   {
-    float d[64];
-    tmem_ld32(tlane, d);
-    tmem_ld32(tlane + 32, d + 32);
-    store_row_scaled(r1, tid, d, 1.f);  // [W^T; U~^T] over T (MMA2 is complete)
+    float d[32];
+    tmem_ld32(tlane + 32 * h, d);
+    store_half_sw(r1, r, h, d, 1.f);  // [W^T; U~^T] over T (MMA2 is complete)
   }
   fence_async_smem();
   tc_fence_before();
@@ -479,28 +509,18 @@ __global__ void __launch_bounds__(128, 3) tc_chunk_map_kernel(ChunkArgs a, int n
     unsigned char* map = reinterpret_cast<unsigned char*>(a.workspace) +
                          (size_t)(bh * nchunks + c) * kMapBytes;
     // The map images are staged in shared memory (the MMA3 operands are dead)
-    // and leave in two bulk copies: row-scattered 16-byte global stores would
-    // touch a different 128-byte line per thread.
+    // and leave in two bulk copies.
     unsigned char* mc_stage = a3;  // 16 KB
     unsigned char* nc_stage = r1;  // 16 KB
-    float d[64];
-    tmem_ld32(tlane, d);
-    tmem_ld32(tlane + 32, d + 32);
+    float d[32];
+    tmem_ld32(tlane + 32 * h, d);
     // Mc row: rows < 64 -> -Xt^T W ; rows >= 64 -> e^{g_i} q_i - P W
-    const float eg = (tid >= 64) ? __expf(sc.g[tid - 64]) : 0.f;
+    const float eg = (r >= 64) ? __expf(sc.g[r - 64]) : 0.f;
 #pragma unroll
-    for (int j = 0; j < 64; ++j) d[j] = (tid < 64) ? -d[j] : eg * x[j] - d[j];
-#pragma unroll
-    for (int cc = 0; cc < 8; ++cc)
-      *reinterpret_cast<uint4*>(mc_stage + tid * 128 + ((cc ^ (tid & 7)) << 4)) =
-          pack8(d + 8 * cc, 1.f);
-    tmem_ld32(tlane + 64, d);
-    tmem_ld32(tlane + 96, d + 32);
-    // Nc row: 16-byte chunk cc stored at chunk position cc ^ (tid & 7)
-#pragma unroll
-    for (int cc = 0; cc < 8; ++cc)
-      *reinterpret_cast<uint4*>(nc_stage + tid * 128 + ((cc ^ (tid & 7)) << 4)) =
-          pack8(d + 8 * cc, 1.f);
+    for (int j = 0; j < 32; ++j) d[j] = (r < 64) ? -d[j] : eg * x[j] - d[j];
+    store_half_sw(mc_stage, r, h, d, 1.f);
+    tmem_ld32(tlane + 64 + 32 * h, d);
+    store_half_sw(nc_stage, r, h, d, 1.f);  // Nc: chunk cc at position cc ^ (row & 7)
     fence_async_smem();
     __syncthreads();
     if (tid == 0) {
@@ -698,7 +718,8 @@ cudaError_t launch_tc_chunked(const ChunkArgs& a, int* err, cudaStream_t stream)
   cudaError_t e = cudaFuncSetAttribute(tc_chunk_map_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)map_smem);
   if (e != cudaSuccess) return e;
-  tc_chunk_map_kernel<<<dim3(nchunks, (unsigned)a.BH), 128, map_smem, stream>>>(a, nchunks, err);
+  tc_chunk_map_kernel<<<dim3(nchunks, (unsigned)a.BH), kMapThreads, map_smem, stream>>>(a, nchunks,
+                                                                                   err);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const size_t scan_smem = sizeof(ScanSmem) + 1024;
