@@ -33,6 +33,7 @@
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
+#include "tmap.cuh"
 
 namespace falcon {
 
@@ -60,21 +61,6 @@ __device__ __forceinline__ void flag_error(int* err) {
   if (err) atomicExch(err, 1);
 }
 
-// phi in place; returns ||phi(u)||^2 (eight independent partial sums).
-__device__ __forceinline__ float apply_phi(float* v, int phi) {
-  float p[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int j = 0; j < 64; ++j) p[j & 7] += v[j] * v[j];
-  float ss = ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
-  if (phi == FALCON_PHI_L2) {
-    const float inv = 1.f / fmaxf(sqrtf(ss), 1e-12f);
-#pragma unroll
-    for (int j = 0; j < 64; ++j) v[j] *= inv;
-    ss *= inv * inv;
-  }
-  return ss;
-}
-
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -88,14 +74,6 @@ __device__ __forceinline__ uint4 pack8(const float* v, float scale) {
   pk.z = pack_bf16(scale * v[4], scale * v[5]);
   pk.w = pack_bf16(scale * v[6], scale * v[7]);
   return pk;
-}
-
-// Row r of a 64-wide bf16 tile with the 128-byte swizzle (chunk c -> c ^ (r & 7)).
-__device__ __forceinline__ void store_row_scaled(unsigned char* tile, int r, const float* v,
-                                                 float scale) {
-#pragma unroll
-  for (int c = 0; c < 8; ++c)
-    *reinterpret_cast<uint4*>(tile + r * 128 + ((c ^ (r & 7)) << 4)) = pack8(v + 8 * c, scale);
 }
 
 // Warp-level bf16 MMA, 16 x 8 x 16, fp32 accumulate (used for the 16-row
@@ -541,24 +519,28 @@ teardown:
 }
 
 // ---------------------------------------------------------------------------
-// Scan kernel, 256 threads per head.  TMEM lane rules give warps 0,1,4,5 the
-// state rows (lanes 0..63) and warps 2,3,6,7 the output rows (lanes 64..127);
-// warps 0..3 take columns 0..31 of their rows and warps 4..7 columns 32..63.
-// The state path (MMA -> state update -> next B operand) is the critical
-// chain; the output rows and the refills of the map pipeline run beside it,
-// handed off through mbarriers, with a double-buffered TMEM accumulator.
+// Scan kernel, one CTA per head: sixteen math warps and one issue warp.  TMEM
+// lane rules give math warps w with (w & 3) < 2 the state rows (lanes 0..63)
+// and the others the output rows (lanes 64..127); warp w takes columns
+// 16 (w >> 2) .. +15 of its rows.  The state path (MMA -> state update ->
+// next B operand) is the critical chain; the issue warp only waits and issues
+// (the MMA of chunk c, then the refill of the stage chunk c-1 used), the output
+// rows run beside the chain, and the accumulator is double-buffered in TMEM.
+// Every hand-off is one mbarrier arrival per warp.
 constexpr int kStages = 3;
-constexpr int kScanThreads = 256;
+constexpr int kScanMathWarps = 16;
+constexpr int kScanThreads = 32 * (kScanMathWarps + 1);
 
 struct ScanSmem {
   unsigned char mc[kStages][kMcBytes];  // A tiles of the state MMA (K-major)
   unsigned char nc[kStages][kNcBytes];  // Nc rows (bf16, 16-byte chunks swizzled)
   unsigned char sop[8192];              // S as MN-major B operand (rows = m, 64 bf16 along d_v)
+  unsigned char ostage[2][8192];        // o tiles (64 tokens x 64 bf16, 128B-swizzled) for TMA
   float gc[kStages][4];
   uint64_t full[kStages];   // map of the stage has arrived
-  uint64_t empty[kStages];  // every thread is done with the stage
+  uint64_t empty[kStages];  // every math warp is done with the stage
   uint64_t mma_done[2];     // MMA into accumulator buffer b has completed
-  uint64_t o_done[2];       // output rows have read accumulator buffer b
+  uint64_t o_done[2];       // output warps have read accumulator buffer b
   uint64_t s_ready;         // the next state operand is in sop
   uint32_t tmem_base;
   int fail;
@@ -571,129 +553,185 @@ __device__ __forceinline__ void issue_map_load(ScanSmem& s, int st, const unsign
   bulk_g2s(s.gc[st], m + kMcBytes + kNcBytes, 16, &s.full[st]);
 }
 
-__global__ void __launch_bounds__(kScanThreads) tc_chunk_scan_kernel(ChunkArgs a, int nchunks,
-                                                                     int* err) {
+// Sixteen bf16 values (two 16-byte chunks) added to d.
+__device__ __forceinline__ void add_bf16x16(float* d, uint4 p0, uint4 p1) {
+  const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&p0);
+  const __nv_bfloat162* h1 = reinterpret_cast<const __nv_bfloat162*>(&p1);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f0 = __bfloat1622float2(h0[e]);
+    const float2 f1 = __bfloat1622float2(h1[e]);
+    d[2 * e] += f0.x;
+    d[2 * e + 1] += f0.y;
+    d[8 + 2 * e] += f1.x;
+    d[8 + 2 * e + 1] += f1.y;
+  }
+}
+
+__global__ void __launch_bounds__(kScanThreads)
+    tc_chunk_scan_kernel(ChunkArgs a, int nchunks, int* err, const __grid_constant__ CUtensorMap tm_o) {
   extern __shared__ unsigned char smem_raw[];
   ScanSmem& s = *reinterpret_cast<ScanSmem*>(align1024(smem_raw));
   volatile int* fail = &s.fail;
   const int64_t bh = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool issuer = warp == kScanMathWarps;
   const int row = 32 * (warp & 3) + lane;  // TMEM lane = row of [S'; O]
-  const int h = warp >> 2;                 // column half: 32h .. 32h+31
-  const bool srow = row < 64;
+  const int qc = (warp >> 2) & 3;          // column quarter: 16 qc .. 16 qc + 15
+  const bool srow = !issuer && row < 64;
+  // The two 16-byte chunks of this thread's columns, at their swizzled places.
+  const uint32_t ch0 = (uint32_t)(((2 * qc) ^ (row & 7)) << 4);
+  const uint32_t ch1 = (uint32_t)(((2 * qc + 1) ^ (row & 7)) << 4);
   const unsigned char* ws = reinterpret_cast<const unsigned char*>(a.workspace) +
                             (size_t)bh * nchunks * kMapBytes;
   if (warp == 0) tmem_alloc(&s.tmem_base, 128);
   if (tid == 0) {
     for (int st = 0; st < kStages; ++st) {
       mbar_init(&s.full[st], 1);
-      mbar_init(&s.empty[st], kScanThreads);
+      mbar_init(&s.empty[st], kScanMathWarps);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s.mma_done[b], 1);
-      mbar_init(&s.o_done[b], kScanThreads / 2);
+      mbar_init(&s.o_done[b], kScanMathWarps / 2);
     }
-    mbar_init(&s.s_ready, kScanThreads / 2);
+    mbar_init(&s.s_ready, kScanMathWarps / 2);
     fence_mbar_init();
     s.fail = 0;
   }
-  // State: each state thread keeps 32 columns of its row in fp32 registers.
-  float S[32];
+  // State: each state thread keeps 16 columns of its row in fp32 registers.
+  float S[16];
   if (srow) {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) S[j] = a.S0 ? a.S0[(bh * 64 + row) * 64 + 32 * h + j] : 0.f;
+    for (int j = 0; j < 16; ++j) S[j] = a.S0 ? a.S0[(bh * 64 + row) * 64 + 16 * qc + j] : 0.f;
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   // The maps are written by the preceding launch: wait for it to complete.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (tid == 0)
-    for (int st = 0; st < kStages && st < nchunks; ++st)
-      issue_map_load(s, st, ws + (size_t)st * kMapBytes);
   const uint32_t tmem = s.tmem_base;
-  const uint32_t tlane = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 32 * h;
-  __nv_bfloat16* og = reinterpret_cast<__nv_bfloat16*>(a.o);
 
-  if (srow) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      *reinterpret_cast<uint4*>(s.sop + row * 128 + (((4 * h + q) ^ (row & 7)) << 4)) =
-          pack8(S + 8 * q, 1.f);
-    fence_async_smem();
-    mbar_arrive(&s.s_ready);
-  }
-
-  for (int c = 0; c < nchunks; ++c) {
-    if (*fail) break;
-    const int st = c % kStages, b = c & 1;
-    if (tid == 0) {
-      bool ok = mbar_wait(&s.full[st], (uint32_t)(c / kStages) & 1u);
-      ok = ok && mbar_wait(&s.s_ready, (uint32_t)c & 1u);
-      if (c >= 2) ok = ok && mbar_wait(&s.o_done[b], (uint32_t)((c - 2) >> 1) & 1u);
-      if (ok) {
+  if (issuer) {
+    if (lane == 0) {
+      for (int st = 0; st < kStages && st < nchunks; ++st)
+        issue_map_load(s, st, ws + (size_t)st * kMapBytes);
+      for (int c = 0; c < nchunks; ++c) {
+        const int st = c % kStages, b = c & 1;
+        // The state operand is the last to be ready: wait for it last.
+        bool ok = c < 2 || mbar_wait(&s.o_done[b], (uint32_t)((c - 2) >> 1) & 1u);
+        ok = ok && mbar_wait(&s.full[st], (uint32_t)(c / kStages) & 1u);
+        ok = ok && mbar_wait(&s.s_ready, (uint32_t)c & 1u);
+        if (!ok) {
+          *fail = 1;
+          break;
+        }
         tc_fence_after();
         mma_k64(tmem + 64 * b, smem_addr(s.mc[st]), false, 16, smem_addr(s.sop), true, 8192,
                 idesc_bf16(128, 64, false, true), false);
         mma_commit(&s.mma_done[b]);
-      } else {
-        *fail = 1;
-      }
-    }
-    if (!mbar_wait(&s.mma_done[b], (uint32_t)(c >> 1) & 1u)) {
-      *fail = 1;
-      break;
-    }
-    tc_fence_after();
-    float d[32];
-    tmem_ld32(tlane + 64 * b, d);
-    {
-      // + Nc row, columns 32h..32h+31 (16-byte chunk cc at position cc ^ (row & 7))
-      const unsigned char* nrow = s.nc[st] + row * 128;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint4 pk = *reinterpret_cast<const uint4*>(nrow + (((4 * h + q) ^ (row & 7)) << 4));
-        const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&pk);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __bfloat1622float2(hv[e]);
-          d[8 * q + 2 * e] += f.x;
-          d[8 * q + 2 * e + 1] += f.y;
+        // Refill the stage of chunk c - 1 once every math warp is done with it.
+        const int cp = c - 1;
+        if (cp >= 0 && cp + kStages < nchunks) {
+          const int sp = cp % kStages;
+          if (!mbar_wait(&s.empty[sp], (uint32_t)(cp / kStages) & 1u)) {
+            *fail = 1;
+            break;
+          }
+          issue_map_load(s, sp, ws + (size_t)(cp + kStages) * kMapBytes);
         }
       }
     }
-    const float gC = s.gc[st][0];
-    tc_fence_before();
-    mbar_arrive(&s.empty[st]);
-    if (srow) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) S[j] = gC * S[j] + d[j];
-#pragma unroll
-      for (int q = 0; q < 4; ++q)  // the MMA of this chunk has completed
-        *reinterpret_cast<uint4*>(s.sop + row * 128 + (((4 * h + q) ^ (row & 7)) << 4)) =
-            pack8(S + 8 * q, 1.f);
-      fence_async_smem();
-      mbar_arrive(&s.s_ready);
-    } else {
-      mbar_arrive(&s.o_done[b]);
-      // o row t, columns 32h..32h+31 (rows past T skipped)
-      const int64_t t = (int64_t)c * kC + (row - 64);
-      if (t < a.T) {
-        uint4* orow = reinterpret_cast<uint4*>(og + (bh * a.T + t) * 64 + 32 * h);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) orow[q] = pack8(d + 8 * q, 1.f);
+    __syncwarp();
+  } else if (srow) {
+    // ---- state warps: the critical chain ----
+    const uint32_t tlane = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 16 * qc;
+    *reinterpret_cast<uint4*>(s.sop + row * 128 + ch0) = pack8(S, 1.f);
+    *reinterpret_cast<uint4*>(s.sop + row * 128 + ch1) = pack8(S + 8, 1.f);
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s.s_ready);
+    for (int c = 0; c < nchunks; ++c) {
+      // Exits are warp-uniform, so every __syncwarp sees all lanes.
+      if (__any_sync(0xffffffffu, *fail)) break;
+      const int st = c % kStages, b = c & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&s.full[st], (uint32_t)(c / kStages) & 1u))) {
+        *fail = 1;
+        break;
       }
-      if (tid == 64 && c + kStages < nchunks) {
-        if (mbar_wait(&s.empty[st], (uint32_t)(c / kStages) & 1u))
-          issue_map_load(s, st, ws + (size_t)(c + kStages) * kMapBytes);
-        else
-          *fail = 1;
+      // Nc (this thread's 16 columns) and e^{g_C} before the MMA completes.
+      const unsigned char* nrow = s.nc[st] + row * 128;
+      const uint4 n0 = *reinterpret_cast<const uint4*>(nrow + ch0);
+      const uint4 n1 = *reinterpret_cast<const uint4*>(nrow + ch1);
+      const float gC = s.gc[st][0];
+      if (!__all_sync(0xffffffffu, mbar_wait(&s.mma_done[b], (uint32_t)(c >> 1) & 1u))) {
+        *fail = 1;
+        break;
+      }
+      tc_fence_after();
+      float d[16];
+      tmem_ld16(tlane + 64 * b, d);
+      tc_fence_before();
+      add_bf16x16(d, n0, n1);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) S[j] = gC * S[j] + d[j];
+      *reinterpret_cast<uint4*>(s.sop + row * 128 + ch0) = pack8(S, 1.f);
+      *reinterpret_cast<uint4*>(s.sop + row * 128 + ch1) = pack8(S + 8, 1.f);
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&s.s_ready);
+        mbar_arrive(&s.empty[st]);  // Nc read; the MMA has read Mc
       }
     }
+  } else {
+    // ---- output warps: o rows, off the chain.  The o tile of a chunk leaves
+    // by one TMA store issued by the first lane of warp 2; rows past T are
+    // dropped by the tensor map.  Exits are agreed on by all output warps at
+    // a named barrier, so none is left waiting there.
+    const uint32_t tlane = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 16 * qc;
+    const bool o_issuer = warp == 2 && lane == 0;
+    constexpr int kOutThreads = 32 * kScanMathWarps / 2;
+    for (int c = 0; c < nchunks; ++c) {
+      const int st = c % kStages, b = c & 1;
+      bool ok = !*fail && mbar_wait(&s.full[st], (uint32_t)(c / kStages) & 1u);
+      uint4 n0 = make_uint4(0u, 0u, 0u, 0u), n1 = n0;
+      if (ok) {
+        const unsigned char* nrow = s.nc[st] + row * 128;
+        n0 = *reinterpret_cast<const uint4*>(nrow + ch0);
+        n1 = *reinterpret_cast<const uint4*>(nrow + ch1);
+      }
+      ok = ok && mbar_wait(&s.mma_done[b], (uint32_t)(c >> 1) & 1u);
+      // Staging buffer b was last read by the TMA store of chunk c - 2.
+      if (o_issuer) bulk_wait_read<1>();
+      if (named_sync_or(1, kOutThreads, !ok)) {
+        *fail = 1;
+        break;
+      }
+      tc_fence_after();
+      float d[16];
+      tmem_ld16(tlane + 64 * b, d);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&s.o_done[b]);  // accumulator b is read
+        mbar_arrive(&s.empty[st]);  // Nc read; the MMA has read Mc
+      }
+      add_bf16x16(d, n0, n1);
+      unsigned char* orow = s.ostage[b] + (row - 64) * 128;
+      *reinterpret_cast<uint4*>(orow + ch0) = pack8(d, 1.f);
+      *reinterpret_cast<uint4*>(orow + ch1) = pack8(d + 8, 1.f);
+      fence_async_smem();
+      named_sync(1, kOutThreads);
+      if (o_issuer) {
+        tma_store_3d(&tm_o, s.ostage[b], 0, c * kC, (int)bh);
+        bulk_commit();
+      }
+    }
+    if (o_issuer) bulk_wait<0>();  // the o stores have landed
   }
   if (!*fail && srow)
 #pragma unroll
-    for (int j = 0; j < 32; ++j) a.S_out[(bh * 64 + row) * 64 + 32 * h + j] = S[j];
+    for (int j = 0; j < 16; ++j) a.S_out[(bh * 64 + row) * 64 + 16 * qc + j] = S[j];
   __syncthreads();
   if (*fail && tid == 0) flag_error(err);
   tc_fence_before();
@@ -738,7 +776,10 @@ cudaError_t launch_tc_chunked(const ChunkArgs& a, int* err, cudaStream_t stream)
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_chunk_scan_kernel, a, nchunks, err);
+  CUtensorMap tm_o;
+  if (!encode_rows_bf16(&tm_o, a.o, 64, (uint64_t)a.T, (uint64_t)a.BH, 64, kC))
+    return cudaErrorInvalidValue;
+  return cudaLaunchKernelEx(&cfg, tc_chunk_scan_kernel, a, nchunks, err, tm_o);
 }
 
 }  // namespace falcon

@@ -106,6 +106,44 @@ __device__ __forceinline__ void bulk_wait() {
   asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// ---- tensor copies (TMA, through a tensor map) ---------------------------
+// Shared -> global box at coordinates (x, y, z) of a 3-D tensor map, tracked
+// by the issuing thread's bulk group.  x * element size must be a multiple of
+// 16 bytes.
+__device__ __forceinline__ void tma_store_3d(const void* map, const void* src, int x, int y,
+                                             int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+          map),
+      "r"(x), "r"(y), "r"(z), "r"(smem_addr(src))
+      : "memory");
+}
+// Global -> shared box, completion counted on `bar`.
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* map, int x, int y, int z,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Named barrier over `nthreads` threads (a multiple of 32), id 1..15.
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// The same barrier, returning whether `pred` held in any participating thread.
+__device__ __forceinline__ bool named_sync_or(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
 // Generic-proxy shared-memory writes become visible to the async proxy
 // (tensor core, bulk copies) after this fence plus a barrier.
 __device__ __forceinline__ void fence_async_smem() {
@@ -182,8 +220,23 @@ __device__ __forceinline__ void mma_k64(uint32_t d_tmem, uint32_t a_saddr, bool 
   }
 }
 
-// TMEM -> registers: 32 consecutive 32-bit columns of this thread's lane
-// (warp w of the CTA reads lanes 32w..32w+31).
+// TMEM -> registers (warp w of the CTA reads lanes 32 (w % 4) .. +31, one lane
+// per thread).  16 consecutive 32-bit columns of this thread's lane, then wait.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+// 32 consecutive 32-bit columns of this thread's lane, then wait.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   uint32_t r[32];
   asm volatile(
