@@ -125,7 +125,7 @@ int fwd_chunked(int rule, const falcon_shape* s, const void* q, const void* k, c
   a.S_out = S_out;
   a.x_last = x_last;
   a.workspace = workspace;
-  if (falcon::tc_path_applies(s->dtype, s->m, s->dv, s->chunk)) {
+  if (falcon::tc_path_applies(s->dtype, s->m, s->dv, s->chunk, s->B * s->H, s->T)) {
     int* err = device_error_word();
     if (!err) return FALCON_ERR_CUDA;
     return to_status(falcon::launch_tc_chunked(a, err, stream));
@@ -189,8 +189,8 @@ extern "C" {
 
 size_t falcon_workspace_bytes(const falcon_shape* s) {
   if (check_shape(s) != FALCON_OK) return 0;
-  if (falcon::tc_path_applies(s->dtype, s->m, s->dv, s->chunk))
-    return falcon::tc_workspace_bytes(s->B * s->H, s->T);
+  if (falcon::tc_path_applies(s->dtype, s->m, s->dv, s->chunk, s->B * s->H, s->T))
+    return falcon::tc_workspace_bytes(s->m, s->B * s->H, s->T);
   return falcon::generic_workspace_bytes(s->B * s->H, s->T, s->m, s->dv, s->chunk);
 }
 

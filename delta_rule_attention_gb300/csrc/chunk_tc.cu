@@ -42,6 +42,7 @@ namespace {
 using namespace tc;
 
 constexpr int kC = 64;
+// Chunk map for m = d_v = 64: Mc as the scan's A operand, Nc, e^{g_C}.
 constexpr uint32_t kMcBytes = 128 * 128;  // 128 rows x 64 bf16 (swizzled operand image)
 constexpr uint32_t kNcBytes = 128 * 128;  // 128 rows x 64 bf16 (rows swizzled by 16 B)
 constexpr uint32_t kMapBytes = kMcBytes + kNcBytes + 128;  // + e^{g_C} (padded)
@@ -107,17 +108,60 @@ __device__ __forceinline__ void frag_b(uint32_t (&b)[2], const float* M, int ld,
 }
 
 // ---------------------------------------------------------------------------
-// Map kernel.  Shared memory, in bytes from a 1024-aligned base (buffers with
-// disjoint lifetimes share space):
-//   R1  [0, 17408)      [X; Q] (MMA1 operand) -> A (fp32, rows of 68 floats)
-//                       -> T (bf16, MMA2 B) -> [W^T; U~^T] (MMA3 B)
-//   R2  [17408, 37888)  solve scratch (T in fp32 rows of 65, right-hand sides)
+// Map kernel.  One CTA per (head, chunk) for m = d_v = 64; for m = d_v = 128
+// two CTAs per chunk, CTA j taking the column half j of W, U~ and of the map
+// (K-atom j of Mc, d_v slice j of Nc); the Gram matrix, the solve and T are
+// the same in both.  Shared memory, in bytes from a 1024-aligned base (buffers
+// with disjoint lifetimes share space), m = 64:
+//   K   [0, 8192)       raw k rows t0-1 .. t0+62 as landed by TMA (128B-swizzled;
+//                       row r holds the write feature x_r before phi) -> Xt
+//                       (atom 0 of MMA3a's MN-major A)
+//   Q   [8192, 16384)   raw q rows as landed by TMA; [K; Q] is MMA1's A operand
+//                       -> zero tile (atom 1 of MMA3a; rows 0..63 of MMA3b)
+//   P   [16384, 24576)  P (rows 64..127 of MMA3b, K-major)
+//   R1  [24576, 41984)  A (fp32, rows of 68 floats) -> T (bf16, MMA2 B)
+//                       -> [W^T; U~^T] (MMA3 B) -> Nc staging
+//   R2  [41984, 62464)  solve scratch (T in fp32 rows of 65, right-hand sides)
 //                       -> Xh rows (atom 0 of MMA2's MN-major A)
-//   VH  [37888, 46080)  v rows as copied in, then Vh rows in place (atom 1)
-//   A3  [46080, 70656)  raw k and q rows as copied in; then Xt | zero | P tiles
+//   VH  [62464, 70656)  raw v rows as landed by TMA, then Vh = Diag(eta) V in
+//                       place (atom 1 of MMA2's A)
 //   SC  [70656, ...)    per-token scalars and barriers
-constexpr uint32_t kOffR1 = 0, kOffR2 = 17408, kOffVH = 37888, kOffA3 = 46080, kOffSC = 70656;
-constexpr uint32_t kLboA2 = kOffVH - kOffR2;  // Xh atom -> Vh atom of MMA2's A operand
+// m = 128: [K; Q] is two K-atoms of 16 KB, [K_a0 | Q_a0 | K_a1 | Q_a1]
+// (columns 0..63 and 64..127); afterwards Xt's two M-atoms replace K_a0 and
+// K_a1 and P replaces Q_a0; MMA3a (Xt^T [W | U~], 128 rows) and MMA3b
+// ([junk; P] [W | U~]) go to separate accumulators, so no zero tile is used.
+// R1, R2, VH follow at 32768, 50176, 70656 (VH holds the v columns of half j).
+// MMA1 runs on the raw bf16 rows; phi's normalisation enters afterwards as
+// fp32 row and column scalings of the accumulators and of the later operand
+// copies.
+template <int M>
+struct MapLayout;
+template <>
+struct MapLayout<64> {
+  static constexpr uint32_t K = 0, Q = 8192, P = 16384, R1 = 24576, R2 = 41984, VH = 62464,
+                            SC = 70656;
+  static constexpr uint32_t kAtom = 0;  // K-atom stride of [K; Q] (one atom)
+  static constexpr int kHalves = 1;
+  static constexpr int kMinBlocks = 3;
+  static constexpr uint32_t kTmemCols = 128;
+  static constexpr uint32_t kMapBytes = 128 * 128 * 2 + 128;  // Mc, Nc, e^{g_C}
+};
+template <>
+struct MapLayout<128> {
+  static constexpr uint32_t K = 0, Q = 8192, P = 8192, R1 = 32768, R2 = 50176, VH = 70656,
+                            SC = 78848;
+  static constexpr uint32_t kAtom = 16384;
+  static constexpr int kHalves = 2;
+  static constexpr int kMinBlocks = 2;
+  static constexpr uint32_t kTmemCols = 256;
+  // Per chunk: Mc K-atoms 0 and 1 (192 rows x 128 B each: 128 state rows,
+  // then 64 output rows), Nc d_v slices 0 and 1 (192 rows x 128 B), e^{g_C}.
+  static constexpr uint32_t kMcAtom = 192 * 128;
+  static constexpr uint32_t kMapBytes = 4 * kMcAtom + 128;
+};
+constexpr uint32_t kLboA2 = 20480;  // Xh atom -> Vh atom of MMA2's A operand (VH - R2)
+static_assert(MapLayout<64>::VH - MapLayout<64>::R2 == kLboA2, "MMA2 operand layout");
+static_assert(MapLayout<128>::VH - MapLayout<128>::R2 == kLboA2, "MMA2 operand layout");
 constexpr int kLdA = 68;  // fp32 row stride of A (16-byte aligned rows)
 constexpr int kLdT = 65;  // fp32 row stride of T during the solve
 constexpr int kLdR = 49;  // fp32 row stride of the block right-hand sides
@@ -125,21 +169,26 @@ constexpr int kLdR = 49;  // fp32 row stride of the block right-hand sides
 struct MapScalars {
   float eta[64], g[64], gx[64];
   float fu[64], fv[64], fw[64];  // rank-1 decay factors (span <= kFactorSpan)
+  float nrm[128];                // phi's scale of row r of [K; Q] (1 / ||row||, or 1)
   float ssp[2][128];             // half-row partial sums of squares
   float carry;
   int fail;
   uint64_t bar_in, bar_mma;
   uint32_t tmem_base;
 };
-constexpr size_t kMapSmemBytes = kOffSC + sizeof(MapScalars);
+template <int M>
+constexpr size_t map_smem_bytes() {
+  return MapLayout<M>::SC + sizeof(MapScalars);
+}
 constexpr int kMapThreads = 256;
 
 // Half-row helpers: a thread owns columns 32h .. 32h+31 of row r (four
-// 16-byte chunks).  "plain": unswizzled 128-byte rows; "sw": 128-byte swizzle.
-__device__ __forceinline__ void load_half_plain(const unsigned char* tile, int r, int h, float* v) {
+// 16-byte chunks) of a 64-wide bf16 tile with the 128-byte swizzle.
+__device__ __forceinline__ void load_half_sw(const unsigned char* tile, int r, int h, float* v) {
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    const uint4 pk = *reinterpret_cast<const uint4*>(tile + r * 128 + 16 * (4 * h + c));
+    const uint4 pk =
+        *reinterpret_cast<const uint4*>(tile + r * 128 + (((4 * h + c) ^ (r & 7)) << 4));
     const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&pk);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -163,6 +212,14 @@ __device__ __forceinline__ float sumsq32(const float* v) {
 #pragma unroll
   for (int j = 0; j < 32; ++j) p[j & 7] += v[j] * v[j];
   return ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
+}
+
+// phi's scale for a row with squared norm ss: 1 / max(||u||, 1e-12) for the
+// l2 map (0 for an all-zero row, which makes no difference to phi(u) = 0 and
+// keeps products with the exponential factors finite), 1 for the identity.
+__device__ __forceinline__ float phi_scale(float ss, int phi) {
+  if (phi != FALCON_PHI_L2) return 1.f;
+  return ss > 0.f ? rsqrtf(fmaxf(ss, 1e-24f)) : 0.f;
 }
 
 // T = (I + A)^{-1} for the strictly lower 64 x 64 A (rows of kLdA floats),
@@ -230,27 +287,33 @@ __device__ void solve_unit_lower(const float* As, float* Ts, float* Rs) {
   }
 }
 
-// 256 threads per chunk: thread t owns row r = t & 127 (its TMEM lane) and
-// columns 32h .. 32h+31 with h = t >> 7.
-__global__ void __launch_bounds__(kMapThreads, 3) tc_chunk_map_kernel(ChunkArgs a, int nchunks,
-                                                                      int* err) {
+// 256 threads per CTA: thread t owns row r = t & 127 (its TMEM lane) and
+// columns 32h .. 32h+31 (h = t >> 7) of the CTA's 64-column half j.
+template <int M>
+__global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
+    tc_chunk_map_kernel(ChunkArgs a, int nchunks, int* err,
+                        const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_v) {
+  using L = MapLayout<M>;
+  constexpr bool kWide = M == 128;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* const base = align1024(smem_raw);
-  unsigned char* const r1 = base + kOffR1;
-  unsigned char* const r2 = base + kOffR2;
-  unsigned char* const vh = base + kOffVH;
-  unsigned char* const a3 = base + kOffA3;
-  MapScalars& sc = *reinterpret_cast<MapScalars*>(base + kOffSC);
+  unsigned char* const kt = base + L::K;
+  unsigned char* const qt = base + L::Q;
+  unsigned char* const p_tile = base + L::P;
+  unsigned char* const r1 = base + L::R1;
+  unsigned char* const r2 = base + L::R2;
+  unsigned char* const vh = base + L::VH;
+  MapScalars& sc = *reinterpret_cast<MapScalars*>(base + L::SC);
   float* const As = reinterpret_cast<float*>(r1);
   float* const Ts = reinterpret_cast<float*>(r2);
   float* const Rs = Ts + 64 * kLdT;
-  unsigned char* const kst = a3;              // raw k rows: row r = k_{t0-1+r}
-  unsigned char* const qst = a3 + 65 * 128;   // raw q rows
-  unsigned char* const xt_tile = a3;          // MN-major A of MMA3a, atom 0
-  unsigned char* const zero_tile = a3 + 8192;  // atom 1 of MMA3a; rows 0..63 of MMA3b
-  unsigned char* const p_tile = a3 + 16384;   // rows 64..127 of MMA3b (K-major)
+  unsigned char* const xt_tile = kt;    // MN-major A of MMA3a, atom 0
+  unsigned char* const zero_tile = qt;  // m = 64: atom 1 of MMA3a; rows 0..63 of MMA3b
 
-  const int c = blockIdx.x;
+  const int c = blockIdx.x / L::kHalves;
+  const int j = blockIdx.x % L::kHalves;  // column half of this CTA
   const int64_t bh = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r = tid & 127, h = tid >> 7;
@@ -258,81 +321,110 @@ __global__ void __launch_bounds__(kMapThreads, 3) tc_chunk_map_kernel(ChunkArgs 
   const int n = (int)min((int64_t)kC, a.T - t0);
   const bool f1 = a.rule == kFalcon1;
   const bool last = c == nchunks - 1;
-  const __nv_bfloat16* qg = reinterpret_cast<const __nv_bfloat16*>(a.q);
-  const __nv_bfloat16* kg = reinterpret_cast<const __nv_bfloat16*>(a.k);
-  const __nv_bfloat16* vg = reinterpret_cast<const __nv_bfloat16*>(a.v);
   const int64_t rowbase = bh * a.T;
+  // Row 0 of the first chunk is x_1: x_prev as given (already phi-mapped), or
+  // the sentinel zero (the TMA box starts at row -1, which reads as zeros).
+  const bool carried_row = c == 0 && r == 0;
+  const bool patch = c == 0 && a.x_prev != nullptr;
 
-  if (warp == 0) tmem_alloc(&sc.tmem_base, 128);
+  if (warp == 0) tmem_alloc(&sc.tmem_base, L::kTmemCols);
   if (tid == 0) {
     mbar_init(&sc.bar_in, 1);
     mbar_init(&sc.bar_mma, 1);
     fence_mbar_init();
     sc.fail = 0;
-    // Every input row of the chunk in flight at once (k rows t0-1 .. t0+n-1).
-    const uint32_t kbytes = (uint32_t)(t0 > 0 ? n + 1 : n) * 128u;
-    const uint32_t rbytes = (uint32_t)n * 128u;
-    mbar_expect_tx(&sc.bar_in, kbytes + 2 * rbytes);
-    bulk_g2s(t0 > 0 ? kst : kst + 128, kg + (rowbase + (t0 > 0 ? t0 - 1 : 0)) * 64, kbytes,
-             &sc.bar_in);
-    bulk_g2s(qst, qg + (rowbase + t0) * 64, rbytes, &sc.bar_in);
-    bulk_g2s(vh, vg + (rowbase + t0) * 64, rbytes, &sc.bar_in);
+    // k rows t0-1 .. t0+62, q and v rows t0 .. t0+63 (rows past T read as zeros).
+    mbar_expect_tx(&sc.bar_in, (kWide ? 5 : 3) * 8192);
+#pragma unroll
+    for (int at = 0; at < (kWide ? 2 : 1); ++at) {
+      tma_load_3d(kt + at * L::kAtom, &tm_k, 64 * at, (int)(t0 - 1), (int)bh, &sc.bar_in);
+      tma_load_3d(qt + at * L::kAtom, &tm_q, 64 * at, (int)t0, (int)bh, &sc.bar_in);
+    }
+    tma_load_3d(vh, &tm_v, 64 * j, (int)t0, (int)bh, &sc.bar_in);
   }
   float beta_t = 0.f, lam_t = 0.f;
   if (tid < n) {
     beta_t = a.beta[rowbase + t0 + tid];
     lam_t = a.lambda[rowbase + t0 + tid];
   }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sc.tmem_base;
+  const uint32_t tlane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
   if (!mbar_wait(&sc.bar_in, 0)) sc.fail = 1;
+  if (patch) {
+    // x_1 = x_prev in row 0 of the K tile (bf16) for MMA1.
+    if (tid < 8 * (M / 64)) {
+      const int at = tid >> 3, ch = tid & 7;
+      float v8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v8[e] = a.x_prev[bh * M + 64 * at + 8 * ch + e];
+      // row 0: no swizzle shift
+      *reinterpret_cast<uint4*>(kt + at * L::kAtom + (ch << 4)) = pack8(v8, 1.f);
+    }
+    fence_async_smem();
+    __syncthreads();
+  }
+
+  // ---- MMA1: D[0:64) = [K; Q] K^T on the raw rows, issued before the features ----
+  if (tid == 0 && !sc.fail) {
+    tc_fence_after();
+#pragma unroll
+    for (int at = 0; at < (kWide ? 2 : 1); ++at)
+      mma_k64(tmem, smem_addr(kt + at * L::kAtom), false, 16, smem_addr(kt + at * L::kAtom),
+              false, 16, idesc_bf16(128, 64, false, false), at > 0);
+    mma_commit(&sc.bar_mma);
+  }
 
   // ---- features: rows 0..63 are the write features x_r = phi(k_{t0+r-1}),
-  //      rows 64..127 are phi(q_{t0+r-64}); rows past the sequence are zero.
-  float x[32];
-  const bool carried_row = (r == 0 && t0 == 0);  // x_1: x_prev as given, or the sentinel zero
-  if (r < 64) {
-    if (!carried_row && r <= n) {
-      load_half_plain(kst, r, h, x);
-    } else if (carried_row && a.x_prev) {
+  //      rows 64..127 are phi(q_{t0+r-64}); a thread keeps its raw half row
+  //      (of column half j) and the row's phi scale nr.  m = 128: the other
+  //      half (xo) enters the norm and Xt.
+  float x[32], xo[32];
+  if (carried_row && a.x_prev) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) x[j] = a.x_prev[bh * 64 + 32 * h + j];
-    } else {
+    for (int i = 0; i < 32; ++i) x[i] = a.x_prev[bh * M + 64 * j + 32 * h + i];
+    if (kWide) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) x[j] = 0.f;
+      for (int i = 0; i < 32; ++i) xo[i] = a.x_prev[bh * M + 64 * (1 - j) + 32 * h + i];
     }
-  } else if (r - 64 < n) {
-    load_half_plain(qst, r - 64, h, x);
   } else {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) x[j] = 0.f;
+    const unsigned char* rt = (r < 64 ? kt : qt);
+    load_half_sw(rt + j * L::kAtom, r & 63, h, x);
+    if (kWide) load_half_sw(rt + (1 - j) * L::kAtom, r & 63, h, xo);
   }
-  sc.ssp[h][r] = sumsq32(x);
+  if (kWide)  // same summation order in both halves' CTAs
+    sc.ssp[h][r] = j == 0 ? sumsq32(x) + sumsq32(xo) : sumsq32(xo) + sumsq32(x);
+  else
+    sc.ssp[h][r] = sumsq32(x);
   __syncthreads();
-  float E = sc.ssp[0][r] + sc.ssp[1][r];  // ||x_r||^2 (rows < 64)
-  if (a.phi == FALCON_PHI_L2 && !carried_row) {
-    const float inv = rsqrtf(fmaxf(E, 1e-24f));  // 1 / max(||u||, 1e-12)
-#pragma unroll
-    for (int j = 0; j < 32; ++j) x[j] *= inv;
-    E *= inv * inv;
-  }
+  const float ss = sc.ssp[0][r] + sc.ssp[1][r];
+  const float nr = carried_row ? 1.f : phi_scale(ss, a.phi);
+  const float E = ss * nr * nr;  // ||x_r||^2 (rows < 64)
+  if (h == 0) sc.nrm[r] = nr;
   if (a.x_last && last) {
-    // phi(k_{T-1}): row n of the features when the last chunk is partial,
-    // otherwise raw k row n of the staging (normalised here).
+    // phi(k_{T-1}) (columns of half j): row n of the features when the last
+    // chunk is partial, otherwise the row after the K tile, from global memory.
+    float* xl = a.x_last + bh * M + 64 * j + 32 * h;
     if (n < kC && r == n) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) a.x_last[bh * 64 + 32 * h + j] = x[j];
+      for (int i = 0; i < 32; ++i) xl[i] = x[i] * nr;
     } else if (n == kC && r == 64) {
-      float kl[32], kr[32];
-      load_half_plain(kst, n, 0, kl);
-      load_half_plain(kst, n, 1, kr);
-      const float s2 = sumsq32(kl) + sumsq32(kr);
-      const float inv = (a.phi == FALCON_PHI_L2) ? rsqrtf(fmaxf(s2, 1e-24f)) : 1.f;
-      const float* src = h ? kr : kl;
+      const __nv_bfloat16* kl =
+          reinterpret_cast<const __nv_bfloat16*>(a.k) + (rowbase + a.T - 1) * M;
+      float part[32];
+      float s2 = 0.f;
+      for (int pc = 0; pc < M / 32; ++pc) {  // fixed order over the whole row
 #pragma unroll
-      for (int j = 0; j < 32; ++j) a.x_last[bh * 64 + 32 * h + j] = src[j] * inv;
+        for (int i = 0; i < 32; ++i) part[i] = __bfloat162float(kl[32 * pc + i]);
+        s2 += sumsq32(part);
+      }
+      const float s = phi_scale(s2, a.phi);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) xl[i] = __bfloat162float(kl[64 * j + 32 * h + i]) * s;
     }
   }
-  store_half_sw(r1, r, h, x, 1.f);  // [X; Q]
 
   // ---- step sizes, log-decays, chunk-local inclusive prefix g (threads 0..63) ----
   float eta = 0.f, lg = 0.f;
@@ -355,51 +447,44 @@ __global__ void __launch_bounds__(kMapThreads, 3) tc_chunk_map_kernel(ChunkArgs 
     sc.g[tid] = incl;
     sc.gx[tid] = incl - lg;
   }
-  fence_async_smem();
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = sc.tmem_base;
-  const uint32_t tlane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
   const float gC = sc.g[kC - 1];
   const bool factored = -gC <= kFactorSpan;
-
-  // ---- MMA1: D[0:64) = [X; Q] X^T ----
-  if (tid == 0 && !sc.fail) {
-    mma_k64(tmem, smem_addr(r1), false, 16, smem_addr(r1), false, 16,
-            idesc_bf16(128, 64, false, false), false);
-    mma_commit(&sc.bar_mma);
-  }
-  // Meanwhile: the zero tile, Xt = Diag(e^{g_C - g}) X, the rank-1 decay
-  // factors around rr = g_C / 2 (fu_l = e^{rr - g_l}, fv_j = eta_j e^{g_{j-1} - rr},
-  // fw_i = e^{g_i - rr}), and the raw v halves (Vh is written in place after
-  // the next barrier: a row's two halves swap chunks under the swizzle).
-  reinterpret_cast<uint4*>(zero_tile)[tid] = make_uint4(0u, 0u, 0u, 0u);
-  reinterpret_cast<uint4*>(zero_tile)[tid + 256] = make_uint4(0u, 0u, 0u, 0u);
-  float v[32];
-  if (r < 64) {
-    store_half_sw(xt_tile, r, h, x, __expf(gC - sc.g[r]));
-    if (h == 0 && factored) {
-      const float rr = 0.5f * gC;
-      sc.fu[r] = __expf(rr - sc.g[r]);
-      sc.fv[r] = sc.eta[r] * __expf(sc.gx[r] - rr);
-      sc.fw[r] = __expf(sc.g[r] - rr);
-    }
-  } else if (r - 64 < n) {
-    load_half_plain(vh, r - 64, h, v);
-  } else {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = 0.f;
+  // Rank-1 decay factors around rr = g_C / 2: fu_l = e^{rr - g_l},
+  // fv_j = eta_j e^{g_{j-1} - rr}, fw_i = e^{g_i - rr}.
+  if (r < 64 && h == 0 && factored) {
+    const float rr = 0.5f * gC;
+    sc.fu[r] = __expf(rr - sc.g[r]);
+    sc.fv[r] = sc.eta[r] * __expf(sc.gx[r] - rr);
+    sc.fw[r] = __expf(sc.g[r] - rr);
   }
   if (!sc.fail && !mbar_wait(&sc.bar_mma, 0)) sc.fail = 1;
   tc_fence_after();
-  __syncthreads();  // fu/fv/fw visible; raw v read; MMA1 has finished reading [X; Q]
-  if (r >= 64) store_half_sw(vh, r - 64, h, v, sc.eta[r - 64]);
+  __syncthreads();  // factors visible; MMA1 has finished reading [K; Q]
+
+  // Xt = Diag(e^{g_C - g}) X over the K tile, the zero tile (m = 64), Vh in place.
+  if (!kWide) {
+    reinterpret_cast<uint4*>(zero_tile)[tid] = make_uint4(0u, 0u, 0u, 0u);
+    reinterpret_cast<uint4*>(zero_tile)[tid + 256] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (r < 64) {
+    const float xs = __expf(gC - sc.g[r]) * nr;
+    store_half_sw(xt_tile + j * L::kAtom, r, h, x, xs);
+    if (kWide) store_half_sw(xt_tile + (1 - j) * L::kAtom, r, h, xo, xs);
+  } else {
+    // Each thread rewrites exactly the four chunks it reads.
+    float v[32];
+    load_half_sw(vh, r - 64, h, v);
+    store_half_sw(vh, r - 64, h, v, sc.eta[r - 64]);
+  }
   {
     float d[32];
     tmem_ld32(tlane + 32 * h, d);
+    // Cosines first: d_l = <phi(row r), x_l> (bounded), then the decay factors.
+#pragma unroll
+    for (int l = 0; l < 32; ++l) d[l] = (d[l] * nr) * sc.nrm[32 * h + l];
     if (r < 64) {
-      // A row r: eta_r e^{g_{r-1} - g_l} G[r][l] for l < r (computed, then stored)
+      // A row r: eta_r e^{g_{r-1} - g_l} <x_r, x_l> for l < r (computed, then stored)
       if (f1) {
         if (factored) {
           const float vr = sc.fv[r];
@@ -417,7 +502,7 @@ __global__ void __launch_bounds__(kMapThreads, 3) tc_chunk_map_kernel(ChunkArgs 
           arow[l4] = make_float4(d[4 * l4], d[4 * l4 + 1], d[4 * l4 + 2], d[4 * l4 + 3]);
       }
     } else {
-      // P row i: e^{g_i - g_j} (Q X^T)[i][j] for j <= i
+      // P row i: e^{g_i - g_j} <phi(q_i), x_j> for j <= i
       const int i = r - 64;
       if (factored) {
         const float wi = sc.fw[i];
@@ -442,20 +527,20 @@ __global__ void __launch_bounds__(kMapThreads, 3) tc_chunk_map_kernel(ChunkArgs 
     float trow[32];
     const int end = (r | 15) + 1;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int col = 32 * h + j;
-      trow[j] = f1 ? ((col < end) ? Ts[r * kLdT + col] : 0.f) : ((col == r) ? 1.f : 0.f);
+    for (int i = 0; i < 32; ++i) {
+      const int col = 32 * h + i;
+      trow[i] = f1 ? ((col < end) ? Ts[r * kLdT + col] : 0.f) : ((col == r) ? 1.f : 0.f);
     }
     store_half_sw(r1, r, h, trow, 1.f);
   }
   __syncthreads();  // Xh overwrites the solve scratch
-  if (r < 64) store_half_sw(r2, r, h, x, f1 ? sc.eta[r] * __expf(sc.gx[r]) : 0.f);
+  if (r < 64) store_half_sw(r2, r, h, x, f1 ? sc.eta[r] * __expf(sc.gx[r]) * nr : 0.f);
   fence_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
 
-  // ---- MMA2: D[0:64) = [Xh^T; Vh^T] T^T = [W^T; U~^T] ----
+  // ---- MMA2: D[0:64) = [Xh^T; Vh^T] T^T = [W^T; U~^T] (columns of half j) ----
   if (tid == 0) {
     mma_k64(tmem, smem_addr(r2), true, kLboA2, smem_addr(r1), false, 16,
             idesc_bf16(128, 64, true, false), false);
@@ -473,40 +558,86 @@ __global__ void __launch_bounds__(kMapThreads, 3) tc_chunk_map_kernel(ChunkArgs 
   if (__syncthreads_or(sc.fail)) goto teardown;
   tc_fence_after();
 
-  // ---- MMA3: D[0:128) = [Xt^T; 0] [W | U~] + [0; P] [W | U~] ----
+  // ---- MMA3 ----
+  //   m = 64:  D[0:128) = [Xt^T; 0] [W | U~] + [0; P] [W | U~]
+  //   m = 128: D[0:128) = Xt^T [W | U~];  D[128:256) = [junk; P] [W | U~]
   if (tid == 0) {
-    mma_k64(tmem, smem_addr(xt_tile), true, 8192, smem_addr(r1), false, 16,
-            idesc_bf16(128, 128, true, false), false);
-    mma_k64(tmem, smem_addr(zero_tile), false, 16, smem_addr(r1), false, 16,
-            idesc_bf16(128, 128, false, false), true);
+    if (kWide) {
+      mma_k64(tmem, smem_addr(xt_tile), true, L::kAtom, smem_addr(r1), false, 16,
+              idesc_bf16(128, 128, true, false), false);
+      mma_k64(tmem + 128, smem_addr(p_tile - 8192), false, 16, smem_addr(r1), false, 16,
+              idesc_bf16(128, 128, false, false), false);
+    } else {
+      mma_k64(tmem, smem_addr(xt_tile), true, 8192, smem_addr(r1), false, 16,
+              idesc_bf16(128, 128, true, false), false);
+      mma_k64(tmem, smem_addr(zero_tile), false, 16, smem_addr(r1), false, 16,
+              idesc_bf16(128, 128, false, false), true);
+    }
     mma_commit(&sc.bar_mma);
   }
   if (!mbar_wait(&sc.bar_mma, 0)) sc.fail = 1;
   tc_fence_after();
   if (!__syncthreads_or(sc.fail)) {
     unsigned char* map = reinterpret_cast<unsigned char*>(a.workspace) +
-                         (size_t)(bh * nchunks + c) * kMapBytes;
+                         (size_t)(bh * nchunks + c) * L::kMapBytes;
     // The map images are staged in shared memory (the MMA3 operands are dead)
-    // and leave in two bulk copies.
-    unsigned char* mc_stage = a3;  // 16 KB
-    unsigned char* nc_stage = r1;  // 16 KB
+    // and leave by bulk copies.
     float d[32];
-    tmem_ld32(tlane + 32 * h, d);
-    // Mc row: rows < 64 -> -Xt^T W ; rows >= 64 -> e^{g_i} q_i - P W
-    const float eg = (r >= 64) ? __expf(sc.g[r - 64]) : 0.f;
+    if constexpr (!kWide) {
+      unsigned char* mc_stage = kt;  // 16 KB over the K and Q tiles
+      unsigned char* nc_stage = r1;  // 16 KB
+      tmem_ld32(tlane + 32 * h, d);
+      // Mc row: rows < 64 -> -Xt^T W ; rows >= 64 -> e^{g_i} phi(q_i) - P W
+      const float eq = (r >= 64) ? __expf(sc.g[r - 64]) * nr : 0.f;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) d[j] = (r < 64) ? -d[j] : eg * x[j] - d[j];
-    store_half_sw(mc_stage, r, h, d, 1.f);
-    tmem_ld32(tlane + 64 + 32 * h, d);
-    store_half_sw(nc_stage, r, h, d, 1.f);  // Nc: chunk cc at position cc ^ (row & 7)
-    fence_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-      *reinterpret_cast<float*>(map + kMcBytes + kNcBytes) = __expf(gC);
-      bulk_s2g(map, mc_stage, kMcBytes);
-      bulk_s2g(map + kMcBytes, nc_stage, kNcBytes);
-      bulk_commit();
-      bulk_wait<0>();  // the staging must outlive the copies; the map is complete
+      for (int i = 0; i < 32; ++i) d[i] = (r < 64) ? -d[i] : eq * x[i] - d[i];
+      store_half_sw(mc_stage, r, h, d, 1.f);
+      tmem_ld32(tlane + 64 + 32 * h, d);
+      store_half_sw(nc_stage, r, h, d, 1.f);  // Nc: chunk cc at position cc ^ (row & 7)
+      fence_async_smem();
+      __syncthreads();
+      if (tid == 0) {
+        *reinterpret_cast<float*>(map + kMcBytes + kNcBytes) = __expf(gC);
+        bulk_s2g(map, mc_stage, kMcBytes);
+        bulk_s2g(map + kMcBytes, nc_stage, kNcBytes);
+        bulk_commit();
+        bulk_wait_read<0>();  // the staging must outlive the copies' reads
+      }
+    } else {
+      // K-atom j of Mc (rows 0..127: -Xt^T W_j; rows 128..191: e^g phi(Q)_j - P W_j)
+      // and d_v slice j of Nc (rows 0..127: Xt^T U~_j; rows 128..191: P U~_j).
+      unsigned char* mcs_stage = base;          // 16 KB
+      unsigned char* mco_stage = base + 16384;  // 8 KB
+      unsigned char* nco_stage = base + 24576;  // 8 KB
+      unsigned char* ncs_stage = r1;            // 16 KB
+      tmem_ld32(tlane + 32 * h, d);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) d[i] = -d[i];
+      store_half_sw(mcs_stage, r, h, d, 1.f);
+      tmem_ld32(tlane + 64 + 32 * h, d);
+      store_half_sw(ncs_stage, r, h, d, 1.f);
+      if (r >= 64) {  // warps 2, 3, 6, 7: lanes 64..127 hold P [W_j | U~_j]
+        const float eq = __expf(sc.g[r - 64]) * nr;
+        tmem_ld32(tlane + 128 + 32 * h, d);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) d[i] = eq * x[i] - d[i];
+        store_half_sw(mco_stage, r - 64, h, d, 1.f);
+        tmem_ld32(tlane + 192 + 32 * h, d);
+        store_half_sw(nco_stage, r - 64, h, d, 1.f);
+      }
+      fence_async_smem();
+      __syncthreads();
+      if (tid == 0) {
+        unsigned char* mc = map + j * L::kMcAtom;
+        unsigned char* nc = map + (2 + j) * L::kMcAtom;
+        if (j == 0) *reinterpret_cast<float*>(map + 4 * L::kMcAtom) = __expf(gC);
+        bulk_s2g(mc, mcs_stage, 16384);
+        bulk_s2g(mc + 16384, mco_stage, 8192);
+        bulk_s2g(nc, ncs_stage, 16384);
+        bulk_s2g(nc + 16384, nco_stage, 8192);
+        bulk_commit();
+        bulk_wait_read<0>();
+      }
     }
   }
 
@@ -515,7 +646,7 @@ teardown:
   if (sc.fail && tid == 0) flag_error(err);
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 128);
+  if (warp == 0) tmem_dealloc(tmem, L::kTmemCols);
 }
 
 // ---------------------------------------------------------------------------
@@ -739,47 +870,300 @@ __global__ void __launch_bounds__(kScanThreads)
   if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
+// ---------------------------------------------------------------------------
+// Scan kernel for m = d_v = 128: one CTA per (head, d_v slice j of 64
+// columns); the slices are independent (the map acts on each column of S).
+// Per chunk two MMAs read the same state operand S_j (128 x 64, bf16): rows
+// 0..127 of Mc (the state rows, K = 128 over two K-atoms) and rows 128..255
+// (the 64 output rows, then 64 rows past the map that land in unused
+// accumulator lanes).  Warps 0..15 own the state rows (lane quarter w & 3,
+// columns 16 (w >> 2) .. +15), warps 16, 17, 20, 21 the output rows (lane
+// quarters 0 and 1, column halves), warp 18 issues MMAs and refills, warp 19
+// has no work.
+constexpr int kStages128 = 2;
+constexpr int kScan128Threads = 32 * 22;
+constexpr uint32_t kStage128Bytes = 73 * 1024;  // Mc atoms (2 x 24 KB), Nc slice (24 KB), e^{g_C}
+
+struct Scan128Smem {
+  unsigned char stage[kStages128][kStage128Bytes];
+  unsigned char sop[16384];        // S_j as MN-major B operand (128 rows = m, 64 bf16 along d_v)
+  unsigned char ostage[2][8192];   // o tiles (64 tokens x 64 bf16, 128B-swizzled) for TMA
+  uint64_t full[kStages128];       // map of the stage has arrived
+  uint64_t empty[kStages128];      // every math warp is done with the stage
+  uint64_t mma_done[2];            // MMAs into accumulator buffer b have completed
+  uint64_t o_done[2];              // output warps have read accumulator buffer b
+  uint64_t s_ready;                // the next state operand is in sop
+  uint32_t tmem_base;
+  int fail;
+};
+
+__device__ __forceinline__ void issue_map_load128(Scan128Smem& s, int st, const unsigned char* m,
+                                                  int j) {
+  constexpr uint32_t kA = MapLayout<128>::kMcAtom;
+  unsigned char* dst = s.stage[st];
+  mbar_expect_tx(&s.full[st], 3 * kA + 16);
+  bulk_g2s(dst, m, kA, &s.full[st]);
+  bulk_g2s(dst + kA, m + kA, kA, &s.full[st]);
+  bulk_g2s(dst + 2 * kA, m + (2 + j) * kA, kA, &s.full[st]);
+  bulk_g2s(dst + 3 * kA, m + 4 * kA, 16, &s.full[st]);
+}
+
+__global__ void __launch_bounds__(kScan128Threads)
+    tc_chunk_scan128_kernel(ChunkArgs a, int nchunks, int* err,
+                            const __grid_constant__ CUtensorMap tm_o) {
+  constexpr uint32_t kA = MapLayout<128>::kMcAtom;
+  constexpr uint32_t kMap = MapLayout<128>::kMapBytes;
+  constexpr int kOutWarps = 4;
+  extern __shared__ unsigned char smem_raw[];
+  Scan128Smem& s = *reinterpret_cast<Scan128Smem*>(align1024(smem_raw));
+  volatile int* fail = &s.fail;
+  const int64_t bh = blockIdx.x >> 1;
+  const int j = blockIdx.x & 1;  // d_v slice
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool issuer = warp == 18;
+  const bool swarp = warp < 16;
+  const bool owarp = warp == 16 || warp == 17 || warp == 20 || warp == 21;
+  const int row = 32 * (warp & 3) + lane;  // TMEM lane
+  const unsigned char* ws = reinterpret_cast<const unsigned char*>(a.workspace) +
+                            (size_t)bh * nchunks * kMap;
+  if (warp == 0) tmem_alloc(&s.tmem_base, 256);
+  if (tid == 0) {
+    for (int st = 0; st < kStages128; ++st) {
+      mbar_init(&s.full[st], 1);
+      mbar_init(&s.empty[st], 16 + kOutWarps);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s.mma_done[b], 1);
+      mbar_init(&s.o_done[b], kOutWarps);
+    }
+    mbar_init(&s.s_ready, 16);
+    fence_mbar_init();
+    s.fail = 0;
+  }
+  // State: each state thread keeps 16 columns of its row in fp32 registers.
+  const int qc = (warp >> 2) & 3;  // state warps: column quarter
+  float S[16];
+  if (swarp) {
+    const float* src = a.S0 ? a.S0 + (bh * 128 + row) * 128 + 64 * j + 16 * qc : nullptr;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) S[i] = src ? src[i] : 0.f;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const uint32_t tmem = s.tmem_base;
+
+  if (issuer) {
+    if (lane == 0) {
+      for (int st = 0; st < kStages128 && st < nchunks; ++st)
+        issue_map_load128(s, st, ws + (size_t)st * kMap, j);
+      for (int c = 0; c < nchunks; ++c) {
+        const int st = c % kStages128, b = c & 1;
+        bool ok = c < 2 || mbar_wait(&s.o_done[b], (uint32_t)((c - 2) >> 1) & 1u);
+        ok = ok && mbar_wait(&s.full[st], (uint32_t)(c / kStages128) & 1u);
+        ok = ok && mbar_wait(&s.s_ready, (uint32_t)c & 1u);
+        if (!ok) {
+          *fail = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t mc = smem_addr(s.stage[st]), sop = smem_addr(s.sop);
+        const uint32_t idesc = idesc_bf16(128, 64, false, true);
+        // State rows, then output rows; K = 128 as two 64-wide atoms.
+        mma_k64(tmem + 128 * b, mc, false, 16, sop, true, 8192, idesc, false);
+        mma_k64(tmem + 128 * b, mc + kA, false, 16, sop + 8192, true, 8192, idesc, true);
+        mma_k64(tmem + 128 * b + 64, mc + 16384, false, 16, sop, true, 8192, idesc, false);
+        mma_k64(tmem + 128 * b + 64, mc + kA + 16384, false, 16, sop + 8192, true, 8192, idesc,
+                true);
+        mma_commit(&s.mma_done[b]);
+        const int cp = c - 1;
+        if (cp >= 0 && cp + kStages128 < nchunks) {
+          const int sp = cp % kStages128;
+          if (!mbar_wait(&s.empty[sp], (uint32_t)(cp / kStages128) & 1u)) {
+            *fail = 1;
+            break;
+          }
+          issue_map_load128(s, sp, ws + (size_t)(cp + kStages128) * kMap, j);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (swarp) {
+    const uint32_t tlane = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 16 * qc;
+    const uint32_t ch0 = (uint32_t)(((2 * qc) ^ (row & 7)) << 4);
+    const uint32_t ch1 = (uint32_t)(((2 * qc + 1) ^ (row & 7)) << 4);
+    *reinterpret_cast<uint4*>(s.sop + row * 128 + ch0) = pack8(S, 1.f);
+    *reinterpret_cast<uint4*>(s.sop + row * 128 + ch1) = pack8(S + 8, 1.f);
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s.s_ready);
+    for (int c = 0; c < nchunks; ++c) {
+      if (__any_sync(0xffffffffu, *fail)) break;
+      const int st = c % kStages128, b = c & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&s.full[st], (uint32_t)(c / kStages128) & 1u))) {
+        *fail = 1;
+        break;
+      }
+      const unsigned char* nrow = s.stage[st] + 2 * kA + row * 128;
+      const uint4 n0 = *reinterpret_cast<const uint4*>(nrow + ch0);
+      const uint4 n1 = *reinterpret_cast<const uint4*>(nrow + ch1);
+      const float gC = *reinterpret_cast<const float*>(s.stage[st] + 3 * kA);
+      if (!__all_sync(0xffffffffu, mbar_wait(&s.mma_done[b], (uint32_t)(c >> 1) & 1u))) {
+        *fail = 1;
+        break;
+      }
+      tc_fence_after();
+      float d[16];
+      tmem_ld16(tlane + 128 * b, d);
+      tc_fence_before();
+      add_bf16x16(d, n0, n1);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) S[i] = gC * S[i] + d[i];
+      *reinterpret_cast<uint4*>(s.sop + row * 128 + ch0) = pack8(S, 1.f);
+      *reinterpret_cast<uint4*>(s.sop + row * 128 + ch1) = pack8(S + 8, 1.f);
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&s.s_ready);
+        mbar_arrive(&s.empty[st]);
+      }
+    }
+    if (!*fail) {
+      float* dst = a.S_out + (bh * 128 + row) * 128 + 64 * j + 16 * qc;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) dst[i] = S[i];
+    }
+  } else if (owarp) {
+    // Output rows 0..63 (lanes 0..63 of the second accumulator), 32 columns
+    // per thread; the o tile leaves by one TMA store per chunk (warp 16, lane
+    // 0); exits are agreed on by the output warps at a named barrier.
+    const int oh = (warp - 16) >> 2;  // column half: 32 oh .. 32 oh + 31
+    const uint32_t tlane = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 64 + 32 * oh;
+    const bool o_issuer = warp == 16 && lane == 0;
+    for (int c = 0; c < nchunks; ++c) {
+      const int st = c % kStages128, b = c & 1;
+      bool ok = !*fail && mbar_wait(&s.full[st], (uint32_t)(c / kStages128) & 1u);
+      ok = ok && mbar_wait(&s.mma_done[b], (uint32_t)(c >> 1) & 1u);
+      if (o_issuer) bulk_wait_read<1>();
+      if (named_sync_or(1, 32 * kOutWarps, !ok)) {
+        *fail = 1;
+        break;
+      }
+      tc_fence_after();
+      float d[32];
+      tmem_ld32(tlane + 128 * b, d);
+      tc_fence_before();
+      {
+        // + Nc rows 128.. (output rows), this thread's four 16-byte chunks
+        const unsigned char* nrow = s.stage[st] + 2 * kA + (128 + row) * 128;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 pk =
+              *reinterpret_cast<const uint4*>(nrow + (((4 * oh + q) ^ (row & 7)) << 4));
+          const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&pk);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(hv[e]);
+            d[8 * q + 2 * e] += f.x;
+            d[8 * q + 2 * e + 1] += f.y;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&s.o_done[b]);
+        mbar_arrive(&s.empty[st]);
+      }
+      unsigned char* orow = s.ostage[b] + row * 128;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4*>(orow + (((4 * oh + q) ^ (row & 7)) << 4)) = pack8(d + 8 * q, 1.f);
+      fence_async_smem();
+      named_sync(1, 32 * kOutWarps);
+      if (o_issuer) {
+        tma_store_3d(&tm_o, s.ostage[b], 64 * j, c * kC, (int)bh);
+        bulk_commit();
+      }
+    }
+    if (o_issuer) bulk_wait<0>();
+  }
+  __syncthreads();
+  if (*fail && tid == 0) flag_error(err);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
 }  // namespace
 
-bool tc_path_applies(int dtype, int m, int dv, int C) {
-  return dtype == FALCON_BF16 && m == 64 && dv == 64 && C == 64;
+bool tc_path_applies(int dtype, int m, int dv, int C, int64_t BH, int64_t T) {
+  // TMA box coordinates are 32-bit: rows and heads stay below 2^31.
+  return dtype == FALCON_BF16 && (m == 64 || m == 128) && dv == m && C == 64 &&
+         T < (int64_t(1) << 31) - kC && BH < (int64_t(1) << 30);
 }
 
-size_t tc_workspace_bytes(int64_t BH, int64_t T) {
+size_t tc_workspace_bytes(int m, int64_t BH, int64_t T) {
   const int64_t nch = (T + kC - 1) / kC;
-  return (size_t)(BH * nch) * kMapBytes;
+  return (size_t)(BH * nch) * (m == 128 ? MapLayout<128>::kMapBytes : MapLayout<64>::kMapBytes);
 }
 
-cudaError_t launch_tc_chunked(const ChunkArgs& a, int* err, cudaStream_t stream) {
-  const int nchunks = (int)((a.T + kC - 1) / kC);
-  const size_t map_smem = kMapSmemBytes + 1024;
-  cudaError_t e = cudaFuncSetAttribute(tc_chunk_map_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)map_smem);
+namespace {
+
+template <int M>
+cudaError_t launch_map(const ChunkArgs& a, int nchunks, int* err, cudaStream_t stream) {
+  const size_t smem = map_smem_bytes<M>() + 1024;
+  cudaError_t e = cudaFuncSetAttribute(tc_chunk_map_kernel<M>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  tc_chunk_map_kernel<<<dim3(nchunks, (unsigned)a.BH), kMapThreads, map_smem, stream>>>(a, nchunks,
-                                                                                   err);
-  e = cudaGetLastError();
+  CUtensorMap tm_k, tm_q, tm_v;
+  if (!encode_rows_bf16(&tm_k, a.k, M, (uint64_t)a.T, (uint64_t)a.BH, 64, kC) ||
+      !encode_rows_bf16(&tm_q, a.q, M, (uint64_t)a.T, (uint64_t)a.BH, 64, kC) ||
+      !encode_rows_bf16(&tm_v, a.v, M, (uint64_t)a.T, (uint64_t)a.BH, 64, kC))
+    return cudaErrorInvalidValue;
+  tc_chunk_map_kernel<M><<<dim3(nchunks * MapLayout<M>::kHalves, (unsigned)a.BH), kMapThreads,
+                           smem, stream>>>(a, nchunks, err, tm_k, tm_q, tm_v);
+  return cudaGetLastError();
+}
+
+// Programmatic dependent launch: the scan grid may be scheduled while the map
+// grid drains; griddepcontrol.wait in the scan orders it after every map write.
+template <typename Kernel>
+cudaError_t launch_scan(Kernel kernel, unsigned grid, unsigned threads, size_t smem,
+                        const ChunkArgs& a, int nchunks, int* err, const CUtensorMap& tm_o,
+                        cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
   if (e != cudaSuccess) return e;
-  const size_t scan_smem = sizeof(ScanSmem) + 1024;
-  e = cudaFuncSetAttribute(tc_chunk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)scan_smem);
-  if (e != cudaSuccess) return e;
-  // Programmatic dependent launch: the scan grid may be scheduled while the map
-  // grid drains; griddepcontrol.wait in the scan orders it after every map write.
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)a.BH);
-  cfg.blockDim = dim3(kScanThreads);
-  cfg.dynamicSmemBytes = scan_smem;
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a, nchunks, err, tm_o);
+}
+
+}  // namespace
+
+cudaError_t launch_tc_chunked(const ChunkArgs& a, int* err, cudaStream_t stream) {
+  const int nchunks = (int)((a.T + kC - 1) / kC);
+  const bool wide = a.m == 128;
+  cudaError_t e = wide ? launch_map<128>(a, nchunks, err, stream)
+                       : launch_map<64>(a, nchunks, err, stream);
+  if (e != cudaSuccess) return e;
   CUtensorMap tm_o;
-  if (!encode_rows_bf16(&tm_o, a.o, 64, (uint64_t)a.T, (uint64_t)a.BH, 64, kC))
+  if (!encode_rows_bf16(&tm_o, a.o, a.m, (uint64_t)a.T, (uint64_t)a.BH, 64, kC))
     return cudaErrorInvalidValue;
-  return cudaLaunchKernelEx(&cfg, tc_chunk_scan_kernel, a, nchunks, err, tm_o);
+  if (wide)
+    return launch_scan(tc_chunk_scan128_kernel, (unsigned)(2 * a.BH), kScan128Threads,
+                       sizeof(Scan128Smem) + 1024, a, nchunks, err, tm_o, stream);
+  return launch_scan(tc_chunk_scan_kernel, (unsigned)a.BH, kScanThreads, sizeof(ScanSmem) + 1024,
+                     a, nchunks, err, tm_o, stream);
 }
 
 }  // namespace falcon

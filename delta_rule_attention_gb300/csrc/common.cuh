@@ -73,9 +73,9 @@ struct ChunkArgs {
 size_t generic_workspace_bytes(int64_t BH, int64_t T, int m, int dv, int C);
 cudaError_t launch_generic_chunked(const ChunkArgs& a, cudaStream_t stream);
 
-// Tensor-core path (bf16, m = dv = chunk = 64).
-bool tc_path_applies(int dtype, int m, int dv, int C);
-size_t tc_workspace_bytes(int64_t BH, int64_t T);
+// Tensor-core path (bf16, m = dv in {64, 128}, chunk = 64).
+bool tc_path_applies(int dtype, int m, int dv, int C, int64_t BH, int64_t T);
+size_t tc_workspace_bytes(int m, int64_t BH, int64_t T);
 cudaError_t launch_tc_chunked(const ChunkArgs& a, int* err, cudaStream_t stream);
 
 struct DecodeArgs {
