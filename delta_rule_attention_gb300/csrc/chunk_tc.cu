@@ -658,7 +658,7 @@ teardown:
 // (the MMA of chunk c, then the refill of the stage chunk c-1 used), the output
 // rows run beside the chain, and the accumulator is double-buffered in TMEM.
 // Every hand-off is one mbarrier arrival per warp.
-constexpr int kStages = 3;
+constexpr int kStages = 5;
 constexpr int kScanMathWarps = 16;
 constexpr int kScanThreads = 32 * (kScanMathWarps + 1);
 
@@ -746,6 +746,8 @@ __global__ void __launch_bounds__(kScanThreads)
     if (lane == 0) {
       for (int st = 0; st < kStages && st < nchunks; ++st)
         issue_map_load(s, st, ws + (size_t)st * kMapBytes);
+      const uint64_t bdesc = sw128_desc(smem_addr(s.sop), 8192, 1024);
+      const uint32_t idesc = idesc_bf16(128, 64, false, true);
       for (int c = 0; c < nchunks; ++c) {
         const int st = c % kStages, b = c & 1;
         // The state operand is the last to be ready: wait for it last.
@@ -757,8 +759,8 @@ __global__ void __launch_bounds__(kScanThreads)
           break;
         }
         tc_fence_after();
-        mma_k64(tmem + 64 * b, smem_addr(s.mc[st]), false, 16, smem_addr(s.sop), true, 8192,
-                idesc_bf16(128, 64, false, true), false);
+        mma_k64_desc(tmem + 64 * b, sw128_desc(smem_addr(s.mc[st]), 16, 1024), kStepK, bdesc,
+                     kStepMN, idesc, false);
         mma_commit(&s.mma_done[b]);
         // Refill the stage of chunk c - 1 once every math warp is done with it.
         const int cp = c - 1;
@@ -880,17 +882,24 @@ __global__ void __launch_bounds__(kScanThreads)
 // columns 16 (w >> 2) .. +15), warps 16, 17, 20, 21 the output rows (lane
 // quarters 0 and 1, column halves), warp 18 issues MMAs and refills, warp 19
 // has no work.
-constexpr int kStages128 = 2;
+// The Mc atoms go through a three-stage shared-memory ring; Nc rows are read
+// from global memory (brought into L2 ahead by the issue warp) one chunk ahead
+// into registers, which keeps three map stages within shared memory.
+constexpr int kStages128 = 3;
 constexpr int kScan128Threads = 32 * 22;
-constexpr uint32_t kStage128Bytes = 73 * 1024;  // Mc atoms (2 x 24 KB), Nc slice (24 KB), e^{g_C}
+constexpr uint32_t kStage128Bytes = 49 * 1024;  // Mc atoms (2 x 24 KB), e^{g_C}
 
 struct Scan128Smem {
   unsigned char stage[kStages128][kStage128Bytes];
-  unsigned char sop[16384];        // S_j as MN-major B operand (128 rows = m, 64 bf16 along d_v)
+  // S_j as MN-major B operand (128 rows = m, 64 bf16 along d_v), double-buffered:
+  // chunk c reads sop[c & 1] while the state warps write S_{c+1} to the other
+  // buffer (the output MMAs of chunk c may still be reading it).
+  unsigned char sop[2][16384];
   unsigned char ostage[2][8192];   // o tiles (64 tokens x 64 bf16, 128B-swizzled) for TMA
   uint64_t full[kStages128];       // map of the stage has arrived
   uint64_t empty[kStages128];      // every math warp is done with the stage
-  uint64_t mma_done[2];            // MMAs into accumulator buffer b have completed
+  uint64_t mma_done[2];            // state MMAs into accumulator buffer b have completed
+  uint64_t omma_done[2];           // output MMAs into accumulator buffer b have completed
   uint64_t o_done[2];              // output warps have read accumulator buffer b
   uint64_t s_ready;                // the next state operand is in sop
   uint32_t tmem_base;
@@ -901,11 +910,16 @@ __device__ __forceinline__ void issue_map_load128(Scan128Smem& s, int st, const 
                                                   int j) {
   constexpr uint32_t kA = MapLayout<128>::kMcAtom;
   unsigned char* dst = s.stage[st];
-  mbar_expect_tx(&s.full[st], 3 * kA + 16);
+  mbar_expect_tx(&s.full[st], 2 * kA + 16);
   bulk_g2s(dst, m, kA, &s.full[st]);
   bulk_g2s(dst + kA, m + kA, kA, &s.full[st]);
-  bulk_g2s(dst + 2 * kA, m + (2 + j) * kA, kA, &s.full[st]);
-  bulk_g2s(dst + 3 * kA, m + 4 * kA, 16, &s.full[st]);
+  bulk_g2s(dst + 2 * kA, m + 4 * kA, 16, &s.full[st]);
+  bulk_prefetch_l2(m + (2 + j) * kA, kA);  // this CTA's Nc slice
+}
+
+// 16 bytes of the (read-only) workspace.
+__device__ __forceinline__ uint4 ld_map16(const unsigned char* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
 }
 
 __global__ void __launch_bounds__(kScan128Threads)
@@ -934,6 +948,7 @@ __global__ void __launch_bounds__(kScan128Threads)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s.mma_done[b], 1);
+      mbar_init(&s.omma_done[b], 1);
       mbar_init(&s.o_done[b], kOutWarps);
     }
     mbar_init(&s.s_ready, 16);
@@ -958,6 +973,7 @@ __global__ void __launch_bounds__(kScan128Threads)
     if (lane == 0) {
       for (int st = 0; st < kStages128 && st < nchunks; ++st)
         issue_map_load128(s, st, ws + (size_t)st * kMap, j);
+      const uint32_t idesc = idesc_bf16(128, 64, false, true);
       for (int c = 0; c < nchunks; ++c) {
         const int st = c % kStages128, b = c & 1;
         bool ok = c < 2 || mbar_wait(&s.o_done[b], (uint32_t)((c - 2) >> 1) & 1u);
@@ -968,15 +984,19 @@ __global__ void __launch_bounds__(kScan128Threads)
           break;
         }
         tc_fence_after();
-        const uint32_t mc = smem_addr(s.stage[st]), sop = smem_addr(s.sop);
-        const uint32_t idesc = idesc_bf16(128, 64, false, true);
-        // State rows, then output rows; K = 128 as two 64-wide atoms.
-        mma_k64(tmem + 128 * b, mc, false, 16, sop, true, 8192, idesc, false);
-        mma_k64(tmem + 128 * b, mc + kA, false, 16, sop + 8192, true, 8192, idesc, true);
-        mma_k64(tmem + 128 * b + 64, mc + 16384, false, 16, sop, true, 8192, idesc, false);
-        mma_k64(tmem + 128 * b + 64, mc + kA + 16384, false, 16, sop + 8192, true, 8192, idesc,
-                true);
+        // State rows (committed on their own: the state chain waits only for
+        // them), then output rows; K = 128 as two 64-wide atoms.
+        const uint64_t ad = sw128_desc(smem_addr(s.stage[st]), 16, 1024);
+        const uint64_t bdesc0 = sw128_desc(smem_addr(s.sop[c & 1]), 8192, 1024);
+        const uint64_t bdesc1 = bdesc0 + (8192 >> 4);  // state rows 64..127
+        mma_k64_desc(tmem + 128 * b, ad, kStepK, bdesc0, kStepMN, idesc, false);
+        mma_k64_desc(tmem + 128 * b, ad + (kA >> 4), kStepK, bdesc1, kStepMN, idesc, true);
         mma_commit(&s.mma_done[b]);
+        mma_k64_desc(tmem + 128 * b + 64, ad + (16384 >> 4), kStepK, bdesc0, kStepMN, idesc,
+                     false);
+        mma_k64_desc(tmem + 128 * b + 64, ad + ((kA + 16384) >> 4), kStepK, bdesc1, kStepMN,
+                     idesc, true);
+        mma_commit(&s.omma_done[b]);
         const int cp = c - 1;
         if (cp >= 0 && cp + kStages128 < nchunks) {
           const int sp = cp % kStages128;
@@ -993,22 +1013,31 @@ __global__ void __launch_bounds__(kScan128Threads)
     const uint32_t tlane = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 16 * qc;
     const uint32_t ch0 = (uint32_t)(((2 * qc) ^ (row & 7)) << 4);
     const uint32_t ch1 = (uint32_t)(((2 * qc + 1) ^ (row & 7)) << 4);
-    *reinterpret_cast<uint4*>(s.sop + row * 128 + ch0) = pack8(S, 1.f);
-    *reinterpret_cast<uint4*>(s.sop + row * 128 + ch1) = pack8(S + 8, 1.f);
+    *reinterpret_cast<uint4*>(s.sop[0] + row * 128 + ch0) = pack8(S, 1.f);
+    *reinterpret_cast<uint4*>(s.sop[0] + row * 128 + ch1) = pack8(S + 8, 1.f);
     fence_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&s.s_ready);
+    // Nc rows of this thread (state rows 0..127 of slice j), chunk 0 first.
+    const unsigned char* ncg = ws + (2 + j) * kA + row * 128;
+    uint4 n0 = ld_map16(ncg + ch0), n1 = ld_map16(ncg + ch1);
     for (int c = 0; c < nchunks; ++c) {
       if (__any_sync(0xffffffffu, *fail)) break;
       const int st = c % kStages128, b = c & 1;
+      // mma_done of chunk c also covers the MMAs of chunk c - 1 (issued
+      // earlier), the last readers of sop[(c + 1) & 1].
+      unsigned char* sop_next = s.sop[(c + 1) & 1];
       if (!__all_sync(0xffffffffu, mbar_wait(&s.full[st], (uint32_t)(c / kStages128) & 1u))) {
         *fail = 1;
         break;
       }
-      const unsigned char* nrow = s.stage[st] + 2 * kA + row * 128;
-      const uint4 n0 = *reinterpret_cast<const uint4*>(nrow + ch0);
-      const uint4 n1 = *reinterpret_cast<const uint4*>(nrow + ch1);
-      const float gC = *reinterpret_cast<const float*>(s.stage[st] + 3 * kA);
+      const float gC = *reinterpret_cast<const float*>(s.stage[st] + 2 * kA);
+      uint4 m0 = make_uint4(0u, 0u, 0u, 0u), m1 = m0;  // Nc of chunk c + 1
+      if (c + 1 < nchunks) {
+        const unsigned char* nrow = ncg + (size_t)(c + 1) * kMap;
+        m0 = ld_map16(nrow + ch0);
+        m1 = ld_map16(nrow + ch1);
+      }
       if (!__all_sync(0xffffffffu, mbar_wait(&s.mma_done[b], (uint32_t)(c >> 1) & 1u))) {
         *fail = 1;
         break;
@@ -1018,10 +1047,12 @@ __global__ void __launch_bounds__(kScan128Threads)
       tmem_ld16(tlane + 128 * b, d);
       tc_fence_before();
       add_bf16x16(d, n0, n1);
+      n0 = m0;
+      n1 = m1;
 #pragma unroll
       for (int i = 0; i < 16; ++i) S[i] = gC * S[i] + d[i];
-      *reinterpret_cast<uint4*>(s.sop + row * 128 + ch0) = pack8(S, 1.f);
-      *reinterpret_cast<uint4*>(s.sop + row * 128 + ch1) = pack8(S + 8, 1.f);
+      *reinterpret_cast<uint4*>(sop_next + row * 128 + ch0) = pack8(S, 1.f);
+      *reinterpret_cast<uint4*>(sop_next + row * 128 + ch1) = pack8(S + 8, 1.f);
       fence_async_smem();
       __syncwarp();
       if (lane == 0) {
@@ -1041,10 +1072,20 @@ __global__ void __launch_bounds__(kScan128Threads)
     const int oh = (warp - 16) >> 2;  // column half: 32 oh .. 32 oh + 31
     const uint32_t tlane = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 64 + 32 * oh;
     const bool o_issuer = warp == 16 && lane == 0;
+    // Nc rows 128 + row (the output rows of slice j), one chunk ahead.
+    const unsigned char* ncg = ws + (2 + j) * kA + (128 + row) * 128;
+    uint4 nq[4], mq[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) nq[q] = ld_map16(ncg + (((4 * oh + q) ^ (row & 7)) << 4));
     for (int c = 0; c < nchunks; ++c) {
       const int st = c % kStages128, b = c & 1;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        mq[q] = (c + 1 < nchunks)
+                    ? ld_map16(ncg + (size_t)(c + 1) * kMap + (((4 * oh + q) ^ (row & 7)) << 4))
+                    : make_uint4(0u, 0u, 0u, 0u);
       bool ok = !*fail && mbar_wait(&s.full[st], (uint32_t)(c / kStages128) & 1u);
-      ok = ok && mbar_wait(&s.mma_done[b], (uint32_t)(c >> 1) & 1u);
+      ok = ok && mbar_wait(&s.omma_done[b], (uint32_t)(c >> 1) & 1u);
       if (o_issuer) bulk_wait_read<1>();
       if (named_sync_or(1, 32 * kOutWarps, !ok)) {
         *fail = 1;
@@ -1056,11 +1097,10 @@ __global__ void __launch_bounds__(kScan128Threads)
       tc_fence_before();
       {
         // + Nc rows 128.. (output rows), this thread's four 16-byte chunks
-        const unsigned char* nrow = s.stage[st] + 2 * kA + (128 + row) * 128;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const uint4 pk =
-              *reinterpret_cast<const uint4*>(nrow + (((4 * oh + q) ^ (row & 7)) << 4));
+          const uint4 pk = nq[q];
+          nq[q] = mq[q];
           const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&pk);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {

@@ -89,6 +89,11 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// Hint: bring `bytes` (multiple of 16, 16-byte aligned) of global memory into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Shared -> global, tracked by the issuing thread's bulk group.
 __device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
@@ -219,6 +224,21 @@ __device__ __forceinline__ void mma_k64(uint32_t d_tmem, uint32_t a_saddr, bool 
              idesc, (accumulate || ks > 0) ? 1u : 0u);
   }
 }
+
+// The same four k-steps from precomputed descriptors: the start-address field
+// is the low 14 bits (address >> 4), so a k-step adds step >> 4 to the
+// descriptor (2 for a K-major step of 32 B, 128 for an MN-major step of
+// 2048 B; addresses stay below 256 KB, so the field never carries).
+__device__ __forceinline__ void mma_k64_desc(uint32_t d_tmem, uint64_t adesc, uint32_t a_step,
+                                             uint64_t bdesc, uint32_t b_step, uint32_t idesc,
+                                             bool accumulate) {
+#pragma unroll
+  for (int ks = 0; ks < 4; ++ks)
+    mma_bf16(d_tmem, adesc + (uint64_t)(ks * a_step), bdesc + (uint64_t)(ks * b_step), idesc,
+             (accumulate || ks > 0) ? 1u : 0u);
+}
+constexpr uint32_t kStepK = 2;     // K-major k-step in descriptor units (32 B)
+constexpr uint32_t kStepMN = 128;  // MN-major k-step in descriptor units (2048 B)
 
 // TMEM -> registers (warp w of the CTA reads lanes 32 (w % 4) .. +31, one lane
 // per thread).  16 consecutive 32-bit columns of this thread's lane, then wait.
