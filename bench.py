@@ -468,6 +468,40 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+def run_profile(args):
+    """Profiler target: one workload's library calls only (no timing line), so
+    that ncu captures run committed code on a chosen, possibly reduced, size."""
+    import delta_rule_attention_gb300 as falcon
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    calls = args.steps or 3
+    if args.profile == "decode":
+        d = workloads.DECODE
+        if args.profile_size:
+            d = dataclasses.replace(d, n_seq=max(1, args.profile_size // d.H))
+        stream = workloads.DecodeStream(d, device=dev)
+        S = stream.initial_state()
+        xp = torch.zeros((d.N, d.m), device=dev)
+        o = torch.empty((d.N, d.dv), dtype=d.dtype, device=dev)
+        for _ in range(calls):
+            x = stream.step()
+            falcon.falcon1_decode_step(x["q"], x["k"], x["v"], x["beta"], x["lambda"], S, xp,
+                                       phi=d.phi, o=o)
+        name, size = d.name, d.N
+    else:
+        w = {"lm": workloads.LM, "lm1a": workloads.LM_1A, "long": workloads.LONG}[args.profile]
+        if args.profile_size:
+            w = dataclasses.replace(w, T=args.profile_size)
+        x = workloads.generate(w, device=dev)
+        fn = falcon.falcon1_fwd_chunked if w.rule == "falcon1" else falcon.falcon1a_fwd_chunked
+        for _ in range(calls):
+            fn(x["q"], x["k"], x["v"], x["beta"], x["lambda"], chunk=w.chunk, phi=w.phi)
+        name, size = w.name, w.T
+    torch.cuda.synchronize()
+    assert falcon.falcon_sync_check() == 0
+    print(json.dumps({"profile": name, "size": size, "calls": calls, "ok": True}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -477,10 +511,16 @@ def main():
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--profile", choices=["lm", "lm1a", "long", "decode"], default=None,
+                    help="profiler target: run --steps calls of one workload, print no timing")
+    ap.add_argument("--profile-size", type=int, default=None,
+                    help="with --profile: tokens per head (chunked) or states (decode)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.profile:
+        run_profile(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
