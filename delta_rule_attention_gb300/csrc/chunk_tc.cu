@@ -1,13 +1,15 @@
-// Tensor-core (tcgen05) chunked forward for bf16 inputs with m = d_v = C = 64.
+// Tensor-core (tcgen05) chunked forward for bf16 inputs with m = d_v in
+// {64, 128} and chunk C = 64.
 //
 // Two launches:
 //
-//  1. tc_chunk_map_kernel -- one CTA (128 threads) per (head, chunk), all
-//     chunks in parallel.  It turns the chunk into an affine map of the state
-//     entering it (the chunk-local log-space form of the positive-decay
-//     renormalisation of page hyper.ai/fr/papers/2608.27763, Section 4.4
-//     Eq. (4.15)-(4.16); WY/UT form with one triangular solve per chunk, as
-//     the complexity table of page juhoplayground.github.io describes):
+//  1. tc_chunk_map_kernel<M> -- all chunks in parallel (one CTA per chunk for
+//     m = 64, two for m = 128, each taking one column half).  It turns the
+//     chunk into an affine map of the state entering it (the chunk-local
+//     log-space form of the positive-decay renormalisation of page
+//     hyper.ai/fr/papers/2608.27763, Section 4.4 Eq. (4.15)-(4.16); WY/UT form
+//     with one triangular solve per chunk, as the complexity table of page
+//     juhoplayground.github.io describes):
 //
 //        S'  = e^{g_C} S + Mc_top S + Nc_top,   Mc_top = -Xt^T W,    Nc_top = Xt^T U~
 //        O   =             Mc_bot S + Nc_bot,   Mc_bot = Diag(e^g) Q - P W,  Nc_bot = P U~
@@ -15,19 +17,20 @@
 //     with W = T Diag(eta e^{g_-}) X, U~ = T Diag(eta) V, T = (I + A)^{-1}.
 //     tcgen05 MMAs (bf16 operands in shared memory, fp32 accumulators in TMEM)
 //     do the contractions:
-//        MMA1   [X; Q] X^T                 -> G = X X^T (lanes 0..63), Q X^T (64..127)
+//        MMA1   [K; Q] K^T (raw rows)      -> Gram of the write features, Q X^T
 //        MMA2   [Xh^T; Vh^T] T^T           -> [W^T; U~^T]
-//        MMA3   [Xt^T; 0] [W|U~] + [0; P] [W|U~] -> [Xt^T W | Xt^T U~ ; P W | P U~]
+//        MMA3   [Xt^T; P] [W | U~]         -> [Xt^T W | Xt^T U~ ; P W | P U~]
 //     The unit-lower solve runs in fp32 (diagonal 16 x 16 blocks) with warp
 //     MMAs for the off-diagonal block products.  The map goes to the workspace
-//     as two ready-to-use bf16 tiles (Mc swizzled as an MMA operand, Nc with
-//     rows swizzled at 16-byte granularity) plus e^{g_C}.
+//     as ready-to-use bf16 tiles (Mc swizzled as an MMA operand, Nc with rows
+//     swizzled at 16-byte granularity) plus e^{g_C}.
 //     Falcon-1A takes the same path with T = I and W = 0.
 //
-//  2. tc_chunk_scan_kernel -- one CTA per head, sequential over chunks: one
-//     M=128 tcgen05 MMA per chunk, [Mc_top; Mc_bot] S, with the maps of the
-//     next chunks prefetched by bulk copies.  The e^{g_C} S part of the state
-//     update stays in fp32 registers (only the correction goes through bf16
+//  2. tc_chunk_scan_kernel (m = 64) / tc_chunk_scan128_kernel (m = 128) --
+//     sequential over chunks, one CTA per head (per head and d_v slice for
+//     m = 128): per chunk the state MMA [Mc_top; Mc_bot] S, with the maps of
+//     the next chunks prefetched.  The e^{g_C} S part of the state update
+//     stays in fp32 registers (only the correction goes through bf16
 //     operands), so an undecayed state does not drift over long sequences.
 #include <cuda_bf16.h>
 
