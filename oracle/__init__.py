@@ -1,4 +1,4 @@
-"""fp64 CPU oracle for the Falcon-1 / Falcon-1A recurrences.
+"""fp64 CPU oracle for the Falcon-1 / Falcon-1A and Falcon-2 / Falcon-2A recurrences.
 
 TEST INFRASTRUCTURE ONLY.  Nothing in the library path imports this package:
 only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline legs of
@@ -27,7 +27,10 @@ _lib = None
 
 FALCON1 = 1  # regression rule (Section 3.1, Eq. (3.3))
 FALCON1A = 2  # inner-product rule (Section 4.3, Eq. (4.6))
+FALCON2 = 3  # per-column regression rule (Section 3.1, Section 4.2)
+FALCON2A = 4  # per-column inner-product rule (Section 4.3)
 _RULES = {"falcon1": FALCON1, "falcon1a": FALCON1A, FALCON1: FALCON1, FALCON1A: FALCON1A}
+_RULES2 = {"falcon2": FALCON2, "falcon2a": FALCON2A, FALCON2: FALCON2, FALCON2A: FALCON2A}
 _PHIS = {"identity": 0, "l2": 1}
 
 
@@ -54,6 +57,11 @@ def _load():
             lib.falcon_oracle_forward.argtypes = [
                 ctypes.c_int, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_double, ctypes.c_double, d, d, d, d, d, d, d, d, d, d, d,
+                ctypes.c_int]
+            lib.falcon2_oracle_forward.restype = ctypes.c_int
+            lib.falcon2_oracle_forward.argtypes = [
+                ctypes.c_int, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_double, ctypes.c_double, d, d, d, d, d, d, d, d, d, d,
                 ctypes.c_int]
             lib.falcon_oracle_decode_step.restype = ctypes.c_int
             lib.falcon_oracle_decode_step.argtypes = [
@@ -117,6 +125,37 @@ def forward(rule, q, k, v, beta, lam, S0=None, x_prev=None, phi="l2",
     if trajectory:
         out["S_traj"] = traj
     return out
+
+
+def forward2(rule, q, k, v, beta, lam, S0=None, x_prev=None, phi="l2",
+             eps=1e-6, eps_gamma=1e-6, threads=None):
+    """Falcon-2 / Falcon-2A over whole sequences: as ``forward`` except that
+    ``beta`` has one gain per value column, shape [..., T, dv], and ``rule`` is
+    "falcon2" or "falcon2a".  Returns a dict with o, S and x_last."""
+    lib = _load()
+    q, k, v, beta, lam = (_f64(t) for t in (q, k, v, beta, lam))
+    S0, x_prev = _f64(S0), _f64(x_prev)
+    lead = q.shape[:-2]
+    T, m = q.shape[-2], q.shape[-1]
+    dv = v.shape[-1]
+    BH = int(np.prod(lead)) if lead else 1
+    assert k.shape == q.shape and v.shape == lead + (T, dv)
+    assert beta.shape == lead + (T, dv) and lam.shape == lead + (T,)
+    if S0 is not None:
+        assert S0.shape == lead + (m, dv)
+    if x_prev is not None:
+        assert x_prev.shape == lead + (m,)
+    o = np.zeros(lead + (T, dv))
+    S = np.zeros(lead + (m, dv))
+    x_last = np.zeros(lead + (m,))
+    nthreads = threads or os.cpu_count() or 1
+    rc = lib.falcon2_oracle_forward(
+        _RULES2[rule], BH, T, m, dv, _PHIS[phi], eps, eps_gamma, _ptr(q), _ptr(k),
+        _ptr(v), _ptr(beta), _ptr(lam), _ptr(S0), _ptr(x_prev), _ptr(o), _ptr(S),
+        _ptr(x_last), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (rc={rc})")
+    return {"o": o, "S": S, "x_last": x_last}
 
 
 def decode_step(rule, q, k, v, beta, lam, S, x_prev, fresh=None, phi="l2",

@@ -28,6 +28,15 @@
  *   - one-step pseudocode with the same order of operations: page
  *     rcap.io/posts/fast-weight-attention-for-continual-learning-2026-08-27.
  *
+ *   - Falcon-2 (per-column step sizes eta_{j,t} = beta_{j,t} / (||x_t||^2 +
+ *     lambda_t + eps), S_t = S_{t-1}(I - lambda_t Diag(eta_t)) +
+ *     x_t (eta_t o r_t)^T): Section 3.1, the regression-family display and
+ *     the "Per-column NLMS step sizes" paragraph of Section 4.2;
+ *   - Falcon-2A (the same with r_t replaced by y_t = v_t, E_t = ||x_t||^2):
+ *     Section 4.3, "Falcon-2A: per-column inner-product write" and the
+ *     Falcon-1A/Falcon-2A step sizes; the clamp acts per column (the
+ *     effective ridge alpha_{j,t} / eta_{j,t} of the same paragraph).
+ *
  * Readings where the pages are silent:
  *   - phi is either the identity or the l2 normalisation u / max(||u||, 1e-12)
  *     ("QK-l2" in the experiment tables of page juhoplayground.github.io);
@@ -42,6 +51,8 @@
 
 #define ORACLE_FALCON1 1  /* regression rule, Eq. (3.3) */
 #define ORACLE_FALCON1A 2 /* inner-product rule, Eq. (4.6) */
+#define ORACLE_FALCON2 3  /* per-column regression rule (Section 3.1, 4.2) */
+#define ORACLE_FALCON2A 4 /* per-column inner-product rule (Section 4.3) */
 #define ORACLE_PHI_IDENTITY 0
 #define ORACLE_PHI_L2 1
 
@@ -231,5 +242,108 @@ int falcon_oracle_decode_step(int rule, int64_t N, int m, int dv, int phi,
   free(x);
   free(qf);
   free(r);
+  return 0;
+}
+
+/*
+ * Falcon-2 / Falcon-2A over whole sequences: every column j of S (one value
+ * channel) follows its own step size eta_{j,t} and decay gamma_{j,t} =
+ * 1 - min(eta_{j,t} lambda_t, 1 - eps_gamma); the write feature x_t, the
+ * ridge lambda_t and the read phi(q_t) are shared by the columns.
+ * Layouts as falcon_oracle_forward, except beta: [BH, T, dv] (one gain per
+ * column and token).  Returns 0, or -1 on a bad argument.
+ */
+typedef struct {
+  int rule, m, dv, phi;
+  int64_t T;
+  double eps, eps_gamma;
+  const double *q, *k, *v, *beta, *lambda, *S0, *x_prev;
+  double *o, *S_out, *x_last;
+} fwd2_args;
+
+static void forward2_head(const fwd2_args *a, int64_t bh) {
+  const int m = a->m, dv = a->dv;
+  const int64_t T = a->T;
+  double *S = (double *)calloc((size_t)m * dv, sizeof(double));
+  double *x = (double *)calloc((size_t)m, sizeof(double));
+  double *qf = (double *)malloc(sizeof(double) * (size_t)m);
+  if (a->S0) memcpy(S, a->S0 + bh * m * dv, sizeof(double) * (size_t)m * dv);
+  int sentinel = 1;
+  if (a->x_prev) {
+    memcpy(x, a->x_prev + bh * m, sizeof(double) * (size_t)m);
+    sentinel = 0;
+  }
+  for (int64_t t = 0; t < T; ++t) {
+    const int64_t row = bh * T + t;
+    const double lambda = a->lambda[row];
+    double E = 0.0;
+    for (int i = 0; i < m; ++i) E += x[i] * x[i];
+    const double den = E + lambda + a->eps;
+    feature_map(a->phi, m, a->q + row * m, qf);
+    for (int j = 0; j < dv; ++j) {
+      /* column j: its own eta_{j,t}, clamped decay, residual (or target) */
+      double eta = 0.0;
+      if (!(sentinel && t == 0) && den > 0.0) eta = a->beta[row * dv + j] / den;
+      double alpha = eta * lambda;
+      if (alpha > 1.0 - a->eps_gamma) alpha = 1.0 - a->eps_gamma;
+      const double gamma = 1.0 - alpha;
+      double r = a->v[row * dv + j];
+      if (a->rule == ORACLE_FALCON2) {
+        double pred = 0.0; /* S_{t-1}[:, j]^T x_t, before the update */
+        for (int i = 0; i < m; ++i) pred += S[(int64_t)i * dv + j] * x[i];
+        r -= pred;
+      }
+      double acc = 0.0;
+      for (int i = 0; i < m; ++i) {
+        double *s = &S[(int64_t)i * dv + j];
+        *s = gamma * *s + eta * x[i] * r;
+        acc += *s * qf[i]; /* read after write */
+      }
+      a->o[row * dv + j] = acc;
+    }
+    feature_map(a->phi, m, a->k + row * m, x);
+  }
+  if (a->S_out) memcpy(a->S_out + bh * m * dv, S, sizeof(double) * (size_t)m * dv);
+  if (a->x_last) memcpy(a->x_last + bh * m, x, sizeof(double) * (size_t)m);
+  free(S);
+  free(x);
+  free(qf);
+}
+
+typedef struct {
+  const fwd2_args *a;
+  int64_t begin, end;
+} fwd2_slice;
+
+static void *forward2_worker(void *p) {
+  const fwd2_slice *s = (const fwd2_slice *)p;
+  for (int64_t bh = s->begin; bh < s->end; ++bh) forward2_head(s->a, bh);
+  return NULL;
+}
+
+int falcon2_oracle_forward(int rule, int64_t BH, int64_t T, int m, int dv, int phi,
+                           double eps, double eps_gamma, const double *q,
+                           const double *k, const double *v, const double *beta,
+                           const double *lambda, const double *S0,
+                           const double *x_prev, double *o, double *S_out,
+                           double *x_last, int nthreads) {
+  if (rule != ORACLE_FALCON2 && rule != ORACLE_FALCON2A) return -1;
+  if (BH < 0 || T < 0 || m <= 0 || dv <= 0) return -1;
+  fwd2_args a = {rule, m, dv, phi, T, eps, eps_gamma, q, k, v, beta, lambda,
+                 S0, x_prev, o, S_out, x_last};
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > BH) nthreads = (int)(BH > 0 ? BH : 1);
+  pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+  fwd2_slice *sl = (fwd2_slice *)malloc(sizeof(fwd2_slice) * (size_t)nthreads);
+  for (int w = 0; w < nthreads; ++w) {
+    sl[w].a = &a;
+    sl[w].begin = BH * w / nthreads;
+    sl[w].end = BH * (w + 1) / nthreads;
+  }
+  for (int w = 1; w < nthreads; ++w) pthread_create(&tid[w], NULL, forward2_worker, &sl[w]);
+  forward2_worker(&sl[0]);
+  for (int w = 1; w < nthreads; ++w) pthread_join(tid[w], NULL);
+  free(tid);
+  free(sl);
   return 0;
 }
