@@ -86,11 +86,13 @@ def profiled_traffic():
 
 
 def algorithmic_bytes(w, with_S0=False):
-    """Bytes one chunked-forward call must move: q, k, v read, beta, lambda
-    read, o written, S_T (and x_last) written, S0 read if given."""
+    """Bytes one forward call must move: q, k, v read, beta, lambda read (beta
+    per value column for Falcon-2/2A), o written, S_T (and x_last) written, S0
+    read if given."""
     es = torch.finfo(w.dtype).bits // 8
     BH = w.B * w.H
-    b = BH * w.T * (2 * w.m + w.dv) * es + BH * w.T * 8 + BH * w.T * w.dv * es
+    gains = 4 * w.dv if w.per_column else 4  # beta per value column (Falcon-2/2A) or per token
+    b = BH * w.T * (2 * w.m + w.dv) * es + BH * w.T * (gains + 4) + BH * w.T * w.dv * es
     b += BH * w.m * w.dv * 4 + BH * w.m * 4
     if with_S0:
         b += BH * w.m * w.dv * 4
@@ -372,18 +374,27 @@ def extra_workloads(falcon, dev):
     """The other workloads, timed the same way (device-resident inputs)."""
     out = []
     pk = peaks()
-    for w, steps in ((workloads.LM_1A, 200), (workloads.LONG, 5)):
-        sets = input_sets(w, 2 if w is workloads.LM_1A else 1, dev)
-        fn = falcon.falcon1_fwd_chunked if w.rule == "falcon1" else falcon.falcon1a_fwd_chunked
+    for w, steps in ((workloads.LM_1A, 200), (workloads.LONG, 5), (workloads.LM_2, 20),
+                     (workloads.LM_2A, 20)):
+        sets = input_sets(w, 1 if w is workloads.LONG else 2, dev)
         o = torch.empty((w.B, w.H, w.T, w.dv), dtype=w.dtype, device=dev)
         S = torch.empty((w.B, w.H, w.m, w.dv), dtype=torch.float32, device=dev)
-        shape = falcon.make_shape(w.B, w.H, w.T, w.m, w.dv, w.chunk, w.dtype, w.phi)
-        wsb = torch.empty(max(falcon.falcon_workspace_bytes(shape), 1), dtype=torch.uint8,
-                          device=dev)
+        if w.per_column:
+            fn2 = {"falcon2": falcon.falcon2_fwd_recurrent,
+                   "falcon2a": falcon.falcon2a_fwd_recurrent}[w.rule]
 
-        def step(x):
-            fn(x["q"], x["k"], x["v"], x["beta"], x["lambda"], chunk=w.chunk, phi=w.phi,
-               o=o, S_out=S, workspace=wsb, want_x_last=False)
+            def step(x):
+                fn2(x["q"], x["k"], x["v"], x["beta"], x["lambda"], phi=w.phi, o=o, S_out=S,
+                    want_x_last=False)
+        else:
+            fn = falcon.falcon1_fwd_chunked if w.rule == "falcon1" else falcon.falcon1a_fwd_chunked
+            shape = falcon.make_shape(w.B, w.H, w.T, w.m, w.dv, w.chunk, w.dtype, w.phi)
+            wsb = torch.empty(max(falcon.falcon_workspace_bytes(shape), 1), dtype=torch.uint8,
+                              device=dev)
+
+            def step(x):
+                fn(x["q"], x["k"], x["v"], x["beta"], x["lambda"], chunk=w.chunk, phi=w.phi,
+                   o=o, S_out=S, workspace=wsb, want_x_last=False)
         secs = time_device(step, sets, steps, 2, 1)
         b = algorithmic_bytes(w)
         out.append({"workload": w.name, "tokens_per_s": w.tokens * steps / secs,
@@ -489,13 +500,20 @@ def run_profile(args):
                                        phi=d.phi, o=o)
         name, size = d.name, d.N
     else:
-        w = {"lm": workloads.LM, "lm1a": workloads.LM_1A, "long": workloads.LONG}[args.profile]
+        w = {"lm": workloads.LM, "lm1a": workloads.LM_1A, "long": workloads.LONG,
+             "lm2": workloads.LM_2, "lm2a": workloads.LM_2A}[args.profile]
         if args.profile_size:
             w = dataclasses.replace(w, T=args.profile_size)
         x = workloads.generate(w, device=dev)
-        fn = falcon.falcon1_fwd_chunked if w.rule == "falcon1" else falcon.falcon1a_fwd_chunked
         for _ in range(calls):
-            fn(x["q"], x["k"], x["v"], x["beta"], x["lambda"], chunk=w.chunk, phi=w.phi)
+            if w.per_column:
+                fn2 = (falcon.falcon2_fwd_recurrent if w.rule == "falcon2"
+                       else falcon.falcon2a_fwd_recurrent)
+                fn2(x["q"], x["k"], x["v"], x["beta"], x["lambda"], phi=w.phi)
+            else:
+                fn = (falcon.falcon1_fwd_chunked if w.rule == "falcon1"
+                      else falcon.falcon1a_fwd_chunked)
+                fn(x["q"], x["k"], x["v"], x["beta"], x["lambda"], chunk=w.chunk, phi=w.phi)
         name, size = w.name, w.T
     torch.cuda.synchronize()
     assert falcon.falcon_sync_check() == 0
@@ -511,7 +529,8 @@ def main():
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
-    ap.add_argument("--profile", choices=["lm", "lm1a", "long", "decode"], default=None,
+    ap.add_argument("--profile", choices=["lm", "lm1a", "long", "decode", "lm2", "lm2a"],
+                    default=None,
                     help="profiler target: run --steps calls of one workload, print no timing")
     ap.add_argument("--profile-size", type=int, default=None,
                     help="with --profile: tokens per head (chunked) or states (decode)")

@@ -32,7 +32,7 @@ EXPORTS = (
     "falcon_workspace_bytes", "falcon1_fwd_chunked", "falcon1a_fwd_chunked",
     "falcon1_decode_step", "falcon1a_decode_step", "falcon_sync_check",
     "falcon_strerror", "falcon_version", "falcon1_fwd_chunked_fixed_scratch",
-    "falcon_selftest_wait_timeout",
+    "falcon_selftest_wait_timeout", "falcon2_fwd_recurrent", "falcon2a_fwd_recurrent",
 )
 FALCON_ERR_SCRATCH_LIMIT = -10
 FALCON_FIXED_SCRATCH_BYTES = 16 * 1024 * 1024
@@ -81,6 +81,10 @@ def load_library(path: str | None = None):
             fn.restype = ctypes.c_int
             fn.argtypes = [i64, i32, i32, i32, i32, ctypes.c_float, ctypes.c_float,
                            vp, vp, vp, f32p, f32p, f32p, f32p, vp, vp, vp]
+        for name in ("falcon2_fwd_recurrent", "falcon2a_fwd_recurrent"):
+            fn = getattr(lib, name)
+            fn.restype = ctypes.c_int
+            fn.argtypes = [shp, vp, vp, vp, f32p, f32p, f32p, f32p, vp, f32p, f32p, vp]
         lib.falcon1_fwd_chunked_fixed_scratch.restype = ctypes.c_int
         lib.falcon1_fwd_chunked_fixed_scratch.argtypes = [shp, vp, vp, vp, f32p, f32p, f32p,
                                                           f32p, vp, f32p, f32p, vp]
@@ -231,6 +235,55 @@ def falcon1a_fwd_chunked(q, k, v, beta, lam, S0=None, x_prev=None, chunk=64, phi
     """Falcon-1A chunk-parallel forward; arguments as falcon1_fwd_chunked."""
     return _fwd("falcon1a_fwd_chunked", q, k, v, beta, lam, S0, x_prev, chunk, phi, eps,
                 eps_gamma, **kw)
+
+
+def _fwd2(name, q, k, v, beta, lam, S0=None, x_prev=None, phi="l2", eps=1e-6,
+          eps_gamma=1e-6, o=None, S_out=None, x_last=None, stream=None, want_x_last=True):
+    lib = load_library()
+    _need(q, "q")
+    B, H, T, m = q.shape
+    dv = v.shape[-1]
+    dt = q.dtype
+    if dt not in _DTYPE:
+        raise TypeError("q, k, v must be bfloat16 or float32")
+    _need(k, "k", dt, (B, H, T, m))
+    _need(v, "v", dt, (B, H, T, dv))
+    _need(beta, "beta", torch.float32, (B, H, T, dv))
+    _need(lam, "lambda", torch.float32, (B, H, T))
+    if S0 is not None:
+        _need(S0, "S0", torch.float32, (B, H, m, dv))
+    if x_prev is not None:
+        _need(x_prev, "x_prev", torch.float32, (B, H, m))
+    dev = q.device
+    if o is None:
+        o = torch.empty((B, H, T, dv), dtype=dt, device=dev)
+    if S_out is None:
+        S_out = torch.empty((B, H, m, dv), dtype=torch.float32, device=dev)
+    if x_last is None and want_x_last:
+        x_last = torch.empty((B, H, m), dtype=torch.float32, device=dev)
+    shape = make_shape(B, H, T, m, dv, 64, dt, phi, eps, eps_gamma)
+    rc = getattr(lib, name)(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+                            _ptr(lam), _ptr(S0), _ptr(x_prev), _ptr(o), _ptr(S_out),
+                            _ptr(x_last), _stream(stream))
+    _check(rc, name)
+    return o, S_out, x_last
+
+
+def falcon2_fwd_recurrent(q, k, v, beta, lam, S0=None, x_prev=None, phi="l2", eps=1e-6,
+                          eps_gamma=1e-6, **kw):
+    """Falcon-2 forward (per-column step sizes), token-recurrent.  As
+    falcon1_fwd_chunked except beta [B,H,T,dv] fp32 (one gain per value column)
+    and no chunk or workspace.  Returns (o, S_T, x_last)."""
+    return _fwd2("falcon2_fwd_recurrent", q, k, v, beta, lam, S0, x_prev, phi, eps, eps_gamma,
+                 **kw)
+
+
+def falcon2a_fwd_recurrent(q, k, v, beta, lam, S0=None, x_prev=None, phi="l2", eps=1e-6,
+                           eps_gamma=1e-6, **kw):
+    """Falcon-2A forward (per-column inner-product rule); arguments as
+    falcon2_fwd_recurrent."""
+    return _fwd2("falcon2a_fwd_recurrent", q, k, v, beta, lam, S0, x_prev, phi, eps, eps_gamma,
+                 **kw)
 
 
 def _decode(name, q, k, v, beta, lam, S, x_prev, fresh=None, phi="l2", eps=1e-6,

@@ -85,7 +85,9 @@ int fwd_chunked(int rule, const falcon_shape* s, const void* q, const void* k, c
   const void* ptrs[] = {q, k, v, beta, lambda, S0, x_prev, o, S_out, x_last};
   for (const void* p : ptrs)
     if (misaligned(p)) return FALCON_ERR_MISALIGNED;
-  const size_t need = falcon_workspace_bytes(s);
+  // The per-column rules run in the token-recurrent form: no workspace.
+  const bool per_column = rule == falcon::kFalcon2 || rule == falcon::kFalcon2A;
+  const size_t need = per_column ? 0 : falcon_workspace_bytes(s);
   if (need > 0 && (!workspace || workspace_bytes < need)) return FALCON_ERR_WORKSPACE;
   if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return FALCON_ERR_MISALIGNED;
   rc = check_device();
@@ -125,6 +127,11 @@ int fwd_chunked(int rule, const falcon_shape* s, const void* q, const void* k, c
   a.S_out = S_out;
   a.x_last = x_last;
   a.workspace = workspace;
+  if (per_column) {
+    int* err = device_error_word();
+    if (!err) return FALCON_ERR_CUDA;
+    return to_status(falcon::launch_falcon2_recurrent(a, err, stream));
+  }
   if (falcon::tc_path_applies(s->dtype, s->m, s->dv, s->chunk, s->B * s->H, s->T)) {
     int* err = device_error_word();
     if (!err) return FALCON_ERR_CUDA;
@@ -208,6 +215,22 @@ int falcon1a_fwd_chunked(const falcon_shape* s, const void* q, const void* k, co
                          void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   return fwd_chunked(falcon::kFalcon1A, s, q, k, v, beta, lambda, S0, x_prev, o, S_out, x_last,
                      workspace, workspace_bytes, stream);
+}
+
+int falcon2_fwd_recurrent(const falcon_shape* s, const void* q, const void* k, const void* v,
+                          const float* beta, const float* lambda, const float* S0,
+                          const float* x_prev, void* o, float* S_out, float* x_last,
+                          cudaStream_t stream) {
+  return fwd_chunked(falcon::kFalcon2, s, q, k, v, beta, lambda, S0, x_prev, o, S_out, x_last,
+                     nullptr, 0, stream);
+}
+
+int falcon2a_fwd_recurrent(const falcon_shape* s, const void* q, const void* k, const void* v,
+                           const float* beta, const float* lambda, const float* S0,
+                           const float* x_prev, void* o, float* S_out, float* x_last,
+                           cudaStream_t stream) {
+  return fwd_chunked(falcon::kFalcon2A, s, q, k, v, beta, lambda, S0, x_prev, o, S_out, x_last,
+                     nullptr, 0, stream);
 }
 
 int falcon1_decode_step(int64_t N, int32_t m, int32_t dv, int32_t dtype, int32_t phi, float eps,

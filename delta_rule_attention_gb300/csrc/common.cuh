@@ -10,8 +10,9 @@
 namespace falcon {
 
 // Rule selector shared by kernels: Falcon-1 writes the residual
-// r_t = v_t - S_{t-1}^T x_t, Falcon-1A writes the target v_t.
-enum Rule : int { kFalcon1 = 1, kFalcon1A = 2 };
+// r_t = v_t - S_{t-1}^T x_t, Falcon-1A writes the target v_t; Falcon-2 and
+// Falcon-2A are their per-column counterparts (one step size per column).
+enum Rule : int { kFalcon1 = 1, kFalcon1A = 2, kFalcon2 = 3, kFalcon2A = 4 };
 
 __device__ __forceinline__ float load_elem(const void* p, int64_t i, int dtype) {
   if (dtype == FALCON_BF16)
@@ -72,6 +73,10 @@ struct ChunkArgs {
 };
 size_t generic_workspace_bytes(int64_t BH, int64_t T, int m, int dv, int C);
 cudaError_t launch_generic_chunked(const ChunkArgs& a, cudaStream_t stream);
+
+// Falcon-2 / Falcon-2A, token-recurrent form (rule kFalcon2 or kFalcon2A;
+// beta is [B*H, T, dv]: one gain per column and token).
+cudaError_t launch_falcon2_recurrent(const ChunkArgs& a, int* err, cudaStream_t stream);
 
 // Tensor-core path (bf16, m = dv in {64, 128}, chunk = 64).
 bool tc_path_applies(int dtype, int m, int dv, int C, int64_t BH, int64_t T);

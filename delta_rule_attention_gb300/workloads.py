@@ -1,6 +1,6 @@
 """Seeded synthetic workloads (inputs only; none of the method's arithmetic).
 
-The five workloads are shaped like the 124M-130M-parameter language-model
+The workloads are shaped like the 124M-130M-parameter language-model
 layers of the experiments on the pages (heads of width 64, about 12 heads,
 sequence 1024-2048) plus a long-context stress case and a batched decode.
 The pages train on FineWeb-Edu and evaluate on lm-eval tasks and a digit-
@@ -12,8 +12,10 @@ N(0, 1), and the gain and ridge are fixed transforms of N(0, 1) draws:
 
 Draw order for one workload: q, k, v, then the beta normals, then the lambda
 normals, all in float32 row-major [B, H, T, .] from one torch.Generator seeded
-with the workload's seed; q, k, v are then rounded to the workload dtype.
-Workloads small enough for the host (tiny, lm, lm-1A) draw on the CPU
+with the workload's seed; q, k, v are then rounded to the workload dtype.  The
+per-column workloads (Falcon-2, Falcon-2A) draw one beta normal per value
+column, [B, H, T, d_v], in the same place of the order.
+Workloads small enough for the host (tiny, lm, lm-1A, lm-2, lm-2A) draw on the CPU
 generator, so they are the same on every machine; the long-context and decode
 workloads (hundreds of millions of draws) draw on the device's generator.
 """
@@ -42,6 +44,7 @@ class Workload:
     host_rng: bool = True
     eps: float = 1e-6
     eps_gamma: float = 1e-6
+    per_column: bool = False  # Falcon-2/2A: one gain per value column, beta [B, H, T, dv]
 
     @property
     def tokens(self) -> int:
@@ -56,7 +59,12 @@ LM_1A = Workload("falcon1a_lm_B8H12T2048_d64_bf16", "falcon1a", 8, 12, 2048, 64,
                  torch.bfloat16, "l2", 64, -3.0, 2)
 LONG = Workload("falcon1_long_B1H16T65536_d128_bf16", "falcon1", 1, 16, 65536, 128, 128,
                 torch.bfloat16, "l2", 64, 1.0, 3, host_rng=False)
-WORKLOADS = {w.name: w for w in (TINY, LM, LM_1A, LONG)}
+# Falcon-2 / Falcon-2A (per-column step sizes) on the lm shape.
+LM_2 = Workload("falcon2_lm_B8H12T2048_d64_bf16", "falcon2", 8, 12, 2048, 64, 64, torch.bfloat16,
+                "l2", 64, -3.0, 5, per_column=True)
+LM_2A = Workload("falcon2a_lm_B8H12T2048_d64_bf16", "falcon2a", 8, 12, 2048, 64, 64,
+                 torch.bfloat16, "l2", 64, -3.0, 6, per_column=True)
+WORKLOADS = {w.name: w for w in (TINY, LM, LM_1A, LONG, LM_2, LM_2A)}
 
 
 @dataclass(frozen=True)
@@ -97,7 +105,7 @@ def generate(w: Workload, device="cpu"):
     q = torch.randn((B, H, T, m), generator=g, device=gen_dev)
     k = torch.randn((B, H, T, m), generator=g, device=gen_dev)
     v = torch.randn((B, H, T, dv), generator=g, device=gen_dev)
-    nb = torch.randn((B, H, T), generator=g, device=gen_dev)
+    nb = torch.randn((B, H, T, dv) if w.per_column else (B, H, T), generator=g, device=gen_dev)
     nl = torch.randn((B, H, T), generator=g, device=gen_dev)
     beta, lam = gain_and_ridge(nb, nl, w.lam_shift)
     if w.lambda_first_zero and T > 0:
@@ -108,13 +116,15 @@ def generate(w: Workload, device="cpu"):
 
 
 def random_case(B, H, T, m, dv, dtype=torch.float32, seed=0, lam_shift=-2.0, device="cpu",
-                with_state=False, with_x_prev=False):
-    """Small seeded case for parity tests of arbitrary shape (CPU generator)."""
+                with_state=False, with_x_prev=False, per_column=False):
+    """Small seeded case for parity tests of arbitrary shape (CPU generator);
+    per_column draws one gain per value column (beta [B, H, T, dv])."""
     g = torch.Generator().manual_seed(seed)
     q = torch.randn((B, H, T, m), generator=g)
     k = torch.randn((B, H, T, m), generator=g)
     v = torch.randn((B, H, T, dv), generator=g)
-    beta, lam = gain_and_ridge(torch.randn((B, H, T), generator=g),
+    beta, lam = gain_and_ridge(torch.randn((B, H, T, dv) if per_column else (B, H, T),
+                                           generator=g),
                                torch.randn((B, H, T), generator=g), lam_shift)
     out = {"q": q.to(dtype), "k": k.to(dtype), "v": v.to(dtype), "beta": beta, "lambda": lam}
     if with_state:

@@ -1,7 +1,8 @@
 /*
  * falcon.h -- C ABI of the GB300 (sm_103a) Falcon fast-weight attention
- * library: chunk-parallel forward of Falcon-1 and Falcon-1A, and the
- * single-token recurrent decode step.
+ * library: chunk-parallel forward of Falcon-1 and Falcon-1A, the
+ * token-recurrent forward of Falcon-2 and Falcon-2A (per-column step sizes),
+ * and the single-token recurrent decode step.
  *
  * The operations are defined on the page hyper.ai/fr/papers/2608.27763
  * ("Fast Weight Attention for Continual Learning"):
@@ -157,6 +158,36 @@ int falcon1a_fwd_chunked(const falcon_shape *shape, const void *q,
                          const float *x_prev, void *o, float *S_out,
                          float *x_last, void *workspace, size_t workspace_bytes,
                          cudaStream_t stream);
+
+/* Falcon-2 forward (per-column step sizes), token-recurrent form: every
+ * column j of the state follows its own step size and clamped decay,
+ *   eta_{j,t} = beta_{j,t} / (||x_t||^2 + lambda_t + eps)  (0 at the sentinel
+ *   and when the denominator is 0), gamma_{j,t} = 1 - min(eta_{j,t} lambda_t,
+ *   1 - eps_gamma), S_t[:, j] = gamma_{j,t} S_{t-1}[:, j] + eta_{j,t} x_t r_{t,j},
+ *   r_t = v_t - S_{t-1}^T x_t,  o_t = S_t^T phi(q_t);
+ * page hyper.ai/fr/papers/2608.27763, the regression-family display of
+ * Section 3.1 and the per-column NLMS step sizes of Section 4.2.
+ * Arguments, layouts, ownership and errors are those of falcon1_fwd_chunked
+ * except:
+ *   beta    [B,H,T,dv] f32: one gain per value column and token
+ *   shape->chunk is checked (16, 32 or 64) but not used: the call runs the
+ *           recurrence token by token, and needs no workspace.
+ * One CTA per head and 32 value columns runs the tokens in order; the state
+ * stays in registers. */
+int falcon2_fwd_recurrent(const falcon_shape *shape, const void *q,
+                          const void *k, const void *v, const float *beta,
+                          const float *lambda, const float *S0,
+                          const float *x_prev, void *o, float *S_out,
+                          float *x_last, cudaStream_t stream);
+
+/* Falcon-2A, the per-column inner-product rule (Section 4.3, "Falcon-2A:
+ * per-column inner-product write"): as falcon2_fwd_recurrent with r_t
+ * replaced by v_t and E_t = ||x_t||^2 in the step size. */
+int falcon2a_fwd_recurrent(const falcon_shape *shape, const void *q,
+                           const void *k, const void *v, const float *beta,
+                           const float *lambda, const float *S0,
+                           const float *x_prev, void *o, float *S_out,
+                           float *x_last, cudaStream_t stream);
 
 /* One recurrent token (read after write) for N independent states: the
  * Falcon-1 update of Section 3.1 Eq. (3.3), as in the one-step listing of page
