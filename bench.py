@@ -57,15 +57,20 @@ def peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
+# The sources that define the headline path's two kernels (the tensor-core
+# map and scan launches): profiled counters are tied to them.
+TC_PATH_SOURCES = ("chunk_tc.cu", "tc_ptx.cuh", "tmap.cu", "tmap.cuh", "common.cuh")
+
+
 def kernel_sources_digest():
-    """sha256 over the CUDA sources (sorted), to tie profiled counters to them."""
-    import glob
+    """sha256 over the headline path's CUDA sources, to tie profiled counters
+    to them."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "delta_rule_attention_gb300", "csrc")
-    for f in sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh"))):
-        h.update(os.path.basename(f).encode())
-        h.update(open(f, "rb").read())
+    for name in TC_PATH_SOURCES:
+        h.update(name.encode())
+        h.update(open(os.path.join(csrc, name), "rb").read())
     return h.hexdigest()
 
 
