@@ -34,6 +34,8 @@
 //     operands), so an undecayed state does not drift over long sequences.
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "tc_ptx.cuh"
 #include "tmap.cuh"
@@ -294,7 +296,7 @@ __device__ void solve_unit_lower(const float* As, float* Ts, float* Rs) {
 // columns 32h .. 32h+31 (h = t >> 7) of the CTA's 64-column half j.
 template <int M>
 __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
-    tc_chunk_map_kernel(ChunkArgs a, int nchunks, int* err,
+    tc_chunk_map_kernel(ChunkArgs a, int nchunks, int c_begin, int* err,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_v) {
@@ -315,7 +317,7 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
   unsigned char* const xt_tile = kt;    // MN-major A of MMA3a, atom 0
   unsigned char* const zero_tile = qt;  // m = 64: atom 1 of MMA3a; rows 0..63 of MMA3b
 
-  const int c = blockIdx.x / L::kHalves;
+  const int c = c_begin + (int)(blockIdx.x / L::kHalves);
   const int j = blockIdx.x % L::kHalves;  // column half of this CTA
   const int64_t bh = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -703,7 +705,8 @@ __device__ __forceinline__ void add_bf16x16(float* d, uint4 p0, uint4 p1) {
 }
 
 __global__ void __launch_bounds__(kScanThreads)
-    tc_chunk_scan_kernel(ChunkArgs a, int nchunks, int* err, const __grid_constant__ CUtensorMap tm_o) {
+    tc_chunk_scan_kernel(ChunkArgs a, int nchunks, int c_begin, int n, const float* S_in, int* err,
+                         const __grid_constant__ CUtensorMap tm_o) {
   extern __shared__ unsigned char smem_raw[];
   ScanSmem& s = *reinterpret_cast<ScanSmem*>(align1024(smem_raw));
   volatile int* fail = &s.fail;
@@ -717,7 +720,7 @@ __global__ void __launch_bounds__(kScanThreads)
   const uint32_t ch0 = (uint32_t)(((2 * qc) ^ (row & 7)) << 4);
   const uint32_t ch1 = (uint32_t)(((2 * qc + 1) ^ (row & 7)) << 4);
   const unsigned char* ws = reinterpret_cast<const unsigned char*>(a.workspace) +
-                            (size_t)bh * nchunks * kMapBytes;
+                            ((size_t)bh * nchunks + c_begin) * kMapBytes;  // this range's maps
   if (warp == 0) tmem_alloc(&s.tmem_base, 128);
   if (tid == 0) {
     for (int st = 0; st < kStages; ++st) {
@@ -736,7 +739,7 @@ __global__ void __launch_bounds__(kScanThreads)
   float S[16];
   if (srow) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) S[j] = a.S0 ? a.S0[(bh * 64 + row) * 64 + 16 * qc + j] : 0.f;
+    for (int j = 0; j < 16; ++j) S[j] = S_in ? S_in[(bh * 64 + row) * 64 + 16 * qc + j] : 0.f;
   }
   tc_fence_before();
   __syncthreads();
@@ -747,11 +750,11 @@ __global__ void __launch_bounds__(kScanThreads)
 
   if (issuer) {
     if (lane == 0) {
-      for (int st = 0; st < kStages && st < nchunks; ++st)
+      for (int st = 0; st < kStages && st < n; ++st)
         issue_map_load(s, st, ws + (size_t)st * kMapBytes);
       const uint64_t bdesc = sw128_desc(smem_addr(s.sop), 8192, 1024);
       const uint32_t idesc = idesc_bf16(128, 64, false, true);
-      for (int c = 0; c < nchunks; ++c) {
+      for (int c = 0; c < n; ++c) {
         const int st = c % kStages, b = c & 1;
         // The state operand is the last to be ready: wait for it last.
         bool ok = c < 2 || mbar_wait(&s.o_done[b], (uint32_t)((c - 2) >> 1) & 1u);
@@ -767,7 +770,7 @@ __global__ void __launch_bounds__(kScanThreads)
         mma_commit(&s.mma_done[b]);
         // Refill the stage of chunk c - 1 once every math warp is done with it.
         const int cp = c - 1;
-        if (cp >= 0 && cp + kStages < nchunks) {
+        if (cp >= 0 && cp + kStages < n) {
           const int sp = cp % kStages;
           if (!mbar_wait(&s.empty[sp], (uint32_t)(cp / kStages) & 1u)) {
             *fail = 1;
@@ -786,7 +789,7 @@ __global__ void __launch_bounds__(kScanThreads)
     fence_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&s.s_ready);
-    for (int c = 0; c < nchunks; ++c) {
+    for (int c = 0; c < n; ++c) {
       // Exits are warp-uniform, so every __syncwarp sees all lanes.
       if (__any_sync(0xffffffffu, *fail)) break;
       const int st = c % kStages, b = c & 1;
@@ -827,7 +830,7 @@ __global__ void __launch_bounds__(kScanThreads)
     const uint32_t tlane = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 16 * qc;
     const bool o_issuer = warp == 2 && lane == 0;
     constexpr int kOutThreads = 32 * kScanMathWarps / 2;
-    for (int c = 0; c < nchunks; ++c) {
+    for (int c = 0; c < n; ++c) {
       const int st = c % kStages, b = c & 1;
       bool ok = !*fail && mbar_wait(&s.full[st], (uint32_t)(c / kStages) & 1u);
       uint4 n0 = make_uint4(0u, 0u, 0u, 0u), n1 = n0;
@@ -859,7 +862,7 @@ __global__ void __launch_bounds__(kScanThreads)
       fence_async_smem();
       named_sync(1, kOutThreads);
       if (o_issuer) {
-        tma_store_3d(&tm_o, s.ostage[b], 0, c * kC, (int)bh);
+        tma_store_3d(&tm_o, s.ostage[b], 0, (c_begin + c) * kC, (int)bh);
         bulk_commit();
       }
     }
@@ -926,7 +929,8 @@ __device__ __forceinline__ uint4 ld_map16(const unsigned char* p) {
 }
 
 __global__ void __launch_bounds__(kScan128Threads)
-    tc_chunk_scan128_kernel(ChunkArgs a, int nchunks, int* err,
+    tc_chunk_scan128_kernel(ChunkArgs a, int nchunks, int c_begin, int n, const float* S_in,
+                            int* err,
                             const __grid_constant__ CUtensorMap tm_o) {
   constexpr uint32_t kA = MapLayout<128>::kMcAtom;
   constexpr uint32_t kMap = MapLayout<128>::kMapBytes;
@@ -942,7 +946,7 @@ __global__ void __launch_bounds__(kScan128Threads)
   const bool owarp = warp == 16 || warp == 17 || warp == 20 || warp == 21;
   const int row = 32 * (warp & 3) + lane;  // TMEM lane
   const unsigned char* ws = reinterpret_cast<const unsigned char*>(a.workspace) +
-                            (size_t)bh * nchunks * kMap;
+                            ((size_t)bh * nchunks + c_begin) * kMap;  // this range's maps
   if (warp == 0) tmem_alloc(&s.tmem_base, 256);
   if (tid == 0) {
     for (int st = 0; st < kStages128; ++st) {
@@ -962,7 +966,7 @@ __global__ void __launch_bounds__(kScan128Threads)
   const int qc = (warp >> 2) & 3;  // state warps: column quarter
   float S[16];
   if (swarp) {
-    const float* src = a.S0 ? a.S0 + (bh * 128 + row) * 128 + 64 * j + 16 * qc : nullptr;
+    const float* src = S_in ? S_in + (bh * 128 + row) * 128 + 64 * j + 16 * qc : nullptr;
 #pragma unroll
     for (int i = 0; i < 16; ++i) S[i] = src ? src[i] : 0.f;
   }
@@ -974,10 +978,10 @@ __global__ void __launch_bounds__(kScan128Threads)
 
   if (issuer) {
     if (lane == 0) {
-      for (int st = 0; st < kStages128 && st < nchunks; ++st)
+      for (int st = 0; st < kStages128 && st < n; ++st)
         issue_map_load128(s, st, ws + (size_t)st * kMap, j);
       const uint32_t idesc = idesc_bf16(128, 64, false, true);
-      for (int c = 0; c < nchunks; ++c) {
+      for (int c = 0; c < n; ++c) {
         const int st = c % kStages128, b = c & 1;
         bool ok = c < 2 || mbar_wait(&s.o_done[b], (uint32_t)((c - 2) >> 1) & 1u);
         ok = ok && mbar_wait(&s.full[st], (uint32_t)(c / kStages128) & 1u);
@@ -1001,7 +1005,7 @@ __global__ void __launch_bounds__(kScan128Threads)
                      idesc, true);
         mma_commit(&s.omma_done[b]);
         const int cp = c - 1;
-        if (cp >= 0 && cp + kStages128 < nchunks) {
+        if (cp >= 0 && cp + kStages128 < n) {
           const int sp = cp % kStages128;
           if (!mbar_wait(&s.empty[sp], (uint32_t)(cp / kStages128) & 1u)) {
             *fail = 1;
@@ -1024,7 +1028,7 @@ __global__ void __launch_bounds__(kScan128Threads)
     // Nc rows of this thread (state rows 0..127 of slice j), chunk 0 first.
     const unsigned char* ncg = ws + (2 + j) * kA + row * 128;
     uint4 n0 = ld_map16(ncg + ch0), n1 = ld_map16(ncg + ch1);
-    for (int c = 0; c < nchunks; ++c) {
+    for (int c = 0; c < n; ++c) {
       if (__any_sync(0xffffffffu, *fail)) break;
       const int st = c % kStages128, b = c & 1;
       // mma_done of chunk c also covers the MMAs of chunk c - 1 (issued
@@ -1036,7 +1040,7 @@ __global__ void __launch_bounds__(kScan128Threads)
       }
       const float gC = *reinterpret_cast<const float*>(s.stage[st] + 2 * kA);
       uint4 m0 = make_uint4(0u, 0u, 0u, 0u), m1 = m0;  // Nc of chunk c + 1
-      if (c + 1 < nchunks) {
+      if (c + 1 < n) {
         const unsigned char* nrow = ncg + (size_t)(c + 1) * kMap;
         m0 = ld_map16(nrow + ch0);
         m1 = ld_map16(nrow + ch1);
@@ -1080,11 +1084,11 @@ __global__ void __launch_bounds__(kScan128Threads)
     uint4 nq[4], mq[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) nq[q] = ld_map16(ncg + (((4 * oh + q) ^ (row & 7)) << 4));
-    for (int c = 0; c < nchunks; ++c) {
+    for (int c = 0; c < n; ++c) {
       const int st = c % kStages128, b = c & 1;
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        mq[q] = (c + 1 < nchunks)
+        mq[q] = (c + 1 < n)
                     ? ld_map16(ncg + (size_t)(c + 1) * kMap + (((4 * oh + q) ^ (row & 7)) << 4))
                     : make_uint4(0u, 0u, 0u, 0u);
       bool ok = !*fail && mbar_wait(&s.full[st], (uint32_t)(c / kStages128) & 1u);
@@ -1125,7 +1129,7 @@ __global__ void __launch_bounds__(kScan128Threads)
       fence_async_smem();
       named_sync(1, 32 * kOutWarps);
       if (o_issuer) {
-        tma_store_3d(&tm_o, s.ostage[b], 64 * j, c * kC, (int)bh);
+        tma_store_3d(&tm_o, s.ostage[b], 64 * j, (c_begin + c) * kC, (int)bh);
         bulk_commit();
       }
     }
@@ -1154,27 +1158,24 @@ size_t tc_workspace_bytes(int m, int64_t BH, int64_t T) {
 namespace {
 
 template <int M>
-cudaError_t launch_map(const ChunkArgs& a, int nchunks, int* err, cudaStream_t stream) {
+cudaError_t launch_map(const ChunkArgs& a, int nchunks, int c_begin, int n, int* err,
+                       const CUtensorMap& tm_k, const CUtensorMap& tm_q, const CUtensorMap& tm_v,
+                       cudaStream_t stream) {
   const size_t smem = map_smem_bytes<M>() + 1024;
   cudaError_t e = cudaFuncSetAttribute(tc_chunk_map_kernel<M>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  CUtensorMap tm_k, tm_q, tm_v;
-  if (!encode_rows_bf16(&tm_k, a.k, M, (uint64_t)a.T, (uint64_t)a.BH, 64, kC) ||
-      !encode_rows_bf16(&tm_q, a.q, M, (uint64_t)a.T, (uint64_t)a.BH, 64, kC) ||
-      !encode_rows_bf16(&tm_v, a.v, M, (uint64_t)a.T, (uint64_t)a.BH, 64, kC))
-    return cudaErrorInvalidValue;
-  tc_chunk_map_kernel<M><<<dim3(nchunks * MapLayout<M>::kHalves, (unsigned)a.BH), kMapThreads,
-                           smem, stream>>>(a, nchunks, err, tm_k, tm_q, tm_v);
+  tc_chunk_map_kernel<M><<<dim3(n * MapLayout<M>::kHalves, (unsigned)a.BH), kMapThreads, smem,
+                           stream>>>(a, nchunks, c_begin, err, tm_k, tm_q, tm_v);
   return cudaGetLastError();
 }
 
-// Programmatic dependent launch: the scan grid may be scheduled while the map
-// grid drains; griddepcontrol.wait in the scan orders it after every map write.
+// pdl: programmatic dependent launch after the preceding map launch on the
+// same stream (griddepcontrol.wait in the scan orders it after every map write).
 template <typename Kernel>
-cudaError_t launch_scan(Kernel kernel, unsigned grid, unsigned threads, size_t smem,
-                        const ChunkArgs& a, int nchunks, int* err, const CUtensorMap& tm_o,
-                        cudaStream_t stream) {
+cudaError_t launch_scan(Kernel kernel, unsigned grid, unsigned threads, size_t smem, bool pdl,
+                        const ChunkArgs& a, int nchunks, int c_begin, int n, const float* S_in,
+                        int* err, const CUtensorMap& tm_o, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
@@ -1187,26 +1188,108 @@ cudaError_t launch_scan(Kernel kernel, unsigned grid, unsigned threads, size_t s
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, a, nchunks, err, tm_o);
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, a, nchunks, c_begin, n, S_in, err, tm_o);
+}
+
+// Pieces of the chunk range: with few heads and many chunks the scan runs on
+// few SMs for a long time, so the call is cut into chunk ranges whose scans run
+// on a second stream while the maps of the next range run on the caller's
+// stream (event-ordered; no kernel waits on another).  With many heads the
+// scan already fills most SMs and a single range is kept (measured on the lm
+// shape: 1 range 118 us, 2 ranges 136 us; on the long shape, 1024 chunks of 16
+// heads: 1, 4, 8, 16, 32 ranges took 2.65, 2.18, 1.94, 1.90, 2.06 ms).
+int piece_count(int64_t BH, int nchunks, bool wide) {
+  const int64_t scan_ctas = BH * (wide ? 2 : 1);
+  if (scan_ctas > 64 || nchunks < 64) return 1;
+  return nchunks >= 512 ? 16 : (nchunks >= 256 ? 8 : 4);
+}
+
+constexpr int kMaxPieces = 16;
+constexpr int kMaxDevices = 64;
+
+// Per-device second stream and events (created once, on first use).
+struct PieceStreams {
+  cudaStream_t side = nullptr;
+  cudaEvent_t map_done[kMaxPieces] = {};
+  cudaEvent_t scans_done = nullptr;
+  bool ready = false;
+};
+std::mutex g_piece_mu;
+PieceStreams g_piece[kMaxDevices];
+
+cudaError_t piece_streams(PieceStreams** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  PieceStreams& ps = g_piece[dev];
+  if (!ps.ready) {
+    if ((e = cudaStreamCreateWithFlags(&ps.side, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    for (int i = 0; i < kMaxPieces; ++i)
+      if ((e = cudaEventCreateWithFlags(&ps.map_done[i], cudaEventDisableTiming)) != cudaSuccess)
+        return e;
+    if ((e = cudaEventCreateWithFlags(&ps.scans_done, cudaEventDisableTiming)) != cudaSuccess)
+      return e;
+    ps.ready = true;
+  }
+  *out = &ps;
+  return cudaSuccess;
+}
+
+template <int M>
+cudaError_t launch_scan_range(const ChunkArgs& a, int nchunks, int c_begin, int n,
+                              const float* S_in, bool pdl, int* err, const CUtensorMap& tm_o,
+                              cudaStream_t stream) {
+  if (M == 128)
+    return launch_scan(tc_chunk_scan128_kernel, (unsigned)(2 * a.BH), kScan128Threads,
+                       sizeof(Scan128Smem) + 1024, pdl, a, nchunks, c_begin, n, S_in, err, tm_o,
+                       stream);
+  return launch_scan(tc_chunk_scan_kernel, (unsigned)a.BH, kScanThreads, sizeof(ScanSmem) + 1024,
+                     pdl, a, nchunks, c_begin, n, S_in, err, tm_o, stream);
+}
+
+template <int M>
+cudaError_t launch_tc(const ChunkArgs& a, int* err, cudaStream_t stream) {
+  const int nchunks = (int)((a.T + kC - 1) / kC);
+  CUtensorMap tm_k, tm_q, tm_v, tm_o;
+  if (!encode_rows_bf16(&tm_k, a.k, M, (uint64_t)a.T, (uint64_t)a.BH, 64, kC) ||
+      !encode_rows_bf16(&tm_q, a.q, M, (uint64_t)a.T, (uint64_t)a.BH, 64, kC) ||
+      !encode_rows_bf16(&tm_v, a.v, M, (uint64_t)a.T, (uint64_t)a.BH, 64, kC) ||
+      !encode_rows_bf16(&tm_o, a.o, M, (uint64_t)a.T, (uint64_t)a.BH, 64, kC))
+    return cudaErrorInvalidValue;
+  const int pieces = piece_count(a.BH, nchunks, M == 128);
+  if (pieces == 1) {
+    cudaError_t e = launch_map<M>(a, nchunks, 0, nchunks, err, tm_k, tm_q, tm_v, stream);
+    if (e != cudaSuccess) return e;
+    return launch_scan_range<M>(a, nchunks, 0, nchunks, a.S0, true, err, tm_o, stream);
+  }
+  // The scans of consecutive ranges run in order on the side stream, each after
+  // its range's maps; the running state goes through S_out (S_out may alias
+  // S0: a scan reads its initial state before writing the same elements).
+  std::lock_guard<std::mutex> lock(g_piece_mu);
+  PieceStreams* ps = nullptr;
+  cudaError_t e = piece_streams(&ps);
+  if (e != cudaSuccess) return e;
+  for (int p = 0; p < pieces; ++p) {
+    const int c0 = (int)((int64_t)nchunks * p / pieces);
+    const int c1 = (int)((int64_t)nchunks * (p + 1) / pieces);
+    if ((e = launch_map<M>(a, nchunks, c0, c1 - c0, err, tm_k, tm_q, tm_v, stream)) != cudaSuccess)
+      return e;
+    if ((e = cudaEventRecord(ps->map_done[p], stream)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(ps->side, ps->map_done[p], 0)) != cudaSuccess) return e;
+    e = launch_scan_range<M>(a, nchunks, c0, c1 - c0, p == 0 ? a.S0 : a.S_out, false, err, tm_o,
+                             ps->side);
+    if (e != cudaSuccess) return e;
+  }
+  if ((e = cudaEventRecord(ps->scans_done, ps->side)) != cudaSuccess) return e;
+  return cudaStreamWaitEvent(stream, ps->scans_done, 0);
 }
 
 }  // namespace
 
 cudaError_t launch_tc_chunked(const ChunkArgs& a, int* err, cudaStream_t stream) {
-  const int nchunks = (int)((a.T + kC - 1) / kC);
-  const bool wide = a.m == 128;
-  cudaError_t e = wide ? launch_map<128>(a, nchunks, err, stream)
-                       : launch_map<64>(a, nchunks, err, stream);
-  if (e != cudaSuccess) return e;
-  CUtensorMap tm_o;
-  if (!encode_rows_bf16(&tm_o, a.o, a.m, (uint64_t)a.T, (uint64_t)a.BH, 64, kC))
-    return cudaErrorInvalidValue;
-  if (wide)
-    return launch_scan(tc_chunk_scan128_kernel, (unsigned)(2 * a.BH), kScan128Threads,
-                       sizeof(Scan128Smem) + 1024, a, nchunks, err, tm_o, stream);
-  return launch_scan(tc_chunk_scan_kernel, (unsigned)a.BH, kScanThreads, sizeof(ScanSmem) + 1024,
-                     a, nchunks, err, tm_o, stream);
+  return a.m == 128 ? launch_tc<128>(a, err, stream) : launch_tc<64>(a, err, stream);
 }
 
 }  // namespace falcon

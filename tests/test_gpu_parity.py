@@ -261,3 +261,24 @@ def test_zero_denominator_is_a_no_op(falcon):
     assert np.isfinite(o.numpy()).all()
     assert head_err(o, ref["o"]) < 1e-4
     assert head_err(S, ref["S"]) < 1e-4
+
+
+@pytest.mark.parametrize("rule", ["falcon1", "falcon1a"])
+@pytest.mark.parametrize("m", [64, 128])
+def test_chunk_range_pieces(falcon, rule, m):
+    """Few heads and many chunks: the call runs as chunk-range pieces (maps on
+    the caller's stream, scans on a second stream, the running state through
+    S_out).  Ragged tail, carried state and x_prev, and S_out aliasing S0."""
+    T = 64 * 64 + 17
+    x = workloads.random_case(1, 2, T, m, m, torch.bfloat16, seed=300 + m, device="cuda",
+                              with_state=True, with_x_prev=True)
+    ref = ref_of(rule, x, "l2")
+    S_alias = x["S0"].clone()
+    fn = falcon.falcon1_fwd_chunked if rule == "falcon1" else falcon.falcon1a_fwd_chunked
+    o, S, xl = fn(x["q"], x["k"], x["v"], x["beta"], x["lambda"], S0=S_alias,
+                  x_prev=x["x_prev"], chunk=64, phi="l2", S_out=S_alias)
+    assert falcon.falcon_sync_check() == 0
+    assert S.data_ptr() == S_alias.data_ptr()
+    assert head_err(o.float().cpu(), ref["o"]) < 2e-2
+    assert head_err(S.cpu(), ref["S"]) < 2e-2
+    np.testing.assert_allclose(xl.cpu().numpy(), ref["x_last"], rtol=1e-6, atol=1e-6)
