@@ -29,6 +29,11 @@
  *   - Every call is asynchronous on the caller's `stream` (0 = legacy default
  *     stream) and returns before the GPU work ends.  A nonzero return means
  *     nothing was launched (argument errors) or a launch failed (FALCON_ERR_CUDA).
+ *   - A chunked call with few heads and many chunks runs part of its work on a
+ *     second stream the library creates once per device (with its events):
+ *     the call forks from the caller's stream and joins back to it by events,
+ *     so later work on the caller's stream sees the call complete, and a
+ *     stream capture of the call captures the fork and the join.
  *   - Tensors are dense, row-major, contiguous; [B,H,T,m] means element
  *     (b,h,t,i) is at ((b*H + h)*T + t)*m + i.
  *   - Every pointer must be 16-byte aligned (FALCON_ERR_MISALIGNED otherwise).
