@@ -31,7 +31,8 @@ FALCON2 = 3  # per-column regression rule (Section 3.1, Section 4.2)
 FALCON2A = 4  # per-column inner-product rule (Section 4.3)
 _RULES = {"falcon1": FALCON1, "falcon1a": FALCON1A, FALCON1: FALCON1, FALCON1A: FALCON1A}
 _RULES2 = {"falcon2": FALCON2, "falcon2a": FALCON2A, FALCON2: FALCON2, FALCON2A: FALCON2A}
-_PHIS = {"identity": 0, "l2": 1}
+_PHIS = {"identity": 0, "l2": 1, "rms": 2}
+_RIDGES = {"given": 0, "scaled": 1}
 
 
 def build(force: bool = False) -> str:
@@ -55,17 +56,17 @@ def _load():
             i64 = ctypes.c_int64
             lib.falcon_oracle_forward.restype = ctypes.c_int
             lib.falcon_oracle_forward.argtypes = [
-                ctypes.c_int, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_double, ctypes.c_double, d, d, d, d, d, d, d, d, d, d, d,
                 ctypes.c_int]
             lib.falcon2_oracle_forward.restype = ctypes.c_int
             lib.falcon2_oracle_forward.argtypes = [
-                ctypes.c_int, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_double, ctypes.c_double, d, d, d, d, d, d, d, d, d, d,
                 ctypes.c_int]
             lib.falcon_oracle_decode_step.restype = ctypes.c_int
             lib.falcon_oracle_decode_step.argtypes = [
-                ctypes.c_int, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_double, ctypes.c_double, d, d, d, d, d, d, d,
                 ctypes.POINTER(ctypes.c_ubyte), d]
             _lib = lib
@@ -88,7 +89,7 @@ def _ptr(a):
 
 
 def forward(rule, q, k, v, beta, lam, S0=None, x_prev=None, phi="l2",
-            eps=1e-6, eps_gamma=1e-6, trajectory=False, threads=None):
+            eps=1e-6, eps_gamma=1e-6, trajectory=False, threads=None, ridge="given"):
     """Run the recurrence over whole sequences.
 
     Shapes: q, k [..., T, m]; v [..., T, dv]; beta, lam [..., T];
@@ -96,6 +97,8 @@ def forward(rule, q, k, v, beta, lam, S0=None, x_prev=None, phi="l2",
     The leading dims (B, H, ...) are flattened into independent heads.
     Returns a dict with o [..., T, dv], S [..., m, dv], x_last [..., m] and,
     if ``trajectory``, S_traj [..., T, m, dv] (the state after each token).
+    phi: "identity", "l2" or "rms"; ridge: "given" (lam is lambda_t) or
+    "scaled" (lam is the base ridge, lambda_t = lam_t * ||x_t||^2).
     """
     lib = _load()
     q, k, v, beta, lam = (_f64(t) for t in (q, k, v, beta, lam))
@@ -116,7 +119,7 @@ def forward(rule, q, k, v, beta, lam, S0=None, x_prev=None, phi="l2",
     traj = np.zeros(lead + (T, m, dv)) if trajectory else None
     nthreads = threads or os.cpu_count() or 1
     rc = lib.falcon_oracle_forward(
-        _RULES[rule], BH, T, m, dv, _PHIS[phi], eps, eps_gamma, _ptr(q), _ptr(k),
+        _RULES[rule], BH, T, m, dv, _PHIS[phi], _RIDGES[ridge], eps, eps_gamma, _ptr(q), _ptr(k),
         _ptr(v), _ptr(beta), _ptr(lam), _ptr(S0), _ptr(x_prev), _ptr(o), _ptr(S),
         _ptr(x_last), _ptr(traj), int(nthreads))
     if rc != 0:
@@ -128,7 +131,7 @@ def forward(rule, q, k, v, beta, lam, S0=None, x_prev=None, phi="l2",
 
 
 def forward2(rule, q, k, v, beta, lam, S0=None, x_prev=None, phi="l2",
-             eps=1e-6, eps_gamma=1e-6, threads=None):
+             eps=1e-6, eps_gamma=1e-6, threads=None, ridge="given"):
     """Falcon-2 / Falcon-2A over whole sequences: as ``forward`` except that
     ``beta`` has one gain per value column, shape [..., T, dv], and ``rule`` is
     "falcon2" or "falcon2a".  Returns a dict with o, S and x_last."""
@@ -150,7 +153,7 @@ def forward2(rule, q, k, v, beta, lam, S0=None, x_prev=None, phi="l2",
     x_last = np.zeros(lead + (m,))
     nthreads = threads or os.cpu_count() or 1
     rc = lib.falcon2_oracle_forward(
-        _RULES2[rule], BH, T, m, dv, _PHIS[phi], eps, eps_gamma, _ptr(q), _ptr(k),
+        _RULES2[rule], BH, T, m, dv, _PHIS[phi], _RIDGES[ridge], eps, eps_gamma, _ptr(q), _ptr(k),
         _ptr(v), _ptr(beta), _ptr(lam), _ptr(S0), _ptr(x_prev), _ptr(o), _ptr(S),
         _ptr(x_last), int(nthreads))
     if rc != 0:
@@ -159,7 +162,7 @@ def forward2(rule, q, k, v, beta, lam, S0=None, x_prev=None, phi="l2",
 
 
 def decode_step(rule, q, k, v, beta, lam, S, x_prev, fresh=None, phi="l2",
-                eps=1e-6, eps_gamma=1e-6):
+                eps=1e-6, eps_gamma=1e-6, ridge="given"):
     """One token for N independent states.  ``S`` [N, m, dv] and ``x_prev``
     [N, m] must be float64 numpy arrays; they are updated in place.  ``fresh``
     ([N] bool or None) marks states whose sequence starts at this token.
@@ -177,7 +180,8 @@ def decode_step(rule, q, k, v, beta, lam, S, x_prev, fresh=None, phi="l2",
         fr = np.ascontiguousarray(np.asarray(fresh, dtype=np.uint8))
         fr = fr.ctypes.data_as(ctypes.POINTER(ctypes.c_ubyte))
     rc = lib.falcon_oracle_decode_step(
-        _RULES[rule], N, m, dv, _PHIS[phi], eps, eps_gamma, _ptr(q), _ptr(k), _ptr(v),
+        _RULES[rule], N, m, dv, _PHIS[phi], _RIDGES[ridge], eps, eps_gamma, _ptr(q), _ptr(k),
+        _ptr(v),
         _ptr(beta), _ptr(lam), _ptr(S), _ptr(x_prev), fr, _ptr(o))
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (rc={rc})")

@@ -38,8 +38,9 @@
  *     effective ridge alpha_{j,t} / eta_{j,t} of the same paragraph).
  *
  * Readings where the pages are silent:
- *   - phi is either the identity or the l2 normalisation u / max(||u||, 1e-12)
- *     ("QK-l2" in the experiment tables of page juhoplayground.github.io);
+ *   - phi is the identity, the l2 normalisation u / max(||u||, 1e-12)
+ *     ("QK-l2" in the experiment tables of page juhoplayground.github.io), or
+ *     RMSNorm with eps_rms = 1e-6 (the pages name eps_rms without a value);
  *   - a caller that carries state across calls passes x_prev = phi(k_T) of the
  *     previous segment; then step 1 writes with x_1 = x_prev (no sentinel).
  */
@@ -55,10 +56,20 @@
 #define ORACLE_FALCON2A 4 /* per-column inner-product rule (Section 4.3) */
 #define ORACLE_PHI_IDENTITY 0
 #define ORACLE_PHI_L2 1
+#define ORACLE_PHI_RMS 2 /* RMSNorm, Section 4.1 "Scaled features" */
+#define ORACLE_EPS_RMS 1e-6 /* eps_rms: not given by the pages (a reading) */
+#define ORACLE_RIDGE_GIVEN 0  /* lambda_t as given */
+#define ORACLE_RIDGE_SCALED 1 /* lambda_t = lambda_bar_t * E_t, Section 4.1 */
 
-/* phi applied to one m-vector (Section 2.2 feature map; l2 variant). */
+/* phi applied to one m-vector: identity, the l2 map, or RMSNorm(u) =
+ * u / sqrt(||u||^2 / m + eps_rms) (Section 4.1, "Scaled features"). */
 static void feature_map(int phi, int m, const double *u, double *out) {
-  if (phi == ORACLE_PHI_L2) {
+  if (phi == ORACLE_PHI_RMS) {
+    double ss = 0.0;
+    for (int i = 0; i < m; ++i) ss += u[i] * u[i];
+    const double den = sqrt(ss / m + ORACLE_EPS_RMS);
+    for (int i = 0; i < m; ++i) out[i] = u[i] / den;
+  } else if (phi == ORACLE_PHI_L2) {
     double ss = 0.0;
     for (int i = 0; i < m; ++i) ss += u[i] * u[i];
     double nrm = sqrt(ss);
@@ -69,14 +80,17 @@ static void feature_map(int phi, int m, const double *u, double *out) {
   }
 }
 
-/* eta_t and gamma_t of one step (Eq. (3.4) and the decay clamp). */
+/* eta_t and gamma_t of one step (Eq. (3.4) and the decay clamp).  With the
+ * scale-coupled ridge (Section 4.1) the argument is the base ridge lambda_bar
+ * and the recurrence uses lambda_t = lambda_bar * E_t, E_t = ||x_t||^2. */
 static void step_scalars(int sentinel, int m, const double *x, double beta,
-                         double lambda, double eps, double eps_gamma,
+                         double lambda, int ridge, double eps, double eps_gamma,
                          double *eta_out, double *gamma_out) {
   double eta = 0.0;
+  double E = 0.0;
+  for (int i = 0; i < m; ++i) E += x[i] * x[i];
+  if (ridge == ORACLE_RIDGE_SCALED) lambda *= E;
   if (!sentinel) {
-    double E = 0.0;
-    for (int i = 0; i < m; ++i) E += x[i] * x[i];
     double den = E + lambda + eps;
     eta = (den > 0.0) ? beta / den : 0.0;
   }
@@ -115,7 +129,7 @@ static void one_token(int rule, int m, int dv, double *S, const double *x,
 }
 
 typedef struct {
-  int rule, m, dv, phi;
+  int rule, m, dv, phi, ridge;
   int64_t T;
   double eps, eps_gamma;
   const double *q, *k, *v, *beta, *lambda, *S0, *x_prev;
@@ -139,7 +153,7 @@ static void forward_head(const fwd_args *a, int64_t bh) {
   for (int64_t t = 0; t < T; ++t) {
     const int64_t row = bh * T + t;
     double eta, gamma;
-    step_scalars(sentinel && t == 0, m, x, a->beta[row], a->lambda[row],
+    step_scalars(sentinel && t == 0, m, x, a->beta[row], a->lambda[row], a->ridge,
                  a->eps, a->eps_gamma, &eta, &gamma);
     feature_map(a->phi, m, a->q + row * m, qf);
     one_token(a->rule, m, dv, S, x, qf, a->v + row * dv, eta, gamma, r,
@@ -178,7 +192,7 @@ static void *forward_worker(void *p) {
  * Returns 0, or -1 on a bad argument.
  */
 int falcon_oracle_forward(int rule, int64_t BH, int64_t T, int m, int dv,
-                          int phi, double eps, double eps_gamma,
+                          int phi, int ridge, double eps, double eps_gamma,
                           const double *q, const double *k, const double *v,
                           const double *beta, const double *lambda,
                           const double *S0, const double *x_prev, double *o,
@@ -186,7 +200,7 @@ int falcon_oracle_forward(int rule, int64_t BH, int64_t T, int m, int dv,
                           int nthreads) {
   if (rule != ORACLE_FALCON1 && rule != ORACLE_FALCON1A) return -1;
   if (BH < 0 || T < 0 || m <= 0 || dv <= 0) return -1;
-  fwd_args a = {rule, m, dv, phi, T, eps, eps_gamma, q, k, v, beta, lambda,
+  fwd_args a = {rule, m, dv, phi, ridge, T, eps, eps_gamma, q, k, v, beta, lambda,
                 S0, x_prev, o, S_out, x_last, S_traj};
   if (nthreads < 1) nthreads = 1;
   if (nthreads > BH) nthreads = (int)(BH > 0 ? BH : 1);
@@ -216,7 +230,7 @@ int falcon_oracle_forward(int rule, int64_t BH, int64_t T, int m, int dv,
  *           where the sentinel applies (x = 0, eta = 0).
  */
 int falcon_oracle_decode_step(int rule, int64_t N, int m, int dv, int phi,
-                              double eps, double eps_gamma, const double *q,
+                              int ridge, double eps, double eps_gamma, const double *q,
                               const double *k, const double *v,
                               const double *beta, const double *lambda,
                               double *S, double *x_prev,
@@ -233,7 +247,7 @@ int falcon_oracle_decode_step(int rule, int64_t N, int m, int dv, int phi,
     else
       memcpy(x, x_prev + n * m, sizeof(double) * (size_t)m);
     double eta, gamma;
-    step_scalars(sentinel, m, x, beta[n], lambda[n], eps, eps_gamma, &eta, &gamma);
+    step_scalars(sentinel, m, x, beta[n], lambda[n], ridge, eps, eps_gamma, &eta, &gamma);
     feature_map(phi, m, q + n * m, qf);
     one_token(rule, m, dv, S + n * m * dv, x, qf, v + n * dv, eta, gamma, r,
               o + n * dv);
@@ -254,7 +268,7 @@ int falcon_oracle_decode_step(int rule, int64_t N, int m, int dv, int phi,
  * column and token).  Returns 0, or -1 on a bad argument.
  */
 typedef struct {
-  int rule, m, dv, phi;
+  int rule, m, dv, phi, ridge;
   int64_t T;
   double eps, eps_gamma;
   const double *q, *k, *v, *beta, *lambda, *S0, *x_prev;
@@ -275,9 +289,10 @@ static void forward2_head(const fwd2_args *a, int64_t bh) {
   }
   for (int64_t t = 0; t < T; ++t) {
     const int64_t row = bh * T + t;
-    const double lambda = a->lambda[row];
     double E = 0.0;
     for (int i = 0; i < m; ++i) E += x[i] * x[i];
+    const double lambda =
+        a->ridge == ORACLE_RIDGE_SCALED ? a->lambda[row] * E : a->lambda[row];
     const double den = E + lambda + a->eps;
     feature_map(a->phi, m, a->q + row * m, qf);
     for (int j = 0; j < dv; ++j) {
@@ -322,14 +337,14 @@ static void *forward2_worker(void *p) {
 }
 
 int falcon2_oracle_forward(int rule, int64_t BH, int64_t T, int m, int dv, int phi,
-                           double eps, double eps_gamma, const double *q,
+                           int ridge, double eps, double eps_gamma, const double *q,
                            const double *k, const double *v, const double *beta,
                            const double *lambda, const double *S0,
                            const double *x_prev, double *o, double *S_out,
                            double *x_last, int nthreads) {
   if (rule != ORACLE_FALCON2 && rule != ORACLE_FALCON2A) return -1;
   if (BH < 0 || T < 0 || m <= 0 || dv <= 0) return -1;
-  fwd2_args a = {rule, m, dv, phi, T, eps, eps_gamma, q, k, v, beta, lambda,
+  fwd2_args a = {rule, m, dv, phi, ridge, T, eps, eps_gamma, q, k, v, beta, lambda,
                  S0, x_prev, o, S_out, x_last};
   if (nthreads < 1) nthreads = 1;
   if (nthreads > BH) nthreads = (int)(BH > 0 ? BH : 1);
