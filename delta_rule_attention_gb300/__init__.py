@@ -24,7 +24,11 @@ FALCON_BF16 = 0
 FALCON_F32 = 1
 FALCON_PHI_IDENTITY = 0
 FALCON_PHI_L2 = 1
-_PHI = {"identity": FALCON_PHI_IDENTITY, "l2": FALCON_PHI_L2}
+FALCON_PHI_RMS = 2
+_PHI = {"identity": FALCON_PHI_IDENTITY, "l2": FALCON_PHI_L2, "rms": FALCON_PHI_RMS}
+FALCON_RIDGE_GIVEN = 0
+FALCON_RIDGE_SCALED = 1
+_RIDGE = {"given": FALCON_RIDGE_GIVEN, "scaled": FALCON_RIDGE_SCALED}
 _DTYPE = {torch.bfloat16: FALCON_BF16, torch.float32: FALCON_F32}
 
 # Entry points declared in include/falcon.h.
@@ -48,7 +52,7 @@ class falcon_shape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int64), ("H", ctypes.c_int64), ("T", ctypes.c_int64),
                 ("m", ctypes.c_int32), ("dv", ctypes.c_int32), ("chunk", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("phi", ctypes.c_int32),
-                ("eps", ctypes.c_float), ("eps_gamma", ctypes.c_float)]
+                ("eps", ctypes.c_float), ("eps_gamma", ctypes.c_float), ("ridge", ctypes.c_int32)]
 
 
 _lib = None
@@ -79,7 +83,7 @@ def load_library(path: str | None = None):
         for name in ("falcon1_decode_step", "falcon1a_decode_step"):
             fn = getattr(lib, name)
             fn.restype = ctypes.c_int
-            fn.argtypes = [i64, i32, i32, i32, i32, ctypes.c_float, ctypes.c_float,
+            fn.argtypes = [i64, i32, i32, i32, i32, i32, ctypes.c_float, ctypes.c_float,
                            vp, vp, vp, f32p, f32p, f32p, f32p, vp, vp, vp]
         for name in ("falcon2_fwd_recurrent", "falcon2a_fwd_recurrent"):
             fn = getattr(lib, name)
@@ -136,11 +140,14 @@ def _need(t, name, dtype=None, shape=None):
     return t
 
 
-def make_shape(B, H, T, m, dv, chunk, dtype, phi="l2", eps=1e-6, eps_gamma=1e-6):
+def make_shape(B, H, T, m, dv, chunk, dtype, phi="l2", eps=1e-6, eps_gamma=1e-6,
+               ridge="given"):
+    """phi: "identity", "l2" or "rms"; ridge: "given" (lambda is lambda_t) or
+    "scaled" (lambda is the base ridge, lambda_t = lambda * ||x_t||^2)."""
     return falcon_shape(int(B), int(H), int(T), int(m), int(dv), int(chunk),
                         _DTYPE[dtype] if isinstance(dtype, torch.dtype) else int(dtype),
                         _PHI[phi] if isinstance(phi, str) else int(phi), float(eps),
-                        float(eps_gamma))
+                        float(eps_gamma), _RIDGE[ridge] if isinstance(ridge, str) else int(ridge))
 
 
 def falcon_workspace_bytes(shape: falcon_shape) -> int:
@@ -149,7 +156,7 @@ def falcon_workspace_bytes(shape: falcon_shape) -> int:
 
 def _fwd(name, q, k, v, beta, lam, S0=None, x_prev=None, chunk=64, phi="l2", eps=1e-6,
          eps_gamma=1e-6, o=None, S_out=None, x_last=None, workspace=None, stream=None,
-         want_x_last=True):
+         want_x_last=True, ridge="given"):
     lib = load_library()
     _need(q, "q")
     B, H, T, m = q.shape
@@ -172,7 +179,7 @@ def _fwd(name, q, k, v, beta, lam, S0=None, x_prev=None, chunk=64, phi="l2", eps
         S_out = torch.empty((B, H, m, dv), dtype=torch.float32, device=dev)
     if x_last is None and want_x_last:
         x_last = torch.empty((B, H, m), dtype=torch.float32, device=dev)
-    shape = make_shape(B, H, T, m, dv, chunk, dt, phi, eps, eps_gamma)
+    shape = make_shape(B, H, T, m, dv, chunk, dt, phi, eps, eps_gamma, ridge)
     need = int(lib.falcon_workspace_bytes(ctypes.byref(shape)))
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
@@ -195,7 +202,7 @@ def falcon1_fwd_chunked(q, k, v, beta, lam, S0=None, x_prev=None, chunk=64, phi=
 
 def falcon1_fwd_chunked_fixed_scratch(q, k, v, beta, lam, S0=None, x_prev=None, chunk=64,
                                       phi="l2", eps=1e-6, eps_gamma=1e-6, o=None, S_out=None,
-                                      x_last=None, stream=None):
+                                      x_last=None, stream=None, ridge="given"):
     """Falcon-1 chunked forward that needs no workspace: for callers that
     cannot allocate device memory, the library uses a fixed scratch array of
     FALCON_FIXED_SCRATCH_BYTES built into it.  Pass preallocated o, S_out,
@@ -222,7 +229,7 @@ def falcon1_fwd_chunked_fixed_scratch(q, k, v, beta, lam, S0=None, x_prev=None, 
                     (S_out, "S_out"), (x_last, "x_last"), (S0, "S0"), (x_prev, "x_prev")):
         if t is not None:
             _need(t, name)
-    shape = make_shape(B, H, T, m, dv, chunk, dt, phi, eps, eps_gamma)
+    shape = make_shape(B, H, T, m, dv, chunk, dt, phi, eps, eps_gamma, ridge)
     rc = lib.falcon1_fwd_chunked_fixed_scratch(
         ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(lam), _ptr(S0),
         _ptr(x_prev), _ptr(o), _ptr(S_out), _ptr(x_last), _stream(stream))
@@ -238,7 +245,8 @@ def falcon1a_fwd_chunked(q, k, v, beta, lam, S0=None, x_prev=None, chunk=64, phi
 
 
 def _fwd2(name, q, k, v, beta, lam, S0=None, x_prev=None, phi="l2", eps=1e-6,
-          eps_gamma=1e-6, o=None, S_out=None, x_last=None, stream=None, want_x_last=True):
+          eps_gamma=1e-6, o=None, S_out=None, x_last=None, stream=None, want_x_last=True,
+          ridge="given"):
     lib = load_library()
     _need(q, "q")
     B, H, T, m = q.shape
@@ -261,7 +269,7 @@ def _fwd2(name, q, k, v, beta, lam, S0=None, x_prev=None, phi="l2", eps=1e-6,
         S_out = torch.empty((B, H, m, dv), dtype=torch.float32, device=dev)
     if x_last is None and want_x_last:
         x_last = torch.empty((B, H, m), dtype=torch.float32, device=dev)
-    shape = make_shape(B, H, T, m, dv, 64, dt, phi, eps, eps_gamma)
+    shape = make_shape(B, H, T, m, dv, 64, dt, phi, eps, eps_gamma, ridge)
     rc = getattr(lib, name)(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
                             _ptr(lam), _ptr(S0), _ptr(x_prev), _ptr(o), _ptr(S_out),
                             _ptr(x_last), _stream(stream))
@@ -287,7 +295,7 @@ def falcon2a_fwd_recurrent(q, k, v, beta, lam, S0=None, x_prev=None, phi="l2", e
 
 
 def _decode(name, q, k, v, beta, lam, S, x_prev, fresh=None, phi="l2", eps=1e-6,
-            eps_gamma=1e-6, o=None, stream=None):
+            eps_gamma=1e-6, o=None, stream=None, ridge="given"):
     lib = load_library()
     _need(q, "q")
     N, m = q.shape
@@ -303,7 +311,8 @@ def _decode(name, q, k, v, beta, lam, S, x_prev, fresh=None, phi="l2", eps=1e-6,
         _need(fresh, "fresh", torch.uint8, (N,))
     if o is None:
         o = torch.empty((N, dv), dtype=dt, device=q.device)
-    rc = getattr(lib, name)(N, m, dv, _DTYPE[dt], _PHI[phi], float(eps), float(eps_gamma),
+    rc = getattr(lib, name)(N, m, dv, _DTYPE[dt], _PHI[phi], _RIDGE[ridge], float(eps),
+                            float(eps_gamma),
                             _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(lam), _ptr(S),
                             _ptr(x_prev), _ptr(fresh), _ptr(o), _stream(stream))
     _check(rc, name)
@@ -311,18 +320,18 @@ def _decode(name, q, k, v, beta, lam, S, x_prev, fresh=None, phi="l2", eps=1e-6,
 
 
 def falcon1_decode_step(q, k, v, beta, lam, S, x_prev, fresh=None, phi="l2", eps=1e-6,
-                        eps_gamma=1e-6, o=None, stream=None):
+                        eps_gamma=1e-6, o=None, stream=None, ridge="given"):
     """One Falcon-1 token for N states: S [N,m,dv] and x_prev [N,m] are updated
     in place; fresh [N] uint8 marks sequences starting at this token.  Returns o."""
     return _decode("falcon1_decode_step", q, k, v, beta, lam, S, x_prev, fresh, phi, eps,
-                   eps_gamma, o, stream)
+                   eps_gamma, o, stream, ridge)
 
 
 def falcon1a_decode_step(q, k, v, beta, lam, S, x_prev, fresh=None, phi="l2", eps=1e-6,
-                         eps_gamma=1e-6, o=None, stream=None):
+                         eps_gamma=1e-6, o=None, stream=None, ridge="given"):
     """One Falcon-1A token for N states (see falcon1_decode_step)."""
     return _decode("falcon1a_decode_step", q, k, v, beta, lam, S, x_prev, fresh, phi, eps,
-                   eps_gamma, o, stream)
+                   eps_gamma, o, stream, ridge)
 
 
 def falcon_sync_check(stream=None) -> int:

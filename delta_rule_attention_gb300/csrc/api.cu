@@ -34,9 +34,11 @@ int check_device() {
   return (major == 10 && minor == 3) ? FALCON_OK : FALCON_ERR_DEVICE;
 }
 
-int check_common(int dtype, int phi, float eps, float eps_gamma) {
+int check_common(int dtype, int phi, int ridge, float eps, float eps_gamma) {
   if (dtype != FALCON_BF16 && dtype != FALCON_F32) return FALCON_ERR_BAD_DTYPE;
-  if (phi != FALCON_PHI_IDENTITY && phi != FALCON_PHI_L2) return FALCON_ERR_BAD_DTYPE;
+  if (phi != FALCON_PHI_IDENTITY && phi != FALCON_PHI_L2 && phi != FALCON_PHI_RMS)
+    return FALCON_ERR_BAD_DTYPE;
+  if (ridge != FALCON_RIDGE_GIVEN && ridge != FALCON_RIDGE_SCALED) return FALCON_ERR_BAD_ARG;
   if (!(eps >= 0.f) || !(eps_gamma > 0.f) || !(eps_gamma < 1.f)) return FALCON_ERR_BAD_ARG;
   return FALCON_OK;
 }
@@ -49,7 +51,7 @@ int check_shape(const falcon_shape* s) {
   // Grid limits: B*H CTAs along y of the prep grid, chunks along x.
   if (s->B * s->H > 65535 || (s->T + s->chunk - 1) / s->chunk > 0x7fffffffLL)
     return FALCON_ERR_BAD_SHAPE;
-  return check_common(s->dtype, s->phi, s->eps, s->eps_gamma);
+  return check_common(s->dtype, s->phi, s->ridge, s->eps, s->eps_gamma);
 }
 
 int to_status(cudaError_t e) { return e == cudaSuccess ? FALCON_OK : FALCON_ERR_CUDA; }
@@ -114,6 +116,7 @@ int fwd_chunked(int rule, const falcon_shape* s, const void* q, const void* k, c
   a.C = s->chunk;
   a.dtype = s->dtype;
   a.phi = s->phi;
+  a.ridge = s->ridge;
   a.eps = s->eps;
   a.eps_gamma = s->eps_gamma;
   a.q = q;
@@ -155,12 +158,12 @@ __global__ void wait_timeout_kernel(uint64_t limit_ns, int* err) {
   if (threadIdx.x == 0) atomicExch(err, 1);
 }
 
-int decode(int rule, int64_t N, int32_t m, int32_t dv, int32_t dtype, int32_t phi, float eps,
-           float eps_gamma, const void* q, const void* k, const void* v, const float* beta,
+int decode(int rule, int64_t N, int32_t m, int32_t dv, int32_t dtype, int32_t phi, int32_t ridge,
+           float eps, float eps_gamma, const void* q, const void* k, const void* v, const float* beta,
            const float* lambda, float* S, float* x_prev, const uint8_t* fresh, void* o,
            cudaStream_t stream) {
   if (N < 0 || N > 0x7fffffffLL || !dim_ok(m) || !dim_ok(dv)) return FALCON_ERR_BAD_SHAPE;
-  int rc = check_common(dtype, phi, eps, eps_gamma);
+  int rc = check_common(dtype, phi, ridge, eps, eps_gamma);
   if (rc) return rc;
   if (N == 0) return FALCON_OK;
   if (!q || !k || !v || !beta || !lambda || !S || !x_prev || !o) return FALCON_ERR_NULL_PTR;
@@ -176,6 +179,7 @@ int decode(int rule, int64_t N, int32_t m, int32_t dv, int32_t dtype, int32_t ph
   a.dv = dv;
   a.dtype = dtype;
   a.phi = phi;
+  a.ridge = ridge;
   a.eps = eps;
   a.eps_gamma = eps_gamma;
   a.q = q;
@@ -233,20 +237,20 @@ int falcon2a_fwd_recurrent(const falcon_shape* s, const void* q, const void* k, 
                      nullptr, 0, stream);
 }
 
-int falcon1_decode_step(int64_t N, int32_t m, int32_t dv, int32_t dtype, int32_t phi, float eps,
-                        float eps_gamma, const void* q, const void* k, const void* v,
-                        const float* beta, const float* lambda, float* S, float* x_prev,
-                        const uint8_t* fresh, void* o, cudaStream_t stream) {
-  return decode(falcon::kFalcon1, N, m, dv, dtype, phi, eps, eps_gamma, q, k, v, beta, lambda,
-                S, x_prev, fresh, o, stream);
+int falcon1_decode_step(int64_t N, int32_t m, int32_t dv, int32_t dtype, int32_t phi,
+                        int32_t ridge, float eps, float eps_gamma, const void* q, const void* k,
+                        const void* v, const float* beta, const float* lambda, float* S,
+                        float* x_prev, const uint8_t* fresh, void* o, cudaStream_t stream) {
+  return decode(falcon::kFalcon1, N, m, dv, dtype, phi, ridge, eps, eps_gamma, q, k, v, beta,
+                lambda, S, x_prev, fresh, o, stream);
 }
 
 int falcon1a_decode_step(int64_t N, int32_t m, int32_t dv, int32_t dtype, int32_t phi,
-                         float eps, float eps_gamma, const void* q, const void* k, const void* v,
-                         const float* beta, const float* lambda, float* S, float* x_prev,
-                         const uint8_t* fresh, void* o, cudaStream_t stream) {
-  return decode(falcon::kFalcon1A, N, m, dv, dtype, phi, eps, eps_gamma, q, k, v, beta, lambda,
-                S, x_prev, fresh, o, stream);
+                         int32_t ridge, float eps, float eps_gamma, const void* q, const void* k,
+                         const void* v, const float* beta, const float* lambda, float* S,
+                         float* x_prev, const uint8_t* fresh, void* o, cudaStream_t stream) {
+  return decode(falcon::kFalcon1A, N, m, dv, dtype, phi, ridge, eps, eps_gamma, q, k, v, beta,
+                lambda, S, x_prev, fresh, o, stream);
 }
 
 int falcon_selftest_wait_timeout(uint32_t limit_us, cudaStream_t stream) {
@@ -291,6 +295,6 @@ const char* falcon_strerror(int code) {
   return "unknown error code";
 }
 
-int falcon_version(void) { return 100; }
+int falcon_version(void) { return 10100; }
 
 }  // extern "C"

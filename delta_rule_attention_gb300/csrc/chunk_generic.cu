@@ -53,8 +53,7 @@ __device__ float warp_feature(const void* src, int64_t off, int m, int dtype, in
     ss += u[e] * u[e];
   }
   ss = warp_sum(ss);
-  float scale = 1.f;
-  if (phi == FALCON_PHI_L2) scale = 1.f / fmaxf(sqrtf(ss), 1e-12f);
+  const float scale = feature_scale(ss, m, phi);
   float out_ss = 0.f;
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
@@ -134,8 +133,9 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(ChunkArgs a, int n
     float lg = 0.f, e = 0.f, gam;
     if (i < n) {
       const bool sentinel = (t0 + i == 0) && (a.x_prev == nullptr);
-      e = step_eta_gamma(sentinel, E[i], a.beta[rowbase + t0 + i], a.lambda[rowbase + t0 + i],
-                         a.eps, a.eps_gamma, &gam, &lg);
+      e = step_eta_gamma(sentinel, E[i], a.beta[rowbase + t0 + i],
+                         ridge_of(a.lambda[rowbase + t0 + i], E[i], a.ridge), a.eps, a.eps_gamma,
+                         &gam, &lg);
     }
     eta[i] = e;
     g[i] = lg;  // prefix below

@@ -219,10 +219,12 @@ __device__ __forceinline__ float sumsq32(const float* v) {
   return ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
 }
 
-// phi's scale for a row with squared norm ss: 1 / max(||u||, 1e-12) for the
-// l2 map (0 for an all-zero row, which makes no difference to phi(u) = 0 and
-// keeps products with the exponential factors finite), 1 for the identity.
-__device__ __forceinline__ float phi_scale(float ss, int phi) {
+// phi's scale for a row of m values with squared norm ss: 1 / max(||u||,
+// 1e-12) for the l2 map (0 for an all-zero row, which makes no difference to
+// phi(u) = 0 and keeps products with the exponential factors finite),
+// 1 / sqrt(ss / m + eps_rms) for RMSNorm, 1 for the identity.
+__device__ __forceinline__ float phi_scale(float ss, int m, int phi) {
+  if (phi == FALCON_PHI_RMS) return rsqrtf(ss / (float)m + kEpsRms);
   if (phi != FALCON_PHI_L2) return 1.f;
   return ss > 0.f ? rsqrtf(fmaxf(ss, 1e-24f)) : 0.f;
 }
@@ -405,7 +407,7 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
     sc.ssp[h][r] = sumsq32(x);
   __syncthreads();
   const float ss = sc.ssp[0][r] + sc.ssp[1][r];
-  const float nr = carried_row ? 1.f : phi_scale(ss, a.phi);
+  const float nr = carried_row ? 1.f : phi_scale(ss, M, a.phi);
   const float E = ss * nr * nr;  // ||x_r||^2 (rows < 64)
   if (h == 0) sc.nrm[r] = nr;
   if (a.x_last && last) {
@@ -425,7 +427,7 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
         for (int i = 0; i < 32; ++i) part[i] = __bfloat162float(kl[32 * pc + i]);
         s2 += sumsq32(part);
       }
-      const float s = phi_scale(s2, a.phi);
+      const float s = phi_scale(s2, M, a.phi);
 #pragma unroll
       for (int i = 0; i < 32; ++i) xl[i] = __bfloat162float(kl[64 * j + 32 * h + i]) * s;
     }
@@ -436,7 +438,8 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
   if (tid < 64 && tid < n) {
     float gam;
     const bool sentinel = (t0 + tid == 0) && (a.x_prev == nullptr);
-    eta = step_eta_gamma(sentinel, E, beta_t, lam_t, a.eps, a.eps_gamma, &gam, &lg);
+    eta = step_eta_gamma(sentinel, E, beta_t, ridge_of(lam_t, E, a.ridge), a.eps, a.eps_gamma,
+                         &gam, &lg);
   }
   float incl = lg;
 #pragma unroll

@@ -33,6 +33,22 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
+// phi's scale for a row u of m values with squared norm ss: 1 for the
+// identity, 1 / max(||u||, 1e-12) for the l2 map, 1 / sqrt(ss / m + eps_rms)
+// for RMSNorm (eps_rms = 1e-6: the pages name the stabiliser without a value).
+constexpr float kEpsRms = 1e-6f;
+__device__ __forceinline__ float feature_scale(float ss, int m, int phi) {
+  if (phi == FALCON_PHI_L2) return 1.f / fmaxf(sqrtf(ss), 1e-12f);
+  if (phi == FALCON_PHI_RMS) return rsqrtf(ss / (float)m + kEpsRms);
+  return 1.f;
+}
+
+// lambda_t used by the recurrence: as given, or the scale-coupled form
+// lambda_bar_t * E_t with E_t = ||x_t||^2.
+__device__ __forceinline__ float ridge_of(float lam, float E, int ridge) {
+  return ridge == FALCON_RIDGE_SCALED ? lam * E : lam;
+}
+
 // Step size and decay of one token (Eq. (3.4) and the decay clamp).
 // Returns eta; writes gamma = 1 - min(eta*lambda, 1 - eps_gamma) and its log.
 // On the clamped branch gamma is exactly eps_gamma: forming 1 - (1 - eps_gamma)
@@ -63,7 +79,7 @@ namespace falcon {
 struct ChunkArgs {
   int rule;
   int64_t BH, T;
-  int m, dv, C, dtype, phi;
+  int m, dv, C, dtype, phi, ridge;
   float eps, eps_gamma;
   const void *q, *k, *v;
   const float *beta, *lambda, *S0, *x_prev;
@@ -86,7 +102,7 @@ cudaError_t launch_tc_chunked(const ChunkArgs& a, int* err, cudaStream_t stream)
 struct DecodeArgs {
   int rule;
   int64_t N;
-  int m, dv, dtype, phi;
+  int m, dv, dtype, phi, ridge;
   float eps, eps_gamma;
   const void *q, *k, *v;
   const float *beta, *lambda;

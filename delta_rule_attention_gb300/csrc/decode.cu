@@ -79,11 +79,7 @@ __global__ void __launch_bounds__(DecodeCfg<M, DV>::kThreads)
     sq = warp_sum(sq);
     sk = warp_sum(sk);
     const float E = warp_sum(sx);
-    float fq = 1.f, fk = 1.f;
-    if (a.phi == FALCON_PHI_L2) {
-      fq = 1.f / fmaxf(sqrtf(sq), 1e-12f);
-      fk = 1.f / fmaxf(sqrtf(sk), 1e-12f);
-    }
+    const float fq = feature_scale(sq, M, a.phi), fk = feature_scale(sk, M, a.phi);
     float xq = 0.f;
 #pragma unroll
     for (int e = 0; e < (M + 31) / 32; ++e) {
@@ -98,8 +94,8 @@ __global__ void __launch_bounds__(DecodeCfg<M, DV>::kThreads)
     xq = warp_sum(xq);
     if (tid == 0) {
       float gamma, lg;
-      const float eta = step_eta_gamma(fresh, E, a.beta[n], a.lambda[n], a.eps, a.eps_gamma,
-                                       &gamma, &lg);
+      const float eta = step_eta_gamma(fresh, E, a.beta[n], ridge_of(a.lambda[n], E, a.ridge),
+                                       a.eps, a.eps_gamma, &gamma, &lg);
       scal[0] = eta;
       scal[1] = gamma;
       scal[2] = xq;

@@ -194,11 +194,7 @@ __global__ void __launch_bounds__(F2Cfg<M>::kThreads)
         sk += __shfl_xor_sync(0xffffffffu, sk, o);
         sq += __shfl_xor_sync(0xffffffffu, sq, o);
       }
-      float fk = 1.f, fq = 1.f;
-      if (a.phi == FALCON_PHI_L2) {
-        fk = 1.f / fmaxf(sqrtf(sk), 1e-12f);
-        fq = 1.f / fmaxf(sqrtf(sq), 1e-12f);
-      }
+      const float fk = feature_scale(sk, M, a.phi), fq = feature_scale(sq, M, a.phi);
       if (sl < nb) {
         float* xr = &sm.xs[sl + 1][20 * sg];
         float* qr = &sm.qs[sl][20 * sg];
@@ -243,7 +239,7 @@ __global__ void __launch_bounds__(F2Cfg<M>::kThreads)
     for (int p = tid; p < kTB * 32; p += C::kThreads) {
       const int l = p >> 5, c = p & 31;
       const int gc = cg * 32 + c;
-      const float lam = __shfl_sync(0xffffffffu, lam_l, l);
+      const float lam = ridge_of(__shfl_sync(0xffffffffu, lam_l, l), sm.Es[l], a.ridge);
       if (l < nb && gc < a.dv) {
         // eta_{j,t} and the clamped decay (as step_eta_gamma, without the log)
         const bool sent = sentinel0 && (t0 + l == 0);

@@ -72,9 +72,19 @@ extern "C" {
 #define FALCON_BF16 0
 #define FALCON_F32 1
 
-/* Feature map phi applied to q and k. */
+/* Feature map phi applied to q and k: the identity, the l2 map
+ * u / max(||u||_2, 1e-12), or RMSNorm(u) = u / sqrt(||u||_2^2 / d + eps_rms)
+ * with eps_rms = 1e-6 (Section 4.1, "Scaled features": the pages' default
+ * feature map; they name eps_rms without a value). */
 #define FALCON_PHI_IDENTITY 0
 #define FALCON_PHI_L2 1
+#define FALCON_PHI_RMS 2
+
+/* Ridge parameterisation (Section 4.1, "Scaled DeltaNet and the common ridge
+ * parameterization"): lambda as given, or a base ridge lambda_bar from which
+ * the recurrence takes lambda_t = lambda_bar_t * ||x_t||^2. */
+#define FALCON_RIDGE_GIVEN 0
+#define FALCON_RIDGE_SCALED 1
 
 /* Problem description for the chunked forward calls.
  *   B, H   batch and heads; the B*H heads are independent.
@@ -86,9 +96,11 @@ extern "C" {
  *   chunk  chunk length C used by the chunk-parallel form: 16, 32 or 64.  It
  *          changes only the rounding, never the result in exact arithmetic.
  *   dtype  FALCON_BF16 or FALCON_F32 (q, k, v, o).
- *   phi    FALCON_PHI_IDENTITY or FALCON_PHI_L2.
+ *   phi    FALCON_PHI_IDENTITY, FALCON_PHI_L2 or FALCON_PHI_RMS.
  *   eps    >= 0, the step-size stabiliser of Eq. (3.4).
- *   eps_gamma in (0, 1), the clamp margin: gamma_t >= eps_gamma. */
+ *   eps_gamma in (0, 1), the clamp margin: gamma_t >= eps_gamma.
+ *   ridge  FALCON_RIDGE_GIVEN (lambda is lambda_t) or FALCON_RIDGE_SCALED
+ *          (lambda is the base ridge; lambda_t = lambda_t(input) * ||x_t||^2). */
 typedef struct {
   int64_t B, H, T;
   int32_t m, dv, chunk;
@@ -96,6 +108,7 @@ typedef struct {
   int32_t phi;
   float eps;
   float eps_gamma;
+  int32_t ridge;
 } falcon_shape;
 
 /* Bytes of device workspace a chunked forward call with this shape needs
@@ -204,17 +217,20 @@ int falcon2a_fwd_recurrent(const falcon_shape *shape, const void *q,
  *   fresh   [N] bytes, nullable: nonzero marks a state whose sequence starts
  *           at this token (sentinel: x_t = 0, eta_t = 0, so S is not
  *           decayed and o = S^T phi(q)); NULL means no state is fresh
+ * phi and ridge as in falcon_shape.
  * m, dv in {16, 32, 64, 128}.  N >= 0 (N = 0 launches nothing).
  * Errors as for falcon1_fwd_chunked (no workspace). */
 int falcon1_decode_step(int64_t N, int32_t m, int32_t dv, int32_t dtype,
-                        int32_t phi, float eps, float eps_gamma, const void *q,
+                        int32_t phi, int32_t ridge, float eps, float eps_gamma,
+                        const void *q,
                         const void *k, const void *v, const float *beta,
                         const float *lambda, float *S, float *x_prev,
                         const uint8_t *fresh, void *o, cudaStream_t stream);
 
 /* The same single-token step for Falcon-1A (Section 4.3 Eq. (4.6)). */
 int falcon1a_decode_step(int64_t N, int32_t m, int32_t dv, int32_t dtype,
-                         int32_t phi, float eps, float eps_gamma, const void *q,
+                         int32_t phi, int32_t ridge, float eps, float eps_gamma,
+                         const void *q,
                          const void *k, const void *v, const float *beta,
                          const float *lambda, float *S, float *x_prev,
                          const uint8_t *fresh, void *o, cudaStream_t stream);

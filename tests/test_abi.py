@@ -47,7 +47,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_strerror(lib):
-    assert lib.falcon_version() == 100
+    assert lib.falcon_version() == 10100
     assert lib.falcon_strerror(0) == b"ok"
     for code in range(-9, 0):
         assert lib.falcon_strerror(code) != b"unknown error code"
@@ -83,7 +83,7 @@ def _fake(addr=0x10000):
 @pytest.mark.parametrize("bad,code", [
     (dict(m=24), -2), (dict(dv=256), -2), (dict(chunk=48), -2), (dict(T=-1), -2),
     (dict(dtype=7), -3), (dict(phi=3), -3), (dict(eps=-1.0), -8), (dict(eps_gamma=1.0), -8),
-    (dict(eps_gamma=0.0), -8),
+    (dict(eps_gamma=0.0), -8), (dict(ridge=2), -8), (dict(ridge=-1), -8),
 ])
 def test_forward_rejects_bad_shapes_without_a_device(lib, fn, bad, code):
     s = _shape(**bad)
@@ -116,12 +116,14 @@ def test_forward_rejects_null_misaligned_and_small_workspace(lib, fn):
 def test_decode_rejects_bad_arguments_without_a_device(lib, fn):
     f = getattr(lib, fn)
     p, odd = _fake(), _fake(0x10004)
-    args = lambda N=4, m=64, dv=64, dt=0, phi=1, eps=1e-6, eg=1e-6, q=p, S=p: f(
-        N, m, dv, dt, phi, ctypes.c_float(eps), ctypes.c_float(eg), q, p, p, p, p, S, p, None,
-        p, None)
+    args = lambda N=4, m=64, dv=64, dt=0, phi=1, ridge=0, eps=1e-6, eg=1e-6, q=p, S=p: f(
+        N, m, dv, dt, phi, ridge, ctypes.c_float(eps), ctypes.c_float(eg), q, p, p, p, p, S, p,
+        None, p, None)
     assert args(m=48) == -2
     assert args(N=-1) == -2
     assert args(dt=5) == -3
+    assert args(phi=3) == -3
+    assert args(ridge=2) == -8
     assert args(eg=2.0) == -8
     assert args(q=None) == -1
     assert args(S=odd) == -4
