@@ -1,4 +1,4 @@
-"""fp64 CPU oracle for the Falcon-1 / Falcon-1A and Falcon-2 / Falcon-2A recurrences.
+"""fp64 CPU oracle for the Falcon-1 / Falcon-1A, Falcon-2 / Falcon-2A and Falcon-3A recurrences.
 
 TEST INFRASTRUCTURE ONLY.  Nothing in the library path imports this package:
 only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline legs of
@@ -64,6 +64,10 @@ def _load():
                 ctypes.c_int, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_double, ctypes.c_double, d, d, d, d, d, d, d, d, d, d,
                 ctypes.c_int]
+            lib.falcon3a_oracle_forward.restype = ctypes.c_int
+            lib.falcon3a_oracle_forward.argtypes = [
+                i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_double, ctypes.c_double, d, d, d, d, d, d, d, d, d, ctypes.c_int]
             lib.falcon_oracle_decode_step.restype = ctypes.c_int
             lib.falcon_oracle_decode_step.argtypes = [
                 ctypes.c_int, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -156,6 +160,34 @@ def forward2(rule, q, k, v, beta, lam, S0=None, x_prev=None, phi="l2",
         _RULES2[rule], BH, T, m, dv, _PHIS[phi], _RIDGES[ridge], eps, eps_gamma, _ptr(q), _ptr(k),
         _ptr(v), _ptr(beta), _ptr(lam), _ptr(S0), _ptr(x_prev), _ptr(o), _ptr(S),
         _ptr(x_last), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (rc={rc})")
+    return {"o": o, "S": S, "x_last": x_last}
+
+
+def forward3a(q, k, v, beta, lam, window, S0=None, phi="l2", eps=1e-6, eps_gamma=1e-6,
+              threads=None, ridge="given"):
+    """Falcon-3A (sliding window of ``window`` write pairs) over whole fresh
+    sequences; shapes as ``forward`` (no x_prev: the window does not reach
+    into a previous segment).  Returns a dict with o, S and x_last."""
+    lib = _load()
+    q, k, v, beta, lam = (_f64(t) for t in (q, k, v, beta, lam))
+    S0 = _f64(S0)
+    lead = q.shape[:-2]
+    T, m = q.shape[-2], q.shape[-1]
+    dv = v.shape[-1]
+    BH = int(np.prod(lead)) if lead else 1
+    assert k.shape == q.shape and v.shape == lead + (T, dv)
+    assert beta.shape == lead + (T,) and lam.shape == lead + (T,)
+    if S0 is not None:
+        assert S0.shape == lead + (m, dv)
+    o = np.zeros(lead + (T, dv))
+    S = np.zeros(lead + (m, dv))
+    x_last = np.zeros(lead + (m,))
+    nthreads = threads or os.cpu_count() or 1
+    rc = lib.falcon3a_oracle_forward(
+        BH, T, m, dv, _PHIS[phi], _RIDGES[ridge], int(window), eps, eps_gamma, _ptr(q), _ptr(k),
+        _ptr(v), _ptr(beta), _ptr(lam), _ptr(S0), _ptr(o), _ptr(S), _ptr(x_last), int(nthreads))
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (rc={rc})")
     return {"o": o, "S": S, "x_last": x_last}

@@ -32,6 +32,9 @@
  *     lambda_t + eps), S_t = S_{t-1}(I - lambda_t Diag(eta_t)) +
  *     x_t (eta_t o r_t)^T): Section 3.1, the regression-family display and
  *     the "Per-column NLMS step sizes" paragraph of Section 4.2;
+ *   - Falcon-3A (sliding-window inner product, window of B pairs): Section
+ *     4.5, the windowed loss, N_bar and E_bar, the step size with E_t^{(B)}
+ *     = E_bar, and S_t = (1 - eta_t lambda_t) S_{t-1} + eta_t N_bar_t;
  *   - Falcon-2A (the same with r_t replaced by y_t = v_t, E_t = ||x_t||^2):
  *     Section 4.3, "Falcon-2A: per-column inner-product write" and the
  *     Falcon-1A/Falcon-2A step sizes; the clamp acts per column (the
@@ -357,6 +360,110 @@ int falcon2_oracle_forward(int rule, int64_t BH, int64_t T, int m, int dv, int p
   }
   for (int w = 1; w < nthreads; ++w) pthread_create(&tid[w], NULL, forward2_worker, &sl[w]);
   forward2_worker(&sl[0]);
+  for (int w = 1; w < nthreads; ++w) pthread_join(tid[w], NULL);
+  free(tid);
+  free(sl);
+  return 0;
+}
+
+/*
+ * Falcon-3A over whole fresh sequences (Section 4.5): for t >= 2 the window
+ * I_t = {max(2, t - B + 1), ..., t} of write pairs (x_j, v_j), B_t = |I_t|,
+ *   N_bar_t = (1/B_t) sum_{j in I_t} x_j v_j^T,  E_bar_t = (1/B_t) sum ||x_j||^2,
+ *   eta_t = beta_t / (E_bar_t + lambda_t + eps)  (lambda_t = lambda_bar_t *
+ *   E_bar_t with the scale-coupled ridge), alpha_t = min(eta_t lambda_t,
+ *   1 - eps_gamma), S_t = (1 - alpha_t) S_{t-1} + eta_t N_bar_t;
+ * t = 1 is the boundary (no update).  o_t = S_t^T phi(q_t).  The window
+ * reaches back only within the call (a fresh sequence: x_1 = 0).
+ * Layouts as falcon_oracle_forward (beta, lambda: [BH, T]); no x_prev.
+ */
+typedef struct {
+  int m, dv, phi, ridge, B;
+  int64_t T;
+  double eps, eps_gamma;
+  const double *q, *k, *v, *beta, *lambda, *S0;
+  double *o, *S_out, *x_last;
+} fwd3_args;
+
+static void forward3a_head(const fwd3_args *a, int64_t bh) {
+  const int m = a->m, dv = a->dv;
+  const int64_t T = a->T;
+  double *S = (double *)calloc((size_t)m * dv, sizeof(double));
+  double *X = (double *)calloc((size_t)(T > 0 ? T : 1) * m, sizeof(double)); /* x_t, t = 1..T */
+  double *qf = (double *)malloc(sizeof(double) * (size_t)m);
+  double *N = (double *)malloc(sizeof(double) * (size_t)m * dv);
+  if (a->S0) memcpy(S, a->S0 + bh * m * dv, sizeof(double) * (size_t)m * dv);
+  /* write features: x_1 = 0, x_t = phi(k_{t-1}) */
+  for (int64_t t = 1; t < T; ++t) feature_map(a->phi, m, a->k + (bh * T + t - 1) * m, X + t * m);
+  for (int64_t t = 0; t < T; ++t) { /* t is 0-based: token t + 1 */
+    const int64_t row = bh * T + t;
+    if (t >= 1) {
+      const int64_t j0 = (t - a->B + 1 > 1) ? t - a->B + 1 : 1; /* 0-based window start (>= token 2) */
+      const int64_t Bt = t - j0 + 1;
+      double Ebar = 0.0;
+      memset(N, 0, sizeof(double) * (size_t)m * dv);
+      for (int64_t j = j0; j <= t; ++j) {
+        const double *xj = X + j * m, *vj = a->v + (bh * T + j) * dv;
+        for (int i = 0; i < m; ++i) {
+          Ebar += xj[i] * xj[i];
+          for (int c = 0; c < dv; ++c) N[(int64_t)i * dv + c] += xj[i] * vj[c];
+        }
+      }
+      Ebar /= (double)Bt;
+      double lambda = a->lambda[row];
+      if (a->ridge == ORACLE_RIDGE_SCALED) lambda *= Ebar;
+      const double den = Ebar + lambda + a->eps;
+      const double eta = den > 0.0 ? a->beta[row] / den : 0.0;
+      double alpha = eta * lambda;
+      if (alpha > 1.0 - a->eps_gamma) alpha = 1.0 - a->eps_gamma;
+      for (int64_t e = 0; e < (int64_t)m * dv; ++e)
+        S[e] = (1.0 - alpha) * S[e] + eta * N[e] / (double)Bt;
+    }
+    feature_map(a->phi, m, a->q + row * m, qf);
+    for (int c = 0; c < dv; ++c) {
+      double acc = 0.0;
+      for (int i = 0; i < m; ++i) acc += S[(int64_t)i * dv + c] * qf[i];
+      a->o[row * dv + c] = acc;
+    }
+  }
+  if (a->S_out) memcpy(a->S_out + bh * m * dv, S, sizeof(double) * (size_t)m * dv);
+  if (a->x_last && T > 0) feature_map(a->phi, m, a->k + (bh * T + T - 1) * m, a->x_last + bh * m);
+  free(S);
+  free(X);
+  free(qf);
+  free(N);
+}
+
+typedef struct {
+  const fwd3_args *a;
+  int64_t begin, end;
+} fwd3_slice;
+
+static void *forward3a_worker(void *p) {
+  const fwd3_slice *s = (const fwd3_slice *)p;
+  for (int64_t bh = s->begin; bh < s->end; ++bh) forward3a_head(s->a, bh);
+  return NULL;
+}
+
+int falcon3a_oracle_forward(int64_t BH, int64_t T, int m, int dv, int phi, int ridge, int B,
+                            double eps, double eps_gamma, const double *q, const double *k,
+                            const double *v, const double *beta, const double *lambda,
+                            const double *S0, double *o, double *S_out, double *x_last,
+                            int nthreads) {
+  if (BH < 0 || T < 0 || m <= 0 || dv <= 0 || B < 1) return -1;
+  fwd3_args a = {m, dv, phi, ridge, B, T, eps, eps_gamma, q, k, v, beta, lambda, S0,
+                 o, S_out, x_last};
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > BH) nthreads = (int)(BH > 0 ? BH : 1);
+  pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+  fwd3_slice *sl = (fwd3_slice *)malloc(sizeof(fwd3_slice) * (size_t)nthreads);
+  for (int w = 0; w < nthreads; ++w) {
+    sl[w].a = &a;
+    sl[w].begin = BH * w / nthreads;
+    sl[w].end = BH * (w + 1) / nthreads;
+  }
+  for (int w = 1; w < nthreads; ++w) pthread_create(&tid[w], NULL, forward3a_worker, &sl[w]);
+  forward3a_worker(&sl[0]);
   for (int w = 1; w < nthreads; ++w) pthread_join(tid[w], NULL);
   free(tid);
   free(sl);
