@@ -380,11 +380,16 @@ def extra_workloads(falcon, dev):
     out = []
     pk = peaks()
     for w, steps in ((workloads.LM_1A, 200), (workloads.LONG, 5), (workloads.LM_2, 20),
-                     (workloads.LM_2A, 20)):
+                     (workloads.LM_2A, 20), (workloads.LM_3A, 20)):
         sets = input_sets(w, 1 if w is workloads.LONG else 2, dev)
         o = torch.empty((w.B, w.H, w.T, w.dv), dtype=w.dtype, device=dev)
         S = torch.empty((w.B, w.H, w.m, w.dv), dtype=torch.float32, device=dev)
-        if w.per_column:
+        if w.rule == "falcon3a":
+            def step(x):
+                falcon.falcon3a_fwd_recurrent(x["q"], x["k"], x["v"], x["beta"], x["lambda"],
+                                              workloads.LM_3A_WINDOW, phi=w.phi, o=o, S_out=S,
+                                              want_x_last=False)
+        elif w.per_column:
             fn2 = {"falcon2": falcon.falcon2_fwd_recurrent,
                    "falcon2a": falcon.falcon2a_fwd_recurrent}[w.rule]
 
@@ -506,12 +511,15 @@ def run_profile(args):
         name, size = d.name, d.N
     else:
         w = {"lm": workloads.LM, "lm1a": workloads.LM_1A, "long": workloads.LONG,
-             "lm2": workloads.LM_2, "lm2a": workloads.LM_2A}[args.profile]
+             "lm2": workloads.LM_2, "lm2a": workloads.LM_2A, "lm3a": workloads.LM_3A}[args.profile]
         if args.profile_size:
             w = dataclasses.replace(w, T=args.profile_size)
         x = workloads.generate(w, device=dev)
         for _ in range(calls):
-            if w.per_column:
+            if w.rule == "falcon3a":
+                falcon.falcon3a_fwd_recurrent(x["q"], x["k"], x["v"], x["beta"], x["lambda"],
+                                              workloads.LM_3A_WINDOW, phi=w.phi)
+            elif w.per_column:
                 fn2 = (falcon.falcon2_fwd_recurrent if w.rule == "falcon2"
                        else falcon.falcon2a_fwd_recurrent)
                 fn2(x["q"], x["k"], x["v"], x["beta"], x["lambda"], phi=w.phi)
@@ -534,8 +542,8 @@ def main():
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
-    ap.add_argument("--profile", choices=["lm", "lm1a", "long", "decode", "lm2", "lm2a"],
-                    default=None,
+    ap.add_argument("--profile",
+                    choices=["lm", "lm1a", "long", "decode", "lm2", "lm2a", "lm3a"], default=None,
                     help="profiler target: run --steps calls of one workload, print no timing")
     ap.add_argument("--profile-size", type=int, default=None,
                     help="with --profile: tokens per head (chunked) or states (decode)")

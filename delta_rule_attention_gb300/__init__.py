@@ -37,6 +37,7 @@ EXPORTS = (
     "falcon1_decode_step", "falcon1a_decode_step", "falcon_sync_check",
     "falcon_strerror", "falcon_version", "falcon1_fwd_chunked_fixed_scratch",
     "falcon_selftest_wait_timeout", "falcon2_fwd_recurrent", "falcon2a_fwd_recurrent",
+    "falcon3a_fwd_recurrent",
 )
 FALCON_ERR_SCRATCH_LIMIT = -10
 FALCON_FIXED_SCRATCH_BYTES = 16 * 1024 * 1024
@@ -89,6 +90,9 @@ def load_library(path: str | None = None):
             fn = getattr(lib, name)
             fn.restype = ctypes.c_int
             fn.argtypes = [shp, vp, vp, vp, f32p, f32p, f32p, f32p, vp, f32p, f32p, vp]
+        lib.falcon3a_fwd_recurrent.restype = ctypes.c_int
+        lib.falcon3a_fwd_recurrent.argtypes = [shp, i32, vp, vp, vp, f32p, f32p, f32p, vp, f32p,
+                                               f32p, vp]
         lib.falcon1_fwd_chunked_fixed_scratch.restype = ctypes.c_int
         lib.falcon1_fwd_chunked_fixed_scratch.argtypes = [shp, vp, vp, vp, f32p, f32p, f32p,
                                                           f32p, vp, f32p, f32p, vp]
@@ -292,6 +296,40 @@ def falcon2a_fwd_recurrent(q, k, v, beta, lam, S0=None, x_prev=None, phi="l2", e
     falcon2_fwd_recurrent."""
     return _fwd2("falcon2a_fwd_recurrent", q, k, v, beta, lam, S0, x_prev, phi, eps, eps_gamma,
                  **kw)
+
+
+def falcon3a_fwd_recurrent(q, k, v, beta, lam, window, S0=None, phi="l2", eps=1e-6,
+                           eps_gamma=1e-6, o=None, S_out=None, x_last=None, stream=None,
+                           want_x_last=True, ridge="given"):
+    """Falcon-3A forward (sliding window of ``window`` write pairs, 1..32) over
+    fresh sequences.  q, k [B,H,T,m], v [B,H,T,dv] (bf16 or fp32), beta, lam
+    [B,H,T] fp32; S0 [B,H,m,dv] fp32 or None.  Returns (o, S_T, x_last)."""
+    lib = load_library()
+    _need(q, "q")
+    B, H, T, m = q.shape
+    dv = v.shape[-1]
+    dt = q.dtype
+    if dt not in _DTYPE:
+        raise TypeError("q, k, v must be bfloat16 or float32")
+    _need(k, "k", dt, (B, H, T, m))
+    _need(v, "v", dt, (B, H, T, dv))
+    _need(beta, "beta", torch.float32, (B, H, T))
+    _need(lam, "lambda", torch.float32, (B, H, T))
+    if S0 is not None:
+        _need(S0, "S0", torch.float32, (B, H, m, dv))
+    dev = q.device
+    if o is None:
+        o = torch.empty((B, H, T, dv), dtype=dt, device=dev)
+    if S_out is None:
+        S_out = torch.empty((B, H, m, dv), dtype=torch.float32, device=dev)
+    if x_last is None and want_x_last:
+        x_last = torch.empty((B, H, m), dtype=torch.float32, device=dev)
+    shape = make_shape(B, H, T, m, dv, 64, dt, phi, eps, eps_gamma, ridge)
+    rc = lib.falcon3a_fwd_recurrent(ctypes.byref(shape), int(window), _ptr(q), _ptr(k), _ptr(v),
+                                    _ptr(beta), _ptr(lam), _ptr(S0), _ptr(o), _ptr(S_out),
+                                    _ptr(x_last), _stream(stream))
+    _check(rc, "falcon3a_fwd_recurrent")
+    return o, S_out, x_last
 
 
 def _decode(name, q, k, v, beta, lam, S, x_prev, fresh=None, phi="l2", eps=1e-6,

@@ -77,7 +77,7 @@ int* device_error_word() {
 int fwd_chunked(int rule, const falcon_shape* s, const void* q, const void* k, const void* v,
                 const float* beta, const float* lambda, const float* S0, const float* x_prev,
                 void* o, float* S_out, float* x_last, void* workspace, size_t workspace_bytes,
-                cudaStream_t stream) {
+                cudaStream_t stream, int window = 1) {
   int rc = check_shape(s);
   if (rc) return rc;
   const int64_t BH = s->B * s->H;
@@ -87,9 +87,13 @@ int fwd_chunked(int rule, const falcon_shape* s, const void* q, const void* k, c
   const void* ptrs[] = {q, k, v, beta, lambda, S0, x_prev, o, S_out, x_last};
   for (const void* p : ptrs)
     if (misaligned(p)) return FALCON_ERR_MISALIGNED;
-  // The per-column rules run in the token-recurrent form: no workspace.
+  // The per-column and windowed rules run in the token-recurrent form: no
+  // workspace.  The window of Falcon-3A holds at most 32 pairs and does not
+  // reach into a previous segment (no x_prev).
   const bool per_column = rule == falcon::kFalcon2 || rule == falcon::kFalcon2A;
-  const size_t need = per_column ? 0 : falcon_workspace_bytes(s);
+  const bool windowed = rule == falcon::kFalcon3A;
+  if (windowed && (window < 1 || window > 32 || x_prev)) return FALCON_ERR_BAD_ARG;
+  const size_t need = (per_column || windowed) ? 0 : falcon_workspace_bytes(s);
   if (need > 0 && (!workspace || workspace_bytes < need)) return FALCON_ERR_WORKSPACE;
   if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return FALCON_ERR_MISALIGNED;
   rc = check_device();
@@ -130,10 +134,11 @@ int fwd_chunked(int rule, const falcon_shape* s, const void* q, const void* k, c
   a.S_out = S_out;
   a.x_last = x_last;
   a.workspace = workspace;
-  if (per_column) {
+  if (per_column || windowed) {
     int* err = device_error_word();
     if (!err) return FALCON_ERR_CUDA;
-    return to_status(falcon::launch_falcon2_recurrent(a, err, stream));
+    return to_status(windowed ? falcon::launch_falcon3a_recurrent(a, window, err, stream)
+                              : falcon::launch_falcon2_recurrent(a, err, stream));
   }
   if (falcon::tc_path_applies(s->dtype, s->m, s->dv, s->chunk, s->B * s->H, s->T)) {
     int* err = device_error_word();
@@ -235,6 +240,14 @@ int falcon2a_fwd_recurrent(const falcon_shape* s, const void* q, const void* k, 
                            cudaStream_t stream) {
   return fwd_chunked(falcon::kFalcon2A, s, q, k, v, beta, lambda, S0, x_prev, o, S_out, x_last,
                      nullptr, 0, stream);
+}
+
+int falcon3a_fwd_recurrent(const falcon_shape* s, int32_t window, const void* q, const void* k,
+                           const void* v, const float* beta, const float* lambda,
+                           const float* S0, void* o, float* S_out, float* x_last,
+                           cudaStream_t stream) {
+  return fwd_chunked(falcon::kFalcon3A, s, q, k, v, beta, lambda, S0, nullptr, o, S_out, x_last,
+                     nullptr, 0, stream, window);
 }
 
 int falcon1_decode_step(int64_t N, int32_t m, int32_t dv, int32_t dtype, int32_t phi,

@@ -12,7 +12,7 @@ namespace falcon {
 // Rule selector shared by kernels: Falcon-1 writes the residual
 // r_t = v_t - S_{t-1}^T x_t, Falcon-1A writes the target v_t; Falcon-2 and
 // Falcon-2A are their per-column counterparts (one step size per column).
-enum Rule : int { kFalcon1 = 1, kFalcon1A = 2, kFalcon2 = 3, kFalcon2A = 4 };
+enum Rule : int { kFalcon1 = 1, kFalcon1A = 2, kFalcon2 = 3, kFalcon2A = 4, kFalcon3A = 5 };
 
 __device__ __forceinline__ float load_elem(const void* p, int64_t i, int dtype) {
   if (dtype == FALCON_BF16)
@@ -93,6 +93,10 @@ cudaError_t launch_generic_chunked(const ChunkArgs& a, cudaStream_t stream);
 // Falcon-2 / Falcon-2A, token-recurrent form (rule kFalcon2 or kFalcon2A;
 // beta is [B*H, T, dv]: one gain per column and token).
 cudaError_t launch_falcon2_recurrent(const ChunkArgs& a, int* err, cudaStream_t stream);
+
+// Falcon-3A, token-recurrent form over fresh sequences, window 1 .. 32 pairs.
+cudaError_t launch_falcon3a_recurrent(const ChunkArgs& a, int window, int* err,
+                                      cudaStream_t stream);
 
 // Tensor-core path (bf16, m = dv in {64, 128}, chunk = 64).
 bool tc_path_applies(int dtype, int m, int dv, int C, int64_t BH, int64_t T);

@@ -15,7 +15,7 @@ normals, all in float32 row-major [B, H, T, .] from one torch.Generator seeded
 with the workload's seed; q, k, v are then rounded to the workload dtype.  The
 per-column workloads (Falcon-2, Falcon-2A) draw one beta normal per value
 column, [B, H, T, d_v], in the same place of the order.
-Workloads small enough for the host (tiny, lm, lm-1A, lm-2, lm-2A) draw on the CPU
+Workloads small enough for the host (tiny, lm, lm-1A, lm-2, lm-2A, lm-3A) draw on the CPU
 generator, so they are the same on every machine; the long-context and decode
 workloads (hundreds of millions of draws) draw on the device's generator.
 """
@@ -64,7 +64,12 @@ LM_2 = Workload("falcon2_lm_B8H12T2048_d64_bf16", "falcon2", 8, 12, 2048, 64, 64
                 "l2", 64, -3.0, 5, per_column=True)
 LM_2A = Workload("falcon2a_lm_B8H12T2048_d64_bf16", "falcon2a", 8, 12, 2048, 64, 64,
                  torch.bfloat16, "l2", 64, -3.0, 6, per_column=True)
-WORKLOADS = {w.name: w for w in (TINY, LM, LM_1A, LONG, LM_2, LM_2A)}
+# Falcon-3A (sliding window of 4 write pairs: the pages give no window for
+# their runs; 4 is the reading taken) on the lm shape.
+LM_3A = Workload("falcon3a_lm_B8H12T2048_d64_bf16_w4", "falcon3a", 8, 12, 2048, 64, 64,
+                 torch.bfloat16, "l2", 64, -3.0, 7)
+LM_3A_WINDOW = 4
+WORKLOADS = {w.name: w for w in (TINY, LM, LM_1A, LONG, LM_2, LM_2A, LM_3A)}
 
 
 @dataclass(frozen=True)

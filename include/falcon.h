@@ -1,8 +1,9 @@
 /*
  * falcon.h -- C ABI of the GB300 (sm_103a) Falcon fast-weight attention
  * library: chunk-parallel forward of Falcon-1 and Falcon-1A, the
- * token-recurrent forward of Falcon-2 and Falcon-2A (per-column step sizes),
- * and the single-token recurrent decode step.
+ * token-recurrent forward of Falcon-2 and Falcon-2A (per-column step sizes)
+ * and of Falcon-3A (sliding window), and the single-token recurrent decode
+ * step.
  *
  * The operations are defined on the page hyper.ai/fr/papers/2608.27763
  * ("Fast Weight Attention for Continual Learning"):
@@ -205,6 +206,25 @@ int falcon2a_fwd_recurrent(const falcon_shape *shape, const void *q,
                            const void *k, const void *v, const float *beta,
                            const float *lambda, const float *S0,
                            const float *x_prev, void *o, float *S_out,
+                           float *x_last, cudaStream_t stream);
+
+/* Falcon-3A forward, the sliding-window inner-product rule (Section 4.5),
+ * token-recurrent form, for fresh sequences:
+ *   for t >= 2 the window I_t of the last `window` write pairs (x_j, v_j),
+ *   j >= 2, B_t = |I_t|: N_bar_t = (1/B_t) sum x_j v_j^T, E_bar_t =
+ *   (1/B_t) sum ||x_j||^2, eta_t = beta_t / (E_bar_t + lambda_t + eps)
+ *   (lambda_t = lambda_bar_t * E_bar_t with FALCON_RIDGE_SCALED), gamma_t =
+ *   1 - min(eta_t lambda_t, 1 - eps_gamma), S_t = gamma_t S_{t-1} +
+ *   eta_t N_bar_t; token 1 is the boundary (no update); o_t = S_t^T phi(q_t).
+ *   window  1 .. 32 (window 1 is Falcon-1A); FALCON_ERR_BAD_ARG otherwise.
+ * Arguments, layouts, ownership and errors are those of falcon1_fwd_chunked
+ * except: no x_prev (the window does not reach into a previous segment: exact
+ * continuation would need the last window - 1 pairs), no workspace, and
+ * shape->chunk is checked but not used. */
+int falcon3a_fwd_recurrent(const falcon_shape *shape, int32_t window,
+                           const void *q, const void *k, const void *v,
+                           const float *beta, const float *lambda,
+                           const float *S0, void *o, float *S_out,
                            float *x_last, cudaStream_t stream);
 
 /* One recurrent token (read after write) for N independent states: the
