@@ -1,4 +1,5 @@
-"""fp64 CPU oracle for the Falcon-1 / Falcon-1A, Falcon-2 / Falcon-2A and Falcon-3A recurrences.
+"""fp64 CPU oracle for the Falcon-1 / Falcon-1A, Falcon-2 / Falcon-2A and Falcon-3A recurrences,
+and the backward pass of Falcon-1 / Falcon-1A.
 
 TEST INFRASTRUCTURE ONLY.  Nothing in the library path imports this package:
 only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline legs of
@@ -68,6 +69,10 @@ def _load():
             lib.falcon3a_oracle_forward.argtypes = [
                 i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_double, ctypes.c_double, d, d, d, d, d, d, d, d, d, ctypes.c_int]
+            lib.falcon_oracle_backward.restype = ctypes.c_int
+            lib.falcon_oracle_backward.argtypes = [
+                ctypes.c_int, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_double, ctypes.c_double] + [d] * 17 + [ctypes.c_int]
             lib.falcon_oracle_decode_step.restype = ctypes.c_int
             lib.falcon_oracle_decode_step.argtypes = [
                 ctypes.c_int, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -131,6 +136,43 @@ def forward(rule, q, k, v, beta, lam, S0=None, x_prev=None, phi="l2",
     out = {"o": o, "S": S, "x_last": x_last}
     if trajectory:
         out["S_traj"] = traj
+    return out
+
+
+def backward(rule, q, k, v, beta, lam, dO, S0=None, x_prev=None, dS_T=None, dx_last=None,
+             phi="l2", eps=1e-6, eps_gamma=1e-6, threads=None, ridge="given"):
+    """Gradients of L = <dO, o> + <dS_T, S_T> + <dx_last, x_last> through the
+    Falcon-1 / Falcon-1A recurrence (reverse mode, token by token, fp64).
+
+    Shapes as ``forward``; dO [..., T, dv]; dS_T [..., m, dv] and dx_last
+    [..., m] may be None (zero cotangents).  Returns a dict with dq, dk
+    [..., T, m], dv [..., T, dv], dbeta, dlambda [..., T] (dlambda is the
+    gradient for the lam input: the base ridge when ridge="scaled"), dS0
+    [..., m, dv] and dx_prev [..., m] (zeros for a fresh sequence).
+    """
+    lib = _load()
+    q, k, v, beta, lam, dO = (_f64(t) for t in (q, k, v, beta, lam, dO))
+    S0, x_prev, dS_T, dx_last = (_f64(t) for t in (S0, x_prev, dS_T, dx_last))
+    lead = q.shape[:-2]
+    T, m = q.shape[-2], q.shape[-1]
+    dv = v.shape[-1]
+    BH = int(np.prod(lead)) if lead else 1
+    assert k.shape == q.shape and v.shape == lead + (T, dv) and dO.shape == v.shape
+    assert beta.shape == lead + (T,) and lam.shape == lead + (T,)
+    for t, shp in ((S0, (m, dv)), (dS_T, (m, dv)), (x_prev, (m,)), (dx_last, (m,))):
+        if t is not None:
+            assert t.shape == lead + shp
+    out = {"dq": np.zeros(q.shape), "dk": np.zeros(q.shape), "dv": np.zeros(v.shape),
+           "dbeta": np.zeros(beta.shape), "dlambda": np.zeros(beta.shape),
+           "dS0": np.zeros(lead + (m, dv)), "dx_prev": np.zeros(lead + (m,))}
+    nthreads = threads or os.cpu_count() or 1
+    rc = lib.falcon_oracle_backward(
+        _RULES[rule], BH, T, m, dv, _PHIS[phi], _RIDGES[ridge], eps, eps_gamma, _ptr(q), _ptr(k),
+        _ptr(v), _ptr(beta), _ptr(lam), _ptr(S0), _ptr(x_prev), _ptr(dO), _ptr(dS_T),
+        _ptr(dx_last), _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dbeta"]),
+        _ptr(out["dlambda"]), _ptr(out["dS0"]), _ptr(out["dx_prev"]), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (rc={rc})")
     return out
 
 

@@ -469,3 +469,267 @@ int falcon3a_oracle_forward(int64_t BH, int64_t T, int m, int dv, int phi, int r
   free(sl);
   return 0;
 }
+
+/* ------------------------------------------------------------------------
+ * Backward pass of Falcon-1 / Falcon-1A: reverse-mode differentiation of the
+ * token recurrence above, in fp64.
+ *
+ * The pages state that training differentiates through the update, so that
+ * the slow weights producing q, k, v, beta and lambda learn (page
+ * hyper.ai/fr/papers/2608.27763, Section 3, "Implicit fast-memory
+ * objective"), and that the backward pass differentiates through the
+ * log-decay renormalisation and the normalised step size (Section 4.6,
+ * "Backward pass"; its appendix is not on the pages).  Nothing else is given,
+ * so this is the gradient of the forward function as written above, taken by
+ * the chain rule one token at a time, newest token first:
+ *
+ *   o_t = S_t^T qf_t                 dS_t += qf_t do_t^T,  dqf_t = S_t do_t
+ *   S_t = gamma S_{t-1} + eta x r^T  dgamma = <dS_t, S_{t-1}>,
+ *                                    deta = x^T dS_t r,  dx = eta dS_t r,
+ *                                    dr = eta dS_t^T x,  dS_{t-1} = gamma dS_t
+ *   r = v - S_{t-1}^T x (Falcon-1)   dv = dr,  dS_{t-1} -= x dr^T,
+ *                                    dx -= S_{t-1} dr
+ *   r = v (Falcon-1A)                dv = dr
+ *   gamma = 1 - alpha, alpha = min(eta lambda, 1 - eps_gamma):
+ *       on the clamped branch alpha is a constant; otherwise
+ *       deta += lambda dalpha, dlambda += eta dalpha with dalpha = -dgamma
+ *   eta = beta / (E + lambda + eps): dbeta = deta / den,
+ *       dE = dlambda_den = -deta eta / den  (eta := 0, a constant, if den <= 0)
+ *   lambda_t = lambda_bar E (scaled ridge): dlambda_bar = dlambda E,
+ *       dE += dlambda lambda_bar
+ *   E = ||x||^2: dx += 2 dE x
+ *   x_t = phi(k_{t-1}): dk_{t-1} = J_phi(k_{t-1})^T dx_t; x_1 = x_prev or
+ *       the sentinel zero (no gradient); qf_t = phi(q_t): dq_t = J_phi^T dqf_t
+ * The sentinel token (eta = 0, gamma = 1) passes no gradient to beta_1,
+ * lambda_1.  At the clamp's kink (eta lambda = 1 - eps_gamma exactly) the
+ * unclamped branch is taken, as in the forward.
+ * ------------------------------------------------------------------------ */
+
+/* J_phi(u)^T g for the feature maps of feature_map(). */
+static void feature_map_vjp(int phi, int m, const double *u, const double *g, double *out) {
+  if (phi == ORACLE_PHI_RMS) {
+    /* phi = u s, s = (||u||^2/m + eps)^(-1/2): d phi_i / d u_j = s delta_ij - s^3 u_i u_j / m */
+    double ss = 0.0, ug = 0.0;
+    for (int i = 0; i < m; ++i) {
+      ss += u[i] * u[i];
+      ug += u[i] * g[i];
+    }
+    const double s = 1.0 / sqrt(ss / m + ORACLE_EPS_RMS);
+    for (int i = 0; i < m; ++i) out[i] = s * g[i] - s * s * s * u[i] * ug / m;
+  } else if (phi == ORACLE_PHI_L2) {
+    /* phi = u / n, n = ||u|| (> 1e-12): d phi_i / d u_j = (delta_ij - phi_i phi_j) / n */
+    double ss = 0.0;
+    for (int i = 0; i < m; ++i) ss += u[i] * u[i];
+    const double n = sqrt(ss);
+    if (n < 1e-12) {
+      for (int i = 0; i < m; ++i) out[i] = g[i] / 1e-12;
+    } else {
+      double pg = 0.0;
+      for (int i = 0; i < m; ++i) pg += u[i] / n * g[i];
+      for (int i = 0; i < m; ++i) out[i] = (g[i] - u[i] / n * pg) / n;
+    }
+  } else {
+    for (int i = 0; i < m; ++i) out[i] = g[i];
+  }
+}
+
+typedef struct {
+  int rule, m, dv, phi, ridge;
+  int64_t T;
+  double eps, eps_gamma;
+  const double *q, *k, *v, *beta, *lambda, *S0, *x_prev;
+  const double *dO, *dS_T, *dx_last;
+  double *dq, *dk, *dvv, *dbeta, *dlambda, *dS0, *dx_prev;
+} bwd_args;
+
+static void backward_head(const bwd_args *a, int64_t bh) {
+  const int m = a->m, dv = a->dv;
+  const int64_t T = a->T;
+  const size_t md = (size_t)m * dv;
+  /* forward, keeping every pre-update state S_{t-1} and write feature x_t */
+  double *Spre = (double *)malloc(sizeof(double) * md * (size_t)(T > 0 ? T : 1));
+  double *X = (double *)calloc((size_t)(T + 1) * m, sizeof(double));
+  double *S = (double *)calloc(md, sizeof(double));
+  double *qf = (double *)malloc(sizeof(double) * (size_t)m);
+  double *r = (double *)malloc(sizeof(double) * (size_t)dv);
+  double *o = (double *)malloc(sizeof(double) * (size_t)dv);
+  if (a->S0) memcpy(S, a->S0 + bh * md, sizeof(double) * md);
+  const int fresh = a->x_prev == NULL;
+  if (!fresh) memcpy(X, a->x_prev + bh * m, sizeof(double) * (size_t)m);
+  for (int64_t t = 0; t < T; ++t) {
+    const int64_t row = bh * T + t;
+    double eta, gamma;
+    step_scalars(fresh && t == 0, m, X + t * m, a->beta[row], a->lambda[row], a->ridge, a->eps,
+                 a->eps_gamma, &eta, &gamma);
+    memcpy(Spre + (size_t)t * md, S, sizeof(double) * md);
+    feature_map(a->phi, m, a->q + row * m, qf);
+    one_token(a->rule, m, dv, S, X + t * m, qf, a->v + row * dv, eta, gamma, r, o);
+    feature_map(a->phi, m, a->k + row * m, X + (t + 1) * m);
+  }
+  /* S now holds S_T; walk back */
+  double *dS = (double *)calloc(md, sizeof(double));
+  double *Spost = (double *)malloc(sizeof(double) * md);
+  double *dx = (double *)malloc(sizeof(double) * (size_t)m);
+  double *dxn = (double *)calloc((size_t)m, sizeof(double)); /* d x_{t+1} */
+  double *dr = (double *)malloc(sizeof(double) * (size_t)dv);
+  double *dqf = (double *)malloc(sizeof(double) * (size_t)m);
+  if (a->dS_T) memcpy(dS, a->dS_T + bh * md, sizeof(double) * md);
+  if (a->dx_last) memcpy(dxn, a->dx_last + bh * m, sizeof(double) * (size_t)m);
+  memcpy(Spost, S, sizeof(double) * md);
+  for (int64_t t = T - 1; t >= 0; --t) {
+    const int64_t row = bh * T + t;
+    const double *x = X + t * m;
+    const double *Sp = Spre + (size_t)t * md;
+    /* x_{t+1} = phi(k_t) */
+    feature_map_vjp(a->phi, m, a->k + row * m, dxn, a->dk + row * m);
+    /* scalars of this token, as the forward computed them */
+    const int sentinel = fresh && t == 0;
+    double E = 0.0;
+    for (int i = 0; i < m; ++i) E += x[i] * x[i];
+    const double lam_in = a->lambda[row];
+    const double lam = (a->ridge == ORACLE_RIDGE_SCALED) ? lam_in * E : lam_in;
+    double eta = 0.0, den = E + lam + a->eps;
+    if (!sentinel && den > 0.0) eta = a->beta[row] / den;
+    const int clamped = eta * lam > 1.0 - a->eps_gamma;
+    const double gamma = 1.0 - (clamped ? 1.0 - a->eps_gamma : eta * lam);
+    /* r from the pre-update state */
+    for (int j = 0; j < dv; ++j) {
+      double pred = 0.0;
+      if (a->rule == ORACLE_FALCON1)
+        for (int i = 0; i < m; ++i) pred += Sp[(size_t)i * dv + j] * x[i];
+      r[j] = a->v[row * dv + j] - pred;
+    }
+    /* read: o_t = S_t^T qf */
+    feature_map(a->phi, m, a->q + row * m, qf);
+    const double *dot = a->dO + row * dv;
+    for (int i = 0; i < m; ++i) {
+      double acc = 0.0;
+      for (int j = 0; j < dv; ++j) {
+        acc += Spost[(size_t)i * dv + j] * dot[j];
+        dS[(size_t)i * dv + j] += qf[i] * dot[j];
+      }
+      dqf[i] = acc;
+    }
+    feature_map_vjp(a->phi, m, a->q + row * m, dqf, a->dq + row * m);
+    /* write: S_t = gamma S_{t-1} + eta x r^T */
+    double dgamma = 0.0, deta = 0.0;
+    for (int i = 0; i < m; ++i) {
+      double dsr = 0.0;
+      for (int j = 0; j < dv; ++j) {
+        dgamma += dS[(size_t)i * dv + j] * Sp[(size_t)i * dv + j];
+        dsr += dS[(size_t)i * dv + j] * r[j];
+      }
+      deta += x[i] * dsr;
+      dx[i] = eta * dsr;
+    }
+    for (int j = 0; j < dv; ++j) {
+      double acc = 0.0;
+      for (int i = 0; i < m; ++i) acc += dS[(size_t)i * dv + j] * x[i];
+      dr[j] = eta * acc;
+      a->dvv[row * dv + j] = dr[j];
+    }
+    for (size_t e = 0; e < md; ++e) dS[e] *= gamma;
+    if (a->rule == ORACLE_FALCON1) {
+      for (int i = 0; i < m; ++i) {
+        double acc = 0.0;
+        for (int j = 0; j < dv; ++j) {
+          dS[(size_t)i * dv + j] -= x[i] * dr[j];
+          acc += Sp[(size_t)i * dv + j] * dr[j];
+        }
+        dx[i] -= acc;
+      }
+    }
+    /* step size and decay */
+    double dbeta = 0.0, dlam_in = 0.0;
+    if (!sentinel && den > 0.0) {
+      double dlam = 0.0;
+      if (!clamped) {
+        const double dalpha = -dgamma;
+        deta += lam * dalpha;
+        dlam += eta * dalpha;
+      }
+      dbeta = deta / den;
+      const double dden = -deta * eta / den;
+      double dE = dden;
+      dlam += dden;
+      if (a->ridge == ORACLE_RIDGE_SCALED) {
+        dlam_in = dlam * E;
+        dE += dlam * lam_in;
+      } else {
+        dlam_in = dlam;
+      }
+      for (int i = 0; i < m; ++i) dx[i] += 2.0 * dE * x[i];
+    }
+    a->dbeta[row] = dbeta;
+    a->dlambda[row] = dlam_in;
+    memcpy(dxn, dx, sizeof(double) * (size_t)m);
+    memcpy(Spost, Sp, sizeof(double) * md);
+  }
+  if (a->dS0) memcpy(a->dS0 + bh * md, dS, sizeof(double) * md);
+  if (a->dx_prev) {
+    if (fresh)
+      memset(a->dx_prev + bh * m, 0, sizeof(double) * (size_t)m);
+    else
+      memcpy(a->dx_prev + bh * m, dxn, sizeof(double) * (size_t)m);
+  }
+  free(Spre);
+  free(X);
+  free(S);
+  free(qf);
+  free(r);
+  free(o);
+  free(dS);
+  free(Spost);
+  free(dx);
+  free(dxn);
+  free(dr);
+  free(dqf);
+}
+
+typedef struct {
+  const bwd_args *a;
+  int64_t begin, end;
+} bwd_slice;
+
+static void *backward_worker(void *p) {
+  const bwd_slice *s = (const bwd_slice *)p;
+  for (int64_t bh = s->begin; bh < s->end; ++bh) backward_head(s->a, bh);
+  return NULL;
+}
+
+/*
+ * Gradients of L = <dO, o> + <dS_T, S_T> + <dx_last, x_last> with respect to
+ * every input of falcon_oracle_forward.  Layouts as there; dO [BH, T, dv];
+ * dS_T [BH, m, dv] and dx_last [BH, m] nullable (zero cotangents).  Outputs:
+ * dq, dk [BH, T, m], dv [BH, T, dv], dbeta, dlambda [BH, T] (dlambda is the
+ * gradient with respect to the lambda input: lambda_bar for the scaled
+ * ridge), dS0 [BH, m, dv] and dx_prev [BH, m] (nullable; dx_prev is zero for
+ * a fresh sequence).  Returns 0, or -1 on a bad argument.
+ */
+int falcon_oracle_backward(int rule, int64_t BH, int64_t T, int m, int dv, int phi, int ridge,
+                           double eps, double eps_gamma, const double *q, const double *k,
+                           const double *v, const double *beta, const double *lambda,
+                           const double *S0, const double *x_prev, const double *dO,
+                           const double *dS_T, const double *dx_last, double *dq, double *dk,
+                           double *dvv, double *dbeta, double *dlambda, double *dS0,
+                           double *dx_prev, int nthreads) {
+  if (rule != ORACLE_FALCON1 && rule != ORACLE_FALCON1A) return -1;
+  if (BH < 0 || T < 0 || m <= 0 || dv <= 0) return -1;
+  bwd_args a = {rule, m, dv, phi, ridge, T, eps, eps_gamma, q, k, v, beta, lambda, S0, x_prev,
+                dO, dS_T, dx_last, dq, dk, dvv, dbeta, dlambda, dS0, dx_prev};
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > BH) nthreads = (int)(BH > 0 ? BH : 1);
+  pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+  bwd_slice *sl = (bwd_slice *)malloc(sizeof(bwd_slice) * (size_t)nthreads);
+  for (int w = 0; w < nthreads; ++w) {
+    sl[w].a = &a;
+    sl[w].begin = BH * w / nthreads;
+    sl[w].end = BH * (w + 1) / nthreads;
+  }
+  for (int w = 1; w < nthreads; ++w) pthread_create(&tid[w], NULL, backward_worker, &sl[w]);
+  backward_worker(&sl[0]);
+  for (int w = 1; w < nthreads; ++w) pthread_join(tid[w], NULL);
+  free(tid);
+  free(sl);
+  return 0;
+}
