@@ -37,7 +37,8 @@ EXPORTS = (
     "falcon1_decode_step", "falcon1a_decode_step", "falcon_sync_check",
     "falcon_strerror", "falcon_version", "falcon1_fwd_chunked_fixed_scratch",
     "falcon_selftest_wait_timeout", "falcon2_fwd_recurrent", "falcon2a_fwd_recurrent",
-    "falcon3a_fwd_recurrent",
+    "falcon3a_fwd_recurrent", "falcon_bwd_workspace_bytes", "falcon1_bwd_chunked",
+    "falcon1a_bwd_chunked",
 )
 FALCON_ERR_SCRATCH_LIMIT = -10
 FALCON_FIXED_SCRATCH_BYTES = 16 * 1024 * 1024
@@ -81,6 +82,13 @@ def load_library(path: str | None = None):
             fn = getattr(lib, name)
             fn.restype = ctypes.c_int
             fn.argtypes = [shp, vp, vp, vp, f32p, f32p, f32p, f32p, vp, f32p, f32p, vp, sz, vp]
+        lib.falcon_bwd_workspace_bytes.restype = sz
+        lib.falcon_bwd_workspace_bytes.argtypes = [shp]
+        for name in ("falcon1_bwd_chunked", "falcon1a_bwd_chunked"):
+            fn = getattr(lib, name)
+            fn.restype = ctypes.c_int
+            fn.argtypes = [shp, vp, vp, vp, f32p, f32p, f32p, f32p, vp, f32p, f32p, vp, vp, vp,
+                           f32p, f32p, f32p, f32p, vp, sz, vp]
         for name in ("falcon1_decode_step", "falcon1a_decode_step"):
             fn = getattr(lib, name)
             fn.restype = ctypes.c_int
@@ -246,6 +254,69 @@ def falcon1a_fwd_chunked(q, k, v, beta, lam, S0=None, x_prev=None, chunk=64, phi
     """Falcon-1A chunk-parallel forward; arguments as falcon1_fwd_chunked."""
     return _fwd("falcon1a_fwd_chunked", q, k, v, beta, lam, S0, x_prev, chunk, phi, eps,
                 eps_gamma, **kw)
+
+
+def falcon_bwd_workspace_bytes(shape: falcon_shape) -> int:
+    return int(load_library().falcon_bwd_workspace_bytes(ctypes.byref(shape)))
+
+
+def _bwd(name, q, k, v, beta, lam, dO, S0=None, x_prev=None, dS_T=None, dx_last=None, chunk=64,
+         phi="l2", eps=1e-6, eps_gamma=1e-6, ridge="given", workspace=None, stream=None,
+         grads=None):
+    lib = load_library()
+    _need(q, "q")
+    B, H, T, m = q.shape
+    dv = v.shape[-1]
+    dt = q.dtype
+    if dt not in _DTYPE:
+        raise TypeError("q, k, v must be bfloat16 or float32")
+    _need(k, "k", dt, (B, H, T, m))
+    _need(v, "v", dt, (B, H, T, dv))
+    _need(dO, "dO", dt, (B, H, T, dv))
+    _need(beta, "beta", torch.float32, (B, H, T))
+    _need(lam, "lambda", torch.float32, (B, H, T))
+    for t, nm, shp in ((S0, "S0", (B, H, m, dv)), (dS_T, "dS_T", (B, H, m, dv)),
+                       (x_prev, "x_prev", (B, H, m)), (dx_last, "dx_last", (B, H, m))):
+        if t is not None:
+            _need(t, nm, torch.float32, shp)
+    dev = q.device
+    g = grads if grads is not None else {}
+    g.setdefault("dq", torch.empty_like(q))
+    g.setdefault("dk", torch.empty_like(k))
+    g.setdefault("dv", torch.empty_like(v))
+    g.setdefault("dbeta", torch.empty_like(beta))
+    g.setdefault("dlambda", torch.empty_like(lam))
+    g.setdefault("dS0", torch.empty((B, H, m, dv), dtype=torch.float32, device=dev))
+    g.setdefault("dx_prev", torch.empty((B, H, m), dtype=torch.float32, device=dev))
+    shape = make_shape(B, H, T, m, dv, chunk, dt, phi, eps, eps_gamma, ridge)
+    need = int(lib.falcon_bwd_workspace_bytes(ctypes.byref(shape)))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = getattr(lib, name)(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+                            _ptr(lam), _ptr(S0), _ptr(x_prev), _ptr(dO), _ptr(dS_T),
+                            _ptr(dx_last), _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]),
+                            _ptr(g["dbeta"]), _ptr(g["dlambda"]), _ptr(g["dS0"]),
+                            _ptr(g["dx_prev"]), _ptr(workspace), ws_bytes, _stream(stream))
+    _check(rc, name)
+    return g
+
+
+def falcon1_bwd_chunked(q, k, v, beta, lam, dO, S0=None, x_prev=None, dS_T=None, dx_last=None,
+                        chunk=64, phi="l2", eps=1e-6, eps_gamma=1e-6, **kw):
+    """Backward of falcon1_fwd_chunked: gradients of <dO, o> + <dS_T, S_T> +
+    <dx_last, x_last>.  dO has the dtype of q; dS_T [B,H,m,dv] and dx_last
+    [B,H,m] fp32 or None.  Returns a dict with dq, dk, dv (dtype of q), dbeta,
+    dlambda, dS0, dx_prev (fp32).  ``grads`` may pass preallocated outputs."""
+    return _bwd("falcon1_bwd_chunked", q, k, v, beta, lam, dO, S0, x_prev, dS_T, dx_last,
+                chunk, phi, eps, eps_gamma, **kw)
+
+
+def falcon1a_bwd_chunked(q, k, v, beta, lam, dO, S0=None, x_prev=None, dS_T=None, dx_last=None,
+                         chunk=64, phi="l2", eps=1e-6, eps_gamma=1e-6, **kw):
+    """Backward of falcon1a_fwd_chunked; arguments as falcon1_bwd_chunked."""
+    return _bwd("falcon1a_bwd_chunked", q, k, v, beta, lam, dO, S0, x_prev, dS_T, dx_last,
+                chunk, phi, eps, eps_gamma, **kw)
 
 
 def _fwd2(name, q, k, v, beta, lam, S0=None, x_prev=None, phi="l2", eps=1e-6,

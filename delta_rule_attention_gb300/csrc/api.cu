@@ -148,6 +148,82 @@ int fwd_chunked(int rule, const falcon_shape* s, const void* q, const void* k, c
   return to_status(falcon::launch_generic_chunked(a, stream));
 }
 
+int bwd_chunked(int rule, const falcon_shape* s, const void* q, const void* k, const void* v,
+                const float* beta, const float* lambda, const float* S0, const float* x_prev,
+                const void* dO, const float* dS_T, const float* dx_last, void* dq, void* dk,
+                void* dv, float* dbeta, float* dlambda, float* dS0, float* dx_prev,
+                void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  int rc = check_shape(s);
+  if (rc) return rc;
+  const int64_t BH = s->B * s->H;
+  if (BH == 0) return FALCON_OK;
+  if (s->T > 0 && (!q || !k || !v || !beta || !lambda || !dO || !dq || !dk || !dv || !dbeta ||
+                   !dlambda))
+    return FALCON_ERR_NULL_PTR;
+  const void* ptrs[] = {q,  k,  v,  beta,    lambda, S0,  x_prev,  dO,
+                        dS_T, dx_last, dq, dk, dv, dbeta, dlambda, dS0, dx_prev};
+  for (const void* p : ptrs)
+    if (misaligned(p)) return FALCON_ERR_MISALIGNED;
+  const size_t need = falcon_bwd_workspace_bytes(s);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return FALCON_ERR_WORKSPACE;
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return FALCON_ERR_MISALIGNED;
+  rc = check_device();
+  if (rc) return rc;
+  if (s->T == 0) {  // S_T = S0 and x_last = x_prev: the cotangents pass through
+    cudaError_t e = cudaSuccess;
+    const size_t state_bytes = sizeof(float) * (size_t)BH * s->m * s->dv;
+    const size_t feat_bytes = sizeof(float) * (size_t)BH * s->m;
+    if (dS0 && dS_T && dS0 != dS_T)
+      e = cudaMemcpyAsync(dS0, dS_T, state_bytes, cudaMemcpyDeviceToDevice, stream);
+    else if (dS0 && !dS_T)
+      e = cudaMemsetAsync(dS0, 0, state_bytes, stream);
+    if (e == cudaSuccess && dx_prev) {
+      if (x_prev && dx_last) {
+        if (dx_prev != dx_last)
+          e = cudaMemcpyAsync(dx_prev, dx_last, feat_bytes, cudaMemcpyDeviceToDevice, stream);
+      } else {
+        e = cudaMemsetAsync(dx_prev, 0, feat_bytes, stream);
+      }
+    }
+    return to_status(e);
+  }
+  falcon::BwdArgs b;
+  ChunkArgs& a = b.f;
+  a.rule = rule;
+  a.BH = BH;
+  a.T = s->T;
+  a.m = s->m;
+  a.dv = s->dv;
+  a.C = s->chunk;
+  a.dtype = s->dtype;
+  a.phi = s->phi;
+  a.ridge = s->ridge;
+  a.eps = s->eps;
+  a.eps_gamma = s->eps_gamma;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.beta = beta;
+  a.lambda = lambda;
+  a.S0 = S0;
+  a.x_prev = x_prev;
+  a.o = nullptr;
+  a.S_out = nullptr;
+  a.x_last = nullptr;
+  a.workspace = workspace;
+  b.dO = dO;
+  b.dS_T = dS_T;
+  b.dx_last = dx_last;
+  b.dq = dq;
+  b.dk = dk;
+  b.dv = dv;
+  b.dbeta = dbeta;
+  b.dlambda = dlambda;
+  b.dS0 = dS0;
+  b.dx_prev = dx_prev;
+  return to_status(falcon::launch_bwd_chunked(b, stream));
+}
+
 // Failure-path diagnostic: every thread waits on an mbarrier that nothing
 // completes, gives up after limit_ns and records the expiry in the device
 // error word (the same path the tensor-core kernels take on a lost wait).
@@ -224,6 +300,33 @@ int falcon1a_fwd_chunked(const falcon_shape* s, const void* q, const void* k, co
                          void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   return fwd_chunked(falcon::kFalcon1A, s, q, k, v, beta, lambda, S0, x_prev, o, S_out, x_last,
                      workspace, workspace_bytes, stream);
+}
+
+size_t falcon_bwd_workspace_bytes(const falcon_shape* s) {
+  if (check_shape(s) != FALCON_OK) return 0;
+  return falcon::bwd_workspace_bytes(s->B * s->H, s->T, s->m, s->dv, s->chunk);
+}
+
+int falcon1_bwd_chunked(const falcon_shape* s, const void* q, const void* k, const void* v,
+                        const float* beta, const float* lambda, const float* S0,
+                        const float* x_prev, const void* dO, const float* dS_T,
+                        const float* dx_last, void* dq, void* dk, void* dv, float* dbeta,
+                        float* dlambda, float* dS0, float* dx_prev, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream) {
+  return bwd_chunked(falcon::kFalcon1, s, q, k, v, beta, lambda, S0, x_prev, dO, dS_T, dx_last,
+                     dq, dk, dv, dbeta, dlambda, dS0, dx_prev, workspace, workspace_bytes,
+                     stream);
+}
+
+int falcon1a_bwd_chunked(const falcon_shape* s, const void* q, const void* k, const void* v,
+                         const float* beta, const float* lambda, const float* S0,
+                         const float* x_prev, const void* dO, const float* dS_T,
+                         const float* dx_last, void* dq, void* dk, void* dv, float* dbeta,
+                         float* dlambda, float* dS0, float* dx_prev, void* workspace,
+                         size_t workspace_bytes, cudaStream_t stream) {
+  return bwd_chunked(falcon::kFalcon1A, s, q, k, v, beta, lambda, S0, x_prev, dO, dS_T, dx_last,
+                     dq, dk, dv, dbeta, dlambda, dS0, dx_prev, workspace, workspace_bytes,
+                     stream);
 }
 
 int falcon2_fwd_recurrent(const falcon_shape* s, const void* q, const void* k, const void* v,
@@ -308,6 +411,6 @@ const char* falcon_strerror(int code) {
   return "unknown error code";
 }
 
-int falcon_version(void) { return 10100; }
+int falcon_version(void) { return 10200; }
 
 }  // extern "C"

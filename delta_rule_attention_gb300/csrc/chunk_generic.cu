@@ -16,7 +16,8 @@
 //      Nc go to the workspace.
 //   2. chunk_scan_kernel, one CTA per (head, slice of dv columns): the
 //      inter-chunk recurrence, sequential over chunks.  Columns of S evolve
-//      independently, so slicing dv is exact.
+//      independently, so slicing dv is exact.  For the backward pass it can
+//      also record the state entering every chunk (and skip o).
 //
 // Only non-positive exponents are ever exponentiated (the chunk-local
 // log-space form of the positive-decay renormalisation, page
@@ -214,7 +215,8 @@ __global__ void __launch_bounds__(kThreads) chunk_prep_kernel(ChunkArgs a, int n
   }
 }
 
-__global__ void __launch_bounds__(kThreads) chunk_scan_kernel(ChunkArgs a, int nchunks, int NV) {
+__global__ void __launch_bounds__(kThreads)
+    chunk_scan_kernel(ChunkArgs a, int nchunks, int NV, float* S_starts) {
   const int64_t bh = blockIdx.x;
   const int j0 = blockIdx.y * NV;
   const int m = a.m, dv = a.dv, C = a.C;
@@ -231,6 +233,11 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(ChunkArgs a, int n
     const float* gM = reinterpret_cast<const float*>(a.workspace) +
                       (bh * nchunks + c) * map_floats(m, dv, C);
     const float* gN = gM + (int64_t)R * m;
+    if (S_starts) {  // the state entering chunk c
+      float* dst = S_starts + (bh * nchunks + c) * (int64_t)m * dv;
+      for (int idx = threadIdx.x; idx < m * NV; idx += kThreads)
+        dst[(idx / NV) * dv + j0 + idx % NV] = S[idx];
+    }
     for (int idx = threadIdx.x; idx < R * m; idx += kThreads) Mc[idx] = gM[idx];
     for (int idx = threadIdx.x; idx < R * NV; idx += kThreads) {
       const int r = idx / NV, j = idx % NV;
@@ -250,22 +257,24 @@ __global__ void __launch_bounds__(kThreads) chunk_scan_kernel(ChunkArgs a, int n
       const int r = idx / NV, j = idx % NV;
       if (r < m) {
         S[idx] = Ns[idx];
-      } else {
+      } else if (a.o) {
         const int64_t t = t0 + (r - m);
         if (t < a.T) store_elem(a.o, (bh * a.T + t) * dv + j0 + j, Ns[idx], a.dtype);
       }
     }
     __syncthreads();
   }
-  for (int idx = threadIdx.x; idx < m * NV; idx += kThreads) {
-    const int r = idx / NV, j = idx % NV;
-    a.S_out[(bh * m + r) * dv + j0 + j] = S[idx];
+  if (a.S_out) {
+    for (int idx = threadIdx.x; idx < m * NV; idx += kThreads) {
+      const int r = idx / NV, j = idx % NV;
+      a.S_out[(bh * m + r) * dv + j0 + j] = S[idx];
+    }
   }
 }
 
 }  // namespace
 
-cudaError_t launch_generic_chunked(const ChunkArgs& a, cudaStream_t stream) {
+cudaError_t launch_generic_chunked(const ChunkArgs& a, cudaStream_t stream, float* S_starts) {
   const int nchunks = (int)((a.T + a.C - 1) / a.C);
   const int m = a.m, dv = a.dv, C = a.C;
   const size_t prep_smem =
@@ -286,7 +295,7 @@ cudaError_t launch_generic_chunked(const ChunkArgs& a, cudaStream_t stream) {
                              (int)scan_smem);
   if (err != cudaSuccess) return err;
   dim3 g2((unsigned)a.BH, dv / NV);
-  chunk_scan_kernel<<<g2, kThreads, scan_smem, stream>>>(a, nchunks, NV);
+  chunk_scan_kernel<<<g2, kThreads, scan_smem, stream>>>(a, nchunks, NV, S_starts);
   return cudaGetLastError();
 }
 

@@ -88,7 +88,10 @@ struct ChunkArgs {
   void* workspace;
 };
 size_t generic_workspace_bytes(int64_t BH, int64_t T, int m, int dv, int C);
-cudaError_t launch_generic_chunked(const ChunkArgs& a, cudaStream_t stream);
+// a.o and a.S_out may be null (not written); S_starts (nullable) receives the
+// state entering every chunk, [B*H, chunks, m, dv] f32.
+cudaError_t launch_generic_chunked(const ChunkArgs& a, cudaStream_t stream,
+                                   float* S_starts = nullptr);
 
 // Falcon-2 / Falcon-2A, token-recurrent form (rule kFalcon2 or kFalcon2A;
 // beta is [B*H, T, dv]: one gain per column and token).
@@ -102,6 +105,19 @@ cudaError_t launch_falcon3a_recurrent(const ChunkArgs& a, int window, int* err,
 bool tc_path_applies(int dtype, int m, int dv, int C, int64_t BH, int64_t T);
 size_t tc_workspace_bytes(int m, int64_t BH, int64_t T);
 cudaError_t launch_tc_chunked(const ChunkArgs& a, int* err, cudaStream_t stream);
+
+// Backward pass of Falcon-1 / Falcon-1A (chunk form).  Cotangents dO (dtype),
+// dS_T and dx_last (f32, nullable = zero); gradients dq, dk, dv (dtype),
+// dbeta, dlambda (f32), dS0 and dx_prev (f32, nullable = not written).
+struct BwdArgs {
+  ChunkArgs f;  // the forward problem (f.o, f.S_out, f.x_last unused)
+  const void* dO;
+  const float *dS_T, *dx_last;
+  void *dq, *dk, *dv;
+  float *dbeta, *dlambda, *dS0, *dx_prev;
+};
+size_t bwd_workspace_bytes(int64_t BH, int64_t T, int m, int dv, int C);
+cudaError_t launch_bwd_chunked(const BwdArgs& b, cudaStream_t stream);
 
 struct DecodeArgs {
   int rule;

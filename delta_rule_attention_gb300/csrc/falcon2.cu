@@ -42,7 +42,6 @@ template <int M>
 struct F2Cfg {
   static constexpr int kP = M / 16;         // threads per column (16 state rows each)
   static constexpr int kThreads = 32 * kP;  // 32 columns per CTA
-  static constexpr int kWarps = kP;
   static constexpr int kLd = M / 16 * 20;   // fp32 row stride: 16 values + 4 gap per segment
 };
 

@@ -140,6 +140,18 @@ def random_case(B, H, T, m, dv, dtype=torch.float32, seed=0, lam_shift=-2.0, dev
     return {n: t.to(device).contiguous() for n, t in out.items()}
 
 
+def cotangents(B, H, T, m, dv, dtype=torch.float32, seed=0, device="cpu", ends=False):
+    """Seeded cotangents for the backward pass: dO [B,H,T,dv] N(0,1) in `dtype`
+    and, with ``ends``, dS_T [B,H,m,dv] and dx_last [B,H,m] N(0,1) fp32 (a
+    training step on a fresh, final segment has zero end cotangents)."""
+    g = torch.Generator().manual_seed(10_000 + seed)
+    out = {"dO": torch.randn((B, H, T, dv), generator=g).to(dtype)}
+    if ends:
+        out["dS_T"] = torch.randn((B, H, m, dv), generator=g)
+        out["dx_last"] = torch.randn((B, H, m), generator=g)
+    return {n: t.to(device).contiguous() for n, t in out.items()}
+
+
 class DecodeStream:
     """Per-step inputs of the decode workload, drawn step after step from one
     generator on `device` (the initial state first, then for every step q, k,

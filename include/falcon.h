@@ -1,9 +1,9 @@
 /*
  * falcon.h -- C ABI of the GB300 (sm_103a) Falcon fast-weight attention
- * library: chunk-parallel forward of Falcon-1 and Falcon-1A, the
- * token-recurrent forward of Falcon-2 and Falcon-2A (per-column step sizes)
- * and of Falcon-3A (sliding window), and the single-token recurrent decode
- * step.
+ * library: chunk-parallel forward of Falcon-1 and Falcon-1A and its backward
+ * pass, the token-recurrent forward of Falcon-2 and Falcon-2A (per-column
+ * step sizes) and of Falcon-3A (sliding window), and the single-token
+ * recurrent decode step.
  *
  * The operations are defined on the page hyper.ai/fr/papers/2608.27763
  * ("Fast Weight Attention for Continual Learning"):
@@ -178,6 +178,53 @@ int falcon1a_fwd_chunked(const falcon_shape *shape, const void *q,
                          float *x_last, void *workspace, size_t workspace_bytes,
                          cudaStream_t stream);
 
+/* Bytes of device workspace falcon1_bwd_chunked / falcon1a_bwd_chunked need
+ * for this shape (0 for an invalid shape; the call then reports the error). */
+size_t falcon_bwd_workspace_bytes(const falcon_shape *shape);
+/* Backward pass of the Falcon-1 chunk-parallel forward: the gradient of
+ *   L = <dO, o> + <dS_T, S_T> + <dx_last, x_last>
+ * with respect to every input of falcon1_fwd_chunked.  The pages state that
+ * training differentiates through the update, so that the slow weights that
+ * produce q, k, v, beta and lambda learn (Section 3, "Implicit fast-memory
+ * objective"), through the log-decay renormalisation and the normalised step
+ * size (Section 4.6, "Backward pass"); this is the exact gradient of the
+ * forward as computed, with two conventions: on the clamped branch of the
+ * decay (eta_t lambda_t >= 1 - eps_gamma) gamma_t = eps_gamma is a constant,
+ * and the boundary sentinel (eta_1 = 0) passes no gradient to beta_1,
+ * lambda_1.  The call recomputes the forward (chunk maps and the state
+ * entering every chunk) in its workspace; it needs none of the forward's
+ * outputs.
+ *   shape, q, k, v, beta, lambda, S0, x_prev: the forward's arguments
+ *           (S0 and x_prev nullable as there)
+ *   dO      [B,H,T,dv] dtype, the cotangent of o
+ *   dS_T    [B,H,m,dv] f32, nullable (zero), the cotangent of S_T
+ *   dx_last [B,H,m] f32, nullable (zero), the cotangent of x_last
+ *   dq, dk  [B,H,T,m] dtype, out;   dv [B,H,T,dv] dtype, out
+ *   dbeta, dlambda [B,H,T] f32, out (with FALCON_RIDGE_SCALED, dlambda is
+ *           the gradient for the lambda input, the base ridge)
+ *   dS0     [B,H,m,dv] f32, out, nullable (not written); may alias dS_T
+ *   dx_prev [B,H,m] f32, out, nullable (not written); zeros when x_prev is
+ *           NULL (the sentinel feature is a constant)
+ *   workspace, workspace_bytes: at least falcon_bwd_workspace_bytes(shape)
+ *           bytes, 256-byte aligned; contents are overwritten.
+ * Every shape and dtype of falcon1_fwd_chunked is accepted (fp32 arithmetic
+ * on CUDA cores).  Errors as for falcon1_fwd_chunked. */
+int falcon1_bwd_chunked(const falcon_shape *shape, const void *q, const void *k,
+                        const void *v, const float *beta, const float *lambda,
+                        const float *S0, const float *x_prev, const void *dO,
+                        const float *dS_T, const float *dx_last, void *dq, void *dk,
+                        void *dv, float *dbeta, float *dlambda, float *dS0,
+                        float *dx_prev, void *workspace, size_t workspace_bytes,
+                        cudaStream_t stream);
+/* The backward pass of falcon1a_fwd_chunked (Section 4.3 Eq. (4.6)).
+ * Arguments, layouts, ownership and errors are those of falcon1_bwd_chunked. */
+int falcon1a_bwd_chunked(const falcon_shape *shape, const void *q, const void *k,
+                         const void *v, const float *beta, const float *lambda,
+                         const float *S0, const float *x_prev, const void *dO,
+                         const float *dS_T, const float *dx_last, void *dq, void *dk,
+                         void *dv, float *dbeta, float *dlambda, float *dS0,
+                         float *dx_prev, void *workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
 /* Falcon-2 forward (per-column step sizes), token-recurrent form: every
  * column j of the state follows its own step size and clamped decay,
  *   eta_{j,t} = beta_{j,t} / (||x_t||^2 + lambda_t + eps)  (0 at the sentinel

@@ -47,7 +47,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_strerror(lib):
-    assert lib.falcon_version() == 10100
+    assert lib.falcon_version() == 10200
     assert lib.falcon_strerror(0) == b"ok"
     for code in range(-9, 0):
         assert lib.falcon_strerror(code) != b"unknown error code"
@@ -128,3 +128,37 @@ def test_decode_rejects_bad_arguments_without_a_device(lib, fn):
     assert args(q=None) == -1
     assert args(S=odd) == -4
     assert args(N=0, q=None) == 0
+
+
+@pytest.mark.parametrize("fn", ["falcon1_bwd_chunked", "falcon1a_bwd_chunked"])
+def test_backward_rejects_bad_arguments_without_a_device(lib, fn):
+    f = getattr(lib, fn)
+    p, odd = _fake(), _fake(0x10008)
+    big = ctypes.c_size_t(1 << 40)
+
+    def call(s, q=p, dO=p, dq=p, dS0=None, ws=p, wsb=big):
+        return f(ctypes.byref(s) if s is not None else None, q, p, p, p, p, None, None, dO, None,
+                 None, dq, p, p, p, p, dS0, None, ws, wsb, None)
+
+    for bad, code in ((dict(m=24), -2), (dict(chunk=48), -2), (dict(dtype=7), -3),
+                      (dict(phi=3), -3), (dict(ridge=2), -8), (dict(eps_gamma=1.0), -8)):
+        assert call(_shape(**bad)) == code, bad
+    s = _shape()
+    assert call(None) == -1
+    assert call(s, q=None) == -1
+    assert call(s, dO=None) == -1
+    assert call(s, dq=None) == -1
+    assert call(s, dq=odd) == -4
+    assert call(s, dS0=odd) == -4
+    assert call(s, ws=None) == -5
+    assert call(s, wsb=ctypes.c_size_t(64)) == -5
+    assert call(_shape(B=0), q=None, dO=None, dq=None, ws=None, wsb=ctypes.c_size_t(0)) == 0
+
+
+def test_backward_workspace_bytes(lib):
+    s = _shape()  # B1 H2 T64 m16 dv16 C16: 4 chunks per head
+    BH, nch, m, dv, C, T = 2, 4, 16, 16, 16, 64
+    floats = [BH * nch * (m + C) * (m + dv), BH * nch * m * dv, BH * nch * m * dv, BH * T * m]
+    want = sum((n + 63) // 64 * 64 for n in floats) * 4
+    assert lib.falcon_bwd_workspace_bytes(ctypes.byref(s)) == want
+    assert lib.falcon_bwd_workspace_bytes(ctypes.byref(_shape(m=24))) == 0

@@ -1,0 +1,157 @@
+"""GPU parity of the backward pass (falcon1_bwd_chunked / falcon1a_bwd_chunked)
+against the oracle's reverse mode through the recurrence (fp64).
+
+Error measure, as for the forward: ||err||_F / ||ref||_F per head for every
+gradient (dq, dk over T x m; dv over T x dv; dbeta, dlambda over T; dS0 over
+m x dv; dx_prev over m), maximum over heads.  Bound: 1e-4 for fp32 inputs,
+2e-2 for bf16 inputs (dq, dk, dv are rounded to bf16 on output, the rest is
+fp32 arithmetic on the rounded inputs).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from delta_rule_attention_gb300 import workloads
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+TOL = {torch.float32: 1e-4, torch.bfloat16: 2e-2}
+HEAD_DIMS = {"dq": 2, "dk": 2, "dv": 2, "dbeta": 1, "dlambda": 1, "dS0": 2, "dx_prev": 1}
+
+
+@pytest.fixture(scope="module")
+def falcon():
+    import delta_rule_attention_gb300 as f
+    f.load_library()
+    return f
+
+
+def head_err(got, ref, head_dims=2):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    g = got.reshape(-1, int(np.prod(got.shape[-head_dims:])))
+    r = ref.reshape(g.shape)
+    num = np.linalg.norm(g - r, axis=1)
+    den = np.maximum(np.linalg.norm(r, axis=1), 1e-30)
+    return float((num / den).max())
+
+
+def run_bwd(falcon, rule, x, ct, chunk, phi, ridge="given", carried=True):
+    fn = falcon.falcon1_bwd_chunked if rule == "falcon1" else falcon.falcon1a_bwd_chunked
+    g = fn(x["q"], x["k"], x["v"], x["beta"], x["lambda"], ct["dO"], S0=x.get("S0"),
+           x_prev=x.get("x_prev"), dS_T=ct.get("dS_T"), dx_last=ct.get("dx_last"), chunk=chunk,
+           phi=phi, ridge=ridge)
+    assert falcon.falcon_sync_check() == 0
+    return {n: t.float().cpu().numpy() for n, t in g.items()}
+
+
+def ref_bwd(rule, x, ct, phi, ridge="given", threads=None):
+    cpu = {n: t.cpu() for n, t in x.items()}
+    c = {n: t.cpu() for n, t in ct.items()}
+    return oracle.backward(rule, cpu["q"], cpu["k"], cpu["v"], cpu["beta"], cpu["lambda"],
+                           c["dO"], S0=cpu.get("S0"), x_prev=cpu.get("x_prev"),
+                           dS_T=c.get("dS_T"), dx_last=c.get("dx_last"), phi=phi, ridge=ridge,
+                           threads=threads)
+
+
+def check(got, ref, tol, names=None):
+    for n in names or HEAD_DIMS:
+        err = head_err(got[n], ref[n], HEAD_DIMS[n])
+        assert err < tol, (n, err)
+
+
+CASES = [
+    # B, H, T, m, dv, chunk, dtype, phi
+    (1, 2, 64, 16, 16, 16, torch.float32, "identity"),
+    (2, 3, 3 * 64 + 5, 64, 64, 64, torch.bfloat16, "l2"),
+    (1, 2, 2 * 32 + 17, 32, 128, 32, torch.float32, "l2"),
+    (2, 1, 100, 128, 32, 64, torch.bfloat16, "l2"),
+    (1, 3, 257, 128, 128, 64, torch.bfloat16, "l2"),
+    (1, 2, 40, 16, 64, 16, torch.float32, "identity"),
+    (3, 2, 7, 64, 16, 64, torch.float32, "l2"),       # shorter than one chunk
+    (1, 2, 1, 64, 64, 64, torch.bfloat16, "l2"),      # a single token
+    (2, 2, 130, 64, 64, 64, torch.float32, "l2"),
+    (1, 2, 190, 128, 128, 64, torch.float32, "rms"),
+]
+
+
+@pytest.mark.parametrize("rule", ["falcon1", "falcon1a"])
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c[:6])) + str(c[6])[-4:])
+@pytest.mark.parametrize("carried", [False, True])
+def test_backward_small_shapes_against_oracle(falcon, rule, case, carried):
+    B, H, T, m, dv, C, dt, phi = case
+    seed = 300 + CASES.index(case)
+    x = workloads.random_case(B, H, T, m, dv, dt, seed=seed, device="cuda",
+                              with_state=carried, with_x_prev=carried)
+    ct = workloads.cotangents(B, H, T, m, dv, dt, seed=seed, device="cuda", ends=carried)
+    got = run_bwd(falcon, rule, x, ct, C, phi)
+    ref = ref_bwd(rule, x, ct, phi)
+    check(got, ref, TOL[dt], None if carried else
+          ["dq", "dk", "dv", "dbeta", "dlambda", "dS0"])
+    if not carried:
+        assert np.all(got["dx_prev"] == 0)
+
+
+@pytest.mark.parametrize("rule", ["falcon1", "falcon1a"])
+@pytest.mark.parametrize("phi,ridge", [("rms", "scaled"), ("l2", "scaled"),
+                                       ("identity", "given")])
+def test_backward_feature_and_ridge_variants(falcon, rule, phi, ridge):
+    x = workloads.random_case(2, 2, 150, 32, 32, torch.float32, seed=41, device="cuda",
+                              with_state=True, with_x_prev=True)
+    ct = workloads.cotangents(2, 2, 150, 32, 32, torch.float32, seed=41, device="cuda",
+                              ends=True)
+    got = run_bwd(falcon, rule, x, ct, 32, phi, ridge)
+    ref = ref_bwd(rule, x, ct, phi, ridge)
+    check(got, ref, TOL[torch.float32])
+
+
+@pytest.mark.parametrize("rule", ["falcon1", "falcon1a"])
+def test_backward_clamp_active(falcon, rule):
+    """lambda = softplus(n + 3), beta = 1.95: the decay clamp fires on many
+    tokens (no gradient through alpha there) and chunk decays underflow."""
+    x = workloads.random_case(2, 2, 200, 64, 64, torch.float32, seed=77, lam_shift=3.0,
+                              device="cuda", with_state=True)
+    x["beta"] = torch.full_like(x["beta"], 1.95)
+    ct = workloads.cotangents(2, 2, 200, 64, 64, torch.float32, seed=77, device="cuda",
+                              ends=True)
+    got = run_bwd(falcon, rule, x, ct, 64, "l2")
+    ref = ref_bwd(rule, x, ct, "l2")
+    for n in got:
+        assert np.isfinite(got[n]).all(), n
+    check(got, ref, TOL[torch.float32], ["dq", "dk", "dv", "dbeta", "dlambda", "dS0"])
+
+
+def test_backward_empty_sequence(falcon):
+    """T = 0: S_T = S0 and x_last = x_prev, so dS0 = dS_T and dx_prev =
+    dx_last; B*H = 0 is a no-op."""
+    x = workloads.random_case(1, 3, 0, 32, 16, torch.float32, seed=3, device="cuda",
+                              with_state=True, with_x_prev=True)
+    ct = workloads.cotangents(1, 3, 0, 32, 16, torch.float32, seed=3, device="cuda", ends=True)
+    got = run_bwd(falcon, "falcon1", x, ct, 16, "l2")
+    np.testing.assert_array_equal(got["dS0"], ct["dS_T"].cpu().numpy())
+    np.testing.assert_array_equal(got["dx_prev"], ct["dx_last"].cpu().numpy())
+    x0 = workloads.random_case(0, 2, 8, 16, 16, torch.float32, seed=3, device="cuda")
+    ct0 = workloads.cotangents(0, 2, 8, 16, 16, torch.float32, seed=3, device="cuda")
+    run_bwd(falcon, "falcon1", x0, ct0, 16, "l2")
+
+
+@pytest.mark.parametrize("w", [workloads.LM, workloads.LM_1A], ids=lambda w: w.name)
+def test_backward_lm_workload_sampled_heads(falcon, w):
+    """B8 H12 T2048 d64 bf16 in one call; four heads recomputed by the oracle."""
+    x = workloads.generate(w, device="cuda")
+    ct = workloads.cotangents(w.B, w.H, w.T, w.m, w.dv, w.dtype, seed=w.seed, device="cuda")
+    got = run_bwd(falcon, w.rule, x, ct, w.chunk, w.phi)
+    pick = [(0, 0), (3, 7), (5, 2), (7, 11)]
+    bs = torch.tensor([p[0] for p in pick])
+    hs = torch.tensor([p[1] for p in pick])
+    sub = {n: t.cpu()[bs, hs].unsqueeze(0) for n, t in x.items()}
+    csub = {n: t.cpu()[bs, hs].unsqueeze(0) for n, t in ct.items()}
+    ref = ref_bwd(w.rule, sub, csub, w.phi, threads=4)
+    for n in ("dq", "dk", "dv", "dbeta", "dlambda", "dS0"):
+        g = got[n][bs.numpy(), hs.numpy()][None]
+        err = head_err(g, ref[n], HEAD_DIMS[n])
+        assert err < 2e-2, (n, err)
+    for n in got:
+        assert np.isfinite(got[n]).all(), n
