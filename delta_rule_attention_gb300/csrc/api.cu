@@ -221,7 +221,9 @@ int bwd_chunked(int rule, const falcon_shape* s, const void* q, const void* k, c
   b.dlambda = dlambda;
   b.dS0 = dS0;
   b.dx_prev = dx_prev;
-  return to_status(falcon::launch_bwd_chunked(b, stream));
+  int* err = device_error_word();
+  if (!err) return FALCON_ERR_CUDA;
+  return to_status(falcon::launch_bwd_chunked(b, err, stream));
 }
 
 // Failure-path diagnostic: every thread waits on an mbarrier that nothing

@@ -537,11 +537,14 @@ __global__ void __launch_bounds__(kThreads) bwd_feature_kernel(BwdArgs b, const 
 
 }  // namespace
 
+cudaError_t launch_generic_grad(const BwdArgs& b, int nchunks, const float* S_starts,
+                                const float* dS_ends, float* dXw, cudaStream_t stream);
+
 size_t bwd_workspace_bytes(int64_t BH, int64_t T, int m, int dv, int C) {
   return (size_t)bwd_layout(BH, T, m, dv, C).total * sizeof(float);
 }
 
-cudaError_t launch_bwd_chunked(const BwdArgs& b, cudaStream_t stream) {
+cudaError_t launch_bwd_chunked(const BwdArgs& b, int* err, cudaStream_t stream) {
   const ChunkArgs& a = b.f;
   const int m = a.m, dv = a.dv, C = a.C;
   const int nchunks = (int)((a.T + C - 1) / C);
@@ -570,16 +573,11 @@ cudaError_t launch_bwd_chunked(const BwdArgs& b, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
 
   // 3. per-chunk gradients
-  const size_t grad_smem =
-      sizeof(float) * (2 * (size_t)C * (m + 1) + 4 * (size_t)C * C + 2 * (size_t)C * dv +
-                       16 * (size_t)C + 4) +
-      sizeof(int) * (size_t)C;
-  e = cudaFuncSetAttribute(bwd_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)grad_smem);
-  if (e != cudaSuccess) return e;
-  bwd_grad_kernel<<<dim3(nchunks, (unsigned)a.BH), kThreads, grad_smem, stream>>>(
-      b, nchunks, ws + L.S_starts, ws + L.dS_ends, ws + L.dX);
-  e = cudaGetLastError();
+  if (tc_bwd_applies(a.dtype, m, dv, C)) {
+    e = launch_tc_bwd_grad(b, ws + L.S_starts, ws + L.dS_ends, ws + L.dX, err, stream);
+  } else {
+    e = launch_generic_grad(b, nchunks, ws + L.S_starts, ws + L.dS_ends, ws + L.dX, stream);
+  }
   if (e != cudaSuccess) return e;
 
   // 4. dk, dx_prev
@@ -587,6 +585,23 @@ cudaError_t launch_bwd_chunked(const BwdArgs& b, cudaStream_t stream) {
   const int64_t blocks = (rows + kWarps - 1) / kWarps;
   bwd_feature_kernel<<<(unsigned)(blocks < 65535 * 16 ? blocks : 65535 * 16), kThreads, 0,
                        stream>>>(b, ws + L.dX);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_generic_grad(const BwdArgs& b, int nchunks, const float* S_starts,
+                                const float* dS_ends, float* dXw, cudaStream_t stream) {
+  const ChunkArgs& a = b.f;
+  const int m = a.m, dv = a.dv, C = a.C;
+  const size_t grad_smem =
+      sizeof(float) * (2 * (size_t)C * (m + 1) + 4 * (size_t)C * C + 2 * (size_t)C * dv +
+                       16 * (size_t)C + 4) +
+      sizeof(int) * (size_t)C;
+  cudaError_t e = cudaFuncSetAttribute(bwd_grad_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)grad_smem);
+  if (e != cudaSuccess) return e;
+  bwd_grad_kernel<<<dim3(nchunks, (unsigned)a.BH), kThreads, grad_smem, stream>>>(
+      b, nchunks, S_starts, dS_ends, dXw);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,636 @@
+// Tensor-core (tcgen05) per-chunk gradients of the Falcon-1 / Falcon-1A
+// backward pass, for bf16 inputs with m = d_v = 64 and chunk C = 64.
+//
+// It computes what bwd_grad_kernel of chunk_bwd.cu computes (the chunk form of
+// the gradient; page hyper.ai/fr/papers/2608.27763, Section 3.1 Eq. (3.3),
+// Section 4.3 Eq. (4.6), Section 4.4 Eq. (4.15)-(4.16)): with the state S
+// entering the chunk and the cotangent dS' of the state leaving it,
+//
+//   R  = Diag(eta) V - Diag(eta e^{g_-}) X S,   U = T R,   T = (I + A)^{-1}
+//   dU = P^T dO + Diag(e^{g_C - g}) X dS',       dR = T^T dU
+//   dA = -(dR U^T) (j < i),  dP = (dO U^T) (j <= i),  dV = Diag(eta) dR
+//   dQ = Diag(e^g) dO S^T + (dP o E) X
+//   dX = -Diag(eta e^{g_-}) dR S^T + (dP o E)^T Q + Diag(e^{g_C - g}) U dS'^T
+//        + (dK + dK^T) X + 2 Diag(dE) X
+//
+// and the step-size chain (log-prefix cotangent, clamp, eta, ridge).  Every
+// contraction is a 64 x 64 x 64 tcgen05 MMA on bf16 operands in 128B-swizzled
+// shared-memory tiles with fp32 accumulators in TMEM; two products that share
+// an operand are stacked into one M = 128 MMA (the unused half of an M = 128
+// operand reads a neighbouring tile and lands in accumulator lanes nobody
+// reads).  Transposed operands are the same row-major tiles read MN-major.
+// The unit-lower inverse T is the forward's fp32 solve.  Epilogues run one
+// accumulator row per thread (two threads per row, one per column half), so
+// the per-row reductions of the step-size chain stay local; column sums go
+// through shared-memory atomics.  Falcon-1A takes the same path with T = I
+// and A = 0.
+// The products that enter the residual r = v - S^T x (X S, and with them Q S
+// and X dS') run as three bf16 MMAs on split operands, hi hi + hi lo + lo hi
+// (v = hi + lo, hi = bf16(v)): the residual is a difference of nearly equal
+// terms, and the step-size gradients are inner products with it.  P^T dO and
+// T^T dU (the residual's cotangent) split P and dU the same way.  They and
+// the other row sums of the step-size chain are formed from fp32 accumulator
+// values.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+#include "tc_util.cuh"
+#include "tmap.cuh"
+
+namespace falcon {
+
+namespace {
+
+using namespace tc;
+using namespace tcu;
+
+constexpr int kBC = 64;
+constexpr int kBThreads = 256;
+constexpr uint32_t kTile = 8192;  // 64 rows x 64 bf16, 128B-swizzled
+// Tile order matters where two tiles form one 128-row operand ([X; Q],
+// [S; dS'], [dR; dO]) or where an M = 128 operand's unused half reads the next
+// tile (T, U, P, dPE, dKs).
+enum : int {
+  kX = 0, kQt, kS, kdS, kdR, kdO, kP, kT, kR, kU, kdPE, kdKs, kV,
+  kXlo, kQlo, kSlo, kdSlo,  // low parts v - bf16(v) of X, Q, S, dS'
+  kPlo, kdUlo,              // and of P and dU
+  kNumTiles
+};
+constexpr uint32_t kAfOff = kNumTiles * kTile;          // A (fp32, rows of kLdA)
+constexpr uint32_t kTfOff = kAfOff + 64 * kLdA * 4;     // T (fp32, kLdT), later dK
+constexpr uint32_t kRsOff = kTfOff + 64 * kLdT * 4;     // solve scratch (16 x kLdR)
+constexpr uint32_t kScOff = kRsOff + 4096;
+static_assert(16 * kLdR * 4 <= 4096, "solve scratch");
+
+struct BwdScalars {
+  float eta[64], g[64], gx[64], E[64], lame[64], den[64], gam[64];
+  float deta[64], dg[64], dE[64], xwd[64];
+  // accumulated with shared-memory atomics (zeroed first)
+  float qz[64], rv[64], xy[64], xw[64], sAr[64], sAc[64], spr[64], spc[64];
+  float ssp[2][128];  // half-row partial sums
+  float ugp[2][128];
+  float sds;          // <dS', S>_F
+  int flag[64];
+  int fail;
+  uint64_t bar_in, bar_mma;
+  uint32_t tmem_base;
+};
+constexpr size_t kBwdSmem = kScOff + sizeof(BwdScalars) + 1024;
+constexpr uint32_t kTmemCols = 512;
+// TMEM columns of the accumulators (128 lanes each).
+constexpr uint32_t kD1 = 0;    // [X; Q] X^T          (64)
+constexpr uint32_t kD2a = 64;  // [X; Q] S            (64)  -> later [junk; dPE] X
+constexpr uint32_t kD2b = 128; // [X; Q] dS'          (64)  -> later dPE^T Q + dKs X
+constexpr uint32_t kD3 = 192;  // T R, P^T dO, T^T dU (64, one after another)
+constexpr uint32_t kD6 = 256;  // [dR; dO] U^T        (64)
+constexpr uint32_t kD7 = 320;  // [dR; dO] [S; dS']^T (128)
+constexpr uint32_t kD8 = 448;  // [U; junk] dS'^T     (64)
+enum : int { kLive = 1, kClamped = 2 };
+
+__device__ __forceinline__ float expn(float x) { return __expf(fminf(x, 0.f)); }
+
+// Half row (32 values) of a swizzled tile as bf16 hi parts, and the rounding
+// remainders as the lo tile.
+__device__ __forceinline__ void store_half_split(unsigned char* hi, unsigned char* lo, int r,
+                                                 int h, const float* v) {
+  float rest[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) rest[j] = v[j] - __bfloat162float(__float2bfloat16_rn(v[j]));
+  store_half_sw(hi, r, h, v, 1.f);
+  store_half_sw(lo, r, h, rest, 1.f);
+}
+
+// Wait for the MMA group committed last, with the CTA-wide failure agreement.
+__device__ __forceinline__ bool wait_mma(BwdScalars& sc, uint32_t& phase) {
+  if (!mbar_wait(&sc.bar_mma, phase)) sc.fail = 1;
+  phase ^= 1u;
+  tc_fence_after();
+  return !__syncthreads_or(sc.fail);
+}
+
+// Generic-proxy tile writes of this CTA become visible to the next MMA.
+__device__ __forceinline__ void publish_tiles() {
+  tc_fence_before();
+  fence_async_smem();
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kBThreads, 1)
+    tc_bwd_grad_kernel(BwdArgs b, int nchunks, const float* S_starts, const float* dS_ends,
+                       float* dXw, int* err, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_do) {
+  const ChunkArgs& a = b.f;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* base = align1024(smem_raw);
+  float* Af = reinterpret_cast<float*>(base + kAfOff);
+  float* Tf = reinterpret_cast<float*>(base + kTfOff);
+  float* Rs = reinterpret_cast<float*>(base + kRsOff);
+  BwdScalars& sc = *reinterpret_cast<BwdScalars*>(base + kScOff);
+  auto tile = [&](int i) { return base + i * kTile; };
+  auto taddr = [&](int i) { return smem_addr(base + i * kTile); };
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int r = tid & 127, h = tid >> 7;  // accumulator lane, column half
+  const int c = blockIdx.x;
+  const int64_t bh = blockIdx.y;
+  const int64_t T = a.T, t0 = (int64_t)c * kBC, rowbase = bh * T;
+  const int n = (int)min((int64_t)kBC, T - t0);
+  const bool f1 = a.rule == kFalcon1;
+  const float* S = S_starts + (bh * nchunks + c) * 4096;
+  const float* dSp = dS_ends + (bh * nchunks + c) * 4096;
+
+  if (warp == 0) tmem_alloc(&sc.tmem_base, kTmemCols);
+  if (tid == 0) {
+    mbar_init(&sc.bar_in, 1);
+    mbar_init(&sc.bar_mma, 1);
+    fence_mbar_init();
+    sc.fail = 0;
+    sc.sds = 0.f;
+    // raw k rows t0-1 .. t0+62 (row -1 reads zeros), q, v and dO rows t0 ..
+    mbar_expect_tx(&sc.bar_in, 4 * kTile);
+    tma_load_3d(tile(kX), &tm_k, 0, (int)(t0 - 1), (int)bh, &sc.bar_in);
+    tma_load_3d(tile(kQt), &tm_q, 0, (int)t0, (int)bh, &sc.bar_in);
+    tma_load_3d(tile(kV), &tm_v, 0, (int)t0, (int)bh, &sc.bar_in);
+    tma_load_3d(tile(kdO), &tm_do, 0, (int)t0, (int)bh, &sc.bar_in);
+  }
+  if (tid < 64) {
+    sc.qz[tid] = sc.rv[tid] = sc.xy[tid] = sc.xw[tid] = 0.f;
+    sc.sAr[tid] = sc.sAc[tid] = sc.spr[tid] = sc.spc[tid] = 0.f;
+  }
+  // [S; dS'] as bf16 operand tiles (thread: row r of the pair, half h)
+  {
+    const float* src = (r < 64 ? S + r * 64 : dSp + (r - 64) * 64) + 32 * h;
+    float v[32];
+#pragma unroll
+    for (int q4 = 0; q4 < 8; ++q4) {
+      const float4 f = reinterpret_cast<const float4*>(src)[q4];
+      v[4 * q4] = f.x;
+      v[4 * q4 + 1] = f.y;
+      v[4 * q4 + 2] = f.z;
+      v[4 * q4 + 3] = f.w;
+    }
+    store_half_split(tile(kS), tile(kSlo), r, h, v);
+  }
+  __syncthreads();  // barriers initialised, accumulators zeroed
+  {
+    float acc = 0.f;  // <dS', S>_F, 16 elements per thread
+    const float4* s4 = reinterpret_cast<const float4*>(S) + 4 * tid;
+    const float4* d4 = reinterpret_cast<const float4*>(dSp) + 4 * tid;
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const float4 x = s4[q4], y = d4[q4];
+      acc += x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w;
+    }
+    acc = warp_sum(acc);
+    if ((tid & 31) == 0) atomicAdd(&sc.sds, acc);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sc.tmem_base;
+  const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 32 * h;  // + column
+  uint32_t phase = 0;
+  float gC = 0.f;
+  if (!mbar_wait(&sc.bar_in, 0)) sc.fail = 1;
+  if (__syncthreads_or(sc.fail)) goto teardown;
+
+  // ---- features: rows 0..63 of [X; Q] are x_i = phi(k_{t0+i-1}) (x_prev, or
+  //      the sentinel zero, at t = 0), rows 64..127 are phi(q_{t0+i}); rows
+  //      past the chunk's tokens are zero.
+  {
+    float v[32];
+    load_half_sw(tile(kX), r, h, v);
+    const int i = r & 63;
+    const bool xrow = r < 64;
+    const bool given = xrow && t0 + i == 0 && a.x_prev != nullptr;
+    const bool dead = i >= n || (xrow && t0 + i == 0 && a.x_prev == nullptr);
+    if (given)
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = a.x_prev[bh * 64 + 32 * h + j];
+    sc.ssp[h][r] = sumsq32(v);
+    __syncthreads();
+    const float ss = sc.ssp[0][r] + sc.ssp[1][r];
+    const float s = dead ? 0.f : (given ? 1.f : phi_scale(ss, 64, a.phi));
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] *= s;
+    store_half_split(tile(kX), tile(kXlo), r, h, v);
+    if (xrow && h == 0) sc.E[i] = ss * s * s;
+  }
+  __syncthreads();
+  // ---- per-token scalars as the forward forms them, then the log prefixes
+  if (tid < 64) {
+    const int i = tid;
+    float et = 0.f, gm = 1.f, lg = 0.f, le = 0.f, d = 1.f;
+    int fl = 0;
+    if (i < n) {
+      const int64_t t = t0 + i;
+      const bool sentinel = (t == 0) && (a.x_prev == nullptr);
+      le = ridge_of(a.lambda[rowbase + t], sc.E[i], a.ridge);
+      d = sc.E[i] + le + a.eps;
+      et = step_eta_gamma(sentinel, sc.E[i], a.beta[rowbase + t], le, a.eps, a.eps_gamma, &gm,
+                          &lg);
+      if (!sentinel && d > 0.f) fl |= kLive;
+      if (et * le >= 1.f - a.eps_gamma) fl |= kClamped;
+    }
+    sc.eta[i] = et;
+    sc.gam[i] = gm;
+    sc.g[i] = lg;
+    sc.lame[i] = le;
+    sc.den[i] = d;
+    sc.flag[i] = fl;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float run = 0.f;
+    for (int i = 0; i < 64; ++i) {
+      sc.gx[i] = run;
+      run += sc.g[i];
+      sc.g[i] = run;
+    }
+  }
+  publish_tiles();
+  gC = sc.g[63];
+
+  // ---- MMA: [X; Q] X^T, [X; Q] S, [X; Q] dS'
+  if (tid == 0) {
+    tc_fence_after();
+    mma_k64(tmem + kD1, taddr(kX), false, 16, taddr(kX), false, 16,
+            idesc_bf16(128, 64, false, false), false);
+    const uint32_t id = idesc_bf16(128, 64, false, true);
+    mma_k64(tmem + kD2a, taddr(kX), false, 16, taddr(kS), true, kTile, id, false);
+    mma_k64(tmem + kD2a, taddr(kX), false, 16, taddr(kSlo), true, kTile, id, true);
+    mma_k64(tmem + kD2a, taddr(kXlo), false, 16, taddr(kS), true, kTile, id, true);
+    mma_k64(tmem + kD2b, taddr(kX), false, 16, taddr(kdS), true, kTile, id, false);
+    mma_k64(tmem + kD2b, taddr(kX), false, 16, taddr(kdSlo), true, kTile, id, true);
+    mma_k64(tmem + kD2b, taddr(kXlo), false, 16, taddr(kdS), true, kTile, id, true);
+    mma_commit(&sc.bar_mma);
+  }
+  if (!wait_mma(sc, phase)) goto teardown;
+  // A (fp32, for the solve), R = Diag(eta) V - Diag(eta e^{g_-}) X S, P, qz
+  {
+    float d[32], w[32];
+    const int i = r & 63;
+    if (r < 64) {
+      const float ei = sc.eta[i], gxi = sc.gx[i];
+      tmem_ld32(tl + kD1, d);
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) {
+        const int j = 32 * h + jj;
+        Af[i * kLdA + j] = (f1 && j < i) ? ei * expn(gxi - sc.g[j]) * d[jj] : 0.f;
+      }
+      tmem_ld32(tl + kD2a, d);
+      load_half_sw(tile(kV), i, h, w);
+      const float bx = f1 ? __expf(gxi) : 0.f;
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) w[jj] = w[jj] - bx * d[jj];  // residual part
+      store_half_sw(tile(kR), i, h, w, ei);
+    } else {
+      const float gi = sc.g[i];
+      tmem_ld32(tl + kD1, d);
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) {
+        const int j = 32 * h + jj;
+        d[jj] = (j <= i) ? expn(gi - sc.g[j]) * d[jj] : 0.f;
+      }
+      store_half_split(tile(kP), tile(kPlo), i, h, d);
+      tmem_ld32(tl + kD2a, d);
+      load_half_sw(tile(kdO), i, h, w);
+      float acc = 0.f;
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) acc += w[jj] * d[jj];
+      atomicAdd(&sc.qz[i], acc);
+    }
+  }
+  __syncthreads();
+  // ---- T = (I + A)^{-1} (T = I for Falcon-1A), as a bf16 tile
+  if (f1) {
+    solve_unit_lower(Af, Tf, Rs);
+  } else {
+    for (int idx = tid; idx < 64 * 64; idx += kBThreads)
+      Tf[(idx >> 6) * kLdT + (idx & 63)] = ((idx >> 6) == (idx & 63)) ? 1.f : 0.f;
+  }
+  __syncthreads();
+  if (r < 64) {
+    float v[32];
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) {
+      const int j = 32 * h + jj;
+      v[jj] = (j <= r) ? Tf[r * kLdT + j] : 0.f;
+    }
+    store_half_sw(tile(kT), r, h, v, 1.f);
+  }
+  publish_tiles();
+  // ---- U = T R
+  if (tid == 0) {
+    tc_fence_after();
+    mma_k64(tmem + kD3, taddr(kT), false, 16, taddr(kR), true, kTile,
+            idesc_bf16(128, 64, false, true), false);
+    mma_commit(&sc.bar_mma);
+  }
+  if (!wait_mma(sc, phase)) goto teardown;
+  if (r < 64) {
+    float d[32], xd[32];
+    tmem_ld32(tl + kD3, d);
+    store_half_sw(tile(kU), r, h, d, 1.f);
+    tmem_ld32(tl + kD2b, xd);  // <x_i, dS' U_i> = <(X dS')_i, U_i>
+    float acc = 0.f;
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) acc += xd[jj] * d[jj];
+    atomicAdd(&sc.xw[r], acc);
+  }
+  publish_tiles();
+  // ---- P^T dO
+  if (tid == 0) {
+    tc_fence_after();
+    const uint32_t id = idesc_bf16(128, 64, true, true);
+    mma_k64(tmem + kD3, taddr(kP), true, kTile, taddr(kdO), true, kTile, id, false);
+    mma_k64(tmem + kD3, taddr(kPlo), true, kTile, taddr(kdO), true, kTile, id, true);
+    mma_commit(&sc.bar_mma);
+  }
+  if (!wait_mma(sc, phase)) goto teardown;
+  // dU = P^T dO + Diag(e^{g_C - g}) X dS' (into the R tile)
+  if (r < 64) {
+    float d[32], xd[32];
+    tmem_ld32(tl + kD3, d);
+    tmem_ld32(tl + kD2b, xd);
+    const float f = expn(gC - sc.g[r]);
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) d[jj] += f * xd[jj];
+    store_half_split(tile(kR), tile(kdUlo), r, h, d);
+  }
+  publish_tiles();
+  // ---- dR = T^T dU
+  if (tid == 0) {
+    tc_fence_after();
+    const uint32_t id = idesc_bf16(128, 64, true, true);
+    mma_k64(tmem + kD3, taddr(kT), true, kTile, taddr(kR), true, kTile, id, false);
+    mma_k64(tmem + kD3, taddr(kT), true, kTile, taddr(kdUlo), true, kTile, id, true);
+    mma_commit(&sc.bar_mma);
+  }
+  if (!wait_mma(sc, phase)) goto teardown;
+  // dR tile, dv = Diag(eta) dR, rv_i = <dR_i, v_i>
+  if (r < 64) {
+    float d[32], w[32], xs[32];
+    tmem_ld32(tl + kD3, d);
+    store_half_sw(tile(kdR), r, h, d, 1.f);
+    load_half_sw(tile(kV), r, h, w);
+    tmem_ld32(tl + kD2a, xs);
+    const float bx = f1 ? __expf(sc.gx[r]) : 0.f;
+    float acc = 0.f, axs = 0.f;
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) {
+      acc += d[jj] * (w[jj] - bx * xs[jj]);  // <dR_i, v_i - e^{g_{i-1}} (X S)_i>
+      axs += d[jj] * xs[jj];                 // <dR_i, (X S)_i> = <x_i, (dR S^T)_i>
+    }
+    atomicAdd(&sc.rv[r], acc);
+    atomicAdd(&sc.xy[r], axs);
+    if (r < n) {
+      const float ei = sc.eta[r];
+      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(b.dv) +
+                                            (rowbase + t0 + r) * 64 + 32 * h);
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8) dst[q8] = pack8(d + 8 * q8, ei);
+    }
+  }
+  publish_tiles();
+  // ---- [dR; dO] U^T, [dR; dO] [S; dS']^T, U dS'^T
+  if (tid == 0) {
+    tc_fence_after();
+    mma_k64(tmem + kD6, taddr(kdR), false, 16, taddr(kU), false, 16,
+            idesc_bf16(128, 64, false, false), false);
+    mma_k64(tmem + kD7, taddr(kdR), false, 16, taddr(kS), false, 16,
+            idesc_bf16(128, 128, false, false), false);
+    mma_k64(tmem + kD8, taddr(kU), false, 16, taddr(kdS), false, 16,
+            idesc_bf16(128, 64, false, false), false);
+    mma_commit(&sc.bar_mma);
+  }
+  if (!wait_mma(sc, phase)) goto teardown;
+  {
+    float d[32], e[32];
+    const int i = r & 63;
+    if (r < 64) {
+      // dA (Falcon-1), its products with A, and dK
+      const float ei = sc.eta[i], gxi = sc.gx[i];
+      tmem_ld32(tl + kD6, d);
+      float sar = 0.f;
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) {
+        const int j = 32 * h + jj;
+        const float da = (f1 && j < i) ? -d[jj] : 0.f;
+        const float pa = da * Af[i * kLdA + j];
+        sar += pa;
+        if (pa != 0.f) atomicAdd(&sc.sAc[j], pa);
+        Tf[i * kLdT + j] = da * ei * expn(gxi - sc.g[j]);  // dK_ij
+      }
+      atomicAdd(&sc.sAr[i], sar);
+    } else {
+      // dP, its products with P (fp32, from the Gram accumulator), dP o E
+      const float gi = sc.g[i];
+      tmem_ld32(tl + kD6, d);
+      tmem_ld32(tl + kD1, e);
+      float spr = 0.f;
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) {
+        const int j = 32 * h + jj;
+        const float ef = (j <= i) ? expn(gi - sc.g[j]) : 0.f;
+        const float pp = d[jj] * ef * e[jj];
+        spr += pp;
+        if (pp != 0.f) atomicAdd(&sc.spc[j], pp);
+        d[jj] *= ef;
+      }
+      atomicAdd(&sc.spr[i], spr);
+      store_half_sw(tile(kdPE), i, h, d, 1.f);
+    }
+  }
+  __syncthreads();
+  // ---- the step-size cotangent, the log-prefix cotangent and its suffix sums,
+  //      then dbeta, dlambda and dE per token
+  if (tid < 64) {
+    const int i = tid;
+    float de = sc.rv[i];  // <dR_i, v_i - e^{g_{i-1}} (X S)_i>
+    if (f1 && sc.eta[i] != 0.f) de += sc.sAr[i] / sc.eta[i];
+    sc.deta[i] = de;
+    const float xwd = expn(gC - sc.g[i]) * sc.xw[i];
+    sc.xwd[i] = xwd;
+    sc.dg[i] = __expf(sc.g[i]) * sc.qz[i] + sc.spr[i] - sc.spc[i] - xwd - (f1 ? sc.sAc[i] : 0.f);
+  }
+  // dKs = dK + dK^T (rows of the dKs tile)
+  if (r < 64) {
+    float v[32];
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) {
+      const int j = 32 * h + jj;
+      v[jj] = Tf[r * kLdT + j] + Tf[j * kLdT + r];
+    }
+    store_half_sw(tile(kdKs), r, h, v, 1.f);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float tail = __expf(gC) * sc.sds;
+    for (int j = 0; j < 64; ++j) tail += sc.xwd[j];
+    sc.dg[63] += tail;
+    if (f1)
+      for (int i = 1; i < 64; ++i)
+        sc.dg[i - 1] += -sc.eta[i] * __expf(sc.gx[i]) * sc.xy[i] + sc.sAr[i];
+    float run = 0.f;
+    for (int i = 63; i >= 0; --i) {
+      run += sc.dg[i];
+      sc.dg[i] = run;
+    }
+  }
+  __syncthreads();
+  if (tid < 64) {
+    const int i = tid;
+    float dEi = 0.f;
+    if (i < n) {
+      float db = 0.f, dl_in = 0.f;
+      if (sc.flag[i] & kLive) {
+        float de = sc.deta[i], dl = 0.f;
+        if (!(sc.flag[i] & kClamped)) {
+          const float dal = -sc.dg[i] / sc.gam[i];
+          de += sc.lame[i] * dal;
+          dl += sc.eta[i] * dal;
+        }
+        db = de / sc.den[i];
+        const float dden = -de * sc.eta[i] / sc.den[i];
+        dEi = dden;
+        dl += dden;
+        if (a.ridge == FALCON_RIDGE_SCALED) {
+          dl_in = dl * sc.E[i];
+          dEi += dl * a.lambda[rowbase + t0 + i];
+        } else {
+          dl_in = dl;
+        }
+      }
+      b.dbeta[rowbase + t0 + i] = db;
+      b.dlambda[rowbase + t0 + i] = dl_in;
+    }
+    sc.dE[i] = dEi;
+  }
+  publish_tiles();
+  // ---- [junk; dPE] X, dPE^T Q + dKs X
+  if (tid == 0) {
+    tc_fence_after();
+    mma_k64(tmem + kD2a, taddr(kU), false, 16, taddr(kX), true, kTile,
+            idesc_bf16(128, 64, false, true), false);
+    mma_k64(tmem + kD2b, taddr(kdPE), true, kTile, taddr(kQt), true, kTile,
+            idesc_bf16(128, 64, true, true), false);
+    mma_k64(tmem + kD2b, taddr(kdKs), false, 16, taddr(kX), true, kTile,
+            idesc_bf16(128, 64, false, true), true);
+    mma_commit(&sc.bar_mma);
+  }
+  if (!wait_mma(sc, phase)) goto teardown;
+  {
+    float d[32], e[32], x[32];
+    const int i = r & 63;
+    if (r < 64) {
+      // dX_i -> the workspace (dk is formed from it)
+      tmem_ld32(tl + kD2b, d);
+      tmem_ld32(tl + kD8, e);
+      load_half_sw(tile(kX), i, h, x);
+      const float fw = expn(gC - sc.g[i]), fe = 2.f * sc.dE[i];
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) d[jj] += fw * e[jj] + fe * x[jj];
+      tmem_ld32(tl + kD7, e);
+      const float fy = f1 ? sc.eta[i] * __expf(sc.gx[i]) : 0.f;
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) d[jj] -= fy * e[jj];
+      if (i < n) {
+        float4* dst = reinterpret_cast<float4*>(dXw + (rowbase + t0 + i) * 64 + 32 * h);
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4)
+          dst[q4] = make_float4(d[4 * q4], d[4 * q4 + 1], d[4 * q4 + 2], d[4 * q4 + 3]);
+      }
+      sc.ssp[h][r] = 0.f;
+      sc.ugp[h][r] = 0.f;
+    } else {
+      // dQ_i = e^{g_i} (dO S^T)_i + (dPE X)_i, then dq = J_phi(q_i)^T dQ_i
+      tmem_ld32(tl + kD2a, d);
+      tmem_ld32(tl + kD7, e);
+      const float fg = __expf(sc.g[i]);
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) d[jj] += fg * e[jj];
+      float ss = 0.f, ug = 0.f;
+      if (i < n) {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            reinterpret_cast<const __nv_bfloat16*>(a.q) + (rowbase + t0 + i) * 64 + 32 * h);
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8) {
+          const uint4 pk = src[q8];
+          const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&pk);
+#pragma unroll
+          for (int e2 = 0; e2 < 4; ++e2) {
+            const float2 f = __bfloat1622float2(hv[e2]);
+            x[8 * q8 + 2 * e2] = f.x;
+            x[8 * q8 + 2 * e2 + 1] = f.y;
+          }
+        }
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          ss += x[jj] * x[jj];
+          ug += x[jj] * d[jj];
+        }
+      }
+      sc.ssp[h][r] = ss;
+      sc.ugp[h][r] = ug;
+    }
+    __syncthreads();
+    if (r >= 64 && i < n) {
+      const float ss = sc.ssp[0][r] + sc.ssp[1][r], ug = sc.ugp[0][r] + sc.ugp[1][r];
+      if (a.phi == FALCON_PHI_L2) {
+        const float nrm = sqrtf(ss);
+        if (nrm < 1e-12f) {
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) d[jj] *= 1e12f;
+        } else {
+          const float inv = 1.f / nrm, c2 = ug * inv * inv;
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) d[jj] = (d[jj] - x[jj] * c2) * inv;
+        }
+      } else if (a.phi == FALCON_PHI_RMS) {
+        const float s = rsqrtf(ss / 64.f + kEpsRms), c3 = s * s * s * ug / 64.f;
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) d[jj] = s * d[jj] - c3 * x[jj];
+      }
+      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(b.dq) +
+                                            (rowbase + t0 + i) * 64 + 32 * h);
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8) dst[q8] = pack8(d + 8 * q8, 1.f);
+    }
+  }
+
+teardown:
+  if (sc.fail && tid == 0) atomicExch(err, 1);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+bool tc_bwd_applies(int dtype, int m, int dv, int C) {
+  return dtype == FALCON_BF16 && m == 64 && dv == 64 && C == kBC;
+}
+
+cudaError_t launch_tc_bwd_grad(const BwdArgs& b, const float* S_starts, const float* dS_ends,
+                               float* dXw, int* err, cudaStream_t stream) {
+  const ChunkArgs& a = b.f;
+  const int nchunks = (int)((a.T + kBC - 1) / kBC);
+  CUtensorMap tm_k, tm_q, tm_v, tm_do;
+  if (!encode_rows_bf16(&tm_k, a.k, 64, (uint64_t)a.T, (uint64_t)a.BH, 64, kBC) ||
+      !encode_rows_bf16(&tm_q, a.q, 64, (uint64_t)a.T, (uint64_t)a.BH, 64, kBC) ||
+      !encode_rows_bf16(&tm_v, a.v, 64, (uint64_t)a.T, (uint64_t)a.BH, 64, kBC) ||
+      !encode_rows_bf16(&tm_do, b.dO, 64, (uint64_t)a.T, (uint64_t)a.BH, 64, kBC))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(tc_bwd_grad_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBwdSmem);
+  if (e != cudaSuccess) return e;
+  tc_bwd_grad_kernel<<<dim3(nchunks, (unsigned)a.BH), kBThreads, kBwdSmem, stream>>>(
+      b, nchunks, S_starts, dS_ends, dXw, err, tm_k, tm_q, tm_v, tm_do);
+  return cudaGetLastError();
+}
+
+}  // namespace falcon

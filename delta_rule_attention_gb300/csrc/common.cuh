@@ -117,7 +117,11 @@ struct BwdArgs {
   float *dbeta, *dlambda, *dS0, *dx_prev;
 };
 size_t bwd_workspace_bytes(int64_t BH, int64_t T, int m, int dv, int C);
-cudaError_t launch_bwd_chunked(const BwdArgs& b, cudaStream_t stream);
+cudaError_t launch_bwd_chunked(const BwdArgs& b, int* err, cudaStream_t stream);
+// Tensor-core per-chunk gradients (bf16, m = dv = 64, chunk 64).
+bool tc_bwd_applies(int dtype, int m, int dv, int C);
+cudaError_t launch_tc_bwd_grad(const BwdArgs& b, const float* S_starts, const float* dS_ends,
+                               float* dXw, int* err, cudaStream_t stream);
 
 struct DecodeArgs {
   int rule;

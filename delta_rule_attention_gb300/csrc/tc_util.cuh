@@ -1,0 +1,188 @@
+// Building blocks shared by the tensor-core kernels (forward map kernel and
+// the backward chunk kernel): bf16 packing, the 128-byte swizzled half-row
+// accessors of 64-wide tiles, phi's scale, and the fp32 unit-lower inverse
+// of a 64 x 64 chunk matrix with warp MMAs.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace falcon {
+namespace tcu {
+namespace {
+
+using namespace tc;
+
+constexpr int kLdA = 68;  // fp32 row stride of A (16-byte aligned rows)
+constexpr int kLdT = 65;  // fp32 row stride of T during the solve
+constexpr int kLdR = 49;  // fp32 row stride of the block right-hand sides
+
+// 1024-byte aligned base inside the dynamic shared buffer.  The offset is added
+// to the __shared__ pointer itself (not via an integer round trip), so the
+// compiler keeps the shared address space and emits shared loads and stores.
+__device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
+  const uint32_t off = (1024u - (smem_addr(p) & 1023u)) & 1023u;
+  return p + off;
+}
+
+__device__ __forceinline__ void flag_error(int* err) {
+  if (err) atomicExch(err, 1);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// 8 consecutive values (scaled) as one 16-byte bf16 chunk.
+__device__ __forceinline__ uint4 pack8(const float* v, float scale) {
+  uint4 pk;
+  pk.x = pack_bf16(scale * v[0], scale * v[1]);
+  pk.y = pack_bf16(scale * v[2], scale * v[3]);
+  pk.z = pack_bf16(scale * v[4], scale * v[5]);
+  pk.w = pack_bf16(scale * v[6], scale * v[7]);
+  return pk;
+}
+
+// Warp-level bf16 MMA, 16 x 8 x 16, fp32 accumulate (used for the 16-row
+// blocks of the triangular solve, below the 64-row minimum of tcgen05).
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4],
+                                         const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// A fragment (rows r0..r0+15, cols k0..k0+15) of a row-major fp32 matrix.
+__device__ __forceinline__ void frag_a(uint32_t (&a)[4], const float* M, int ld, int r0, int k0) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const float* p0 = M + (r0 + g) * ld + k0 + 2 * t;
+  const float* p1 = p0 + 8 * ld;
+  a[0] = pack_bf16(p0[0], p0[1]);
+  a[1] = pack_bf16(p1[0], p1[1]);
+  a[2] = pack_bf16(p0[8], p0[9]);
+  a[3] = pack_bf16(p1[8], p1[9]);
+}
+
+// B fragment (K rows k0..k0+15, N cols n0..n0+7) of a row-major fp32 K x N matrix.
+__device__ __forceinline__ void frag_b(uint32_t (&b)[2], const float* M, int ld, int k0, int n0) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const float* p = M + (k0 + 2 * t) * ld + n0 + g;
+  b[0] = pack_bf16(p[0], p[ld]);
+  b[1] = pack_bf16(p[8 * ld], p[9 * ld]);
+}
+
+// Half-row helpers: a thread owns columns 32h .. 32h+31 of row r (four
+// 16-byte chunks) of a 64-wide bf16 tile with the 128-byte swizzle.
+__device__ __forceinline__ void load_half_sw(const unsigned char* tile, int r, int h, float* v) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint4 pk =
+        *reinterpret_cast<const uint4*>(tile + r * 128 + (((4 * h + c) ^ (r & 7)) << 4));
+    const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&pk);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(hv[e]);
+      v[8 * c + 2 * e] = f.x;
+      v[8 * c + 2 * e + 1] = f.y;
+    }
+  }
+}
+
+__device__ __forceinline__ void store_half_sw(unsigned char* tile, int r, int h, const float* v,
+                                              float scale) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    *reinterpret_cast<uint4*>(tile + r * 128 + (((4 * h + c) ^ (r & 7)) << 4)) =
+        pack8(v + 8 * c, scale);
+}
+
+__device__ __forceinline__ float sumsq32(const float* v) {
+  float p[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < 32; ++j) p[j & 7] += v[j] * v[j];
+  return ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
+}
+
+// phi's scale for a row of m values with squared norm ss: 1 / max(||u||,
+// 1e-12) for the l2 map (0 for an all-zero row, which makes no difference to
+// phi(u) = 0 and keeps products with the exponential factors finite),
+// 1 / sqrt(ss / m + eps_rms) for RMSNorm, 1 for the identity.
+__device__ __forceinline__ float phi_scale(float ss, int m, int phi) {
+  if (phi == FALCON_PHI_RMS) return rsqrtf(ss / (float)m + kEpsRms);
+  if (phi != FALCON_PHI_L2) return 1.f;
+  return ss > 0.f ? rsqrtf(fmaxf(ss, 1e-24f)) : 0.f;
+}
+
+// T = (I + A)^{-1} for the strictly lower 64 x 64 A (rows of kLdA floats),
+// eight warps.  Diagonal block b = warp & 3 is inverted in fp32 by forward
+// substitution: warp w owns columns 8 (w >> 2) .. +7 of the block, two lanes
+// per row with four columns each, and broadcasts finished rows by shuffles;
+// the result stays as the diagonal block of T.  Block rows b = 1..3 then
+// follow T_{b,<b} = T_bb (-A_{b,<b} T_{<b}) with warp MMAs, one n-tile per warp.
+__device__ void solve_unit_lower(const float* As, float* Ts, float* Rs) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  {
+    const int b = warp & 3, hh = warp >> 2, rr = lane >> 1, q = lane & 1, row = 16 * b + rr;
+    float arow[15];
+#pragma unroll
+    for (int k = 0; k < 15; ++k) arow[k] = As[row * kLdA + 16 * b + k];
+    float dv4[4];
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) dv4[jj] = (8 * hh + 4 * q + jj == rr) ? 1.f : 0.f;
+#pragma unroll
+    for (int k = 0; k < 15; ++k) {
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const float tkj = __shfl_sync(0xffffffffu, dv4[jj], 2 * k + q);
+        if (rr > k) dv4[jj] -= arow[k] * tkj;
+      }
+    }
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) Ts[row * kLdT + 16 * b + 8 * hh + 4 * q + jj] = dv4[jj];
+  }
+  __syncthreads();
+  const int g = lane >> 2, t = lane & 3;
+  for (int b = 1; b < 4; ++b) {
+    const int w = 16 * b;  // columns left of block b: 2b n-tiles of 8
+    const int nt = warp;
+    // R = -A[w:w+16, 0:w] T[0:w, 0:w]; T[k][n] = 0 for k < n, so those k-steps are skipped.
+    if (nt < 2 * b) {
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int kb = nt >> 1; kb < b; ++kb) {
+        uint32_t fa[4], fb[2];
+        frag_a(fa, As, kLdA, w, 16 * kb);
+        frag_b(fb, Ts, kLdT, 16 * kb, 8 * nt);
+        mma16816(d, fa, fb);
+      }
+      float* r0 = Rs + g * kLdR + 8 * nt + 2 * t;
+      r0[0] = -d[0];
+      r0[1] = -d[1];
+      r0[8 * kLdR] = -d[2];
+      r0[8 * kLdR + 1] = -d[3];
+    }
+    __syncthreads();
+    // T[w:w+16, 0:w] = T_bb R  (T_bb: diagonal block b of T)
+    if (nt < 2 * b) {
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t fa[4], fb[2];
+      frag_a(fa, Ts, kLdT, w, w);
+      frag_b(fb, Rs, kLdR, 0, 8 * nt);
+      mma16816(d, fa, fb);
+      float* t0 = Ts + (w + g) * kLdT + 8 * nt + 2 * t;
+      t0[0] = d[0];
+      t0[1] = d[1];
+      t0[8 * kLdT] = d[2];
+      t0[8 * kLdT + 1] = d[3];
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+}  // namespace tcu
+}  // namespace falcon

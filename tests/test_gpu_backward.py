@@ -108,6 +108,25 @@ def test_backward_feature_and_ridge_variants(falcon, rule, phi, ridge):
 
 
 @pytest.mark.parametrize("rule", ["falcon1", "falcon1a"])
+@pytest.mark.parametrize("phi,ridge,lam_shift", [("l2", "given", -2.0), ("rms", "scaled", -2.0),
+                                                 ("identity", "given", -2.0),
+                                                 ("l2", "given", 3.0)])
+def test_backward_tensor_core_shape(falcon, rule, phi, ridge, lam_shift):
+    """bf16, m = d_v = 64, chunk 64 (the tensor-core chunk kernel): carried
+    state and feature, end cotangents, a ragged tail; lam_shift 3 puts many
+    tokens on the clamped decay."""
+    B, H, T = 2, 2, 3 * 64 + 17
+    x = workloads.random_case(B, H, T, 64, 64, torch.bfloat16, seed=51, lam_shift=lam_shift,
+                              device="cuda", with_state=True, with_x_prev=True)
+    ct = workloads.cotangents(B, H, T, 64, 64, torch.bfloat16, seed=51, device="cuda", ends=True)
+    got = run_bwd(falcon, rule, x, ct, 64, phi, ridge)
+    ref = ref_bwd(rule, x, ct, phi, ridge)
+    for n in got:
+        assert np.isfinite(got[n]).all(), n
+    check(got, ref, TOL[torch.bfloat16])
+
+
+@pytest.mark.parametrize("rule", ["falcon1", "falcon1a"])
 def test_backward_clamp_active(falcon, rule):
     """lambda = softplus(n + 3), beta = 1.95: the decay clamp fires on many
     tokens (no gradient through alpha there) and chunk decays underflow."""
