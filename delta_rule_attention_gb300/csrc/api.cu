@@ -306,7 +306,7 @@ int falcon1a_fwd_chunked(const falcon_shape* s, const void* q, const void* k, co
 
 size_t falcon_bwd_workspace_bytes(const falcon_shape* s) {
   if (check_shape(s) != FALCON_OK) return 0;
-  return falcon::bwd_workspace_bytes(s->B * s->H, s->T, s->m, s->dv, s->chunk);
+  return falcon::bwd_workspace_bytes(s->dtype, s->B * s->H, s->T, s->m, s->dv, s->chunk);
 }
 
 int falcon1_bwd_chunked(const falcon_shape* s, const void* q, const void* k, const void* v,

@@ -32,6 +32,11 @@
 //      token), dx_prev = dX_1 when the call carried x_prev.
 // The clamped branch of the decay is a constant (no gradient through alpha);
 // the sentinel token passes no gradient to beta_1, lambda_1.
+//
+// For bf16 inputs with m = dv = 64 and chunk 64, steps 1-3 run on the
+// tensor cores instead: the tensor-core forward (maps and scan, recording the
+// chunk-start states), its reverse scan (chunk_tc_bwd.cu) and the tensor-core
+// chunk kernel; step 4 is shared.
 #include "common.cuh"
 
 namespace falcon {
@@ -44,7 +49,7 @@ constexpr int kWarps = kThreads / 32;
 __host__ __device__ inline int64_t align_floats(int64_t n) { return (n + 63) & ~int64_t(63); }
 
 struct BwdLayout {  // float offsets inside the workspace
-  int64_t maps, S_starts, dS_ends, dX, total;
+  int64_t maps, S_starts, dS_ends, dX, o, S_out, total;
 };
 
 __host__ __device__ inline BwdLayout bwd_layout(int64_t BH, int64_t T, int m, int dv, int C) {
@@ -55,7 +60,28 @@ __host__ __device__ inline BwdLayout bwd_layout(int64_t BH, int64_t T, int m, in
   L.dS_ends = align_floats(L.S_starts + BH * nch * (int64_t)m * dv);
   L.dX = align_floats(L.dS_ends + BH * nch * (int64_t)m * dv);
   L.total = align_floats(L.dX + BH * T * (int64_t)m);
+  L.o = L.S_out = L.total;
   return L;
+}
+
+// Tensor-core path: the forward's bf16 maps, the recomputed forward's o and
+// S_T (written, not used), then the same state and cotangent buffers.
+BwdLayout tc_bwd_layout(int64_t BH, int64_t T) {
+  const int64_t nch = (T + 63) / 64;
+  BwdLayout L;
+  L.maps = 0;
+  L.S_starts = align_floats((int64_t)((tc_workspace_bytes(64, BH, T) + 3) / 4));
+  L.dS_ends = align_floats(L.S_starts + BH * nch * 4096);
+  L.dX = align_floats(L.dS_ends + BH * nch * 4096);
+  L.o = align_floats(L.dX + BH * T * 64);
+  L.S_out = align_floats(L.o + BH * T * 32);  // bf16 o: 32 floats per row
+  L.total = align_floats(L.S_out + BH * 4096);
+  return L;
+}
+
+bool use_tc_bwd(const ChunkArgs& a) {
+  return tc_bwd_applies(a.dtype, a.m, a.dv, a.C) &&
+         tc_path_applies(a.dtype, a.m, a.dv, a.C, a.BH, a.T);
 }
 
 // phi of one m-vector (m <= 128) held by a warp, lane owning elements lane +
@@ -540,42 +566,52 @@ __global__ void __launch_bounds__(kThreads) bwd_feature_kernel(BwdArgs b, const 
 cudaError_t launch_generic_grad(const BwdArgs& b, int nchunks, const float* S_starts,
                                 const float* dS_ends, float* dXw, cudaStream_t stream);
 
-size_t bwd_workspace_bytes(int64_t BH, int64_t T, int m, int dv, int C) {
-  return (size_t)bwd_layout(BH, T, m, dv, C).total * sizeof(float);
+size_t bwd_workspace_bytes(int dtype, int64_t BH, int64_t T, int m, int dv, int C) {
+  const bool tc = tc_bwd_applies(dtype, m, dv, C) && tc_path_applies(dtype, m, dv, C, BH, T);
+  return (size_t)(tc ? tc_bwd_layout(BH, T) : bwd_layout(BH, T, m, dv, C)).total * sizeof(float);
 }
 
 cudaError_t launch_bwd_chunked(const BwdArgs& b, int* err, cudaStream_t stream) {
   const ChunkArgs& a = b.f;
   const int m = a.m, dv = a.dv, C = a.C;
   const int nchunks = (int)((a.T + C - 1) / C);
-  const BwdLayout L = bwd_layout(a.BH, a.T, m, dv, C);
+  const bool tc = use_tc_bwd(a);
+  const BwdLayout L = tc ? tc_bwd_layout(a.BH, a.T) : bwd_layout(a.BH, a.T, m, dv, C);
   float* ws = reinterpret_cast<float*>(a.workspace);
+  cudaError_t e;
 
   // 1. chunk maps and the state entering every chunk
   ChunkArgs f = a;
-  f.o = nullptr;
-  f.S_out = nullptr;
   f.x_last = nullptr;
   f.workspace = ws + L.maps;
-  cudaError_t e = launch_generic_chunked(f, stream, ws + L.S_starts);
+  if (tc) {
+    f.o = ws + L.o;
+    f.S_out = ws + L.S_out;
+    f.S_starts = ws + L.S_starts;
+    e = launch_tc_chunked(f, err, stream);
+  } else {
+    f.o = nullptr;
+    f.S_out = nullptr;
+    e = launch_generic_chunked(f, stream, ws + L.S_starts);
+  }
   if (e != cudaSuccess) return e;
 
-  // 2. reverse scan of the state cotangent
-  const int NV = dv < 32 ? dv : 32;
-  const size_t scan_smem =
-      sizeof(float) * ((size_t)m * NV + (size_t)(m + C) * m + (size_t)(m + C) * NV);
-  e = cudaFuncSetAttribute(bwd_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)scan_smem);
-  if (e != cudaSuccess) return e;
-  bwd_scan_kernel<<<dim3((unsigned)a.BH, dv / NV), kThreads, scan_smem, stream>>>(
-      b, nchunks, NV, ws + L.maps, ws + L.dS_ends);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-
-  // 3. per-chunk gradients
-  if (tc_bwd_applies(a.dtype, m, dv, C)) {
+  // 2. reverse scan of the state cotangent, 3. per-chunk gradients
+  if (tc) {
+    e = launch_tc_bwd_scan(b, ws + L.maps, ws + L.dS_ends, err, stream);
+    if (e != cudaSuccess) return e;
     e = launch_tc_bwd_grad(b, ws + L.S_starts, ws + L.dS_ends, ws + L.dX, err, stream);
   } else {
+    const int NV = dv < 32 ? dv : 32;
+    const size_t scan_smem =
+        sizeof(float) * ((size_t)m * NV + (size_t)(m + C) * m + (size_t)(m + C) * NV);
+    e = cudaFuncSetAttribute(bwd_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)scan_smem);
+    if (e != cudaSuccess) return e;
+    bwd_scan_kernel<<<dim3((unsigned)a.BH, dv / NV), kThreads, scan_smem, stream>>>(
+        b, nchunks, NV, ws + L.maps, ws + L.dS_ends);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     e = launch_generic_grad(b, nchunks, ws + L.S_starts, ws + L.dS_ends, ws + L.dX, stream);
   }
   if (e != cudaSuccess) return e;

@@ -49,10 +49,6 @@ using namespace tc;
 using namespace tcu;
 
 constexpr int kC = 64;
-// Chunk map for m = d_v = 64: Mc as the scan's A operand, Nc, e^{g_C}.
-constexpr uint32_t kMcBytes = 128 * 128;  // 128 rows x 64 bf16 (swizzled operand image)
-constexpr uint32_t kNcBytes = 128 * 128;  // 128 rows x 64 bf16 (rows swizzled by 16 B)
-constexpr uint32_t kMapBytes = kMcBytes + kNcBytes + 128;  // + e^{g_C} (padded)
 // A chunk whose log-decay spans at most this much factors e^{a-b} as
 // e^{a-r} e^{r-b} (both factors stay within fp32 range).
 constexpr float kFactorSpan = 80.f;
@@ -542,6 +538,8 @@ __device__ __forceinline__ void add_bf16x16(float* d, uint4 p0, uint4 p1) {
   }
 }
 
+// kRecord: also write the state entering every chunk to a.S_starts.
+template <bool kRecord>
 __global__ void __launch_bounds__(kScanThreads)
     tc_chunk_scan_kernel(ChunkArgs a, int nchunks, int c_begin, int n, const float* S_in, int* err,
                          const __grid_constant__ CUtensorMap tm_o) {
@@ -630,6 +628,13 @@ __global__ void __launch_bounds__(kScanThreads)
     for (int c = 0; c < n; ++c) {
       // Exits are warp-uniform, so every __syncwarp sees all lanes.
       if (__any_sync(0xffffffffu, *fail)) break;
+      if (kRecord) {  // the state entering chunk c (for the backward pass)
+        float4* dst = reinterpret_cast<float4*>(
+            a.S_starts + (((size_t)bh * nchunks + c_begin + c) * 64 + row) * 64 + 16 * qc);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          dst[q4] = make_float4(S[4 * q4], S[4 * q4 + 1], S[4 * q4 + 2], S[4 * q4 + 3]);
+      }
       const int st = c % kStages, b = c & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&s.full[st], (uint32_t)(c / kStages) & 1u))) {
         *fail = 1;
@@ -1083,8 +1088,13 @@ cudaError_t launch_scan_range(const ChunkArgs& a, int nchunks, int c_begin, int 
     return launch_scan(tc_chunk_scan128_kernel, (unsigned)(2 * a.BH), kScan128Threads,
                        sizeof(Scan128Smem) + 1024, pdl, a, nchunks, c_begin, n, S_in, err, tm_o,
                        stream);
-  return launch_scan(tc_chunk_scan_kernel, (unsigned)a.BH, kScanThreads, sizeof(ScanSmem) + 1024,
-                     pdl, a, nchunks, c_begin, n, S_in, err, tm_o, stream);
+  if (a.S_starts)
+    return launch_scan(tc_chunk_scan_kernel<true>, (unsigned)a.BH, kScanThreads,
+                       sizeof(ScanSmem) + 1024, pdl, a, nchunks, c_begin, n, S_in, err, tm_o,
+                       stream);
+  return launch_scan(tc_chunk_scan_kernel<false>, (unsigned)a.BH, kScanThreads,
+                     sizeof(ScanSmem) + 1024, pdl, a, nchunks, c_begin, n, S_in, err, tm_o,
+                     stream);
 }
 
 template <int M>

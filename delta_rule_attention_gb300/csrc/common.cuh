@@ -86,6 +86,9 @@ struct ChunkArgs {
   void* o;
   float *S_out, *x_last;
   void* workspace;
+  // Tensor-core path, m = 64: the state entering every chunk is also written
+  // here when non-null ([B*H, chunks, m, dv] f32; for the backward pass).
+  float* S_starts = nullptr;
 };
 size_t generic_workspace_bytes(int64_t BH, int64_t T, int m, int dv, int C);
 // a.o and a.S_out may be null (not written); S_starts (nullable) receives the
@@ -116,12 +119,15 @@ struct BwdArgs {
   void *dq, *dk, *dv;
   float *dbeta, *dlambda, *dS0, *dx_prev;
 };
-size_t bwd_workspace_bytes(int64_t BH, int64_t T, int m, int dv, int C);
+size_t bwd_workspace_bytes(int dtype, int64_t BH, int64_t T, int m, int dv, int C);
 cudaError_t launch_bwd_chunked(const BwdArgs& b, int* err, cudaStream_t stream);
 // Tensor-core per-chunk gradients (bf16, m = dv = 64, chunk 64).
 bool tc_bwd_applies(int dtype, int m, int dv, int C);
 cudaError_t launch_tc_bwd_grad(const BwdArgs& b, const float* S_starts, const float* dS_ends,
                                float* dXw, int* err, cudaStream_t stream);
+// Reverse scan of the state cotangent over the tensor-core forward's maps.
+cudaError_t launch_tc_bwd_scan(const BwdArgs& b, const void* maps, float* dS_ends, int* err,
+                               cudaStream_t stream);
 
 struct DecodeArgs {
   int rule;

@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(F2Cfg<M>::kThreads)
   const RawLayout R = raw_layout(M, a.dv, es);
   unsigned char* raw0 = smem_raw + ((sizeof(F2Smem<M>) + 127) & ~size_t(127));
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, lane = tid & 31;
   const int64_t bh = blockIdx.x / ncg;
   const int cg = blockIdx.x % ncg;
   const int cl = tid / C::kP;    // local column

@@ -15,6 +15,12 @@ namespace {
 
 using namespace tc;
 
+// Chunk map of the m = d_v = 64 tensor-core forward, per (head, chunk): Mc as
+// the scan's A operand, Nc, e^{g_C}.
+constexpr uint32_t kMcBytes = 128 * 128;  // 128 rows x 64 bf16 (swizzled operand image)
+constexpr uint32_t kNcBytes = 128 * 128;  // 128 rows x 64 bf16 (rows swizzled by 16 B)
+constexpr uint32_t kMapBytes = kMcBytes + kNcBytes + 128;  // + e^{g_C} (padded)
+
 constexpr int kLdA = 68;  // fp32 row stride of A (16-byte aligned rows)
 constexpr int kLdT = 65;  // fp32 row stride of T during the solve
 constexpr int kLdR = 49;  // fp32 row stride of the block right-hand sides
