@@ -62,6 +62,7 @@ constexpr uint32_t kTfOff = kAfOff + 64 * kLdA * 4;     // T (fp32, kLdT), later
 constexpr uint32_t kRsOff = kTfOff + 64 * kLdT * 4;     // solve scratch (16 x kLdR)
 constexpr uint32_t kScOff = kRsOff + 4096;
 static_assert(16 * kLdR * 4 <= 4096, "solve scratch");
+static_assert(64 * 65 * 4 <= 4 * kTile, "dP o P over the dead low-part tiles");
 
 struct BwdScalars {
   float eta[64], g[64], gx[64], E[64], lame[64], den[64], gam[64];
@@ -109,6 +110,35 @@ __device__ __forceinline__ bool wait_mma(BwdScalars& sc, uint32_t& phase) {
   return !__syncthreads_or(sc.fail);
 }
 
+// Warp-wide scans of 64 values, two per lane.  Prefix: lane l takes elements
+// 2l, 2l+1 and writes the exclusive and inclusive prefix sums.  Suffix: lane l
+// takes elements 63-2l, 62-2l of v and writes sum_{j >= i} v_j to out.
+__device__ __forceinline__ float warp_incl_scan(float s) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float t = __shfl_up_sync(0xffffffffu, s, o);
+    if (lane >= o) s += t;
+  }
+  return s;
+}
+__device__ __forceinline__ void warp_prefix64(float* v, float* excl) {
+  const int l = threadIdx.x & 31;
+  const float a = v[2 * l], b = v[2 * l + 1];
+  const float e = warp_incl_scan(a + b) - (a + b);
+  excl[2 * l] = e;
+  excl[2 * l + 1] = e + a;
+  v[2 * l] = e + a;
+  v[2 * l + 1] = (e + a) + b;
+}
+__device__ __forceinline__ void warp_suffix64(const float* v0, const float* v1, float* out) {
+  const int l = threadIdx.x & 31;
+  const float a = v0[0], b = v1[0];  // elements 63 - 2l and 62 - 2l
+  const float e = warp_incl_scan(a + b) - (a + b);
+  out[63 - 2 * l] = e + a;
+  out[62 - 2 * l] = (e + a) + b;
+}
+
 // Generic-proxy tile writes of this CTA become visible to the next MMA.
 __device__ __forceinline__ void publish_tiles() {
   tc_fence_before();
@@ -130,6 +160,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
   float* Rs = reinterpret_cast<float*>(base + kRsOff);
   BwdScalars& sc = *reinterpret_cast<BwdScalars*>(base + kScOff);
   auto tile = [&](int i) { return base + i * kTile; };
+  float* Pm = reinterpret_cast<float*>(base + kXlo * kTile);  // dP o P, 64 x 65 (late)
   auto taddr = [&](int i) { return smem_addr(base + i * kTile); };
 
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -243,14 +274,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
     sc.flag[i] = fl;
   }
   __syncthreads();
-  if (tid == 0) {
-    float run = 0.f;
-    for (int i = 0; i < 64; ++i) {
-      sc.gx[i] = run;
-      run += sc.g[i];
-      sc.g[i] = run;
-    }
-  }
+  if (warp == 0) warp_prefix64(sc.g, sc.gx);  // g: inclusive, gx: exclusive
   publish_tiles();
   gC = sc.g[63];
 
@@ -422,7 +446,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
         const float da = (f1 && j < i) ? -d[jj] : 0.f;
         const float pa = da * Af[i * kLdA + j];
         sar += pa;
-        if (pa != 0.f) atomicAdd(&sc.sAc[j], pa);
+        Af[i * kLdA + j] = pa;  // dA o A (A is not needed any more)
         Tf[i * kLdT + j] = da * ei * expn(gxi - sc.g[j]);  // dK_ij
       }
       atomicAdd(&sc.sAr[i], sar);
@@ -438,7 +462,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
         const float ef = (j <= i) ? expn(gi - sc.g[j]) : 0.f;
         const float pp = d[jj] * ef * e[jj];
         spr += pp;
-        if (pp != 0.f) atomicAdd(&sc.spc[j], pp);
+        Pm[i * 65 + j] = pp;  // dP o P
         d[jj] *= ef;
       }
       atomicAdd(&sc.spr[i], spr);
@@ -450,12 +474,19 @@ __global__ void __launch_bounds__(kBThreads, 1)
   //      then dbeta, dlambda and dE per token
   if (tid < 64) {
     const int i = tid;
+    float sac = 0.f, spc = 0.f;  // column sums of dA o A and dP o P
+    for (int k = 0; k < 64; ++k) {
+      sac += Af[k * kLdA + i];
+      spc += Pm[k * 65 + i];
+    }
+    sc.sAc[i] = sac;
+    sc.spc[i] = spc;
     float de = sc.rv[i];  // <dR_i, v_i - e^{g_{i-1}} (X S)_i>
     if (f1 && sc.eta[i] != 0.f) de += sc.sAr[i] / sc.eta[i];
     sc.deta[i] = de;
     const float xwd = expn(gC - sc.g[i]) * sc.xw[i];
     sc.xwd[i] = xwd;
-    sc.dg[i] = __expf(sc.g[i]) * sc.qz[i] + sc.spr[i] - sc.spc[i] - xwd - (f1 ? sc.sAc[i] : 0.f);
+    sc.dg[i] = __expf(sc.g[i]) * sc.qz[i] + sc.spr[i] - spc - xwd - (f1 ? sac : 0.f);
   }
   // dKs = dK + dK^T (rows of the dKs tile)
   if (r < 64) {
@@ -468,18 +499,22 @@ __global__ void __launch_bounds__(kBThreads, 1)
     store_half_sw(tile(kdKs), r, h, v, 1.f);
   }
   __syncthreads();
-  if (tid == 0) {
-    float tail = __expf(gC) * sc.sds;
-    for (int j = 0; j < 64; ++j) tail += sc.xwd[j];
-    sc.dg[63] += tail;
-    if (f1)
-      for (int i = 1; i < 64; ++i)
-        sc.dg[i - 1] += -sc.eta[i] * __expf(sc.gx[i]) * sc.xy[i] + sc.sAr[i];
-    float run = 0.f;
-    for (int i = 63; i >= 0; --i) {
-      run += sc.dg[i];
-      sc.dg[i] = run;
+  if (warp == 0) {
+    // terms at index i - 1 (Falcon-1) and at C - 1, then the suffix sums
+    const int l = tid;
+    const float tail = warp_sum(sc.xwd[2 * l] + sc.xwd[2 * l + 1]) + __expf(gC) * sc.sds;
+    float v[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int i = 63 - 2 * l - u;
+      float x = sc.dg[i];
+      if (f1 && i < 63)
+        x += -sc.eta[i + 1] * __expf(sc.gx[i + 1]) * sc.xy[i + 1] + sc.sAr[i + 1];
+      if (i == 63) x += tail;
+      v[u] = x;
     }
+    __syncwarp();
+    warp_suffix64(&v[0], &v[1], sc.dg);
   }
   __syncthreads();
   if (tid < 64) {
