@@ -72,8 +72,8 @@ BwdLayout tc_bwd_layout(int64_t BH, int64_t T) {
   L.maps = 0;
   L.S_starts = align_floats((int64_t)((tc_workspace_bytes(64, BH, T) + 3) / 4));
   L.dS_ends = align_floats(L.S_starts + BH * nch * 4096);
-  L.dX = align_floats(L.dS_ends + BH * nch * 4096);
-  L.o = align_floats(L.dX + BH * T * 64);
+  L.dX = align_floats(L.dS_ends + BH * nch * 4096);  // row 0 of every chunk's dX
+  L.o = align_floats(L.dX + BH * nch * 64);
   L.S_out = align_floats(L.o + BH * T * 32);  // bf16 o: 32 floats per row
   L.total = align_floats(L.S_out + BH * 4096);
   return L;
@@ -600,7 +600,8 @@ cudaError_t launch_bwd_chunked(const BwdArgs& b, int* err, cudaStream_t stream) 
   if (tc) {
     e = launch_tc_bwd_scan(b, ws + L.maps, ws + L.dS_ends, err, stream);
     if (e != cudaSuccess) return e;
-    e = launch_tc_bwd_grad(b, ws + L.S_starts, ws + L.dS_ends, ws + L.dX, err, stream);
+    // dq, dv, dbeta, dlambda and dk (the chunk-end tokens by a small kernel)
+    return launch_tc_bwd_grad(b, ws + L.S_starts, ws + L.dS_ends, ws + L.dX, err, stream);
   } else {
     const int NV = dv < 32 ? dv : 32;
     const size_t scan_smem =

@@ -69,6 +69,7 @@ struct BwdScalars {
   float deta[64], dg[64], dE[64], xwd[64];
   // accumulated with shared-memory atomics (zeroed first)
   float qz[64], rv[64], xy[64], xw[64], sAr[64], sAc[64], spr[64], spc[64];
+  float ssk[64];      // ||k_{t0+i-1}||^2 of the raw write-feature rows
   float ssp[2][128];  // half-row partial sums
   float ugp[2][128];
   float sds;          // <dS', S>_F
@@ -139,6 +140,44 @@ __device__ __forceinline__ void warp_suffix64(const float* v0, const float* v1, 
   out[62 - 2 * l] = (e + a) + b;
 }
 
+// g <- J_phi(u)^T g for a half row (32 values) of a 64-wide feature row u,
+// given the row's ||u||^2 and <u, g> (phi as in the forward: l2 u / ||u||,
+// RMSNorm u / sqrt(||u||^2 / 64 + eps_rms), or the identity).
+__device__ __forceinline__ void phi_vjp_half(float* g, const float* u, float ss, float ug,
+                                             int phi) {
+  if (phi == FALCON_PHI_L2) {
+    const float nrm = sqrtf(ss);
+    if (nrm < 1e-12f) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) g[j] *= 1e12f;
+    } else {
+      const float inv = 1.f / nrm, c2 = ug * inv * inv;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) g[j] = (g[j] - u[j] * c2) * inv;
+    }
+  } else if (phi == FALCON_PHI_RMS) {
+    const float sr = rsqrtf(ss / 64.f + kEpsRms), c3 = sr * sr * sr * ug / 64.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) g[j] = sr * g[j] - c3 * u[j];
+  }
+}
+
+// 32 bf16 values (64 bytes) from global memory.
+__device__ __forceinline__ void load_bf16x32(const void* p, float* v) {
+  const uint4* src = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+  for (int q8 = 0; q8 < 4; ++q8) {
+    const uint4 pk = src[q8];
+    const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&pk);
+#pragma unroll
+    for (int e2 = 0; e2 < 4; ++e2) {
+      const float2 f = __bfloat1622float2(hv[e2]);
+      v[8 * q8 + 2 * e2] = f.x;
+      v[8 * q8 + 2 * e2 + 1] = f.y;
+    }
+  }
+}
+
 // Generic-proxy tile writes of this CTA become visible to the next MMA.
 __device__ __forceinline__ void publish_tiles() {
   tc_fence_before();
@@ -148,7 +187,7 @@ __device__ __forceinline__ void publish_tiles() {
 
 __global__ void __launch_bounds__(kBThreads, 1)
     tc_bwd_grad_kernel(BwdArgs b, int nchunks, const float* S_starts, const float* dS_ends,
-                       float* dXw, int* err, const __grid_constant__ CUtensorMap tm_k,
+                       float* edge, int* err, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_do) {
@@ -248,7 +287,10 @@ __global__ void __launch_bounds__(kBThreads, 1)
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] *= s;
     store_half_split(tile(kX), tile(kXlo), r, h, v);
-    if (xrow && h == 0) sc.E[i] = ss * s * s;
+    if (xrow && h == 0) {
+      sc.E[i] = ss * s * s;
+      sc.ssk[i] = ss;
+    }
   }
   __syncthreads();
   // ---- per-token scalars as the forward forms them, then the log prefixes
@@ -559,81 +601,64 @@ __global__ void __launch_bounds__(kBThreads, 1)
   }
   if (!wait_mma(sc, phase)) goto teardown;
   {
-    float d[32], e[32], x[32];
+    float d[32], e[32], u[32];
     const int i = r & 63;
+    float ss = 0.f, ug = 0.f;
     if (r < 64) {
-      // dX_i -> the workspace (dk is formed from it)
+      // dX_i; row i >= 1 is the cotangent of x_i = phi(k_{t0+i-1}), so dk of
+      // that token follows here; row 0 (the previous chunk's last token, or
+      // x_prev) goes to the edge buffer.
       tmem_ld32(tl + kD2b, d);
       tmem_ld32(tl + kD8, e);
-      load_half_sw(tile(kX), i, h, x);
+      load_half_sw(tile(kX), i, h, u);
       const float fw = expn(gC - sc.g[i]), fe = 2.f * sc.dE[i];
 #pragma unroll
-      for (int jj = 0; jj < 32; ++jj) d[jj] += fw * e[jj] + fe * x[jj];
+      for (int jj = 0; jj < 32; ++jj) d[jj] += fw * e[jj] + fe * u[jj];
       tmem_ld32(tl + kD7, e);
       const float fy = f1 ? sc.eta[i] * __expf(sc.gx[i]) : 0.f;
 #pragma unroll
       for (int jj = 0; jj < 32; ++jj) d[jj] -= fy * e[jj];
-      if (i < n) {
-        float4* dst = reinterpret_cast<float4*>(dXw + (rowbase + t0 + i) * 64 + 32 * h);
+      if (i == 0) {
+        float4* dst = reinterpret_cast<float4*>(edge + (bh * nchunks + c) * 64 + 32 * h);
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4)
           dst[q4] = make_float4(d[4 * q4], d[4 * q4 + 1], d[4 * q4 + 2], d[4 * q4 + 3]);
+      } else if (i < n) {
+        load_bf16x32(reinterpret_cast<const __nv_bfloat16*>(a.k) + (rowbase + t0 + i - 1) * 64 +
+                         32 * h, u);
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) ug += u[jj] * d[jj];
+        ss = sc.ssk[i];
       }
-      sc.ssp[h][r] = 0.f;
-      sc.ugp[h][r] = 0.f;
     } else {
-      // dQ_i = e^{g_i} (dO S^T)_i + (dPE X)_i, then dq = J_phi(q_i)^T dQ_i
+      // dQ_i = e^{g_i} (dO S^T)_i + (dPE X)_i
       tmem_ld32(tl + kD2a, d);
       tmem_ld32(tl + kD7, e);
       const float fg = __expf(sc.g[i]);
 #pragma unroll
       for (int jj = 0; jj < 32; ++jj) d[jj] += fg * e[jj];
-      float ss = 0.f, ug = 0.f;
       if (i < n) {
-        const uint4* src = reinterpret_cast<const uint4*>(
-            reinterpret_cast<const __nv_bfloat16*>(a.q) + (rowbase + t0 + i) * 64 + 32 * h);
-#pragma unroll
-        for (int q8 = 0; q8 < 4; ++q8) {
-          const uint4 pk = src[q8];
-          const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&pk);
-#pragma unroll
-          for (int e2 = 0; e2 < 4; ++e2) {
-            const float2 f = __bfloat1622float2(hv[e2]);
-            x[8 * q8 + 2 * e2] = f.x;
-            x[8 * q8 + 2 * e2 + 1] = f.y;
-          }
-        }
+        load_bf16x32(reinterpret_cast<const __nv_bfloat16*>(a.q) + (rowbase + t0 + i) * 64 +
+                         32 * h, u);
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) {
-          ss += x[jj] * x[jj];
-          ug += x[jj] * d[jj];
+          ss += u[jj] * u[jj];
+          ug += u[jj] * d[jj];
         }
       }
-      sc.ssp[h][r] = ss;
-      sc.ugp[h][r] = ug;
     }
+    sc.ssp[h][r] = ss;
+    sc.ugp[h][r] = ug;
     __syncthreads();
-    if (r >= 64 && i < n) {
-      const float ss = sc.ssp[0][r] + sc.ssp[1][r], ug = sc.ugp[0][r] + sc.ugp[1][r];
-      if (a.phi == FALCON_PHI_L2) {
-        const float nrm = sqrtf(ss);
-        if (nrm < 1e-12f) {
+    // dk = J_phi(k)^T dX (rows 1 .. n-1), dq = J_phi(q)^T dQ (rows < n)
+    const bool out = (r < 64) ? (i >= 1 && i < n) : (i < n);
+    if (out) {
+      const float ssr = (r < 64) ? sc.ssk[i] : sc.ssp[0][r] + sc.ssp[1][r];
+      phi_vjp_half(d, u, ssr, sc.ugp[0][r] + sc.ugp[1][r], a.phi);
+      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(r < 64 ? b.dk : b.dq) +
+                           (rowbase + t0 + i - (r < 64 ? 1 : 0)) * 64 + 32 * h;
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) d[jj] *= 1e12f;
-        } else {
-          const float inv = 1.f / nrm, c2 = ug * inv * inv;
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj) d[jj] = (d[jj] - x[jj] * c2) * inv;
-        }
-      } else if (a.phi == FALCON_PHI_RMS) {
-        const float s = rsqrtf(ss / 64.f + kEpsRms), c3 = s * s * s * ug / 64.f;
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) d[jj] = s * d[jj] - c3 * x[jj];
-      }
-      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(b.dq) +
-                                            (rowbase + t0 + i) * 64 + 32 * h);
-#pragma unroll
-      for (int q8 = 0; q8 < 4; ++q8) dst[q8] = pack8(d + 8 * q8, 1.f);
+      for (int q8 = 0; q8 < 4; ++q8) reinterpret_cast<uint4*>(dst)[q8] = pack8(d + 8 * q8, 1.f);
     }
   }
 
@@ -763,10 +788,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
   if (warp == 0) tmem_dealloc(tmem, 64);
 }
 
-}  // namespace
-
-cudaError_t launch_tc_bwd_scan(const BwdArgs& b, const void* maps, float* dS_ends, int* err,
-                               cudaStream_t stream) {
+cudaError_t launch_tc_bwd_scan_impl(const BwdArgs& b, const void* maps, float* dS_ends,
+                                    int* err, cudaStream_t stream) {
   const ChunkArgs& a = b.f;
   const int nchunks = (int)((a.T + kBC - 1) / kBC);
   CUtensorMap tm_do;
@@ -781,12 +804,75 @@ cudaError_t launch_tc_bwd_scan(const BwdArgs& b, const void* maps, float* dS_end
   return cudaGetLastError();
 }
 
+// dk of the tokens that end a chunk (from the next chunk's row 0) and of the
+// last token (from dx_last), and dx_prev; one warp per item, items c = 1 ..
+// nchunks-1 (token 64c - 1), nchunks (token T - 1) and 0 (dx_prev).
+__global__ void __launch_bounds__(kBThreads) tc_bwd_edge_kernel(BwdArgs b, int nchunks,
+                                                                const float* edge) {
+  const ChunkArgs& a = b.f;
+  const int lane = threadIdx.x & 31;
+  const int64_t items = a.BH * (nchunks + 1);
+  for (int64_t it = (int64_t)blockIdx.x * (kBThreads / 32) + threadIdx.x / 32; it < items;
+       it += (int64_t)gridDim.x * (kBThreads / 32)) {
+    const int64_t bh = it / (nchunks + 1);
+    const int c = (int)(it % (nchunks + 1));
+    if (c == 0) {
+      if (b.dx_prev)
+        for (int j = lane; j < 64; j += 32)
+          b.dx_prev[bh * 64 + j] = a.x_prev ? edge[(bh * nchunks) * 64 + j] : 0.f;
+      continue;
+    }
+    const int64_t t = (c < nchunks) ? (int64_t)c * kBC - 1 : a.T - 1;
+    float u[2], g[2];
+    float ss = 0.f, ug = 0.f;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int j = lane + 32 * e;
+      u[e] = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.k)[(bh * a.T + t) * 64 + j]);
+      g[e] = (c < nchunks) ? edge[(bh * nchunks + c) * 64 + j] : (b.dx_last ? b.dx_last[bh * 64 + j] : 0.f);
+      ss += u[e] * u[e];
+      ug += u[e] * g[e];
+    }
+    ss = warp_sum(ss);
+    ug = warp_sum(ug);
+    float out[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) out[e] = g[e];
+    if (a.phi == FALCON_PHI_L2) {
+      const float nrm = sqrtf(ss);
+      if (nrm < 1e-12f) {
+        out[0] *= 1e12f;
+        out[1] *= 1e12f;
+      } else {
+        const float inv = 1.f / nrm, c2 = ug * inv * inv;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) out[e] = (g[e] - u[e] * c2) * inv;
+      }
+    } else if (a.phi == FALCON_PHI_RMS) {
+      const float sr = rsqrtf(ss / 64.f + kEpsRms), c3 = sr * sr * sr * ug / 64.f;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) out[e] = sr * g[e] - c3 * u[e];
+    }
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+      reinterpret_cast<__nv_bfloat16*>(b.dk)[(bh * a.T + t) * 64 + lane + 32 * e] =
+          __float2bfloat16_rn(out[e]);
+  }
+}
+
+}  // namespace
+
 bool tc_bwd_applies(int dtype, int m, int dv, int C) {
   return dtype == FALCON_BF16 && m == 64 && dv == 64 && C == kBC;
 }
 
+cudaError_t launch_tc_bwd_scan(const BwdArgs& b, const void* maps, float* dS_ends, int* err,
+                               cudaStream_t stream) {
+  return launch_tc_bwd_scan_impl(b, maps, dS_ends, err, stream);
+}
+
 cudaError_t launch_tc_bwd_grad(const BwdArgs& b, const float* S_starts, const float* dS_ends,
-                               float* dXw, int* err, cudaStream_t stream) {
+                               float* edge, int* err, cudaStream_t stream) {
   const ChunkArgs& a = b.f;
   const int nchunks = (int)((a.T + kBC - 1) / kBC);
   CUtensorMap tm_k, tm_q, tm_v, tm_do;
@@ -799,7 +885,13 @@ cudaError_t launch_tc_bwd_grad(const BwdArgs& b, const float* S_starts, const fl
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBwdSmem);
   if (e != cudaSuccess) return e;
   tc_bwd_grad_kernel<<<dim3(nchunks, (unsigned)a.BH), kBThreads, kBwdSmem, stream>>>(
-      b, nchunks, S_starts, dS_ends, dXw, err, tm_k, tm_q, tm_v, tm_do);
+      b, nchunks, S_starts, dS_ends, edge, err, tm_k, tm_q, tm_v, tm_do);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t items = a.BH * (nchunks + 1);
+  const int64_t blocks = (items + kBThreads / 32 - 1) / (kBThreads / 32);
+  tc_bwd_edge_kernel<<<(unsigned)(blocks < 65535 * 16 ? blocks : 65535 * 16), kBThreads, 0,
+                       stream>>>(b, nchunks, edge);
   return cudaGetLastError();
 }
 

@@ -121,10 +121,11 @@ struct BwdArgs {
 };
 size_t bwd_workspace_bytes(int dtype, int64_t BH, int64_t T, int m, int dv, int C);
 cudaError_t launch_bwd_chunked(const BwdArgs& b, int* err, cudaStream_t stream);
-// Tensor-core per-chunk gradients (bf16, m = dv = 64, chunk 64).
+// Tensor-core per-chunk gradients (bf16, m = dv = 64, chunk 64), dk included
+// (edge: [B*H, chunks, 64] f32 scratch for row 0 of every chunk's dX).
 bool tc_bwd_applies(int dtype, int m, int dv, int C);
 cudaError_t launch_tc_bwd_grad(const BwdArgs& b, const float* S_starts, const float* dS_ends,
-                               float* dXw, int* err, cudaStream_t stream);
+                               float* edge, int* err, cudaStream_t stream);
 // Reverse scan of the state cotangent over the tensor-core forward's maps.
 cudaError_t launch_tc_bwd_scan(const BwdArgs& b, const void* maps, float* dS_ends, int* err,
                                cudaStream_t stream);
