@@ -48,21 +48,28 @@ using namespace tcu;
 constexpr int kBC = 64;
 constexpr int kBThreads = 256;
 constexpr uint32_t kTile = 8192;  // 64 rows x 64 bf16, 128B-swizzled
-// Tile order matters where two tiles form one 128-row operand ([X; Q],
-// [S; dS'], [dR; dO]) or where an M = 128 operand's unused half reads the next
-// tile (T, U, P, dPE, dKs).
-enum : int {
-  kX = 0, kQt, kS, kdS, kdR, kdO, kP, kT, kR, kU, kdPE, kdKs, kV,
-  kXlo, kQlo, kSlo, kdSlo,  // low parts v - bf16(v) of X, Q, S, dS'
-  kPlo, kdUlo,              // and of P and dU
-  kNumTiles
-};
-constexpr uint32_t kAfOff = kNumTiles * kTile;          // A (fp32, rows of kLdA)
-constexpr uint32_t kTfOff = kAfOff + 64 * kLdA * 4;     // T (fp32, kLdT), later dK
-constexpr uint32_t kRsOff = kTfOff + 64 * kLdT * 4;     // solve scratch (16 x kLdR)
-constexpr uint32_t kScOff = kRsOff + 4096;
-static_assert(16 * kLdR * 4 <= 4096, "solve scratch");
-static_assert(64 * 65 * 4 <= 4 * kTile, "dP o P over the dead low-part tiles");
+// Shared memory: 13 tile slots of 8 KB from a 1024-aligned base, then the
+// scalars.  Tiles whose lifetimes do not overlap share a slot (write -> last
+// read):
+//   0 X  1 Q  2 S  3 dS'  (the whole kernel)   6 dO (-> [dR; dO] U^T)
+//   4 V (-> rv) | dPE                          5 dR (before dO: [dR; dO])
+//   7 T (solve -> T^T dU) | dOs = Diag(e^g) dO
+//   8 Xlo | A (fp32) | R | dU | dK             9 Qlo | A | U
+//   10 Slo | T (fp32) | Us = Diag(e^{g_C-g}) U 11 dSlo | T (fp32) | P | dUlo
+//   12 T (fp32), solve scratch | Plo | dRs = -Diag(eta e^{g_-}) dR
+// The unused half of an M = 128 K-major operand reads the next slot (slot 13
+// is the scalars: valid memory), that of an MN-major operand the slot LBO
+// bytes on.  With 113 KB of shared memory and 256 TMEM columns two CTAs share
+// an SM.
+enum : int { kX = 0, kQt, kS, kdS, kV, kdR, kdO, kT, kW8, kW9, kW10, kW11, kW12, kSlots };
+constexpr int kdPE = kV, kdOs = kT, kXlo = kW8, kSlo = kW10, kdSlo = kW11;  // Qlo = slot 9
+constexpr int kR = kW8, kdU = kW8, kdK = kW8, kU = kW9, kUs = kW10, kP = kW11, kdUlo = kW11;
+constexpr int kPlo = kW12, kdRs = kW12;
+constexpr uint32_t kAfOff = kW8 * kTile;               // A (fp32, rows of kLdA)
+constexpr uint32_t kTfOff = kAfOff + 64 * kLdA * 4;    // T (fp32, rows of kLdT)
+constexpr uint32_t kRsOff = kTfOff + 64 * kLdT * 4;    // solve scratch (16 x kLdR)
+constexpr uint32_t kScOff = kSlots * kTile;
+static_assert(kRsOff + 16 * kLdR * 4 <= kScOff, "solve buffers within slots 8..12");
 
 struct BwdScalars {
   float eta[64], g[64], gx[64], E[64], lame[64], den[64], gam[64];
@@ -78,16 +85,17 @@ struct BwdScalars {
   uint64_t bar_in, bar_mma;
   uint32_t tmem_base;
 };
-constexpr size_t kBwdSmem = kScOff + sizeof(BwdScalars) + 1024;
-constexpr uint32_t kTmemCols = 512;
+// The scalars get a full slot: the unused half of the operands in slot 12
+// reads it.  Two CTAs of kBwdSmem (+1 KB reserved each) fill an SM's 228 KB.
+static_assert(sizeof(BwdScalars) <= kTile, "scalars within one slot");
+constexpr size_t kBwdSmem = kScOff + kTile + 1024;
+static_assert(2 * (kBwdSmem + 1024) <= 228 * 1024, "two CTAs per SM");
+constexpr uint32_t kTmemCols = 256;
 // TMEM columns of the accumulators (128 lanes each).
-constexpr uint32_t kD1 = 0;    // [X; Q] X^T          (64)
-constexpr uint32_t kD2a = 64;  // [X; Q] S            (64)  -> later [junk; dPE] X
-constexpr uint32_t kD2b = 128; // [X; Q] dS'          (64)  -> later dPE^T Q + dKs X
-constexpr uint32_t kD3 = 192;  // T R, P^T dO, T^T dU (64, one after another)
-constexpr uint32_t kD6 = 256;  // [dR; dO] U^T        (64)
-constexpr uint32_t kD7 = 320;  // [dR; dO] [S; dS']^T (128)
-constexpr uint32_t kD8 = 448;  // [U; junk] dS'^T     (64)
+constexpr uint32_t kD1 = 0;     // [X; Q] X^T (until the dA, dP epilogue)
+constexpr uint32_t kD2a = 64;   // [X; Q] S  -> dQ = [.; dPE] X + [.; dOs] S^T
+constexpr uint32_t kD2b = 128;  // [X; Q] dS' -> dX - 2 Diag(dE) X
+constexpr uint32_t kD3 = 192;   // T R, P^T dO, T^T dU, [dR; dO] U^T in turn
 enum : int { kLive = 1, kClamped = 2 };
 
 __device__ __forceinline__ float expn(float x) { return __expf(fminf(x, 0.f)); }
@@ -185,7 +193,25 @@ __device__ __forceinline__ void publish_tiles() {
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(kBThreads, 1)
+// Column sums of a warp's 32 rows: v holds 32 consecutive columns of this
+// lane's row; afterwards lane l returns the sum over the warp's rows of column
+// l (recursive halving, 31 shuffles).
+__device__ __forceinline__ float warp_col_sum32(float (&v)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int sh = 16; sh >= 1; sh >>= 1) {
+    const bool up = (lane & sh) != 0;
+#pragma unroll
+    for (int k = 0; k < sh; ++k) {
+      const float send = up ? v[k] : v[k + sh];
+      const float keep = up ? v[k + sh] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, sh);
+    }
+  }
+  return v[0];
+}
+
+__global__ void __launch_bounds__(kBThreads, 2)
     tc_bwd_grad_kernel(BwdArgs b, int nchunks, const float* S_starts, const float* dS_ends,
                        float* edge, int* err, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_q,
@@ -199,11 +225,11 @@ __global__ void __launch_bounds__(kBThreads, 1)
   float* Rs = reinterpret_cast<float*>(base + kRsOff);
   BwdScalars& sc = *reinterpret_cast<BwdScalars*>(base + kScOff);
   auto tile = [&](int i) { return base + i * kTile; };
-  float* Pm = reinterpret_cast<float*>(base + kXlo * kTile);  // dP o P, 64 x 65 (late)
   auto taddr = [&](int i) { return smem_addr(base + i * kTile); };
 
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r = tid & 127, h = tid >> 7;  // accumulator lane, column half
+  const int i = r & 63;                   // row of the 64-row tile this thread serves
   const int c = blockIdx.x;
   const int64_t bh = blockIdx.y;
   const int64_t T = a.T, t0 = (int64_t)c * kBC, rowbase = bh * T;
@@ -230,7 +256,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
     sc.qz[tid] = sc.rv[tid] = sc.xy[tid] = sc.xw[tid] = 0.f;
     sc.sAr[tid] = sc.sAc[tid] = sc.spr[tid] = sc.spc[tid] = 0.f;
   }
-  // [S; dS'] as bf16 operand tiles (thread: row r of the pair, half h)
+  // [S; dS'] as split bf16 operand tiles (thread: row r of the pair, half h)
   {
     const float* src = (r < 64 ? S + r * 64 : dSp + (r - 64) * 64) + 32 * h;
     float v[32];
@@ -255,7 +281,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
       acc += x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w;
     }
     acc = warp_sum(acc);
-    if ((tid & 31) == 0) atomicAdd(&sc.sds, acc);
+    if (lane == 0) atomicAdd(&sc.sds, acc);
   }
   tc_fence_before();
   __syncthreads();
@@ -273,7 +299,6 @@ __global__ void __launch_bounds__(kBThreads, 1)
   {
     float v[32];
     load_half_sw(tile(kX), r, h, v);
-    const int i = r & 63;
     const bool xrow = r < 64;
     const bool given = xrow && t0 + i == 0 && a.x_prev != nullptr;
     const bool dead = i >= n || (xrow && t0 + i == 0 && a.x_prev == nullptr);
@@ -295,32 +320,31 @@ __global__ void __launch_bounds__(kBThreads, 1)
   __syncthreads();
   // ---- per-token scalars as the forward forms them, then the log prefixes
   if (tid < 64) {
-    const int i = tid;
     float et = 0.f, gm = 1.f, lg = 0.f, le = 0.f, d = 1.f;
     int fl = 0;
-    if (i < n) {
-      const int64_t t = t0 + i;
+    if (tid < n) {
+      const int64_t t = t0 + tid;
       const bool sentinel = (t == 0) && (a.x_prev == nullptr);
-      le = ridge_of(a.lambda[rowbase + t], sc.E[i], a.ridge);
-      d = sc.E[i] + le + a.eps;
-      et = step_eta_gamma(sentinel, sc.E[i], a.beta[rowbase + t], le, a.eps, a.eps_gamma, &gm,
+      le = ridge_of(a.lambda[rowbase + t], sc.E[tid], a.ridge);
+      d = sc.E[tid] + le + a.eps;
+      et = step_eta_gamma(sentinel, sc.E[tid], a.beta[rowbase + t], le, a.eps, a.eps_gamma, &gm,
                           &lg);
       if (!sentinel && d > 0.f) fl |= kLive;
       if (et * le >= 1.f - a.eps_gamma) fl |= kClamped;
     }
-    sc.eta[i] = et;
-    sc.gam[i] = gm;
-    sc.g[i] = lg;
-    sc.lame[i] = le;
-    sc.den[i] = d;
-    sc.flag[i] = fl;
+    sc.eta[tid] = et;
+    sc.gam[tid] = gm;
+    sc.g[tid] = lg;
+    sc.lame[tid] = le;
+    sc.den[tid] = d;
+    sc.flag[tid] = fl;
   }
   __syncthreads();
   if (warp == 0) warp_prefix64(sc.g, sc.gx);  // g: inclusive, gx: exclusive
   publish_tiles();
   gC = sc.g[63];
 
-  // ---- MMA: [X; Q] X^T, [X; Q] S, [X; Q] dS'
+  // ---- MMA: [X; Q] X^T, [X; Q] S and [X; Q] dS' (split operands)
   if (tid == 0) {
     tc_fence_after();
     mma_k64(tmem + kD1, taddr(kX), false, 16, taddr(kX), false, 16,
@@ -335,10 +359,9 @@ __global__ void __launch_bounds__(kBThreads, 1)
     mma_commit(&sc.bar_mma);
   }
   if (!wait_mma(sc, phase)) goto teardown;
-  // A (fp32, for the solve), R = Diag(eta) V - Diag(eta e^{g_-}) X S, P, qz
+  // A (fp32, for the solve; over the dead low parts), qz_i = <dO_i, (Q S)_i>
   {
     float d[32], w[32];
-    const int i = r & 63;
     if (r < 64) {
       const float ei = sc.eta[i], gxi = sc.gx[i];
       tmem_ld32(tl + kD1, d);
@@ -347,21 +370,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
         const int j = 32 * h + jj;
         Af[i * kLdA + j] = (f1 && j < i) ? ei * expn(gxi - sc.g[j]) * d[jj] : 0.f;
       }
-      tmem_ld32(tl + kD2a, d);
-      load_half_sw(tile(kV), i, h, w);
-      const float bx = f1 ? __expf(gxi) : 0.f;
-#pragma unroll
-      for (int jj = 0; jj < 32; ++jj) w[jj] = w[jj] - bx * d[jj];  // residual part
-      store_half_sw(tile(kR), i, h, w, ei);
     } else {
-      const float gi = sc.g[i];
-      tmem_ld32(tl + kD1, d);
-#pragma unroll
-      for (int jj = 0; jj < 32; ++jj) {
-        const int j = 32 * h + jj;
-        d[jj] = (j <= i) ? expn(gi - sc.g[j]) * d[jj] : 0.f;
-      }
-      store_half_split(tile(kP), tile(kPlo), i, h, d);
       tmem_ld32(tl + kD2a, d);
       load_half_sw(tile(kdO), i, h, w);
       float acc = 0.f;
@@ -371,7 +380,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
     }
   }
   __syncthreads();
-  // ---- T = (I + A)^{-1} (T = I for Falcon-1A), as a bf16 tile
+  // ---- T = (I + A)^{-1} (T = I for Falcon-1A)
   if (f1) {
     solve_unit_lower(Af, Tf, Rs);
   } else {
@@ -379,14 +388,21 @@ __global__ void __launch_bounds__(kBThreads, 1)
       Tf[(idx >> 6) * kLdT + (idx & 63)] = ((idx >> 6) == (idx & 63)) ? 1.f : 0.f;
   }
   __syncthreads();
+  // T as a bf16 tile; R = Diag(eta) (V - Diag(e^{g_-}) X S) (over A, now dead)
   if (r < 64) {
-    float v[32];
+    float v[32], w[32];
 #pragma unroll
     for (int jj = 0; jj < 32; ++jj) {
       const int j = 32 * h + jj;
-      v[jj] = (j <= r) ? Tf[r * kLdT + j] : 0.f;
+      v[jj] = (j <= i) ? Tf[i * kLdT + j] : 0.f;
     }
-    store_half_sw(tile(kT), r, h, v, 1.f);
+    store_half_sw(tile(kT), i, h, v, 1.f);
+    tmem_ld32(tl + kD2a, v);
+    load_half_sw(tile(kV), i, h, w);
+    const float bx = f1 ? __expf(sc.gx[i]) : 0.f;
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) w[jj] = w[jj] - bx * v[jj];  // residual part
+    store_half_sw(tile(kR), i, h, w, sc.eta[i]);
   }
   publish_tiles();
   // ---- U = T R
@@ -397,18 +413,31 @@ __global__ void __launch_bounds__(kBThreads, 1)
     mma_commit(&sc.bar_mma);
   }
   if (!wait_mma(sc, phase)) goto teardown;
-  if (r < 64) {
-    float d[32], xd[32];
-    tmem_ld32(tl + kD3, d);
-    store_half_sw(tile(kU), r, h, d, 1.f);
-    tmem_ld32(tl + kD2b, xd);  // <x_i, dS' U_i> = <(X dS')_i, U_i>
-    float acc = 0.f;
+  // U and Us = Diag(e^{g_C - g}) U tiles, xw_i = <(X dS')_i, U_i>; P (split)
+  {
+    float d[32], e[32];
+    if (r < 64) {
+      tmem_ld32(tl + kD3, d);
+      store_half_sw(tile(kU), i, h, d, 1.f);
+      store_half_sw(tile(kUs), i, h, d, expn(gC - sc.g[i]));
+      tmem_ld32(tl + kD2b, e);
+      float acc = 0.f;
 #pragma unroll
-    for (int jj = 0; jj < 32; ++jj) acc += xd[jj] * d[jj];
-    atomicAdd(&sc.xw[r], acc);
+      for (int jj = 0; jj < 32; ++jj) acc += e[jj] * d[jj];
+      atomicAdd(&sc.xw[i], acc);
+    } else {
+      const float gi = sc.g[i];
+      tmem_ld32(tl + kD1, d);
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) {
+        const int j = 32 * h + jj;
+        d[jj] = (j <= i) ? expn(gi - sc.g[j]) * d[jj] : 0.f;
+      }
+      store_half_split(tile(kP), tile(kPlo), i, h, d);
+    }
   }
   publish_tiles();
-  // ---- P^T dO
+  // ---- P^T dO (split P)
   if (tid == 0) {
     tc_fence_after();
     const uint32_t id = idesc_bf16(128, 64, true, true);
@@ -417,142 +446,125 @@ __global__ void __launch_bounds__(kBThreads, 1)
     mma_commit(&sc.bar_mma);
   }
   if (!wait_mma(sc, phase)) goto teardown;
-  // dU = P^T dO + Diag(e^{g_C - g}) X dS' (into the R tile)
+  // dU = P^T dO + Diag(e^{g_C - g}) X dS' (split)
   if (r < 64) {
     float d[32], xd[32];
     tmem_ld32(tl + kD3, d);
     tmem_ld32(tl + kD2b, xd);
-    const float f = expn(gC - sc.g[r]);
+    const float f = expn(gC - sc.g[i]);
 #pragma unroll
     for (int jj = 0; jj < 32; ++jj) d[jj] += f * xd[jj];
-    store_half_split(tile(kR), tile(kdUlo), r, h, d);
+    store_half_split(tile(kdU), tile(kdUlo), i, h, d);
   }
   publish_tiles();
   // ---- dR = T^T dU
   if (tid == 0) {
     tc_fence_after();
     const uint32_t id = idesc_bf16(128, 64, true, true);
-    mma_k64(tmem + kD3, taddr(kT), true, kTile, taddr(kR), true, kTile, id, false);
+    mma_k64(tmem + kD3, taddr(kT), true, kTile, taddr(kdU), true, kTile, id, false);
     mma_k64(tmem + kD3, taddr(kT), true, kTile, taddr(kdUlo), true, kTile, id, true);
     mma_commit(&sc.bar_mma);
   }
   if (!wait_mma(sc, phase)) goto teardown;
-  // dR tile, dv = Diag(eta) dR, rv_i = <dR_i, v_i>
+  // dR and dRs = -Diag(eta e^{g_-}) dR tiles; dv = Diag(eta) dR;
+  // rv_i = <dR_i, v_i - e^{g_{i-1}} (X S)_i>, xy_i = <dR_i, (X S)_i>
   if (r < 64) {
     float d[32], w[32], xs[32];
     tmem_ld32(tl + kD3, d);
-    store_half_sw(tile(kdR), r, h, d, 1.f);
-    load_half_sw(tile(kV), r, h, w);
+    store_half_sw(tile(kdR), i, h, d, 1.f);
+    const float ei = sc.eta[i], bx = f1 ? __expf(sc.gx[i]) : 0.f;
+    store_half_sw(tile(kdRs), i, h, d, -ei * bx);
+    load_half_sw(tile(kV), i, h, w);
     tmem_ld32(tl + kD2a, xs);
-    const float bx = f1 ? __expf(sc.gx[r]) : 0.f;
     float acc = 0.f, axs = 0.f;
 #pragma unroll
     for (int jj = 0; jj < 32; ++jj) {
-      acc += d[jj] * (w[jj] - bx * xs[jj]);  // <dR_i, v_i - e^{g_{i-1}} (X S)_i>
-      axs += d[jj] * xs[jj];                 // <dR_i, (X S)_i> = <x_i, (dR S^T)_i>
+      acc += d[jj] * (w[jj] - bx * xs[jj]);
+      axs += d[jj] * xs[jj];
     }
-    atomicAdd(&sc.rv[r], acc);
-    atomicAdd(&sc.xy[r], axs);
-    if (r < n) {
-      const float ei = sc.eta[r];
+    atomicAdd(&sc.rv[i], acc);
+    atomicAdd(&sc.xy[i], axs);
+    if (i < n) {
       uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(b.dv) +
-                                            (rowbase + t0 + r) * 64 + 32 * h);
+                                            (rowbase + t0 + i) * 64 + 32 * h);
 #pragma unroll
       for (int q8 = 0; q8 < 4; ++q8) dst[q8] = pack8(d + 8 * q8, ei);
     }
   }
   publish_tiles();
-  // ---- [dR; dO] U^T, [dR; dO] [S; dS']^T, U dS'^T
+  // ---- [dR; dO] U^T: rows 0..63 -dA (before masking), rows 64..127 dP
   if (tid == 0) {
     tc_fence_after();
-    mma_k64(tmem + kD6, taddr(kdR), false, 16, taddr(kU), false, 16,
-            idesc_bf16(128, 64, false, false), false);
-    mma_k64(tmem + kD7, taddr(kdR), false, 16, taddr(kS), false, 16,
-            idesc_bf16(128, 128, false, false), false);
-    mma_k64(tmem + kD8, taddr(kU), false, 16, taddr(kdS), false, 16,
+    mma_k64(tmem + kD3, taddr(kdR), false, 16, taddr(kU), false, 16,
             idesc_bf16(128, 64, false, false), false);
     mma_commit(&sc.bar_mma);
   }
   if (!wait_mma(sc, phase)) goto teardown;
   {
-    float d[32], e[32];
-    const int i = r & 63;
+    float d[32], e[32], pr[32];
     if (r < 64) {
-      // dA (Falcon-1), its products with A, and dK
+      // dA (Falcon-1) with A recomputed from the Gram accumulator; dK tile
       const float ei = sc.eta[i], gxi = sc.gx[i];
-      tmem_ld32(tl + kD6, d);
+      tmem_ld32(tl + kD3, d);
+      tmem_ld32(tl + kD1, e);
       float sar = 0.f;
 #pragma unroll
       for (int jj = 0; jj < 32; ++jj) {
         const int j = 32 * h + jj;
-        const float da = (f1 && j < i) ? -d[jj] : 0.f;
-        const float pa = da * Af[i * kLdA + j];
-        sar += pa;
-        Af[i * kLdA + j] = pa;  // dA o A (A is not needed any more)
-        Tf[i * kLdT + j] = da * ei * expn(gxi - sc.g[j]);  // dK_ij
+        const float fa = (f1 && j < i) ? ei * expn(gxi - sc.g[j]) : 0.f;
+        const float da = -d[jj];
+        pr[jj] = da * fa * e[jj];  // dA_ij A_ij
+        sar += pr[jj];
+        d[jj] = da * fa;           // dK_ij
       }
       atomicAdd(&sc.sAr[i], sar);
+      store_half_sw(tile(kdK), i, h, d, 1.f);
+      atomicAdd(&sc.sAc[32 * h + lane], warp_col_sum32(pr));
     } else {
-      // dP, its products with P (fp32, from the Gram accumulator), dP o E
+      // dP with P (fp32) from the Gram accumulator; dPE and dOs tiles
       const float gi = sc.g[i];
-      tmem_ld32(tl + kD6, d);
+      tmem_ld32(tl + kD3, d);
       tmem_ld32(tl + kD1, e);
       float spr = 0.f;
 #pragma unroll
       for (int jj = 0; jj < 32; ++jj) {
         const int j = 32 * h + jj;
         const float ef = (j <= i) ? expn(gi - sc.g[j]) : 0.f;
-        const float pp = d[jj] * ef * e[jj];
-        spr += pp;
-        Pm[i * 65 + j] = pp;  // dP o P
+        pr[jj] = d[jj] * ef * e[jj];  // dP_ij P_ij
+        spr += pr[jj];
         d[jj] *= ef;
       }
       atomicAdd(&sc.spr[i], spr);
       store_half_sw(tile(kdPE), i, h, d, 1.f);
+      load_half_sw(tile(kdO), i, h, e);
+      store_half_sw(tile(kdOs), i, h, e, __expf(gi));
+      atomicAdd(&sc.spc[32 * h + lane], warp_col_sum32(pr));
     }
   }
   __syncthreads();
   // ---- the step-size cotangent, the log-prefix cotangent and its suffix sums,
   //      then dbeta, dlambda and dE per token
   if (tid < 64) {
-    const int i = tid;
-    float sac = 0.f, spc = 0.f;  // column sums of dA o A and dP o P
-    for (int k = 0; k < 64; ++k) {
-      sac += Af[k * kLdA + i];
-      spc += Pm[k * 65 + i];
-    }
-    sc.sAc[i] = sac;
-    sc.spc[i] = spc;
-    float de = sc.rv[i];  // <dR_i, v_i - e^{g_{i-1}} (X S)_i>
-    if (f1 && sc.eta[i] != 0.f) de += sc.sAr[i] / sc.eta[i];
-    sc.deta[i] = de;
-    const float xwd = expn(gC - sc.g[i]) * sc.xw[i];
-    sc.xwd[i] = xwd;
-    sc.dg[i] = __expf(sc.g[i]) * sc.qz[i] + sc.spr[i] - spc - xwd - (f1 ? sac : 0.f);
-  }
-  // dKs = dK + dK^T (rows of the dKs tile)
-  if (r < 64) {
-    float v[32];
-#pragma unroll
-    for (int jj = 0; jj < 32; ++jj) {
-      const int j = 32 * h + jj;
-      v[jj] = Tf[r * kLdT + j] + Tf[j * kLdT + r];
-    }
-    store_half_sw(tile(kdKs), r, h, v, 1.f);
+    float de = sc.rv[tid];  // <dR_i, v_i - e^{g_{i-1}} (X S)_i>
+    if (f1 && sc.eta[tid] != 0.f) de += sc.sAr[tid] / sc.eta[tid];
+    sc.deta[tid] = de;
+    const float xwd = expn(gC - sc.g[tid]) * sc.xw[tid];
+    sc.xwd[tid] = xwd;
+    sc.dg[tid] = __expf(sc.g[tid]) * sc.qz[tid] + sc.spr[tid] - sc.spc[tid] - xwd -
+                 (f1 ? sc.sAc[tid] : 0.f);
   }
   __syncthreads();
   if (warp == 0) {
     // terms at index i - 1 (Falcon-1) and at C - 1, then the suffix sums
-    const int l = tid;
-    const float tail = warp_sum(sc.xwd[2 * l] + sc.xwd[2 * l + 1]) + __expf(gC) * sc.sds;
+    const float tail = warp_sum(sc.xwd[2 * lane] + sc.xwd[2 * lane + 1]) + __expf(gC) * sc.sds;
     float v[2];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
-      const int i = 63 - 2 * l - u;
-      float x = sc.dg[i];
-      if (f1 && i < 63)
-        x += -sc.eta[i + 1] * __expf(sc.gx[i + 1]) * sc.xy[i + 1] + sc.sAr[i + 1];
-      if (i == 63) x += tail;
+      const int k = 63 - 2 * lane - u;
+      float x = sc.dg[k];
+      if (f1 && k < 63)
+        x += -sc.eta[k + 1] * __expf(sc.gx[k + 1]) * sc.xy[k + 1] + sc.sAr[k + 1];
+      if (k == 63) x += tail;
       v[u] = x;
     }
     __syncwarp();
@@ -560,64 +572,66 @@ __global__ void __launch_bounds__(kBThreads, 1)
   }
   __syncthreads();
   if (tid < 64) {
-    const int i = tid;
     float dEi = 0.f;
-    if (i < n) {
+    if (tid < n) {
       float db = 0.f, dl_in = 0.f;
-      if (sc.flag[i] & kLive) {
-        float de = sc.deta[i], dl = 0.f;
-        if (!(sc.flag[i] & kClamped)) {
-          const float dal = -sc.dg[i] / sc.gam[i];
-          de += sc.lame[i] * dal;
-          dl += sc.eta[i] * dal;
+      if (sc.flag[tid] & kLive) {
+        float de = sc.deta[tid], dl = 0.f;
+        if (!(sc.flag[tid] & kClamped)) {
+          const float dal = -sc.dg[tid] / sc.gam[tid];
+          de += sc.lame[tid] * dal;
+          dl += sc.eta[tid] * dal;
         }
-        db = de / sc.den[i];
-        const float dden = -de * sc.eta[i] / sc.den[i];
+        db = de / sc.den[tid];
+        const float dden = -de * sc.eta[tid] / sc.den[tid];
         dEi = dden;
         dl += dden;
         if (a.ridge == FALCON_RIDGE_SCALED) {
-          dl_in = dl * sc.E[i];
-          dEi += dl * a.lambda[rowbase + t0 + i];
+          dl_in = dl * sc.E[tid];
+          dEi += dl * a.lambda[rowbase + t0 + tid];
         } else {
           dl_in = dl;
         }
       }
-      b.dbeta[rowbase + t0 + i] = db;
-      b.dlambda[rowbase + t0 + i] = dl_in;
+      b.dbeta[rowbase + t0 + tid] = db;
+      b.dlambda[rowbase + t0 + tid] = dl_in;
     }
-    sc.dE[i] = dEi;
+    sc.dE[tid] = dEi;
   }
   publish_tiles();
-  // ---- [junk; dPE] X, dPE^T Q + dKs X
+  // ---- dQ = [.; dPE] X + [.; dOs] S^T (rows 64..127 of kD2a);
+  //      dX - 2 Diag(dE) X = dPE^T Q + dK X + dK^T X + dRs S^T + Us dS'^T (rows 0..63 of kD2b)
   if (tid == 0) {
     tc_fence_after();
-    mma_k64(tmem + kD2a, taddr(kU), false, 16, taddr(kX), true, kTile,
+    mma_k64(tmem + kD2a, taddr(kdPE - 1), false, 16, taddr(kX), true, kTile,
             idesc_bf16(128, 64, false, true), false);
+    mma_k64(tmem + kD2a, taddr(kdOs - 1), false, 16, taddr(kS), false, 16,
+            idesc_bf16(128, 64, false, false), true);
     mma_k64(tmem + kD2b, taddr(kdPE), true, kTile, taddr(kQt), true, kTile,
             idesc_bf16(128, 64, true, true), false);
-    mma_k64(tmem + kD2b, taddr(kdKs), false, 16, taddr(kX), true, kTile,
+    mma_k64(tmem + kD2b, taddr(kdK), false, 16, taddr(kX), true, kTile,
             idesc_bf16(128, 64, false, true), true);
+    mma_k64(tmem + kD2b, taddr(kdK), true, kTile, taddr(kX), true, kTile,
+            idesc_bf16(128, 64, true, true), true);
+    mma_k64(tmem + kD2b, taddr(kdRs), false, 16, taddr(kS), false, 16,
+            idesc_bf16(128, 64, false, false), true);
+    mma_k64(tmem + kD2b, taddr(kUs), false, 16, taddr(kdS), false, 16,
+            idesc_bf16(128, 64, false, false), true);
     mma_commit(&sc.bar_mma);
   }
   if (!wait_mma(sc, phase)) goto teardown;
   {
-    float d[32], e[32], u[32];
-    const int i = r & 63;
+    float d[32], u[32];
     float ss = 0.f, ug = 0.f;
     if (r < 64) {
       // dX_i; row i >= 1 is the cotangent of x_i = phi(k_{t0+i-1}), so dk of
       // that token follows here; row 0 (the previous chunk's last token, or
       // x_prev) goes to the edge buffer.
       tmem_ld32(tl + kD2b, d);
-      tmem_ld32(tl + kD8, e);
       load_half_sw(tile(kX), i, h, u);
-      const float fw = expn(gC - sc.g[i]), fe = 2.f * sc.dE[i];
+      const float fe = 2.f * sc.dE[i];
 #pragma unroll
-      for (int jj = 0; jj < 32; ++jj) d[jj] += fw * e[jj] + fe * u[jj];
-      tmem_ld32(tl + kD7, e);
-      const float fy = f1 ? sc.eta[i] * __expf(sc.gx[i]) : 0.f;
-#pragma unroll
-      for (int jj = 0; jj < 32; ++jj) d[jj] -= fy * e[jj];
+      for (int jj = 0; jj < 32; ++jj) d[jj] += fe * u[jj];
       if (i == 0) {
         float4* dst = reinterpret_cast<float4*>(edge + (bh * nchunks + c) * 64 + 32 * h);
 #pragma unroll
@@ -628,15 +642,9 @@ __global__ void __launch_bounds__(kBThreads, 1)
                          32 * h, u);
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) ug += u[jj] * d[jj];
-        ss = sc.ssk[i];
       }
     } else {
-      // dQ_i = e^{g_i} (dO S^T)_i + (dPE X)_i
-      tmem_ld32(tl + kD2a, d);
-      tmem_ld32(tl + kD7, e);
-      const float fg = __expf(sc.g[i]);
-#pragma unroll
-      for (int jj = 0; jj < 32; ++jj) d[jj] += fg * e[jj];
+      tmem_ld32(tl + kD2a, d);  // dQ_i
       if (i < n) {
         load_bf16x32(reinterpret_cast<const __nv_bfloat16*>(a.q) + (rowbase + t0 + i) * 64 +
                          32 * h, u);
