@@ -59,7 +59,8 @@ def peaks():
 
 # The sources that define the headline path's two kernels (the tensor-core
 # map and scan launches): profiled counters are tied to them.
-TC_PATH_SOURCES = ("chunk_tc.cu", "tc_ptx.cuh", "tmap.cu", "tmap.cuh", "common.cuh")
+TC_PATH_SOURCES = ("chunk_tc.cu", "tc_ptx.cuh", "tc_util.cuh", "tmap.cu", "tmap.cuh",
+                   "common.cuh")
 
 
 def kernel_sources_digest():
@@ -101,6 +102,18 @@ def algorithmic_bytes(w, with_S0=False):
     b += BH * w.m * w.dv * 4 + BH * w.m * 4
     if with_S0:
         b += BH * w.m * w.dv * 4
+    return b
+
+
+def algorithmic_bytes_bwd(w):
+    """Bytes one backward call must move at the least: q, k, v, dO read, beta,
+    lambda read; dq, dk, dv written, dbeta, dlambda written, dS0 and dx_prev
+    written (fresh sequences, zero end cotangents)."""
+    es = torch.finfo(w.dtype).bits // 8
+    BH = w.B * w.H
+    b = BH * w.T * (2 * w.m + 2 * w.dv) * es + BH * w.T * 8          # q, k, v, dO; beta, lambda
+    b += BH * w.T * (2 * w.m + w.dv) * es + BH * w.T * 8             # dq, dk, dv; dbeta, dlambda
+    b += BH * w.m * w.dv * 4 + BH * w.m * 4                          # dS0, dx_prev
     return b
 
 
@@ -411,6 +424,29 @@ def extra_workloads(falcon, dev):
                     "ms_per_call": secs * 1e3 / steps,
                     "hbm_frac": b / (secs / steps) / 1e9 / pk["hbm_gbs"]})
         del sets
+    # backward of the chunked forward (lm shapes): gradients for q, k, v, beta,
+    # lambda, S0 and x_prev from a seeded dO
+    for w in (workloads.LM, workloads.LM_1A):
+        sets = input_sets(w, 2, dev)
+        for k, x in enumerate(sets):
+            x.update(workloads.cotangents(w.B, w.H, w.T, w.m, w.dv, w.dtype, seed=w.seed + 7 * k,
+                                          device=dev))
+        fnb = falcon.falcon1_bwd_chunked if w.rule == "falcon1" else falcon.falcon1a_bwd_chunked
+        shape = falcon.make_shape(w.B, w.H, w.T, w.m, w.dv, w.chunk, w.dtype, w.phi)
+        wsb = torch.empty(max(falcon.falcon_bwd_workspace_bytes(shape), 1), dtype=torch.uint8,
+                          device=dev)
+        grads = {}
+
+        def bstep(x):
+            fnb(x["q"], x["k"], x["v"], x["beta"], x["lambda"], x["dO"], chunk=w.chunk,
+                phi=w.phi, workspace=wsb, grads=grads)
+        steps = 50
+        secs = time_device(bstep, sets, steps, 3, 1)
+        b = algorithmic_bytes_bwd(w)
+        out.append({"workload": w.name.replace("_lm_", "_lm_bwd_"),
+                    "tokens_per_s": w.tokens * steps / secs, "ms_per_call": secs * 1e3 / steps,
+                    "hbm_frac": b / (secs / steps) / 1e9 / pk["hbm_gbs"]})
+        del sets, wsb, grads
     # decode: rotating per-step inputs, state resident
     d = workloads.DECODE
     stream = workloads.DecodeStream(d, device=dev)
@@ -510,13 +546,23 @@ def run_profile(args):
                                        phi=d.phi, o=o)
         name, size = d.name, d.N
     else:
+        bwd = args.profile.endswith("bwd")
         w = {"lm": workloads.LM, "lm1a": workloads.LM_1A, "long": workloads.LONG,
-             "lm2": workloads.LM_2, "lm2a": workloads.LM_2A, "lm3a": workloads.LM_3A}[args.profile]
+             "lm2": workloads.LM_2, "lm2a": workloads.LM_2A, "lm3a": workloads.LM_3A,
+             "lmbwd": workloads.LM, "lm1abwd": workloads.LM_1A}[args.profile]
         if args.profile_size:
             w = dataclasses.replace(w, T=args.profile_size)
         x = workloads.generate(w, device=dev)
+        if bwd:
+            x.update(workloads.cotangents(w.B, w.H, w.T, w.m, w.dv, w.dtype, seed=w.seed,
+                                          device=dev))
         for _ in range(calls):
-            if w.rule == "falcon3a":
+            if bwd:
+                fnb = (falcon.falcon1_bwd_chunked if w.rule == "falcon1"
+                       else falcon.falcon1a_bwd_chunked)
+                fnb(x["q"], x["k"], x["v"], x["beta"], x["lambda"], x["dO"], chunk=w.chunk,
+                    phi=w.phi)
+            elif w.rule == "falcon3a":
                 falcon.falcon3a_fwd_recurrent(x["q"], x["k"], x["v"], x["beta"], x["lambda"],
                                               workloads.LM_3A_WINDOW, phi=w.phi)
             elif w.per_column:
@@ -543,7 +589,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--profile",
-                    choices=["lm", "lm1a", "long", "decode", "lm2", "lm2a", "lm3a"], default=None,
+                    choices=["lm", "lm1a", "long", "decode", "lm2", "lm2a", "lm3a", "lmbwd",
+                             "lm1abwd"], default=None,
                     help="profiler target: run --steps calls of one workload, print no timing")
     ap.add_argument("--profile-size", type=int, default=None,
                     help="with --profile: tokens per head (chunked) or states (decode)")
