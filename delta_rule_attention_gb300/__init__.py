@@ -38,7 +38,7 @@ EXPORTS = (
     "falcon_strerror", "falcon_version", "falcon1_fwd_chunked_fixed_scratch",
     "falcon_selftest_wait_timeout", "falcon2_fwd_recurrent", "falcon2a_fwd_recurrent",
     "falcon3a_fwd_recurrent", "falcon_bwd_workspace_bytes", "falcon1_bwd_chunked",
-    "falcon1a_bwd_chunked",
+    "falcon1a_bwd_chunked", "falcon3a_fwd_chunked",
 )
 FALCON_ERR_SCRATCH_LIMIT = -10
 FALCON_FIXED_SCRATCH_BYTES = 16 * 1024 * 1024
@@ -98,6 +98,9 @@ def load_library(path: str | None = None):
             fn = getattr(lib, name)
             fn.restype = ctypes.c_int
             fn.argtypes = [shp, vp, vp, vp, f32p, f32p, f32p, f32p, vp, f32p, f32p, vp]
+        lib.falcon3a_fwd_chunked.restype = ctypes.c_int
+        lib.falcon3a_fwd_chunked.argtypes = [shp, i32, vp, vp, vp, f32p, f32p, f32p, vp, f32p,
+                                             f32p, vp, sz, vp]
         lib.falcon3a_fwd_recurrent.restype = ctypes.c_int
         lib.falcon3a_fwd_recurrent.argtypes = [shp, i32, vp, vp, vp, f32p, f32p, f32p, vp, f32p,
                                                f32p, vp]
@@ -400,6 +403,45 @@ def falcon3a_fwd_recurrent(q, k, v, beta, lam, window, S0=None, phi="l2", eps=1e
                                     _ptr(beta), _ptr(lam), _ptr(S0), _ptr(o), _ptr(S_out),
                                     _ptr(x_last), _stream(stream))
     _check(rc, "falcon3a_fwd_recurrent")
+    return o, S_out, x_last
+
+
+def falcon3a_fwd_chunked(q, k, v, beta, lam, window, S0=None, phi="l2", eps=1e-6,
+                         eps_gamma=1e-6, o=None, S_out=None, x_last=None, workspace=None,
+                         stream=None, want_x_last=True, ridge="given"):
+    """Falcon-3A forward in chunk form (the masked-attention form; tensor cores
+    for bf16 with m = dv = 64, the token-recurrent kernel otherwise).
+    Arguments as falcon3a_fwd_recurrent, plus an optional workspace of
+    falcon_workspace_bytes(shape) bytes.  Returns (o, S_T, x_last)."""
+    lib = load_library()
+    _need(q, "q")
+    B, H, T, m = q.shape
+    dv = v.shape[-1]
+    dt = q.dtype
+    if dt not in _DTYPE:
+        raise TypeError("q, k, v must be bfloat16 or float32")
+    _need(k, "k", dt, (B, H, T, m))
+    _need(v, "v", dt, (B, H, T, dv))
+    _need(beta, "beta", torch.float32, (B, H, T))
+    _need(lam, "lambda", torch.float32, (B, H, T))
+    if S0 is not None:
+        _need(S0, "S0", torch.float32, (B, H, m, dv))
+    dev = q.device
+    if o is None:
+        o = torch.empty((B, H, T, dv), dtype=dt, device=dev)
+    if S_out is None:
+        S_out = torch.empty((B, H, m, dv), dtype=torch.float32, device=dev)
+    if x_last is None and want_x_last:
+        x_last = torch.empty((B, H, m), dtype=torch.float32, device=dev)
+    shape = make_shape(B, H, T, m, dv, 64, dt, phi, eps, eps_gamma, ridge)
+    need = int(lib.falcon_workspace_bytes(ctypes.byref(shape)))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.falcon3a_fwd_chunked(ctypes.byref(shape), int(window), _ptr(q), _ptr(k), _ptr(v),
+                                  _ptr(beta), _ptr(lam), _ptr(S0), _ptr(o), _ptr(S_out),
+                                  _ptr(x_last), _ptr(workspace), ws_bytes, _stream(stream))
+    _check(rc, "falcon3a_fwd_chunked")
     return o, S_out, x_last
 
 

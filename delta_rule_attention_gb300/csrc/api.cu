@@ -77,7 +77,7 @@ int* device_error_word() {
 int fwd_chunked(int rule, const falcon_shape* s, const void* q, const void* k, const void* v,
                 const float* beta, const float* lambda, const float* S0, const float* x_prev,
                 void* o, float* S_out, float* x_last, void* workspace, size_t workspace_bytes,
-                cudaStream_t stream, int window = 1) {
+                cudaStream_t stream, int window = 1, bool window_chunked = false) {
   int rc = check_shape(s);
   if (rc) return rc;
   const int64_t BH = s->B * s->H;
@@ -93,7 +93,12 @@ int fwd_chunked(int rule, const falcon_shape* s, const void* q, const void* k, c
   const bool per_column = rule == falcon::kFalcon2 || rule == falcon::kFalcon2A;
   const bool windowed = rule == falcon::kFalcon3A;
   if (windowed && (window < 1 || window > 32 || x_prev)) return FALCON_ERR_BAD_ARG;
-  const size_t need = (per_column || windowed) ? 0 : falcon_workspace_bytes(s);
+  // Falcon-3A in chunk form where the tensor-core path applies (it writes the
+  // chunk maps to the workspace); otherwise the token-recurrent kernel.
+  const bool window_tc = windowed && window_chunked &&
+                         falcon::tc_falcon3a_applies(s->dtype, s->m, s->dv, s->chunk, BH, s->T);
+  const size_t need =
+      (per_column || (windowed && !window_tc)) ? 0 : falcon_workspace_bytes(s);
   if (need > 0 && (!workspace || workspace_bytes < need)) return FALCON_ERR_WORKSPACE;
   if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return FALCON_ERR_MISALIGNED;
   rc = check_device();
@@ -137,6 +142,7 @@ int fwd_chunked(int rule, const falcon_shape* s, const void* q, const void* k, c
   if (per_column || windowed) {
     int* err = device_error_word();
     if (!err) return FALCON_ERR_CUDA;
+    if (window_tc) return to_status(falcon::launch_tc_falcon3a(a, window, err, stream));
     return to_status(windowed ? falcon::launch_falcon3a_recurrent(a, window, err, stream)
                               : falcon::launch_falcon2_recurrent(a, err, stream));
   }
@@ -353,6 +359,14 @@ int falcon3a_fwd_recurrent(const falcon_shape* s, int32_t window, const void* q,
                            cudaStream_t stream) {
   return fwd_chunked(falcon::kFalcon3A, s, q, k, v, beta, lambda, S0, nullptr, o, S_out, x_last,
                      nullptr, 0, stream, window);
+}
+
+int falcon3a_fwd_chunked(const falcon_shape* s, int32_t window, const void* q, const void* k,
+                         const void* v, const float* beta, const float* lambda, const float* S0,
+                         void* o, float* S_out, float* x_last, void* workspace,
+                         size_t workspace_bytes, cudaStream_t stream) {
+  return fwd_chunked(falcon::kFalcon3A, s, q, k, v, beta, lambda, S0, nullptr, o, S_out, x_last,
+                     workspace, workspace_bytes, stream, window, true);
 }
 
 int falcon1_decode_step(int64_t N, int32_t m, int32_t dv, int32_t dtype, int32_t phi,

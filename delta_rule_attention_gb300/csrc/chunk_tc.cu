@@ -1136,6 +1136,14 @@ cudaError_t launch_tc(const ChunkArgs& a, int* err, cudaStream_t stream) {
 
 }  // namespace
 
+cudaError_t launch_tc_scan64(const ChunkArgs& a, int* err, cudaStream_t stream) {
+  const int nchunks = (int)((a.T + kC - 1) / kC);
+  CUtensorMap tm_o;
+  if (!encode_rows_bf16(&tm_o, a.o, 64, (uint64_t)a.T, (uint64_t)a.BH, 64, kC))
+    return cudaErrorInvalidValue;
+  return launch_scan_range<64>(a, nchunks, 0, nchunks, a.S0, true, err, tm_o, stream);
+}
+
 cudaError_t launch_tc_chunked(const ChunkArgs& a, int* err, cudaStream_t stream) {
   return a.m == 128 ? launch_tc<128>(a, err, stream) : launch_tc<64>(a, err, stream);
 }

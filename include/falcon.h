@@ -274,6 +274,24 @@ int falcon3a_fwd_recurrent(const falcon_shape *shape, int32_t window,
                            const float *S0, void *o, float *S_out,
                            float *x_last, cudaStream_t stream);
 
+/* Falcon-3A forward in chunk form: the same result as falcon3a_fwd_recurrent
+ * (up to rounding), computed as the masked-attention form of Section 4.6:
+ * within a chunk of 64 tokens the state after token t is e^{g_t} S plus the
+ * write pairs of the chunk and of the B - 1 pairs before it, each weighted by
+ * w_{t,j} = sum over the chunk's tokens s <= t whose window holds pair j of
+ * e^{g_t - g_s} eta_s / B_s; the chunk maps are composed across chunks by the
+ * tensor-core scan.  For bf16 q, k, v with m = dv = 64 and shape->chunk = 64
+ * this runs on the tensor cores and needs a workspace of
+ * falcon_workspace_bytes(shape) bytes (256-byte aligned); for every other
+ * shape it runs falcon3a_fwd_recurrent and ignores the workspace.
+ * Arguments, layouts and errors are those of falcon3a_fwd_recurrent, plus
+ * workspace / workspace_bytes as in falcon1_fwd_chunked. */
+int falcon3a_fwd_chunked(const falcon_shape *shape, int32_t window,
+                         const void *q, const void *k, const void *v,
+                         const float *beta, const float *lambda,
+                         const float *S0, void *o, float *S_out,
+                         float *x_last, void *workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
 /* One recurrent token (read after write) for N independent states: the
  * Falcon-1 update of Section 3.1 Eq. (3.3), as in the one-step listing of page
  * rcap.io/posts/fast-weight-attention-for-continual-learning-2026-08-27.
