@@ -398,10 +398,14 @@ def extra_workloads(falcon, dev):
         o = torch.empty((w.B, w.H, w.T, w.dv), dtype=w.dtype, device=dev)
         S = torch.empty((w.B, w.H, w.m, w.dv), dtype=torch.float32, device=dev)
         if w.rule == "falcon3a":
+            shape = falcon.make_shape(w.B, w.H, w.T, w.m, w.dv, w.chunk, w.dtype, w.phi)
+            wsb = torch.empty(max(falcon.falcon_workspace_bytes(shape), 1), dtype=torch.uint8,
+                              device=dev)
+
             def step(x):
-                falcon.falcon3a_fwd_recurrent(x["q"], x["k"], x["v"], x["beta"], x["lambda"],
-                                              workloads.LM_3A_WINDOW, phi=w.phi, o=o, S_out=S,
-                                              want_x_last=False)
+                falcon.falcon3a_fwd_chunked(x["q"], x["k"], x["v"], x["beta"], x["lambda"],
+                                            workloads.LM_3A_WINDOW, phi=w.phi, o=o, S_out=S,
+                                            workspace=wsb, want_x_last=False)
         elif w.per_column:
             fn2 = {"falcon2": falcon.falcon2_fwd_recurrent,
                    "falcon2a": falcon.falcon2a_fwd_recurrent}[w.rule]
@@ -563,8 +567,8 @@ def run_profile(args):
                 fnb(x["q"], x["k"], x["v"], x["beta"], x["lambda"], x["dO"], chunk=w.chunk,
                     phi=w.phi)
             elif w.rule == "falcon3a":
-                falcon.falcon3a_fwd_recurrent(x["q"], x["k"], x["v"], x["beta"], x["lambda"],
-                                              workloads.LM_3A_WINDOW, phi=w.phi)
+                falcon.falcon3a_fwd_chunked(x["q"], x["k"], x["v"], x["beta"], x["lambda"],
+                                            workloads.LM_3A_WINDOW, phi=w.phi)
             elif w.per_column:
                 fn2 = (falcon.falcon2_fwd_recurrent if w.rule == "falcon2"
                        else falcon.falcon2a_fwd_recurrent)

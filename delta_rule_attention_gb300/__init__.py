@@ -38,7 +38,7 @@ EXPORTS = (
     "falcon_strerror", "falcon_version", "falcon1_fwd_chunked_fixed_scratch",
     "falcon_selftest_wait_timeout", "falcon2_fwd_recurrent", "falcon2a_fwd_recurrent",
     "falcon3a_fwd_recurrent", "falcon_bwd_workspace_bytes", "falcon1_bwd_chunked",
-    "falcon1a_bwd_chunked", "falcon3a_fwd_chunked",
+    "falcon1a_bwd_chunked", "falcon3a_fwd_chunked", "falcon2a_fwd_chunked",
 )
 FALCON_ERR_SCRATCH_LIMIT = -10
 FALCON_FIXED_SCRATCH_BYTES = 16 * 1024 * 1024
@@ -98,6 +98,9 @@ def load_library(path: str | None = None):
             fn = getattr(lib, name)
             fn.restype = ctypes.c_int
             fn.argtypes = [shp, vp, vp, vp, f32p, f32p, f32p, f32p, vp, f32p, f32p, vp]
+        lib.falcon2a_fwd_chunked.restype = ctypes.c_int
+        lib.falcon2a_fwd_chunked.argtypes = [shp, vp, vp, vp, f32p, f32p, f32p, f32p, vp, f32p,
+                                             f32p, vp, sz, vp]
         lib.falcon3a_fwd_chunked.restype = ctypes.c_int
         lib.falcon3a_fwd_chunked.argtypes = [shp, i32, vp, vp, vp, f32p, f32p, f32p, vp, f32p,
                                              f32p, vp, sz, vp]
@@ -324,7 +327,7 @@ def falcon1a_bwd_chunked(q, k, v, beta, lam, dO, S0=None, x_prev=None, dS_T=None
 
 def _fwd2(name, q, k, v, beta, lam, S0=None, x_prev=None, phi="l2", eps=1e-6,
           eps_gamma=1e-6, o=None, S_out=None, x_last=None, stream=None, want_x_last=True,
-          ridge="given"):
+          ridge="given", workspace=None, chunked=False):
     lib = load_library()
     _need(q, "q")
     B, H, T, m = q.shape
@@ -348,11 +351,29 @@ def _fwd2(name, q, k, v, beta, lam, S0=None, x_prev=None, phi="l2", eps=1e-6,
     if x_last is None and want_x_last:
         x_last = torch.empty((B, H, m), dtype=torch.float32, device=dev)
     shape = make_shape(B, H, T, m, dv, 64, dt, phi, eps, eps_gamma, ridge)
-    rc = getattr(lib, name)(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
-                            _ptr(lam), _ptr(S0), _ptr(x_prev), _ptr(o), _ptr(S_out),
-                            _ptr(x_last), _stream(stream))
+    if chunked:
+        need = int(lib.falcon_workspace_bytes(ctypes.byref(shape)))
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        rc = getattr(lib, name)(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+                                _ptr(lam), _ptr(S0), _ptr(x_prev), _ptr(o), _ptr(S_out),
+                                _ptr(x_last), _ptr(workspace), ws_bytes, _stream(stream))
+    else:
+        rc = getattr(lib, name)(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+                                _ptr(lam), _ptr(S0), _ptr(x_prev), _ptr(o), _ptr(S_out),
+                                _ptr(x_last), _stream(stream))
     _check(rc, name)
     return o, S_out, x_last
+
+
+def falcon2a_fwd_chunked(q, k, v, beta, lam, S0=None, x_prev=None, phi="l2", eps=1e-6,
+                         eps_gamma=1e-6, **kw):
+    """Falcon-2A forward in chunk form (tensor cores for bf16 with m = dv = 64,
+    the token-recurrent kernel otherwise); arguments as falcon2a_fwd_recurrent,
+    plus an optional workspace of falcon_workspace_bytes(shape) bytes."""
+    return _fwd2("falcon2a_fwd_chunked", q, k, v, beta, lam, S0, x_prev, phi, eps, eps_gamma,
+                 chunked=True, **kw)
 
 
 def falcon2_fwd_recurrent(q, k, v, beta, lam, S0=None, x_prev=None, phi="l2", eps=1e-6,

@@ -77,7 +77,7 @@ int* device_error_word() {
 int fwd_chunked(int rule, const falcon_shape* s, const void* q, const void* k, const void* v,
                 const float* beta, const float* lambda, const float* S0, const float* x_prev,
                 void* o, float* S_out, float* x_last, void* workspace, size_t workspace_bytes,
-                cudaStream_t stream, int window = 1, bool window_chunked = false) {
+                cudaStream_t stream, int window = 1, bool chunked_form = false) {
   int rc = check_shape(s);
   if (rc) return rc;
   const int64_t BH = s->B * s->H;
@@ -95,10 +95,14 @@ int fwd_chunked(int rule, const falcon_shape* s, const void* q, const void* k, c
   if (windowed && (window < 1 || window > 32 || x_prev)) return FALCON_ERR_BAD_ARG;
   // Falcon-3A in chunk form where the tensor-core path applies (it writes the
   // chunk maps to the workspace); otherwise the token-recurrent kernel.
-  const bool window_tc = windowed && window_chunked &&
+  const bool window_tc = windowed && chunked_form &&
                          falcon::tc_falcon3a_applies(s->dtype, s->m, s->dv, s->chunk, BH, s->T);
-  const size_t need =
-      (per_column || (windowed && !window_tc)) ? 0 : falcon_workspace_bytes(s);
+  // Falcon-2A likewise (the regression rule Falcon-2 stays token-recurrent).
+  const bool column_tc = rule == falcon::kFalcon2A && chunked_form &&
+                         falcon::tc_falcon2a_applies(s->dtype, s->m, s->dv, s->chunk, BH, s->T);
+  const size_t need = ((per_column && !column_tc) || (windowed && !window_tc))
+                          ? 0
+                          : falcon_workspace_bytes(s);
   if (need > 0 && (!workspace || workspace_bytes < need)) return FALCON_ERR_WORKSPACE;
   if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return FALCON_ERR_MISALIGNED;
   rc = check_device();
@@ -143,6 +147,7 @@ int fwd_chunked(int rule, const falcon_shape* s, const void* q, const void* k, c
     int* err = device_error_word();
     if (!err) return FALCON_ERR_CUDA;
     if (window_tc) return to_status(falcon::launch_tc_falcon3a(a, window, err, stream));
+    if (column_tc) return to_status(falcon::launch_tc_falcon2a(a, err, stream));
     return to_status(windowed ? falcon::launch_falcon3a_recurrent(a, window, err, stream)
                               : falcon::launch_falcon2_recurrent(a, err, stream));
   }
@@ -289,8 +294,13 @@ extern "C" {
 
 size_t falcon_workspace_bytes(const falcon_shape* s) {
   if (check_shape(s) != FALCON_OK) return 0;
-  if (falcon::tc_path_applies(s->dtype, s->m, s->dv, s->chunk, s->B * s->H, s->T))
-    return falcon::tc_workspace_bytes(s->m, s->B * s->H, s->T);
+  if (falcon::tc_path_applies(s->dtype, s->m, s->dv, s->chunk, s->B * s->H, s->T)) {
+    const size_t tc = falcon::tc_workspace_bytes(s->m, s->B * s->H, s->T);
+    if (s->m != 64) return tc;
+    // m = 64: room for the Falcon-2A chunk maps too (a little larger)
+    const size_t c2a = falcon::tc_falcon2a_workspace_bytes(s->B * s->H, s->T);
+    return tc > c2a ? tc : c2a;
+  }
   return falcon::generic_workspace_bytes(s->B * s->H, s->T, s->m, s->dv, s->chunk);
 }
 
@@ -359,6 +369,14 @@ int falcon3a_fwd_recurrent(const falcon_shape* s, int32_t window, const void* q,
                            cudaStream_t stream) {
   return fwd_chunked(falcon::kFalcon3A, s, q, k, v, beta, lambda, S0, nullptr, o, S_out, x_last,
                      nullptr, 0, stream, window);
+}
+
+int falcon2a_fwd_chunked(const falcon_shape* s, const void* q, const void* k, const void* v,
+                         const float* beta, const float* lambda, const float* S0,
+                         const float* x_prev, void* o, float* S_out, float* x_last,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return fwd_chunked(falcon::kFalcon2A, s, q, k, v, beta, lambda, S0, x_prev, o, S_out, x_last,
+                     workspace, workspace_bytes, stream, 1, true);
 }
 
 int falcon3a_fwd_chunked(const falcon_shape* s, int32_t window, const void* q, const void* k,

@@ -274,6 +274,24 @@ int falcon3a_fwd_recurrent(const falcon_shape *shape, int32_t window,
                            const float *S0, void *o, float *S_out,
                            float *x_last, cudaStream_t stream);
 
+/* Falcon-2A forward in chunk form: the same result as falcon2a_fwd_recurrent
+ * (up to rounding).  Every value column j has its own step sizes and
+ * decays, so within a chunk of 64 tokens o_{t,j} = e^{G_{j,t}} (Q S)_{t,j} +
+ * sum_{s<=t} <phi(q_t), x_s> e^{G_{j,t} - G_{j,s}} eta_{j,s} v_{s,j} and the
+ * state leaving it is S o e^{G_C} + X^T V' (G_{j,.} the chunk-local log
+ * prefix of column j; no triangular solve: the inner-product rule writes the
+ * target itself).  For bf16 q, k, v with m = dv = 64 and shape->chunk = 64
+ * this runs on the tensor cores and needs a workspace of
+ * falcon_workspace_bytes(shape) bytes (256-byte aligned); for every other
+ * shape it runs falcon2a_fwd_recurrent and ignores the workspace.
+ * Arguments, layouts and errors are those of falcon2a_fwd_recurrent, plus
+ * workspace / workspace_bytes as in falcon1_fwd_chunked. */
+int falcon2a_fwd_chunked(const falcon_shape *shape, const void *q,
+                         const void *k, const void *v, const float *beta,
+                         const float *lambda, const float *S0,
+                         const float *x_prev, void *o, float *S_out,
+                         float *x_last, void *workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
 /* Falcon-3A forward in chunk form: the same result as falcon3a_fwd_recurrent
  * (up to rounding), computed as the masked-attention form of Section 4.6:
  * within a chunk of 64 tokens the state after token t is e^{g_t} S plus the
