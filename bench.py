@@ -407,12 +407,18 @@ def extra_workloads(falcon, dev):
                                             workloads.LM_3A_WINDOW, phi=w.phi, o=o, S_out=S,
                                             workspace=wsb, want_x_last=False)
         elif w.per_column:
-            fn2 = {"falcon2": falcon.falcon2_fwd_recurrent,
-                   "falcon2a": falcon.falcon2a_fwd_recurrent}[w.rule]
-
-            def step(x):
-                fn2(x["q"], x["k"], x["v"], x["beta"], x["lambda"], phi=w.phi, o=o, S_out=S,
-                    want_x_last=False)
+            shape = falcon.make_shape(w.B, w.H, w.T, w.m, w.dv, w.chunk, w.dtype, w.phi)
+            wsb = torch.empty(max(falcon.falcon_workspace_bytes(shape), 1), dtype=torch.uint8,
+                              device=dev)
+            if w.rule == "falcon2a":
+                def step(x):
+                    falcon.falcon2a_fwd_chunked(x["q"], x["k"], x["v"], x["beta"], x["lambda"],
+                                                phi=w.phi, o=o, S_out=S, workspace=wsb,
+                                                want_x_last=False)
+            else:
+                def step(x):
+                    falcon.falcon2_fwd_recurrent(x["q"], x["k"], x["v"], x["beta"], x["lambda"],
+                                                 phi=w.phi, o=o, S_out=S, want_x_last=False)
         else:
             fn = falcon.falcon1_fwd_chunked if w.rule == "falcon1" else falcon.falcon1a_fwd_chunked
             shape = falcon.make_shape(w.B, w.H, w.T, w.m, w.dv, w.chunk, w.dtype, w.phi)
@@ -571,7 +577,7 @@ def run_profile(args):
                                             workloads.LM_3A_WINDOW, phi=w.phi)
             elif w.per_column:
                 fn2 = (falcon.falcon2_fwd_recurrent if w.rule == "falcon2"
-                       else falcon.falcon2a_fwd_recurrent)
+                       else falcon.falcon2a_fwd_chunked)
                 fn2(x["q"], x["k"], x["v"], x["beta"], x["lambda"], phi=w.phi)
             else:
                 fn = (falcon.falcon1_fwd_chunked if w.rule == "falcon1"
