@@ -52,12 +52,14 @@ constexpr float kSpan2A = 160.f;
 // the dead ones: Nc over A and U~, E over V'.
 enum : int { kX2 = 0, kQ2, kV2, kA2, kU2, kVp2, k2Slots };
 constexpr int kLdG = 65;
-constexpr uint32_t kEtaOff = k2Slots * k2Tile;        // eta (fp32, 64 x 64, from beta)
-constexpr uint32_t kGOff = kEtaOff + 64 * 64 * 4;     // G (fp32, 64 x kLdG)
+constexpr uint32_t kBetaOff = k2Slots * k2Tile;      // beta rows as copied (fp32, 64 x 64)
+constexpr uint32_t kEtaOff = kBetaOff + 64 * 64 * 4;  // eta (fp32, 64 x kLdG)
+constexpr uint32_t kGOff = kEtaOff + 64 * kLdG * 4;   // G (fp32, 64 x kLdG)
 constexpr uint32_t kSc2Off = kGOff + 64 * kLdG * 4;
 
 struct F2Scalars {
-  float E[64], den[64], lam[64], r[64], gC[64];
+  float E[64], den[64], lam[64], r[64], gC[64], half[64];
+  float part[4][64];  // column sums of the four quarters of the token range
   float ssp[2][128];
   int fail, slow;
   uint64_t bar_in, bar_mma;
@@ -79,8 +81,9 @@ __global__ void __launch_bounds__(k2Threads, 2)
                            const __grid_constant__ CUtensorMap tm_v) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base = align1024(smem_raw);
-  float* Eta = reinterpret_cast<float*>(base + kEtaOff);  // beta, then eta, [t][j]
-  float* G = reinterpret_cast<float*>(base + kGOff);      // log gamma, then the prefix
+  float* Beta = reinterpret_cast<float*>(base + kBetaOff);  // [t][j], as copied
+  float* Eta = reinterpret_cast<float*>(base + kEtaOff);    // [t][j], rows of kLdG
+  float* G = reinterpret_cast<float*>(base + kGOff);        // log gamma, then the prefix
   F2Scalars& sc = *reinterpret_cast<F2Scalars*>(base + kSc2Off);
   auto tile = [&](int i) { return base + i * k2Tile; };
   auto taddr = [&](int i) { return smem_addr(base + i * k2Tile); };
@@ -104,7 +107,7 @@ __global__ void __launch_bounds__(k2Threads, 2)
     tma_load_3d(tile(kX2), &tm_k, 0, (int)(t0 - 1), (int)bh, &sc.bar_in);
     tma_load_3d(tile(kQ2), &tm_q, 0, (int)t0, (int)bh, &sc.bar_in);
     tma_load_3d(tile(kV2), &tm_v, 0, (int)t0, (int)bh, &sc.bar_in);
-    bulk_g2s(Eta, a.beta + (rowbase + t0) * 64, (uint32_t)n * 256u, &sc.bar_in);
+    bulk_g2s(Beta, a.beta + (rowbase + t0) * 64, (uint32_t)n * 256u, &sc.bar_in);
   }
   if (tid < 64) sc.lam[tid] = tid < n ? a.lambda[rowbase + t0 + tid] : 0.f;
   tc_fence_before();
@@ -151,22 +154,37 @@ __global__ void __launch_bounds__(k2Threads, 2)
     float eta = 0.f, gm = 1.f, lg = 0.f;
     if (t < n) {
       const bool sentinel = (t0 + t == 0) && (a.x_prev == nullptr);
-      eta = step_eta_gamma(sentinel, sc.E[t], Eta[idx], sc.lam[t], a.eps, a.eps_gamma, &gm,
+      eta = step_eta_gamma(sentinel, sc.E[t], Beta[idx], sc.lam[t], a.eps, a.eps_gamma, &gm,
                            &lg);
     }
-    Eta[idx] = eta;
+    Eta[t * kLdG + j] = eta;
     G[t * kLdG + j] = lg;
   }
   __syncthreads();
-  if (tid < 64) {
+  {
+    // column prefixes: thread (j, p) sums tokens 16p .. 16p + 15 of column j,
+    // then adds the sums of the quarters before it
+    const int j = tid & 63, p = tid >> 6;
     float run = 0.f;
-    for (int t = 0; t < 64; ++t) {
-      run += G[t * kLdG + tid];
-      G[t * kLdG + tid] = run;
+#pragma unroll
+    for (int t = 16 * p; t < 16 * p + 16; ++t) {
+      run += G[t * kLdG + j];
+      G[t * kLdG + j] = run;
     }
-    sc.gC[tid] = run;
-    sc.r[tid] = 0.5f * run;
-    if (-run > kSpan2A) atomicOr(&sc.slow, 1);
+    sc.part[p][j] = run;
+    __syncthreads();
+    float off = 0.f;
+    for (int q = 0; q < p; ++q) off += sc.part[q][j];
+    if (p > 0)
+#pragma unroll
+      for (int t = 16 * p; t < 16 * p + 16; ++t) G[t * kLdG + j] += off;
+    if (p == 3) {
+      const float gc = off + run;
+      sc.gC[j] = gc;
+      sc.r[j] = 0.5f * gc;
+      sc.half[j] = __expf(0.5f * gc);  // e^{G_C - r}
+      if (-gc > kSpan2A) atomicOr(&sc.slow, 1);
+    }
   }
   publish_f2();
   slow = sc.slow != 0;
@@ -183,14 +201,21 @@ __global__ void __launch_bounds__(k2Threads, 2)
     const int s = r & 63;
     float v[32];
     load_half_sw(tile(kV2), s, h, v);
+    float u[32];
 #pragma unroll
     for (int jj = 0; jj < 32; ++jj) {
       const int j = 32 * h + jj;
-      const float ev = Eta[s * 64 + j] * v[jj];
-      v[jj] = (r < 64) ? (slow ? 0.f : __expf(sc.r[j] - G[s * kLdG + j]) * ev)
-                       : __expf(fminf(sc.gC[j] - G[s * kLdG + j], 0.f)) * ev;
+      const float ev = Eta[s * kLdG + j] * v[jj];
+      if (slow) {
+        u[jj] = 0.f;
+        v[jj] = __expf(fminf(sc.gC[j] - G[s * kLdG + j], 0.f)) * ev;
+      } else {
+        // U~ = e^{r - G_s} eta v; V' = e^{G_C - G_s} eta v = e^{G_C - r} U~
+        u[jj] = __expf(sc.r[j] - G[s * kLdG + j]) * ev;
+        v[jj] = sc.half[j] * u[jj];
+      }
     }
-    store_half_sw(tile(r < 64 ? kU2 : kVp2), s, h, v, 1.f);
+    store_half_sw(tile(r < 64 ? kU2 : kVp2), s, h, r < 64 ? u : v, 1.f);
   }
   if (!mbar_wait(&sc.bar_mma, phase)) sc.fail = 1;
   phase ^= 1u;
@@ -242,20 +267,23 @@ __global__ void __launch_bounds__(k2Threads, 2)
           for (int jj = 0; jj < 32; ++jj) {
             const int j = 32 * h + jj;
             o[jj] += qx[s] * __expf(fminf(G[t * kLdG + j] - G[s * kLdG + j], 0.f)) *
-                     Eta[s * 64 + j] * v[jj];
+                     Eta[s * kLdG + j] * v[jj];
           }
-        }
-      } else {
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const int j = 32 * h + jj;
-          o[jj] *= __expf(G[t * kLdG + j] - sc.r[j]);
         }
       }
       // (rows past the chunk's tokens: q_t = 0, so their o rows are zero)
       float e[32];
 #pragma unroll
       for (int jj = 0; jj < 32; ++jj) e[jj] = __expf(G[t * kLdG + 32 * h + jj]);
+      if (!slow) {
+        // F = e^{G_t - r}: E / e^{r} would overflow nothing but lose range when
+        // e^{G_t} underflows, so it takes its own exponential
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const int j = 32 * h + jj;
+          o[jj] *= __expf(G[t * kLdG + j] - sc.r[j]);
+        }
+      }
       __syncwarp();
       // Writing over A and U~ is safe: both MMAs that read them have completed.
       store_half_sw(nc_stage, t, h, d, 1.f);
