@@ -57,6 +57,7 @@ constexpr uint32_t kSc3Off = kWOff + 64 * kLdW * 4;
 struct F3Scalars {
   float E[128];     // ||x_j||^2 of the 128 pairs
   float wC[128];    // w_{C,j}: the coefficients of the state leaving the chunk
+  float w31[128];   // w_{31,j}, carried into the second half of the chunk
   float coef[64];   // eta_t / B_t
   float gam[64];
   float g[64], gx[64];
@@ -188,17 +189,31 @@ __global__ void __launch_bounds__(k3Threads, 2)
             idesc_bf16(128, 128, false, false), false);
     mma_commit(&sc.bar_mma);
   }
-  // ---- W: column j of pair j = t0 - 64 + j, w_t = gamma_t w_{t-1} + [j in I_t] c_t
-  if (tid < 128) {
-    const int64_t jg = t0 - 64 + tid;
+  // ---- W: column j of pair j = t0 - 64 + j, w_t = gamma_t w_{t-1} + [j in I_t] c_t.
+  //      Two threads per column, one per half of the chunk's tokens; the second
+  //      half starts from zero and then adds (prod_{r=32}^{t} gamma_r) w_31.
+  {
+    const int col = tid & 127, hf = tid >> 7;
+    const int64_t jg = t0 - 64 + col;
     float w = 0.f;
-    for (int i = 0; i < 64; ++i) {
+    for (int ii = 0; ii < 32; ++ii) {
+      const int i = 32 * hf + ii;
       const int64_t t = t0 + i;
       const bool in = jg >= 1 && jg <= t && t <= jg + window - 1;
       w = sc.gam[i] * w + (in ? sc.coef[i] : 0.f);
-      W[i * kLdW + tid] = w;
+      W[i * kLdW + col] = w;
     }
-    sc.wC[tid] = w;
+    if (hf == 0) sc.w31[col] = w;
+    __syncthreads();
+    if (hf == 1) {
+      const float w31 = sc.w31[col];
+      float p = 1.f;
+      for (int i = 32; i < 64; ++i) {
+        p *= sc.gam[i];
+        W[i * kLdW + col] += p * w31;
+      }
+      sc.wC[col] = W[63 * kLdW + col];
+    }
   }
   __syncthreads();
   // Vs = Diag(w_C) V~ (rows r of the two V tiles)
