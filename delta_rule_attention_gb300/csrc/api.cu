@@ -285,6 +285,8 @@ int decode(int rule, int64_t N, int32_t m, int32_t dv, int32_t dtype, int32_t ph
   a.x_prev = x_prev;
   a.fresh = fresh;
   a.o = o;
+  a.err = device_error_word();
+  if (!a.err) return FALCON_ERR_CUDA;
   return to_status(falcon::launch_decode(a, stream));
 }
 

@@ -149,6 +149,7 @@ struct DecodeArgs {
   float *S, *x_prev;
   const uint8_t* fresh;
   void* o;
+  int* err = nullptr;  // device error word (a bounded wait that gave up)
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 }  // namespace falcon

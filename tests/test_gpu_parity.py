@@ -182,6 +182,41 @@ def test_decode_small_against_oracle(falcon, rule, dt):
     assert head_err(S.cpu(), S_ref) < TOL[dt]
 
 
+@pytest.mark.parametrize("m,dv", [(64, 64), (128, 64), (64, 128), (128, 32), (32, 128),
+                                  (128, 128), (16, 64), (32, 32), (16, 16), (32, 16),
+                                  (16, 128)])
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
+def test_decode_many_states_per_cta(falcon, m, dv, dt):
+    """Many states per persistent CTA (64 MB of state, or 4 per SM at least)
+    with a ragged last round: every state after three steps against the
+    oracle.  Fresh states at the first step get NaN in x_prev, which the
+    sentinel must ignore (x_t = 0)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    N = max(sms * 4, (1 << 26) // (m * dv * 4)) + 37
+    g = torch.Generator().manual_seed(m * 1000 + dv)
+    S = (0.3 * torch.randn((N, m, dv), generator=g)).cuda()
+    xp = torch.randn((N, m), generator=g)
+    xp = (xp / xp.norm(dim=-1, keepdim=True)).cuda()
+    fresh = (torch.rand(N, generator=g) < 0.3).to(torch.uint8)
+    xp_ref = xp.double().cpu().numpy().copy()
+    xp_ref[fresh.numpy() != 0] = 0.0
+    xp[fresh.cuda() != 0] = float("nan")
+    S_ref = S.double().cpu().numpy().copy()
+    fresh = fresh.cuda()
+    for step in range(3):
+        q, k, v = (torch.randn((N, d), generator=g).to(dt).cuda() for d in (m, m, dv))
+        beta = (2 * torch.sigmoid(torch.randn(N, generator=g))).cuda()
+        lam = torch.nn.functional.softplus(torch.randn(N, generator=g) - 1.0).cuda()
+        f = fresh if step == 0 else None
+        o = falcon.falcon1_decode_step(q, k, v, beta, lam, S, xp, fresh=f)
+        o_ref = oracle.decode_step("falcon1", q, k, v, beta, lam, S_ref, xp_ref,
+                                   fresh=None if f is None else f.cpu().numpy())
+        assert head_err(o.float().cpu(), o_ref, head_dims=1) < TOL[dt]
+    assert falcon.falcon_sync_check() == 0
+    assert head_err(S.cpu(), S_ref) < TOL[dt]
+    np.testing.assert_allclose(xp.cpu().numpy(), xp_ref, rtol=2e-6, atol=2e-6)
+
+
 @pytest.mark.parametrize("rule", ["falcon1", "falcon1a"])
 def test_decode_loop_equals_chunked(falcon, rule):
     """GPU vs GPU: T single-token steps (fresh at the first) reproduce the
