@@ -79,6 +79,7 @@ struct BwdScalars {
   float ssk[64];      // ||k_{t0+i-1}||^2 of the raw write-feature rows
   float ssp[2][128];  // half-row partial sums
   float ugp[2][128];
+  float fc[64];       // e^{r - g_j}, r = g_C / 2 (chunks with a log-decay span <= kBwdFactorSpan)
   float sds;          // <dS', S>_F
   int flag[64];
   int fail;
@@ -99,6 +100,12 @@ constexpr uint32_t kD3 = 192;   // T R, P^T dO, T^T dU, [dR; dO] U^T in turn
 enum : int { kLive = 1, kClamped = 2 };
 
 __device__ __forceinline__ float expn(float x) { return __expf(fminf(x, 0.f)); }
+
+// A chunk whose log-decay spans at most this much factors every e^{a - b} of
+// its decay tiles as e^{a - r} e^{r - b} with r = g_C / 2 (both factors stay
+// within fp32 range): one exponential per row and per column instead of one
+// per element.
+constexpr float kBwdFactorSpan = 80.f;
 
 // Half row (32 values) of a swizzled tile as bf16 hi parts, and the rounding
 // remainders as the lo tile.
@@ -238,6 +245,12 @@ __global__ void __launch_bounds__(kBThreads, 2)
   const float* S = S_starts + (bh * nchunks + c) * 4096;
   const float* dSp = dS_ends + (bh * nchunks + c) * 4096;
 
+  // The state entering the chunk and the cotangent leaving it are read only
+  // after the feature phase: start bringing them into L2 now.
+  if (tid == 0) {
+    bulk_prefetch_l2(S, 4096 * 4);
+    bulk_prefetch_l2(dSp, 4096 * 4);
+  }
   if (warp == 0) tmem_alloc(&sc.tmem_base, kTmemCols);
   if (tid == 0) {
     mbar_init(&sc.bar_in, 1);
@@ -252,44 +265,24 @@ __global__ void __launch_bounds__(kBThreads, 2)
     tma_load_3d(tile(kV), &tm_v, 0, (int)t0, (int)bh, &sc.bar_in);
     tma_load_3d(tile(kdO), &tm_do, 0, (int)t0, (int)bh, &sc.bar_in);
   }
+  // Per-token inputs of threads 0..63, loaded early (used after the features).
+  float beta_t = 0.f, lam_t = 0.f;
+  if (tid < n) {
+    beta_t = a.beta[rowbase + t0 + tid];
+    lam_t = a.lambda[rowbase + t0 + tid];
+  }
   if (tid < 64) {
     sc.qz[tid] = sc.rv[tid] = sc.xy[tid] = sc.xw[tid] = 0.f;
     sc.sAr[tid] = sc.sAc[tid] = sc.spr[tid] = sc.spc[tid] = 0.f;
   }
-  // [S; dS'] as split bf16 operand tiles (thread: row r of the pair, half h)
-  {
-    const float* src = (r < 64 ? S + r * 64 : dSp + (r - 64) * 64) + 32 * h;
-    float v[32];
-#pragma unroll
-    for (int q4 = 0; q4 < 8; ++q4) {
-      const float4 f = reinterpret_cast<const float4*>(src)[q4];
-      v[4 * q4] = f.x;
-      v[4 * q4 + 1] = f.y;
-      v[4 * q4 + 2] = f.z;
-      v[4 * q4 + 3] = f.w;
-    }
-    store_half_split(tile(kS), tile(kSlo), r, h, v);
-  }
-  __syncthreads();  // barriers initialised, accumulators zeroed
-  {
-    float acc = 0.f;  // <dS', S>_F, 16 elements per thread
-    const float4* s4 = reinterpret_cast<const float4*>(S) + 4 * tid;
-    const float4* d4 = reinterpret_cast<const float4*>(dSp) + 4 * tid;
-#pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
-      const float4 x = s4[q4], y = d4[q4];
-      acc += x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w;
-    }
-    acc = warp_sum(acc);
-    if (lane == 0) atomicAdd(&sc.sds, acc);
-  }
   tc_fence_before();
-  __syncthreads();
+  __syncthreads();  // barriers initialised, accumulators zeroed
   tc_fence_after();
   const uint32_t tmem = sc.tmem_base;
   const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 32 * h;  // + column
   uint32_t phase = 0;
-  float gC = 0.f;
+  float gC = 0.f, rr = 0.f;
+  bool factored = false;
   if (!mbar_wait(&sc.bar_in, 0)) sc.fail = 1;
   if (__syncthreads_or(sc.fail)) goto teardown;
 
@@ -318,6 +311,20 @@ __global__ void __launch_bounds__(kBThreads, 2)
     }
   }
   __syncthreads();
+  // The state row (or cotangent row) of this thread and, for the state rows,
+  // the matching cotangent row: requested now, consumed after the scalars.
+  float4 srow[8], drow[8];
+  {
+    const float4* src = reinterpret_cast<const float4*>(
+        (r < 64 ? S + r * 64 : dSp + (r - 64) * 64) + 32 * h);
+    const float4* d4 = reinterpret_cast<const float4*>(dSp + (r & 63) * 64 + 32 * h);
+#pragma unroll
+    for (int q4 = 0; q4 < 8; ++q4) srow[q4] = src[q4];
+    if (r < 64) {
+#pragma unroll
+      for (int q4 = 0; q4 < 8; ++q4) drow[q4] = d4[q4];
+    }
+  }
   // ---- per-token scalars as the forward forms them, then the log prefixes
   if (tid < 64) {
     float et = 0.f, gm = 1.f, lg = 0.f, le = 0.f, d = 1.f;
@@ -325,9 +332,9 @@ __global__ void __launch_bounds__(kBThreads, 2)
     if (tid < n) {
       const int64_t t = t0 + tid;
       const bool sentinel = (t == 0) && (a.x_prev == nullptr);
-      le = ridge_of(a.lambda[rowbase + t], sc.E[tid], a.ridge);
+      le = ridge_of(lam_t, sc.E[tid], a.ridge);
       d = sc.E[tid] + le + a.eps;
-      et = step_eta_gamma(sentinel, sc.E[tid], a.beta[rowbase + t], le, a.eps, a.eps_gamma, &gm,
+      et = step_eta_gamma(sentinel, sc.E[tid], beta_t, le, a.eps, a.eps_gamma, &gm,
                           &lg);
       if (!sentinel && d > 0.f) fl |= kLive;
       if (et * le >= 1.f - a.eps_gamma) fl |= kClamped;
@@ -341,8 +348,33 @@ __global__ void __launch_bounds__(kBThreads, 2)
   }
   __syncthreads();
   if (warp == 0) warp_prefix64(sc.g, sc.gx);  // g: inclusive, gx: exclusive
+  // [S; dS'] as split bf16 operand tiles (thread: row r of the pair, half h),
+  // and <dS', S>_F from the state rows' threads.
+  {
+    float v[32];
+#pragma unroll
+    for (int q4 = 0; q4 < 8; ++q4) {
+      v[4 * q4] = srow[q4].x;
+      v[4 * q4 + 1] = srow[q4].y;
+      v[4 * q4 + 2] = srow[q4].z;
+      v[4 * q4 + 3] = srow[q4].w;
+    }
+    float acc = 0.f;
+    if (r < 64) {
+#pragma unroll
+      for (int q4 = 0; q4 < 8; ++q4) {
+        const float4 y = drow[q4];
+        acc += v[4 * q4] * y.x + v[4 * q4 + 1] * y.y + v[4 * q4 + 2] * y.z + v[4 * q4 + 3] * y.w;
+      }
+    }
+    acc = warp_sum(acc);  // warps 2, 3, 6, 7 (rows of dS') add zeros
+    if (lane == 0 && r < 64) atomicAdd(&sc.sds, acc);
+    store_half_split(tile(kS), tile(kSlo), r, h, v);
+  }
   publish_tiles();
   gC = sc.g[63];
+  factored = -gC <= kBwdFactorSpan;
+  rr = 0.5f * gC;
 
   // ---- MMA: [X; Q] X^T, [X; Q] S and [X; Q] dS' (split operands)
   if (tid == 0) {
@@ -358,6 +390,7 @@ __global__ void __launch_bounds__(kBThreads, 2)
     mma_k64(tmem + kD2b, taddr(kXlo), false, 16, taddr(kdS), true, kTile, id, true);
     mma_commit(&sc.bar_mma);
   }
+  if (tid < 64 && factored) sc.fc[tid] = __expf(rr - sc.g[tid]);
   if (!wait_mma(sc, phase)) goto teardown;
   // A (fp32, for the solve; over the dead low parts), qz_i = <dO_i, (Q S)_i>
   {
@@ -365,10 +398,19 @@ __global__ void __launch_bounds__(kBThreads, 2)
     if (r < 64) {
       const float ei = sc.eta[i], gxi = sc.gx[i];
       tmem_ld32(tl + kD1, d);
+      if (factored) {
+        const float ea = ei * __expf(gxi - rr);
 #pragma unroll
-      for (int jj = 0; jj < 32; ++jj) {
-        const int j = 32 * h + jj;
-        Af[i * kLdA + j] = (f1 && j < i) ? ei * expn(gxi - sc.g[j]) * d[jj] : 0.f;
+        for (int jj = 0; jj < 32; ++jj) {
+          const int j = 32 * h + jj;
+          Af[i * kLdA + j] = (f1 && j < i) ? ea * sc.fc[j] * d[jj] : 0.f;
+        }
+      } else {
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const int j = 32 * h + jj;
+          Af[i * kLdA + j] = (f1 && j < i) ? ei * expn(gxi - sc.g[j]) * d[jj] : 0.f;
+        }
       }
     } else {
       tmem_ld32(tl + kD2a, d);
@@ -428,10 +470,19 @@ __global__ void __launch_bounds__(kBThreads, 2)
     } else {
       const float gi = sc.g[i];
       tmem_ld32(tl + kD1, d);
+      if (factored) {
+        const float ep = __expf(gi - rr);
 #pragma unroll
-      for (int jj = 0; jj < 32; ++jj) {
-        const int j = 32 * h + jj;
-        d[jj] = (j <= i) ? expn(gi - sc.g[j]) * d[jj] : 0.f;
+        for (int jj = 0; jj < 32; ++jj) {
+          const int j = 32 * h + jj;
+          d[jj] = (j <= i) ? ep * sc.fc[j] * d[jj] : 0.f;
+        }
+      } else {
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const int j = 32 * h + jj;
+          d[jj] = (j <= i) ? expn(gi - sc.g[j]) * d[jj] : 0.f;
+        }
       }
       store_half_split(tile(kP), tile(kPlo), i, h, d);
     }
@@ -505,13 +556,15 @@ __global__ void __launch_bounds__(kBThreads, 2)
     if (r < 64) {
       // dA (Falcon-1) with A recomputed from the Gram accumulator; dK tile
       const float ei = sc.eta[i], gxi = sc.gx[i];
+      const float ea = factored ? ei * __expf(gxi - rr) : 0.f;
       tmem_ld32(tl + kD3, d);
       tmem_ld32(tl + kD1, e);
       float sar = 0.f;
 #pragma unroll
       for (int jj = 0; jj < 32; ++jj) {
         const int j = 32 * h + jj;
-        const float fa = (f1 && j < i) ? ei * expn(gxi - sc.g[j]) : 0.f;
+        const float fa = (f1 && j < i) ? (factored ? ea * sc.fc[j] : ei * expn(gxi - sc.g[j]))
+                                       : 0.f;
         const float da = -d[jj];
         pr[jj] = da * fa * e[jj];  // dA_ij A_ij
         sar += pr[jj];
@@ -523,13 +576,14 @@ __global__ void __launch_bounds__(kBThreads, 2)
     } else {
       // dP with P (fp32) from the Gram accumulator; dPE and dOs tiles
       const float gi = sc.g[i];
+      const float ep = factored ? __expf(gi - rr) : 0.f;
       tmem_ld32(tl + kD3, d);
       tmem_ld32(tl + kD1, e);
       float spr = 0.f;
 #pragma unroll
       for (int jj = 0; jj < 32; ++jj) {
         const int j = 32 * h + jj;
-        const float ef = (j <= i) ? expn(gi - sc.g[j]) : 0.f;
+        const float ef = (j <= i) ? (factored ? ep * sc.fc[j] : expn(gi - sc.g[j])) : 0.f;
         pr[jj] = d[jj] * ef * e[jj];  // dP_ij P_ij
         spr += pr[jj];
         d[jj] *= ef;
@@ -588,7 +642,7 @@ __global__ void __launch_bounds__(kBThreads, 2)
         dl += dden;
         if (a.ridge == FALCON_RIDGE_SCALED) {
           dl_in = dl * sc.E[tid];
-          dEi += dl * a.lambda[rowbase + t0 + tid];
+          dEi += dl * lam_t;
         } else {
           dl_in = dl;
         }
