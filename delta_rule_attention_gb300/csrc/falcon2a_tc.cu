@@ -58,7 +58,7 @@ constexpr uint32_t kGOff = kEtaOff + 64 * kLdG * 4;   // G (fp32, 64 x kLdG)
 constexpr uint32_t kSc2Off = kGOff + 64 * kLdG * 4;
 
 struct F2Scalars {
-  float E[64], den[64], lam[64], r[64], gC[64], half[64];
+  float E[64], inv[64], lam[64], r[64], gC[64], half[64];  // inv: 1 / (E + lambda + eps), 0 if none
   float part[4][64];  // column sums of the four quarters of the token range
   float ssp[2][128];
   int fail, slow;
@@ -142,23 +142,31 @@ __global__ void __launch_bounds__(k2Threads, 2)
   }
   __syncthreads();
   if (tid < 64) {
+    // The step-size denominator is shared by the token's columns: one
+    // reciprocal per token (0 for the sentinel and a non-positive denominator).
     const float lam = ridge_of(sc.lam[tid], sc.E[tid], a.ridge);
     sc.lam[tid] = lam;
-    sc.den[tid] = sc.E[tid] + lam + a.eps;
+    const float den = sc.E[tid] + lam + a.eps;
+    const bool sentinel = (t0 + tid == 0) && (a.x_prev == nullptr);
+    sc.inv[tid] = (!sentinel && den > 0.f) ? 1.f / den : 0.f;
   }
   __syncthreads();
-  // ---- eta_{j,t} and log gamma_{j,t} per (token, column), then the prefix
-  //      down each column
-  for (int idx = tid; idx < 64 * 64; idx += k2Threads) {
-    const int t = idx >> 6, j = idx & 63;
-    float eta = 0.f, gm = 1.f, lg = 0.f;
-    if (t < n) {
-      const bool sentinel = (t0 + t == 0) && (a.x_prev == nullptr);
-      eta = step_eta_gamma(sentinel, sc.E[t], Beta[idx], sc.lam[t], a.eps, a.eps_gamma, &gm,
-                           &lg);
+  // ---- eta_{j,t} and log gamma_{j,t} per (token, column) (the decay clamp of
+  //      step_eta_gamma: gamma = eps_gamma exactly on the clamped branch), then
+  //      the prefix down each column
+  {
+    const float lg_clamped = logf(a.eps_gamma);
+    for (int idx = tid; idx < 64 * 64; idx += k2Threads) {
+      const int t = idx >> 6, j = idx & 63;
+      float eta = 0.f, lg = 0.f;
+      if (t < n) {
+        eta = Beta[idx] * sc.inv[t];
+        const float al = eta * sc.lam[t];
+        lg = al >= 1.f - a.eps_gamma ? lg_clamped : log1pf(-al);
+      }
+      Eta[t * kLdG + j] = eta;
+      G[t * kLdG + j] = lg;
     }
-    Eta[t * kLdG + j] = eta;
-    G[t * kLdG + j] = lg;
   }
   __syncthreads();
   {
