@@ -540,7 +540,7 @@ __device__ __forceinline__ void add_bf16x16(float* d, uint4 p0, uint4 p1) {
 
 // kRecord: also write the state entering every chunk to a.S_starts.
 template <bool kRecord>
-__global__ void __launch_bounds__(kScanThreads)
+__global__ void __launch_bounds__(kScanThreads, 1)
     tc_chunk_scan_kernel(ChunkArgs a, int nchunks, int c_begin, int n, const float* S_in, int* err,
                          const __grid_constant__ CUtensorMap tm_o) {
   extern __shared__ unsigned char smem_raw[];
