@@ -20,8 +20,9 @@
 //        MMA1   [K; Q] K^T (raw rows)      -> Gram of the write features, Q X^T
 //        MMA2   [Xh^T; Vh^T] T^T           -> [W^T; U~^T]
 //        MMA3   [Xt^T; P] [W | U~]         -> [Xt^T W | Xt^T U~ ; P W | P U~]
-//     The unit-lower solve runs in fp32 (diagonal 16 x 16 blocks) with warp
-//     MMAs for the off-diagonal block products.  The map goes to the workspace
+//     The unit-lower solve runs in fp32 on the diagonal 16 x 16 blocks; the
+//     blocks below them follow in 8-column strips, one warp each, with warp
+//     MMAs whose operands stay in registers.  The map goes to the workspace
 //     as ready-to-use bf16 tiles (Mc swizzled as an MMA operand, Nc with rows
 //     swizzled at 16-byte granularity) plus e^{g_C}.
 //     Falcon-1A takes the same path with T = I and W = 0.
@@ -65,18 +66,20 @@ constexpr float kFactorSpan = 80.f;
 //   Q   [8192, 16384)   raw q rows as landed by TMA; [K; Q] is MMA1's A operand
 //                       -> zero tile (atom 1 of MMA3a; rows 0..63 of MMA3b)
 //   P   [16384, 24576)  P (rows 64..127 of MMA3b, K-major)
-//   R1  [24576, 41984)  A (fp32, rows of 68 floats) -> T (bf16, MMA2 B)
-//                       -> [W^T; U~^T] (MMA3 B) -> Nc staging
-//   R2  [41984, 62464)  solve scratch (T in fp32 rows of 65, right-hand sides)
-//                       -> Xh rows (atom 0 of MMA2's MN-major A)
-//   VH  [62464, 70656)  raw v rows as landed by TMA, then Vh = Diag(eta) V in
+//   A   [24576, 32768)  A as bf16 (the solve's MMA operand) -> [W^T; U~^T]
+//                       (MMA3 B, 16 KB over A, AD and T) -> Nc staging
+//   AD  [32768, 37120)  the fp32 diagonal 16 x 16 blocks of A (rows of 17)
+//   T   [37888, 46080)  T = (I + A)^{-1} as bf16 (MMA2 B, K-major)
+//   XH  [46080, 54272)  Xh rows (atom 0 of MMA2's MN-major A)
+//   VH  [54272, 62464)  raw v rows as landed by TMA, then Vh = Diag(eta) V in
 //                       place (atom 1 of MMA2's A)
-//   SC  [70656, ...)    per-token scalars and barriers
+//   SC  [62464, ...)    per-token scalars and barriers
 // m = 128: [K; Q] is two K-atoms of 16 KB, [K_a0 | Q_a0 | K_a1 | Q_a1]
 // (columns 0..63 and 64..127); afterwards Xt's two M-atoms replace K_a0 and
 // K_a1 and P replaces Q_a0; MMA3a (Xt^T [W | U~], 128 rows) and MMA3b
 // ([junk; P] [W | U~]) go to separate accumulators, so no zero tile is used.
-// R1, R2, VH follow at 32768, 50176, 70656 (VH holds the v columns of half j).
+// A, AD, T, XH, VH follow at 32768, 40960, 46080, 54272, 62464 (XH holds the
+// x columns and VH the v columns of half j).
 // MMA1 runs on the raw bf16 rows; phi's normalisation enters afterwards as
 // fp32 row and column scalings of the accumulators and of the later operand
 // copies.
@@ -84,8 +87,8 @@ template <int M>
 struct MapLayout;
 template <>
 struct MapLayout<64> {
-  static constexpr uint32_t K = 0, Q = 8192, P = 16384, R1 = 24576, R2 = 41984, VH = 62464,
-                            SC = 70656;
+  static constexpr uint32_t K = 0, Q = 8192, P = 16384, A = 24576, AD = 32768, T = 37888,
+                            XH = 46080, VH = 54272, SC = 62464;
   static constexpr uint32_t kAtom = 0;  // K-atom stride of [K; Q] (one atom)
   static constexpr int kHalves = 1;
   static constexpr int kMinBlocks = 3;
@@ -94,8 +97,8 @@ struct MapLayout<64> {
 };
 template <>
 struct MapLayout<128> {
-  static constexpr uint32_t K = 0, Q = 8192, P = 8192, R1 = 32768, R2 = 50176, VH = 70656,
-                            SC = 78848;
+  static constexpr uint32_t K = 0, Q = 8192, P = 8192, A = 32768, AD = 40960, T = 46080,
+                            XH = 54272, VH = 62464, SC = 70656;
   static constexpr uint32_t kAtom = 16384;
   static constexpr int kHalves = 2;
   static constexpr int kMinBlocks = 2;
@@ -105,9 +108,15 @@ struct MapLayout<128> {
   static constexpr uint32_t kMcAtom = 192 * 128;
   static constexpr uint32_t kMapBytes = 4 * kMcAtom + 128;
 };
-constexpr uint32_t kLboA2 = 20480;  // Xh atom -> Vh atom of MMA2's A operand (VH - R2)
-static_assert(MapLayout<64>::VH - MapLayout<64>::R2 == kLboA2, "MMA2 operand layout");
-static_assert(MapLayout<128>::VH - MapLayout<128>::R2 == kLboA2, "MMA2 operand layout");
+template <int M>
+constexpr bool map_layout_ok() {
+  using L = MapLayout<M>;
+  return L::A % 1024 == 0 && L::T % 1024 == 0 && L::XH % 1024 == 0 && L::VH % 1024 == 0 &&
+         L::AD >= L::A + 8192 && L::AD + 64 * kLdD * 4 <= L::T && L::XH >= L::T + 8192 &&
+         L::VH >= L::XH + 8192 && L::SC >= L::VH + 8192 &&
+         L::A + 16384 <= L::XH;  // [W^T; U~^T] over A, AD and T only
+}
+static_assert(map_layout_ok<64>() && map_layout_ok<128>(), "map kernel shared-memory layout");
 
 struct MapScalars {
   float eta[64], g[64], gx[64];
@@ -140,13 +149,13 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
   unsigned char* const kt = base + L::K;
   unsigned char* const qt = base + L::Q;
   unsigned char* const p_tile = base + L::P;
-  unsigned char* const r1 = base + L::R1;
-  unsigned char* const r2 = base + L::R2;
+  unsigned char* const a_tile = base + L::A;
+  unsigned char* const t_tile = base + L::T;
+  unsigned char* const xh_tile = base + L::XH;
+  unsigned char* const wu_tile = base + L::A;  // [W^T; U~^T], later the Nc staging
   unsigned char* const vh = base + L::VH;
   MapScalars& sc = *reinterpret_cast<MapScalars*>(base + L::SC);
-  float* const As = reinterpret_cast<float*>(r1);
-  float* const Ts = reinterpret_cast<float*>(r2);
-  float* const Rs = Ts + 64 * kLdT;
+  float* const a_diag = reinterpret_cast<float*>(base + L::AD);
   unsigned char* const xt_tile = kt;    // MN-major A of MMA3a, atom 0
   unsigned char* const zero_tile = qt;  // m = 64: atom 1 of MMA3a; rows 0..63 of MMA3b
 
@@ -297,6 +306,17 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
     sc.fv[r] = sc.eta[r] * __expf(sc.gx[r] - rr);
     sc.fw[r] = __expf(sc.g[r] - rr);
   }
+  if (r < 64) {
+    // Xh = Diag(eta e^{g_-}) X (MMA2's A, columns of half j); Falcon-1A: W = 0
+    // and T = I, whose rows are written here (the solve writes Falcon-1's T).
+    store_half_sw(xh_tile, r, h, x, f1 ? sc.eta[r] * __expf(sc.gx[r]) * nr : 0.f);
+    if (!f1) {
+      float trow[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) trow[i] = (32 * h + i == r) ? 1.f : 0.f;
+      store_half_sw(t_tile, r, h, trow, 1.f);
+    }
+  }
   if (!sc.fail && !mbar_wait(&sc.bar_mma, 0)) sc.fail = 1;
   tc_fence_after();
   __syncthreads();  // factors visible; MMA1 has finished reading [K; Q]
@@ -335,10 +355,19 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
           for (int l = 0; l < 32; ++l)
             d[l] = (32 * h + l < r) ? er * __expf(fminf(gxr - sc.g[32 * h + l], 0.f)) * d[l] : 0.f;
         }
-        float4* arow = reinterpret_cast<float4*>(As + r * kLdA + 32 * h);
+        // A row r as bf16 for the solve's MMAs; its diagonal block (columns
+        // 16 (r / 16) .. +15, in this thread's half when h == r / 32) in fp32.
+        store_half_sw(a_tile, r, h, d, 1.f);
+        if (h == (r >> 5)) {
+          float* drow = a_diag + r * kLdD;
+          if (r & 16) {
 #pragma unroll
-        for (int l4 = 0; l4 < 8; ++l4)
-          arow[l4] = make_float4(d[4 * l4], d[4 * l4 + 1], d[4 * l4 + 2], d[4 * l4 + 3]);
+            for (int k = 0; k < 16; ++k) drow[k] = d[16 + k];
+          } else {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) drow[k] = d[k];
+          }
+        }
       }
     } else {
       // P row i: e^{g_i - g_j} <phi(q_i), x_j> for j <= i
@@ -359,21 +388,8 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
   }
   if (__syncthreads_or(sc.fail)) goto teardown;  // A and P complete
 
-  // ---- T = (I + A)^{-1} (identity for Falcon-1A), then the MMA2 operands ----
-  if (f1) solve_unit_lower(As, Ts, Rs);
-  if (r < 64) {
-    // T row r as bf16 into R1 (A is dead): up to the end of the diagonal block, zero beyond.
-    float trow[32];
-    const int end = (r | 15) + 1;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int col = 32 * h + i;
-      trow[i] = f1 ? ((col < end) ? Ts[r * kLdT + col] : 0.f) : ((col == r) ? 1.f : 0.f);
-    }
-    store_half_sw(r1, r, h, trow, 1.f);
-  }
-  __syncthreads();  // Xh overwrites the solve scratch
-  if (r < 64) store_half_sw(r2, r, h, x, f1 ? sc.eta[r] * __expf(sc.gx[r]) * nr : 0.f);
+  // ---- T = (I + A)^{-1} into the T tile (Falcon-1A: the identity, written above) ----
+  if (f1) solve_unit_lower_sw(a_tile, a_diag, t_tile);
   fence_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -381,7 +397,7 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
 
   // ---- MMA2: D[0:64) = [Xh^T; Vh^T] T^T = [W^T; U~^T] (columns of half j) ----
   if (tid == 0) {
-    mma_k64(tmem, smem_addr(r2), true, kLboA2, smem_addr(r1), false, 16,
+    mma_k64(tmem, smem_addr(xh_tile), true, L::VH - L::XH, smem_addr(t_tile), false, 16,
             idesc_bf16(128, 64, true, false), false);
     mma_commit(&sc.bar_mma);
   }
@@ -390,7 +406,7 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
   {
     float d[32];
     tmem_ld32(tlane + 32 * h, d);
-    store_half_sw(r1, r, h, d, 1.f);  // [W^T; U~^T] over T (MMA2 is complete)
+    store_half_sw(wu_tile, r, h, d, 1.f);  // [W^T; U~^T] over A, AD, T (MMA2 is complete)
   }
   fence_async_smem();
   tc_fence_before();
@@ -402,14 +418,14 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
   //   m = 128: D[0:128) = Xt^T [W | U~];  D[128:256) = [junk; P] [W | U~]
   if (tid == 0) {
     if (kWide) {
-      mma_k64(tmem, smem_addr(xt_tile), true, L::kAtom, smem_addr(r1), false, 16,
+      mma_k64(tmem, smem_addr(xt_tile), true, L::kAtom, smem_addr(wu_tile), false, 16,
               idesc_bf16(128, 128, true, false), false);
-      mma_k64(tmem + 128, smem_addr(p_tile - 8192), false, 16, smem_addr(r1), false, 16,
+      mma_k64(tmem + 128, smem_addr(p_tile - 8192), false, 16, smem_addr(wu_tile), false, 16,
               idesc_bf16(128, 128, false, false), false);
     } else {
-      mma_k64(tmem, smem_addr(xt_tile), true, 8192, smem_addr(r1), false, 16,
+      mma_k64(tmem, smem_addr(xt_tile), true, 8192, smem_addr(wu_tile), false, 16,
               idesc_bf16(128, 128, true, false), false);
-      mma_k64(tmem, smem_addr(zero_tile), false, 16, smem_addr(r1), false, 16,
+      mma_k64(tmem, smem_addr(zero_tile), false, 16, smem_addr(wu_tile), false, 16,
               idesc_bf16(128, 128, false, false), true);
     }
     mma_commit(&sc.bar_mma);
@@ -424,7 +440,7 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
     float d[32];
     if constexpr (!kWide) {
       unsigned char* mc_stage = kt;  // 16 KB over the K and Q tiles
-      unsigned char* nc_stage = r1;  // 16 KB
+      unsigned char* nc_stage = wu_tile;  // 16 KB
       tmem_ld32(tlane + 32 * h, d);
       // Mc row: rows < 64 -> -Xt^T W ; rows >= 64 -> e^{g_i} phi(q_i) - P W
       const float eq = (r >= 64) ? __expf(sc.g[r - 64]) * nr : 0.f;
@@ -448,7 +464,7 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
       unsigned char* mcs_stage = base;          // 16 KB
       unsigned char* mco_stage = base + 16384;  // 8 KB
       unsigned char* nco_stage = base + 24576;  // 8 KB
-      unsigned char* ncs_stage = r1;            // 16 KB
+      unsigned char* ncs_stage = wu_tile;       // 16 KB
       tmem_ld32(tlane + 32 * h, d);
 #pragma unroll
       for (int i = 0; i < 32; ++i) d[i] = -d[i];
@@ -1038,14 +1054,19 @@ cudaError_t launch_scan(Kernel kernel, unsigned grid, unsigned threads, size_t s
 // Pieces of the chunk range: with few heads and many chunks the scan runs on
 // few SMs for a long time, so the call is cut into chunk ranges whose scans run
 // on a second stream while the maps of the next range run on the caller's
-// stream (event-ordered; no kernel waits on another).  With many heads the
-// scan already fills most SMs and a single range is kept (measured on the lm
-// shape: 1 range 118 us, 2 ranges 136 us; on the long shape, 1024 chunks of 16
-// heads: 1, 4, 8, 16, 32 ranges took 2.65, 2.18, 1.94, 1.90, 2.06 ms).
+// stream (event-ordered; no kernel waits on another).  The second stream has
+// the highest priority, so the CTAs of a pending scan (the sequential part,
+// which bounds the call) are placed ahead of the next range's map CTAs.  With
+// many heads the scan already fills most SMs and a single range is kept
+// (measured on the lm shape: 1 range 118 us, 2 ranges 136 us).  Long shape,
+// 1024 chunks of 16 heads, side stream at the default priority: 1, 4, 8, 16,
+// 32 ranges took 2.65, 2.18, 1.94, 1.90, 2.06 ms; with the current map kernel
+// and the side stream at the highest priority, 8, 16, 32 ranges took 1.75,
+// 1.84, 2.09 ms.
 int piece_count(int64_t BH, int nchunks, bool wide) {
   const int64_t scan_ctas = BH * (wide ? 2 : 1);
   if (scan_ctas > 64 || nchunks < 64) return 1;
-  return nchunks >= 512 ? 16 : (nchunks >= 256 ? 8 : 4);
+  return nchunks >= 256 ? 8 : 4;
 }
 
 constexpr int kMaxPieces = 16;
@@ -1068,7 +1089,11 @@ cudaError_t piece_streams(PieceStreams** out) {
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   PieceStreams& ps = g_piece[dev];
   if (!ps.ready) {
-    if ((e = cudaStreamCreateWithFlags(&ps.side, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    int least = 0, greatest = 0;
+    if ((e = cudaDeviceGetStreamPriorityRange(&least, &greatest)) != cudaSuccess) return e;
+    if ((e = cudaStreamCreateWithPriority(&ps.side, cudaStreamNonBlocking, greatest)) !=
+        cudaSuccess)
+      return e;
     for (int i = 0; i < kMaxPieces; ++i)
       if ((e = cudaEventCreateWithFlags(&ps.map_done[i], cudaEventDisableTiming)) != cudaSuccess)
         return e;

@@ -189,6 +189,124 @@ __device__ void solve_unit_lower(const float* As, float* Ts, float* Rs) {
   }
 }
 
+// ---- the same inverse with its off-diagonal blocks in registers ----------
+// Byte offset of 16-byte chunk c of row r in a 64-wide bf16 tile with the
+// 128-byte swizzle.
+__device__ __forceinline__ uint32_t sw_chunk(int r, int c) {
+  return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// Four 8 x 8 bf16 matrices from shared memory in the mma.sync A-fragment
+// layout (lanes 0-7, 8-15, 16-23, 24-31 give the row addresses of matrices
+// 0..3).
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t saddr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(saddr)
+               : "memory");
+}
+
+// Two 8 x 8 bf16 matrices, transposed on the way (rows of a row-major K x N
+// tile become the mma.sync B fragment; lanes 0-15 give the row addresses).
+__device__ __forceinline__ void ldsm_x2_trans(uint32_t (&r)[2], uint32_t saddr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(saddr)
+               : "memory");
+}
+
+// Transpose of an 8 x 8 bf16 matrix held one 32-bit pair per lane (row
+// lane / 4, columns 2 (lane % 4) and +1) across the warp.
+__device__ __forceinline__ uint32_t movm_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
+constexpr int kLdD = 17;  // fp32 row stride of the diagonal blocks of A
+
+// T = (I + A)^{-1} for the strictly lower 64 x 64 A, eight warps, the result
+// written as bf16 into the 128-byte swizzled 64 x 64 tile t_tile (rows of T,
+// the K-major operand image), zero above the diagonal blocks.  Inputs: a_tile,
+// A as bf16 in the same layout, and a_diag, the fp32 diagonal blocks (row i
+// holds A[i][16 (i / 16) + k], k = 0..15, rows of kLdD floats).
+//
+// Diagonal block b is inverted in fp32 by forward substitution exactly as in
+// solve_unit_lower.  Below it, T_{b,<b} = T_bb (-A_{b,<b} T_{<b}) splits into
+// independent 8-column strips: strip n (columns 8n .. 8n+7, n = 0..5) of
+// block row b needs only strip n of the block rows above it.  Warp n runs its
+// strip down the block rows with warp MMAs, keeping each finished block as
+// the next MMA's B operand in registers: an accumulator tile, packed to bf16,
+// is transposed across the warp by movmatrix into operand layout, so neither
+// the right-hand side nor the finished blocks go through shared memory and the
+// warps do not wait on one another.  Every operand is rounded to bf16 at the
+// same point as in solve_unit_lower, so the two give the same T.
+// The caller fences and synchronises before T is read.
+__device__ void solve_unit_lower_sw(const unsigned char* a_tile, const float* a_diag,
+                                    unsigned char* t_tile) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  {
+    const int b = warp & 3, hh = warp >> 2, rr = lane >> 1, q = lane & 1, row = 16 * b + rr;
+    float arow[15];
+#pragma unroll
+    for (int k = 0; k < 15; ++k) arow[k] = a_diag[row * kLdD + k];
+    float dv4[4];
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) dv4[jj] = (8 * hh + 4 * q + jj == rr) ? 1.f : 0.f;
+#pragma unroll
+    for (int k = 0; k < 15; ++k) {
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const float tkj = __shfl_sync(0xffffffffu, dv4[jj], 2 * k + q);
+        if (rr > k) dv4[jj] -= arow[k] * tkj;
+      }
+    }
+    // Columns 16b + 8hh + 4q .. +3 of the row; the four threads of a row zero
+    // the chunks right of the diagonal block.
+    *reinterpret_cast<uint2*>(t_tile + sw_chunk(row, 2 * b + hh) + 8 * q) =
+        make_uint2(pack_bf16(dv4[0], dv4[1]), pack_bf16(dv4[2], dv4[3]));
+    for (int z = 2 * b + 2 + 2 * hh + q; z < 8; z += 4)
+      *reinterpret_cast<uint4*>(t_tile + sw_chunk(row, z)) = make_uint4(0u, 0u, 0u, 0u);
+  }
+  __syncthreads();  // diagonal blocks of T complete
+  if (warp < 6) {
+    const int nt = warp, kb0 = nt >> 1, g = lane >> 2, t = lane & 3;
+    const int la = (lane & 7) + 8 * ((lane >> 3) & 1), ca = lane >> 4;
+    const uint32_t abase = smem_addr(a_tile), tbase = smem_addr(t_tile);
+    uint32_t tb[4][2];  // finished blocks (kb, strip) as B fragments
+#pragma unroll
+    for (int kb = 0; kb < 3; ++kb)
+      if (kb == kb0) ldsm_x2_trans(tb[kb], tbase + sw_chunk(16 * kb + la, nt));
+#pragma unroll
+    for (int b = 1; b < 4; ++b) {
+      if (b <= kb0) continue;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kb = 0; kb < b; ++kb) {
+        if (kb < kb0) continue;
+        uint32_t fa[4];
+        ldsm_x4(fa, abase + sw_chunk(16 * b + la, 2 * kb + ca));
+        mma16816(acc, fa, tb[kb]);
+      }
+      // R = -A_{b,<b} T_{<b} (strip nt) as the B operand of T_bb R.
+      const uint32_t rb[2] = {movm_trans(pack_bf16(-acc[0], -acc[1])),
+                              movm_trans(pack_bf16(-acc[2], -acc[3]))};
+      uint32_t fd[4];
+      ldsm_x4(fd, tbase + sw_chunk(16 * b + la, 2 * b + ca));
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      mma16816(c, fd, rb);
+      const uint32_t lo = pack_bf16(c[0], c[1]), hi = pack_bf16(c[2], c[3]);
+      const int r0 = 16 * b + g;
+      *reinterpret_cast<uint32_t*>(t_tile + sw_chunk(r0, nt) + 4 * t) = lo;
+      *reinterpret_cast<uint32_t*>(t_tile + sw_chunk(r0 + 8, nt) + 4 * t) = hi;
+      if (b < 3) {
+        tb[b][0] = movm_trans(lo);
+        tb[b][1] = movm_trans(hi);
+      }
+    }
+  }
+}
+
 }  // namespace
 }  // namespace tcu
 }  // namespace falcon
