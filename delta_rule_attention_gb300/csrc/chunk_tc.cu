@@ -71,15 +71,18 @@ constexpr float kFactorSpan = 80.f;
 //   AD  [32768, 37120)  the fp32 diagonal 16 x 16 blocks of A (rows of 17)
 //   T   [37888, 46080)  T = (I + A)^{-1} as bf16 (MMA2 B, K-major)
 //   XH  [46080, 54272)  Xh rows (atom 0 of MMA2's MN-major A)
-//   VH  [54272, 62464)  raw v rows as landed by TMA, then Vh = Diag(eta) V in
-//                       place (atom 1 of MMA2's A)
-//   SC  [62464, ...)    per-token scalars and barriers
+//   VH  [54272, 62464)  raw v rows as landed by TMA (atom 1 of MMA2's A)
+//   DB  [62464, 64512)  the unscaled diagonal blocks of T (bf16, the solve's)
+//   SC  [64512, ...)    per-token scalars and barriers
 // m = 128: [K; Q] is two K-atoms of 16 KB, [K_a0 | Q_a0 | K_a1 | Q_a1]
 // (columns 0..63 and 64..127); afterwards Xt's two M-atoms replace K_a0 and
 // K_a1 and P replaces Q_a0; MMA3a (Xt^T [W | U~], 128 rows) and MMA3b
 // ([junk; P] [W | U~]) go to separate accumulators, so no zero tile is used.
-// A, AD, T, XH, VH follow at 32768, 40960, 46080, 54272, 62464 (XH holds the
-// x columns and VH the v columns of half j).
+// A, AD, T, XH, VH, DB follow at 32768, 40960, 46080, 54272, 62464, 70656
+// (XH holds the x columns and VH the v columns of half j).
+// T carries the step sizes in its columns, T' = T Diag(eta), so that
+// MMA2 = [Xh^T; V^T] T'^T gives W^T = (T Diag(eta e^{g_-}) X)^T with
+// Xh = Diag(e^{g_-}) X and U~^T = (T Diag(eta) V)^T from the raw v rows.
 // MMA1 runs on the raw bf16 rows; phi's normalisation enters afterwards as
 // fp32 row and column scalings of the accumulators and of the later operand
 // copies.
@@ -88,7 +91,7 @@ struct MapLayout;
 template <>
 struct MapLayout<64> {
   static constexpr uint32_t K = 0, Q = 8192, P = 16384, A = 24576, AD = 32768, T = 37888,
-                            XH = 46080, VH = 54272, SC = 62464;
+                            XH = 46080, VH = 54272, DB = 62464, SC = 64512;
   static constexpr uint32_t kAtom = 0;  // K-atom stride of [K; Q] (one atom)
   static constexpr int kHalves = 1;
   static constexpr int kMinBlocks = 3;
@@ -98,7 +101,7 @@ struct MapLayout<64> {
 template <>
 struct MapLayout<128> {
   static constexpr uint32_t K = 0, Q = 8192, P = 8192, A = 32768, AD = 40960, T = 46080,
-                            XH = 54272, VH = 62464, SC = 70656;
+                            XH = 54272, VH = 62464, DB = 70656, SC = 72704;
   static constexpr uint32_t kAtom = 16384;
   static constexpr int kHalves = 2;
   static constexpr int kMinBlocks = 2;
@@ -113,14 +116,18 @@ constexpr bool map_layout_ok() {
   using L = MapLayout<M>;
   return L::A % 1024 == 0 && L::T % 1024 == 0 && L::XH % 1024 == 0 && L::VH % 1024 == 0 &&
          L::AD >= L::A + 8192 && L::AD + 64 * kLdD * 4 <= L::T && L::XH >= L::T + 8192 &&
-         L::VH >= L::XH + 8192 && L::SC >= L::VH + 8192 &&
+         L::VH >= L::XH + 8192 && L::DB >= L::VH + 8192 && L::SC >= L::DB + 2048 &&
+         L::SC % 16 == 0 &&
          L::A + 16384 <= L::XH;  // [W^T; U~^T] over A, AD and T only
 }
 static_assert(map_layout_ok<64>() && map_layout_ok<128>(), "map kernel shared-memory layout");
 
 struct MapScalars {
   float eta[64], g[64], gx[64];
-  float fu[64], fv[64], fw[64];  // rank-1 decay factors (span <= kFactorSpan)
+  // Rank-1 decay factors (span <= kFactorSpan), with phi's scale of x_l in the
+  // column factor: cu_l = e^{rr - g_l} / ||x_l||, fv_j = eta_j e^{g_{j-1} - rr},
+  // fw_i = e^{g_i - rr}.
+  float cu[64], fv[64], fw[64];
   float nrm[128];                // phi's scale of row r of [K; Q] (1 / ||row||, or 1)
   float ssp[2][128];             // half-row partial sums of squares
   float carry;
@@ -298,22 +305,23 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
   __syncthreads();
   const float gC = sc.g[kC - 1];
   const bool factored = -gC <= kFactorSpan;
-  // Rank-1 decay factors around rr = g_C / 2: fu_l = e^{rr - g_l},
-  // fv_j = eta_j e^{g_{j-1} - rr}, fw_i = e^{g_i - rr}.
+  // Rank-1 decay factors around rr = g_C / 2: e^{rr - g_l} (times phi's scale
+  // of x_l), fv_j = eta_j e^{g_{j-1} - rr}, fw_i = e^{g_i - rr}.
   if (r < 64 && h == 0 && factored) {
     const float rr = 0.5f * gC;
-    sc.fu[r] = __expf(rr - sc.g[r]);
+    sc.cu[r] = __expf(rr - sc.g[r]) * nr;
     sc.fv[r] = sc.eta[r] * __expf(sc.gx[r] - rr);
     sc.fw[r] = __expf(sc.g[r] - rr);
   }
   if (r < 64) {
-    // Xh = Diag(eta e^{g_-}) X (MMA2's A, columns of half j); Falcon-1A: W = 0
-    // and T = I, whose rows are written here (the solve writes Falcon-1's T).
-    store_half_sw(xh_tile, r, h, x, f1 ? sc.eta[r] * __expf(sc.gx[r]) * nr : 0.f);
+    // Xh = Diag(e^{g_-}) X (MMA2's A, columns of half j); Falcon-1A: W = 0 and
+    // T' = Diag(eta), whose rows are written here (the solve writes Falcon-1's).
+    store_half_sw(xh_tile, r, h, x, f1 ? __expf(sc.gx[r]) * nr : 0.f);
     if (!f1) {
       float trow[32];
+      const float er = sc.eta[r];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) trow[i] = (32 * h + i == r) ? 1.f : 0.f;
+      for (int i = 0; i < 32; ++i) trow[i] = (32 * h + i == r) ? er : 0.f;
       store_half_sw(t_tile, r, h, trow, 1.f);
     }
   }
@@ -321,34 +329,41 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
   tc_fence_after();
   __syncthreads();  // factors visible; MMA1 has finished reading [K; Q]
 
-  // Xt = Diag(e^{g_C - g}) X over the K tile, the zero tile (m = 64), Vh in place.
+  // Xt = Diag(e^{g_C - g}) X over the K tile (m = 64: by the threads of rows
+  // 64..127, each rewriting in place the four chunks it reads; m = 128: from
+  // the rows held in registers), and the zero tile (m = 64).
   if (!kWide) {
     reinterpret_cast<uint4*>(zero_tile)[tid] = make_uint4(0u, 0u, 0u, 0u);
     reinterpret_cast<uint4*>(zero_tile)[tid + 256] = make_uint4(0u, 0u, 0u, 0u);
-  }
-  if (r < 64) {
+    if (r >= 64 && !(patch && r == 64)) {
+      const int l = r - 64;
+      scale_half_sw(xt_tile, l, h, __expf(gC - sc.g[l]) * sc.nrm[l]);
+    } else if (patch && r == 0) {
+      // x_1 = x_prev from the fp32 values (the tile holds them rounded)
+      store_half_sw(xt_tile, 0, h, x, __expf(gC - sc.g[0]) * nr);
+    }
+  } else if (r < 64) {
     const float xs = __expf(gC - sc.g[r]) * nr;
     store_half_sw(xt_tile + j * L::kAtom, r, h, x, xs);
-    if (kWide) store_half_sw(xt_tile + (1 - j) * L::kAtom, r, h, xo, xs);
-  } else {
-    // Each thread rewrites exactly the four chunks it reads.
-    float v[32];
-    load_half_sw(vh, r - 64, h, v);
-    store_half_sw(vh, r - 64, h, v, sc.eta[r - 64]);
+    store_half_sw(xt_tile + (1 - j) * L::kAtom, r, h, xo, xs);
   }
   {
     float d[32];
     tmem_ld32(tlane + 32 * h, d);
-    // Cosines first: d_l = <phi(row r), x_l> (bounded), then the decay factors.
+    // Factored decay: one row factor (phi's scale of row r times fv or fw) and
+    // one column factor cu_l = fu_l phi-scale(x_l); otherwise the cosines first
+    // (bounded), then per-element exponentials of non-positive arguments.
+    if (!factored) {
 #pragma unroll
-    for (int l = 0; l < 32; ++l) d[l] = (d[l] * nr) * sc.nrm[32 * h + l];
+      for (int l = 0; l < 32; ++l) d[l] = (d[l] * nr) * sc.nrm[32 * h + l];
+    }
     if (r < 64) {
       // A row r: eta_r e^{g_{r-1} - g_l} <x_r, x_l> for l < r (computed, then stored)
       if (f1) {
         if (factored) {
-          const float vr = sc.fv[r];
+          const float vr = nr * sc.fv[r];
 #pragma unroll
-          for (int l = 0; l < 32; ++l) d[l] = (32 * h + l < r) ? vr * sc.fu[32 * h + l] * d[l] : 0.f;
+          for (int l = 0; l < 32; ++l) d[l] = (32 * h + l < r) ? (d[l] * vr) * sc.cu[32 * h + l] : 0.f;
         } else {
           const float er = sc.eta[r], gxr = sc.gx[r];
 #pragma unroll
@@ -373,10 +388,10 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
       // P row i: e^{g_i - g_j} <phi(q_i), x_j> for j <= i
       const int i = r - 64;
       if (factored) {
-        const float wi = sc.fw[i];
+        const float wi = nr * sc.fw[i];
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj)
-          d[jj] = (32 * h + jj <= i) ? wi * sc.fu[32 * h + jj] * d[jj] : 0.f;
+          d[jj] = (32 * h + jj <= i) ? (d[jj] * wi) * sc.cu[32 * h + jj] : 0.f;
       } else {
         const float gi = sc.g[i];
 #pragma unroll
@@ -388,8 +403,8 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
   }
   if (__syncthreads_or(sc.fail)) goto teardown;  // A and P complete
 
-  // ---- T = (I + A)^{-1} into the T tile (Falcon-1A: the identity, written above) ----
-  if (f1) solve_unit_lower_sw(a_tile, a_diag, t_tile);
+  // ---- T' = (I + A)^{-1} Diag(eta) into the T tile (Falcon-1A: Diag(eta), written above) ----
+  if (f1) solve_unit_lower_sw(a_tile, a_diag, t_tile, base + L::DB, sc.eta);
   fence_async_smem();
   tc_fence_before();
   __syncthreads();

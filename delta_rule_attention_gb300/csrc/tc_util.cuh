@@ -107,6 +107,24 @@ __device__ __forceinline__ void store_half_sw(unsigned char* tile, int r, int h,
         pack8(v + 8 * c, scale);
 }
 
+// Scales, in place, the four chunks of the half row (one chunk at a time).
+__device__ __forceinline__ void scale_half_sw(unsigned char* tile, int r, int h, float scale) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint4* p = reinterpret_cast<uint4*>(tile + r * 128 + (((4 * h + c) ^ (r & 7)) << 4));
+    const uint4 pk = *p;
+    const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&pk);
+    float v[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(hv[e]);
+      v[2 * e] = f.x;
+      v[2 * e + 1] = f.y;
+    }
+    *p = pack8(v, scale);
+  }
+}
+
 __device__ __forceinline__ float sumsq32(const float* v) {
   float p[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -225,11 +243,20 @@ __device__ __forceinline__ uint32_t movm_trans(uint32_t a) {
 
 constexpr int kLdD = 17;  // fp32 row stride of the diagonal blocks of A
 
-// T = (I + A)^{-1} for the strictly lower 64 x 64 A, eight warps, the result
-// written as bf16 into the 128-byte swizzled 64 x 64 tile t_tile (rows of T,
-// the K-major operand image), zero above the diagonal blocks.  Inputs: a_tile,
-// A as bf16 in the same layout, and a_diag, the fp32 diagonal blocks (row i
-// holds A[i][16 (i / 16) + k], k = 0..15, rows of kLdD floats).
+// Byte offset of 16-byte chunk c (0 or 1) of row r in the copy of T's
+// diagonal blocks (32-byte rows, the chunk flipped every four rows so that
+// ldmatrix row reads do not collide in shared-memory banks).
+__device__ __forceinline__ uint32_t dblk_chunk(int r, int c) {
+  return (uint32_t)(r * 32 + ((c ^ ((r >> 2) & 1)) << 4));
+}
+
+// T = (I + A)^{-1} for the strictly lower 64 x 64 A, eight warps.  The result
+// leaves with its columns scaled, T Diag(col_scale), as bf16 in the 128-byte
+// swizzled 64 x 64 tile t_tile (rows, the K-major operand image), zero above
+// the diagonal blocks.  Inputs: a_tile, A as bf16 in the same layout; a_diag,
+// the fp32 diagonal blocks (row i holds A[i][16 (i / 16) + k], k = 0..15, rows
+// of kLdD floats); col_scale, 64 floats.  d_blk (2 KB) receives the unscaled
+// diagonal blocks of T as bf16, which the strips below read.
 //
 // Diagonal block b is inverted in fp32 by forward substitution exactly as in
 // solve_unit_lower.  Below it, T_{b,<b} = T_bb (-A_{b,<b} T_{<b}) splits into
@@ -240,10 +267,11 @@ constexpr int kLdD = 17;  // fp32 row stride of the diagonal blocks of A
 // is transposed across the warp by movmatrix into operand layout, so neither
 // the right-hand side nor the finished blocks go through shared memory and the
 // warps do not wait on one another.  Every operand is rounded to bf16 at the
-// same point as in solve_unit_lower, so the two give the same T.
-// The caller fences and synchronises before T is read.
+// same point as in solve_unit_lower; the column scaling enters only the
+// stored copy.  The caller fences and synchronises before t_tile is read.
 __device__ void solve_unit_lower_sw(const unsigned char* a_tile, const float* a_diag,
-                                    unsigned char* t_tile) {
+                                    unsigned char* t_tile, unsigned char* d_blk,
+                                    const float* col_scale) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   {
     const int b = warp & 3, hh = warp >> 2, rr = lane >> 1, q = lane & 1, row = 16 * b + rr;
@@ -261,10 +289,13 @@ __device__ void solve_unit_lower_sw(const unsigned char* a_tile, const float* a_
         if (rr > k) dv4[jj] -= arow[k] * tkj;
       }
     }
-    // Columns 16b + 8hh + 4q .. +3 of the row; the four threads of a row zero
-    // the chunks right of the diagonal block.
-    *reinterpret_cast<uint2*>(t_tile + sw_chunk(row, 2 * b + hh) + 8 * q) =
+    // Columns 16b + 8hh + 4q .. +3 of the row (unscaled into d_blk, scaled into
+    // t_tile); the four threads of a row zero the chunks right of the block.
+    *reinterpret_cast<uint2*>(d_blk + dblk_chunk(row, hh) + 8 * q) =
         make_uint2(pack_bf16(dv4[0], dv4[1]), pack_bf16(dv4[2], dv4[3]));
+    const float4 cs = *reinterpret_cast<const float4*>(col_scale + 16 * b + 8 * hh + 4 * q);
+    *reinterpret_cast<uint2*>(t_tile + sw_chunk(row, 2 * b + hh) + 8 * q) = make_uint2(
+        pack_bf16(dv4[0] * cs.x, dv4[1] * cs.y), pack_bf16(dv4[2] * cs.z, dv4[3] * cs.w));
     for (int z = 2 * b + 2 + 2 * hh + q; z < 8; z += 4)
       *reinterpret_cast<uint4*>(t_tile + sw_chunk(row, z)) = make_uint4(0u, 0u, 0u, 0u);
   }
@@ -272,11 +303,12 @@ __device__ void solve_unit_lower_sw(const unsigned char* a_tile, const float* a_
   if (warp < 6) {
     const int nt = warp, kb0 = nt >> 1, g = lane >> 2, t = lane & 3;
     const int la = (lane & 7) + 8 * ((lane >> 3) & 1), ca = lane >> 4;
-    const uint32_t abase = smem_addr(a_tile), tbase = smem_addr(t_tile);
-    uint32_t tb[4][2];  // finished blocks (kb, strip) as B fragments
+    const uint32_t abase = smem_addr(a_tile), dbase = smem_addr(d_blk);
+    const float cs0 = col_scale[8 * nt + 2 * t], cs1 = col_scale[8 * nt + 2 * t + 1];
+    uint32_t tb[4][2];  // finished blocks (kb, strip) as B fragments, unscaled
 #pragma unroll
     for (int kb = 0; kb < 3; ++kb)
-      if (kb == kb0) ldsm_x2_trans(tb[kb], tbase + sw_chunk(16 * kb + la, nt));
+      if (kb == kb0) ldsm_x2_trans(tb[kb], dbase + dblk_chunk(16 * kb + la, nt & 1));
 #pragma unroll
     for (int b = 1; b < 4; ++b) {
       if (b <= kb0) continue;
@@ -292,16 +324,17 @@ __device__ void solve_unit_lower_sw(const unsigned char* a_tile, const float* a_
       const uint32_t rb[2] = {movm_trans(pack_bf16(-acc[0], -acc[1])),
                               movm_trans(pack_bf16(-acc[2], -acc[3]))};
       uint32_t fd[4];
-      ldsm_x4(fd, tbase + sw_chunk(16 * b + la, 2 * b + ca));
+      ldsm_x4(fd, dbase + dblk_chunk(16 * b + la, ca));
       float c[4] = {0.f, 0.f, 0.f, 0.f};
       mma16816(c, fd, rb);
-      const uint32_t lo = pack_bf16(c[0], c[1]), hi = pack_bf16(c[2], c[3]);
       const int r0 = 16 * b + g;
-      *reinterpret_cast<uint32_t*>(t_tile + sw_chunk(r0, nt) + 4 * t) = lo;
-      *reinterpret_cast<uint32_t*>(t_tile + sw_chunk(r0 + 8, nt) + 4 * t) = hi;
+      *reinterpret_cast<uint32_t*>(t_tile + sw_chunk(r0, nt) + 4 * t) =
+          pack_bf16(c[0] * cs0, c[1] * cs1);
+      *reinterpret_cast<uint32_t*>(t_tile + sw_chunk(r0 + 8, nt) + 4 * t) =
+          pack_bf16(c[2] * cs0, c[3] * cs1);
       if (b < 3) {
-        tb[b][0] = movm_trans(lo);
-        tb[b][1] = movm_trans(hi);
+        tb[b][0] = movm_trans(pack_bf16(c[0], c[1]));
+        tb[b][1] = movm_trans(pack_bf16(c[2], c[3]));
       }
     }
   }
