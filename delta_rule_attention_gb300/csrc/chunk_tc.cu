@@ -520,17 +520,18 @@ teardown:
 }
 
 // ---------------------------------------------------------------------------
-// Scan kernel, one CTA per head: sixteen math warps and one issue warp.  TMEM
-// lane rules give math warps w with (w & 3) < 2 the state rows (lanes 0..63)
-// and the others the output rows (lanes 64..127); warp w takes columns
-// 16 (w >> 2) .. +15 of its rows.  The state path (MMA -> state update ->
-// next B operand) is the critical chain; the issue warp only waits and issues
-// (the MMA of chunk c, then the refill of the stage chunk c-1 used), the output
-// rows run beside the chain, and the accumulator is double-buffered in TMEM.
-// Every hand-off is one mbarrier arrival per warp.
+// Scan kernel, one CTA per head: sixteen math warps, one issue warp and one
+// refill warp.  TMEM lane rules give math warps w with (w & 3) < 2 the state
+// rows (lanes 0..63) and the others the output rows (lanes 64..127); warp w
+// takes columns 16 (w >> 2) .. +15 of its rows.  The state path (MMA -> state
+// update -> next B operand) is the critical chain; the issue warp only waits
+// and issues the MMA of each chunk, the refill warp puts the map of chunk
+// c + kStages into the stage of chunk c once every math warp is done with it,
+// the output rows run beside the chain, and the accumulator is
+// double-buffered in TMEM.  Every hand-off is one mbarrier arrival per warp.
 constexpr int kStages = 5;
 constexpr int kScanMathWarps = 16;
-constexpr int kScanThreads = 32 * (kScanMathWarps + 1);
+constexpr int kScanThreads = 32 * (kScanMathWarps + 2);
 
 struct ScanSmem {
   unsigned char mc[kStages][kMcBytes];  // A tiles of the state MMA (K-major)
@@ -580,9 +581,10 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   const int64_t bh = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool issuer = warp == kScanMathWarps;
+  const bool refiller = warp == kScanMathWarps + 1;
   const int row = 32 * (warp & 3) + lane;  // TMEM lane = row of [S'; O]
   const int qc = (warp >> 2) & 3;          // column quarter: 16 qc .. 16 qc + 15
-  const bool srow = !issuer && row < 64;
+  const bool srow = warp < kScanMathWarps && row < 64;
   // The two 16-byte chunks of this thread's columns, at their swizzled places.
   const uint32_t ch0 = (uint32_t)(((2 * qc) ^ (row & 7)) << 4);
   const uint32_t ch1 = (uint32_t)(((2 * qc + 1) ^ (row & 7)) << 4);
@@ -635,16 +637,21 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         mma_k64_desc(tmem + 64 * b, sw128_desc(smem_addr(s.mc[st]), 16, 1024), kStepK, bdesc,
                      kStepMN, idesc, false);
         mma_commit(&s.mma_done[b]);
-        // Refill the stage of chunk c - 1 once every math warp is done with it.
-        const int cp = c - 1;
-        if (cp >= 0 && cp + kStages < n) {
-          const int sp = cp % kStages;
-          if (!mbar_wait(&s.empty[sp], (uint32_t)(cp / kStages) & 1u)) {
-            *fail = 1;
-            break;
-          }
-          issue_map_load(s, sp, ws + (size_t)(cp + kStages) * kMapBytes);
+      }
+    }
+    __syncwarp();
+  } else if (refiller) {
+    // The stage of chunk c gets chunk c + kStages once every math warp is done
+    // with it (the MMA of chunk c has then completed too).
+    if (lane == 0) {
+      for (int c = 0; c + kStages < n; ++c) {
+        if (*fail) break;
+        const int st = c % kStages;
+        if (!mbar_wait(&s.empty[st], (uint32_t)(c / kStages) & 1u)) {
+          *fail = 1;
+          break;
         }
+        issue_map_load(s, st, ws + (size_t)(c + kStages) * kMapBytes);
       }
     }
     __syncwarp();
@@ -760,10 +767,13 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 // (the 64 output rows, then 64 rows past the map that land in unused
 // accumulator lanes).  Warps 0..15 own the state rows (lane quarter w & 3,
 // columns 16 (w >> 2) .. +15), warps 16, 17, 20, 21 the output rows (lane
-// quarters 0 and 1, column halves), warp 18 issues MMAs and refills, warp 19
-// has no work.
+// quarters 0 and 1, column halves).  Warp 18 issues the MMAs: per chunk the
+// state MMA (committed on its own barrier, so the state chain does not wait
+// for the output rows), then the output MMA, which runs on the tensor pipe
+// while the state warps update S.  Warp 19 refills the map ring, so the
+// issuing thread waits only for what the next MMA reads.
 // The Mc atoms go through a three-stage shared-memory ring; Nc rows are read
-// from global memory (brought into L2 ahead by the issue warp) one chunk ahead
+// from global memory (brought into L2 ahead by the refill warp) one chunk ahead
 // into registers, which keeps three map stages within shared memory.
 constexpr int kStages128 = 3;
 constexpr int kScan128Threads = 32 * 22;
@@ -816,6 +826,7 @@ __global__ void __launch_bounds__(kScan128Threads)
   const int j = blockIdx.x & 1;  // d_v slice
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool issuer = warp == 18;
+  const bool refiller = warp == 19;
   const bool swarp = warp < 16;
   const bool owarp = warp == 16 || warp == 17 || warp == 20 || warp == 21;
   const int row = 32 * (warp & 3) + lane;  // TMEM lane
@@ -857,6 +868,8 @@ __global__ void __launch_bounds__(kScan128Threads)
       const uint32_t idesc = idesc_bf16(128, 64, false, true);
       for (int c = 0; c < n; ++c) {
         const int st = c % kStages128, b = c & 1;
+        // Accumulator buffer b free (output rows of chunk c - 2 read), the map
+        // in its stage; the state operand is the last to be ready: wait for it last.
         bool ok = c < 2 || mbar_wait(&s.o_done[b], (uint32_t)((c - 2) >> 1) & 1u);
         ok = ok && mbar_wait(&s.full[st], (uint32_t)(c / kStages128) & 1u);
         ok = ok && mbar_wait(&s.s_ready, (uint32_t)c & 1u);
@@ -865,28 +878,34 @@ __global__ void __launch_bounds__(kScan128Threads)
           break;
         }
         tc_fence_after();
-        // State rows (committed on their own: the state chain waits only for
-        // them), then output rows; K = 128 as two 64-wide atoms.
+        // State rows, K = 128 as two 64-wide atoms.
         const uint64_t ad = sw128_desc(smem_addr(s.stage[st]), 16, 1024);
         const uint64_t bdesc0 = sw128_desc(smem_addr(s.sop[c & 1]), 8192, 1024);
         const uint64_t bdesc1 = bdesc0 + (8192 >> 4);  // state rows 64..127
         mma_k64_desc(tmem + 128 * b, ad, kStepK, bdesc0, kStepMN, idesc, false);
         mma_k64_desc(tmem + 128 * b, ad + (kA >> 4), kStepK, bdesc1, kStepMN, idesc, true);
         mma_commit(&s.mma_done[b]);
+        // Output rows (Mc rows 128..255), same operand.
         mma_k64_desc(tmem + 128 * b + 64, ad + (16384 >> 4), kStepK, bdesc0, kStepMN, idesc,
                      false);
         mma_k64_desc(tmem + 128 * b + 64, ad + ((kA + 16384) >> 4), kStepK, bdesc1, kStepMN,
                      idesc, true);
         mma_commit(&s.omma_done[b]);
-        const int cp = c - 1;
-        if (cp >= 0 && cp + kStages128 < n) {
-          const int sp = cp % kStages128;
-          if (!mbar_wait(&s.empty[sp], (uint32_t)(cp / kStages128) & 1u)) {
-            *fail = 1;
-            break;
-          }
-          issue_map_load128(s, sp, ws + (size_t)(cp + kStages128) * kMap, j);
+      }
+    }
+    __syncwarp();
+  } else if (refiller) {
+    // The stage of chunk c gets chunk c + kStages128 once every math warp is
+    // done with it (both MMAs of chunk c have then completed too).
+    if (lane == 0) {
+      for (int c = 0; c + kStages128 < n; ++c) {
+        if (*fail) break;
+        const int st = c % kStages128;
+        if (!mbar_wait(&s.empty[st], (uint32_t)(c / kStages128) & 1u)) {
+          *fail = 1;
+          break;
         }
+        issue_map_load128(s, st, ws + (size_t)(c + kStages128) * kMap, j);
       }
     }
     __syncwarp();
@@ -899,37 +918,40 @@ __global__ void __launch_bounds__(kScan128Threads)
     fence_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&s.s_ready);
-    // Nc rows of this thread (state rows 0..127 of slice j), chunk 0 first.
+    // Nc rows of this thread (state rows 0..127 of slice j), one chunk ahead
+    // of their use.  The loop runs two chunks per pass so that the rows of the
+    // next chunk land in the other register pair, with no copy that would
+    // wait for the load on the chain.
     const unsigned char* ncg = ws + (2 + j) * kA + row * 128;
-    uint4 n0 = ld_map16(ncg + ch0), n1 = ld_map16(ncg + ch1);
-    for (int c = 0; c < n; ++c) {
-      if (__any_sync(0xffffffffu, *fail)) break;
+    uint4 na0 = ld_map16(ncg + ch0), na1 = ld_map16(ncg + ch1);
+    uint4 nb0 = make_uint4(0u, 0u, 0u, 0u), nb1 = nb0;
+    // One chunk: uses (cur0, cur1), loads chunk c + 1 into (nxt0, nxt1).
+    auto chunk_step = [&](int c, const uint4& cur0, const uint4& cur1, uint4& nxt0,
+                          uint4& nxt1) -> bool {
+      if (__any_sync(0xffffffffu, *fail)) return false;
       const int st = c % kStages128, b = c & 1;
       // mma_done of chunk c also covers the MMAs of chunk c - 1 (issued
-      // earlier), the last readers of sop[(c + 1) & 1].
+      // earlier by the same thread), the last readers of sop[(c + 1) & 1].
       unsigned char* sop_next = s.sop[(c + 1) & 1];
       if (!__all_sync(0xffffffffu, mbar_wait(&s.full[st], (uint32_t)(c / kStages128) & 1u))) {
         *fail = 1;
-        break;
+        return false;
       }
       const float gC = *reinterpret_cast<const float*>(s.stage[st] + 2 * kA);
-      uint4 m0 = make_uint4(0u, 0u, 0u, 0u), m1 = m0;  // Nc of chunk c + 1
       if (c + 1 < n) {
         const unsigned char* nrow = ncg + (size_t)(c + 1) * kMap;
-        m0 = ld_map16(nrow + ch0);
-        m1 = ld_map16(nrow + ch1);
+        nxt0 = ld_map16(nrow + ch0);
+        nxt1 = ld_map16(nrow + ch1);
       }
       if (!__all_sync(0xffffffffu, mbar_wait(&s.mma_done[b], (uint32_t)(c >> 1) & 1u))) {
         *fail = 1;
-        break;
+        return false;
       }
       tc_fence_after();
       float d[16];
       tmem_ld16(tlane + 128 * b, d);
       tc_fence_before();
-      add_bf16x16(d, n0, n1);
-      n0 = m0;
-      n1 = m1;
+      add_bf16x16(d, cur0, cur1);
 #pragma unroll
       for (int i = 0; i < 16; ++i) S[i] = gC * S[i] + d[i];
       *reinterpret_cast<uint4*>(sop_next + row * 128 + ch0) = pack8(S, 1.f);
@@ -940,6 +962,11 @@ __global__ void __launch_bounds__(kScan128Threads)
         mbar_arrive(&s.s_ready);
         mbar_arrive(&s.empty[st]);
       }
+      return true;
+    };
+    for (int c = 0; c < n; c += 2) {
+      if (!chunk_step(c, na0, na1, nb0, nb1)) break;
+      if (c + 1 < n && !chunk_step(c + 1, nb0, nb1, na0, na1)) break;
     }
     if (!*fail) {
       float* dst = a.S_out + (bh * 128 + row) * 128 + 64 * j + 16 * qc;
@@ -955,46 +982,48 @@ __global__ void __launch_bounds__(kScan128Threads)
     const bool o_issuer = warp == 16 && lane == 0;
     // Nc rows 128 + row (the output rows of slice j), one chunk ahead.
     const unsigned char* ncg = ws + (2 + j) * kA + (128 + row) * 128;
-    uint4 nq[4], mq[4];
+    // Two chunks per pass, so the rows of the next chunk land in the other
+    // register set with no copy that would wait for the load.
+    uint4 na[4], nb[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) nq[q] = ld_map16(ncg + (((4 * oh + q) ^ (row & 7)) << 4));
-    for (int c = 0; c < n; ++c) {
+    for (int q = 0; q < 4; ++q) {
+      na[q] = ld_map16(ncg + (((4 * oh + q) ^ (row & 7)) << 4));
+      nb[q] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    // One chunk: uses cur, loads the rows of chunk c + 1 into nxt.
+    auto out_step = [&](int c, const uint4 (&cur)[4], uint4 (&nxt)[4]) -> bool {
       const int st = c % kStages128, b = c & 1;
+      if (c + 1 < n) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        mq[q] = (c + 1 < n)
-                    ? ld_map16(ncg + (size_t)(c + 1) * kMap + (((4 * oh + q) ^ (row & 7)) << 4))
-                    : make_uint4(0u, 0u, 0u, 0u);
+        for (int q = 0; q < 4; ++q)
+          nxt[q] = ld_map16(ncg + (size_t)(c + 1) * kMap + (((4 * oh + q) ^ (row & 7)) << 4));
+      }
       bool ok = !*fail && mbar_wait(&s.full[st], (uint32_t)(c / kStages128) & 1u);
       ok = ok && mbar_wait(&s.omma_done[b], (uint32_t)(c >> 1) & 1u);
       if (o_issuer) bulk_wait_read<1>();
       if (named_sync_or(1, 32 * kOutWarps, !ok)) {
         *fail = 1;
-        break;
+        return false;
       }
       tc_fence_after();
       float d[32];
       tmem_ld32(tlane + 128 * b, d);
       tc_fence_before();
-      {
-        // + Nc rows 128.. (output rows), this thread's four 16-byte chunks
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint4 pk = nq[q];
-          nq[q] = mq[q];
-          const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&pk);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = __bfloat1622float2(hv[e]);
-            d[8 * q + 2 * e] += f.x;
-            d[8 * q + 2 * e + 1] += f.y;
-          }
-        }
-      }
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&s.o_done[b]);
-        mbar_arrive(&s.empty[st]);
+        mbar_arrive(&s.o_done[b]);  // accumulator b is read
+        mbar_arrive(&s.empty[st]);  // the MMAs of chunk c have read its stage
+      }
+      // + Nc rows 128.. (output rows), this thread's four 16-byte chunks
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&cur[q]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(hv[e]);
+          d[8 * q + 2 * e] += f.x;
+          d[8 * q + 2 * e + 1] += f.y;
+        }
       }
       unsigned char* orow = s.ostage[b] + row * 128;
 #pragma unroll
@@ -1006,6 +1035,11 @@ __global__ void __launch_bounds__(kScan128Threads)
         tma_store_3d(&tm_o, s.ostage[b], 64 * j, (c_begin + c) * kC, (int)bh);
         bulk_commit();
       }
+      return true;
+    };
+    for (int c = 0; c < n; c += 2) {
+      if (!out_step(c, na, nb)) break;
+      if (c + 1 < n && !out_step(c + 1, nb, na)) break;
     }
     if (o_issuer) bulk_wait<0>();
   }
