@@ -182,6 +182,10 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
   const bool patch = c == 0 && a.x_prev != nullptr;
 
   if (warp == 0) tmem_alloc(&sc.tmem_base, L::kTmemCols);
+  // Launched behind the previous call's scan (programmatic dependent launch),
+  // the CTA may start while that grid still runs: no input is read, and no
+  // output or workspace byte written, before the preceding grid has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (tid == 0) {
     mbar_init(&sc.bar_in, 1);
     mbar_init(&sc.bar_mma, 1);
@@ -590,6 +594,9 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   const uint32_t ch1 = (uint32_t)(((2 * qc + 1) ^ (row & 7)) << 4);
   const unsigned char* ws = reinterpret_cast<const unsigned char*>(a.workspace) +
                             ((size_t)bh * nchunks + c_begin) * kMapBytes;  // this range's maps
+  // A following map launch may start now; it waits for this grid to complete
+  // before it touches memory.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (warp == 0) tmem_alloc(&s.tmem_base, 128);
   if (tid == 0) {
     for (int st = 0; st < kStages; ++st) {
@@ -832,6 +839,9 @@ __global__ void __launch_bounds__(kScan128Threads)
   const int row = 32 * (warp & 3) + lane;  // TMEM lane
   const unsigned char* ws = reinterpret_cast<const unsigned char*>(a.workspace) +
                             ((size_t)bh * nchunks + c_begin) * kMap;  // this range's maps
+  // A following map launch may start now; it waits for this grid to complete
+  // before it touches memory.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (warp == 0) tmem_alloc(&s.tmem_base, 256);
   if (tid == 0) {
     for (int st = 0; st < kStages128; ++st) {
@@ -1065,17 +1075,28 @@ size_t tc_workspace_bytes(int m, int64_t BH, int64_t T) {
 
 namespace {
 
+// pdl: programmatic dependent launch behind the preceding kernel on the stream
+// (the map kernel waits for it with griddepcontrol.wait before reading inputs).
 template <int M>
 cudaError_t launch_map(const ChunkArgs& a, int nchunks, int c_begin, int n, int* err,
                        const CUtensorMap& tm_k, const CUtensorMap& tm_q, const CUtensorMap& tm_v,
-                       cudaStream_t stream) {
+                       bool pdl, cudaStream_t stream) {
   const size_t smem = map_smem_bytes<M>() + 1024;
   cudaError_t e = cudaFuncSetAttribute(tc_chunk_map_kernel<M>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  tc_chunk_map_kernel<M><<<dim3(n * MapLayout<M>::kHalves, (unsigned)a.BH), kMapThreads, smem,
-                           stream>>>(a, nchunks, c_begin, err, tm_k, tm_q, tm_v);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n * MapLayout<M>::kHalves, (unsigned)a.BH);
+  cfg.blockDim = dim3(kMapThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, tc_chunk_map_kernel<M>, a, nchunks, c_begin, err, tm_k, tm_q,
+                            tm_v);
 }
 
 // pdl: programmatic dependent launch after the preceding map launch on the
@@ -1182,7 +1203,7 @@ cudaError_t launch_tc(const ChunkArgs& a, int* err, cudaStream_t stream) {
     return cudaErrorInvalidValue;
   const int pieces = piece_count(a.BH, nchunks, M == 128);
   if (pieces == 1) {
-    cudaError_t e = launch_map<M>(a, nchunks, 0, nchunks, err, tm_k, tm_q, tm_v, stream);
+    cudaError_t e = launch_map<M>(a, nchunks, 0, nchunks, err, tm_k, tm_q, tm_v, true, stream);
     if (e != cudaSuccess) return e;
     return launch_scan_range<M>(a, nchunks, 0, nchunks, a.S0, true, err, tm_o, stream);
   }
@@ -1196,7 +1217,8 @@ cudaError_t launch_tc(const ChunkArgs& a, int* err, cudaStream_t stream) {
   for (int p = 0; p < pieces; ++p) {
     const int c0 = (int)((int64_t)nchunks * p / pieces);
     const int c1 = (int)((int64_t)nchunks * (p + 1) / pieces);
-    if ((e = launch_map<M>(a, nchunks, c0, c1 - c0, err, tm_k, tm_q, tm_v, stream)) != cudaSuccess)
+    if ((e = launch_map<M>(a, nchunks, c0, c1 - c0, err, tm_k, tm_q, tm_v, false, stream)) !=
+        cudaSuccess)
       return e;
     if ((e = cudaEventRecord(ps->map_done[p], stream)) != cudaSuccess) return e;
     if ((e = cudaStreamWaitEvent(ps->side, ps->map_done[p], 0)) != cudaSuccess) return e;
