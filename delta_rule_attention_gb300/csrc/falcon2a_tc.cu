@@ -96,6 +96,9 @@ __global__ void __launch_bounds__(k2Threads, 2)
   const int n = (int)min((int64_t)k2C, T - t0);
 
   if (warp == 0) tmem_alloc(&sc.tmem_base, 256);
+  // Launched behind the previous call's scan (programmatic dependent launch):
+  // nothing is read or written before the preceding grid has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (tid == 0) {
     mbar_init(&sc.bar_in, 1);
     mbar_init(&sc.bar_mma, 1);
@@ -377,6 +380,9 @@ __global__ void __launch_bounds__(k2Threads, 1)
   const int row = 32 * (warp & 3) + lane, h = warp >> 2;
   const unsigned char* hmaps = reinterpret_cast<const unsigned char*>(a.workspace) +
                                (size_t)bh * nchunks * kMap2ABytes;
+  // A following map launch may start now; it waits for this grid to complete
+  // before it touches memory.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (warp == 0) tmem_alloc(&s.tmem_base, 64);
   if (tid == 0) {
     for (int st = 0; st < kS2Stages; ++st) mbar_init(&s.full[st], 1);
@@ -477,9 +483,22 @@ cudaError_t launch_tc_falcon2a(const ChunkArgs& a, int* err, cudaStream_t stream
   cudaError_t e = cudaFuncSetAttribute(tc_falcon2a_map_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kF2Smem);
   if (e != cudaSuccess) return e;
-  tc_falcon2a_map_kernel<<<dim3(nchunks, (unsigned)a.BH), k2Threads, kF2Smem, stream>>>(
-      a, nchunks, err, tm_k, tm_q, tm_v);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // Both launches are programmatic dependent launches: the maps behind the
+  // preceding kernel, the scan behind the maps; each waits (griddepcontrol.wait)
+  // for its predecessor before touching memory.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t mcfg = {};
+  mcfg.gridDim = dim3(nchunks, (unsigned)a.BH);
+  mcfg.blockDim = dim3(k2Threads);
+  mcfg.dynamicSmemBytes = kF2Smem;
+  mcfg.stream = stream;
+  mcfg.attrs = attr;
+  mcfg.numAttrs = 1;
+  if ((e = cudaLaunchKernelEx(&mcfg, tc_falcon2a_map_kernel, a, nchunks, err, tm_k, tm_q, tm_v)) !=
+      cudaSuccess)
+    return e;
   const size_t smem = sizeof(S2Smem) + 1024;
   e = cudaFuncSetAttribute(tc_falcon2a_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem);
@@ -489,9 +508,6 @@ cudaError_t launch_tc_falcon2a(const ChunkArgs& a, int* err, cudaStream_t stream
   cfg.blockDim = dim3(k2Threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, tc_falcon2a_scan_kernel, a, nchunks, err, tm_o);

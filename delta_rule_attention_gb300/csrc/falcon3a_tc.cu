@@ -96,6 +96,9 @@ __global__ void __launch_bounds__(k3Threads, 2)
   const int n = (int)min((int64_t)k3C, T - t0);
 
   if (warp == 0) tmem_alloc(&sc.tmem_base, 256);
+  // Launched behind the previous call's scan (programmatic dependent launch):
+  // nothing is read or written before the preceding grid has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (tid == 0) {
     mbar_init(&sc.bar_in, 1);
     mbar_init(&sc.bar_mma, 1);
@@ -321,9 +324,19 @@ cudaError_t launch_tc_falcon3a(const ChunkArgs& a, int window, int* err, cudaStr
   cudaError_t e = cudaFuncSetAttribute(tc_falcon3a_map_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kF3Smem);
   if (e != cudaSuccess) return e;
-  tc_falcon3a_map_kernel<<<dim3(nchunks, (unsigned)a.BH), k3Threads, kF3Smem, stream>>>(
-      a, window, nchunks, err, tm_k, tm_q, tm_v);
-  e = cudaGetLastError();
+  // Programmatic dependent launch behind the preceding kernel (the map kernel
+  // waits for it with griddepcontrol.wait before touching memory).
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(nchunks, (unsigned)a.BH);
+  cfg.blockDim = dim3(k3Threads);
+  cfg.dynamicSmemBytes = kF3Smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, tc_falcon3a_map_kernel, a, window, nchunks, err, tm_k, tm_q, tm_v);
   if (e != cudaSuccess) return e;
   return launch_tc_scan64(a, err, stream);
 }
