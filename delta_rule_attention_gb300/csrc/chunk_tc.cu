@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
   if (__syncthreads_or(sc.fail)) goto teardown;  // A and P complete
 
   // ---- T' = (I + A)^{-1} Diag(eta) into the T tile (Falcon-1A: Diag(eta), written above) ----
-  if (f1) solve_unit_lower_sw(a_tile, a_diag, t_tile, base + L::DB, sc.eta);
+  if (f1) solve_unit_lower_sw<true>(a_tile, a_diag, t_tile, base + L::DB, sc.eta);
   fence_async_smem();
   tc_fence_before();
   __syncthreads();

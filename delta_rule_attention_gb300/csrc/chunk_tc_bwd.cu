@@ -19,7 +19,8 @@
 // an operand are stacked into one M = 128 MMA (the unused half of an M = 128
 // operand reads a neighbouring tile and lands in accumulator lanes nobody
 // reads).  Transposed operands are the same row-major tiles read MN-major.
-// The unit-lower inverse T is the forward's fp32 solve.  Epilogues run one
+// The unit-lower inverse T is the forward map kernel's solve (fp32 diagonal
+// blocks, register-resident 8-column strips below them).  Epilogues run one
 // accumulator row per thread (two threads per row, one per column half), so
 // the per-row reductions of the step-size chain stay local; column sums go
 // through shared-memory atomics.  Falcon-1A takes the same path with T = I
@@ -54,9 +55,9 @@ constexpr uint32_t kTile = 8192;  // 64 rows x 64 bf16, 128B-swizzled
 //   0 X  1 Q  2 S  3 dS'  (the whole kernel)   6 dO (-> [dR; dO] U^T)
 //   4 V (-> rv) | dPE                          5 dR (before dO: [dR; dO])
 //   7 T (solve -> T^T dU) | dOs = Diag(e^g) dO
-//   8 Xlo | A (fp32) | R | dU | dK             9 Qlo | A | U
-//   10 Slo | T (fp32) | Us = Diag(e^{g_C-g}) U 11 dSlo | T (fp32) | P | dUlo
-//   12 T (fp32), solve scratch | Plo | dRs = -Diag(eta e^{g_-}) dR
+//   8 Xlo | A (bf16) | R | dU | dK              9 Qlo | A's diagonal blocks (fp32) | U
+//   10 Slo | T's diagonal blocks (solve) | Us = Diag(e^{g_C-g}) U
+//   11 dSlo | P | dUlo                          12 Plo | dRs = -Diag(eta e^{g_-}) dR
 // The unused half of an M = 128 K-major operand reads the next slot (slot 13
 // is the scalars: valid memory), that of an MN-major operand the slot LBO
 // bytes on.  With 113 KB of shared memory and 256 TMEM columns two CTAs share
@@ -65,11 +66,8 @@ enum : int { kX = 0, kQt, kS, kdS, kV, kdR, kdO, kT, kW8, kW9, kW10, kW11, kW12,
 constexpr int kdPE = kV, kdOs = kT, kXlo = kW8, kSlo = kW10, kdSlo = kW11;  // Qlo = slot 9
 constexpr int kR = kW8, kdU = kW8, kdK = kW8, kU = kW9, kUs = kW10, kP = kW11, kdUlo = kW11;
 constexpr int kPlo = kW12, kdRs = kW12;
-constexpr uint32_t kAfOff = kW8 * kTile;               // A (fp32, rows of kLdA)
-constexpr uint32_t kTfOff = kAfOff + 64 * kLdA * 4;    // T (fp32, rows of kLdT)
-constexpr uint32_t kRsOff = kTfOff + 64 * kLdT * 4;    // solve scratch (16 x kLdR)
 constexpr uint32_t kScOff = kSlots * kTile;
-static_assert(kRsOff + 16 * kLdR * 4 <= kScOff, "solve buffers within slots 8..12");
+static_assert(64 * kLdD * 4 <= kTile, "A's diagonal blocks within one slot");
 
 struct BwdScalars {
   float eta[64], g[64], gx[64], E[64], lame[64], den[64], gam[64];
@@ -227,9 +225,6 @@ __global__ void __launch_bounds__(kBThreads, 2)
   const ChunkArgs& a = b.f;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base = align1024(smem_raw);
-  float* Af = reinterpret_cast<float*>(base + kAfOff);
-  float* Tf = reinterpret_cast<float*>(base + kTfOff);
-  float* Rs = reinterpret_cast<float*>(base + kRsOff);
   BwdScalars& sc = *reinterpret_cast<BwdScalars*>(base + kScOff);
   auto tile = [&](int i) { return base + i * kTile; };
   auto taddr = [&](int i) { return smem_addr(base + i * kTile); };
@@ -392,7 +387,8 @@ __global__ void __launch_bounds__(kBThreads, 2)
   }
   if (tid < 64 && factored) sc.fc[tid] = __expf(rr - sc.g[tid]);
   if (!wait_mma(sc, phase)) goto teardown;
-  // A (fp32, for the solve; over the dead low parts), qz_i = <dO_i, (Q S)_i>
+  // A (for the solve, over the dead low parts: bf16 in slot 8, its fp32
+  // diagonal blocks in slot 9), qz_i = <dO_i, (Q S)_i>
   {
     float d[32], w[32];
     if (r < 64) {
@@ -403,13 +399,24 @@ __global__ void __launch_bounds__(kBThreads, 2)
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) {
           const int j = 32 * h + jj;
-          Af[i * kLdA + j] = (f1 && j < i) ? ea * sc.fc[j] * d[jj] : 0.f;
+          d[jj] = (f1 && j < i) ? ea * sc.fc[j] * d[jj] : 0.f;
         }
       } else {
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) {
           const int j = 32 * h + jj;
-          Af[i * kLdA + j] = (f1 && j < i) ? ei * expn(gxi - sc.g[j]) * d[jj] : 0.f;
+          d[jj] = (f1 && j < i) ? ei * expn(gxi - sc.g[j]) * d[jj] : 0.f;
+        }
+      }
+      store_half_sw(tile(kW8), i, h, d, 1.f);
+      if (h == (i >> 5)) {  // columns 16 (i / 16) .. +15 lie in this half
+        float* drow = reinterpret_cast<float*>(tile(kW9)) + i * kLdD;
+        if (i & 16) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) drow[k] = d[16 + k];
+        } else {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) drow[k] = d[k];
         }
       }
     } else {
@@ -422,23 +429,20 @@ __global__ void __launch_bounds__(kBThreads, 2)
     }
   }
   __syncthreads();
-  // ---- T = (I + A)^{-1} (T = I for Falcon-1A)
+  // ---- T = (I + A)^{-1} as a bf16 tile (T = I for Falcon-1A)
   if (f1) {
-    solve_unit_lower(Af, Tf, Rs);
-  } else {
-    for (int idx = tid; idx < 64 * 64; idx += kBThreads)
-      Tf[(idx >> 6) * kLdT + (idx & 63)] = ((idx >> 6) == (idx & 63)) ? 1.f : 0.f;
+    solve_unit_lower_sw<false>(tile(kW8), reinterpret_cast<const float*>(tile(kW9)), tile(kT),
+                               tile(kW10), nullptr);
+  } else if (r < 64) {
+    float v[32];
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) v[jj] = (32 * h + jj == i) ? 1.f : 0.f;
+    store_half_sw(tile(kT), i, h, v, 1.f);
   }
   __syncthreads();
-  // T as a bf16 tile; R = Diag(eta) (V - Diag(e^{g_-}) X S) (over A, now dead)
+  // R = Diag(eta) (V - Diag(e^{g_-}) X S) (over A, now dead)
   if (r < 64) {
     float v[32], w[32];
-#pragma unroll
-    for (int jj = 0; jj < 32; ++jj) {
-      const int j = 32 * h + jj;
-      v[jj] = (j <= i) ? Tf[i * kLdT + j] : 0.f;
-    }
-    store_half_sw(tile(kT), i, h, v, 1.f);
     tmem_ld32(tl + kD2a, v);
     load_half_sw(tile(kV), i, h, w);
     const float bx = f1 ? __expf(sc.gx[i]) : 0.f;

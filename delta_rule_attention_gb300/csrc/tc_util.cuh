@@ -1,7 +1,7 @@
 // Building blocks shared by the tensor-core kernels (forward map kernel and
 // the backward chunk kernel): bf16 packing, the 128-byte swizzled half-row
-// accessors of 64-wide tiles, phi's scale, and the fp32 unit-lower inverse
-// of a 64 x 64 chunk matrix with warp MMAs.
+// accessors of 64-wide tiles, phi's scale, and the unit-lower inverse of a
+// 64 x 64 chunk matrix (fp32 diagonal blocks, warp MMAs below them).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -20,10 +20,6 @@ using namespace tc;
 constexpr uint32_t kMcBytes = 128 * 128;  // 128 rows x 64 bf16 (swizzled operand image)
 constexpr uint32_t kNcBytes = 128 * 128;  // 128 rows x 64 bf16 (rows swizzled by 16 B)
 constexpr uint32_t kMapBytes = kMcBytes + kNcBytes + 128;  // + e^{g_C} (padded)
-
-constexpr int kLdA = 68;  // fp32 row stride of A (16-byte aligned rows)
-constexpr int kLdT = 65;  // fp32 row stride of T during the solve
-constexpr int kLdR = 49;  // fp32 row stride of the block right-hand sides
 
 // 1024-byte aligned base inside the dynamic shared buffer.  The offset is added
 // to the __shared__ pointer itself (not via an integer round trip), so the
@@ -61,25 +57,6 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4],
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
-
-// A fragment (rows r0..r0+15, cols k0..k0+15) of a row-major fp32 matrix.
-__device__ __forceinline__ void frag_a(uint32_t (&a)[4], const float* M, int ld, int r0, int k0) {
-  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  const float* p0 = M + (r0 + g) * ld + k0 + 2 * t;
-  const float* p1 = p0 + 8 * ld;
-  a[0] = pack_bf16(p0[0], p0[1]);
-  a[1] = pack_bf16(p1[0], p1[1]);
-  a[2] = pack_bf16(p0[8], p0[9]);
-  a[3] = pack_bf16(p1[8], p1[9]);
-}
-
-// B fragment (K rows k0..k0+15, N cols n0..n0+7) of a row-major fp32 K x N matrix.
-__device__ __forceinline__ void frag_b(uint32_t (&b)[2], const float* M, int ld, int k0, int n0) {
-  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  const float* p = M + (k0 + 2 * t) * ld + n0 + g;
-  b[0] = pack_bf16(p[0], p[ld]);
-  b[1] = pack_bf16(p[8 * ld], p[9 * ld]);
 }
 
 // Half-row helpers: a thread owns columns 32h .. 32h+31 of row r (four
@@ -142,72 +119,7 @@ __device__ __forceinline__ float phi_scale(float ss, int m, int phi) {
   return ss > 0.f ? rsqrtf(fmaxf(ss, 1e-24f)) : 0.f;
 }
 
-// T = (I + A)^{-1} for the strictly lower 64 x 64 A (rows of kLdA floats),
-// eight warps.  Diagonal block b = warp & 3 is inverted in fp32 by forward
-// substitution: warp w owns columns 8 (w >> 2) .. +7 of the block, two lanes
-// per row with four columns each, and broadcasts finished rows by shuffles;
-// the result stays as the diagonal block of T.  Block rows b = 1..3 then
-// follow T_{b,<b} = T_bb (-A_{b,<b} T_{<b}) with warp MMAs, one n-tile per warp.
-__device__ void solve_unit_lower(const float* As, float* Ts, float* Rs) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  {
-    const int b = warp & 3, hh = warp >> 2, rr = lane >> 1, q = lane & 1, row = 16 * b + rr;
-    float arow[15];
-#pragma unroll
-    for (int k = 0; k < 15; ++k) arow[k] = As[row * kLdA + 16 * b + k];
-    float dv4[4];
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) dv4[jj] = (8 * hh + 4 * q + jj == rr) ? 1.f : 0.f;
-#pragma unroll
-    for (int k = 0; k < 15; ++k) {
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const float tkj = __shfl_sync(0xffffffffu, dv4[jj], 2 * k + q);
-        if (rr > k) dv4[jj] -= arow[k] * tkj;
-      }
-    }
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) Ts[row * kLdT + 16 * b + 8 * hh + 4 * q + jj] = dv4[jj];
-  }
-  __syncthreads();
-  const int g = lane >> 2, t = lane & 3;
-  for (int b = 1; b < 4; ++b) {
-    const int w = 16 * b;  // columns left of block b: 2b n-tiles of 8
-    const int nt = warp;
-    // R = -A[w:w+16, 0:w] T[0:w, 0:w]; T[k][n] = 0 for k < n, so those k-steps are skipped.
-    if (nt < 2 * b) {
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int kb = nt >> 1; kb < b; ++kb) {
-        uint32_t fa[4], fb[2];
-        frag_a(fa, As, kLdA, w, 16 * kb);
-        frag_b(fb, Ts, kLdT, 16 * kb, 8 * nt);
-        mma16816(d, fa, fb);
-      }
-      float* r0 = Rs + g * kLdR + 8 * nt + 2 * t;
-      r0[0] = -d[0];
-      r0[1] = -d[1];
-      r0[8 * kLdR] = -d[2];
-      r0[8 * kLdR + 1] = -d[3];
-    }
-    __syncthreads();
-    // T[w:w+16, 0:w] = T_bb R  (T_bb: diagonal block b of T)
-    if (nt < 2 * b) {
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t fa[4], fb[2];
-      frag_a(fa, Ts, kLdT, w, w);
-      frag_b(fb, Rs, kLdR, 0, 8 * nt);
-      mma16816(d, fa, fb);
-      float* t0 = Ts + (w + g) * kLdT + 8 * nt + 2 * t;
-      t0[0] = d[0];
-      t0[1] = d[1];
-      t0[8 * kLdT] = d[2];
-      t0[8 * kLdT + 1] = d[3];
-    }
-    __syncthreads();
-  }
-}
-
-// ---- the same inverse with its off-diagonal blocks in registers ----------
+// ---- T = (I + A)^{-1} for a 64 x 64 chunk, off-diagonal blocks in registers ----
 // Byte offset of 16-byte chunk c of row r in a 64-wide bf16 tile with the
 // 128-byte swizzle.
 __device__ __forceinline__ uint32_t sw_chunk(int r, int c) {
@@ -255,20 +167,25 @@ __device__ __forceinline__ uint32_t dblk_chunk(int r, int c) {
 // swizzled 64 x 64 tile t_tile (rows, the K-major operand image), zero above
 // the diagonal blocks.  Inputs: a_tile, A as bf16 in the same layout; a_diag,
 // the fp32 diagonal blocks (row i holds A[i][16 (i / 16) + k], k = 0..15, rows
-// of kLdD floats); col_scale, 64 floats.  d_blk (2 KB) receives the unscaled
-// diagonal blocks of T as bf16, which the strips below read.
+// of kLdD floats); col_scale, 64 floats (kScaled; otherwise T itself is
+// stored).  d_blk (2 KB) receives the unscaled diagonal blocks of T as bf16,
+// which the strips below read.
 //
-// Diagonal block b is inverted in fp32 by forward substitution exactly as in
-// solve_unit_lower.  Below it, T_{b,<b} = T_bb (-A_{b,<b} T_{<b}) splits into
-// independent 8-column strips: strip n (columns 8n .. 8n+7, n = 0..5) of
-// block row b needs only strip n of the block rows above it.  Warp n runs its
+// Diagonal block b = warp & 3 is inverted in fp32 by forward substitution:
+// warp w owns columns 8 (w >> 2) .. +7 of the block, two lanes per row with
+// four columns each, and broadcasts finished rows by shuffles.  Below it,
+// T_{b,<b} = T_bb (-A_{b,<b} T_{<b}) splits into independent 8-column strips:
+// strip n (columns 8n .. 8n+7, n = 0..5) of block row b needs only strip n of
+// the block rows above it.  Warp n runs its
 // strip down the block rows with warp MMAs, keeping each finished block as
 // the next MMA's B operand in registers: an accumulator tile, packed to bf16,
 // is transposed across the warp by movmatrix into operand layout, so neither
 // the right-hand side nor the finished blocks go through shared memory and the
-// warps do not wait on one another.  Every operand is rounded to bf16 at the
-// same point as in solve_unit_lower; the column scaling enters only the
-// stored copy.  The caller fences and synchronises before t_tile is read.
+// warps do not wait on one another.  The MMA operands (A, the diagonal
+// blocks, the right-hand sides and the finished blocks) are bf16, the
+// accumulation fp32; the column scaling enters only the stored copy.  The
+// caller fences and synchronises before t_tile is read.
+template <bool kScaled>
 __device__ void solve_unit_lower_sw(const unsigned char* a_tile, const float* a_diag,
                                     unsigned char* t_tile, unsigned char* d_blk,
                                     const float* col_scale) {
@@ -293,7 +210,9 @@ __device__ void solve_unit_lower_sw(const unsigned char* a_tile, const float* a_
     // t_tile); the four threads of a row zero the chunks right of the block.
     *reinterpret_cast<uint2*>(d_blk + dblk_chunk(row, hh) + 8 * q) =
         make_uint2(pack_bf16(dv4[0], dv4[1]), pack_bf16(dv4[2], dv4[3]));
-    const float4 cs = *reinterpret_cast<const float4*>(col_scale + 16 * b + 8 * hh + 4 * q);
+    const float4 cs = kScaled
+                          ? *reinterpret_cast<const float4*>(col_scale + 16 * b + 8 * hh + 4 * q)
+                          : make_float4(1.f, 1.f, 1.f, 1.f);
     *reinterpret_cast<uint2*>(t_tile + sw_chunk(row, 2 * b + hh) + 8 * q) = make_uint2(
         pack_bf16(dv4[0] * cs.x, dv4[1] * cs.y), pack_bf16(dv4[2] * cs.z, dv4[3] * cs.w));
     for (int z = 2 * b + 2 + 2 * hh + q; z < 8; z += 4)
@@ -304,7 +223,8 @@ __device__ void solve_unit_lower_sw(const unsigned char* a_tile, const float* a_
     const int nt = warp, kb0 = nt >> 1, g = lane >> 2, t = lane & 3;
     const int la = (lane & 7) + 8 * ((lane >> 3) & 1), ca = lane >> 4;
     const uint32_t abase = smem_addr(a_tile), dbase = smem_addr(d_blk);
-    const float cs0 = col_scale[8 * nt + 2 * t], cs1 = col_scale[8 * nt + 2 * t + 1];
+    const float cs0 = kScaled ? col_scale[8 * nt + 2 * t] : 1.f;
+    const float cs1 = kScaled ? col_scale[8 * nt + 2 * t + 1] : 1.f;
     uint32_t tb[4][2];  // finished blocks (kb, strip) as B fragments, unscaled
 #pragma unroll
     for (int kb = 0; kb < 3; ++kb)
