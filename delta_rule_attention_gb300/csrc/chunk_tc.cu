@@ -35,6 +35,8 @@
 //     operands), so an undecayed state does not drift over long sequences.
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -145,7 +147,7 @@ constexpr int kMapThreads = 256;
 // columns 32h .. 32h+31 (h = t >> 7) of the CTA's 64-column half j.
 template <int M>
 __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
-    tc_chunk_map_kernel(ChunkArgs a, int nchunks, int c_begin, int* err,
+    tc_chunk_map_kernel(ChunkArgs a, int nchunks, int c_begin, int* err, uint32_t pf_ahead,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_v) {
@@ -199,6 +201,20 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
       tma_load_3d(qt + at * L::kAtom, &tm_q, 64 * at, (int)t0, (int)bh, &sc.bar_in);
     }
     tma_load_3d(vh, &tm_v, 64 * j, (int)t0, (int)bh, &sc.bar_in);
+  }
+  // CTAs are dispatched close to linear block order, so the one that takes
+  // this CTA's slot is about pf_ahead (the resident CTAs of the device) blocks
+  // on: bring its k, q, v rows into L2 now, so that its tile loads hit L2.
+  if (tid == 32 && pf_ahead > 0) {
+    const uint32_t Lp = blockIdx.x + gridDim.x * blockIdx.y + pf_ahead;
+    if (Lp < gridDim.x * gridDim.y) {
+      const int cp = c_begin + (int)((Lp % gridDim.x) / L::kHalves);
+      const int64_t rp = (int64_t)(Lp / gridDim.x) * a.T + (int64_t)cp * kC;  // first row
+      const uint32_t bytes = (uint32_t)min((int64_t)kC, a.T - (int64_t)cp * kC) * M * 2;
+      bulk_prefetch_l2(reinterpret_cast<const __nv_bfloat16*>(a.k) + rp * M, bytes);
+      bulk_prefetch_l2(reinterpret_cast<const __nv_bfloat16*>(a.q) + rp * M, bytes);
+      bulk_prefetch_l2(reinterpret_cast<const __nv_bfloat16*>(a.v) + rp * M, bytes);
+    }
   }
   float beta_t = 0.f, lam_t = 0.f;
   if (tid < n) {
@@ -1075,6 +1091,25 @@ size_t tc_workspace_bytes(int m, int64_t BH, int64_t T) {
 
 namespace {
 
+// CTAs of tc_chunk_map_kernel<M> resident on the current device at once (SMs x
+// CTAs per SM), cached per device; 0 if the runtime cannot tell (no prefetch).
+template <int M>
+uint32_t map_residency() {
+  static std::atomic<uint32_t> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  uint32_t v = cache[dev].load(std::memory_order_relaxed);
+  if (v != 0) return v;
+  int sms = 0, per_sm = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc_chunk_map_kernel<M>, kMapThreads,
+                                                    map_smem_bytes<M>() + 1024) != cudaSuccess)
+    return 0;
+  v = (uint32_t)(sms > 0 ? sms : 0) * (uint32_t)(per_sm > 0 ? per_sm : 0);
+  cache[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
 // pdl: programmatic dependent launch behind the preceding kernel on the stream
 // (the map kernel waits for it with griddepcontrol.wait before reading inputs).
 template <int M>
@@ -1095,7 +1130,8 @@ cudaError_t launch_map(const ChunkArgs& a, int nchunks, int c_begin, int n, int*
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, tc_chunk_map_kernel<M>, a, nchunks, c_begin, err, tm_k, tm_q,
+  return cudaLaunchKernelEx(&cfg, tc_chunk_map_kernel<M>, a, nchunks, c_begin, err,
+                            map_residency<M>(), tm_k, tm_q,
                             tm_v);
 }
 
