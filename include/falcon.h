@@ -35,6 +35,15 @@
  *     the call forks from the caller's stream and joins back to it by events,
  *     so later work on the caller's stream sees the call complete, and a
  *     stream capture of the call captures the fork and the join.
+ *   - The chunked forwards launch their kernels as programmatic dependent
+ *     launches, and their last kernel lets the next such launch on the
+ *     stream begin early.  Each of the library's kernels waits for the grid
+ *     before it (griddepcontrol.wait) before it reads or writes memory, so
+ *     stream order holds for the library's own calls and for ordinary
+ *     launches.  A kernel of the caller's that is launched right after one of
+ *     these calls with programmatic stream serialization may start before the
+ *     call ends, and must wait for it (cudaGridDependencySynchronize) before it
+ *     reads the call's outputs, as every such launch must.
  *   - Tensors are dense, row-major, contiguous; [B,H,T,m] means element
  *     (b,h,t,i) is at ((b*H + h)*T + t)*m + i.
  *   - Every pointer must be 16-byte aligned (FALCON_ERR_MISALIGNED otherwise).
