@@ -482,13 +482,19 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
 #pragma unroll
       for (int i = 0; i < 32; ++i) d[i] = (r < 64) ? -d[i] : eq * x[i] - d[i];
       store_half_sw(mc_stage, r, h, d, 1.f);
+      fence_async_smem();
       tmem_ld32(tlane + 64 + 32 * h, d);
+      __syncthreads();
+      // Mc leaves while Nc is staged.
+      if (tid == 0) {
+        bulk_s2g(map, mc_stage, kMcBytes);
+        bulk_commit();
+      }
       store_half_sw(nc_stage, r, h, d, 1.f);  // Nc: chunk cc at position cc ^ (row & 7)
       fence_async_smem();
       __syncthreads();
       if (tid == 0) {
         *reinterpret_cast<float*>(map + kMcBytes + kNcBytes) = __expf(gC);
-        bulk_s2g(map, mc_stage, kMcBytes);
         bulk_s2g(map + kMcBytes, nc_stage, kNcBytes);
         bulk_commit();
         bulk_wait_read<0>();  // the staging must outlive the copies' reads
@@ -504,25 +510,33 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
 #pragma unroll
       for (int i = 0; i < 32; ++i) d[i] = -d[i];
       store_half_sw(mcs_stage, r, h, d, 1.f);
-      tmem_ld32(tlane + 64 + 32 * h, d);
-      store_half_sw(ncs_stage, r, h, d, 1.f);
       if (r >= 64) {  // warps 2, 3, 6, 7: lanes 64..127 hold P [W_j | U~_j]
         const float eq = __expf(sc.g[r - 64]) * nr;
         tmem_ld32(tlane + 128 + 32 * h, d);
 #pragma unroll
         for (int i = 0; i < 32; ++i) d[i] = eq * x[i] - d[i];
         store_half_sw(mco_stage, r - 64, h, d, 1.f);
+      }
+      fence_async_smem();
+      __syncthreads();
+      unsigned char* mc = map + j * L::kMcAtom;
+      unsigned char* nc = map + (2 + j) * L::kMcAtom;
+      // The Mc atom leaves while Nc is staged.
+      if (tid == 0) {
+        bulk_s2g(mc, mcs_stage, 16384);
+        bulk_s2g(mc + 16384, mco_stage, 8192);
+        bulk_commit();
+      }
+      tmem_ld32(tlane + 64 + 32 * h, d);
+      store_half_sw(ncs_stage, r, h, d, 1.f);
+      if (r >= 64) {
         tmem_ld32(tlane + 192 + 32 * h, d);
         store_half_sw(nco_stage, r - 64, h, d, 1.f);
       }
       fence_async_smem();
       __syncthreads();
       if (tid == 0) {
-        unsigned char* mc = map + j * L::kMcAtom;
-        unsigned char* nc = map + (2 + j) * L::kMcAtom;
         if (j == 0) *reinterpret_cast<float*>(map + 4 * L::kMcAtom) = __expf(gC);
-        bulk_s2g(mc, mcs_stage, 16384);
-        bulk_s2g(mc + 16384, mco_stage, 8192);
         bulk_s2g(nc, ncs_stage, 16384);
         bulk_s2g(nc + 16384, nco_stage, 8192);
         bulk_commit();
