@@ -183,7 +183,9 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
   const bool carried_row = c == 0 && r == 0;
   const bool patch = c == 0 && a.x_prev != nullptr;
 
-  if (warp == 0) tmem_alloc(&sc.tmem_base, L::kTmemCols);
+  // TMEM is allocated by warp 1, so that thread 0 issues the input tile copies
+  // (the head of the CTA's chain) without waiting for the allocation.
+  if (warp == 1) tmem_alloc(&sc.tmem_base, L::kTmemCols);
   // Launched behind the previous call's scan (programmatic dependent launch),
   // the CTA may start while that grid still runs: no input is read, and no
   // output or workspace byte written, before the preceding grid has completed.
@@ -205,7 +207,7 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
   // CTAs are dispatched close to linear block order, so the one that takes
   // this CTA's slot is about pf_ahead (the resident CTAs of the device) blocks
   // on: bring its k, q, v rows into L2 now, so that its tile loads hit L2.
-  if (tid == 32 && pf_ahead > 0) {
+  if (tid == 64 && pf_ahead > 0) {
     const uint32_t Lp = blockIdx.x + gridDim.x * blockIdx.y + pf_ahead;
     if (Lp < gridDim.x * gridDim.y) {
       const int cp = c_begin + (int)((Lp % gridDim.x) / L::kHalves);
@@ -550,7 +552,7 @@ teardown:
   if (sc.fail && tid == 0) flag_error(err);
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, L::kTmemCols);
+  if (warp == 1) tmem_dealloc(tmem, L::kTmemCols);
 }
 
 // ---------------------------------------------------------------------------

@@ -246,7 +246,9 @@ __global__ void __launch_bounds__(kBThreads, 2)
     bulk_prefetch_l2(S, 4096 * 4);
     bulk_prefetch_l2(dSp, 4096 * 4);
   }
-  if (warp == 0) tmem_alloc(&sc.tmem_base, kTmemCols);
+  // TMEM is allocated by warp 1, so that thread 0 issues the input tile copies
+  // (the head of the CTA's chain) without waiting for the allocation.
+  if (warp == 1) tmem_alloc(&sc.tmem_base, kTmemCols);
   if (tid == 0) {
     mbar_init(&sc.bar_in, 1);
     mbar_init(&sc.bar_mma, 1);
@@ -732,7 +734,7 @@ teardown:
   if (sc.fail && tid == 0) atomicExch(err, 1);
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
 // ---------------------------------------------------------------------------

@@ -95,7 +95,9 @@ __global__ void __launch_bounds__(k2Threads, 2)
   const int64_t T = a.T, t0 = (int64_t)c * k2C, rowbase = bh * T;
   const int n = (int)min((int64_t)k2C, T - t0);
 
-  if (warp == 0) tmem_alloc(&sc.tmem_base, 256);
+  // TMEM is allocated by warp 1, so that thread 0 issues the input tile copies
+  // (the head of the CTA's chain) without waiting for the allocation.
+  if (warp == 1) tmem_alloc(&sc.tmem_base, 256);
   // Launched behind the previous call's scan (programmatic dependent launch):
   // nothing is read or written before the preceding grid has completed.
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -332,7 +334,7 @@ teardown:
   if (sc.fail && tid == 0) atomicExch(err, 1);
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 256);
+  if (warp == 1) tmem_dealloc(tmem, 256);
 }
 
 // ---------------------------------------------------------------------------
