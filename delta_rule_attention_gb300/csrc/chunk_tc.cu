@@ -132,7 +132,6 @@ struct MapScalars {
   float cu[64], fv[64], fw[64];
   float nrm[128];                // phi's scale of row r of [K; Q] (1 / ||row||, or 1)
   float ssp[2][128];             // half-row partial sums of squares
-  float carry;
   int fail;
   uint64_t bar_in, bar_mma;
   uint32_t tmem_base;
@@ -218,10 +217,17 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
       bulk_prefetch_l2(reinterpret_cast<const __nv_bfloat16*>(a.v) + rp * M, bytes);
     }
   }
-  float beta_t = 0.f, lam_t = 0.f;
-  if (tid < n) {
-    beta_t = a.beta[rowbase + t0 + tid];
-    lam_t = a.lambda[rowbase + t0 + tid];
+  // Warps 0 and 1 form the step sizes of all 64 tokens (lane l: tokens l and
+  // l + 32), so each has the whole prefix without an exchange.
+  float beta2[2] = {0.f, 0.f}, lam2[2] = {0.f, 0.f};
+  if (warp < 2) {
+#pragma unroll
+    for (int k2 = 0; k2 < 2; ++k2) {
+      if (lane + 32 * k2 < n) {
+        beta2[k2] = a.beta[rowbase + t0 + lane + 32 * k2];
+        lam2[k2] = a.lambda[rowbase + t0 + lane + 32 * k2];
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -277,7 +283,6 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
   __syncthreads();
   const float ss = sc.ssp[0][r] + sc.ssp[1][r];
   const float nr = carried_row ? 1.f : phi_scale(ss, M, a.phi);
-  const float E = ss * nr * nr;  // ||x_r||^2 (rows < 64)
   if (h == 0) sc.nrm[r] = nr;
   if (a.x_last && last) {
     // phi(k_{T-1}) (columns of half j): row n of the features when the last
@@ -302,39 +307,54 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
     }
   }
 
-  // ---- step sizes, log-decays, chunk-local inclusive prefix g (threads 0..63) ----
-  float eta = 0.f, lg = 0.f;
-  if (tid < 64 && tid < n) {
-    float gam;
-    const bool sentinel = (t0 + tid == 0) && (a.x_prev == nullptr);
-    eta = step_eta_gamma(sentinel, E, beta_t, ridge_of(lam_t, E, a.ridge), a.eps, a.eps_gamma,
-                         &gam, &lg);
-  }
-  float incl = lg;
+  // ---- step sizes, log-decays, chunk-local inclusive prefix g and the rank-1
+  //      decay factors (warps 0 and 1; thread t < 64 publishes token t's) ----
+  if (warp < 2) {
+    float etav[2], lgv[2];
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
+    for (int k2 = 0; k2 < 2; ++k2) {
+      const int tk = lane + 32 * k2;  // token t0 + tk, write-feature row tk
+      const float ssk = sc.ssp[0][tk] + sc.ssp[1][tk];
+      const float nrk = (c == 0 && tk == 0) ? 1.f : phi_scale(ssk, M, a.phi);
+      const float Ek = ssk * nrk * nrk;  // ||x_tk||^2
+      etav[k2] = 0.f;
+      lgv[k2] = 0.f;
+      if (tk < n) {
+        float gam;
+        const bool sentinel = (t0 + tk == 0) && (a.x_prev == nullptr);
+        etav[k2] = step_eta_gamma(sentinel, Ek, beta2[k2], ridge_of(lam2[k2], Ek, a.ridge),
+                                  a.eps, a.eps_gamma, &gam, &lgv[k2]);
+      }
+    }
+    float incl[2] = {lgv[0], lgv[1]};
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+      for (int k2 = 0; k2 < 2; ++k2) {
+        const float y = __shfl_up_sync(0xffffffffu, incl[k2], o);
+        if (lane >= o) incl[k2] += y;
+      }
+    }
+    incl[1] += __shfl_sync(0xffffffffu, incl[0], 31);
+    const float gCw = __shfl_sync(0xffffffffu, incl[1], 31);
+    const float eo = warp == 0 ? etav[0] : etav[1];  // this thread's token, t = tid
+    const float lo = warp == 0 ? lgv[0] : lgv[1];
+    const float go = warp == 0 ? incl[0] : incl[1];
+    sc.eta[tid] = eo;
+    sc.g[tid] = go;
+    sc.gx[tid] = go - lo;
+    // Rank-1 decay factors around rr = g_C / 2: e^{rr - g_l} (times phi's scale
+    // of x_l), fv_j = eta_j e^{g_{j-1} - rr}, fw_i = e^{g_i - rr}.
+    if (-gCw <= kFactorSpan) {
+      const float rr = 0.5f * gCw;
+      sc.cu[tid] = __expf(rr - go) * nr;
+      sc.fv[tid] = eo * __expf((go - lo) - rr);
+      sc.fw[tid] = __expf(go - rr);
+    }
   }
-  if (tid == 31) sc.carry = incl;
-  __syncthreads();
-  if (warp == 1) incl += sc.carry;
-  if (tid < 64) {
-    sc.eta[tid] = eta;
-    sc.g[tid] = incl;
-    sc.gx[tid] = incl - lg;
-  }
-  __syncthreads();
+  __syncthreads();  // step sizes, prefix and decay factors visible
   const float gC = sc.g[kC - 1];
   const bool factored = -gC <= kFactorSpan;
-  // Rank-1 decay factors around rr = g_C / 2: e^{rr - g_l} (times phi's scale
-  // of x_l), fv_j = eta_j e^{g_{j-1} - rr}, fw_i = e^{g_i - rr}.
-  if (r < 64 && h == 0 && factored) {
-    const float rr = 0.5f * gC;
-    sc.cu[r] = __expf(rr - sc.g[r]) * nr;
-    sc.fv[r] = sc.eta[r] * __expf(sc.gx[r] - rr);
-    sc.fw[r] = __expf(sc.g[r] - rr);
-  }
   if (r < 64) {
     // Xh = Diag(e^{g_-}) X (MMA2's A, columns of half j); Falcon-1A: W = 0 and
     // T' = Diag(eta), whose rows are written here (the solve writes Falcon-1's).
@@ -347,9 +367,9 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
       store_half_sw(t_tile, r, h, trow, 1.f);
     }
   }
+  // Every thread sees MMA1 complete before it overwrites the K and Q tiles.
   if (!sc.fail && !mbar_wait(&sc.bar_mma, 0)) sc.fail = 1;
   tc_fence_after();
-  __syncthreads();  // factors visible; MMA1 has finished reading [K; Q]
 
   // Xt = Diag(e^{g_C - g}) X over the K tile (m = 64: by the threads of rows
   // 64..127, each rewriting in place the four chunks it reads; m = 128: from
