@@ -489,7 +489,9 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
   }
   if (!mbar_wait(&sc.bar_mma, 0)) sc.fail = 1;
   tc_fence_after();
-  if (!__syncthreads_or(sc.fail)) {
+  // No barrier here: each thread has seen MMA3 complete (its operands are
+  // dead) before it stages; a failed wait is agreed on at the staging barrier.
+  {
     unsigned char* map = reinterpret_cast<unsigned char*>(a.workspace) +
                          (size_t)(bh * nchunks + c) * L::kMapBytes;
     // The map images are staged in shared memory (the MMA3 operands are dead)
@@ -506,7 +508,7 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
       store_half_sw(mc_stage, r, h, d, 1.f);
       fence_async_smem();
       tmem_ld32(tlane + 64 + 32 * h, d);
-      __syncthreads();
+      if (__syncthreads_or(sc.fail)) goto teardown;
       // Mc leaves while Nc is staged.
       if (tid == 0) {
         bulk_s2g(map, mc_stage, kMcBytes);
@@ -540,7 +542,7 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
         store_half_sw(mco_stage, r - 64, h, d, 1.f);
       }
       fence_async_smem();
-      __syncthreads();
+      if (__syncthreads_or(sc.fail)) goto teardown;
       unsigned char* mc = map + j * L::kMcAtom;
       unsigned char* nc = map + (2 + j) * L::kMcAtom;
       // The Mc atom leaves while Nc is staged.
