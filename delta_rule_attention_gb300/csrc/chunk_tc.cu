@@ -500,6 +500,12 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
     if constexpr (!kWide) {
       unsigned char* mc_stage = kt;  // 16 KB over the K and Q tiles
       unsigned char* nc_stage = wu_tile;  // 16 KB
+      // Rows 0..63 of both images come from warps 0, 1, 4, 5 and rows 64..127
+      // from warps 2, 3, 6, 7: each half synchronises on its own named barrier
+      // and sends its own 8 KB.
+      const int grp = r >= 64 ? 1 : 0;
+      const bool lead = tid == 64 * grp;  // thread 0 and thread 64
+      const uint32_t half = 8192u * (uint32_t)grp;
       tmem_ld32(tlane + 32 * h, d);
       // Mc row: rows < 64 -> -Xt^T W ; rows >= 64 -> e^{g_i} phi(q_i) - P W
       const float eq = (r >= 64) ? __expf(sc.g[r - 64]) * nr : 0.f;
@@ -508,18 +514,22 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
       store_half_sw(mc_stage, r, h, d, 1.f);
       fence_async_smem();
       tmem_ld32(tlane + 64 + 32 * h, d);
-      if (__syncthreads_or(sc.fail)) goto teardown;
+      // (constant barrier ids in each branch: a computed id would reserve all 16)
+      const bool failed = grp ? named_sync_or(2, 128, sc.fail) : named_sync_or(1, 128, sc.fail);
       // Mc leaves while Nc is staged.
-      if (tid == 0) {
-        bulk_s2g(map, mc_stage, kMcBytes);
+      if (lead && !failed) {
+        bulk_s2g(map + half, mc_stage + half, kMcBytes / 2);
         bulk_commit();
       }
       store_half_sw(nc_stage, r, h, d, 1.f);  // Nc: chunk cc at position cc ^ (row & 7)
       fence_async_smem();
-      __syncthreads();
-      if (tid == 0) {
-        *reinterpret_cast<float*>(map + kMcBytes + kNcBytes) = __expf(gC);
-        bulk_s2g(map + kMcBytes, nc_stage, kNcBytes);
+      if (grp)
+        named_sync(2, 128);
+      else
+        named_sync(1, 128);
+      if (lead && !failed) {
+        if (grp == 0) *reinterpret_cast<float*>(map + kMcBytes + kNcBytes) = __expf(gC);
+        bulk_s2g(map + kMcBytes + half, nc_stage + half, kNcBytes / 2);
         bulk_commit();
         bulk_wait_read<0>();  // the staging must outlive the copies' reads
       }
