@@ -124,6 +124,15 @@ __device__ __forceinline__ bool wait_mma(BwdScalars& sc, uint32_t& phase) {
   return !__syncthreads_or(sc.fail);
 }
 
+// The same wait without the barrier: where the thread then only reads the
+// accumulators and overwrites tiles the completed MMAs no longer need, it
+// needs no other thread; a failed wait is agreed on at the next barrier.
+__device__ __forceinline__ void wait_mma_own(BwdScalars& sc, uint32_t& phase) {
+  if (!mbar_wait(&sc.bar_mma, phase)) sc.fail = 1;
+  phase ^= 1u;
+  tc_fence_after();
+}
+
 // Warp-wide scans of 64 values, two per lane.  Prefix: lane l takes elements
 // 2l, 2l+1 and writes the exclusive and inclusive prefix sums.  Suffix: lane l
 // takes elements 63-2l, 62-2l of v and writes sum_{j >= i} v_j to out.
@@ -196,6 +205,13 @@ __device__ __forceinline__ void publish_tiles() {
   tc_fence_before();
   fence_async_smem();
   __syncthreads();
+}
+
+// The same, agreeing on a failed wait: false if any thread saw one.
+__device__ __forceinline__ bool publish_tiles_ok(BwdScalars& sc) {
+  tc_fence_before();
+  fence_async_smem();
+  return !__syncthreads_or(sc.fail);
 }
 
 // Column sums of a warp's 32 rows: v holds 32 consecutive columns of this
@@ -460,7 +476,7 @@ __global__ void __launch_bounds__(kBThreads, 2)
             idesc_bf16(128, 64, false, true), false);
     mma_commit(&sc.bar_mma);
   }
-  if (!wait_mma(sc, phase)) goto teardown;
+  wait_mma_own(sc, phase);
   // U and Us = Diag(e^{g_C - g}) U tiles, xw_i = <(X dS')_i, U_i>; P (split)
   {
     float d[32], e[32];
@@ -493,7 +509,7 @@ __global__ void __launch_bounds__(kBThreads, 2)
       store_half_split(tile(kP), tile(kPlo), i, h, d);
     }
   }
-  publish_tiles();
+  if (!publish_tiles_ok(sc)) goto teardown;
   // ---- P^T dO (split P)
   if (tid == 0) {
     tc_fence_after();
@@ -502,7 +518,7 @@ __global__ void __launch_bounds__(kBThreads, 2)
     mma_k64(tmem + kD3, taddr(kPlo), true, kTile, taddr(kdO), true, kTile, id, true);
     mma_commit(&sc.bar_mma);
   }
-  if (!wait_mma(sc, phase)) goto teardown;
+  wait_mma_own(sc, phase);
   // dU = P^T dO + Diag(e^{g_C - g}) X dS' (split)
   if (r < 64) {
     float d[32], xd[32];
@@ -513,7 +529,7 @@ __global__ void __launch_bounds__(kBThreads, 2)
     for (int jj = 0; jj < 32; ++jj) d[jj] += f * xd[jj];
     store_half_split(tile(kdU), tile(kdUlo), i, h, d);
   }
-  publish_tiles();
+  if (!publish_tiles_ok(sc)) goto teardown;
   // ---- dR = T^T dU
   if (tid == 0) {
     tc_fence_after();
@@ -522,7 +538,7 @@ __global__ void __launch_bounds__(kBThreads, 2)
     mma_k64(tmem + kD3, taddr(kT), true, kTile, taddr(kdUlo), true, kTile, id, true);
     mma_commit(&sc.bar_mma);
   }
-  if (!wait_mma(sc, phase)) goto teardown;
+  wait_mma_own(sc, phase);
   // dR and dRs = -Diag(eta e^{g_-}) dR tiles; dv = Diag(eta) dR;
   // rv_i = <dR_i, v_i - e^{g_{i-1}} (X S)_i>, xy_i = <dR_i, (X S)_i>
   if (r < 64) {
@@ -548,7 +564,7 @@ __global__ void __launch_bounds__(kBThreads, 2)
       for (int q8 = 0; q8 < 4; ++q8) dst[q8] = pack8(d + 8 * q8, ei);
     }
   }
-  publish_tiles();
+  if (!publish_tiles_ok(sc)) goto teardown;
   // ---- [dR; dO] U^T: rows 0..63 -dA (before masking), rows 64..127 dP
   if (tid == 0) {
     tc_fence_after();
@@ -556,7 +572,7 @@ __global__ void __launch_bounds__(kBThreads, 2)
             idesc_bf16(128, 64, false, false), false);
     mma_commit(&sc.bar_mma);
   }
-  if (!wait_mma(sc, phase)) goto teardown;
+  wait_mma_own(sc, phase);
   {
     float d[32], e[32], pr[32];
     if (r < 64) {
@@ -601,7 +617,7 @@ __global__ void __launch_bounds__(kBThreads, 2)
       atomicAdd(&sc.spc[32 * h + lane], warp_col_sum32(pr));
     }
   }
-  __syncthreads();
+  if (__syncthreads_or(sc.fail)) goto teardown;
   // ---- the step-size cotangent, the log-prefix cotangent and its suffix sums,
   //      then dbeta, dlambda and dE per token
   if (tid < 64) {
