@@ -233,7 +233,8 @@ __global__ void __launch_bounds__(k2Threads, 2)
   if (!mbar_wait(&sc.bar_mma, phase)) sc.fail = 1;
   phase ^= 1u;
   tc_fence_after();
-  if (__syncthreads_or(sc.fail)) goto teardown;
+  // No barrier: each thread has seen the MMA complete before it reads its
+  // accumulator rows; a failed wait is agreed on at the next barrier.
   // A = causal part of Q X^T (rows 0..63: lanes of warps 0, 1, 4, 5)
   if ((warp & 3) < 2) {
     float d[32];
@@ -242,7 +243,9 @@ __global__ void __launch_bounds__(k2Threads, 2)
     for (int jj = 0; jj < 32; ++jj) d[jj] = (32 * h + jj <= r) ? d[jj] : 0.f;
     store_half_sw(tile(kA2), r, h, d, 1.f);
   }
-  publish_f2();
+  tc_fence_before();
+  fence_async_smem();
+  if (__syncthreads_or(sc.fail)) goto teardown;
   // ---- D2 = A U~ (output rows), D3 = X^T V' (state rows)
   if (tid == 0) {
     tc_fence_after();
@@ -255,7 +258,8 @@ __global__ void __launch_bounds__(k2Threads, 2)
   if (!mbar_wait(&sc.bar_mma, phase)) sc.fail = 1;
   phase ^= 1u;
   tc_fence_after();
-  if (__syncthreads_or(sc.fail)) goto teardown;
+  // No barrier: each thread has seen the MMAs complete before it overwrites
+  // their operands with the staging; a failed wait is agreed on below.
   // ---- the map: phi(Q) (the Q tile itself), Nc (state rows from D3, output
   //      rows F o D2) over the A and U~ tiles, E over the V' tile, e^{G_C}
   {
@@ -304,7 +308,7 @@ __global__ void __launch_bounds__(k2Threads, 2)
       store_half_sw(e_stage, t, h, e, 1.f);
     }
     fence_async_smem();
-    __syncthreads();
+    if (__syncthreads_or(sc.fail)) goto teardown;
     if (tid == 0) {
       unsigned char* map = reinterpret_cast<unsigned char*>(a.workspace) +
                            (size_t)(bh * nchunks + c) * kMap2ABytes;

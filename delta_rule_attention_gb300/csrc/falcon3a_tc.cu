@@ -230,7 +230,9 @@ __global__ void __launch_bounds__(k3Threads, 2)
   if (!mbar_wait(&sc.bar_mma, phase)) sc.fail = 1;
   phase ^= 1u;
   tc_fence_after();
-  if (__syncthreads_or(sc.fail)) goto teardown;
+  // No barrier: each thread has seen the MMA complete before it reads its
+  // accumulator rows and writes the P tiles; a failed wait is agreed on at
+  // the next barrier.
   // P = (Q X~^T) o W, rows 0..63 (lanes 0..63), two column halves per tile
   if ((warp & 3) < 2) {
     const int i = r;
@@ -245,7 +247,7 @@ __global__ void __launch_bounds__(k3Threads, 2)
   }
   tc_fence_before();
   fence_async_smem();
-  __syncthreads();
+  if (__syncthreads_or(sc.fail)) goto teardown;
   // ---- D2 = P V~ (K = 128), D3 = X~^T Vs (K = 128, X~ read MN-major)
   if (tid == 0) {
     tc_fence_after();
@@ -260,7 +262,8 @@ __global__ void __launch_bounds__(k3Threads, 2)
   if (!mbar_wait(&sc.bar_mma, phase)) sc.fail = 1;
   phase ^= 1u;
   tc_fence_after();
-  if (__syncthreads_or(sc.fail)) goto teardown;
+  // No barrier: each thread has seen the MMAs complete before it overwrites
+  // their operands with the staging; a failed wait is agreed on below.
   // ---- the map: Mc = [0; Diag(e^g) phi(Q)] over the P tiles, Nc = [D3; D2]
   //      over the Vs tiles, e^{g_C}
   {
@@ -282,7 +285,7 @@ __global__ void __launch_bounds__(k3Threads, 2)
       store_half_sw(nc_stage, 64 + r, h, v, 1.f);
     }
     fence_async_smem();
-    __syncthreads();
+    if (__syncthreads_or(sc.fail)) goto teardown;
     if (tid == 0) {
       unsigned char* map = reinterpret_cast<unsigned char*>(a.workspace) +
                            (size_t)(bh * nchunks + c) * kMapBytes;
