@@ -52,6 +52,7 @@ using namespace tc;
 using namespace tcu;
 
 constexpr int kC = 64;
+constexpr int kScanRing = 5;  // map stages the m = 64 scan loads before its first MMA
 // A chunk whose log-decay spans at most this much factors e^{a-b} as
 // e^{a-r} e^{r-b} (both factors stay within fp32 range).
 constexpr float kFactorSpan = 80.f;
@@ -219,6 +220,23 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
   }
   // Warps 0 and 1 form the step sizes of all 64 tokens (lane l: tokens l and
   // l + 32), so each has the whole prefix without an exchange.
+  // The scan opens with the first kScanRing maps of every head, most of them
+  // written early in this grid and out of L2 by its end: the last resident set
+  // of CTAs brings them back (CTA k of that set: head k % BH, chunk k / BH).
+  if constexpr (M == 64) {
+    if (tid == 96 && pf_ahead > 0 && c_begin == 0) {
+      const uint32_t total = gridDim.x * gridDim.y;
+      const uint32_t Lc = blockIdx.x + gridDim.x * blockIdx.y;
+      if (Lc + pf_ahead >= total) {
+        const uint32_t k = Lc + pf_ahead - total;
+        const uint32_t hh = k % gridDim.y, cc = k / gridDim.y;
+        if (cc < (uint32_t)kScanRing && (int)cc < nchunks)
+          bulk_prefetch_l2(reinterpret_cast<const unsigned char*>(a.workspace) +
+                               ((size_t)hh * nchunks + cc) * L::kMapBytes,
+                           L::kMapBytes);
+      }
+    }
+  }
   float beta2[2] = {0.f, 0.f}, lam2[2] = {0.f, 0.f};
   if (warp < 2) {
 #pragma unroll
@@ -597,7 +615,7 @@ teardown:
 // c + kStages into the stage of chunk c once every math warp is done with it,
 // the output rows run beside the chain, and the accumulator is
 // double-buffered in TMEM.  Every hand-off is one mbarrier arrival per warp.
-constexpr int kStages = 5;
+constexpr int kStages = kScanRing;
 constexpr int kScanMathWarps = 16;
 constexpr int kScanThreads = 32 * (kScanMathWarps + 2);
 
