@@ -77,7 +77,8 @@ int* device_error_word() {
 int fwd_chunked(int rule, const falcon_shape* s, const void* q, const void* k, const void* v,
                 const float* beta, const float* lambda, const float* S0, const float* x_prev,
                 void* o, float* S_out, float* x_last, void* workspace, size_t workspace_bytes,
-                cudaStream_t stream, int window = 1, bool chunked_form = false) {
+                cudaStream_t stream, int window = 1, bool chunked_form = false,
+                int (*resolve_workspace)(void**) = nullptr) {
   int rc = check_shape(s);
   if (rc) return rc;
   const int64_t BH = s->B * s->H;
@@ -103,10 +104,19 @@ int fwd_chunked(int rule, const falcon_shape* s, const void* q, const void* k, c
   const size_t need = ((per_column && !column_tc) || (windowed && !window_tc))
                           ? 0
                           : falcon_workspace_bytes(s);
-  if (need > 0 && (!workspace || workspace_bytes < need)) return FALCON_ERR_WORKSPACE;
+  // A resolver stands for a workspace of workspace_bytes whose address is
+  // only known once a device is current: it is asked after every argument
+  // check, so that the codes are the same as for a caller-given workspace.
+  if (need > 0 && ((!workspace && !resolve_workspace) || workspace_bytes < need))
+    return FALCON_ERR_WORKSPACE;
   if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return FALCON_ERR_MISALIGNED;
   rc = check_device();
   if (rc) return rc;
+  if (resolve_workspace) {
+    rc = resolve_workspace(&workspace);
+    if (rc) return rc;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FALCON_ERR_MISALIGNED;
+  }
 
   const size_t state_bytes = sizeof(float) * (size_t)BH * s->m * s->dv;
   if (s->T == 0) {  // nothing to run: S_T = S0, x_last = x_prev
@@ -291,6 +301,18 @@ int decode(int rule, int64_t N, int32_t m, int32_t dv, int32_t dtype, int32_t ph
 }
 
 }  // namespace
+
+namespace falcon {
+// Falcon-1 chunked forward over a workspace of workspace_bytes whose device
+// address `resolve` gives once the device check has passed.
+int fwd_chunked_resolved(const falcon_shape* s, const void* q, const void* k, const void* v,
+                         const float* beta, const float* lambda, const float* S0,
+                         const float* x_prev, void* o, float* S_out, float* x_last,
+                         int (*resolve)(void**), size_t workspace_bytes, cudaStream_t stream) {
+  return fwd_chunked(kFalcon1, s, q, k, v, beta, lambda, S0, x_prev, o, S_out, x_last, nullptr,
+                     workspace_bytes, stream, 1, false, resolve);
+}
+}  // namespace falcon
 
 extern "C" {
 

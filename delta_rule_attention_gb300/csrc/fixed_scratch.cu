@@ -57,12 +57,12 @@ extern "C" int falcon1_fwd_chunked_fixed_scratch(const falcon_shape* shape, cons
                                                  const float* lambda, const float* S0,
                                                  const float* x_prev, void* o, float* S_out,
                                                  float* x_last, cudaStream_t stream) {
-  if (!shape) return FALCON_ERR_NULL_PTR;
+  // falcon_workspace_bytes is 0 for a NULL or invalid shape, which the
+  // forward's own checks then reject; the array's address is resolved only
+  // after every argument check has passed.
   if (falcon_workspace_bytes(shape) > (size_t)FALCON_FIXED_SCRATCH_BYTES)
     return FALCON_ERR_SCRATCH_LIMIT;
-  void* scratch = nullptr;
-  const int rc = fixed_scratch_address(&scratch);
-  if (rc != FALCON_OK) return rc;
-  return falcon1_fwd_chunked(shape, q, k, v, beta, lambda, S0, x_prev, o, S_out, x_last, scratch,
-                             (size_t)FALCON_FIXED_SCRATCH_BYTES, stream);
+  return falcon::fwd_chunked_resolved(shape, q, k, v, beta, lambda, S0, x_prev, o, S_out, x_last,
+                                      fixed_scratch_address, (size_t)FALCON_FIXED_SCRATCH_BYTES,
+                                      stream);
 }
