@@ -107,13 +107,6 @@ cudaError_t launch_falcon3a_recurrent(const ChunkArgs& a, int window, int* err,
 // Tensor-core path (bf16, m = dv in {64, 128}, chunk = 64).
 bool tc_path_applies(int dtype, int m, int dv, int C, int64_t BH, int64_t T);
 size_t tc_workspace_bytes(int m, int64_t BH, int64_t T);
-// Falcon-1 chunked forward whose workspace (workspace_bytes long) is found by
-// `resolve` after the argument and device checks (the C ABI's fixed-scratch
-// entry point).
-int fwd_chunked_resolved(const falcon_shape* s, const void* q, const void* k, const void* v,
-                         const float* beta, const float* lambda, const float* S0,
-                         const float* x_prev, void* o, float* S_out, float* x_last,
-                         int (*resolve)(void**), size_t workspace_bytes, cudaStream_t stream);
 cudaError_t launch_tc_chunked(const ChunkArgs& a, int* err, cudaStream_t stream);
 // The m = 64 tensor-core scan alone, over maps already in a.workspace.
 cudaError_t launch_tc_scan64(const ChunkArgs& a, int* err, cudaStream_t stream);

@@ -26,6 +26,16 @@
 
 #include "common.cuh"
 
+namespace falcon {
+// Defined with the C ABI: the Falcon-1 chunked forward over a workspace of
+// workspace_bytes whose device address `resolve` gives once the argument and
+// device checks have passed.
+int fwd_chunked_resolved(const falcon_shape* s, const void* q, const void* k, const void* v,
+                         const float* beta, const float* lambda, const float* S0,
+                         const float* x_prev, void* o, float* S_out, float* x_last,
+                         int (*resolve)(void**), size_t workspace_bytes, cudaStream_t stream);
+}  // namespace falcon
+
 namespace {
 
 constexpr int kMaxDevices = 64;
