@@ -140,6 +140,7 @@ class ClockSampler:
         self.proc = None
 
     def __enter__(self):
+        self.edge = [self.query_once()]  # right before the timed region
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
@@ -158,12 +159,24 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
                 self.out, _ = self.proc.communicate()
+        self.edge.append(self.query_once())  # right after it
         return False
 
-    def summary(self):
+    def query_once(self):
+        """One nvidia-smi sample now (a CSV line, or "" if it cannot be taken)."""
+        try:
+            out = subprocess.run(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                                  "--format=csv,noheader,nounits"], capture_output=True,
+                                 text=True, timeout=10).stdout
+            return out.strip().splitlines()[0] if out.strip() else ""
+        except (OSError, IndexError, subprocess.TimeoutExpired):
+            return ""
+
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def parse(self, lines):
         sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in (self.out or "").strip().splitlines():
+        for line in lines:
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
@@ -172,25 +185,30 @@ class ClockSampler:
                 mx.append(float(f[2]))
             except ValueError:
                 continue
-            for n, val in zip(names, f[5:9]):
+            for n, val in zip(self.NAMES, f[5:9]):
                 if val.lower().startswith("active"):
                     reasons.add(n)
+        return sm, mx, reasons
+
+    def summary(self):
+        """Median SM clock and the throttle reasons seen in the samples taken
+        during the timed region; with fewer than three of those (a region
+        shorter than the sampling period) the samples taken right before and
+        right after it are included, and the note says so."""
+        sm, mx, reasons = self.parse((self.out or "").strip().splitlines())
+        self.in_region = len(sm)
+        out = {}
+        if len(sm) < 3:
+            e_sm, e_mx, e_r = self.parse(self.edge)
+            sm, mx, reasons = sm + e_sm, mx + e_mx, reasons | e_r
+            out["note"] = ("timed region shorter than the 200 ms sampling period: samples "
+                           "right before and right after it are included")
         if not sm:
-            # The timed region was shorter than the sampling period: one query now.
-            try:
-                out = subprocess.run(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
-                                      "--format=csv,noheader,nounits"], capture_output=True,
-                                     text=True, timeout=10).stdout
-                f = [x.strip() for x in out.strip().splitlines()[0].split(",")]
-                return {"sm_mhz": float(f[1]), "sm_max_mhz": float(f[2]),
-                        "reasons": [n for n, v in zip(names, f[5:9])
-                                    if v.lower().startswith("active")],
-                        "samples": 0, "note": "timed region shorter than the 200 ms sampling "
-                        "period; one sample taken right after it"}
-            except (OSError, IndexError, ValueError, subprocess.TimeoutExpired):
-                return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no_samples"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no_samples"]}
+        out.update({"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                    "reasons": sorted(reasons), "samples": len(sm),
+                    "samples_in_region": self.in_region})
+        return out
 
 
 def barrier(ws):
@@ -299,6 +317,13 @@ def time_e2e(falcon, w, inputs, workspace, steps, warmup, ws, dev):
     return ev0.elapsed_time(ev1) / 1e3, h2d, d2h
 
 
+def workload_config(w, ws):
+    """The config object of the bench line (the same for both arms)."""
+    return {"workload": w.name, "rule": w.rule, "B": w.B, "H": w.H, "T": w.T, "m": w.m,
+            "dv": w.dv, "chunk": w.chunk, "phi": w.phi, "tokens_per_step": w.tokens,
+            "parallelism": f"replica x{ws} (independent batches, no collective)"}
+
+
 def run_ours(args):
     import delta_rule_attention_gb300 as falcon
     import numpy as np
@@ -343,6 +368,17 @@ def run_ours(args):
         secs = time_device(step, sets, steps, args.warmup, ws)
     secs = max_over_ranks(secs, ws)
     assert falcon.falcon_sync_check() == 0
+    clocks = clk.summary()
+    if clocks.get("samples_in_region", 0) < 3:
+        # A short timed region: the clocks under the same load are sampled for
+        # about a second right after it (untimed steps of the same call).
+        with ClockSampler(local) as clk2:
+            t_end = time.perf_counter() + 1.0
+            while time.perf_counter() < t_end:
+                for i in range(64):
+                    step(sets[i % n_sets])
+                torch.cuda.synchronize()
+        clocks["under_same_load"] = clk2.summary()
     ms = secs * 1e3 / steps
     value = w.tokens * ws * steps / secs
 
@@ -361,11 +397,9 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) q,k,v; "
         "beta=2*sigmoid(n), lambda=softplus(n-3))",
-        "config": {"workload": w.name, "rule": w.rule, "B": w.B, "H": w.H, "T": w.T, "m": w.m,
-                   "dv": w.dv, "chunk": w.chunk, "phi": w.phi, "tokens_per_step": w.tokens,
-                   "l2": f"{n_sets} rotating input sets of {per_set / 1e6:.1f} MB (> L2)",
-                   "parallelism": f"replica x{ws} (independent batches, no collective)"},
-        "clocks": clk.summary(),
+        "config": dict(workload_config(w, ws),
+                       l2=f"{n_sets} rotating input sets of {per_set / 1e6:.1f} MB (> L2)"),
+        "clocks": clocks,
         "e2e": {"value": w.tokens * ws * e2e_steps / e2e_secs, "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * (steps + 0),
@@ -375,7 +409,16 @@ def run_ours(args):
                      "peak_source": pk["source"],
                      "kernel": "falcon1_fwd_chunked = tc_chunk_map_kernel + tc_chunk_scan_kernel "
                                "(2 launches per call, timed together)",
-                     "bytes_per_launch": per_set},
+                     "bytes_per_launch": per_set,
+                     # the same call against the bf16 tensor-core peak: the path is
+                     # HBM-bound (88 flop/B, below the ~286 flop/B ridge), so this
+                     # fraction is at most ~0.3 even at the HBM bound
+                     "tensor": {"achieved": algorithmic_flops(w) / (secs / steps) / 1e12,
+                                "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                                "frac": algorithmic_flops(w) / (secs / steps) / 1e12
+                                / pk["bf16_tflops"],
+                                "frac_at_hbm_bound": algorithmic_flops(w) * pk["hbm_gbs"] * 1e9
+                                / per_set / 1e12 / pk["bf16_tflops"]}},
         "flops_per_step": algorithmic_flops(w),
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -478,9 +521,29 @@ def extra_workloads(falcon, dev):
     return out
 
 
+def host_cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.TimeoutExpired):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu model")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
 def cpu_baseline(w, budget_s=12.0, reps_max=20):
     """The fp64 oracle on this host's cores: whole LM workload per rep (all
-    heads), repeated until ~budget_s of CPU time."""
+    heads), repeated until ~budget_s of CPU time; plus one thread on two heads
+    (the single-thread rate)."""
     import oracle
     x = workloads.generate(w, device="cpu")
     cores = os.cpu_count() or 1
@@ -493,25 +556,33 @@ def cpu_baseline(w, budget_s=12.0, reps_max=20):
         el = time.perf_counter() - t0
         if el > budget_s or reps >= reps_max:
             break
+    one = {n: t[:1, :2].contiguous() for n, t in x.items()}
+    t1 = time.perf_counter()
+    oracle.forward(w.rule, one["q"], one["k"], one["v"], one["beta"], one["lambda"], phi=w.phi,
+                   eps=w.eps, eps_gamma=w.eps_gamma, threads=1)
+    el1 = time.perf_counter() - t1
     return {"value": w.tokens * reps / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{reps} x full {w.name} (all {w.B * w.H} heads, fp64, {cores} threads)"}
+            "cpu_model": host_cpu_model(),
+            "sample": f"{reps} x full {w.name} (all {w.B * w.H} heads, fp64, {cores} threads)",
+            "single_thread": {"value": 2 * w.T / el1 / w.H, "unit": "tokens/s",
+                              "sample": f"2 heads of {w.name} on 1 thread, as B*T tokens/s of "
+                                        f"the {w.H}-head workload"}}
 
 
 def run_reference(args):
-    """The fp64 oracle timed on the host cores, one bounded sample per step
-    (batch element 0: all 12 heads, T = 2048), rank 0 only."""
+    """The fp64 oracle timed on the host cores, rank 0 only: one step is the
+    whole workload (all B*H heads, T tokens each), the same config as ours."""
     ws, rank, _ = dist_env()
     if rank != 0:
         return
     import oracle
     w = workloads.LM
     x = workloads.generate(w, device="cpu")
-    sub = {n: t[:1].contiguous() for n, t in x.items()}
     cores = os.cpu_count() or 1
-    steps = args.steps if args.steps is not None else 20
+    steps = args.steps if args.steps is not None else 5
 
     def one():
-        oracle.forward(w.rule, sub["q"], sub["k"], sub["v"], sub["beta"], sub["lambda"],
+        oracle.forward(w.rule, x["q"], x["k"], x["v"], x["beta"], x["lambda"],
                        phi=w.phi, eps=w.eps, eps_gamma=w.eps_gamma, threads=cores)
     for _ in range(args.warmup):
         one()
@@ -519,16 +590,17 @@ def run_reference(args):
     for _ in range(steps):
         one()
     secs = time.perf_counter() - t0
-    tokens = w.T * steps  # one batch element per step
-    value = tokens / secs
-    sample = f"batch element 0 of {w.name} (12 heads x 2048 tokens) per step, fp64"
+    value = w.tokens * steps / secs
+    sample = (f"the whole {w.name} workload per step ({w.B * w.H} heads x {w.T} tokens), fp64, "
+              f"{cores} threads")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": ws, "steps": steps, "warmup": args.warmup,
             "ms_per_step": secs * 1e3 / steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "tokens_per_step": w.T},
+            "config": workload_config(w, ws),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "sample": sample,
+                             "cpu_model": host_cpu_model()},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
@@ -589,6 +661,55 @@ def run_profile(args):
     print(json.dumps({"profile": name, "size": size, "calls": calls, "ok": True}))
 
 
+def host_link(args):
+    """Pinned host <-> device copy bandwidth at the e2e step's sizes (the lm
+    workload's inputs host->device, o and S_T device->host): each direction
+    alone, then both at once on two streams.  Prints one JSON line."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = workloads.LM
+    x = workloads.generate(w, device="cpu")
+    h_in = [t.pin_memory() for t in x.values()]
+    d_in = [torch.empty_like(t, device=dev) for t in h_in]
+    d_out = [torch.empty((w.B, w.H, w.T, w.dv), dtype=w.dtype, device=dev),
+             torch.empty((w.B, w.H, w.m, w.dv), dtype=torch.float32, device=dev)]
+    h_out = [torch.empty_like(t, device="cpu").pin_memory() for t in d_out]
+    b_in = sum(t.numel() * t.element_size() for t in h_in)
+    b_out = sum(t.numel() * t.element_size() for t in h_out)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    reps = args.steps or 50
+
+    def h2d():
+        with torch.cuda.stream(s1):
+            for d, h in zip(d_in, h_in):
+                d.copy_(h, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s2):
+            for h, d in zip(h_out, d_out):
+                h.copy_(d, non_blocking=True)
+
+    def timed(fns):
+        for _ in range(3):
+            for f in fns:
+                f()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            for f in fns:
+                f()
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t0) / reps
+
+    t_in, t_out, t_both = timed([h2d]), timed([d2h]), timed([h2d, d2h])
+    print(json.dumps({
+        "host_link": True, "reps": reps, "h2d_bytes": b_in, "d2h_bytes": b_out,
+        "h2d_gbs": b_in / t_in / 1e9, "d2h_gbs": b_out / t_out / 1e9,
+        "h2d_us": t_in * 1e6, "d2h_us": t_out * 1e6, "both_us": t_both * 1e6,
+        "both_gbs": (b_in + b_out) / t_both / 1e9,
+        "gpu": torch.cuda.get_device_name(dev), "cpu_model": host_cpu_model()}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -602,12 +723,16 @@ def main():
                     choices=["lm", "lm1a", "long", "decode", "lm2", "lm2a", "lm3a", "lmbwd",
                              "lm1abwd"], default=None,
                     help="profiler target: run --steps calls of one workload, print no timing")
+    ap.add_argument("--host-link", action="store_true",
+                    help="measure pinned host<->device copy bandwidth at the e2e sizes")
     ap.add_argument("--profile-size", type=int, default=None,
                     help="with --profile: tokens per head (chunked) or states (decode)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.profile:
+    if args.host_link:
+        host_link(args)
+    elif args.profile:
         run_profile(args)
     elif args.impl == "reference":
         run_reference(args)

@@ -49,7 +49,9 @@ void* g_scratch_ptr[kMaxDevices] = {};
 int fixed_scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FALCON_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return FALCON_ERR_DEVICE;
+  // A device ordinal beyond the library's per-device table: a runtime
+  // configuration the library cannot serve, reported like a failed query.
+  if (dev < 0 || dev >= kMaxDevices) return FALCON_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
   if (!g_scratch_ptr[dev]) {
     void* p = nullptr;

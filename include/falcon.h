@@ -163,7 +163,11 @@ int falcon1_fwd_chunked(const falcon_shape *shape, const void *q, const void *k,
  *     are rejected with FALCON_ERR_SCRATCH_LIMIT (nothing launched).
  *   - The first call on each device, with that device current, resolves the
  *     array's device address (cudaGetSymbolAddress); make that first call
- *     before any stream capture on the device.
+ *     before any stream capture on the device.  A tensor-core shape with
+ *     few heads and many chunks (the chunk-range pieces described above)
+ *     also creates, on its first use on the device, the library's second
+ *     stream and its events, as falcon1_fwd_chunked does; a warm-up call of
+ *     such a shape does that set-up too.
  *   - All calls on a device share the array, which keeps the previous call's
  *     contents (nothing needs clearing: every scratch element read is written
  *     first by the same call).  Calls whose GPU work overlaps race on it: issue
@@ -349,7 +353,12 @@ int falcon1a_decode_step(int64_t N, int32_t m, int32_t dv, int32_t dtype,
 
 /* Waits for `stream`, then reads and clears the library's device error word
  * (set by a kernel whose bounded wait ran out).  Returns FALCON_OK,
- * FALCON_ERR_TIMEOUT, or FALCON_ERR_CUDA if the stream itself failed. */
+ * FALCON_ERR_TIMEOUT, or FALCON_ERR_CUDA if the stream itself failed.
+ * The error word is one per device, not one per call: every call on the
+ * device writes the same word, so with calls in flight on several streams a
+ * timeout in any of them is reported to whichever caller reads the word
+ * first (and cleared for the others).  Callers that need a per-call status
+ * synchronise their streams one at a time. */
 int falcon_sync_check(cudaStream_t stream);
 
 /* Diagnostic of the failure path (no counterpart in the paper): launches a

@@ -94,6 +94,59 @@ def test_clamp_active_large_ridge(falcon, rule):
     assert head_err(S, ref["S"]) < 1e-4
 
 
+def _chunk_log_decay_spans(x, chunk, phi):
+    """-(sum of log gamma_t) over every chunk of every head, and the share of
+    tokens on the clamped branch, from the inputs by the step-size and clamp
+    definitions (test-data check only)."""
+    k = x["k"].double().cpu().numpy()
+    if phi == "l2":
+        k = k / np.maximum(np.linalg.norm(k, axis=-1, keepdims=True), 1e-12)
+    xs = np.zeros_like(k)
+    xs[..., 1:, :] = k[..., :-1, :]
+    if x.get("x_prev") is not None:
+        xs[..., 0, :] = x["x_prev"].double().cpu().numpy()
+    E = (xs ** 2).sum(-1)
+    beta, lam = x["beta"].double().cpu().numpy(), x["lambda"].double().cpu().numpy()
+    eta = beta / (E + lam + 1e-6)
+    if x.get("x_prev") is None:
+        eta[..., 0] = 0.0
+    a = np.minimum(eta * lam, 1.0 - 1e-6)
+    lg = np.log1p(-a)
+    T = lg.shape[-1]
+    pad = (-T) % chunk
+    lg = np.concatenate([lg, np.zeros(lg.shape[:-1] + (pad,))], -1)
+    spans = -lg.reshape(lg.shape[:-1] + (-1, chunk)).sum(-1)
+    return spans, float((eta * lam >= 1.0 - 1e-6).mean())
+
+
+@pytest.mark.parametrize("rule", ["falcon1", "falcon1a"])
+@pytest.mark.parametrize("m", [64, 128])
+def test_tensor_core_strong_decay(falcon, rule, m):
+    """bf16, m = d_v in {64, 128}, chunk 64 (the tensor-core forward) with gains
+    near 2 and ridges that make the clamp fire: head 0 keeps the workload's
+    mild ridge (chunk log-decay spans near 10: the factored decay form), heads
+    1 and 2 take lambda = softplus(n + 1) and softplus(n + 3) (spans far above
+    80: per-element decays of non-positive exponents).  Carried state and
+    x_prev, ragged T; o, S_T and x_last against the oracle."""
+    T = 4 * 64 + 29
+    x = workloads.random_case(1, 3, T, m, m, torch.bfloat16, seed=400 + m, device="cuda",
+                              with_state=True, with_x_prev=True)
+    g = torch.Generator().manual_seed(500 + m)
+    n_l = torch.randn((1, 3, T), generator=g)
+    shift = torch.tensor([-3.0, 1.0, 3.0]).view(1, 3, 1)
+    x["lambda"] = torch.nn.functional.softplus(n_l + shift).cuda()
+    x["beta"] = (1.9 + 0.09 * torch.tanh(torch.randn((1, 3, T), generator=g))).cuda()
+    spans, clamped = _chunk_log_decay_spans(x, 64, "l2")
+    assert spans[0, 0].max() < 80.0 and spans[0, 1:].min() > 80.0
+    assert clamped > 0.05
+    o, S, xl = run(falcon, rule, x, 64, "l2")
+    ref = ref_of(rule, x, "l2")
+    assert np.isfinite(o.numpy()).all() and np.isfinite(S.numpy()).all()
+    assert head_err(o, ref["o"]) < 2e-2
+    assert head_err(S, ref["S"]) < 2e-2
+    np.testing.assert_allclose(xl.numpy(), ref["x_last"], rtol=1e-6, atol=1e-6)
+
+
 def test_tiny_workload(falcon):
     """Falcon-1 tiny: B1 H2 T64 d16 fp32, phi = identity, lambda_1 = 0, C = 16."""
     w = workloads.TINY
@@ -114,51 +167,62 @@ def test_lm_workloads_all_heads(falcon, w):
     assert head_err(S, ref["S"]) < 2e-2
 
 
-def test_long_context_sampled_heads(falcon):
-    """B1 H16 T65536 d128 bf16 with lambda = softplus(n + 1): whole run on the
-    GPU, two heads recomputed by the oracle in full."""
+def test_long_context_all_heads(falcon):
+    """B1 H16 T65536 d128 bf16 with lambda = softplus(n + 1) (the decay
+    underflow stress case): whole run on the GPU, every head recomputed by the
+    oracle in full."""
+    import os
     w = workloads.LONG
     x = workloads.generate(w, device="cuda")
-    o, S, _ = run(falcon, w.rule, x, w.chunk, w.phi)
-    heads = [0, 11]
-    sub = {n: t[:, heads].cpu() for n, t in x.items()}
+    o, S, xl = run(falcon, w.rule, x, w.chunk, w.phi)
+    sub = {n: t.cpu() for n, t in x.items()}
     ref = oracle.forward(w.rule, sub["q"], sub["k"], sub["v"], sub["beta"], sub["lambda"],
-                         phi=w.phi, threads=2)
-    assert head_err(o[:, heads], ref["o"]) < 2e-2
-    assert head_err(S[:, heads], ref["S"]) < 2e-2
+                         phi=w.phi, threads=min(16, os.cpu_count() or 1))
     assert np.isfinite(o.numpy()).all()
+    assert head_err(o, ref["o"]) < 2e-2
+    assert head_err(S, ref["S"]) < 2e-2
+    np.testing.assert_allclose(xl.numpy(), ref["x_last"], rtol=1e-6, atol=1e-6)
 
 
-def test_decode_workload_sampled_states(falcon):
+def test_decode_workload_one_state_per_cta(falcon):
     """256 x 32 states, d128, fp32 state, 4096 bf16 steps; the first step is a
-    sequence start (sentinel).  Eight states are followed by the oracle."""
+    sequence start (sentinel).  The persistent kernel strides the states over
+    one CTA per SM, so the states followed by the oracle include one of every
+    CTA (at different depths of its stride) and the two of the ragged last
+    round; each is checked over all 4096 steps (the oracle runs them as
+    sequences: a decode loop from a fresh start is the sequence recurrence)."""
+    import os
     w = workloads.DECODE
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rounds = w.N // sms
+    pick = sorted({c + sms * (c % rounds) for c in range(sms)} | {w.N - 2, w.N - 1})
+    assert len(pick) >= sms
+    pick_d = torch.tensor(pick, device="cuda")
     stream = workloads.DecodeStream(w, device="cuda")
     S = stream.initial_state()
+    S0_pick = S[pick_d].cpu()
     xp = torch.zeros((w.N, w.m), device="cuda")
-    pick = torch.tensor([0, 1, 777, 2048, 4095, 5000, 8190, 8191])
-    S_ref = S[pick].double().cpu().numpy().copy()
-    xp_ref = np.zeros((len(pick), w.m))
     fresh_all = torch.ones(w.N, dtype=torch.uint8, device="cuda")
-    o_err_num = np.zeros(len(pick))
-    o_err_den = np.zeros(len(pick))
+    seq = {n: [] for n in ("q", "k", "v", "beta", "lambda")}
+    outs = []
     for s in range(w.steps):
         x = stream.step()
         o = falcon.falcon1_decode_step(x["q"], x["k"], x["v"], x["beta"], x["lambda"], S, xp,
                                        fresh=fresh_all if s == 0 else None, phi=w.phi,
                                        eps=w.eps, eps_gamma=w.eps_gamma)
-        sub = {n: t[pick.cuda()].cpu() for n, t in x.items()}
-        o_ref = oracle.decode_step("falcon1", sub["q"], sub["k"], sub["v"], sub["beta"],
-                                   sub["lambda"], S_ref, xp_ref,
-                                   fresh=np.full(len(pick), s == 0), phi=w.phi, eps=w.eps,
-                                   eps_gamma=w.eps_gamma)
-        og = o[pick.cuda()].double().cpu().numpy()
-        o_err_num += ((og - o_ref) ** 2).sum(1)
-        o_err_den += (o_ref ** 2).sum(1)
+        for n in seq:
+            seq[n].append(x[n][pick_d])
+        outs.append(o[pick_d])
     assert falcon.falcon_sync_check() == 0
-    assert np.sqrt(o_err_num / o_err_den).max() < 2e-2
-    assert head_err(S[pick].cpu(), S_ref) < 2e-2
-    np.testing.assert_allclose(xp[pick].cpu().numpy(), xp_ref, rtol=1e-5, atol=1e-6)
+    # [P, steps, ...]: one sequence per followed state
+    seqs = {n: torch.stack(t, 1).cpu() for n, t in seq.items()}
+    o_got = torch.stack(outs, 1).float().cpu()
+    ref = oracle.forward("falcon1", seqs["q"], seqs["k"], seqs["v"], seqs["beta"],
+                         seqs["lambda"], S0=S0_pick, phi=w.phi, eps=w.eps,
+                         eps_gamma=w.eps_gamma, threads=min(16, os.cpu_count() or 1))
+    assert head_err(o_got, ref["o"]) < 2e-2
+    assert head_err(S[pick_d].cpu(), ref["S"]) < 2e-2
+    np.testing.assert_allclose(xp[pick_d].cpu().numpy(), ref["x_last"], rtol=1e-5, atol=1e-6)
 
 
 @pytest.mark.parametrize("rule", ["falcon1", "falcon1a"])

@@ -77,8 +77,22 @@ def test_masked_attention_form(B, lam_shift, phi):
                     M += eta[b, s] / Bs[s] * np.prod(gam[b, s + 1:t + 1])
                 acc = acc + M * (qf[b, t] @ x[b, j]) * v[b, j]
             want[b, t] = acc
+    # The final state in the same form: S_T = delta_T S0 + sum_j M_{T,j} x_j v_j^T,
+    # the mask row of the last token (the read o_T = S_T^T phi(q_T) pins it only
+    # along phi(q_T)).
+    want_S = np.zeros((BH,) + S0.shape[1:])
+    for b in range(BH):
+        t = T - 1
+        acc = np.prod(gam[b, :t + 1]) * S0[b]
+        for j in range(1, t + 1):
+            M = 0.0
+            for s in range(j, min(t, j + B - 1) + 1):
+                M += eta[b, s] / Bs[s] * np.prod(gam[b, s + 1:t + 1])
+            acc = acc + M * np.outer(x[b, j], v[b, j])
+        want_S[b] = acc
     got = oracle.forward3a(q, k, v, beta, lam, B, S0=S0, phi=phi, eps=eps, eps_gamma=eg)
     np.testing.assert_allclose(got["o"], want, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(got["S"], want_S, rtol=1e-10, atol=1e-12)
 
 
 @pytest.mark.parametrize("B", [1, 4])
