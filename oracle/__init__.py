@@ -73,6 +73,10 @@ def _load():
             lib.falcon_oracle_backward.argtypes = [
                 ctypes.c_int, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_double, ctypes.c_double] + [d] * 17 + [ctypes.c_int]
+            lib.falcon1a_oracle_forward_normalized.restype = ctypes.c_int
+            lib.falcon1a_oracle_forward_normalized.argtypes = [
+                i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_double, ctypes.c_double, ctypes.c_double] + [d] * 12 + [ctypes.c_int]
             lib.falcon_oracle_decode_step.restype = ctypes.c_int
             lib.falcon_oracle_decode_step.argtypes = [
                 ctypes.c_int, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -233,6 +237,37 @@ def forward3a(q, k, v, beta, lam, window, S0=None, phi="l2", eps=1e-6, eps_gamma
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (rc={rc})")
     return {"o": o, "S": S, "x_last": x_last}
+
+
+def forward_normalized(q, k, v, beta, lam, S0=None, z0=None, x_prev=None, phi="l2",
+                       eps=1e-6, eps_gamma=1e-6, eps_attn=1e-6, threads=None, ridge="given"):
+    """Falcon-1A with the normalised read o_t = S_t^T phi(q_t) / (z_t^T phi(q_t)
+    + eps_attn), z_t = gamma_t z_{t-1} + eta_t x_t (Section 2.2, Eq. (2.1)-(2.3),
+    with the Falcon-1A gain and decay on the normaliser).  Shapes as in
+    ``forward``; z0 [..., m] or None (zeros).  Returns o, S, z and x_last."""
+    lib = _load()
+    q, k, v, beta, lam = (_f64(t) for t in (q, k, v, beta, lam))
+    S0, z0, x_prev = _f64(S0), _f64(z0), _f64(x_prev)
+    lead = q.shape[:-2]
+    T, m = q.shape[-2], q.shape[-1]
+    dv = v.shape[-1]
+    BH = int(np.prod(lead)) if lead else 1
+    assert k.shape == q.shape and v.shape == lead + (T, dv)
+    assert beta.shape == lead + (T,) and lam.shape == lead + (T,)
+    for name, t, shp in (("S0", S0, lead + (m, dv)), ("z0", z0, lead + (m,)),
+                         ("x_prev", x_prev, lead + (m,))):
+        assert t is None or t.shape == shp, name
+    o = np.zeros(lead + (T, dv))
+    S = np.zeros(lead + (m, dv))
+    z = np.zeros(lead + (m,))
+    x_last = np.zeros(lead + (m,))
+    rc = lib.falcon1a_oracle_forward_normalized(
+        BH, T, m, dv, _PHIS[phi], _RIDGES[ridge], eps, eps_gamma, eps_attn, _ptr(q), _ptr(k),
+        _ptr(v), _ptr(beta), _ptr(lam), _ptr(S0), _ptr(z0), _ptr(x_prev), _ptr(o), _ptr(S),
+        _ptr(z), _ptr(x_last), int(threads or os.cpu_count() or 1))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (rc={rc})")
+    return {"o": o, "S": S, "z": z, "x_last": x_last}
 
 
 def decode_step(rule, q, k, v, beta, lam, S, x_prev, fresh=None, phi="l2",

@@ -46,6 +46,14 @@
  *     RMSNorm with eps_rms = 1e-6 (the pages name eps_rms without a value);
  *   - a caller that carries state across calls passes x_prev = phi(k_T) of the
  *     previous segment; then step 1 writes with x_1 = x_prev (no sentinel).
+ *
+ *   - the normalised read (falcon1a_oracle_forward_normalized): Section 2.2,
+ *     Eq. (2.1)-(2.3) define o_t = S_t^T phi(q_t) / (z_t^T phi(q_t) + eps_attn)
+ *     with an additive normaliser z_t = z_{t-1} + x_t on the shifted stream;
+ *     the Falcon-1A version is deferred to an appendix the pages do not
+ *     include.  Reading taken: z follows the numerator's update with a
+ *     constant unit target, z_t = gamma_t z_{t-1} + eta_t x_t (the same gain
+ *     and clamped decay), which is Eq. (2.3) exactly at lambda = 0, eta = 1.
  */
 #include <math.h>
 #include <pthread.h>
@@ -728,6 +736,105 @@ int falcon_oracle_backward(int rule, int64_t BH, int64_t T, int m, int dv, int p
   }
   for (int w = 1; w < nthreads; ++w) pthread_create(&tid[w], NULL, backward_worker, &sl[w]);
   backward_worker(&sl[0]);
+  for (int w = 1; w < nthreads; ++w) pthread_join(tid[w], NULL);
+  free(tid);
+  free(sl);
+  return 0;
+}
+
+/* ---- Falcon-1A with the normalised read -------------------------------- */
+typedef struct {
+  int m, dv, phi, ridge;
+  int64_t T;
+  double eps, eps_gamma, eps_attn;
+  const double *q, *k, *v, *beta, *lambda, *S0, *z0, *x_prev;
+  double *o, *S_out, *z_out, *x_last;
+} fwdn_args;
+
+/* One head: the Falcon-1A token loop of forward_head, plus the normaliser
+ * z_t = gamma_t z_{t-1} + eta_t x_t and the division of the read. */
+static void forward_norm_head(const fwdn_args *a, int64_t bh) {
+  const int m = a->m, dv = a->dv;
+  const int64_t T = a->T;
+  double *S = (double *)calloc((size_t)m * dv, sizeof(double));
+  double *z = (double *)calloc((size_t)m, sizeof(double));
+  double *x = (double *)calloc((size_t)m, sizeof(double));
+  double *qf = (double *)malloc(sizeof(double) * (size_t)m);
+  double *r = (double *)malloc(sizeof(double) * (size_t)dv);
+  if (a->S0) memcpy(S, a->S0 + bh * m * dv, sizeof(double) * (size_t)m * dv);
+  if (a->z0) memcpy(z, a->z0 + bh * m, sizeof(double) * (size_t)m);
+  int sentinel = 1;
+  if (a->x_prev) {
+    memcpy(x, a->x_prev + bh * m, sizeof(double) * (size_t)m);
+    sentinel = 0;
+  }
+  for (int64_t t = 0; t < T; ++t) {
+    const int64_t row = bh * T + t;
+    double eta, gamma;
+    step_scalars(sentinel && t == 0, m, x, a->beta[row], a->lambda[row], a->ridge,
+                 a->eps, a->eps_gamma, &eta, &gamma);
+    feature_map(a->phi, m, a->q + row * m, qf);
+    /* numerator: the Falcon-1A update and read (into o_t) */
+    double *o = a->o + row * dv;
+    one_token(ORACLE_FALCON1A, m, dv, S, x, qf, a->v + row * dv, eta, gamma, r, o);
+    /* normaliser, then the read's denominator */
+    double den = 0.0;
+    for (int i = 0; i < m; ++i) {
+      z[i] = gamma * z[i] + eta * x[i];
+      den += z[i] * qf[i];
+    }
+    den += a->eps_attn;
+    for (int j = 0; j < dv; ++j) o[j] /= den;
+    feature_map(a->phi, m, a->k + row * m, x);
+  }
+  if (a->S_out) memcpy(a->S_out + bh * m * dv, S, sizeof(double) * (size_t)m * dv);
+  if (a->z_out) memcpy(a->z_out + bh * m, z, sizeof(double) * (size_t)m);
+  if (a->x_last) memcpy(a->x_last + bh * m, x, sizeof(double) * (size_t)m);
+  free(S);
+  free(z);
+  free(x);
+  free(qf);
+  free(r);
+}
+
+typedef struct {
+  const fwdn_args *a;
+  int64_t begin, end;
+} fwdn_slice;
+
+static void *forward_norm_worker(void *p) {
+  const fwdn_slice *s = (const fwdn_slice *)p;
+  for (int64_t bh = s->begin; bh < s->end; ++bh) forward_norm_head(s->a, bh);
+  return NULL;
+}
+
+/*
+ * Falcon-1A with the normalised read o_t = S_t^T phi(q_t) / (z_t^T phi(q_t) +
+ * eps_attn), z_t = gamma_t z_{t-1} + eta_t x_t.  Layouts as in
+ * falcon_oracle_forward; z0 (nullable => zeros) and z_out (nullable): [BH, m].
+ * Returns 0, or -1 on a bad argument.
+ */
+int falcon1a_oracle_forward_normalized(int64_t BH, int64_t T, int m, int dv, int phi, int ridge,
+                                       double eps, double eps_gamma, double eps_attn,
+                                       const double *q, const double *k, const double *v,
+                                       const double *beta, const double *lambda,
+                                       const double *S0, const double *z0, const double *x_prev,
+                                       double *o, double *S_out, double *z_out, double *x_last,
+                                       int nthreads) {
+  if (BH < 0 || T < 0 || m <= 0 || dv <= 0) return -1;
+  fwdn_args a = {m, dv, phi, ridge, T, eps, eps_gamma, eps_attn, q, k, v, beta, lambda,
+                 S0, z0, x_prev, o, S_out, z_out, x_last};
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > BH) nthreads = (int)(BH > 0 ? BH : 1);
+  pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+  fwdn_slice *sl = (fwdn_slice *)malloc(sizeof(fwdn_slice) * (size_t)nthreads);
+  for (int w = 0; w < nthreads; ++w) {
+    sl[w].a = &a;
+    sl[w].begin = BH * w / nthreads;
+    sl[w].end = BH * (w + 1) / nthreads;
+  }
+  for (int w = 1; w < nthreads; ++w) pthread_create(&tid[w], NULL, forward_norm_worker, &sl[w]);
+  forward_norm_worker(&sl[0]);
   for (int w = 1; w < nthreads; ++w) pthread_join(tid[w], NULL);
   free(tid);
   free(sl);
