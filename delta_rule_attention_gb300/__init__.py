@@ -39,6 +39,7 @@ EXPORTS = (
     "falcon_selftest_wait_timeout", "falcon2_fwd_recurrent", "falcon2a_fwd_recurrent",
     "falcon3a_fwd_recurrent", "falcon_bwd_workspace_bytes", "falcon1_bwd_chunked",
     "falcon1a_bwd_chunked", "falcon3a_fwd_chunked", "falcon2a_fwd_chunked",
+    "falcon_normalized_workspace_bytes", "falcon1a_fwd_chunked_normalized",
 )
 FALCON_ERR_SCRATCH_LIMIT = -10
 FALCON_FIXED_SCRATCH_BYTES = 16 * 1024 * 1024
@@ -82,6 +83,12 @@ def load_library(path: str | None = None):
             fn = getattr(lib, name)
             fn.restype = ctypes.c_int
             fn.argtypes = [shp, vp, vp, vp, f32p, f32p, f32p, f32p, vp, f32p, f32p, vp, sz, vp]
+        lib.falcon_normalized_workspace_bytes.restype = sz
+        lib.falcon_normalized_workspace_bytes.argtypes = [shp]
+        lib.falcon1a_fwd_chunked_normalized.restype = ctypes.c_int
+        lib.falcon1a_fwd_chunked_normalized.argtypes = [
+            shp, vp, vp, vp, f32p, f32p, f32p, f32p, f32p, ctypes.c_float, vp, f32p, f32p, f32p,
+            vp, sz, vp]
         lib.falcon_bwd_workspace_bytes.restype = sz
         lib.falcon_bwd_workspace_bytes.argtypes = [shp]
         for name in ("falcon1_bwd_chunked", "falcon1a_bwd_chunked"):
@@ -260,6 +267,55 @@ def falcon1a_fwd_chunked(q, k, v, beta, lam, S0=None, x_prev=None, chunk=64, phi
     """Falcon-1A chunk-parallel forward; arguments as falcon1_fwd_chunked."""
     return _fwd("falcon1a_fwd_chunked", q, k, v, beta, lam, S0, x_prev, chunk, phi, eps,
                 eps_gamma, **kw)
+
+
+def falcon_normalized_workspace_bytes(shape: falcon_shape) -> int:
+    return int(load_library().falcon_normalized_workspace_bytes(ctypes.byref(shape)))
+
+
+def falcon1a_fwd_chunked_normalized(q, k, v, beta, lam, S0=None, z0=None, x_prev=None,
+                                    eps_attn=1e-6, chunk=64, phi="l2", eps=1e-6, eps_gamma=1e-6,
+                                    o=None, S_out=None, z_out=None, x_last=None, workspace=None,
+                                    stream=None, ridge="given"):
+    """Falcon-1A forward with the normalised read o_t = S_t^T phi(q_t) /
+    (z_t^T phi(q_t) + eps_attn), z_t = gamma_t z_{t-1} + eta_t x_t.  Arguments
+    as falcon1a_fwd_chunked, plus z0 [B,H,m] fp32 or None.  Returns
+    (o, S_T, z_T, x_last)."""
+    lib = load_library()
+    _need(q, "q")
+    B, H, T, m = q.shape
+    dv = v.shape[-1]
+    dt = q.dtype
+    if dt not in _DTYPE:
+        raise TypeError("q, k, v must be bfloat16 or float32")
+    _need(k, "k", dt, (B, H, T, m))
+    _need(v, "v", dt, (B, H, T, dv))
+    _need(beta, "beta", torch.float32, (B, H, T))
+    _need(lam, "lambda", torch.float32, (B, H, T))
+    for t, name, shp in ((S0, "S0", (B, H, m, dv)), (z0, "z0", (B, H, m)),
+                         (x_prev, "x_prev", (B, H, m))):
+        if t is not None:
+            _need(t, name, torch.float32, shp)
+    dev = q.device
+    if o is None:
+        o = torch.empty((B, H, T, dv), dtype=dt, device=dev)
+    if S_out is None:
+        S_out = torch.empty((B, H, m, dv), dtype=torch.float32, device=dev)
+    if z_out is None:
+        z_out = torch.empty((B, H, m), dtype=torch.float32, device=dev)
+    if x_last is None:
+        x_last = torch.empty((B, H, m), dtype=torch.float32, device=dev)
+    shape = make_shape(B, H, T, m, dv, chunk, dt, phi, eps, eps_gamma, ridge)
+    need = int(lib.falcon_normalized_workspace_bytes(ctypes.byref(shape)))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.falcon1a_fwd_chunked_normalized(
+        ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(lam), _ptr(S0),
+        _ptr(z0), _ptr(x_prev), float(eps_attn), _ptr(o), _ptr(S_out), _ptr(z_out),
+        _ptr(x_last), _ptr(workspace), ws_bytes, _stream(stream))
+    _check(rc, "falcon1a_fwd_chunked_normalized")
+    return o, S_out, z_out, x_last
 
 
 def falcon_bwd_workspace_bytes(shape: falcon_shape) -> int:

@@ -1,6 +1,7 @@
 // C ABI of the library (declared in include/falcon.h): argument checks, the
 // zero-length cases, and dispatch to the kernels.  Nothing is launched when an
 // argument is rejected.
+#include <math.h>
 #include <stdint.h>
 
 #include <mutex>
@@ -344,6 +345,73 @@ int falcon1a_fwd_chunked(const falcon_shape* s, const void* q, const void* k, co
                      workspace, workspace_bytes, stream);
 }
 
+// The normalised read's own workspace follows the forward's, 256-byte aligned.
+static size_t norm_offset(const falcon_shape* s) {
+  return (falcon_workspace_bytes(s) + 255) / 256 * 256;
+}
+
+size_t falcon_normalized_workspace_bytes(const falcon_shape* s) {
+  if (check_shape(s) != FALCON_OK) return 0;
+  if (s->B * s->H == 0 || s->T == 0) return falcon_workspace_bytes(s);
+  return norm_offset(s) + falcon::norm_workspace_bytes(s->B * s->H, s->T, s->m, s->chunk);
+}
+
+int falcon1a_fwd_chunked_normalized(const falcon_shape* s, const void* q, const void* k,
+                                    const void* v, const float* beta, const float* lambda,
+                                    const float* S0, const float* z0, const float* x_prev,
+                                    float eps_attn, void* o, float* S_out, float* z_out,
+                                    float* x_last, void* workspace, size_t workspace_bytes,
+                                    cudaStream_t stream) {
+  int rc = check_shape(s);
+  if (rc) return rc;
+  if (!(eps_attn >= 0.f) || !(eps_attn < INFINITY)) return FALCON_ERR_BAD_ARG;
+  const int64_t BH = s->B * s->H;
+  if (BH == 0) return FALCON_OK;
+  if (misaligned(z0) || misaligned(z_out)) return FALCON_ERR_MISALIGNED;
+  const size_t need = falcon_normalized_workspace_bytes(s);
+  if (s->T > 0 && need > 0 && (!workspace || workspace_bytes < need)) return FALCON_ERR_WORKSPACE;
+  // The numerator: the Falcon-1A forward (every remaining check is its own;
+  // nothing is launched when one fails).
+  const size_t base = s->T > 0 ? norm_offset(s) : workspace_bytes;
+  rc = fwd_chunked(falcon::kFalcon1A, s, q, k, v, beta, lambda, S0, x_prev, o, S_out, x_last,
+                   workspace, base, stream);
+  if (rc) return rc;
+  const size_t feat_bytes = sizeof(float) * (size_t)BH * s->m;
+  if (s->T == 0) {  // z_T = z0
+    cudaError_t e = cudaSuccess;
+    if (z_out && z0 && z_out != z0)
+      e = cudaMemcpyAsync(z_out, z0, feat_bytes, cudaMemcpyDeviceToDevice, stream);
+    else if (z_out && !z0)
+      e = cudaMemsetAsync(z_out, 0, feat_bytes, stream);
+    return to_status(e);
+  }
+  ChunkArgs a;
+  a.rule = falcon::kFalcon1A;
+  a.BH = BH;
+  a.T = s->T;
+  a.m = s->m;
+  a.dv = s->dv;
+  a.C = s->chunk;
+  a.dtype = s->dtype;
+  a.phi = s->phi;
+  a.ridge = s->ridge;
+  a.eps = s->eps;
+  a.eps_gamma = s->eps_gamma;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.beta = beta;
+  a.lambda = lambda;
+  a.S0 = S0;
+  a.x_prev = x_prev;
+  a.o = o;
+  a.S_out = S_out;
+  a.x_last = x_last;
+  a.workspace = workspace;
+  float* ws = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + base);
+  return to_status(falcon::launch_normalizer(a, z0, z_out, eps_attn, ws, stream));
+}
+
 size_t falcon_bwd_workspace_bytes(const falcon_shape* s) {
   if (check_shape(s) != FALCON_OK) return 0;
   return falcon::bwd_workspace_bytes(s->dtype, s->B * s->H, s->T, s->m, s->dv, s->chunk);
@@ -461,7 +529,9 @@ const char* falcon_strerror(int code) {
     case FALCON_ERR_WORKSPACE: return "workspace missing or too small";
     case FALCON_ERR_CUDA: return "CUDA launch or query failed";
     case FALCON_ERR_TIMEOUT: return "a device-side wait hit its iteration limit";
-    case FALCON_ERR_BAD_ARG: return "eps must be >= 0 and eps_gamma in (0, 1)";
+    case FALCON_ERR_BAD_ARG:
+      return "a scalar argument is out of range (eps >= 0, eps_gamma in (0, 1), eps_attn >= 0, "
+             "window, wait limit)";
     case FALCON_ERR_DEVICE: return "current device is not sm_103 (GB300)";
     case FALCON_ERR_SCRATCH_LIMIT:
       return "problem needs more scratch than the library's fixed array (FALCON_FIXED_SCRATCH_BYTES)";

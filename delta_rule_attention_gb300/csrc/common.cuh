@@ -139,6 +139,13 @@ cudaError_t launch_tc_bwd_grad(const BwdArgs& b, const float* S_starts, const fl
 cudaError_t launch_tc_bwd_scan(const BwdArgs& b, const void* maps, float* dS_ends, int* err,
                                cudaStream_t stream);
 
+// Falcon-1A's normalised read: the denominator z_t^T phi(q_t) + eps_attn
+// (z_t = gamma_t z_{t-1} + eta_t x_t) and the division of o in place, after
+// the Falcon-1A forward has written o.  ws: norm_workspace_bytes bytes.
+size_t norm_workspace_bytes(int64_t BH, int64_t T, int m, int C);
+cudaError_t launch_normalizer(const ChunkArgs& a, const float* z0, float* z_out, float eps_attn,
+                              float* ws, cudaStream_t stream);
+
 struct DecodeArgs {
   int rule;
   int64_t N;

@@ -69,7 +69,7 @@ extern "C" {
 #define FALCON_ERR_WORKSPACE (-5)  /* workspace NULL or smaller than required */
 #define FALCON_ERR_CUDA (-6)       /* a CUDA launch or query failed */
 #define FALCON_ERR_TIMEOUT (-7)    /* a device-side wait hit its limit */
-#define FALCON_ERR_BAD_ARG (-8)    /* eps/eps_gamma out of range */
+#define FALCON_ERR_BAD_ARG (-8)    /* eps/eps_gamma (or another scalar argument) out of range */
 #define FALCON_ERR_DEVICE (-9)     /* the current device is not sm_103 */
 #define FALCON_ERR_SCRATCH_LIMIT (-10) /* needs more than FALCON_FIXED_SCRATCH_BYTES */
 
@@ -190,6 +190,36 @@ int falcon1a_fwd_chunked(const falcon_shape *shape, const void *q,
                          const float *x_prev, void *o, float *S_out,
                          float *x_last, void *workspace, size_t workspace_bytes,
                          cudaStream_t stream);
+
+/* Falcon-1A with the normalised read (Section 2.2, Eq. (2.1)-(2.3): the
+ * normaliser z_t of linear attention on the shifted write stream):
+ *     o_t = S_t^T phi(q_t) / (z_t^T phi(q_t) + eps_attn),
+ *     z_t = gamma_t z_{t-1} + eta_t x_t,
+ * with S_t the Falcon-1A state and z taking the same step size eta_t and
+ * clamped decay gamma_t as the numerator.  The pages define z for plain linear
+ * attention (lambda = 0, unit gain, where this is their Eq. (2.3) exactly) and
+ * defer the Falcon-1A version to an appendix they do not include; this is the
+ * plainest reading.  The denominator is not clamped away from zero (the pages
+ * note that the normalised read is attention-like only for a nonnegative
+ * normaliser): callers with signed features choose eps_attn accordingly.
+ *   z0      [B,H,m] f32, normaliser entering token 1; NULL means zeros
+ *   z_out   [B,H,m] f32, out, nullable: z_T (may alias z0)
+ *   eps_attn >= 0 and finite (FALCON_ERR_BAD_ARG otherwise)
+ *   workspace: at least falcon_normalized_workspace_bytes(shape) bytes.
+ * Other arguments, layouts, ownership and errors are those of
+ * falcon1a_fwd_chunked (o holds the normalised read).  The call runs the
+ * Falcon-1A forward and then three plain kernels for the denominator (ordinary
+ * launches: they start after the forward's kernels complete). */
+size_t falcon_normalized_workspace_bytes(const falcon_shape *shape);
+int falcon1a_fwd_chunked_normalized(const falcon_shape *shape, const void *q,
+                                    const void *k, const void *v,
+                                    const float *beta, const float *lambda,
+                                    const float *S0, const float *z0,
+                                    const float *x_prev, float eps_attn,
+                                    void *o, float *S_out, float *z_out,
+                                    float *x_last, void *workspace,
+                                    size_t workspace_bytes,
+                                    cudaStream_t stream);
 
 /* Bytes of device workspace falcon1_bwd_chunked / falcon1a_bwd_chunked need
  * for this shape (0 for an invalid shape; the call then reports the error). */

@@ -1,5 +1,6 @@
 """Host-side argument checks of the Falcon-2, Falcon-2A and Falcon-3A entry
-points and of the fixed-scratch Falcon-1 forward (no GPU needed).
+points, of the fixed-scratch Falcon-1 forward and of Falcon-1A with the
+normalised read (no GPU needed).
 
 Every call here is invalid in exactly one argument, so each must come back
 with that argument's error code before any device is touched; a valid call
@@ -61,11 +62,15 @@ P, ODD = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x10008)
 BIG = ctypes.c_size_t(1 << 40)
 
 
-def _call(lib, name, s, q=P, S0=None, x_prev=None, S_out=P, ws=P, wsb=BIG, window=4):
+def _call(lib, name, s, q=P, S0=None, x_prev=None, S_out=P, ws=P, wsb=BIG, window=4,
+          z0=None, z_out=None, eps_attn=1e-6):
     """Call `name` with the argument order of its declaration; pointers not
     given are valid-looking fake addresses."""
     f = getattr(lib, name)
     sp = ctypes.byref(s) if s is not None else None
+    if name == "falcon1a_fwd_chunked_normalized":
+        return f(sp, q, P, P, P, P, S0, z0, x_prev, ctypes.c_float(eps_attn), P, S_out, z_out,
+                 None, ws, wsb, None)
     if name in ("falcon2_fwd_recurrent", "falcon2a_fwd_recurrent"):
         return f(sp, q, P, P, P, P, S0, x_prev, P, S_out, None, None)
     if name == "falcon2a_fwd_chunked":
@@ -80,7 +85,8 @@ def _call(lib, name, s, q=P, S0=None, x_prev=None, S_out=P, ws=P, wsb=BIG, windo
 
 
 VARIANTS = ["falcon2_fwd_recurrent", "falcon2a_fwd_recurrent", "falcon2a_fwd_chunked",
-            "falcon3a_fwd_recurrent", "falcon3a_fwd_chunked", "falcon1_fwd_chunked_fixed_scratch"]
+            "falcon3a_fwd_recurrent", "falcon3a_fwd_chunked", "falcon1_fwd_chunked_fixed_scratch",
+            "falcon1a_fwd_chunked_normalized"]
 
 
 @pytest.mark.parametrize("name", VARIANTS)
@@ -108,7 +114,8 @@ def test_variants_with_no_heads_touch_nothing(lib, name):
 
 
 @pytest.mark.parametrize("name", ["falcon2_fwd_recurrent", "falcon2a_fwd_recurrent",
-                                  "falcon2a_fwd_chunked", "falcon1_fwd_chunked_fixed_scratch"])
+                                  "falcon2a_fwd_chunked", "falcon1_fwd_chunked_fixed_scratch",
+                                  "falcon1a_fwd_chunked_normalized"])
 def test_misaligned_x_prev_is_rejected(lib, name):
     assert _call(lib, name, _shape(), x_prev=ODD) == MISALIGNED
 
@@ -156,3 +163,21 @@ def test_fixed_scratch_codes_match_the_workspace_entry_point(lib):
         want = regular(**c)
         assert want < 0, c
         assert _call(lib, "falcon1_fwd_chunked_fixed_scratch", **c) == want, c
+
+
+@pytest.mark.parametrize("eps_attn", [-1e-3, float("nan"), float("inf")])
+def test_normalized_read_rejects_bad_eps_attn(lib, eps_attn):
+    assert _call(lib, "falcon1a_fwd_chunked_normalized", _shape(), eps_attn=eps_attn) == BAD_ARG
+
+
+def test_normalized_read_checks_its_state_and_workspace(lib):
+    name = "falcon1a_fwd_chunked_normalized"
+    assert _call(lib, name, _shape(), z0=ODD) == MISALIGNED
+    assert _call(lib, name, _shape(), z_out=ODD) == MISALIGNED
+    s = _shape()
+    need = lib.falcon_normalized_workspace_bytes(ctypes.byref(s))
+    # room for the denominator beyond the forward's own workspace
+    assert need > lib.falcon_workspace_bytes(ctypes.byref(s)) > 0
+    assert _call(lib, name, s, wsb=ctypes.c_size_t(need - 1)) == WORKSPACE
+    assert _call(lib, name, s, ws=None) == WORKSPACE
+    assert lib.falcon_normalized_workspace_bytes(ctypes.byref(_shape(m=24))) == 0
