@@ -171,9 +171,12 @@ __device__ __forceinline__ uint32_t dblk_chunk(int r, int c) {
 // stored).  d_blk (2 KB) receives the unscaled diagonal blocks of T as bf16,
 // which the strips below read.
 //
-// Diagonal block b = warp & 3 is inverted in fp32 by forward substitution:
-// warp w owns columns 8 (w >> 2) .. +7 of the block, two lanes per row with
-// four columns each, and broadcasts finished rows by shuffles.  Below it,
+// Diagonal block b is inverted in fp32 by forward substitution, one thread
+// per column (threads 0..63: block tid / 16, column tid % 16): going down the
+// column, t_i = delta_ij - sum_{k<i} A_ik t_k with the fused multiply-adds in
+// the order k = 0, 1, ..., the rows of A broadcast from shared memory; the
+// other warps have no part in it.
+// Below it,
 // T_{b,<b} = T_bb (-A_{b,<b} T_{<b}) splits into independent 8-column strips:
 // strip n (columns 8n .. 8n+7, n = 0..5) of block row b needs only strip n of
 // the block rows above it.  Warp n runs its
@@ -190,33 +193,30 @@ __device__ void solve_unit_lower_sw(const unsigned char* a_tile, const float* a_
                                     unsigned char* t_tile, unsigned char* d_blk,
                                     const float* col_scale) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  {
-    const int b = warp & 3, hh = warp >> 2, rr = lane >> 1, q = lane & 1, row = 16 * b + rr;
-    float arow[15];
+  if (tid < 64) {
+    const int b = tid >> 4, j = tid & 15;
+    const float* L = a_diag + 16 * b * kLdD;
+    float t[16];
 #pragma unroll
-    for (int k = 0; k < 15; ++k) arow[k] = a_diag[row * kLdD + k];
-    float dv4[4];
+    for (int i = 0; i < 16; ++i) {
+      float acc = (i == j) ? 1.f : 0.f;
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj) dv4[jj] = (8 * hh + 4 * q + jj == rr) ? 1.f : 0.f;
-#pragma unroll
-    for (int k = 0; k < 15; ++k) {
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const float tkj = __shfl_sync(0xffffffffu, dv4[jj], 2 * k + q);
-        if (rr > k) dv4[jj] -= arow[k] * tkj;
-      }
+      for (int k = 0; k < i; ++k) acc = fmaf(-L[i * kLdD + k], t[k], acc);
+      t[i] = acc;
     }
-    // Columns 16b + 8hh + 4q .. +3 of the row (unscaled into d_blk, scaled into
-    // t_tile); the four threads of a row zero the chunks right of the block.
-    *reinterpret_cast<uint2*>(d_blk + dblk_chunk(row, hh) + 8 * q) =
-        make_uint2(pack_bf16(dv4[0], dv4[1]), pack_bf16(dv4[2], dv4[3]));
-    const float4 cs = kScaled
-                          ? *reinterpret_cast<const float4*>(col_scale + 16 * b + 8 * hh + 4 * q)
-                          : make_float4(1.f, 1.f, 1.f, 1.f);
-    *reinterpret_cast<uint2*>(t_tile + sw_chunk(row, 2 * b + hh) + 8 * q) = make_uint2(
-        pack_bf16(dv4[0] * cs.x, dv4[1] * cs.y), pack_bf16(dv4[2] * cs.z, dv4[3] * cs.w));
-    for (int z = 2 * b + 2 + 2 * hh + q; z < 8; z += 4)
-      *reinterpret_cast<uint4*>(t_tile + sw_chunk(row, z)) = make_uint4(0u, 0u, 0u, 0u);
+    // Column j of T_bb: unscaled into d_blk, scaled into t_tile; each thread
+    // also zeroes the chunks of row 16 b + j right of the diagonal block.
+    const float cs = kScaled ? col_scale[16 * b + j] : 1.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int row = 16 * b + i;
+      *reinterpret_cast<__nv_bfloat16*>(d_blk + dblk_chunk(row, j >> 3) + 2 * (j & 7)) =
+          __float2bfloat16_rn(t[i]);
+      *reinterpret_cast<__nv_bfloat16*>(t_tile + sw_chunk(row, 2 * b + (j >> 3)) +
+                                        2 * (j & 7)) = __float2bfloat16_rn(t[i] * cs);
+    }
+    for (int z = 2 * b + 2; z < 8; ++z)
+      *reinterpret_cast<uint4*>(t_tile + sw_chunk(16 * b + j, z)) = make_uint4(0u, 0u, 0u, 0u);
   }
   __syncthreads();  // diagonal blocks of T complete
   if (warp < 6) {
