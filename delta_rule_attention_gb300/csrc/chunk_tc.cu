@@ -408,22 +408,33 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
     store_half_sw(xt_tile + (1 - j) * L::kAtom, r, h, xo, xs);
   }
   {
-    float d[32];
-    tmem_ld32(tlane + 32 * h, d);
-    // Factored decay: one row factor (phi's scale of row r times fv or fw) and
-    // one column factor cu_l = fu_l phi-scale(x_l); otherwise the cosines first
-    // (bounded), then per-element exponentials of non-positive arguments.
-    if (!factored) {
+    // This warp's half rows may lie wholly above the diagonal (columns 32..63
+    // of rows 0..31, warp-uniform): A there is never read by the solve and P
+    // there is zero, so the warp skips the accumulator.
+    const bool above = h == 1 && (warp & 1) == 0;
+    if (r >= 64 && above) {
 #pragma unroll
-      for (int l = 0; l < 32; ++l) d[l] = (d[l] * nr) * sc.nrm[32 * h + l];
-    }
-    if (r < 64) {
-      // A row r: eta_r e^{g_{r-1} - g_l} <x_r, x_l> for l < r (computed, then stored)
-      if (f1) {
+      for (int cc = 0; cc < 4; ++cc)
+        *reinterpret_cast<uint4*>(p_tile + sw_chunk(r - 64, 4 * h + cc)) =
+            make_uint4(0u, 0u, 0u, 0u);
+    } else if (!above && (r >= 64 || f1)) {
+      float d[32];
+      tmem_ld32(tlane + 32 * h, d);
+      // Factored decay: one row factor (phi's scale of row r times fv or fw)
+      // and one column factor cu_l = fu_l phi-scale(x_l); otherwise the cosines
+      // first (bounded), then per-element exponentials of non-positive
+      // arguments.
+      if (!factored) {
+#pragma unroll
+        for (int l = 0; l < 32; ++l) d[l] = (d[l] * nr) * sc.nrm[32 * h + l];
+      }
+      if (r < 64) {
+        // A row r: eta_r e^{g_{r-1} - g_l} <x_r, x_l> for l < r (computed, then stored)
         if (factored) {
           const float vr = nr * sc.fv[r];
 #pragma unroll
-          for (int l = 0; l < 32; ++l) d[l] = (32 * h + l < r) ? (d[l] * vr) * sc.cu[32 * h + l] : 0.f;
+          for (int l = 0; l < 32; ++l)
+            d[l] = (32 * h + l < r) ? (d[l] * vr) * sc.cu[32 * h + l] : 0.f;
         } else {
           const float er = sc.eta[r], gxr = sc.gx[r];
 #pragma unroll
@@ -443,22 +454,22 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
             for (int k = 0; k < 16; ++k) drow[k] = d[k];
           }
         }
-      }
-    } else {
-      // P row i: e^{g_i - g_j} <phi(q_i), x_j> for j <= i
-      const int i = r - 64;
-      if (factored) {
-        const float wi = nr * sc.fw[i];
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj)
-          d[jj] = (32 * h + jj <= i) ? (d[jj] * wi) * sc.cu[32 * h + jj] : 0.f;
       } else {
-        const float gi = sc.g[i];
+        // P row i: e^{g_i - g_j} <phi(q_i), x_j> for j <= i
+        const int i = r - 64;
+        if (factored) {
+          const float wi = nr * sc.fw[i];
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj)
-          d[jj] = (32 * h + jj <= i) ? __expf(fminf(gi - sc.g[32 * h + jj], 0.f)) * d[jj] : 0.f;
+          for (int jj = 0; jj < 32; ++jj)
+            d[jj] = (32 * h + jj <= i) ? (d[jj] * wi) * sc.cu[32 * h + jj] : 0.f;
+        } else {
+          const float gi = sc.g[i];
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj)
+            d[jj] = (32 * h + jj <= i) ? __expf(fminf(gi - sc.g[32 * h + jj], 0.f)) * d[jj] : 0.f;
+        }
+        store_half_sw(p_tile, i, h, d, 1.f);
       }
-      store_half_sw(p_tile, i, h, d, 1.f);
     }
   }
   if (__syncthreads_or(sc.fail)) goto teardown;  // A and P complete
