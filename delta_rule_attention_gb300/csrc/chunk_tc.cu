@@ -91,13 +91,21 @@ constexpr float kFactorSpan = 80.f;
 // copies.
 template <int M>
 struct MapLayout;
+// m = 64 (four CTAs per SM): buffers are reused as their contents die:
+//   K   raw k rows -> Xh (once MMA1 has read K) -> Xt (once MMA2 has read Xh)
+//       -> with Q, the Mc staging;
+//   Q   raw q rows -> the fp32 diagonal blocks of A (AD) and the solve's bf16
+//       diagonal blocks of T (DB), once MMA1 has read Q -> the zero tile of
+//       MMA3 (once the solve is done);
+//   A and T, contiguous: A and T -> [W^T; U~^T] (MMA3's B) -> the Nc staging.
 template <>
 struct MapLayout<64> {
-  static constexpr uint32_t K = 0, Q = 8192, P = 16384, A = 24576, AD = 32768, T = 37888,
-                            XH = 46080, VH = 54272, DB = 62464, SC = 64512;
+  static constexpr uint32_t K = 0, Q = 8192, P = 16384, A = 24576, T = 32768, VH = 40960,
+                            SC = 49152;
+  static constexpr uint32_t XH = K, AD = Q, DB = Q + 4352;
   static constexpr uint32_t kAtom = 0;  // K-atom stride of [K; Q] (one atom)
   static constexpr int kHalves = 1;
-  static constexpr int kMinBlocks = 3;
+  static constexpr int kMinBlocks = 4;
   static constexpr uint32_t kTmemCols = 128;
   static constexpr uint32_t kMapBytes = 128 * 128 * 2 + 128;  // Mc, Nc, e^{g_C}
 };
@@ -123,7 +131,86 @@ constexpr bool map_layout_ok() {
          L::SC % 16 == 0 &&
          L::A + 16384 <= L::XH;  // [W^T; U~^T] over A, AD and T only
 }
-static_assert(map_layout_ok<64>() && map_layout_ok<128>(), "map kernel shared-memory layout");
+constexpr bool map_layout64_ok() {
+  using L = MapLayout<64>;
+  return L::K % 1024 == 0 && L::Q == L::K + 8192 && L::P == L::Q + 8192 && L::A % 1024 == 0 &&
+         L::T == L::A + 8192 && L::VH % 1024 == 0 && L::VH >= L::T + 8192 &&
+         L::AD + 64 * kLdD * 4 <= L::DB && L::DB % 16 == 0 && L::DB + 2048 <= L::Q + 8192 &&
+         L::SC >= L::VH + 8192 && L::SC % 16 == 0;
+}
+static_assert(map_layout64_ok() && map_layout_ok<128>(), "map kernel shared-memory layout");
+
+// A thread's raw half row (32 bf16 input values) kept as 16 packed bf16
+// pairs: exact, half the registers of fp32.
+__device__ __forceinline__ float bf16_at(const uint32_t (&p)[16], int i) {
+  return __uint_as_float((i & 1) ? (p[i >> 1] & 0xffff0000u) : (p[i >> 1] << 16));
+}
+__device__ __forceinline__ void load_half_raw(const unsigned char* tile, int r, int h,
+                                              uint32_t (&p)[16]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint4 pk =
+        *reinterpret_cast<const uint4*>(tile + r * 128 + (((4 * h + c) ^ (r & 7)) << 4));
+    p[4 * c] = pk.x;
+    p[4 * c + 1] = pk.y;
+    p[4 * c + 2] = pk.z;
+    p[4 * c + 3] = pk.w;
+  }
+}
+__device__ __forceinline__ float sumsq_packed(const uint32_t (&p)[16]) {
+  float q[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < 32; ++i) q[i & 7] = fmaf(bf16_at(p, i), bf16_at(p, i), q[i & 7]);
+  return ((q[0] + q[1]) + (q[2] + q[3])) + ((q[4] + q[5]) + (q[6] + q[7]));
+}
+// The half row times `scale`, as bf16, into a 128B-swizzled tile row.
+__device__ __forceinline__ void store_half_packed(unsigned char* tile, int r, int h,
+                                                  const uint32_t (&p)[16], float scale) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    float v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = bf16_at(p, 8 * c + e);
+    *reinterpret_cast<uint4*>(tile + r * 128 + (((4 * h + c) ^ (r & 7)) << 4)) = pack8(v, scale);
+  }
+}
+
+// A thread's raw half row: packed bf16 pairs where registers are short (m = 64,
+// four CTAs per SM), fp32 otherwise; the same values and products either way.
+template <bool kPacked>
+struct HalfRow;
+template <>
+struct HalfRow<true> {
+  uint32_t p[16];
+  __device__ __forceinline__ void load(const unsigned char* tile, int r, int h) {
+    load_half_raw(tile, r, h, p);
+  }
+  __device__ __forceinline__ void clear() {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) p[i] = 0u;
+  }
+  __device__ __forceinline__ float at(int i) const { return bf16_at(p, i); }
+  __device__ __forceinline__ float sumsq() const { return sumsq_packed(p); }
+  __device__ __forceinline__ void store(unsigned char* tile, int r, int h, float scale) const {
+    store_half_packed(tile, r, h, p, scale);
+  }
+};
+template <>
+struct HalfRow<false> {
+  float v[32];
+  __device__ __forceinline__ void load(const unsigned char* tile, int r, int h) {
+    load_half_sw(tile, r, h, v);
+  }
+  __device__ __forceinline__ void clear() {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = 0.f;
+  }
+  __device__ __forceinline__ float at(int i) const { return v[i]; }
+  __device__ __forceinline__ float sumsq() const { return sumsq32(v); }
+  __device__ __forceinline__ void store(unsigned char* tile, int r, int h, float scale) const {
+    store_half_sw(tile, r, h, v, scale);
+  }
+};
 
 struct MapScalars {
   float eta[64], g[64], gx[64];
@@ -281,23 +368,45 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
   //      rows 64..127 are phi(q_{t0+r-64}); a thread keeps its raw half row
   //      (of column half j) and the row's phi scale nr.  m = 128: the other
   //      half (xo) enters the norm and Xt.
-  float x[32], xo[32];
-  if (carried_row && a.x_prev) {
+  // The raw half rows (xp: half j, xo: the other half, m = 128); the carried
+  // row (x_prev, fp32) is read again from global memory where it is used.
+  const bool carried_fp32 = carried_row && a.x_prev != nullptr;
+  HalfRow<!kWide> xp, xo;
+  if (carried_fp32) {
+    float x[32], y[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) x[i] = a.x_prev[bh * M + 64 * j + 32 * h + i];
     if (kWide) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) xo[i] = a.x_prev[bh * M + 64 * (1 - j) + 32 * h + i];
+      for (int i = 0; i < 32; ++i) y[i] = a.x_prev[bh * M + 64 * (1 - j) + 32 * h + i];
     }
+    if (kWide)  // same summation order in both halves' CTAs
+      sc.ssp[h][r] = j == 0 ? sumsq32(x) + sumsq32(y) : sumsq32(y) + sumsq32(x);
+    else
+      sc.ssp[h][r] = sumsq32(x);
+    xp.clear();  // not used for this row
+    xo.clear();
   } else {
     const unsigned char* rt = (r < 64 ? kt : qt);
-    load_half_sw(rt + j * L::kAtom, r & 63, h, x);
-    if (kWide) load_half_sw(rt + (1 - j) * L::kAtom, r & 63, h, xo);
+    xp.load(rt + j * L::kAtom, r & 63, h);
+    if (kWide) xo.load(rt + (1 - j) * L::kAtom, r & 63, h);
+    if (kWide)
+      sc.ssp[h][r] = j == 0 ? xp.sumsq() + xo.sumsq() : xo.sumsq() + xp.sumsq();
+    else
+      sc.ssp[h][r] = xp.sumsq();
   }
-  if (kWide)  // same summation order in both halves' CTAs
-    sc.ssp[h][r] = j == 0 ? sumsq32(x) + sumsq32(xo) : sumsq32(xo) + sumsq32(x);
-  else
-    sc.ssp[h][r] = sumsq32(x);
+  // This thread's half row (half `part`: j or the other) times `scale` into a tile row.
+  auto store_row = [&](unsigned char* tile, int row, int part, float scale) {
+    if (carried_fp32) {
+      float v[32];
+      const int jj = part == 0 ? j : 1 - j;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = a.x_prev[bh * M + 64 * jj + 32 * h + i];
+      store_half_sw(tile, row, h, v, scale);
+    } else {
+      (part == 0 ? xp : xo).store(tile, row, h, scale);
+    }
+  };
   __syncthreads();
   const float ss = sc.ssp[0][r] + sc.ssp[1][r];
   const float nr = carried_row ? 1.f : phi_scale(ss, M, a.phi);
@@ -308,7 +417,7 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
     float* xl = a.x_last + bh * M + 64 * j + 32 * h;
     if (n < kC && r == n) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) xl[i] = x[i] * nr;
+      for (int i = 0; i < 32; ++i) xl[i] = xp.at(i) * nr;
     } else if (n == kC && r == 64) {
       const __nv_bfloat16* kl =
           reinterpret_cast<const __nv_bfloat16*>(a.k) + (rowbase + a.T - 1) * M;
@@ -373,10 +482,14 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
   __syncthreads();  // step sizes, prefix and decay factors visible
   const float gC = sc.g[kC - 1];
   const bool factored = -gC <= kFactorSpan;
+  // Xh = Diag(e^{g_-}) X (MMA2's A, columns of half j; Falcon-1A: W = 0, so
+  // Xh = 0): m = 128 into its own tile now; m = 64 into the K tile once MMA1
+  // has read it.
+  const float xh_scale = f1 ? __expf(sc.gx[r & 63]) * nr : 0.f;
   if (r < 64) {
-    // Xh = Diag(e^{g_-}) X (MMA2's A, columns of half j); Falcon-1A: W = 0 and
-    // T' = Diag(eta), whose rows are written here (the solve writes Falcon-1's).
-    store_half_sw(xh_tile, r, h, x, f1 ? __expf(sc.gx[r]) * nr : 0.f);
+    if (kWide) store_row(xh_tile, r, 0, xh_scale);
+    // Falcon-1A: T' = Diag(eta), whose rows are written here (the solve writes
+    // Falcon-1's).
     if (!f1) {
       float trow[32];
       const float er = sc.eta[r];
@@ -388,24 +501,14 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
   // Every thread sees MMA1 complete before it overwrites the K and Q tiles.
   if (!sc.fail && !mbar_wait(&sc.bar_mma, 0)) sc.fail = 1;
   tc_fence_after();
-
-  // Xt = Diag(e^{g_C - g}) X over the K tile (m = 64: by the threads of rows
-  // 64..127, each rewriting in place the four chunks it reads; m = 128: from
-  // the rows held in registers), and the zero tile (m = 64).
   if (!kWide) {
-    reinterpret_cast<uint4*>(zero_tile)[tid] = make_uint4(0u, 0u, 0u, 0u);
-    reinterpret_cast<uint4*>(zero_tile)[tid + 256] = make_uint4(0u, 0u, 0u, 0u);
-    if (r >= 64 && !(patch && r == 64)) {
-      const int l = r - 64;
-      scale_half_sw(xt_tile, l, h, __expf(gC - sc.g[l]) * sc.nrm[l]);
-    } else if (patch && r == 0) {
-      // x_1 = x_prev from the fp32 values (the tile holds them rounded)
-      store_half_sw(xt_tile, 0, h, x, __expf(gC - sc.g[0]) * nr);
-    }
+    if (r < 64) store_row(xh_tile, r, 0, xh_scale);
   } else if (r < 64) {
+    // Xt = Diag(e^{g_C - g}) X over the K atoms (m = 128; m = 64 writes Xt
+    // over Xh once MMA2 has read it)
     const float xs = __expf(gC - sc.g[r]) * nr;
-    store_half_sw(xt_tile + j * L::kAtom, r, h, x, xs);
-    store_half_sw(xt_tile + (1 - j) * L::kAtom, r, h, xo, xs);
+    store_row(xt_tile + j * L::kAtom, r, 0, xs);
+    store_row(xt_tile + (1 - j) * L::kAtom, r, 1, xs);
   }
   {
     // This warp's half rows may lie wholly above the diagonal (columns 32..63
@@ -492,7 +595,14 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
   {
     float d[32];
     tmem_ld32(tlane + 32 * h, d);
-    store_half_sw(wu_tile, r, h, d, 1.f);  // [W^T; U~^T] over A, AD, T (MMA2 is complete)
+    store_half_sw(wu_tile, r, h, d, 1.f);  // [W^T; U~^T] over A and T (MMA2 is complete)
+  }
+  if (!kWide) {
+    // m = 64: Xt = Diag(e^{g_C - g}) X over Xh (read by the completed MMA2),
+    // and the zero tile of MMA3 over the solve's blocks in the Q tile.
+    if (r < 64) store_row(xt_tile, r, 0, __expf(gC - sc.g[r]) * nr);
+    reinterpret_cast<uint4*>(zero_tile)[tid] = make_uint4(0u, 0u, 0u, 0u);
+    reinterpret_cast<uint4*>(zero_tile)[tid + 256] = make_uint4(0u, 0u, 0u, 0u);
   }
   fence_async_smem();
   tc_fence_before();
@@ -539,7 +649,7 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
       // Mc row: rows < 64 -> -Xt^T W ; rows >= 64 -> e^{g_i} phi(q_i) - P W
       const float eq = (r >= 64) ? __expf(sc.g[r - 64]) * nr : 0.f;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) d[i] = (r < 64) ? -d[i] : eq * x[i] - d[i];
+      for (int i = 0; i < 32; ++i) d[i] = (r < 64) ? -d[i] : eq * xp.at(i) - d[i];
       store_half_sw(mc_stage, r, h, d, 1.f);
       fence_async_smem();
       tmem_ld32(tlane + 64 + 32 * h, d);
@@ -577,7 +687,7 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
         const float eq = __expf(sc.g[r - 64]) * nr;
         tmem_ld32(tlane + 128 + 32 * h, d);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) d[i] = eq * x[i] - d[i];
+        for (int i = 0; i < 32; ++i) d[i] = eq * xp.at(i) - d[i];
         store_half_sw(mco_stage, r - 64, h, d, 1.f);
       }
       fence_async_smem();
