@@ -109,27 +109,28 @@ struct MapLayout<64> {
   static constexpr uint32_t kTmemCols = 128;
   static constexpr uint32_t kMapBytes = 128 * 128 * 2 + 128;  // Mc, Nc, e^{g_C}
 };
+// m = 128 (three CTAs per SM): the q rows of the second K-atom are dead once
+// MMA1 has read them and take the solve's diagonal blocks (AD, DB).
 template <>
 struct MapLayout<128> {
-  static constexpr uint32_t K = 0, Q = 8192, P = 8192, A = 32768, AD = 40960, T = 46080,
-                            XH = 54272, VH = 62464, DB = 70656, SC = 72704;
+  static constexpr uint32_t K = 0, Q = 8192, P = 8192, A = 32768, T = 40960, XH = 49152,
+                            VH = 57344, SC = 65536;
+  static constexpr uint32_t AD = Q + 16384, DB = AD + 4352;
   static constexpr uint32_t kAtom = 16384;
   static constexpr int kHalves = 2;
-  static constexpr int kMinBlocks = 2;
-  static constexpr uint32_t kTmemCols = 256;
+  static constexpr int kMinBlocks = 3;
+  static constexpr uint32_t kTmemCols = 128;
   // Per chunk: Mc K-atoms 0 and 1 (192 rows x 128 B each: 128 state rows,
   // then 64 output rows), Nc d_v slices 0 and 1 (192 rows x 128 B), e^{g_C}.
   static constexpr uint32_t kMcAtom = 192 * 128;
   static constexpr uint32_t kMapBytes = 4 * kMcAtom + 128;
 };
-template <int M>
-constexpr bool map_layout_ok() {
-  using L = MapLayout<M>;
-  return L::A % 1024 == 0 && L::T % 1024 == 0 && L::XH % 1024 == 0 && L::VH % 1024 == 0 &&
-         L::AD >= L::A + 8192 && L::AD + 64 * kLdD * 4 <= L::T && L::XH >= L::T + 8192 &&
-         L::VH >= L::XH + 8192 && L::DB >= L::VH + 8192 && L::SC >= L::DB + 2048 &&
-         L::SC % 16 == 0 &&
-         L::A + 16384 <= L::XH;  // [W^T; U~^T] over A, AD and T only
+constexpr bool map_layout128_ok() {
+  using L = MapLayout<128>;
+  return L::A % 1024 == 0 && L::T == L::A + 8192 && L::XH % 1024 == 0 &&
+         L::XH >= L::T + 8192 && L::VH == L::XH + 8192 && L::SC >= L::VH + 8192 &&
+         L::AD == L::Q + L::kAtom && L::AD + 64 * kLdD * 4 <= L::DB && L::DB % 16 == 0 &&
+         L::DB + 2048 <= L::AD + 8192 && L::SC % 16 == 0;
 }
 constexpr bool map_layout64_ok() {
   using L = MapLayout<64>;
@@ -138,7 +139,7 @@ constexpr bool map_layout64_ok() {
          L::AD + 64 * kLdD * 4 <= L::DB && L::DB % 16 == 0 && L::DB + 2048 <= L::Q + 8192 &&
          L::SC >= L::VH + 8192 && L::SC % 16 == 0;
 }
-static_assert(map_layout64_ok() && map_layout_ok<128>(), "map kernel shared-memory layout");
+static_assert(map_layout64_ok() && map_layout128_ok(), "map kernel shared-memory layout");
 
 // A thread's raw half row (32 bf16 input values) kept as 16 packed bf16
 // pairs: exact, half the registers of fp32.
@@ -371,7 +372,7 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
   // The raw half rows (xp: half j, xo: the other half, m = 128); the carried
   // row (x_prev, fp32) is read again from global memory where it is used.
   const bool carried_fp32 = carried_row && a.x_prev != nullptr;
-  HalfRow<!kWide> xp, xo;
+  HalfRow<true> xp, xo;
   if (carried_fp32) {
     float x[32], y[32];
 #pragma unroll
@@ -611,12 +612,11 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
 
   // ---- MMA3 ----
   //   m = 64:  D[0:128) = [Xt^T; 0] [W | U~] + [0; P] [W | U~]
-  //   m = 128: D[0:128) = Xt^T [W | U~];  D[128:256) = [junk; P] [W | U~]
+  //   m = 128: D[0:128) = [junk; P] [W | U~] (the output rows, staged), then
+  //            D[0:128) = Xt^T [W | U~] (the state rows) in the same columns
   if (tid == 0) {
     if (kWide) {
-      mma_k64(tmem, smem_addr(xt_tile), true, L::kAtom, smem_addr(wu_tile), false, 16,
-              idesc_bf16(128, 128, true, false), false);
-      mma_k64(tmem + 128, smem_addr(p_tile - 8192), false, 16, smem_addr(wu_tile), false, 16,
+      mma_k64(tmem, smem_addr(p_tile - 8192), false, 16, smem_addr(wu_tile), false, 16,
               idesc_bf16(128, 128, false, false), false);
     } else {
       mma_k64(tmem, smem_addr(xt_tile), true, 8192, smem_addr(wu_tile), false, 16,
@@ -675,41 +675,50 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
     } else {
       // K-atom j of Mc (rows 0..127: -Xt^T W_j; rows 128..191: e^g phi(Q)_j - P W_j)
       // and d_v slice j of Nc (rows 0..127: Xt^T U~_j; rows 128..191: P U~_j).
-      unsigned char* mcs_stage = base;          // 16 KB
-      unsigned char* mco_stage = base + 16384;  // 8 KB
-      unsigned char* nco_stage = base + 24576;  // 8 KB
-      unsigned char* ncs_stage = wu_tile;       // 16 KB
+      // The output rows first (lanes 64..127: P [W_j | U~_j]), staged over the
+      // Xh and Vh tiles that MMA2 has read.
+      unsigned char* mco_stage = xh_tile;  // 8 KB
+      unsigned char* nco_stage = vh;       // 8 KB
+      if (r >= 64) {  // warps 2, 3, 6, 7
+        const float eq = __expf(sc.g[r - 64]) * nr;
+        tmem_ld32(tlane + 32 * h, d);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) d[i] = eq * xp.at(i) - d[i];
+        store_half_sw(mco_stage, r - 64, h, d, 1.f);
+        tmem_ld32(tlane + 64 + 32 * h, d);
+        store_half_sw(nco_stage, r - 64, h, d, 1.f);
+      }
+      fence_async_smem();
+      // Every thread is done with the accumulator before the state half of
+      // MMA3 overwrites it.
+      tc_fence_before();
+      if (__syncthreads_or(sc.fail)) goto teardown;
+      tc_fence_after();
+      if (tid == 0) {
+        mma_k64(tmem, smem_addr(xt_tile), true, L::kAtom, smem_addr(wu_tile), false, 16,
+                idesc_bf16(128, 128, true, false), false);
+        mma_commit(&sc.bar_mma);
+      }
+      if (!mbar_wait(&sc.bar_mma, 1)) sc.fail = 1;
+      tc_fence_after();
+      // The state rows over the operands of the completed MMA3 (Xt's first
+      // atom and P; [W^T; U~^T]).
+      unsigned char* mcs_stage = base;     // 16 KB
+      unsigned char* ncs_stage = wu_tile;  // 16 KB
       tmem_ld32(tlane + 32 * h, d);
 #pragma unroll
       for (int i = 0; i < 32; ++i) d[i] = -d[i];
       store_half_sw(mcs_stage, r, h, d, 1.f);
-      if (r >= 64) {  // warps 2, 3, 6, 7: lanes 64..127 hold P [W_j | U~_j]
-        const float eq = __expf(sc.g[r - 64]) * nr;
-        tmem_ld32(tlane + 128 + 32 * h, d);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) d[i] = eq * xp.at(i) - d[i];
-        store_half_sw(mco_stage, r - 64, h, d, 1.f);
-      }
-      fence_async_smem();
-      if (__syncthreads_or(sc.fail)) goto teardown;
-      unsigned char* mc = map + j * L::kMcAtom;
-      unsigned char* nc = map + (2 + j) * L::kMcAtom;
-      // The Mc atom leaves while Nc is staged.
-      if (tid == 0) {
-        bulk_s2g(mc, mcs_stage, 16384);
-        bulk_s2g(mc + 16384, mco_stage, 8192);
-        bulk_commit();
-      }
       tmem_ld32(tlane + 64 + 32 * h, d);
       store_half_sw(ncs_stage, r, h, d, 1.f);
-      if (r >= 64) {
-        tmem_ld32(tlane + 192 + 32 * h, d);
-        store_half_sw(nco_stage, r - 64, h, d, 1.f);
-      }
       fence_async_smem();
-      __syncthreads();
+      if (__syncthreads_or(sc.fail)) goto teardown;
       if (tid == 0) {
+        unsigned char* mc = map + j * L::kMcAtom;
+        unsigned char* nc = map + (2 + j) * L::kMcAtom;
         if (j == 0) *reinterpret_cast<float*>(map + 4 * L::kMcAtom) = __expf(gC);
+        bulk_s2g(mc, mcs_stage, 16384);
+        bulk_s2g(mc + 16384, mco_stage, 8192);
         bulk_s2g(nc, ncs_stage, 16384);
         bulk_s2g(nc + 16384, nco_stage, 8192);
         bulk_commit();
