@@ -62,27 +62,28 @@ constexpr float kFactorSpan = 80.f;
 // two CTAs per chunk, CTA j taking the column half j of W, U~ and of the map
 // (K-atom j of Mc, d_v slice j of Nc); the Gram matrix, the solve and T are
 // the same in both.  Shared memory, in bytes from a 1024-aligned base (buffers
-// with disjoint lifetimes share space), m = 64:
+// with disjoint lifetimes share space), m = 64 (52 KB, four CTAs per SM):
 //   K   [0, 8192)       raw k rows t0-1 .. t0+62 as landed by TMA (128B-swizzled;
-//                       row r holds the write feature x_r before phi) -> Xt
-//                       (atom 0 of MMA3a's MN-major A)
+//                       row r holds the write feature x_r before phi) -> Xh
+//                       (MMA2's A, atom 0) -> Xt (atom 0 of MMA3a's MN-major A)
 //   Q   [8192, 16384)   raw q rows as landed by TMA; [K; Q] is MMA1's A operand
+//                       -> AD, the fp32 diagonal 16 x 16 blocks of A (rows of
+//                       17), and DB at 12544, the unscaled diagonal blocks of T
 //                       -> zero tile (atom 1 of MMA3a; rows 0..63 of MMA3b)
 //   P   [16384, 24576)  P (rows 64..127 of MMA3b, K-major)
-//   A   [24576, 32768)  A as bf16 (the solve's MMA operand) -> [W^T; U~^T]
-//                       (MMA3 B, 16 KB over A, AD and T) -> Nc staging
-//   AD  [32768, 37120)  the fp32 diagonal 16 x 16 blocks of A (rows of 17)
-//   T   [37888, 46080)  T = (I + A)^{-1} as bf16 (MMA2 B, K-major)
-//   XH  [46080, 54272)  Xh rows (atom 0 of MMA2's MN-major A)
-//   VH  [54272, 62464)  raw v rows as landed by TMA (atom 1 of MMA2's A)
-//   DB  [62464, 64512)  the unscaled diagonal blocks of T (bf16, the solve's)
-//   SC  [64512, ...)    per-token scalars and barriers
-// m = 128: [K; Q] is two K-atoms of 16 KB, [K_a0 | Q_a0 | K_a1 | Q_a1]
-// (columns 0..63 and 64..127); afterwards Xt's two M-atoms replace K_a0 and
-// K_a1 and P replaces Q_a0; MMA3a (Xt^T [W | U~], 128 rows) and MMA3b
-// ([junk; P] [W | U~]) go to separate accumulators, so no zero tile is used.
-// A, AD, T, XH, VH, DB follow at 32768, 40960, 46080, 54272, 62464, 70656
-// (XH holds the x columns and VH the v columns of half j).
+//   A   [24576, 32768)  A as bf16 (the solve's MMA operand)  } [W^T; U~^T] (MMA3's
+//   T   [32768, 40960)  T = (I + A)^{-1} as bf16 (MMA2's B) } B) -> Nc staging
+//   VH  [40960, 49152)  raw v rows as landed by TMA (atom 1 of MMA2's A)
+//   SC  [49152, ...)    per-token scalars and barriers
+// m = 128 (68 KB, three CTAs per SM): [K; Q] is two K-atoms of 16 KB,
+// [K_a0 | Q_a0 | K_a1 | Q_a1] (columns 0..63 and 64..127); afterwards Xt's
+// two M-atoms replace K_a0 and K_a1, P replaces Q_a0, and the dead q rows of
+// Q_a1 take AD and DB.  A, T, XH, VH and SC follow at 32768, 40960, 49152,
+// 57344 and 65536 (XH holds the x columns and VH the v columns of half j).
+// MMA3 runs in two passes through the same 128 TMEM columns: the output rows
+// ([junk; P] [W | U~]) first, staged over the dead XH and VH tiles, then the
+// state rows (Xt^T [W | U~]), staged over the first 16 KB (Xt's first atom
+// and P) and over [W^T; U~^T].
 // T carries the step sizes in its columns, T' = T Diag(eta), so that
 // MMA2 = [Xh^T; V^T] T'^T gives W^T = (T Diag(eta e^{g_-}) X)^T with
 // Xh = Diag(e^{g_-}) X and U~^T = (T Diag(eta) V)^T from the raw v rows.

@@ -758,20 +758,31 @@ teardown:
 // one CTA per head, newest chunk first:
 //   dS_c = e^{g_C} dS' + Mc^T [dS'; dO_c]
 // (Mc as stored: the state rows -Xt^T W without the e^{g_C} I part, the output
-// rows Diag(e^g) Q - P W).  The MMA reads the stored Mc tile MN-major as
-// Mc^T (K = 128: the state rows, then the output rows) and B = [dS'; dO_c]
-// MN-major (dS' in bf16 written by the state threads, dO_c landed by TMA);
-// the e^{g_C} dS' part stays in fp32 registers.  Threads of warps 0, 1, 4, 5
-// own state row 32 (w & 3) + lane and columns 32 (w >> 2) .. +31; lane 0 of
-// warp 2 loads the maps (a ring of kRevStages) and issues the MMAs.
+// rows Diag(e^g) Q - P W).  The MMAs read the stored Mc tile MN-major as Mc^T
+// (K = 128: the state rows, then the output rows).  Per chunk two MMAs go into
+// one of two TMEM accumulators: Mc_bot^T dO_c first (it does not depend on the
+// chain, and is issued as soon as the chunk's stage has landed), then
+// Mc_top^T dS' once the state threads have put dS' (bf16) in the operand tile;
+// the e^{g_C} dS' part stays in fp32 registers.  Warps 0, 1, 4, 5 own state
+// row 32 (w & 3) + lane and columns 32 (w >> 2) .. +31 (TMEM lanes 0..63);
+// lane 0 of warp 2 issues the MMAs; lane 0 of warp 3 refills a ring of
+// kRevStages stages (Mc, dO_c, e^{g_C}) as the MMAs and the state warps are
+// done with one.  Every hand-off is an mbarrier; the chain per chunk is the
+// state MMA, one accumulator read, the fp32 update and the operand write.
 constexpr int kRevStages = 4;
-constexpr uint32_t kRevStage = kMcBytes + 2 * kTile;  // Mc | dS' operand | dO_c
+constexpr int kRevThreads = 192;
+constexpr uint32_t kRevStage = kMcBytes + kTile;  // Mc | dO_c
 
 struct RevSmem {
   unsigned char stage[kRevStages][kRevStage];
+  // dS' as the MN-major B operand; it also takes the unused M-atom that the
+  // output MMA of the last stage reads past that stage (lanes 64..127).
+  unsigned char op[kTile];
   float gc[kRevStages][4];
-  uint64_t full[kRevStages];
-  uint64_t bar_mma;
+  uint64_t full[kRevStages];   // the stage has landed
+  uint64_t empty[kRevStages];  // both MMAs and the state warps are done with the stage
+  uint64_t mma_done[2];        // both MMAs into accumulator b have completed
+  uint64_t s_ready;            // dS' of the next chunk is in op
   uint32_t tmem_base;
   int fail;
 };
@@ -781,95 +792,134 @@ __device__ __forceinline__ void rev_issue_load(RevSmem& s, int st, const unsigne
   mbar_expect_tx(&s.full[st], kMcBytes + 16 + kTile);
   bulk_g2s(s.stage[st], map, kMcBytes, &s.full[st]);
   bulk_g2s(s.gc[st], map + kMcBytes + kNcBytes, 16, &s.full[st]);
-  tma_load_3d(s.stage[st] + kMcBytes + kTile, tm_do, 0, t0, bh, &s.full[st]);
+  tma_load_3d(s.stage[st] + kMcBytes, tm_do, 0, t0, bh, &s.full[st]);
 }
 
-__global__ void __launch_bounds__(kBThreads, 1)
+__global__ void __launch_bounds__(kRevThreads)
     tc_bwd_scan_kernel(BwdArgs b, int nchunks, const unsigned char* maps, float* dS_ends,
                        int* err, const __grid_constant__ CUtensorMap tm_do) {
   extern __shared__ unsigned char smem_raw[];
   RevSmem& s = *reinterpret_cast<RevSmem*>(align1024(smem_raw));
+  volatile int* fail = &s.fail;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t bh = blockIdx.x;
-  const bool state = (warp & 3) < 2;           // warps 0, 1, 4, 5
-  const bool issuer = warp == 2 && lane == 0;
+  const bool state = (warp & 3) < 2;  // warps 0, 1, 4, 5
   const int row = 32 * (warp & 3) + lane, h = warp >> 2;
+  const int n = nchunks;
   const unsigned char* hmaps = maps + (size_t)bh * nchunks * kMapBytes;
-  if (warp == 0) tmem_alloc(&s.tmem_base, 64);
+  if (warp == 0) tmem_alloc(&s.tmem_base, 128);
   if (tid == 0) {
-    for (int st = 0; st < kRevStages; ++st) mbar_init(&s.full[st], 1);
-    mbar_init(&s.bar_mma, 1);
+    for (int st = 0; st < kRevStages; ++st) {
+      mbar_init(&s.full[st], 1);
+      mbar_init(&s.empty[st], 1 + 4);  // the MMAs' commit, the four state warps
+    }
+    mbar_init(&s.mma_done[0], 1);
+    mbar_init(&s.mma_done[1], 1);
+    mbar_init(&s.s_ready, 4);
     fence_mbar_init();
     s.fail = 0;
-  }
-  float dS[32];
-  if (state) {
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      dS[j] = b.dS_T ? b.dS_T[(bh * 64 + row) * 64 + 32 * h + j] : 0.f;
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
-  if (issuer)
-    for (int k = 0; k < kRevStages && k < nchunks; ++k) {
-      const int c = nchunks - 1 - k;
-      rev_issue_load(s, k, hmaps + (size_t)c * kMapBytes, &tm_do, c * kBC, (int)bh);
+
+  if (warp == 2) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(128, 64, true, true);
+      for (int k = 0; k < n; ++k) {
+        const int st = k % kRevStages, bb = k & 1;
+        const uint32_t stg = smem_addr(s.stage[st]);
+        // Accumulator bb was last read for chunk k - 2, before the state
+        // threads signalled the operand of chunk k - 1 (waited for below in
+        // the previous pass).
+        if (!mbar_wait(&s.full[st], (uint32_t)(k / kRevStages) & 1u)) {
+          *fail = 1;
+          break;
+        }
+        tc_fence_after();
+        // K rows 64..127: the output rows of Mc with dO_c (the second M-atom
+        // of A, LBO on, reads past them into lanes 64..127, unused).
+        mma_k64(tmem + 64 * bb, stg + 8192, true, kMcBytes, stg + kMcBytes, true, kTile, idesc,
+                false);
+        if (!mbar_wait(&s.s_ready, (uint32_t)k & 1u)) {
+          *fail = 1;
+          break;
+        }
+        tc_fence_after();
+        // K rows 0..63: the state rows of Mc with dS'.
+        mma_k64(tmem + 64 * bb, stg, true, kMcBytes, smem_addr(s.op), true, kTile, idesc, true);
+        mma_commit(&s.mma_done[bb]);
+        mma_commit(&s.empty[st]);
+      }
     }
-  const uint32_t idesc = idesc_bf16(128, 64, true, true);
-  for (int k = 0; k < nchunks; ++k) {
-    const int c = nchunks - 1 - k, st = k % kRevStages;
-    unsigned char* stg = s.stage[st];
-    if (state) {
-      // the cotangent of the state leaving chunk c: out (fp32) and into the operand
+    __syncwarp();
+  } else if (warp == 3) {
+    if (lane == 0) {
+      for (int k = 0; k < kRevStages && k < n; ++k) {
+        const int c = n - 1 - k;
+        rev_issue_load(s, k, hmaps + (size_t)c * kMapBytes, &tm_do, c * kBC, (int)bh);
+      }
+      for (int k = 0; k + kRevStages < n; ++k) {
+        const int st = k % kRevStages;
+        if (*fail || !mbar_wait(&s.empty[st], (uint32_t)(k / kRevStages) & 1u)) {
+          *fail = 1;
+          break;
+        }
+        const int c = n - 1 - (k + kRevStages);
+        rev_issue_load(s, st, hmaps + (size_t)c * kMapBytes, &tm_do, c * kBC, (int)bh);
+      }
+    }
+    __syncwarp();
+  } else if (state) {
+    float dS[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      dS[j] = b.dS_T ? b.dS_T[(bh * 64 + row) * 64 + 32 * h + j] : 0.f;
+    // The cotangent of the state leaving chunk c: out (fp32) and into the operand.
+    auto publish = [&](int c) {
       float4* dst = reinterpret_cast<float4*>(dS_ends + ((size_t)(bh * nchunks + c) * 64 + row) *
                                                             64 + 32 * h);
 #pragma unroll
       for (int q4 = 0; q4 < 8; ++q4)
         dst[q4] = make_float4(dS[4 * q4], dS[4 * q4 + 1], dS[4 * q4 + 2], dS[4 * q4 + 3]);
-      store_half_sw(stg + kMcBytes, row, h, dS, 1.f);
+      store_half_sw(s.op, row, h, dS, 1.f);
       fence_async_smem();
-    }
-    if (issuer) {
-      if (!mbar_wait(&s.full[st], (uint32_t)(k / kRevStages) & 1u)) s.fail = 1;
-    }
-    if (__syncthreads_or(s.fail)) break;
-    if (issuer) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.s_ready);
+    };
+    if (n > 0) publish(n - 1);
+    const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 32 * h;
+    for (int k = 0; k < n; ++k) {
+      const int c = n - 1 - k, st = k % kRevStages, bb = k & 1;
+      bool ok = !*fail;
+      ok = ok && mbar_wait(&s.full[st], (uint32_t)(k / kRevStages) & 1u);
+      ok = ok && mbar_wait(&s.mma_done[bb], (uint32_t)(k >> 1) & 1u);
+      if (!__all_sync(0xffffffffu, ok)) {
+        *fail = 1;
+        break;
+      }
       tc_fence_after();
-      const uint32_t A = smem_addr(stg), B = smem_addr(stg + kMcBytes);
-      // K rows 0..63: state rows of Mc with dS'; rows 64..127: output rows with dO_c.
-      // The second M atom of A (LBO) reads the operand region: lanes 64..127, unused.
-      mma_k64(tmem, A, true, kMcBytes, B, true, kTile, idesc, false);
-      mma_k64(tmem, A + 8192, true, kMcBytes, B + kTile, true, kTile, idesc, true);
-      mma_commit(&s.bar_mma);
-    }
-    if (!mbar_wait(&s.bar_mma, (uint32_t)k & 1u)) s.fail = 1;
-    tc_fence_after();
-    if (__syncthreads_or(s.fail)) break;
-    if (state) {
       float d[32];
-      tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 32 * h, d);
+      tmem_ld32(tl + 64 * bb, d);
+      tc_fence_before();
       const float gC = s.gc[st][0];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.empty[st]);
 #pragma unroll
       for (int j = 0; j < 32; ++j) dS[j] = gC * dS[j] + d[j];
+      if (c > 0) publish(c - 1);
     }
-    // the MMA has read stage st: refill it with the chunk kRevStages further back
-    if (issuer && k + kRevStages < nchunks) {
-      const int cn = c - kRevStages;
-      rev_issue_load(s, st, hmaps + (size_t)cn * kMapBytes, &tm_do, cn * kBC, (int)bh);
-    }
-    tc_fence_before();
-  }
-  if (!s.fail && state && b.dS0) {
-    float* dst = b.dS0 + (bh * 64 + row) * 64 + 32 * h;
+    if (!*fail && b.dS0) {
+      float* dst = b.dS0 + (bh * 64 + row) * 64 + 32 * h;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) dst[j] = dS[j];
+      for (int j = 0; j < 32; ++j) dst[j] = dS[j];
+    }
   }
-  if (s.fail && tid == 0) atomicExch(err, 1);
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 64);
+  if (s.fail && tid == 0) atomicExch(err, 1);
+  if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
 cudaError_t launch_tc_bwd_scan_impl(const BwdArgs& b, const void* maps, float* dS_ends,
@@ -883,7 +933,7 @@ cudaError_t launch_tc_bwd_scan_impl(const BwdArgs& b, const void* maps, float* d
   cudaError_t e = cudaFuncSetAttribute(tc_bwd_scan_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  tc_bwd_scan_kernel<<<(unsigned)a.BH, kBThreads, smem, stream>>>(
+  tc_bwd_scan_kernel<<<(unsigned)a.BH, kRevThreads, smem, stream>>>(
       b, nchunks, reinterpret_cast<const unsigned char*>(maps), dS_ends, err, tm_do);
   return cudaGetLastError();
 }
