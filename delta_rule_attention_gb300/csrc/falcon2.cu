@@ -13,17 +13,26 @@
 // Section 3.1, the per-column NLMS step sizes of Section 4.2 and Falcon-2A of
 // Section 4.3 (the loss separates over the columns of S).
 //
-// One CTA per (head, 32 columns); each column is held in fp32 registers by
-// m / 16 threads (16 rows each), so the two column reductions per token need
-// only log2(m / 16) shuffle steps.  Tokens go in blocks of 32: the raw k, q,
-// v and beta rows of a block arrive by bulk async copies into a two-buffer
-// ring (requested one block ahead), and are staged as phi(k) and phi(q) rows
-// (fp32, with a 4-float gap after every 16 so that the row segments the
-// threads of a warp read sit in distinct banks), <x_t, phi(q_t)>, and the step
-// sizes and decays eta_{j,t}, gamma_{j,t}, which depend on the inputs only and
-// are computed for the whole block in parallel.  The sequential part per token
-// is then two dot products, a short shuffle reduction and the rank-1 update;
-// o is collected in shared memory and stored once per block.
+// The residual's inner product is taken one token ahead, from the state
+// before the previous write:
+//   s_t^T x_{t+1} = gamma_t (s_{t-1}^T x_{t+1}) + eta_t r_t <x_t, x_{t+1}>,
+// so that both reads of a token (s^T x_{t+1} and s^T phi(q_t)) and its write
+// go in one pass over the state rows, all with the state before the write;
+// the dependent chain from one token to the next is a few scalar operations.
+// A column's state is held in fp32 registers by kP threads (kR = m / kP <= 32
+// rows each, one shuffle step for m = 64).  Scalar fp32 multiply-adds: on
+// sm_103 a lone warp issues one every ~1.2 cycles but the packed f32x2 form
+// only every ~3 (measured), and a broadcast 16-byte shared-memory read costs
+// it ~11 cycles, so the reads of the staged rows make up most of the cost of
+// a token.
+//
+// One CTA of 64 threads per (head, group of 64 / kP columns).  Tokens arrive
+// in blocks of 32: the raw k, q, v and beta rows of a block come by bulk
+// async copies into a two-buffer ring (requested one block ahead) and are
+// staged as phi(k) and phi(q) rows (fp32), with the per-token ||x_t||^2,
+// <x_t, x_{t+1}>, <x_t, phi(q_t)>, lambda_t and 1 / (||x_t||^2 + lambda_t +
+// eps) formed for the whole block in parallel.  o is collected in shared
+// memory and stored once per block.
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -36,50 +45,22 @@ using tc::mbar_expect_tx;
 using tc::mbar_init;
 using tc::mbar_wait;
 
-constexpr int kTB = 32;  // tokens per block
+constexpr int kTB = 32;       // tokens per block
+constexpr int kThreads = 64;  // threads per CTA
 
 template <int M>
 struct F2Cfg {
-  static constexpr int kP = M / 16;         // threads per column (16 state rows each)
-  static constexpr int kThreads = 32 * kP;  // 32 columns per CTA
-  static constexpr int kLd = M / 16 * 20;   // fp32 row stride: 16 values + 4 gap per segment
+  static constexpr int kP = M >= 64 ? M / 32 : 1;  // threads per column
+  static constexpr int kR = M / kP;            // state rows per thread
+  static constexpr int kCols = kThreads / kP;  // columns per CTA
+  static constexpr int kSeg = kR + 4;          // padded row segment (floats)
+  static constexpr int kLd = kP * kSeg;        // staged row stride (floats)
 };
 
-// Position of row element i in a staged row (a 4-float gap after every 16):
-// segment g of 16 values starts at float 20 g.
-__device__ __forceinline__ int pad16(int i) { return i + 4 * (i >> 4); }
-
-// Sixteen consecutive elements e0 .. e0 + 15 (e0 a multiple of 16) of a raw
-// bf16 or fp32 row buffer in shared memory, by 16-byte loads; zeros if !ok.
-__device__ __forceinline__ void load16(const unsigned char* p, int64_t e0, int dtype, bool ok,
-                                       float* out) {
-  if (!ok) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) out[i] = 0.f;
-  } else if (dtype == FALCON_BF16) {
-    const uint4* v = reinterpret_cast<const uint4*>(p + 2 * e0);
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const uint4 pk = v[c];
-      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&pk);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = __bfloat1622float2(h[e]);
-        out[8 * c + 2 * e] = f.x;
-        out[8 * c + 2 * e + 1] = f.y;
-      }
-    }
-  } else {
-    const float4* v = reinterpret_cast<const float4*>(p + 4 * e0);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const float4 f = v[c];
-      out[4 * c] = f.x;
-      out[4 * c + 1] = f.y;
-      out[4 * c + 2] = f.z;
-      out[4 * c + 3] = f.w;
-    }
-  }
+// Position of row element i in a staged row.
+template <int M>
+__device__ __forceinline__ int padded(int i) {
+  return i + 4 * (i / F2Cfg<M>::kR);
 }
 
 // Shared memory: fixed part, then the two raw buffers (dynamic size).
@@ -87,8 +68,8 @@ template <int M>
 struct F2Smem {
   float xs[kTB + 1][F2Cfg<M>::kLd];  // row l: x_{t0+l}; row 0 carried in
   float qs[kTB][F2Cfg<M>::kLd];      // phi(q_{t0+l})
-  float eta[kTB][32], gam[kTB][32], vs[kTB][32], os[kTB][32];
-  float Es[kTB], xqs[kTB];
+  float4 tok[kTB];  // 1 / (||x||^2 + lambda + eps) (0: no write), lambda, <x, x_next>, <x, phi(q)>
+  float os[kTB][F2Cfg<M>::kCols];
   uint64_t full[2];
   int fail;
 };
@@ -107,24 +88,63 @@ __host__ __device__ inline RawLayout raw_layout(int M, int dv, int es) {
   return L;
 }
 
+// n consecutive elements (n a multiple of 8) of a raw bf16 or fp32 row buffer
+// in shared memory, by 16-byte loads, as fp32.
+template <int N>
+__device__ __forceinline__ void load_raw(const unsigned char* p, int64_t e0, int dtype,
+                                         float* out) {
+  if (dtype == FALCON_BF16) {
+    const uint4* v = reinterpret_cast<const uint4*>(p + 2 * e0);
+#pragma unroll
+    for (int c = 0; c < N / 8; ++c) {
+      const uint4 pk = v[c];
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&pk);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(h[e]);
+        out[8 * c + 2 * e] = f.x;
+        out[8 * c + 2 * e + 1] = f.y;
+      }
+    }
+  } else {
+    const float4* v = reinterpret_cast<const float4*>(p + 4 * e0);
+#pragma unroll
+    for (int c = 0; c < N / 4; ++c) {
+      const float4 f = v[c];
+      out[4 * c] = f.x;
+      out[4 * c + 1] = f.y;
+      out[4 * c + 2] = f.z;
+      out[4 * c + 3] = f.w;
+    }
+  }
+}
+
+// Sum over the kP threads of a column (adjacent lanes).
 template <int M>
-__global__ void __launch_bounds__(F2Cfg<M>::kThreads)
+__device__ __forceinline__ float column_sum(float v) {
+#pragma unroll
+  for (int o = 1; o < F2Cfg<M>::kP; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+template <int M, bool kF2>
+__global__ void __launch_bounds__(kThreads)
     falcon2_recurrent_kernel(ChunkArgs a, int ncg, int* err) {
   using C = F2Cfg<M>;
+  constexpr int kR = C::kR, kP = C::kP, kCols = C::kCols, kH = M / 2;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   F2Smem<M>& sm = *reinterpret_cast<F2Smem<M>*>(smem_raw);
   const int es = a.dtype == FALCON_BF16 ? 2 : 4;
   const RawLayout R = raw_layout(M, a.dv, es);
   unsigned char* raw0 = smem_raw + ((sizeof(F2Smem<M>) + 127) & ~size_t(127));
 
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x;
   const int64_t bh = blockIdx.x / ncg;
   const int cg = blockIdx.x % ncg;
-  const int cl = tid / C::kP;    // local column
-  const int part = tid % C::kP;  // rows 16 part .. 16 part + 15
-  const int col = cg * 32 + cl;
+  const int cl = tid / kP;    // local column
+  const int part = tid % kP;  // rows kR part .. kR part + kR - 1
+  const int col = cg * kCols + cl;
   const bool active = col < a.dv;
-  const bool f2 = a.rule == kFalcon2;
   const int64_t T = a.T;
   const int64_t nblk = (T + kTB - 1) / kTB;
   volatile int* fail = &sm.fail;
@@ -146,12 +166,12 @@ __global__ void __launch_bounds__(F2Cfg<M>::kThreads)
     bulk_g2s(buf + R.b, a.beta + row * a.dv, bb, &sm.full[b & 1]);
   };
 
-  float s[16];
+  float s[kR];  // rows kR part .. kR part + kR - 1 of this column
 #pragma unroll
-  for (int i = 0; i < 16; ++i)
-    s[i] = (active && a.S0) ? a.S0[(bh * M + 16 * part + i) * a.dv + col] : 0.f;
-  for (int i = tid; i < M; i += C::kThreads)
-    sm.xs[0][pad16(i)] = a.x_prev ? a.x_prev[bh * M + i] : 0.f;
+  for (int i = 0; i < kR; ++i)
+    s[i] = (active && a.S0) ? a.S0[(bh * M + kR * part + i) * a.dv + col] : 0.f;
+  for (int i = tid; i < M; i += kThreads)
+    sm.xs[0][padded<M>(i)] = a.x_prev ? a.x_prev[bh * M + i] : 0.f;
   const bool sentinel0 = a.x_prev == nullptr;
   if (tid == 0) {
     mbar_init(&sm.full[0], 1);
@@ -161,144 +181,140 @@ __global__ void __launch_bounds__(F2Cfg<M>::kThreads)
     if (nblk > 0) request(0);
   }
   __syncthreads();
+  // x of the next token to write (this thread's rows, registers), and
+  // p = s^T x for it.
+  float xc[kR];
+  {
+    const float4* x4 = reinterpret_cast<const float4*>(sm.xs[0] + C::kSeg * part);
+#pragma unroll
+    for (int c = 0; c < kR / 4; ++c) {
+      const float4 f = x4[c];
+      xc[4 * c] = f.x;
+      xc[4 * c + 1] = f.y;
+      xc[4 * c + 2] = f.z;
+      xc[4 * c + 3] = f.w;
+    }
+  }
+  float p = 0.f;
+  if constexpr (kF2) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < kR; ++i) acc[i & 3] = fmaf(s[i], xc[i], acc[i & 3]);
+    p = column_sum<M>((acc[0] + acc[1]) + (acc[2] + acc[3]));
+  }
 
+  const int hl = tid >> 1, hh = tid & 1;  // staging: row hl, half row hh
   for (int64_t b = 0; b < nblk; ++b) {
     const int64_t t0 = b * kTB;
     const int nb = (int)min((int64_t)kTB, T - t0);
     const unsigned char* buf = raw0 + (b & 1) * R.bytes;
+    const float lam_raw = (hh == 0 && hl < nb) ? a.lambda[bh * T + t0 + hl] : 0.f;
     if (!mbar_wait(&sm.full[b & 1], (uint32_t)(b >> 1) & 1u)) *fail = 1;
     // Every thread has passed the wait; the other buffer (block b - 1) is
     // consumed: request block b + 1 into it.
     __syncthreads();
     if (*fail) break;
     if (tid == 0 && b + 1 < nblk) request(b + 1);
-    const float lam_l = (lane < nb) ? a.lambda[bh * T + t0 + lane] : 0.f;
-    // ---- phi(k) -> x of the next token, phi(q).  Thread (l, g) = (tid / kP,
-    // tid % kP) takes elements 16g .. 16g + 15 of row l; the kP threads of a
-    // row are adjacent lanes and combine their sums by shuffles.
-    const int sl = tid / C::kP, sg = tid % C::kP;
-    {
-      float kk[16], qq[16];
-      const int64_t e0 = (int64_t)sl * M + 16 * sg;
-      load16(buf + R.k, e0, a.dtype, sl < nb, kk);
-      load16(buf + R.q, e0, a.dtype, sl < nb, qq);
-      float sk = 0.f, sq = 0.f;
+    // ---- phi(k) -> x of the next token, then phi(q): two threads per row
+    //      (half rows of M / 2 elements), sums combined by one shuffle
+#pragma unroll 1
+    for (int which = 0; which < 2; ++which) {
+      float kk[kH];
+      float sk = 0.f;
+      if (hl < nb) {
+        load_raw<kH>(buf + (which ? R.q : R.k), (int64_t)hl * M + kH * hh, a.dtype, kk);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        sk += kk[i] * kk[i];
-        sq += qq[i] * qq[i];
+        for (int i = 0; i < kH; ++i) sk = fmaf(kk[i], kk[i], sk);
       }
+      sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+      if (hl < nb) {
+        const float fk = feature_scale(sk, M, a.phi);
+        float* xr = which ? sm.qs[hl] : sm.xs[hl + 1];
 #pragma unroll
-      for (int o = 1; o < C::kP; o <<= 1) {
-        sk += __shfl_xor_sync(0xffffffffu, sk, o);
-        sq += __shfl_xor_sync(0xffffffffu, sq, o);
-      }
-      const float fk = feature_scale(sk, M, a.phi), fq = feature_scale(sq, M, a.phi);
-      if (sl < nb) {
-        float* xr = &sm.xs[sl + 1][20 * sg];
-        float* qr = &sm.qs[sl][20 * sg];
-#pragma unroll
-        for (int i4 = 0; i4 < 4; ++i4) {
-          *reinterpret_cast<float4*>(xr + 4 * i4) =
+        for (int i4 = 0; i4 < kH / 4; ++i4)
+          *reinterpret_cast<float4*>(xr + padded<M>(kH * hh + 4 * i4)) =
               make_float4(kk[4 * i4] * fk, kk[4 * i4 + 1] * fk, kk[4 * i4 + 2] * fk,
                           kk[4 * i4 + 3] * fk);
-          *reinterpret_cast<float4*>(qr + 4 * i4) =
-              make_float4(qq[4 * i4] * fq, qq[4 * i4 + 1] * fq, qq[4 * i4 + 2] * fq,
-                          qq[4 * i4 + 3] * fq);
-        }
       }
     }
     __syncthreads();
-    // ---- ||x_t||^2 and <x_t, phi(q_t)> (x_t = row l of xs, written by row l - 1)
+    // ---- per token: ||x_t||^2, <x_t, x_{t+1}>, <x_t, phi(q_t)> (x_t = row l
+    //      of xs, x_{t+1} = row l + 1), lambda_t and 1 / (||x_t||^2 + lambda_t + eps)
     {
-      float se = 0.f, sxq = 0.f;
-      if (sl < nb) {
+      float se = 0.f, sg = 0.f, sxq = 0.f;
+      if (hl < nb) {
 #pragma unroll
-        for (int i4 = 0; i4 < 4; ++i4) {
-          const float4 xv = *reinterpret_cast<const float4*>(&sm.xs[sl][20 * sg + 4 * i4]);
-          const float4 qv = *reinterpret_cast<const float4*>(&sm.qs[sl][20 * sg + 4 * i4]);
-          se += xv.x * xv.x + xv.y * xv.y + xv.z * xv.z + xv.w * xv.w;
-          sxq += xv.x * qv.x + xv.y * qv.y + xv.z * qv.z + xv.w * qv.w;
+        for (int i4 = 0; i4 < kH / 4; ++i4) {
+          const int e = padded<M>(kH * hh + 4 * i4);
+          const float4 x = *reinterpret_cast<const float4*>(sm.xs[hl] + e);
+          const float4 xn = *reinterpret_cast<const float4*>(sm.xs[hl + 1] + e);
+          const float4 qv = *reinterpret_cast<const float4*>(sm.qs[hl] + e);
+          se = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, fmaf(x.w, x.w, se))));
+          sg = fmaf(x.x, xn.x, fmaf(x.y, xn.y, fmaf(x.z, xn.z, fmaf(x.w, xn.w, sg))));
+          sxq = fmaf(x.x, qv.x, fmaf(x.y, qv.y, fmaf(x.z, qv.z, fmaf(x.w, qv.w, sxq))));
         }
       }
-#pragma unroll
-      for (int o = 1; o < C::kP; o <<= 1) {
-        se += __shfl_xor_sync(0xffffffffu, se, o);
-        sxq += __shfl_xor_sync(0xffffffffu, sxq, o);
-      }
-      if (sg == 0 && sl < nb) {
-        sm.Es[sl] = se;
-        sm.xqs[sl] = sxq;
-      }
-    }
-    __syncthreads();
-    // ---- eta, gamma and v of every (token, column) of the block
-    // (a warp's 32 threads take the 32 columns of one token, so l is uniform
-    // in the warp and lambda_l comes from lane l by one shuffle)
-    for (int p = tid; p < kTB * 32; p += C::kThreads) {
-      const int l = p >> 5, c = p & 31;
-      const int gc = cg * 32 + c;
-      const float lam = ridge_of(__shfl_sync(0xffffffffu, lam_l, l), sm.Es[l], a.ridge);
-      if (l < nb && gc < a.dv) {
-        // eta_{j,t} and the clamped decay (as step_eta_gamma, without the log)
-        const bool sent = sentinel0 && (t0 + l == 0);
-        const float beta = reinterpret_cast<const float*>(buf + R.b)[l * a.dv + gc];
-        const float den = sm.Es[l] + lam + a.eps;
-        const float eta = (!sent && den > 0.f) ? beta / den : 0.f;
-        const float al = eta * lam;
-        sm.eta[l][c] = eta;
-        sm.gam[l][c] = (al >= 1.f - a.eps_gamma) ? a.eps_gamma : 1.f - al;
-        sm.vs[l][c] = load_elem(buf + R.v, (int64_t)l * a.dv + gc, a.dtype);
-      } else if (l < nb) {
-        sm.eta[l][c] = 0.f;
-        sm.gam[l][c] = 1.f;
-        sm.vs[l][c] = 0.f;
+      se += __shfl_xor_sync(0xffffffffu, se, 1);
+      sg += __shfl_xor_sync(0xffffffffu, sg, 1);
+      sxq += __shfl_xor_sync(0xffffffffu, sxq, 1);
+      if (hh == 0 && hl < nb) {
+        const float lam = ridge_of(lam_raw, se, a.ridge);
+        const float den = se + lam + a.eps;
+        const bool sent = sentinel0 && t0 + hl == 0;  // x_1 = 0: no write
+        sm.tok[hl] = make_float4((!sent && den > 0.f) ? 1.f / den : 0.f, lam, sg, sxq);
       }
     }
     __syncthreads();
 
-    // ---- the tokens of the block, in order
-#pragma unroll 2
+    // ---- the tokens of the block, in order: both reads with the state before
+    //      the write, and the write, in one pass over this thread's rows
+    const float* braw = reinterpret_cast<const float*>(buf + R.b);
+#pragma unroll 1
     for (int l = 0; l < nb; ++l) {
-      float x[16], q[16];
+      const float4 tk = sm.tok[l];
+      const float beta = active ? braw[l * a.dv + col] : 0.f;
+      const float v = active ? load_elem(buf + R.v, (int64_t)l * a.dv + col, a.dtype) : 0.f;
+      const float eta = beta * tk.x;
+      const float al = eta * tk.y;
+      const float gam = (al >= 1.f - a.eps_gamma) ? a.eps_gamma : 1.f - al;
+      const float er = eta * (kF2 ? v - p : v);
+      const float4* xn4 = reinterpret_cast<const float4*>(sm.xs[l + 1] + C::kSeg * part);
+      const float4* q4 = reinterpret_cast<const float4*>(sm.qs[l] + C::kSeg * part);
+      float aa[4] = {0.f, 0.f, 0.f, 0.f}, bb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i4 = 0; i4 < 4; ++i4) {
-        const float4 xv = *reinterpret_cast<const float4*>(&sm.xs[l][20 * part + 4 * i4]);
-        const float4 qv = *reinterpret_cast<const float4*>(&sm.qs[l][20 * part + 4 * i4]);
-        x[4 * i4] = xv.x; x[4 * i4 + 1] = xv.y; x[4 * i4 + 2] = xv.z; x[4 * i4 + 3] = xv.w;
-        q[4 * i4] = qv.x; q[4 * i4 + 1] = qv.y; q[4 * i4 + 2] = qv.z; q[4 * i4 + 3] = qv.w;
+      for (int c = 0; c < kR / 4; ++c) {
+        const float4 q = q4[c];
+        bb[0] = fmaf(s[4 * c], q.x, bb[0]);
+        bb[1] = fmaf(s[4 * c + 1], q.y, bb[1]);
+        bb[2] = fmaf(s[4 * c + 2], q.z, bb[2]);
+        bb[3] = fmaf(s[4 * c + 3], q.w, bb[3]);
+        const float4 f = xn4[c];
+        if constexpr (kF2) {
+          aa[0] = fmaf(s[4 * c], f.x, aa[0]);
+          aa[1] = fmaf(s[4 * c + 1], f.y, aa[1]);
+          aa[2] = fmaf(s[4 * c + 2], f.z, aa[2]);
+          aa[3] = fmaf(s[4 * c + 3], f.w, aa[3]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s[4 * c + i] = fmaf(gam, s[4 * c + i], er * xc[4 * c + i]);
+        xc[4 * c] = f.x;
+        xc[4 * c + 1] = f.y;
+        xc[4 * c + 2] = f.z;
+        xc[4 * c + 3] = f.w;
       }
-      float pa0 = 0.f, pa1 = 0.f, pb0 = 0.f, pb1 = 0.f;
-#pragma unroll
-      for (int i = 0; i < 16; i += 2) {
-        pa0 += s[i] * x[i];
-        pa1 += s[i + 1] * x[i + 1];
-        pb0 += s[i] * q[i];
-        pb1 += s[i + 1] * q[i + 1];
-      }
-      float pa = pa0 + pa1, pb = pb0 + pb1;  // s_j^T x_t, s_j^T phi(q_t) (before the write)
-#pragma unroll
-      for (int o = 1; o < C::kP; o <<= 1) {
-        pa += __shfl_xor_sync(0xffffffffu, pa, o);
-        pb += __shfl_xor_sync(0xffffffffu, pb, o);
-      }
-      const float eta = sm.eta[l][cl], gamma = sm.gam[l][cl];
-      const float r = f2 ? sm.vs[l][cl] - pa : sm.vs[l][cl];
-      const float er = eta * r;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) s[i] = gamma * s[i] + er * x[i];
-      // every thread of the column holds the full sums: all write o (one
-      // address per column), which keeps the loop free of a divergent branch
-      sm.os[l][cl] = gamma * pb + er * sm.xqs[l];
+      const float bv = column_sum<M>((bb[0] + bb[1]) + (bb[2] + bb[3]));
+      // s_t^T x_{t+1}, the next token's residual product
+      if constexpr (kF2) p = fmaf(gam, column_sum<M>((aa[0] + aa[1]) + (aa[2] + aa[3])), er * tk.z);
+      if (part == 0) sm.os[l][cl] = fmaf(gam, bv, er * tk.w);
     }
     __syncthreads();
     // o of the block (coalesced), and x of the next block's first token
-    for (int p = tid; p < nb * 32; p += C::kThreads) {
-      const int l = p >> 5, c = p & 31;
-      if (cg * 32 + c < a.dv)
-        store_elem(a.o, (bh * T + t0 + l) * a.dv + cg * 32 + c, sm.os[l][c], a.dtype);
+    for (int p2 = tid; p2 < nb * kCols; p2 += kThreads) {
+      const int l = p2 / kCols, c = p2 % kCols;
+      if (cg * kCols + c < a.dv)
+        store_elem(a.o, (bh * T + t0 + l) * a.dv + cg * kCols + c, sm.os[l][c], a.dtype);
     }
-    for (int i = tid; i < M; i += C::kThreads) sm.xs[0][pad16(i)] = sm.xs[nb][pad16(i)];
+    for (int i = tid; i < M; i += kThreads) sm.xs[0][padded<M>(i)] = sm.xs[nb][padded<M>(i)];
   }
   __syncthreads();
   if (*fail) {
@@ -307,22 +323,25 @@ __global__ void __launch_bounds__(F2Cfg<M>::kThreads)
   }
   if (active) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) a.S_out[(bh * M + 16 * part + i) * a.dv + col] = s[i];
+    for (int i = 0; i < kR; ++i) a.S_out[(bh * M + kR * part + i) * a.dv + col] = s[i];
   }
   if (a.x_last && cg == 0)
-    for (int i = tid; i < M; i += C::kThreads) a.x_last[bh * M + i] = sm.xs[0][pad16(i)];
+    for (int i = tid; i < M; i += kThreads) a.x_last[bh * M + i] = sm.xs[0][padded<M>(i)];
 }
 
 template <int M>
 cudaError_t launch_m(const ChunkArgs& a, int* err, cudaStream_t stream) {
-  const int ncg = (a.dv + 31) / 32;
+  const int ncg = (a.dv + F2Cfg<M>::kCols - 1) / F2Cfg<M>::kCols;
   const int64_t grid = a.BH * ncg;
   const int es = a.dtype == FALCON_BF16 ? 2 : 4;
-  const size_t smem = ((sizeof(F2Smem<M>) + 127) & ~size_t(127)) + 2 * raw_layout(M, a.dv, es).bytes;
-  cudaError_t e = cudaFuncSetAttribute(falcon2_recurrent_kernel<M>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const size_t smem =
+      ((sizeof(F2Smem<M>) + 127) & ~size_t(127)) + 2 * raw_layout(M, a.dv, es).bytes;
+  auto kernel = a.rule == kFalcon2 ? falcon2_recurrent_kernel<M, true>
+                                   : falcon2_recurrent_kernel<M, false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
   if (e != cudaSuccess) return e;
-  falcon2_recurrent_kernel<M><<<(unsigned)grid, F2Cfg<M>::kThreads, smem, stream>>>(a, ncg, err);
+  kernel<<<(unsigned)grid, kThreads, smem, stream>>>(a, ncg, err);
   return cudaGetLastError();
 }
 
