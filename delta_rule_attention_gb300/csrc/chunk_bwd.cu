@@ -64,8 +64,9 @@ __host__ __device__ inline BwdLayout bwd_layout(int64_t BH, int64_t T, int m, in
   return L;
 }
 
-// Tensor-core path: the forward's bf16 maps, the recomputed forward's o and
-// S_T (written, not used), then the same state and cotangent buffers.
+// Tensor-core path: the forward's bf16 maps, then the state and cotangent
+// buffers, then room for the recomputed forward's o (its tensor map needs a
+// buffer; the recording scan writes no o) and S_T (written, not used).
 BwdLayout tc_bwd_layout(int64_t BH, int64_t T) {
   const int64_t nch = (T + 63) / 64;
   BwdLayout L;
@@ -588,7 +589,11 @@ cudaError_t launch_bwd_chunked(const BwdArgs& b, int* err, cudaStream_t stream) 
     f.o = ws + L.o;
     f.S_out = ws + L.S_out;
     f.S_starts = ws + L.S_starts;
-    e = launch_tc_chunked(f, err, stream);
+    // the maps, then the scan that records the state entering every chunk
+    // (no o) and the reverse scan of the state cotangent over the same maps
+    e = launch_tc_map64(f, err, stream);
+    if (e == cudaSuccess) e = launch_tc_scan64(f, err, stream);
+    if (e == cudaSuccess) e = launch_tc_bwd_scan(b, ws + L.maps, ws + L.dS_ends, err, stream);
   } else {
     f.o = nullptr;
     f.S_out = nullptr;
@@ -596,10 +601,9 @@ cudaError_t launch_bwd_chunked(const BwdArgs& b, int* err, cudaStream_t stream) 
   }
   if (e != cudaSuccess) return e;
 
-  // 2. reverse scan of the state cotangent, 3. per-chunk gradients
+  // 2. reverse scan of the state cotangent (tensor-core path: above),
+  // 3. per-chunk gradients
   if (tc) {
-    e = launch_tc_bwd_scan(b, ws + L.maps, ws + L.dS_ends, err, stream);
-    if (e != cudaSuccess) return e;
     // dq, dv, dbeta, dlambda and dk (the chunk-end tokens by a small kernel)
     return launch_tc_bwd_grad(b, ws + L.S_starts, ws + L.dS_ends, ws + L.dX, err, stream);
   } else {

@@ -36,6 +36,7 @@
 #include <cuda_bf16.h>
 
 #include <atomic>
+#include <type_traits>
 
 #include <mutex>
 
@@ -747,25 +748,32 @@ teardown:
 // the output rows run beside the chain, and the accumulator is
 // double-buffered in TMEM.  Every hand-off is one mbarrier arrival per warp.
 constexpr int kStages = kScanRing;
+// The recording variant (the backward's recomputed forward: no o, the state
+// entering every chunk written out) keeps four stages and no o staging.
+constexpr int kRecStages = 4;
 constexpr int kScanMathWarps = 16;
 constexpr int kScanThreads = 32 * (kScanMathWarps + 2);
 
-struct ScanSmem {
-  unsigned char mc[kStages][kMcBytes];  // A tiles of the state MMA (K-major)
-  unsigned char nc[kStages][kNcBytes];  // Nc rows (bf16, 16-byte chunks swizzled)
-  unsigned char sop[8192];              // S as MN-major B operand (rows = m, 64 bf16 along d_v)
-  unsigned char ostage[2][8192];        // o tiles (64 tokens x 64 bf16, 128B-swizzled) for TMA
-  float gc[kStages][4];
-  uint64_t full[kStages];   // map of the stage has arrived
-  uint64_t empty[kStages];  // every math warp is done with the stage
+template <int kSt, bool kOut>
+struct ScanSmemT {
+  unsigned char mc[kSt][kMcBytes];  // A tiles of the state MMA (K-major)
+  unsigned char nc[kSt][kNcBytes];  // Nc rows (bf16, 16-byte chunks swizzled)
+  unsigned char sop[8192];          // S as MN-major B operand (rows = m, 64 bf16 along d_v)
+  unsigned char ostage[kOut ? 2 : 1][kOut ? 8192 : 16];  // o tiles (64 x 64 bf16) for TMA
+  float gc[kSt][4];
+  uint64_t full[kSt];   // map of the stage has arrived
+  uint64_t empty[kSt];  // every math warp is done with the stage
   uint64_t mma_done[2];     // MMA into accumulator buffer b has completed
   uint64_t o_done[2];       // output warps have read accumulator buffer b
   uint64_t s_ready;         // the next state operand is in sop
   uint32_t tmem_base;
   int fail;
 };
+using ScanSmem = ScanSmemT<kStages, true>;
+using RecScanSmem = ScanSmemT<kRecStages, false>;
 
-__device__ __forceinline__ void issue_map_load(ScanSmem& s, int st, const unsigned char* m) {
+template <typename Smem>
+__device__ __forceinline__ void issue_map_load(Smem& s, int st, const unsigned char* m) {
   mbar_expect_tx(&s.full[st], kMcBytes + kNcBytes + 16);
   bulk_g2s(s.mc[st], m, kMcBytes, &s.full[st]);
   bulk_g2s(s.nc[st], m + kMcBytes, kNcBytes, &s.full[st]);
@@ -787,13 +795,16 @@ __device__ __forceinline__ void add_bf16x16(float* d, uint4 p0, uint4 p1) {
   }
 }
 
-// kRecord: also write the state entering every chunk to a.S_starts.
+// kRecord: write the state entering every chunk to a.S_starts and no o (the
+// output warps stay idle; four map stages).
 template <bool kRecord>
 __global__ void __launch_bounds__(kScanThreads, 1)
     tc_chunk_scan_kernel(ChunkArgs a, int nchunks, int c_begin, int n, const float* S_in, int* err,
                          const __grid_constant__ CUtensorMap tm_o) {
+  using Smem = std::conditional_t<kRecord, RecScanSmem, ScanSmem>;
+  constexpr int kSt = kRecord ? kRecStages : kStages;
   extern __shared__ unsigned char smem_raw[];
-  ScanSmem& s = *reinterpret_cast<ScanSmem*>(align1024(smem_raw));
+  Smem& s = *reinterpret_cast<Smem*>(align1024(smem_raw));
   volatile int* fail = &s.fail;
   const int64_t bh = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -812,9 +823,9 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (warp == 0) tmem_alloc(&s.tmem_base, 128);
   if (tid == 0) {
-    for (int st = 0; st < kStages; ++st) {
+    for (int st = 0; st < kSt; ++st) {
       mbar_init(&s.full[st], 1);
-      mbar_init(&s.empty[st], kScanMathWarps);
+      mbar_init(&s.empty[st], kRecord ? kScanMathWarps / 2 : kScanMathWarps);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s.mma_done[b], 1);
@@ -839,15 +850,17 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 
   if (issuer) {
     if (lane == 0) {
-      for (int st = 0; st < kStages && st < n; ++st)
+      for (int st = 0; st < kSt && st < n; ++st)
         issue_map_load(s, st, ws + (size_t)st * kMapBytes);
       const uint64_t bdesc = sw128_desc(smem_addr(s.sop), 8192, 1024);
       const uint32_t idesc = idesc_bf16(128, 64, false, true);
       for (int c = 0; c < n; ++c) {
-        const int st = c % kStages, b = c & 1;
-        // The state operand is the last to be ready: wait for it last.
-        bool ok = c < 2 || mbar_wait(&s.o_done[b], (uint32_t)((c - 2) >> 1) & 1u);
-        ok = ok && mbar_wait(&s.full[st], (uint32_t)(c / kStages) & 1u);
+        const int st = c % kSt, b = c & 1;
+        // The state operand is the last to be ready: wait for it last.  (The
+        // state rows of accumulator b were read before the operand of chunk
+        // c - 1 was signalled; without o nothing else reads it.)
+        bool ok = kRecord || c < 2 || mbar_wait(&s.o_done[b], (uint32_t)((c - 2) >> 1) & 1u);
+        ok = ok && mbar_wait(&s.full[st], (uint32_t)(c / kSt) & 1u);
         ok = ok && mbar_wait(&s.s_ready, (uint32_t)c & 1u);
         if (!ok) {
           *fail = 1;
@@ -861,17 +874,17 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     }
     __syncwarp();
   } else if (refiller) {
-    // The stage of chunk c gets chunk c + kStages once every math warp is done
+    // The stage of chunk c gets chunk c + kSt once every math warp is done
     // with it (the MMA of chunk c has then completed too).
     if (lane == 0) {
-      for (int c = 0; c + kStages < n; ++c) {
+      for (int c = 0; c + kSt < n; ++c) {
         if (*fail) break;
-        const int st = c % kStages;
-        if (!mbar_wait(&s.empty[st], (uint32_t)(c / kStages) & 1u)) {
+        const int st = c % kSt;
+        if (!mbar_wait(&s.empty[st], (uint32_t)(c / kSt) & 1u)) {
           *fail = 1;
           break;
         }
-        issue_map_load(s, st, ws + (size_t)(c + kStages) * kMapBytes);
+        issue_map_load(s, st, ws + (size_t)(c + kSt) * kMapBytes);
       }
     }
     __syncwarp();
@@ -893,8 +906,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         for (int q4 = 0; q4 < 4; ++q4)
           dst[q4] = make_float4(S[4 * q4], S[4 * q4 + 1], S[4 * q4 + 2], S[4 * q4 + 3]);
       }
-      const int st = c % kStages, b = c & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&s.full[st], (uint32_t)(c / kStages) & 1u))) {
+      const int st = c % kSt, b = c & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&s.full[st], (uint32_t)(c / kSt) & 1u))) {
         *fail = 1;
         break;
       }
@@ -923,7 +936,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         mbar_arrive(&s.empty[st]);  // Nc read; the MMA has read Mc
       }
     }
-  } else {
+  } else if constexpr (!kRecord) {
     // ---- output warps: o rows, off the chain.  The o tile of a chunk leaves
     // by one TMA store issued by the first lane of warp 2; rows past T are
     // dropped by the tensor map.  Exits are agreed on by all output warps at
@@ -932,8 +945,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     const bool o_issuer = warp == 2 && lane == 0;
     constexpr int kOutThreads = 32 * kScanMathWarps / 2;
     for (int c = 0; c < n; ++c) {
-      const int st = c % kStages, b = c & 1;
-      bool ok = !*fail && mbar_wait(&s.full[st], (uint32_t)(c / kStages) & 1u);
+      const int st = c % kSt, b = c & 1;
+      bool ok = !*fail && mbar_wait(&s.full[st], (uint32_t)(c / kSt) & 1u);
       uint4 n0 = make_uint4(0u, 0u, 0u, 0u), n1 = n0;
       if (ok) {
         const unsigned char* nrow = s.nc[st] + row * 128;
@@ -1418,7 +1431,7 @@ cudaError_t launch_scan_range(const ChunkArgs& a, int nchunks, int c_begin, int 
                        stream);
   if (a.S_starts)
     return launch_scan(tc_chunk_scan_kernel<true>, (unsigned)a.BH, kScanThreads,
-                       sizeof(ScanSmem) + 1024, pdl, a, nchunks, c_begin, n, S_in, err, tm_o,
+                       sizeof(RecScanSmem) + 1024, pdl, a, nchunks, c_begin, n, S_in, err, tm_o,
                        stream);
   return launch_scan(tc_chunk_scan_kernel<false>, (unsigned)a.BH, kScanThreads,
                      sizeof(ScanSmem) + 1024, pdl, a, nchunks, c_begin, n, S_in, err, tm_o,
@@ -1476,5 +1489,16 @@ cudaError_t launch_tc_scan64(const ChunkArgs& a, int* err, cudaStream_t stream) 
 cudaError_t launch_tc_chunked(const ChunkArgs& a, int* err, cudaStream_t stream) {
   return a.m == 128 ? launch_tc<128>(a, err, stream) : launch_tc<64>(a, err, stream);
 }
+
+cudaError_t launch_tc_map64(const ChunkArgs& a, int* err, cudaStream_t stream) {
+  const int nchunks = (int)((a.T + kC - 1) / kC);
+  CUtensorMap tm_k, tm_q, tm_v;
+  if (!encode_rows_bf16(&tm_k, a.k, 64, (uint64_t)a.T, (uint64_t)a.BH, 64, kC) ||
+      !encode_rows_bf16(&tm_q, a.q, 64, (uint64_t)a.T, (uint64_t)a.BH, 64, kC) ||
+      !encode_rows_bf16(&tm_v, a.v, 64, (uint64_t)a.T, (uint64_t)a.BH, 64, kC))
+    return cudaErrorInvalidValue;
+  return launch_map<64>(a, nchunks, 0, nchunks, err, tm_k, tm_q, tm_v, true, stream);
+}
+
 
 }  // namespace falcon

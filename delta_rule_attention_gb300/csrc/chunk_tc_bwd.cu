@@ -775,9 +775,7 @@ constexpr uint32_t kRevStage = kMcBytes + kTile;  // Mc | dO_c
 
 struct RevSmem {
   unsigned char stage[kRevStages][kRevStage];
-  // dS' as the MN-major B operand; it also takes the unused M-atom that the
-  // output MMA of the last stage reads past that stage (lanes 64..127).
-  unsigned char op[kTile];
+  unsigned char op[kTile];  // dS' as the MN-major B operand
   float gc[kRevStages][4];
   uint64_t full[kRevStages];   // the stage has landed
   uint64_t empty[kRevStages];  // both MMAs and the state warps are done with the stage
@@ -838,17 +836,20 @@ __global__ void __launch_bounds__(kRevThreads)
           break;
         }
         tc_fence_after();
-        // K rows 64..127: the output rows of Mc with dO_c (the second M-atom
-        // of A, LBO on, reads past them into lanes 64..127, unused).
-        mma_k64(tmem + 64 * bb, stg + 8192, true, kMcBytes, stg + kMcBytes, true, kTile, idesc,
+        // K rows 64..127: the output rows of Mc with dO_c.  A has two
+        // M-atoms; the second (lanes 64..127, never read) is taken LBO = 8 KB
+        // on, inside this stage, so that no MMA reads a stage the refill warp
+        // may be writing.
+        mma_k64(tmem + 64 * bb, stg + 8192, true, kTile, stg + kMcBytes, true, kTile, idesc,
                 false);
         if (!mbar_wait(&s.s_ready, (uint32_t)k & 1u)) {
           *fail = 1;
           break;
         }
         tc_fence_after();
-        // K rows 0..63: the state rows of Mc with dS'.
-        mma_k64(tmem + 64 * bb, stg, true, kMcBytes, smem_addr(s.op), true, kTile, idesc, true);
+        // K rows 0..63: the state rows of Mc with dS' (unused M-atom: the
+        // output rows of the same stage).
+        mma_k64(tmem + 64 * bb, stg, true, kTile, smem_addr(s.op), true, kTile, idesc, true);
         mma_commit(&s.mma_done[bb]);
         mma_commit(&s.empty[st]);
       }

@@ -110,6 +110,8 @@ size_t tc_workspace_bytes(int m, int64_t BH, int64_t T);
 cudaError_t launch_tc_chunked(const ChunkArgs& a, int* err, cudaStream_t stream);
 // The m = 64 tensor-core scan alone, over maps already in a.workspace.
 cudaError_t launch_tc_scan64(const ChunkArgs& a, int* err, cudaStream_t stream);
+// The map launch alone (m = d_v = 64), by programmatic dependent launch.
+cudaError_t launch_tc_map64(const ChunkArgs& a, int* err, cudaStream_t stream);
 // Falcon-2A in chunk form on the tensor cores (bf16, m = dv = 64, chunk 64).
 bool tc_falcon2a_applies(int dtype, int m, int dv, int C, int64_t BH, int64_t T);
 size_t tc_falcon2a_workspace_bytes(int64_t BH, int64_t T);
