@@ -15,10 +15,11 @@ The line also carries
   roofline     achieved algorithmic HBM bytes per launch / launch time of
                the dominant kernel against the measured copy bandwidth;
   cpu_baseline the fp64 oracle on this host's cores on a bounded sample;
-  also         the other workloads (Falcon-1A, long context, decode).
+  also         the other workloads (Falcon-1A, long context, Falcon-2, Falcon-2A,
+               Falcon-3A, Falcon-1A with the normalised read, the backward, decode).
 
 `--impl reference` times the fp64 CPU oracle (the only reference this method
-has) on the same workload, a bounded sample per step.
+has) on the same workload: the whole lm workload (all 96 heads) per step.
 """
 from __future__ import annotations
 
@@ -477,6 +478,33 @@ def extra_workloads(falcon, dev):
                     "ms_per_call": secs * 1e3 / steps,
                     "hbm_frac": b / (secs / steps) / 1e9 / pk["hbm_gbs"]})
         del sets
+    # Falcon-1A with the normalised read (z) on the lm-1A shape, positive q, k
+    # (the setting in which the normaliser is attention-like); its bytes add
+    # z_T to the forward's
+    w = workloads.LM_1A
+    sets = input_sets(w, 2, dev)
+    for x in sets:
+        x["q"] = x["q"].abs() + 0.05
+        x["k"] = x["k"].abs() + 0.05
+    o = torch.empty((w.B, w.H, w.T, w.dv), dtype=w.dtype, device=dev)
+    S = torch.empty((w.B, w.H, w.m, w.dv), dtype=torch.float32, device=dev)
+    z = torch.empty((w.B, w.H, w.m), dtype=torch.float32, device=dev)
+    xl = torch.empty((w.B, w.H, w.m), dtype=torch.float32, device=dev)
+    shape = falcon.make_shape(w.B, w.H, w.T, w.m, w.dv, w.chunk, w.dtype, w.phi)
+    wsb = torch.empty(max(falcon.falcon_normalized_workspace_bytes(shape), 1), dtype=torch.uint8,
+                      device=dev)
+
+    def nstep(x):
+        falcon.falcon1a_fwd_chunked_normalized(x["q"], x["k"], x["v"], x["beta"], x["lambda"],
+                                               chunk=w.chunk, phi=w.phi, o=o, S_out=S, z_out=z,
+                                               x_last=xl, workspace=wsb)
+    steps = 200
+    secs = time_device(nstep, sets, steps, 3, 1)
+    b = algorithmic_bytes(w) + w.B * w.H * w.m * 4
+    out.append({"workload": w.name.replace("falcon1a_", "falcon1a_normalized_"),
+                "tokens_per_s": w.tokens * steps / secs, "ms_per_call": secs * 1e3 / steps,
+                "hbm_frac": b / (secs / steps) / 1e9 / pk["hbm_gbs"]})
+    del sets, wsb
     # backward of the chunked forward (lm shapes): gradients for q, k, v, beta,
     # lambda, S0 and x_prev from a seeded dO
     for w in (workloads.LM, workloads.LM_1A):
