@@ -24,11 +24,13 @@
 // format of the Falcon-1 tensor-core forward (Mc, Nc as bf16 operand images,
 // e^{g_C}); tc_chunk_scan_kernel then produces o and S_T.
 //
-// One CTA per (head, chunk), 256 threads, two CTAs per SM.  MMAs (bf16
-// operands in 128B-swizzled tiles, fp32 accumulators in TMEM):
+// One CTA per (head, chunk), 256 threads, three CTAs per SM (74 KB of shared
+// memory, 128 TMEM columns).  MMAs (bf16 operands in 128B-swizzled tiles,
+// fp32 accumulators in TMEM):
 //   D1 = [Q; .] X~^T            (N = 128: the Gram rows of the chunk's q)
 //   D2 = (Q X~^T o W) V~        (K = 128 in two steps of 64)
 //   D3 = X~^T Diag(w_C) V~      (X~ read MN-major, K = 128)
+// D2 and D3 take the TMEM columns of D1 once it is read.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -47,27 +49,36 @@ constexpr int k3C = 64;
 constexpr int k3Threads = 256;
 constexpr uint32_t k3Tile = 8192;
 // Tile slots: X~ (two tiles: pairs t0-64 .. t0-1, t0 .. t0+63), Q, V~ (two),
-// Vs = Diag(w_C) V~ (two), W-masked Gram rows P (two column halves).  After
-// the last MMAs the map stages reuse them: Nc over Vs, Mc over P.
-enum : int { kX0 = 0, kX1, kQ3, kV0, kV1, kVs0, kVs1, kP0, kP1, k3Slots };
-constexpr int kLdW = 129;  // fp32 row stride of the coefficient matrix W (64 x 128)
-constexpr uint32_t kWOff = k3Slots * k3Tile;
-constexpr uint32_t kSc3Off = kWOff + 64 * kLdW * 4;
+// then a 32 KB region R whose contents follow each other as they die: the
+// row norms' partial sums and ||x_j||^2 (features), the fp32 coefficient
+// matrix W (64 x 128), then the W-masked Gram rows P (two column halves) and
+// Vs = Diag(w_C) V~ (two), and last the map stages, Mc over P and Nc over Vs.
+enum : int { kX0 = 0, kX1, kQ3, kV0, kV1, kP0, kP1, kVs0, kVs1, k3Slots };
+constexpr uint32_t kROff = kP0 * k3Tile;  // R: the last four slots
+constexpr uint32_t kSc3Off = k3Slots * k3Tile;
+// W[i][j] at float i * 128 + (j ^ (i & 31)): the recurrence writes a row with
+// consecutive lanes on consecutive columns and the P rows read a column run
+// with consecutive lanes on consecutive rows, both without bank conflicts.
+__device__ __forceinline__ int w_at(int i, int j) { return i * 128 + (j ^ (i & 31)); }
 
+// Scalars kept beside the tiles (the features' partial sums and ||x_j||^2
+// live in R while it is free).
 struct F3Scalars {
-  float E[128];     // ||x_j||^2 of the 128 pairs
   float wC[128];    // w_{C,j}: the coefficients of the state leaving the chunk
-  float w31[128];   // w_{31,j}, carried into the second half of the chunk
   float coef[64];   // eta_t / B_t
   float gam[64];
   float g[64], gx[64];
-  float ssp[2][128];
   int fail;
   uint64_t bar_in, bar_mma;
   uint32_t tmem_base;
 };
+struct F3Early {    // in R, before W
+  float ssp[2][128];
+  float E[128];     // ||x_j||^2 of the 128 pairs
+};
+static_assert(sizeof(F3Early) <= 4 * k3Tile, "features' scratch within R");
 constexpr size_t kF3Smem = kSc3Off + sizeof(F3Scalars) + 1024;
-static_assert(2 * (kF3Smem + 1024) <= 228 * 1024, "two CTAs per SM");
+static_assert(3 * (kF3Smem + 1024) <= 228 * 1024, "three CTAs per SM");
 
 // Generic-proxy tile writes of this CTA become visible to the next MMA.
 __device__ __forceinline__ void publish_tiles_f3() {
@@ -76,15 +87,16 @@ __device__ __forceinline__ void publish_tiles_f3() {
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(k3Threads, 2)
+__global__ void __launch_bounds__(k3Threads, 3)
     tc_falcon3a_map_kernel(ChunkArgs a, int window, int nchunks, int* err,
                            const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_q,
                            const __grid_constant__ CUtensorMap tm_v) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base = align1024(smem_raw);
-  float* W = reinterpret_cast<float*>(base + kWOff);
+  float* W = reinterpret_cast<float*>(base + kROff);
   F3Scalars& sc = *reinterpret_cast<F3Scalars*>(base + kSc3Off);
+  F3Early& ea = *reinterpret_cast<F3Early*>(base + kROff);
   auto tile = [&](int i) { return base + i * k3Tile; };
   auto taddr = [&](int i) { return smem_addr(base + i * k3Tile); };
 
@@ -97,7 +109,7 @@ __global__ void __launch_bounds__(k3Threads, 2)
 
   // TMEM is allocated by warp 1, so that thread 0 issues the input tile copies
   // (the head of the CTA's chain) without waiting for the allocation.
-  if (warp == 1) tmem_alloc(&sc.tmem_base, 256);
+  if (warp == 1) tmem_alloc(&sc.tmem_base, 128);
   // Launched behind the previous call's scan (programmatic dependent launch):
   // nothing is read or written before the preceding grid has completed.
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -130,21 +142,21 @@ __global__ void __launch_bounds__(k3Threads, 2)
   {
     float v[32];
     load_half_sw(tile(kX0), r, h, v);
-    sc.ssp[h][r] = sumsq32(v);
+    ea.ssp[h][r] = sumsq32(v);
     __syncthreads();
-    const float ss = sc.ssp[0][r] + sc.ssp[1][r];
+    const float ss = ea.ssp[0][r] + ea.ssp[1][r];
     const float s = phi_scale(ss, 64, a.phi);
     store_half_sw(tile(kX0), r, h, v, s);
-    if (h == 0) sc.E[r] = ss * s * s;
+    if (h == 0) ea.E[r] = ss * s * s;
     __syncthreads();
     const int qr = tid & 63, qh = (tid >> 6) & 1;
     if (tid < 128) {
       load_half_sw(tile(kQ3), qr, qh, v);
-      sc.ssp[qh][qr] = sumsq32(v);
+      ea.ssp[qh][qr] = sumsq32(v);
     }
     __syncthreads();
     if (tid < 128) {
-      const float sq = sc.ssp[0][qr] + sc.ssp[1][qr];
+      const float sq = ea.ssp[0][qr] + ea.ssp[1][qr];
       store_half_sw(tile(kQ3), qr, qh, v, phi_scale(sq, 64, a.phi));
     }
   }
@@ -157,7 +169,7 @@ __global__ void __launch_bounds__(k3Threads, 2)
       const int64_t j0 = max(t - window + 1, (int64_t)1);
       const int Bt = (int)(t - j0 + 1);
       float e = 0.f;
-      for (int u = 0; u < Bt; ++u) e += sc.E[64 + tid - u];
+      for (int u = 0; u < Bt; ++u) e += ea.E[64 + tid - u];
       const float Ebar = e / (float)Bt;
       const float lam = ridge_of(a.lambda[rowbase + t], Ebar, a.ridge);
       const float eta = step_eta_gamma(false, Ebar, a.beta[rowbase + t], lam, a.eps,
@@ -206,57 +218,73 @@ __global__ void __launch_bounds__(k3Threads, 2)
       const int64_t t = t0 + i;
       const bool in = jg >= 1 && jg <= t && t <= jg + window - 1;
       w = sc.gam[i] * w + (in ? sc.coef[i] : 0.f);
-      W[i * kLdW + col] = w;
+      W[w_at(i, col)] = w;
     }
-    if (hf == 0) sc.w31[col] = w;
     __syncthreads();
     if (hf == 1) {
-      const float w31 = sc.w31[col];
+      const float w31 = W[w_at(31, col)];
       float p = 1.f;
       for (int i = 32; i < 64; ++i) {
         p *= sc.gam[i];
-        W[i * kLdW + col] += p * w31;
+        W[w_at(i, col)] += p * w31;
       }
-      sc.wC[col] = W[63 * kLdW + col];
+      sc.wC[col] = W[w_at(63, col)];
     }
   }
   __syncthreads();
-  // Vs = Diag(w_C) V~ (rows r of the two V tiles)
+  if (!mbar_wait(&sc.bar_mma, phase)) sc.fail = 1;
+  phase ^= 1u;
+  tc_fence_after();
+  // P = (Q X~^T) o W, rows 0..63 (lanes 0..63), two column halves per tile:
+  // every thread reads its part of W before any P row is written over W.
+  {
+    uint32_t pk[2][16];
+    if ((warp & 3) < 2) {
+      const int i = r;
+      float d[32];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        tmem_ld32(tl + 64 * half, d);
+#pragma unroll
+        for (int jj = 0; jj < 32; jj += 2) {
+          pk[half][jj / 2] = pack_bf16(d[jj] * W[w_at(i, 64 * half + 32 * h + jj)],
+                                       d[jj + 1] * W[w_at(i, 64 * half + 32 * h + jj + 1)]);
+        }
+      }
+    }
+    tc_fence_before();
+    if (__syncthreads_or(sc.fail)) goto teardown;  // W read; D1 read
+    if ((warp & 3) < 2) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        unsigned char* row = tile(half ? kP1 : kP0) + r * 128;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<uint4*>(row + (((4 * h + q) ^ (r & 7)) << 4)) =
+              make_uint4(pk[half][4 * q], pk[half][4 * q + 1], pk[half][4 * q + 2],
+                         pk[half][4 * q + 3]);
+      }
+    }
+  }
+  // Vs = Diag(w_C) V~ (rows r of the two V tiles), over the rest of W
   {
     float v[32];
     load_half_sw(tile(kV0), r, h, v);
     store_half_sw(tile(kVs0), r, h, v, sc.wC[r]);
   }
-  if (!mbar_wait(&sc.bar_mma, phase)) sc.fail = 1;
-  phase ^= 1u;
-  tc_fence_after();
-  // No barrier: each thread has seen the MMA complete before it reads its
-  // accumulator rows and writes the P tiles; a failed wait is agreed on at
-  // the next barrier.
-  // P = (Q X~^T) o W, rows 0..63 (lanes 0..63), two column halves per tile
-  if ((warp & 3) < 2) {
-    const int i = r;
-    float d[32];
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      tmem_ld32(tl + 64 * half, d);
-#pragma unroll
-      for (int jj = 0; jj < 32; ++jj) d[jj] *= W[i * kLdW + 64 * half + 32 * h + jj];
-      store_half_sw(tile(half ? kP1 : kP0), i, h, d, 1.f);
-    }
-  }
   tc_fence_before();
   fence_async_smem();
   if (__syncthreads_or(sc.fail)) goto teardown;
-  // ---- D2 = P V~ (K = 128), D3 = X~^T Vs (K = 128, X~ read MN-major)
+  // ---- D2 = P V~ (K = 128), D3 = X~^T Vs (K = 128, X~ read MN-major), in the
+  //      columns D1 held
   if (tid == 0) {
     tc_fence_after();
     const uint32_t id_pv = idesc_bf16(128, 64, false, true);
-    mma_k64(tmem + 128, taddr(kP0), false, 16, taddr(kV0), true, k3Tile, id_pv, false);
-    mma_k64(tmem + 128, taddr(kP1), false, 16, taddr(kV1), true, k3Tile, id_pv, true);
+    mma_k64(tmem, taddr(kP0), false, 16, taddr(kV0), true, k3Tile, id_pv, false);
+    mma_k64(tmem, taddr(kP1), false, 16, taddr(kV1), true, k3Tile, id_pv, true);
     const uint32_t id_xv = idesc_bf16(128, 64, true, true);
-    mma_k64(tmem + 192, taddr(kX0), true, k3Tile, taddr(kVs0), true, k3Tile, id_xv, false);
-    mma_k64(tmem + 192, taddr(kX1), true, k3Tile, taddr(kVs1), true, k3Tile, id_xv, true);
+    mma_k64(tmem + 64, taddr(kX0), true, k3Tile, taddr(kVs0), true, k3Tile, id_xv, false);
+    mma_k64(tmem + 64, taddr(kX1), true, k3Tile, taddr(kVs1), true, k3Tile, id_xv, true);
     mma_commit(&sc.bar_mma);
   }
   if (!mbar_wait(&sc.bar_mma, phase)) sc.fail = 1;
@@ -279,9 +307,9 @@ __global__ void __launch_bounds__(k3Threads, 2)
       store_half_sw(mc_stage, r, h, v, __expf(sc.g[r - 64]));
     }
     if ((warp & 3) < 2) {
-      tmem_ld32(tl + 192, v);
+      tmem_ld32(tl + 64, v);
       store_half_sw(nc_stage, r, h, v, 1.f);
-      tmem_ld32(tl + 128, v);
+      tmem_ld32(tl, v);
       store_half_sw(nc_stage, 64 + r, h, v, 1.f);
     }
     fence_async_smem();
@@ -310,7 +338,7 @@ teardown:
   if (sc.fail && tid == 0) atomicExch(err, 1);
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, 256);
+  if (warp == 1) tmem_dealloc(tmem, 128);
 }
 
 }  // namespace
