@@ -40,6 +40,7 @@ EXPORTS = (
     "falcon3a_fwd_recurrent", "falcon_bwd_workspace_bytes", "falcon1_bwd_chunked",
     "falcon1a_bwd_chunked", "falcon3a_fwd_chunked", "falcon2a_fwd_chunked",
     "falcon_normalized_workspace_bytes", "falcon1a_fwd_chunked_normalized",
+    "falcon2_fwd_chunked",
 )
 FALCON_ERR_SCRATCH_LIMIT = -10
 FALCON_FIXED_SCRATCH_BYTES = 16 * 1024 * 1024
@@ -101,7 +102,7 @@ def load_library(path: str | None = None):
             fn.restype = ctypes.c_int
             fn.argtypes = [i64, i32, i32, i32, i32, i32, ctypes.c_float, ctypes.c_float,
                            vp, vp, vp, f32p, f32p, f32p, f32p, vp, vp, vp]
-        for name in ("falcon2_fwd_recurrent", "falcon2a_fwd_recurrent"):
+        for name in ("falcon2_fwd_recurrent", "falcon2a_fwd_recurrent", "falcon2_fwd_chunked"):
             fn = getattr(lib, name)
             fn.restype = ctypes.c_int
             fn.argtypes = [shp, vp, vp, vp, f32p, f32p, f32p, f32p, vp, f32p, f32p, vp]
@@ -430,6 +431,15 @@ def falcon2a_fwd_chunked(q, k, v, beta, lam, S0=None, x_prev=None, phi="l2", eps
     plus an optional workspace of falcon_workspace_bytes(shape) bytes."""
     return _fwd2("falcon2a_fwd_chunked", q, k, v, beta, lam, S0, x_prev, phi, eps, eps_gamma,
                  chunked=True, **kw)
+
+
+def falcon2_fwd_chunked(q, k, v, beta, lam, S0=None, x_prev=None, phi="l2", eps=1e-6,
+                        eps_gamma=1e-6, **kw):
+    """Falcon-2 forward in chunk form (tensor cores for bf16 with m = dv = 64,
+    one CTA per head; the token-recurrent kernel otherwise); arguments and
+    results as falcon2_fwd_recurrent, no workspace."""
+    return _fwd2("falcon2_fwd_chunked", q, k, v, beta, lam, S0, x_prev, phi, eps, eps_gamma,
+                 **kw)
 
 
 def falcon2_fwd_recurrent(q, k, v, beta, lam, S0=None, x_prev=None, phi="l2", eps=1e-6,

@@ -99,9 +99,12 @@ int fwd_chunked(int rule, const falcon_shape* s, const void* q, const void* k, c
   // chunk maps to the workspace); otherwise the token-recurrent kernel.
   const bool window_tc = windowed && chunked_form &&
                          falcon::tc_falcon3a_applies(s->dtype, s->m, s->dv, s->chunk, BH, s->T);
-  // Falcon-2A likewise (the regression rule Falcon-2 stays token-recurrent).
+  // Falcon-2A likewise (chunk maps in the workspace).  Falcon-2 in chunk form
+  // runs one CTA per head and needs no workspace.
   const bool column_tc = rule == falcon::kFalcon2A && chunked_form &&
                          falcon::tc_falcon2a_applies(s->dtype, s->m, s->dv, s->chunk, BH, s->T);
+  const bool column2_tc = rule == falcon::kFalcon2 && chunked_form &&
+                          falcon::tc_falcon2_applies(s->dtype, s->m, s->dv, s->chunk, BH, s->T);
   const size_t need = ((per_column && !column_tc) || (windowed && !window_tc))
                           ? 0
                           : falcon_workspace_bytes(s);
@@ -159,6 +162,7 @@ int fwd_chunked(int rule, const falcon_shape* s, const void* q, const void* k, c
     if (!err) return FALCON_ERR_CUDA;
     if (window_tc) return to_status(falcon::launch_tc_falcon3a(a, window, err, stream));
     if (column_tc) return to_status(falcon::launch_tc_falcon2a(a, err, stream));
+    if (column2_tc) return to_status(falcon::launch_tc_falcon2(a, err, stream));
     return to_status(windowed ? falcon::launch_falcon3a_recurrent(a, window, err, stream)
                               : falcon::launch_falcon2_recurrent(a, err, stream));
   }
@@ -469,6 +473,14 @@ int falcon2a_fwd_chunked(const falcon_shape* s, const void* q, const void* k, co
                          void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   return fwd_chunked(falcon::kFalcon2A, s, q, k, v, beta, lambda, S0, x_prev, o, S_out, x_last,
                      workspace, workspace_bytes, stream, 1, true);
+}
+
+int falcon2_fwd_chunked(const falcon_shape* s, const void* q, const void* k, const void* v,
+                        const float* beta, const float* lambda, const float* S0,
+                        const float* x_prev, void* o, float* S_out, float* x_last,
+                        cudaStream_t stream) {
+  return fwd_chunked(falcon::kFalcon2, s, q, k, v, beta, lambda, S0, x_prev, o, S_out, x_last,
+                     nullptr, 0, stream, 1, true);
 }
 
 int falcon3a_fwd_chunked(const falcon_shape* s, int32_t window, const void* q, const void* k,

@@ -329,6 +329,26 @@ int falcon3a_fwd_recurrent(const falcon_shape *shape, int32_t window,
  * shape it runs falcon2a_fwd_recurrent and ignores the workspace.
  * Arguments, layouts and errors are those of falcon2a_fwd_recurrent, plus
  * workspace / workspace_bytes as in falcon1_fwd_chunked. */
+/* Falcon-2 forward in chunk form: the same result as falcon2_fwd_recurrent
+ * (up to rounding).  Every value column j runs its own scalar-step delta
+ * rule on the shared write features (Section 3.1, regression display; Section
+ * 4.2, per-column step sizes), so inside a chunk of 64 tokens the written
+ * residuals u_{t,j} = eta_{j,t} r_{t,j} of column j solve a unit-lower system
+ * built from the shared Gram <x_t, x_l> and the column's own decays: one
+ * batched per-column triangular solve per chunk, in four blocks of 16 rows
+ * (the blocks before a block enter through shared-Gram products).  Decays
+ * enter only as products of the gammas, never as exponentials, so clamped
+ * and strong decays stay finite.  The chunks of a head are sequential (the
+ * per-column systems depend on the entering state): one CTA per head.  For
+ * bf16 q, k, v with m = dv = 64 and shape->chunk = 64 this runs on the tensor
+ * cores; for every other shape it runs falcon2_fwd_recurrent.  Arguments,
+ * layouts, ownership and errors are those of falcon2_fwd_recurrent; no
+ * workspace is needed. */
+int falcon2_fwd_chunked(const falcon_shape *shape, const void *q,
+                        const void *k, const void *v, const float *beta,
+                        const float *lambda, const float *S0,
+                        const float *x_prev, void *o, float *S_out,
+                        float *x_last, cudaStream_t stream);
 int falcon2a_fwd_chunked(const falcon_shape *shape, const void *q,
                          const void *k, const void *v, const float *beta,
                          const float *lambda, const float *S0,

@@ -71,7 +71,7 @@ def _call(lib, name, s, q=P, S0=None, x_prev=None, S_out=P, ws=P, wsb=BIG, windo
     if name == "falcon1a_fwd_chunked_normalized":
         return f(sp, q, P, P, P, P, S0, z0, x_prev, ctypes.c_float(eps_attn), P, S_out, z_out,
                  None, ws, wsb, None)
-    if name in ("falcon2_fwd_recurrent", "falcon2a_fwd_recurrent"):
+    if name in ("falcon2_fwd_recurrent", "falcon2a_fwd_recurrent", "falcon2_fwd_chunked"):
         return f(sp, q, P, P, P, P, S0, x_prev, P, S_out, None, None)
     if name == "falcon2a_fwd_chunked":
         return f(sp, q, P, P, P, P, S0, x_prev, P, S_out, None, ws, wsb, None)
@@ -85,6 +85,7 @@ def _call(lib, name, s, q=P, S0=None, x_prev=None, S_out=P, ws=P, wsb=BIG, windo
 
 
 VARIANTS = ["falcon2_fwd_recurrent", "falcon2a_fwd_recurrent", "falcon2a_fwd_chunked",
+            "falcon2_fwd_chunked",
             "falcon3a_fwd_recurrent", "falcon3a_fwd_chunked", "falcon1_fwd_chunked_fixed_scratch",
             "falcon1a_fwd_chunked_normalized"]
 
@@ -114,7 +115,8 @@ def test_variants_with_no_heads_touch_nothing(lib, name):
 
 
 @pytest.mark.parametrize("name", ["falcon2_fwd_recurrent", "falcon2a_fwd_recurrent",
-                                  "falcon2a_fwd_chunked", "falcon1_fwd_chunked_fixed_scratch",
+                                  "falcon2a_fwd_chunked", "falcon2_fwd_chunked",
+                                  "falcon1_fwd_chunked_fixed_scratch",
                                   "falcon1a_fwd_chunked_normalized"])
 def test_misaligned_x_prev_is_rejected(lib, name):
     assert _call(lib, name, _shape(), x_prev=ODD) == MISALIGNED
@@ -136,6 +138,15 @@ def test_tensor_core_chunk_forms_need_an_aligned_workspace(lib, name):
     assert _call(lib, name, s, wsb=ctypes.c_size_t(need - 1)) == WORKSPACE
     # 16-byte aligned is not enough: the workspace must sit on 256 bytes
     assert _call(lib, name, s, ws=ctypes.c_void_p(0x10010)) == MISALIGNED
+
+
+def test_falcon2_chunk_form_needs_no_workspace(lib):
+    """The tensor-core Falcon-2 chunk form runs one CTA per head from its
+    inputs alone: with no workspace the arguments pass and the call stops only
+    at the device check (no GPU here)."""
+    import delta_rule_attention_gb300 as falcon
+    rc = _call(lib, "falcon2_fwd_chunked", _tc_shape(), ws=None, wsb=ctypes.c_size_t(0))
+    assert rc in (-9, -6), rc  # FALCON_ERR_DEVICE, FALCON_ERR_CUDA
 
 
 def test_codes_are_the_headers():
