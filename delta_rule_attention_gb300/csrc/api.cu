@@ -13,6 +13,10 @@ namespace falcon {
 // Device error word: set by a kernel whose bounded wait gave up, read and
 // cleared by falcon_sync_check().
 static __device__ int g_device_error = 0;
+// Falcon-2 in chunk form on the tensor cores (bf16, m = dv = 64, chunk 64;
+// falcon2_tc.cu): one CTA per head, no workspace.
+bool tc_falcon2_applies(int dtype, int m, int dv, int C, int64_t BH, int64_t T);
+cudaError_t launch_tc_falcon2(const ChunkArgs& a, int* err, cudaStream_t stream);
 }  // namespace falcon
 
 namespace {

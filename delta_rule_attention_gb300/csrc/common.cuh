@@ -116,10 +116,6 @@ cudaError_t launch_tc_map64(const ChunkArgs& a, int* err, cudaStream_t stream);
 bool tc_falcon2a_applies(int dtype, int m, int dv, int C, int64_t BH, int64_t T);
 size_t tc_falcon2a_workspace_bytes(int64_t BH, int64_t T);
 cudaError_t launch_tc_falcon2a(const ChunkArgs& a, int* err, cudaStream_t stream);
-// Falcon-2 in chunk form on the tensor cores (bf16, m = dv = 64, chunk 64):
-// one CTA per head, no workspace.
-bool tc_falcon2_applies(int dtype, int m, int dv, int C, int64_t BH, int64_t T);
-cudaError_t launch_tc_falcon2(const ChunkArgs& a, int* err, cudaStream_t stream);
 // Falcon-3A in chunk form on the tensor cores (bf16, m = dv = 64, chunk 64).
 bool tc_falcon3a_applies(int dtype, int m, int dv, int C, int64_t BH, int64_t T);
 cudaError_t launch_tc_falcon3a(const ChunkArgs& a, int window, int* err, cudaStream_t stream);
