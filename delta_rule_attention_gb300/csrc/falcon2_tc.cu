@@ -7,35 +7,46 @@
 //   r_{t,j} = v_{t,j} - s_j^T x_t,   s_j <- gamma_{j,t} s_j + eta_{j,t} x_t r_{t,j},
 // so inside a chunk the written residuals u_{t,j} = eta_{j,t} r_{t,j} of
 // column j solve a unit-lower system built from the shared Gram K = X X^T and
-// the column's own decays (the "batched per-channel triangular solve with a
-// shared Gram matrix").  With e^{G_{j,i}} the product of the column's gammas
-// over the chunk's tokens up to i, and the accumulator
-//   acc^{(i)}_t = e^{G_i} (X S)_t + sum_{l<=i} e^{G_i - G_l} K_{tl} u_l,
-// the residual of row t is v_t - acc^{(t-1)}_t and acc^{(i)} = gamma_i
-// acc^{(i-1)} + K_{.,i} u_i: only products of gammas, never an exponential,
-// so strong and clamped decays cannot overflow anything.  The chunk's 64 rows
-// go in four blocks of 16: inside a block the accumulators run token by token
-// (one thread per column, fp32 registers); the blocks before it enter through
-// the shared matrices, sum_{b'<b} (decay) K_{b,b'} U~^{[b']}, combined in
-// Horner order with the block decays (warp-level bf16 MMAs, fp32 sums).  The
-// output and the state leaving the chunk are
-//   o_{t,j}  = e^{G_t} (Q S)_{t,j} + sum_{l<=t} e^{G_t - G_l} <q_t, x_l> u_{l,j},
-//   S'_{:,j} = e^{G_C} S_{:,j} + sum_l x_l e^{G_C - G_l} u_{l,j}.
+// the column's own decays (a batched per-column triangular solve with a
+// shared Gram matrix).  With E_{t,j} the product of column j's gammas over the
+// chunk's tokens up to t (E_{-1} = 1) and w_{l,j} = u_{l,j} / E_{l,j},
+//   u_t = eta_t v_t - eta_t E_{t-1} ((X S)_t + sum_{l<t} K_{tl} w_l),
+//   o_t = E_t ((Q S)_t + sum_{l<=t} <q_t, x_l> w_l),
+//   S'  = E_C (S + X^T W)             (per column: E_C scales column j),
+// which is the token recurrence unrolled over the chunk (w divides out the
+// decays of the tokens up to l).  Every factor stays within fp32 range while
+// a chunk's decay product is at least e^{-60} in every column; a chunk with a
+// stronger decay (clamped gammas) runs the tokens one by one instead (exact,
+// no factoring).
 //
 // One CTA per head runs the chunks in order (the per-column systems depend on
 // the entering state), with three warp groups:
-//   warps 0, 1  (solve; thread j owns column j): the state column s_j in fp32
-//               registers; per chunk the tcgen05 MMA [S^T; S^T] [X; Q]^T gives
-//               (X S)^T and (Q S)^T with one column per TMEM lane, the blocked
-//               solve, then the MMA (e^{G_C - G} o U)^T X for the state
-//               increment.  These two MMAs and the solve are the sequential
-//               chain.
-//   warps 2, 3  (output; column j): the output rows block by block, behind the
-//               solve, and one TMA store of the o tile per chunk.
-//   warps 4..7  (prep, one chunk ahead): the k, q, v tiles by TMA (three-slot
-//               ring), the Gram MMA [K; Q] K^T on the raw bf16 rows with phi's
-//               scales applied afterwards in fp32, the features phi(k), phi(q)
-//               in place, and per (token, column) eta, gamma and eta * v.
+//   warps 0, 1  (solve; thread j owns column j): per chunk the tcgen05 MMA
+//               S^T X^T gives (X S)^T with one column per TMEM lane; the solve
+//               runs in four blocks of 16 rows: inside a block a thread runs
+//               its column token by token (three dependent operations per
+//               token); the blocks before it enter as one shared-Gram product
+//               K_{b,<b} W_{<b} (warp-level bf16 MMAs).  The w rows, as bf16,
+//               are the operand of the two MMAs that close the chunk: the state
+//               increment W^T X, accumulated onto S^T in TMEM, and P0 W
+//               (P0 = the causal part of Q X^T), accumulated onto Q S.  The
+//               state S^T stays in TMEM in fp32.
+//   warps 2, 3  (output): one chunk ahead, thread j runs column j's tokens in
+//               order to form eta, gamma, the prefix products E and the
+//               solve's per-token factors; then, for the current chunk,
+//               thread t owns token row t: o_t = E_t (Q S + P0 W)_t from TMEM,
+//               and one TMA store of the o tile.
+//   warps 4..7  (prep, one chunk ahead): the k and q tiles (two-slot ring
+//               refilled by the solve's issuing thread), phi's row scales, the
+//               step-size denominators, the Gram MMA [K; Q] K^T on the raw bf16
+//               rows with the scales applied afterwards in fp32.
+// Every MMA reads the raw bf16 rows of k and q (exact inputs); phi's scales
+// n_t enter in fp32, each once: the w rows carry the write features' scales
+// (W' = n o w), the K tile its row scale only (K'_{tl} = n_t <k_t, k_l>, so
+// that K' W' = K w), the rows of X S are scaled as they are read, and the
+// output's Q S + P0 W' (raw q rows, P0 raw) is scaled by the q row's scale.
+// The solve's per-chunk operands are double-buffered, so the prep of chunk
+// c + 1 runs beside the chain of chunk c.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -52,50 +63,54 @@ using namespace tcu;
 
 constexpr int kF2C = 64;         // chunk
 constexpr int kF2Threads = 256;  // warps 0-1 solve, 2-3 output, 4-7 prep
-constexpr int kF2Ring = 3;       // input-tile slots
+constexpr int kF2Ring = 2;       // input-tile slots
+// A chunk whose decay product in some column is below this runs token by
+// token (e^{-60}: the factors 1/E and the w rows stay far inside fp32 range).
+constexpr float kMinChunkDecay = 8.75651e-27f;
 
 // Shared memory (bytes from a 1024-aligned base).
-constexpr uint32_t kSlot = 3 * 8192;            // X | Q | V tiles of one chunk
-constexpr uint32_t kRingOff = 0;                // kF2Ring slots
-constexpr uint32_t kSopOff = kF2Ring * kSlot;   // [S^T; S^T] bf16, K-major (16 KB)
-constexpr uint32_t kDecuOff = kSopOff + 16384;  // (e^{G_C-G} o U)^T bf16, K-major (8 KB);
-                                                // the MMA's rows 64..127 read the KB
-                                                // tile after it (lanes nobody reads)
-constexpr uint32_t kKbOff = kDecuOff + 8192;    // K as bf16, 128B-swizzled rows
-constexpr uint32_t kPbOff = kKbOff + 8192;      // P0 = Q X^T as bf16
-constexpr uint32_t kOstOff = kPbOff + 8192;     // o tile for the TMA store
-constexpr uint32_t kEtaOff = kOstOff + 8192;    // eta [j][t] fp32 (swizzled chunks)
-constexpr uint32_t kGamOff = kEtaOff + 16384;   // gamma [j][t]
-constexpr uint32_t kEtavOff = kGamOff + 16384;  // eta * v [j][t]
-constexpr uint32_t kUOff = kEtavOff + 16384;    // u [j][t]
-constexpr uint32_t kUtOff = kUOff + 16384;      // U~ blocks, bf16 [2][4][64 j][16 l]
-constexpr uint32_t kKdOff = kUtOff + 16384;     // K diagonal blocks fp32 [4][k][t]
-constexpr uint32_t kPdOff = kKdOff + 4096;      // P0 diagonal blocks fp32 [4][i][t]
-constexpr int kTrsLd = 20;                      // fp32 row of the transpose scratch
-constexpr uint32_t kTrsOff = kPdOff + 4096;     // [solve, output][2 warps][32][kTrsLd]
-constexpr uint32_t kDblkOff = kTrsOff + 2 * 2 * 32 * kTrsLd * 4;  // [2][4][64] fp32
-constexpr uint32_t kSc2Off = kDblkOff + 2 * 4 * 64 * 4;
+constexpr uint32_t kSlot = 2 * 8192;           // X | Q tiles (raw bf16 rows) of one chunk
+constexpr uint32_t kRingOff = 0;               // kF2Ring slots
+constexpr uint32_t kSopOff = kF2Ring * kSlot;  // S^T bf16, K-major rows j
+constexpr uint32_t kWOff = kSopOff + 8192;     // W^T bf16, K-major rows j (tokens along K)
+constexpr uint32_t kKbOff = kWOff + 8192;      // [2] K (strictly lower) bf16 rows t
+constexpr uint32_t kPbOff = kKbOff + 2 * 8192; // P0 (causal Q X^T) bf16 rows t
+constexpr uint32_t kOstOff = kPbOff + 8192;    // o tile for the TMA store
+constexpr uint32_t kAOff = kOstOff + 8192;     // [2] eta_t E_{t-1} [j][t] fp32
+constexpr uint32_t kFOff = kAOff + 2 * 16384;  // [2] 1 / E_t [j][t]
+constexpr uint32_t kEvOff = kFOff + 2 * 16384; // [2] eta_t v_t [j][t]
+constexpr uint32_t kE1Off = kEvOff + 2 * 16384;  // [2] E_t [t][j] (the output's scale)
+constexpr uint32_t kKdOff = kE1Off + 2 * 16384;  // [2] K diagonal blocks fp32 [4][k][t]
+constexpr int kTrsLd = 20;                     // fp32 row of the transpose scratch
+constexpr uint32_t kTrsOff = kKdOff + 2 * 4096;  // [2 solve warps][32][kTrsLd]
+constexpr uint32_t kSc2Off = kTrsOff + 2 * 32 * kTrsLd * 4;
+// The MMAs with M = 128 read 64 rows past their operand: the state increment's
+// A (W) reads the first K tile, the output's A (P0 as rows 64..127) starts at
+// the second K tile; the lanes they fill are never read.
+static_assert(kWOff + 8192 == kKbOff && kKbOff + 2 * 8192 == kPbOff, "operand layout");
 
 struct F2cScalars {
-  float nrm[128];  // phi's scale of row p of [X; Q]
-  float E[64], lamr[64], inv[64];
-  uint64_t full[kF2Ring], empty[kF2Ring], xq[kF2Ring];
-  uint64_t gdone, ydone[2], sdone, ybuf_free[2];
-  uint64_t pre_ready, solve_blk[4], out_blk[4], decu_done;
+  float nrm[2][128];  // phi's scale of row p of [X; Q], per chunk parity
+  float lamr[2][64], inv[2][64];  // per token: lambda_t, 1 / (E + lambda + eps)
+  float dC[2][64];    // E_C per column (the chunk's decay), per parity
+  int flag[4];        // chunk c & 3 runs token by token
+  uint64_t full[kF2Ring], xq[kF2Ring];
+  uint64_t gdone, ydone, sdone, odone[2], obuf_free[2];
+  uint64_t tok_ready[2], pre_ready[2], col_ready[2], solve_done[2], pb_ready;
   uint32_t tmem_base;
   int fail;
 };
 constexpr size_t kF2cSmem = kSc2Off + sizeof(F2cScalars) + 1024;
 static_assert(kF2cSmem <= 232448, "Falcon-2 chunk kernel shared memory");
-static_assert(kDecuOff + 8192 == kKbOff, "MMA_S reads rows 64..127 from the KB tile");
 
-// TMEM columns: the (X S | Q S)^T accumulator, double-buffered (128 columns
-// each), the state increment (64) and the Gram (64).
-constexpr uint32_t kTmY = 0, kTmS = 256, kTmG = 320, kTmCols = 512;
+// TMEM columns: (X S)^T (lanes j), [X; Q] S + P0 W double-buffered (lanes t;
+// rows 64..127 are the output), S^T (lanes j, fp32), the Gram (lanes t).
+constexpr uint32_t kTmY = 0, kTmO = 64, kTmState = 192, kTmG = 256, kTmCols = 512;
 
 // Element (j, t) of a [64][64] fp32 array whose 16-byte chunks are swizzled
 // by j, so that a warp reading four consecutive tokens of 32 columns, or
-// writing one column's 32 tokens, meets no bank conflict.
+// writing one column's 32 tokens, meets no bank conflict.  (The [t][j] array
+// E uses the same map with the roles of t and j exchanged.)
 __device__ __forceinline__ int jt(int j, int t) {
   return j * 64 + ((((t >> 2) ^ (j & 15))) << 2) + (t & 3);
 }
@@ -112,19 +127,50 @@ __device__ __forceinline__ void ldsm_x2(uint32_t (&r)[2], uint32_t saddr) {
                : "memory");
 }
 
-// Byte offset of U~ block b (buffer yb), column j, 16-byte chunk c.
-__device__ __forceinline__ uint32_t ut_off(int yb, int b, int j, int c) {
-  return (uint32_t)(yb * 8192 + b * 2048) + dblk_chunk(j, c);
+// Registers -> TMEM: 16 consecutive 32-bit columns of this thread's lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// The contribution of the blocks before block b to the 16 rows of block b,
-//   R = sum_{b'<b} (prod of the block decays after b') M_{b,b'} U~^{[b']},
-// for this warp's 32 columns (Horner order over b'), with M the bf16 tile
-// `mt` (K or P0, 128B-swizzled rows); returned per column: thread `lane`
-// receives rows 0..15 of column 32 w + lane in r.  trs: the warp's transpose
+// Bounded wait for a role that is not on the chain: backs off between polls
+// so that it takes few issue slots from the warps that are.
+__device__ __forceinline__ bool mbar_wait_idle(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    __nanosleep(64);
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// Row j of a K-major 128B-swizzled bf16 tile: the 16 values of chunk pair
+// (2 q, 2 q + 1), i.e. columns 16 q .. 16 q + 15.
+__device__ __forceinline__ void put_row16(unsigned char* tile, int j, int q, const float* v,
+                                          float scale) {
+  *reinterpret_cast<uint4*>(tile + sw_chunk(j, 2 * q)) = pack8(v, scale);
+  *reinterpret_cast<uint4*>(tile + sw_chunk(j, 2 * q + 1)) = pack8(v + 8, scale);
+}
+
+// The contribution of the blocks before block b to its 16 rows, K_{b,<b}
+// W_{<b} (one contraction over the 16 b tokens before the block), for this
+// warp's 32 columns (warp-level bf16 MMAs, fp32 sums); returned per column:
+// thread `lane` receives rows 0..15 of column 32 w + lane.  kb: the K tile
+// (bf16 rows t), wt: the W^T tile (bf16 rows j), trs: the warp's transpose
 // scratch (32 x kTrsLd floats).
-__device__ __forceinline__ void horner16(const unsigned char* base, uint32_t mt_off, int yb,
-                                         int b, int w, const float* dblk, float* trs,
+__device__ __forceinline__ void horner16(uint32_t kb, uint32_t wt, int b, int w, float* trs,
                                          float (&r)[16]) {
   const int lane = threadIdx.x & 31, g = lane >> 2, tq = lane & 3;
   const int la = (lane & 7) + 8 * ((lane >> 3) & 1), ca = lane >> 4;
@@ -133,21 +179,13 @@ __device__ __forceinline__ void horner16(const unsigned char* base, uint32_t mt_
   for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
     for (int e = 0; e < 4; ++e) R[nt][e] = 0.f;
-  const uint32_t mbase = smem_addr(base + mt_off);
-  const uint32_t ubase = smem_addr(base + kUtOff);
   for (int bp = 0; bp < b; ++bp) {
     uint32_t fa[4];
-    ldsm_x4(fa, mbase + sw_chunk(16 * b + la, 2 * bp + ca));
+    ldsm_x4(fa, kb + sw_chunk(16 * b + la, 2 * bp + ca));
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
-      const int col = 32 * w + 8 * nt + 2 * tq;
-      const float d0 = dblk[bp * 64 + col], d1 = dblk[bp * 64 + col + 1];
-      R[nt][0] *= d0;
-      R[nt][1] *= d1;
-      R[nt][2] *= d0;
-      R[nt][3] *= d1;
       uint32_t fb[2];
-      ldsm_x2(fb, ubase + ut_off(yb, bp, 32 * w + 8 * nt + (lane & 7), (lane >> 3) & 1));
+      ldsm_x2(fb, wt + sw_chunk(32 * w + 8 * nt + (lane & 7), 2 * bp + ((lane >> 3) & 1)));
       mma16816(R[nt], fa, fb);
     }
   }
@@ -171,51 +209,68 @@ __device__ __forceinline__ void horner16(const unsigned char* base, uint32_t mt_
   __syncwarp();
 }
 
-// A 64-value fp32 row as bf16 into row r of a 128B-swizzled K-major tile.
-__device__ __forceinline__ void put_row64(unsigned char* tile, int r, const float* v) {
-  store_row_bf16(tile, r, v);
+// One 64-element bf16 row of a 128B-swizzled tile times `scale`, into
+// v[0..63] (fp32).
+__device__ __forceinline__ void row_scaled(const unsigned char* tile, int r, float scale,
+                                           float* v) {
+  load_row_bf16(tile, r, v);
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] *= scale;
 }
 
 __global__ void __launch_bounds__(kF2Threads, 1)
     tc_falcon2_chunk_kernel(ChunkArgs a, int nch, int* err,
                             const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_q,
-                            const __grid_constant__ CUtensorMap tm_v,
                             const __grid_constant__ CUtensorMap tm_o) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* const base = align1024(smem_raw);
   F2cScalars& sc = *reinterpret_cast<F2cScalars*>(base + kSc2Off);
   volatile int* fail = &sc.fail;
-  float* const ETA = reinterpret_cast<float*>(base + kEtaOff);
-  float* const GAM = reinterpret_cast<float*>(base + kGamOff);
-  float* const ETAV = reinterpret_cast<float*>(base + kEtavOff);
-  float* const UB = reinterpret_cast<float*>(base + kUOff);
-  float* const KD = reinterpret_cast<float*>(base + kKdOff);
-  float* const PD = reinterpret_cast<float*>(base + kPdOff);
-  float* const DBLK = reinterpret_cast<float*>(base + kDblkOff);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t bh = blockIdx.x;
   const int64_t T = a.T, rowbase = bh * T;
+  auto arr = [&](uint32_t off, int par) { return reinterpret_cast<float*>(base + off) + par * 4096; };
+  auto slot_addr = [&](int c) { return base + kRingOff + (c % kF2Ring) * kSlot; };
+  // The k rows t0-1 .. t0+62 and q rows of chunk cc into its slot (rows
+  // outside the sequence read as zero), and the chunk's gains, values and
+  // ridges into L2 for the column pass.
+  auto load_chunk = [&](int cc) {
+    const int sl = cc % kF2Ring;
+    unsigned char* dst = base + kRingOff + sl * kSlot;
+    mbar_expect_tx(&sc.full[sl], 2 * 8192);
+    tma_load_3d(dst, &tm_k, 0, cc * kF2C - 1, (int)bh, &sc.full[sl]);
+    tma_load_3d(dst + 8192, &tm_q, 0, cc * kF2C, (int)bh, &sc.full[sl]);
+    const int64_t t0 = (int64_t)cc * kF2C;
+    const int nn = (int)min((int64_t)kF2C, T - t0);
+    bulk_prefetch_l2(a.beta + (rowbase + t0) * 64, (uint32_t)nn * 256u);
+    bulk_prefetch_l2(reinterpret_cast<const __nv_bfloat16*>(a.v) + (rowbase + t0) * 64,
+                     (uint32_t)nn * 128u);
+    const float* lp = a.lambda + rowbase + t0;  // (not 16-byte aligned in general)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(lp));
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(lp + nn - 1));
+    if (nn > 32) asm volatile("prefetch.global.L2 [%0];" ::"l"(lp + 32));
+  };
 
   if (warp == 0) tmem_alloc(&sc.tmem_base, kTmCols);
   if (tid == 32) {
     for (int i = 0; i < kF2Ring; ++i) {
       mbar_init(&sc.full[i], 1);
-      mbar_init(&sc.empty[i], 1);
       mbar_init(&sc.xq[i], 1);
     }
     mbar_init(&sc.gdone, 1);
-    mbar_init(&sc.ydone[0], 1);
-    mbar_init(&sc.ydone[1], 1);
+    mbar_init(&sc.ydone, 1);
     mbar_init(&sc.sdone, 1);
-    mbar_init(&sc.ybuf_free[0], 2);
-    mbar_init(&sc.ybuf_free[1], 2);
-    mbar_init(&sc.pre_ready, 4);
-    for (int b = 0; b < 4; ++b) {
-      mbar_init(&sc.solve_blk[b], 2);
-      mbar_init(&sc.out_blk[b], 2);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sc.odone[i], 1);
+      mbar_init(&sc.obuf_free[i], 2);
+      mbar_init(&sc.tok_ready[i], 4);
+      mbar_init(&sc.pre_ready[i], 4);
+      mbar_init(&sc.col_ready[i], 2);
+      mbar_init(&sc.solve_done[i], 2);
     }
-    mbar_init(&sc.decu_done, 2);
+    mbar_init(&sc.pb_ready, 2);
+    for (int i = 0; i < 4; ++i) sc.flag[i] = 0;
     fence_mbar_init();
     sc.fail = 0;
   }
@@ -233,253 +288,359 @@ __global__ void __launch_bounds__(kF2Threads, 1)
     // ======================= solve: thread j owns column j =======================
     const int j = tid, w = warp;
     float* trs = reinterpret_cast<float*>(base + kTrsOff) + w * 32 * kTrsLd;
-    float s[64];
-#pragma unroll
-    for (int i = 0; i < 64; ++i) s[i] = a.S0 ? a.S0[(bh * 64 + i) * 64 + j] : 0.f;
-    for (int c = 0; c < nch; ++c) {
-      const int slot = c % kF2Ring, yb = c & 1;
-      bool ok = true;
-      // state operand: rows j and 64 + j of [S^T; S^T]
-      put_row64(base + kSopOff, j, s);
-      put_row64(base + kSopOff, 64 + j, s);
-      fence_async_smem();
-      tc_fence_before();
-      if (named_sync_or(1, 64, *fail)) break;
-      if (tid == 0) {
-        bool k2 = mbar_wait(&sc.xq[slot], (uint32_t)(c / kF2Ring) & 1u);
-        if (c >= 2) k2 = k2 && mbar_wait(&sc.ybuf_free[yb], (uint32_t)((c - 2) >> 1) & 1u);
-        if (!k2) {
-          *fail = 1;
-        } else {
-          tc_fence_after();
-          // (X S | Q S)^T: A = [S^T; S^T] (K-major), B = [X; Q] (K-major, N = 128)
-          mma_k64(tmem + kTmY + 128 * yb, smem_addr(base + kSopOff), false, 16,
-                  smem_addr(base + kRingOff + slot * kSlot), false, 16,
-                  idesc_bf16(128, 128, false, false), false);
-          mma_commit(&sc.ydone[yb]);
-        }
+    const uint32_t wt = smem_addr(base + kWOff);
+    // The MMAs that open chunk c: (X S)^T (A = S^T, rows 64..127 past it land
+    // in lanes nobody reads) and [X; Q] S into the output accumulator.
+    auto open_chunk = [&](int c) {
+      const int slot = c % kF2Ring;
+      bool k2 = mbar_wait(&sc.xq[slot], (uint32_t)(c / kF2Ring) & 1u);
+      if (c >= 2) k2 = k2 && mbar_wait(&sc.obuf_free[c & 1], (uint32_t)((c - 2) >> 1) & 1u);
+      if (!k2) {
+        *fail = 1;
+        return;
       }
-      ok = ok && mbar_wait(&sc.pre_ready, (uint32_t)c & 1u);
-      ok = ok && mbar_wait(&sc.ydone[yb], (uint32_t)(c >> 1) & 1u);
       tc_fence_after();
-      float pc = 1.f;  // product of gamma over the blocks before b
-      float u[16];
+      const uint32_t xq = smem_addr(slot_addr(c));
+      mma_k64(tmem + kTmY, smem_addr(base + kSopOff), false, 16, xq, false, 16,
+              idesc_bf16(128, 64, false, false), false);
+      mma_k64(tmem + kTmO + 64 * (c & 1), xq, false, 16, smem_addr(base + kSopOff), false, 16,
+              idesc_bf16(128, 64, false, false), false);
+      mma_commit(&sc.ydone);
+    };
+    // S0 into TMEM (fp32, lane j = column j) and the first state operand
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = a.S0 ? a.S0[(bh * 64 + 16 * q + i) * 64 + j] : 0.f;
+      tmem_st16(tlane + kTmState + 16 * q, v);
+      put_row16(base + kSopOff, j, q, v, 1.f);
+    }
+    tmem_st_wait();
+    fence_async_smem();
+    tc_fence_before();
+    bool go = !named_sync_or(1, 64, false);
+    if (go && tid == 0) open_chunk(0);
+    for (int c = 0; go && c < nch; ++c) {
+      const int slot = c % kF2Ring, par = c & 1;
+      const unsigned char* xt = slot_addr(c);
+      bool ok = mbar_wait(&sc.pre_ready[par], (uint32_t)(c >> 1) & 1u);
+      ok = ok && mbar_wait(&sc.col_ready[par], (uint32_t)(c >> 1) & 1u);
+      const bool tokenwise = sc.flag[c & 3] != 0;
+      const float dC = sc.dC[par][j];  // read before this parity is released
+      const float* A = arr(kAOff, par);
+      const float* F = arr(kFOff, par);
+      const float* EV = arr(kEvOff, par);
+      ok = ok && mbar_wait(&sc.ydone, (uint32_t)c & 1u);
+      tc_fence_after();
+      if (!tokenwise) {
+        const uint32_t kb = smem_addr(base + kKbOff + par * 8192);
+        const float* KD = reinterpret_cast<const float*>(base + kKdOff) + par * 1024;
 #pragma unroll 1
-      for (int b = 0; b < 4; ++b) {
-        float acc[16];
-        tmem_ld16(tlane + kTmY + 128 * yb + 16 * b, acc);
-        if (b > 0) {
-          float r[16];
-          horner16(base, kKbOff, yb, b, w, DBLK + yb * 256, trs, r);
+        for (int b = 0; b < 4; ++b) {
+          float acc[16];
+          tmem_ld16(tlane + kTmY + 16 * b, acc);
+          {
+            // phi's scales of the write features (the MMA read the raw k rows)
+            const float* nx = sc.nrm[par] + 16 * b;
 #pragma unroll
-          for (int t = 0; t < 16; ++t) acc[t] = fmaf(pc, acc[t], r[t]);
-        } else {
+            for (int t = 0; t < 16; ++t) acc[t] *= nx[t];
+          }
+          if (b > 0) {
+            float r[16];
+            horner16(kb, wt, b, w, trs, r);
 #pragma unroll
-          for (int t = 0; t < 16; ++t) acc[t] *= pc;
-        }
-        float eta[16], etav[16], gam[16];
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const float4 e = jt4(ETA, j, 16 * b + 4 * q4);
-          const float4 ev = jt4(ETAV, j, 16 * b + 4 * q4);
-          const float4 g = jt4(GAM, j, 16 * b + 4 * q4);
-          eta[4 * q4] = e.x, eta[4 * q4 + 1] = e.y, eta[4 * q4 + 2] = e.z, eta[4 * q4 + 3] = e.w;
-          etav[4 * q4] = ev.x, etav[4 * q4 + 1] = ev.y, etav[4 * q4 + 2] = ev.z,
-                    etav[4 * q4 + 3] = ev.w;
-          gam[4 * q4] = g.x, gam[4 * q4 + 1] = g.y, gam[4 * q4 + 2] = g.z, gam[4 * q4 + 3] = g.w;
-        }
-        const float* kd = KD + b * 256;
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          u[k] = fmaf(-eta[k], acc[k], etav[k]);
-          float kc[16];
+            for (int t = 0; t < 16; ++t) acc[t] += r[t];
+          }
+          float av[16], fv[16], ev[16];
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
-            const float4 x = *reinterpret_cast<const float4*>(kd + k * 16 + 4 * q4);
-            kc[4 * q4] = x.x, kc[4 * q4 + 1] = x.y, kc[4 * q4 + 2] = x.z, kc[4 * q4 + 3] = x.w;
+            const float4 x = jt4(A, j, 16 * b + 4 * q4);
+            const float4 y = jt4(F, j, 16 * b + 4 * q4);
+            const float4 z = jt4(EV, j, 16 * b + 4 * q4);
+            av[4 * q4] = x.x, av[4 * q4 + 1] = x.y, av[4 * q4 + 2] = x.z, av[4 * q4 + 3] = x.w;
+            fv[4 * q4] = y.x, fv[4 * q4 + 1] = y.y, fv[4 * q4 + 2] = y.z, fv[4 * q4 + 3] = y.w;
+            ev[4 * q4] = z.x, ev[4 * q4 + 1] = z.y, ev[4 * q4 + 2] = z.z, ev[4 * q4 + 3] = z.w;
           }
+          const float* kd = KD + b * 256;
+          float wv[16];
+          // four tokens at a time: their Gram columns are loaded together, so
+          // the shared-memory latency is paid once per four tokens
 #pragma unroll
-          for (int t = k + 1; t < 16; ++t) acc[t] = fmaf(kc[t], u[k], gam[k] * acc[t]);
+          for (int k4 = 0; k4 < 4; ++k4) {
+            float kc[4][16];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int k = 4 * k4 + e;
+#pragma unroll
+              for (int q4 = (k + 1) >> 2; q4 < 4; ++q4) {
+                const float4 x = *reinterpret_cast<const float4*>(kd + k * 16 + 4 * q4);
+                kc[e][4 * q4] = x.x, kc[e][4 * q4 + 1] = x.y, kc[e][4 * q4 + 2] = x.z,
+                    kc[e][4 * q4 + 3] = x.w;
+              }
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int k = 4 * k4 + e;
+              const float u = fmaf(-av[k], acc[k], ev[k]);
+              wv[k] = fv[k] * u;
+#pragma unroll
+              for (int t = k + 1; t < 16; ++t) acc[t] = fmaf(kc[e][t], wv[k], acc[t]);
+            }
+          }
+          // the w rows of this block (bf16, with phi's scales: W') for the later
+          // blocks and the MMAs
+          put_row16(base + kWOff, j, b, wv, 1.f);
+          __syncwarp();
         }
-        // U~ (u decayed to the block's end) and the block decay
-        float d = 1.f;
-        float ut[16];
-#pragma unroll
-        for (int k = 15; k >= 0; --k) {
-          ut[k] = d * u[k];
-          d *= gam[k];
-        }
-        // u of this block is read by the output warps of the previous chunk
-        // until they are past block b.
-        if (c > 0) ok = ok && mbar_wait(&sc.out_blk[b], (uint32_t)(c - 1) & 1u);
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          *reinterpret_cast<float4*>(UB + jt(j, 16 * b + 4 * q4)) =
-              make_float4(u[4 * q4], u[4 * q4 + 1], u[4 * q4 + 2], u[4 * q4 + 3]);
-        *reinterpret_cast<uint4*>(base + kUtOff + ut_off(yb, b, j, 0)) = pack8(ut, 1.f);
-        *reinterpret_cast<uint4*>(base + kUtOff + ut_off(yb, b, j, 1)) = pack8(ut + 8, 1.f);
-        DBLK[yb * 256 + b * 64 + j] = d;
-        pc *= d;
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sc.solve_blk[b]);
-      }
-      // (e^{G_C - G_l} u_l) for the state increment; e^{G_C} = pc
-      {
-        float dv[64];
-        float d = 1.f;
-#pragma unroll
-        for (int q4 = 15; q4 >= 0; --q4) {
-          const float4 uu = jt4(UB, j, 4 * q4);
-          const float4 g = jt4(GAM, j, 4 * q4);
-          dv[4 * q4 + 3] = d * uu.w;
-          d *= g.w;
-          dv[4 * q4 + 2] = d * uu.z;
-          d *= g.z;
-          dv[4 * q4 + 1] = d * uu.y;
-          d *= g.y;
-          dv[4 * q4] = d * uu.x;
-          d *= g.x;
+        if (lane == 0) mbar_arrive(&sc.solve_done[par]);
+        fence_async_smem();
+        tc_fence_before();
+        if (named_sync_or(1, 64, !ok || *fail)) {
+          *fail = 1;
+          break;
         }
-        put_row64(base + kDecuOff, j, dv);
+        if (tid == 0) {
+          if (!mbar_wait(&sc.pb_ready, (uint32_t)c & 1u)) {
+            *fail = 1;
+          } else {
+            tc_fence_after();
+            // S^T += W^T X (A = W^T K-major, B = X MN-major); Q S += P0 W
+            mma_k64(tmem + kTmState, wt, false, 16, smem_addr(xt), true, 8192,
+                    idesc_bf16(128, 64, false, true), true);
+            mma_k64(tmem + kTmO + 64 * par, smem_addr(base + kKbOff + 8192), false, 16, wt,
+                    false, 16, idesc_bf16(128, 64, false, false), true);
+            mma_commit(&sc.sdone);
+            mma_commit(&sc.odone[par]);
+          }
+        }
+        ok = mbar_wait(&sc.sdone, (uint32_t)c & 1u);
+        tc_fence_after();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float sv[16];
+          tmem_ld16(tlane + kTmState + 16 * q, sv);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) sv[i] *= dC;
+          tmem_st16(tlane + kTmState + 16 * q, sv);
+          put_row16(base + kSopOff, j, q, sv, 1.f);
+        }
+      } else {
+        // Token by token (a decay too strong to factor), from the inputs.
+        const int64_t t0 = (int64_t)c * kF2C;
+        const int n = (int)min((int64_t)kF2C, T - t0);
+        float s[64];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_ld16(tlane + kTmState + 16 * q, s + 16 * q);
+        __nv_bfloat16* og = reinterpret_cast<__nv_bfloat16*>(a.o) + (rowbase + t0) * 64 + j;
+        const __nv_bfloat16* vg =
+            reinterpret_cast<const __nv_bfloat16*>(a.v) + (rowbase + t0) * 64 + j;
+        const float* bg = a.beta + (rowbase + t0) * 64 + j;
+        const float eg = a.eps_gamma;
+        for (int t = 0; t < n; ++t) {
+          const float eta = bg[(int64_t)t * 64] * sc.inv[par][t];
+          const float al = eta * sc.lamr[par][t];
+          const float gam = al >= 1.f - eg ? eg : 1.f - al;
+          const float etav = eta * __bfloat162float(vg[(int64_t)t * 64]);
+          float x[64];
+          row_scaled(xt, t, sc.nrm[par][t], x);
+          float d8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int i = 0; i < 64; ++i) d8[i & 7] = fmaf(s[i], x[i], d8[i & 7]);
+          const float d = ((d8[0] + d8[1]) + (d8[2] + d8[3])) + ((d8[4] + d8[5]) + (d8[6] + d8[7]));
+          const float u = fmaf(-eta, d, etav);
+#pragma unroll
+          for (int i = 0; i < 64; ++i) s[i] = fmaf(u, x[i], gam * s[i]);
+          row_scaled(xt + 8192, t, sc.nrm[par][64 + t], x);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) d8[i] = 0.f;
+#pragma unroll
+          for (int i = 0; i < 64; ++i) d8[i & 7] = fmaf(s[i], x[i], d8[i & 7]);
+          og[(int64_t)t * 64] = __float2bfloat16_rn(
+              ((d8[0] + d8[1]) + (d8[2] + d8[3])) + ((d8[4] + d8[5]) + (d8[6] + d8[7])));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sc.solve_done[par]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          tmem_st16(tlane + kTmState + 16 * q, s + 16 * q);
+          put_row16(base + kSopOff, j, q, s + 16 * q, 1.f);
+        }
+        if (named_sync_or(1, 64, !ok || *fail)) {
+          *fail = 1;
+          break;
+        }
+        // no MMA closes this chunk: keep the barriers' phases in step
+        if (tid == 0) {
+          if (!mbar_wait(&sc.pb_ready, (uint32_t)c & 1u)) *fail = 1;
+          mbar_arrive(&sc.sdone);
+          mbar_arrive(&sc.odone[par]);
+        }
+        ok = ok && mbar_wait(&sc.sdone, (uint32_t)c & 1u);
       }
+      tmem_st_wait();
       fence_async_smem();
       tc_fence_before();
       if (named_sync_or(1, 64, !ok || *fail)) {
         *fail = 1;
         break;
       }
-      if (lane == 0) mbar_arrive(&sc.decu_done);
       if (tid == 0) {
-        tc_fence_after();
-        // increment^T = (e^{G_C - G} o U)^T X: A K-major (rows j), B = X MN-major
-        mma_k64(tmem + kTmS, smem_addr(base + kDecuOff), false, 16,
-                smem_addr(base + kRingOff + slot * kSlot), true, 8192,
-                idesc_bf16(128, 64, false, true), false);
-        mma_commit(&sc.sdone);
+        if (c + 1 < nch) open_chunk(c + 1);
+        // the slot of chunk c is free: chunk c + 2 into it
+        if (c + 2 < nch) load_chunk(c + 2);
       }
-      ok = mbar_wait(&sc.sdone, (uint32_t)c & 1u);
-      tc_fence_after();
-      if (tid == 0) mbar_arrive(&sc.empty[slot]);  // X, Q, V of chunk c are no longer read
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float inc[16];
-        tmem_ld16(tlane + kTmS + 16 * q, inc);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) s[16 * q + i] = fmaf(pc, s[16 * q + i], inc[i]);
-      }
-      if (!ok) *fail = 1;
     }
     if (!*fail) {
+      tc_fence_after();
 #pragma unroll
-      for (int i = 0; i < 64; ++i) a.S_out[(bh * 64 + i) * 64 + j] = s[i];
+      for (int q = 0; q < 4; ++q) {
+        float sv[16];
+        tmem_ld16(tlane + kTmState + 16 * q, sv);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) a.S_out[(bh * 64 + 16 * q + i) * 64 + j] = sv[i];
+      }
     }
   } else if (warp < 4) {
-    // ======================= output: thread owns column j =======================
-    const int j = tid - 64, w = warp - 2;
-    float* trs = reinterpret_cast<float*>(base + kTrsOff) + (2 + w) * 32 * kTrsLd;
+    // ======================= output =======================
+    const int me = tid - 64;  // column (the pass ahead) and token row (the output)
     unsigned char* ost = base + kOstOff;
-    for (int c = 0; c < nch; ++c) {
-      const int yb = c & 1;
-      bool ok = true;
-      if (tid == 64) bulk_wait_read<0>();  // the previous o store has read the tile
-      if (named_sync_or(2, 64, *fail)) break;
-      ok = ok && mbar_wait(&sc.pre_ready, (uint32_t)c & 1u);
-      ok = ok && mbar_wait(&sc.ydone[yb], (uint32_t)(c >> 1) & 1u);
-      tc_fence_after();
-      float pc = 1.f;
-#pragma unroll 1
-      for (int b = 0; b < 4; ++b) {
-        float ao[16];
-        tmem_ld16(tlane + kTmY + 128 * yb + 64 + 16 * b, ao);
-        ok = ok && mbar_wait(&sc.solve_blk[b], (uint32_t)c & 1u);
-        if (b > 0) {
-          float r[16];
-          horner16(base, kPbOff, yb, b, w, DBLK + yb * 256, trs, r);
+    float nq[2] = {0.f, 0.f};  // phi's scale of q row `me`, per chunk parity
+    // Column pass of chunk cc: eta, gamma and the prefix products E of column
+    // j = me token by token; the solve's factors A = eta E_{t-1}, F = n_t / E_t,
+    // eta v, the output's E, and the chunk's decay E_C (dC).
+    auto column_pass = [&](int cc) -> bool {
+      const int pp = cc & 1;
+      bool ok = mbar_wait_idle(&sc.tok_ready[pp], (uint32_t)(cc >> 1) & 1u);
+      // this parity's buffers were last read by the solve of chunk cc - 2
+      if (cc >= 2) ok = ok && mbar_wait_idle(&sc.solve_done[pp], (uint32_t)((cc - 2) >> 1) & 1u);
+      float* A = arr(kAOff, pp);
+      float* F = arr(kFOff, pp);
+      float* EV = arr(kEvOff, pp);
+      float* E1 = arr(kE1Off, pp);
+      const int j = me;
+      const float eg = a.eps_gamma;
+      nq[pp] = sc.nrm[pp][64 + me];
+      // the prep staged the column's gains in A and values in EV ([j][t]);
+      // they are overwritten in place with the solve's factors
+      float E = 1.f;  // E_{t-1}
 #pragma unroll
-          for (int t = 0; t < 16; ++t) ao[t] = fmaf(pc, ao[t], r[t]);
-        } else {
+      for (int t4 = 0; t4 < 64; t4 += 4) {
+        const float4 b4 = jt4(A, j, t4), vv4 = jt4(EV, j, t4);
+        const float be[4] = {b4.x, b4.y, b4.z, b4.w}, ve[4] = {vv4.x, vv4.y, vv4.z, vv4.w};
+        float a4[4], f4[4], v4[4], e4[4];
 #pragma unroll
-          for (int t = 0; t < 16; ++t) ao[t] *= pc;
+        for (int e = 0; e < 4; ++e) {
+          const int t = t4 + e;
+          const float eta = be[e] * sc.inv[pp][t];
+          const float al = eta * sc.lamr[pp][t];
+          const float gam = al >= 1.f - eg ? eg : 1.f - al;
+          const float En = E * gam;
+          a4[e] = eta * E;
+          f4[e] = __fdividef(sc.nrm[pp][t], En);  // (E_t >= e^{-60} on the factored path)
+          v4[e] = eta * ve[e];
+          e4[e] = En;
+          E = En;
         }
-        float uu[16], gam[16];
+        *reinterpret_cast<float4*>(A + jt(j, t4)) = make_float4(a4[0], a4[1], a4[2], a4[3]);
+        *reinterpret_cast<float4*>(F + jt(j, t4)) = make_float4(f4[0], f4[1], f4[2], f4[3]);
+        *reinterpret_cast<float4*>(EV + jt(j, t4)) = make_float4(v4[0], v4[1], v4[2], v4[3]);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const float4 x = jt4(UB, j, 16 * b + 4 * q4);
-          const float4 g = jt4(GAM, j, 16 * b + 4 * q4);
-          uu[4 * q4] = x.x, uu[4 * q4 + 1] = x.y, uu[4 * q4 + 2] = x.z, uu[4 * q4 + 3] = x.w;
-          gam[4 * q4] = g.x, gam[4 * q4 + 1] = g.y, gam[4 * q4 + 2] = g.z, gam[4 * q4 + 3] = g.w;
-        }
-        const float* pd = PD + b * 256;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float pcol[16];
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const float4 x = *reinterpret_cast<const float4*>(pd + i * 16 + 4 * q4);
-            pcol[4 * q4] = x.x, pcol[4 * q4 + 1] = x.y, pcol[4 * q4 + 2] = x.z,
-                      pcol[4 * q4 + 3] = x.w;
-          }
-#pragma unroll
-          for (int t = i; t < 16; ++t) ao[t] = fmaf(pcol[t], uu[i], gam[i] * ao[t]);
-        }
-        // o rows 16 b .. 16 b + 15 of column j into the swizzled o tile
-#pragma unroll
-        for (int t = 0; t < 16; ++t)
-          *reinterpret_cast<__nv_bfloat16*>(ost + sw128_off(16 * b + t, j)) =
-              __float2bfloat16_rn(ao[t]);
-        pc *= DBLK[yb * 256 + b * 64 + j];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sc.out_blk[b]);
+        for (int e = 0; e < 4; ++e) E1[jt(t4 + e, j)] = e4[e];
       }
-      tc_fence_before();
+      sc.dC[pp][j] = E;
+      // a column whose decay over the chunk is too strong to factor sends the
+      // whole chunk token by token
+      const bool weak = !(E >= kMinChunkDecay);
+      const bool any = named_sync_or(2, 64, weak);
+      if (me == 0) sc.flag[cc & 3] = any ? 1 : 0;
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sc.ybuf_free[yb]);
-      fence_async_smem();
+      if (lane == 0) mbar_arrive(&sc.col_ready[pp]);
+      return ok;
+    };
+    bool ok = nch > 0 ? column_pass(0) : true;
+    for (int c = 0; c < nch; ++c) {
+      const int par = c & 1, t = me;
+      if (c + 1 < nch) ok = column_pass(c + 1) && ok;
+      if (tid == 64) bulk_wait_read<0>();  // the previous o store has read the tile
       if (named_sync_or(2, 64, !ok || *fail)) {
         *fail = 1;
         break;
       }
-      if (tid == 64) {
-        tma_store_3d(&tm_o, ost, 0, c * kF2C, (int)bh);
-        bulk_commit();
+      ok = mbar_wait_idle(&sc.odone[par], (uint32_t)(c >> 1) & 1u);
+      const bool tokenwise = sc.flag[c & 3] != 0;
+      if (!tokenwise) {
+        tc_fence_after();
+        float d[64];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_ld16(tlane + kTmO + 64 * par + 16 * q, d + 16 * q);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sc.obuf_free[par]);
+        // o_t = E_t n_q (Q S + P0 W')_t (raw q rows and P0), E in [t][j]
+        const float* E1 = arr(kE1Off, par);
+#pragma unroll
+        for (int q4 = 0; q4 < 16; ++q4) {
+          const float4 e = *reinterpret_cast<const float4*>(E1 + jt(t, 4 * q4));
+          d[4 * q4] *= nq[par] * e.x, d[4 * q4 + 1] *= nq[par] * e.y,
+              d[4 * q4 + 2] *= nq[par] * e.z, d[4 * q4 + 3] *= nq[par] * e.w;
+        }
+        store_row_bf16(ost, t, d);
+        fence_async_smem();
+        if (named_sync_or(2, 64, !ok || *fail)) {
+          *fail = 1;
+          break;
+        }
+        if (tid == 64) {
+          tma_store_3d(&tm_o, ost, 0, c * kF2C, (int)bh);
+          bulk_commit();
+        }
+      } else {
+        // the solve warps wrote this chunk's o rows themselves
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sc.obuf_free[par]);
+        if (!ok) *fail = 1;
       }
     }
     if (tid == 64) bulk_wait<0>();
   } else {
     // ======================= prep: one chunk ahead =======================
-    const int p = tid - 128;  // row of [X; Q] (features), token / column half (scalars)
+    const int p = tid - 128;  // row of [X; Q] (features, Gram rows)
+    const int tt = p & 63;
     const bool issuer = p == 0;
-    auto load_chunk = [&](int cc) {
-      const int sl = cc % kF2Ring;
-      unsigned char* dst = base + kRingOff + sl * kSlot;
-      mbar_expect_tx(&sc.full[sl], 3 * 8192);
-      tma_load_3d(dst, &tm_k, 0, cc * kF2C - 1, (int)bh, &sc.full[sl]);
-      tma_load_3d(dst + 8192, &tm_q, 0, cc * kF2C, (int)bh, &sc.full[sl]);
-      tma_load_3d(dst + 16384, &tm_v, 0, cc * kF2C, (int)bh, &sc.full[sl]);
-    };
     if (issuer)
       for (int cc = 0; cc < kF2Ring && cc < nch; ++cc) load_chunk(cc);
-    const float eg = a.eps_gamma;
     for (int c = 0; c < nch; ++c) {
-      const int slot = c % kF2Ring;
+      const int slot = c % kF2Ring, par = c & 1;
       const int64_t t0 = (int64_t)c * kF2C;
       const int n = (int)min((int64_t)kF2C, T - t0);
       unsigned char* xt = base + kRingOff + slot * kSlot;  // X, then Q at +8 KB
-      unsigned char* vt = xt + 16384;
       bool ok = true;
-      // gains of this thread's (token, column half), loaded early
-      const int tt = p & 63, hh = p >> 6;
+      const float lam_t = (p < 64 && p < n) ? a.lambda[rowbase + t0 + p] : 0.f;
+      // gains and values of token tt, columns 32 hh .. 32 hh + 31 (16-byte loads),
+      // staged transposed for the column pass (zero past the sequence)
+      const int hh = p >> 6;
       float4 bet[8];
+      uint4 vraw[4];
 #pragma unroll
       for (int i = 0; i < 8; ++i) bet[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) vraw[i] = make_uint4(0u, 0u, 0u, 0u);
       if (tt < n) {
         const float4* src =
             reinterpret_cast<const float4*>(a.beta + (rowbase + t0 + tt) * 64 + 32 * hh);
 #pragma unroll
         for (int i = 0; i < 8; ++i) bet[i] = src[i];
+        const uint4* vs = reinterpret_cast<const uint4*>(
+            reinterpret_cast<const __nv_bfloat16*>(a.v) + (rowbase + t0 + tt) * 64 + 32 * hh);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) vraw[i] = vs[i];
       }
-      const float lam_t = (p < 64 && p < n) ? a.lambda[rowbase + t0 + p] : 0.f;
-      ok = ok && mbar_wait(&sc.full[slot], (uint32_t)(c / kF2Ring) & 1u);
+      ok = ok && mbar_wait_idle(&sc.full[slot], (uint32_t)(c / kF2Ring) & 1u);
+      // this parity's buffers (phi's scales, the denominators, the Gram tiles)
+      // were last read by the solve of chunk c - 2
+      if (c >= 2) ok = ok && mbar_wait_idle(&sc.solve_done[par], (uint32_t)((c - 2) >> 1) & 1u);
       const bool carried = c == 0 && p == 0 && a.x_prev != nullptr;
       if (c == 0 && a.x_prev != nullptr && p < 8) {
         // x_1 = x_prev (already phi-mapped) in row 0 of the X tile
@@ -499,112 +660,107 @@ __global__ void __launch_bounds__(kF2Threads, 1)
         mma_k64(tmem + kTmG, smem_addr(xt), false, 16, smem_addr(xt), false, 16,
                 idesc_bf16(128, 64, false, false), false);
         mma_commit(&sc.gdone);
+        mbar_arrive(&sc.xq[slot]);  // the tiles are in place for the chain's MMAs
       }
       // phi's scale of row p (p < 64: x_p = phi(k_{t0+p-1}); else phi(q_{t0+p-64}))
-      float row[64];
-      load_row_bf16(xt, p, row);  // X and Q tiles are contiguous: row p of [X; Q]
-      float ss = 0.f;
-      if (carried) {
-#pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const float x = a.x_prev[bh * 64 + i];
-          ss = fmaf(x, x, ss);
-        }
-      } else {
-        float q8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int i = 0; i < 64; ++i) q8[i & 7] = fmaf(row[i], row[i], q8[i & 7]);
-        ss = ((q8[0] + q8[1]) + (q8[2] + q8[3])) + ((q8[4] + q8[5]) + (q8[6] + q8[7]));
-      }
-      const float nr = carried ? 1.f : phi_scale(ss, 64, a.phi);
-      sc.nrm[p] = nr;
-      if (p < 64) {
-        const float E = ss * nr * nr;
-        const float lam = ridge_of(lam_t, E, a.ridge);
-        const float den = E + lam + a.eps;
-        const bool sentinel = t0 + p == 0 && a.x_prev == nullptr;
-        sc.E[p] = E;
-        sc.lamr[p] = lam;
-        sc.inv[p] = (!sentinel && p < n && den > 0.f) ? 1.f / den : 0.f;
-      }
-      // the Gram has read the raw rows: write phi's rows in place
-      ok = ok && mbar_wait(&sc.gdone, (uint32_t)c & 1u);
-      tc_fence_after();
-      if (!carried) {
-#pragma unroll
-        for (int i = 0; i < 64; ++i) row[i] *= nr;
-        put_row64(xt, p, row);
-      }
-      fence_async_smem();
-      if (named_sync_or(3, 128, !ok || *fail)) {
-        *fail = 1;
-        break;
-      }
-      if (issuer) mbar_arrive(&sc.xq[slot]);
-      // eta, gamma, eta v of token tt, columns 32 hh .. 32 hh + 31
-      float ve[32], ge[32], ee[32];
+      // and the token's step-size denominator
+      float nr;
       {
-        float vv[32];
-        load_half_sw(vt, tt, hh, vv);
-        const float inv = sc.inv[tt], lam = sc.lamr[tt];
+        float row[64];
+        load_row_bf16(xt, p, row);  // X and Q tiles are contiguous: row p of [X; Q]
+        float ss = 0.f;
+        if (carried) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) {
+            const float x = a.x_prev[bh * 64 + i];
+            ss = fmaf(x, x, ss);
+          }
+        } else {
+          float q8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int i = 0; i < 64; ++i) q8[i & 7] = fmaf(row[i], row[i], q8[i & 7]);
+          ss = ((q8[0] + q8[1]) + (q8[2] + q8[3])) + ((q8[4] + q8[5]) + (q8[6] + q8[7]));
+        }
+        nr = carried ? 1.f : phi_scale(ss, 64, a.phi);
+        sc.nrm[par][p] = nr;
+        if (p < 64) {
+          const float E = ss * nr * nr;
+          const float lam = ridge_of(lam_t, E, a.ridge);
+          const float den = E + lam + a.eps;
+          const bool sentinel = t0 + p == 0 && a.x_prev == nullptr;
+          sc.lamr[par][p] = lam;
+          sc.inv[par][p] = (!sentinel && p < n && den > 0.f) ? 1.f / den : 0.f;
+        }
+      }
+      {
+        float* Ab = arr(kAOff, par);
+        float* EVb = arr(kEvOff, par);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float bb[4] = {bet[i].x, bet[i].y, bet[i].z, bet[i].w};
 #pragma unroll
+          for (int e = 0; e < 4; ++e) Ab[jt(32 * hh + 4 * i + e, tt)] = bb[e];
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const __nv_bfloat162* h2v = reinterpret_cast<const __nv_bfloat162*>(&vraw[i]);
+#pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float eta = bb[e] * inv;
-            const float al = eta * lam;
-            ee[4 * i + e] = eta;
-            ge[4 * i + e] = al >= 1.f - eg ? eg : 1.f - al;
-            ve[4 * i + e] = eta * vv[4 * i + e];
+            const float2 f = __bfloat1622float2(h2v[e]);
+            EVb[jt(32 * hh + 8 * i + 2 * e, tt)] = f.x;
+            EVb[jt(32 * hh + 8 * i + 2 * e + 1, tt)] = f.y;
           }
         }
       }
-      // the previous chunk's solve and output are done with these buffers
-      if (c > 0) {
-        ok = ok && mbar_wait(&sc.decu_done, (uint32_t)(c - 1) & 1u);
-        ok = ok && mbar_wait(&sc.out_blk[3], (uint32_t)(c - 1) & 1u);
-      }
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int jj = 32 * hh + i;
-        ETA[jt(jj, tt)] = ee[i];
-        GAM[jt(jj, tt)] = ge[i];
-        ETAV[jt(jj, tt)] = ve[i];
-      }
-      // Gram readback: rows 0..63 K = X X^T (l < t), rows 64..127 P0 = Q X^T (l <= t)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sc.tok_ready[par]);
+      // Gram readback: rows 0..63 are K' = n_t <k_t, k_l> (l < t; the column
+      // scale n_l rides on W'), rows 64..127 the raw causal <q_t, k_l> (l <= t)
+      float d[64];
       {
-        float d[64];
+        ok = ok && mbar_wait_idle(&sc.gdone, (uint32_t)c & 1u);
+        tc_fence_after();
         tmem_ld32(tlane + kTmG, d);
         tmem_ld32(tlane + kTmG + 32, d + 32);
         const bool krow = p < 64;
-        const int t = p & 63, bt = t >> 4, tl = t & 15;
-        float* dg = (krow ? KD : PD) + bt * 256;
+        const float rs = krow ? nr : 1.f;
 #pragma unroll
         for (int l = 0; l < 64; ++l) {
-          const bool keep = krow ? (l < t) : (l <= t);
-          d[l] = keep ? d[l] * nr * sc.nrm[l] : 0.f;
+          const bool keep = krow ? (l < tt) : (l <= tt);
+          d[l] = keep ? d[l] * rs : 0.f;
         }
-        put_row64(base + (krow ? kKbOff : kPbOff), t, d);
+        if (krow) {
+          unsigned char* kbt = base + kKbOff + par * 8192;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) dg[k * 16 + tl] = d[16 * bt + k];
+          for (int q = 0; q < 4; ++q) put_row16(kbt, tt, q, d + 16 * q, 1.f);
+          float* dg = reinterpret_cast<float*>(base + kKdOff) + par * 1024 + (tt >> 4) * 256 +
+                      (tt & 15);
+#pragma unroll
+          for (int bb = 0; bb < 4; ++bb)
+            if (bb == (tt >> 4))
+#pragma unroll
+              for (int k = 0; k < 16; ++k) dg[k * 16] = d[16 * bb + k];
+        }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sc.pre_ready);
-      if (!ok) *fail = 1;
-      // refill: chunk c + 2 into the slot of chunk c - 1 once its chain is done
-      if (issuer && c >= 1 && c + 2 < nch) {
-        const int sl = (c + 2) % kF2Ring;
-        if (mbar_wait(&sc.empty[sl], (uint32_t)((c - 1) / kF2Ring) & 1u))
-          load_chunk(c + 2);
-        else
-          *fail = 1;
+      if (lane == 0) mbar_arrive(&sc.pre_ready[par]);
+      // The P0 tile (single buffer: the output MMA of chunk c - 1 has completed)
+      if (p >= 64) {
+        if (c >= 1)
+          ok = ok && mbar_wait_idle(&sc.odone[(c - 1) & 1], (uint32_t)((c - 1) >> 1) & 1u);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) put_row16(base + kPbOff, tt, q, d + 16 * q, 1.f);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sc.pb_ready);
       }
+      if (!ok) *fail = 1;
     }
     // x_last = phi(k_{T-1})
     if (a.x_last && warp == 4) {
-      const __nv_bfloat16* kl = reinterpret_cast<const __nv_bfloat16*>(a.k) + (rowbase + T - 1) * 64;
+      const __nv_bfloat16* kl =
+          reinterpret_cast<const __nv_bfloat16*>(a.k) + (rowbase + T - 1) * 64;
       const float u0 = __bfloat162float(kl[lane]), u1 = __bfloat162float(kl[lane + 32]);
       const float s2 = phi_scale(warp_sum(u0 * u0 + u1 * u1), 64, a.phi);
       a.x_last[bh * 64 + lane] = u0 * s2;
@@ -625,10 +781,9 @@ bool tc_falcon2_applies(int dtype, int m, int dv, int C, int64_t BH, int64_t T) 
 
 cudaError_t launch_tc_falcon2(const ChunkArgs& a, int* err, cudaStream_t stream) {
   const int nch = (int)((a.T + kF2C - 1) / kF2C);
-  CUtensorMap tm_k, tm_q, tm_v, tm_o;
+  CUtensorMap tm_k, tm_q, tm_o;
   if (!encode_rows_bf16(&tm_k, a.k, 64, (uint64_t)a.T, (uint64_t)a.BH, 64, kF2C) ||
       !encode_rows_bf16(&tm_q, a.q, 64, (uint64_t)a.T, (uint64_t)a.BH, 64, kF2C) ||
-      !encode_rows_bf16(&tm_v, a.v, 64, (uint64_t)a.T, (uint64_t)a.BH, 64, kF2C) ||
       !encode_rows_bf16(&tm_o, a.o, 64, (uint64_t)a.T, (uint64_t)a.BH, 64, kF2C))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(tc_falcon2_chunk_kernel,
@@ -645,7 +800,7 @@ cudaError_t launch_tc_falcon2(const ChunkArgs& a, int* err, cudaStream_t stream)
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_falcon2_chunk_kernel, a, nch, err, tm_k, tm_q, tm_v, tm_o);
+  return cudaLaunchKernelEx(&cfg, tc_falcon2_chunk_kernel, a, nch, err, tm_k, tm_q, tm_o);
 }
 
 }  // namespace falcon
