@@ -15,8 +15,9 @@ The line also carries
   roofline     achieved algorithmic HBM bytes per launch / launch time of
                the dominant kernel against the measured copy bandwidth;
   cpu_baseline the fp64 oracle on this host's cores on a bounded sample;
-  also         the other workloads (Falcon-1A, long context, Falcon-2, Falcon-2A,
-               Falcon-3A, Falcon-1A with the normalised read, the backward, decode).
+  also         the other workloads (Falcon-1A, long context, Falcon-2 and Falcon-2A
+               in chunk form, Falcon-3A, Falcon-1A with the normalised read, the
+               backward, decode).
 
 `--impl reference` times the fp64 CPU oracle (the only reference this method
 has) on the same workload: the whole lm workload (all 96 heads) per step.
@@ -461,8 +462,8 @@ def extra_workloads(falcon, dev):
                                                 want_x_last=False)
             else:
                 def step(x):
-                    falcon.falcon2_fwd_recurrent(x["q"], x["k"], x["v"], x["beta"], x["lambda"],
-                                                 phi=w.phi, o=o, S_out=S, want_x_last=False)
+                    falcon.falcon2_fwd_chunked(x["q"], x["k"], x["v"], x["beta"], x["lambda"],
+                                               phi=w.phi, o=o, S_out=S, want_x_last=False)
         else:
             fn = falcon.falcon1_fwd_chunked if w.rule == "falcon1" else falcon.falcon1a_fwd_chunked
             shape = falcon.make_shape(w.B, w.H, w.T, w.m, w.dv, w.chunk, w.dtype, w.phi)
@@ -676,7 +677,7 @@ def run_profile(args):
                 falcon.falcon3a_fwd_chunked(x["q"], x["k"], x["v"], x["beta"], x["lambda"],
                                             workloads.LM_3A_WINDOW, phi=w.phi)
             elif w.per_column:
-                fn2 = (falcon.falcon2_fwd_recurrent if w.rule == "falcon2"
+                fn2 = (falcon.falcon2_fwd_chunked if w.rule == "falcon2"
                        else falcon.falcon2a_fwd_chunked)
                 fn2(x["q"], x["k"], x["v"], x["beta"], x["lambda"], phi=w.phi)
             else:

@@ -1,9 +1,9 @@
 /*
  * falcon.h -- C ABI of the GB300 (sm_103a) Falcon fast-weight attention
  * library: chunk-parallel forward of Falcon-1 and Falcon-1A and its backward
- * pass, the token-recurrent forward of Falcon-2 and Falcon-2A (per-column
- * step sizes) and of Falcon-3A (sliding window), and the single-token
- * recurrent decode step.
+ * pass, the forward of Falcon-2 and Falcon-2A (per-column step sizes) and of
+ * Falcon-3A (sliding window) in token-recurrent and chunk form, and the
+ * single-token recurrent decode step.
  *
  * The operations are defined on the page hyper.ai/fr/papers/2608.27763
  * ("Fast Weight Attention for Continual Learning"):
@@ -335,15 +335,17 @@ int falcon3a_fwd_recurrent(const falcon_shape *shape, int32_t window,
  * 4.2, per-column step sizes), so inside a chunk of 64 tokens the written
  * residuals u_{t,j} = eta_{j,t} r_{t,j} of column j solve a unit-lower system
  * built from the shared Gram <x_t, x_l> and the column's own decays: one
- * batched per-column triangular solve per chunk, in four blocks of 16 rows
- * (the blocks before a block enter through shared-Gram products).  Decays
- * enter only as products of the gammas, never as exponentials, so clamped
- * and strong decays stay finite.  The chunks of a head are sequential (the
- * per-column systems depend on the entering state): one CTA per head.  For
- * bf16 q, k, v with m = dv = 64 and shape->chunk = 64 this runs on the tensor
- * cores; for every other shape it runs falcon2_fwd_recurrent.  Arguments,
- * layouts, ownership and errors are those of falcon2_fwd_recurrent; no
- * workspace is needed. */
+ * batched per-column triangular solve per chunk.  With E_{t,j} the product of
+ * column j's gammas over the chunk up to token t and w = u / E, the solve is
+ * u_t = eta_t v_t - eta_t E_{t-1} ((X S)_t + sum_{l<t} <x_t, x_l> w_l), the
+ * output o_t = E_t ((Q S)_t + sum_{l<=t} <q_t, x_l> w_l) and the state leaving
+ * the chunk E_C (S + X^T W); a chunk whose decay product falls below e^{-60}
+ * in some column (clamped gammas) runs token by token instead.  The chunks of
+ * a head are sequential (the per-column systems depend on the entering
+ * state): one CTA per head.  For bf16 q, k, v with m = dv = 64 and
+ * shape->chunk = 64 this runs on the tensor cores; for every other shape it
+ * runs falcon2_fwd_recurrent.  Arguments, layouts, ownership and errors are
+ * those of falcon2_fwd_recurrent; no workspace is needed. */
 int falcon2_fwd_chunked(const falcon_shape *shape, const void *q,
                         const void *k, const void *v, const float *beta,
                         const float *lambda, const float *S0,

@@ -1,4 +1,5 @@
-"""fp64 check of the Falcon-2 chunk form the CUDA kernel implements.
+"""fp64 check of the Falcon-2 chunk forms (the blocked decayed-accumulator
+form, and the factored form the CUDA kernel implements).
 
 This is neither the oracle nor the CUDA path: it restates, in numpy, the
 chunk algebra derived from the per-column Falcon-2 update (page
@@ -114,6 +115,73 @@ def chunked_forward2(q, k, v, beta, lam, C=64, blk=16, S0=None, x_prev=None, phi
     return o, S_out
 
 
+def factored_forward2(q, k, v, beta, lam, C=64, blk=16, S0=None, x_prev=None, phi="l2",
+                      eps=1e-6, eps_gamma=1e-6, min_decay=np.exp(-60.0)):
+    """The form the tensor-core kernel runs.  With E_t the product of a
+    column's gammas over the chunk up to token t (E_{-1} = 1) and w = u / E:
+      u_t = eta_t v_t - eta_t E_{t-1} ((X S)_t + sum_{l<t} K_{tl} w_l)
+      o_t = E_t ((Q S)_t + sum_{l<=t} <q_t, x_l> w_l),   S' = E_C (S + X^T W)
+    (e^{G_t - G_l} = E_t / E_l).  Inside a block of `blk` rows the u run token
+    by token; the rows before the block enter as one product K_{b,<b} W_{<b}.
+    A chunk whose decay product falls below `min_decay` in some column runs
+    the tokens one by one (the factors 1 / E would leave the fp32 range)."""
+    BH, T, m = q.shape
+    dv = v.shape[-1]
+    Q, Kf = _phi(q, phi), _phi(k, phi)
+    o = np.zeros((BH, T, dv))
+    S_out = np.zeros((BH, m, dv))
+    n_tokenwise = 0
+    for h in range(BH):
+        S = np.zeros((m, dv)) if S0 is None else S0[h].copy()
+        xp = None if x_prev is None else x_prev[h]
+        for c0 in range(0, T, C):
+            n = min(C, T - c0)
+            X = np.zeros((C, m))
+            Qc = np.zeros((C, m))
+            V = np.zeros((C, dv))
+            eta = np.zeros((C, dv))
+            gam = np.ones((C, dv))
+            for i in range(n):
+                t = c0 + i
+                if t > 0:
+                    X[i] = Kf[h, t - 1]
+                elif xp is not None:
+                    X[i] = xp
+                Qc[i] = Q[h, t]
+                V[i] = v[h, t]
+                sentinel = t == 0 and xp is None
+                den = X[i] @ X[i] + lam[h, t] + eps
+                e = np.zeros(dv) if (sentinel or den <= 0) else beta[h, t] / den
+                a = e * lam[h, t]
+                eta[i] = e
+                gam[i] = np.where(a >= 1 - eps_gamma, eps_gamma, 1 - a)
+            E = np.cumprod(gam, axis=0)
+            if (E[-1] < min_decay).any():
+                n_tokenwise += 1
+                for i in range(n):
+                    u = eta[i] * (V[i] - X[i] @ S)
+                    S = gam[i] * S + np.outer(X[i], u)
+                    o[h, c0 + i] = Qc[i] @ S
+                continue
+            Eprev = np.vstack([np.ones((1, dv)), E[:-1]])
+            Kg = X @ X.T
+            P0 = np.tril(Qc @ X.T)
+            XS, QS = X @ S, Qc @ S
+            W = np.zeros((C, dv))
+            for b in range(C // blk):
+                s = b * blk
+                acc = XS[s:s + blk] + Kg[s:s + blk, :s] @ W[:s]
+                for i in range(blk):
+                    u = eta[s + i] * V[s + i] - eta[s + i] * Eprev[s + i] * acc[i]
+                    W[s + i] = u / E[s + i]
+                    acc[i + 1:] += np.outer(Kg[s + i + 1:s + blk, s + i], W[s + i])
+            O = E * (QS + P0 @ W)
+            o[h, c0:c0 + n] = O[:n]
+            S = E[-1] * (S + X.T @ W)
+        S_out[h] = S
+    return o, S_out, n_tokenwise
+
+
 def _case(seed, BH, T, m, dv, lam_shift=-2.0, carried=False, x_prev=False):
     rng = np.random.default_rng(seed)
     q = rng.standard_normal((BH, T, m))
@@ -164,3 +232,27 @@ def test_blocked_chunk_form_tied_gains_is_falcon1():
     ref = oracle.forward("falcon1", q, k, v, beta1, lam, S0=S0, x_prev=xp)
     np.testing.assert_allclose(o, ref["o"], rtol=1e-9, atol=1e-10)
     np.testing.assert_allclose(S, ref["S"], rtol=1e-9, atol=1e-10)
+
+
+@pytest.mark.parametrize("T", [1, 37, 64, 150])
+@pytest.mark.parametrize("carried", [False, True])
+def test_factored_chunk_form_matches_oracle(T, carried):
+    q, k, v, beta, lam, S0, xp = _case(23 + T, 2, T, 16, 12, carried=carried, x_prev=carried)
+    o, S, nt = factored_forward2(q, k, v, beta, lam, S0=S0, x_prev=xp)
+    assert nt == 0
+    ref = oracle.forward2("falcon2", q, k, v, beta, lam, S0=S0, x_prev=xp)
+    np.testing.assert_allclose(o, ref["o"], rtol=1e-9, atol=1e-10)
+    np.testing.assert_allclose(S, ref["S"], rtol=1e-9, atol=1e-10)
+
+
+def test_factored_chunk_form_strong_decay_runs_token_by_token():
+    """lambda = softplus(n + 3): clamped gammas push some chunks' decay
+    products below e^{-60}; those chunks take the token loop, the others the
+    factored form, and the result is the oracle's."""
+    q, k, v, beta, lam, S0, _ = _case(5, 2, 300, 16, 8, lam_shift=3.0, carried=True)
+    o, S, nt = factored_forward2(q, k, v, beta, lam, S0=S0)
+    assert nt > 0
+    ref = oracle.forward2("falcon2", q, k, v, beta, lam, S0=S0)
+    assert np.isfinite(o).all() and np.isfinite(S).all()
+    np.testing.assert_allclose(o, ref["o"], rtol=1e-8, atol=1e-10)
+    np.testing.assert_allclose(S, ref["S"], rtol=1e-8, atol=1e-10)
