@@ -273,6 +273,11 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
   const bool carried_row = c == 0 && r == 0;
   const bool patch = c == 0 && a.x_prev != nullptr;
 
+  // Waits: with four CTAs per SM (m = 64) the other CTAs' phases run while one
+  // waits, so it polls with a sleep between polls.
+  auto wait = [](uint64_t* bar, uint32_t parity) {
+    return M == 64 ? mbar_wait_backoff(bar, parity) : mbar_wait(bar, parity);
+  };
   // TMEM is allocated by warp 1, so that thread 0 issues the input tile copies
   // (the head of the CTA's chain) without waiting for the allocation.
   if (warp == 1) tmem_alloc(&sc.tmem_base, L::kTmemCols);
@@ -342,7 +347,7 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
   tc_fence_after();
   const uint32_t tmem = sc.tmem_base;
   const uint32_t tlane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-  if (!mbar_wait(&sc.bar_in, 0)) sc.fail = 1;
+  if (!wait(&sc.bar_in, 0)) sc.fail = 1;
   if (patch) {
     // x_1 = x_prev in row 0 of the K tile (bf16) for MMA1.
     if (tid < 8 * (M / 64)) {
@@ -502,7 +507,7 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
     }
   }
   // Every thread sees MMA1 complete before it overwrites the K and Q tiles.
-  if (!sc.fail && !mbar_wait(&sc.bar_mma, 0)) sc.fail = 1;
+  if (!sc.fail && !wait(&sc.bar_mma, 0)) sc.fail = 1;
   tc_fence_after();
   if (!kWide) {
     if (r < 64) store_row(xh_tile, r, 0, xh_scale);
@@ -593,7 +598,7 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
             idesc_bf16(128, 64, true, false), false);
     mma_commit(&sc.bar_mma);
   }
-  if (!mbar_wait(&sc.bar_mma, 1)) sc.fail = 1;
+  if (!wait(&sc.bar_mma, 1)) sc.fail = 1;
   tc_fence_after();
   {
     float d[32];
@@ -628,7 +633,7 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
     }
     mma_commit(&sc.bar_mma);
   }
-  if (!mbar_wait(&sc.bar_mma, 0)) sc.fail = 1;
+  if (!wait(&sc.bar_mma, 0)) sc.fail = 1;
   tc_fence_after();
   // No barrier here: each thread has seen MMA3 complete (its operands are
   // dead) before it stages; a failed wait is agreed on at the staging barrier.
@@ -701,7 +706,7 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
                 idesc_bf16(128, 128, true, false), false);
         mma_commit(&sc.bar_mma);
       }
-      if (!mbar_wait(&sc.bar_mma, 1)) sc.fail = 1;
+      if (!wait(&sc.bar_mma, 1)) sc.fail = 1;
       tc_fence_after();
       // The state rows over the operands of the completed MMA3 (Xt's first
       // atom and P; [W^T; U~^T]).

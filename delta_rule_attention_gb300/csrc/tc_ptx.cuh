@@ -65,14 +65,32 @@ __device__ __forceinline__ uint64_t global_ns() {
 // Bounded wait for the phase with the given parity: gives up after limit_ns of
 // wall time (a try_wait may itself suspend the thread for a while, so the
 // bound is on time, not on iterations).  Returns false on expiry; the caller
-// flags the error and stops waiting.
+// flags the error and stops waiting.  Polls back to back for the first half
+// microsecond, then with a short sleep between polls: many threads polling
+// without pause take shared-memory issue slots from the warps that do the
+// work being waited for.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (;;) {
-    for (int i = 0; i < 64; ++i)
+    for (int i = 0; i < 16; ++i)
       if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t dt = global_ns() - t0;
+    if (dt > limit_ns) return false;
+    if (dt > 512) __nanosleep(32);
+  }
+}
+
+// The same bound, with a short sleep between all polls: for waits that are
+// not on a critical chain (several CTAs per SM whose other phases run meanwhile).
+__device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    __nanosleep(32);
+    if (mbar_try_wait(bar, parity)) return true;
     if (global_ns() - t0 > limit_ns) return false;
   }
 }
