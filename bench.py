@@ -658,9 +658,11 @@ def run_profile(args):
         name, size = d.name, d.N
     else:
         bwd = args.profile.endswith("bwd")
+        norm = args.profile == "lm1anorm"
         w = {"lm": workloads.LM, "lm1a": workloads.LM_1A, "long": workloads.LONG,
              "lm2": workloads.LM_2, "lm2a": workloads.LM_2A, "lm3a": workloads.LM_3A,
-             "lmbwd": workloads.LM, "lm1abwd": workloads.LM_1A}[args.profile]
+             "lmbwd": workloads.LM, "lm1abwd": workloads.LM_1A,
+             "lm1anorm": workloads.LM_1A}[args.profile]
         if args.profile_size:
             w = dataclasses.replace(w, T=args.profile_size)
         x = workloads.generate(w, device=dev)
@@ -668,7 +670,10 @@ def run_profile(args):
             x.update(workloads.cotangents(w.B, w.H, w.T, w.m, w.dv, w.dtype, seed=w.seed,
                                           device=dev))
         for _ in range(calls):
-            if bwd:
+            if norm:
+                falcon.falcon1a_fwd_chunked_normalized(x["q"], x["k"], x["v"], x["beta"],
+                                                       x["lambda"], chunk=w.chunk, phi=w.phi)
+            elif bwd:
                 fnb = (falcon.falcon1_bwd_chunked if w.rule == "falcon1"
                        else falcon.falcon1a_bwd_chunked)
                 fnb(x["q"], x["k"], x["v"], x["beta"], x["lambda"], x["dO"], chunk=w.chunk,
@@ -750,7 +755,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--profile",
                     choices=["lm", "lm1a", "long", "decode", "lm2", "lm2a", "lm3a", "lmbwd",
-                             "lm1abwd"], default=None,
+                             "lm1abwd", "lm1anorm"], default=None,
                     help="profiler target: run --steps calls of one workload, print no timing")
     ap.add_argument("--host-link", action="store_true",
                     help="measure pinned host<->device copy bandwidth at the e2e sizes")

@@ -118,7 +118,7 @@ __device__ __forceinline__ void store_half_split(unsigned char* hi, unsigned cha
 
 // Wait for the MMA group committed last, with the CTA-wide failure agreement.
 __device__ __forceinline__ bool wait_mma(BwdScalars& sc, uint32_t& phase) {
-  if (!mbar_wait(&sc.bar_mma, phase)) sc.fail = 1;
+  if (!mbar_wait_backoff(&sc.bar_mma, phase)) sc.fail = 1;
   phase ^= 1u;
   tc_fence_after();
   return !__syncthreads_or(sc.fail);
@@ -128,7 +128,7 @@ __device__ __forceinline__ bool wait_mma(BwdScalars& sc, uint32_t& phase) {
 // accumulators and overwrites tiles the completed MMAs no longer need, it
 // needs no other thread; a failed wait is agreed on at the next barrier.
 __device__ __forceinline__ void wait_mma_own(BwdScalars& sc, uint32_t& phase) {
-  if (!mbar_wait(&sc.bar_mma, phase)) sc.fail = 1;
+  if (!mbar_wait_backoff(&sc.bar_mma, phase)) sc.fail = 1;
   phase ^= 1u;
   tc_fence_after();
 }
@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(kBThreads, 2)
   uint32_t phase = 0;
   float gC = 0.f, rr = 0.f;
   bool factored = false;
-  if (!mbar_wait(&sc.bar_in, 0)) sc.fail = 1;
+  if (!mbar_wait_backoff(&sc.bar_in, 0)) sc.fail = 1;
   if (__syncthreads_or(sc.fail)) goto teardown;
 
   // ---- features: rows 0..63 of [X; Q] are x_i = phi(k_{t0+i-1}) (x_prev, or

@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(k2Threads, 2)
   const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 32 * h;
   uint32_t phase = 0;
   bool slow = false;
-  if (!mbar_wait(&sc.bar_in, 0)) sc.fail = 1;
+  if (!mbar_wait_backoff(&sc.bar_in, 0)) sc.fail = 1;
   if (__syncthreads_or(sc.fail)) goto teardown;
 
   // ---- features: rows 0..63 of [X; Q] are x_t = phi(k_{t-1}) (x_prev, or the
@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(k2Threads, 2)
     }
     store_half_sw(tile(r < 64 ? kU2 : kVp2), s, h, r < 64 ? u : v, 1.f);
   }
-  if (!mbar_wait(&sc.bar_mma, phase)) sc.fail = 1;
+  if (!mbar_wait_backoff(&sc.bar_mma, phase)) sc.fail = 1;
   phase ^= 1u;
   tc_fence_after();
   // No barrier: each thread has seen the MMA complete before it reads its
@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(k2Threads, 2)
             idesc_bf16(128, 64, true, true), false);
     mma_commit(&sc.bar_mma);
   }
-  if (!mbar_wait(&sc.bar_mma, phase)) sc.fail = 1;
+  if (!mbar_wait_backoff(&sc.bar_mma, phase)) sc.fail = 1;
   phase ^= 1u;
   tc_fence_after();
   // No barrier: each thread has seen the MMAs complete before it overwrites

@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(k3Threads, 3)
   const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 32 * h;
   uint32_t phase = 0;
   float gC = 0.f;
-  if (!mbar_wait(&sc.bar_in, 0)) sc.fail = 1;
+  if (!mbar_wait_backoff(&sc.bar_in, 0)) sc.fail = 1;
   if (__syncthreads_or(sc.fail)) goto teardown;
 
   // ---- features: row r of X~ is x_j, j = t0 - 64 + r (x_0 = 0: the boundary
@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(k3Threads, 3)
     }
   }
   __syncthreads();
-  if (!mbar_wait(&sc.bar_mma, phase)) sc.fail = 1;
+  if (!mbar_wait_backoff(&sc.bar_mma, phase)) sc.fail = 1;
   phase ^= 1u;
   tc_fence_after();
   // P = (Q X~^T) o W, rows 0..63 (lanes 0..63), two column halves per tile:
@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(k3Threads, 3)
     mma_k64(tmem + 64, taddr(kX1), true, k3Tile, taddr(kVs1), true, k3Tile, id_xv, true);
     mma_commit(&sc.bar_mma);
   }
-  if (!mbar_wait(&sc.bar_mma, phase)) sc.fail = 1;
+  if (!mbar_wait_backoff(&sc.bar_mma, phase)) sc.fail = 1;
   phase ^= 1u;
   tc_fence_after();
   // No barrier: each thread has seen the MMAs complete before it overwrites
