@@ -184,46 +184,72 @@ __global__ void __launch_bounds__(kNormThreads)
       if (lane >= o) g0 += y0, g1 += y1;
     }
     g1 += __shfl_sync(0xffffffffu, g0, 31);
-    if (lane < C) ws[L.eg() + mi * C + lane] = __expf(g0);
-    if (lane + 32 < C) ws[L.eg() + mi * C + lane + 32] = __expf(g1);
+    if (lane < C) ws[L.eg() + mi * C + lane] = __expf(g0), lg[lane] = g0;
+    if (lane + 32 < C) ws[L.eg() + mi * C + lane + 32] = __expf(g1), lg[lane + 32] = g1;
     const int last = n - 1;
     const float gl = __shfl_sync(0xffffffffu, last < 32 ? g0 : g1, last & 31);
     if (lane == 0) ws[L.dec() + mi * 4] = __expf(gl);
   }
   // in-chunk normaliser, one thread per feature dimension: y_t = gamma_t
-  // y_{t-1} + eta_t x_t, and the products y_t[i] phi(q_t)[i] over q's rows
-  if (tid < m) {
-    float y = 0.f;
-    // (rows at and past n were loaded as zeros and have eta = 0, gamma = 1:
-    // the steps past n leave y as it is)
-    for (int r = 0; r < n; r += 4) {
+  // y_{t-1} + eta_t x_t, and the products y_t[i] phi(q_t)[i] (over the x rows,
+  // each read just before).  With m <= 64 the CTA's two halves take the two
+  // halves of the chunk's tokens, each from y = 0; the second half's reads and
+  // the chunk's increment then add the first half's last y, decayed by
+  // e^{g_t - g_{H-1}}.
+  __shared__ float yh[128], y1s[128];
+  const bool split = 2 * m <= kNormThreads;
+  const int H = split ? C / 2 : C;
+  const int half = split ? tid / m : 0, fi = tid - half * m;
+  float y = 0.f;  // (the prefix g written over lg above is read after the next barrier)
+  if (tid < (split ? 2 * m : m)) {
+    const int rs = half == 0 ? 0 : H, re = half == 0 ? min(n, H) : n;
+    // (rows at and past n were loaded as zeros and have eta = 0, gamma = 1)
+    for (int r = rs; r < re; r += 4) {
       float g4[4], w4[4], s4[4], q4[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int rr = min(r + u, C - 1);
-        g4[u] = r + u < n ? gm[rr] : 1.f;
-        w4[u] = r + u < n ? eta[rr] * xs[rr * m + tid] : 0.f;
+        g4[u] = r + u < re ? gm[rr] : 1.f;
+        w4[u] = r + u < re ? eta[rr] * xs[rr * m + fi] : 0.f;
         s4[u] = sq[rr];
-        q4[u] = qs[rr * m + tid];
+        q4[u] = qs[rr * m + fi];
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         y = fmaf(g4[u], y, w4[u]);
-        if (r + u < C) qs[(r + u) * m + tid] = y * (s4[u] * q4[u]);
+        if (r + u < re) xs[(r + u) * m + fi] = y * (s4[u] * q4[u]);
       }
     }
-    ws[L.inc() + mi * m + tid] = y;
+    if (split) (half == 0 ? yh : y1s)[fi] = y;
   }
   __syncthreads();
+  // the chunk's increment y_C
+  if (tid < m) {
+    float inc = y;
+    if (split) inc = n > H ? fmaf(__expf(lg[n - 1] - lg[H - 1]), yh[tid], y1s[tid]) : yh[tid];
+    ws[L.inc() + mi * m + tid] = inc;
+  }
   // r_t = <phi(q_t), y_t>, one thread per token (element (r, (i + r) mod m):
   // the threads of a warp read different banks)
   if (tid < C) {
     const int r = tid;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    if (r < n)
+    if (r < n) {
       for (int i = 0; i < m; i += 4)
 #pragma unroll
-        for (int u = 0; u < 4; ++u) acc[u] += qs[r * m + ((i + u + r) & (m - 1))];
+        for (int u = 0; u < 4; ++u) acc[u] += xs[r * m + ((i + u + r) & (m - 1))];
+      if (split && r >= H) {
+        float dq[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int i = 0; i < m; i += 4)
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int e = (i + u + r) & (m - 1);
+            dq[u] = fmaf(qs[r * m + e], yh[e], dq[u]);
+          }
+        acc[0] = fmaf(__expf(lg[r] - lg[H - 1]) * sq[r], (dq[0] + dq[1]) + (dq[2] + dq[3]),
+                      acc[0]);
+      }
+    }
     ws[L.rd() + mi * C + r] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
     ws[L.nq() + mi * C + r] = sq[r];
   }
