@@ -292,12 +292,21 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
     sc.fail = 0;
     // k rows t0-1 .. t0+62, q and v rows t0 .. t0+63 (rows past T read as zeros).
     mbar_expect_tx(&sc.bar_in, (kWide ? 5 : 3) * 8192);
+    if constexpr (!kWide) {
+      // The inputs are read once; the chunk maps this grid writes (101 MB on
+      // the lm shape) are read again by the scan: the inputs leave L2 first.
+      const uint64_t pol = l2_evict_first();
+      tma_load_3d_hint(kt, &tm_k, 0, (int)(t0 - 1), (int)bh, &sc.bar_in, pol);
+      tma_load_3d_hint(qt, &tm_q, 0, (int)t0, (int)bh, &sc.bar_in, pol);
+      tma_load_3d_hint(vh, &tm_v, 64 * j, (int)t0, (int)bh, &sc.bar_in, pol);
+    } else {
 #pragma unroll
-    for (int at = 0; at < (kWide ? 2 : 1); ++at) {
-      tma_load_3d(kt + at * L::kAtom, &tm_k, 64 * at, (int)(t0 - 1), (int)bh, &sc.bar_in);
-      tma_load_3d(qt + at * L::kAtom, &tm_q, 64 * at, (int)t0, (int)bh, &sc.bar_in);
+      for (int at = 0; at < (kWide ? 2 : 1); ++at) {
+        tma_load_3d(kt + at * L::kAtom, &tm_k, 64 * at, (int)(t0 - 1), (int)bh, &sc.bar_in);
+        tma_load_3d(qt + at * L::kAtom, &tm_q, 64 * at, (int)t0, (int)bh, &sc.bar_in);
+      }
+      tma_load_3d(vh, &tm_v, 64 * j, (int)t0, (int)bh, &sc.bar_in);
     }
-    tma_load_3d(vh, &tm_v, 64 * j, (int)t0, (int)bh, &sc.bar_in);
   }
   // CTAs are dispatched close to linear block order, so the one that takes
   // this CTA's slot is about pf_ahead (the resident CTAs of the device) blocks
@@ -664,7 +673,7 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
       const bool failed = grp ? named_sync_or(2, 128, sc.fail) : named_sync_or(1, 128, sc.fail);
       // Mc leaves while Nc is staged.
       if (lead && !failed) {
-        bulk_s2g(map + half, mc_stage + half, kMcBytes / 2);
+        bulk_s2g_hint(map + half, mc_stage + half, kMcBytes / 2, l2_evict_last());
         bulk_commit();
       }
       store_half_sw(nc_stage, r, h, d, 1.f);  // Nc: chunk cc at position cc ^ (row & 7)
@@ -675,7 +684,7 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
         named_sync(1, 128);
       if (lead && !failed) {
         if (grp == 0) *reinterpret_cast<float*>(map + kMcBytes + kNcBytes) = __expf(gC);
-        bulk_s2g(map + kMcBytes + half, nc_stage + half, kNcBytes / 2);
+        bulk_s2g_hint(map + kMcBytes + half, nc_stage + half, kNcBytes / 2, l2_evict_last());
         bulk_commit();
         bulk_wait_read<0>();  // the staging must outlive the copies' reads
       }
@@ -780,8 +789,9 @@ using RecScanSmem = ScanSmemT<kRecStages, false>;
 template <typename Smem>
 __device__ __forceinline__ void issue_map_load(Smem& s, int st, const unsigned char* m) {
   mbar_expect_tx(&s.full[st], kMcBytes + kNcBytes + 16);
-  bulk_g2s(s.mc[st], m, kMcBytes, &s.full[st]);
-  bulk_g2s(s.nc[st], m + kMcBytes, kNcBytes, &s.full[st]);
+  const uint64_t pol = l2_evict_first();
+  bulk_g2s_hint(s.mc[st], m, kMcBytes, &s.full[st], pol);
+  bulk_g2s_hint(s.nc[st], m + kMcBytes, kNcBytes, &s.full[st], pol);
   bulk_g2s(s.gc[st], m + kMcBytes + kNcBytes, 16, &s.full[st]);
 }
 

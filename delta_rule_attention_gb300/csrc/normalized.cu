@@ -370,8 +370,8 @@ __global__ void __launch_bounds__(kNormThreads)
         for (int u = 0; u < 4; ++u) f[u] /= den;
       }
       const int64_t row = bh * a.T + t0 + r;
-      *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(a.o) + (row * dv + sub * vec) * es) =
-          ov[k];
+      unsigned char* op = reinterpret_cast<unsigned char*>(a.o) + (row * dv + sub * vec) * es;
+      *reinterpret_cast<uint4*>(op) = ov[k];
     }
   }
 }
