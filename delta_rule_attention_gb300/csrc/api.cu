@@ -83,7 +83,7 @@ int fwd_chunked(int rule, const falcon_shape* s, const void* q, const void* k, c
                 const float* beta, const float* lambda, const float* S0, const float* x_prev,
                 void* o, float* S_out, float* x_last, void* workspace, size_t workspace_bytes,
                 cudaStream_t stream, int window = 1, bool chunked_form = false,
-                int (*resolve_workspace)(void**) = nullptr) {
+                int (*resolve_workspace)(void**) = nullptr, float* norm_ws = nullptr) {
   int rc = check_shape(s);
   if (rc) return rc;
   const int64_t BH = s->B * s->H;
@@ -161,6 +161,7 @@ int fwd_chunked(int rule, const falcon_shape* s, const void* q, const void* k, c
   a.S_out = S_out;
   a.x_last = x_last;
   a.workspace = workspace;
+  a.norm_ws = norm_ws;
   if (per_column || windowed) {
     int* err = device_error_word();
     if (!err) return FALCON_ERR_CUDA;
@@ -381,8 +382,15 @@ int falcon1a_fwd_chunked_normalized(const falcon_shape* s, const void* q, const 
   // The numerator: the Falcon-1A forward (every remaining check is its own;
   // nothing is launched when one fails).
   const size_t base = s->T > 0 ? norm_offset(s) : workspace_bytes;
+  float* ws = s->T > 0
+                  ? reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + base)
+                  : nullptr;
+  // On the tensor-core path with m = 64 the forward's map launch writes the
+  // denominator's per-chunk terms as well.
+  const bool terms_in_maps =
+      ws && s->m == 64 && falcon::tc_path_applies(s->dtype, s->m, s->dv, s->chunk, BH, s->T);
   rc = fwd_chunked(falcon::kFalcon1A, s, q, k, v, beta, lambda, S0, x_prev, o, S_out, x_last,
-                   workspace, base, stream);
+                   workspace, base, stream, 1, false, nullptr, terms_in_maps ? ws : nullptr);
   if (rc) return rc;
   const size_t feat_bytes = sizeof(float) * (size_t)BH * s->m;
   if (s->T == 0) {  // z_T = z0
@@ -416,8 +424,7 @@ int falcon1a_fwd_chunked_normalized(const falcon_shape* s, const void* q, const 
   a.S_out = S_out;
   a.x_last = x_last;
   a.workspace = workspace;
-  float* ws = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + base);
-  return to_status(falcon::launch_normalizer(a, z0, z_out, eps_attn, ws, stream));
+  return to_status(falcon::launch_normalizer(a, z0, z_out, eps_attn, ws, terms_in_maps, stream));
 }
 
 size_t falcon_bwd_workspace_bytes(const falcon_shape* s) {

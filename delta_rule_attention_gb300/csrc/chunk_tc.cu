@@ -235,7 +235,11 @@ constexpr int kMapThreads = 256;
 
 // 256 threads per CTA: thread t owns row r = t & 127 (its TMEM lane) and
 // columns 32h .. 32h+31 (h = t >> 7) of the CTA's 64-column half j.
-template <int M>
+// kNorm (m = 64): the launch also writes the normalised read's per-chunk terms
+// to a.norm_ws (NormLayout): e^{g_t}, e^{g_C}, phi's scale of q_t, the
+// in-chunk read r_t = sum_{j <= t} P_tj eta_j (P's fp32 rows before they are
+// rounded for MMA3) and the increment y_C = sum_j eta_j e^{g_C - g_j} x_j.
+template <int M, bool kNorm = false>
 __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
     tc_chunk_map_kernel(ChunkArgs a, int nchunks, int c_begin, int* err, uint32_t pf_ahead,
                         const __grid_constant__ CUtensorMap tm_k,
@@ -243,6 +247,7 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
                         const __grid_constant__ CUtensorMap tm_v) {
   using L = MapLayout<M>;
   constexpr bool kWide = M == 128;
+  static_assert(!kNorm || M == 64, "the normalised read's terms: m = 64");
   extern __shared__ unsigned char smem_raw[];
   unsigned char* const base = align1024(smem_raw);
   unsigned char* const kt = base + L::K;
@@ -272,6 +277,9 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
   // the sentinel zero (the TMA box starts at row -1, which reads as zeros).
   const bool carried_row = c == 0 && r == 0;
   const bool patch = c == 0 && a.x_prev != nullptr;
+  const NormLayout nl{a.BH * nchunks, 64, kC};
+  const size_t mi = (size_t)(bh * nchunks + c);
+  float ypart = 0.f;  // kNorm: this lane's column of the increment over its warp's rows
 
   // Waits: with four CTAs per SM (m = 64) the other CTAs' phases run while one
   // waits, so it polls with a sleep between polls.
@@ -428,6 +436,9 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
   const float ss = sc.ssp[0][r] + sc.ssp[1][r];
   const float nr = carried_row ? 1.f : phi_scale(ss, M, a.phi);
   if (h == 0) sc.nrm[r] = nr;
+  if constexpr (kNorm) {
+    if (h == 0 && r >= 64) a.norm_ws[nl.nq() + mi * kC + (r - 64)] = r - 64 < n ? nr : 1.f;
+  }
   if (a.x_last && last) {
     // phi(k_{T-1}) (columns of half j): row n of the features when the last
     // chunk is partial, otherwise the row after the K tile, from global memory.
@@ -487,6 +498,10 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
     sc.eta[tid] = eo;
     sc.g[tid] = go;
     sc.gx[tid] = go - lo;
+    if constexpr (kNorm) {
+      a.norm_ws[nl.eg() + mi * kC + tid] = __expf(go);
+      if (tid == 0) a.norm_ws[nl.dec() + mi * 4] = __expf(gCw);
+    }
     // Rank-1 decay factors around rr = g_C / 2: e^{rr - g_l} (times phi's scale
     // of x_l), fv_j = eta_j e^{g_{j-1} - rr}, fw_i = e^{g_i - rr}.
     if (-gCw <= kFactorSpan) {
@@ -537,6 +552,7 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
       for (int cc = 0; cc < 4; ++cc)
         *reinterpret_cast<uint4*>(p_tile + sw_chunk(r - 64, 4 * h + cc)) =
             make_uint4(0u, 0u, 0u, 0u);
+      if constexpr (kNorm) sc.ssp[1][r - 64] = 0.f;  // (the half rows' sums are dead)
     } else if (!above && (r >= 64 || f1)) {
       float d[32];
       tmem_ld32(tlane + 32 * h, d);
@@ -588,11 +604,21 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
           for (int jj = 0; jj < 32; ++jj)
             d[jj] = (32 * h + jj <= i) ? __expf(fminf(gi - sc.g[32 * h + jj], 0.f)) * d[jj] : 0.f;
         }
+        if constexpr (kNorm) {
+          float rs = 0.f;
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) rs = fmaf(d[jj], sc.eta[32 * h + jj], rs);
+          sc.ssp[h][i] = rs;
+        }
         store_half_sw(p_tile, i, h, d, 1.f);
       }
     }
   }
   if (__syncthreads_or(sc.fail)) goto teardown;  // A and P complete
+  if constexpr (kNorm) {
+    if (r >= 64 && h == 0)
+      a.norm_ws[nl.rd() + mi * kC + (r - 64)] = sc.ssp[0][r - 64] + sc.ssp[1][r - 64];
+  }
 
   // ---- T' = (I + A)^{-1} Diag(eta) into the T tile (Falcon-1A: Diag(eta), written above) ----
   if (f1) solve_unit_lower_sw<true>(a_tile, a_diag, t_tile, base + L::DB, sc.eta);
@@ -621,10 +647,45 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
     reinterpret_cast<uint4*>(zero_tile)[tid] = make_uint4(0u, 0u, 0u, 0u);
     reinterpret_cast<uint4*>(zero_tile)[tid + 256] = make_uint4(0u, 0u, 0u, 0u);
   }
+  // The normaliser's increment y_C over this warp's 32 rows (warps 0, 1, 4, 5):
+  // the rows' scaled half rows are summed down the lanes by halving exchanges
+  // (after the one over lane bit b, a lane keeps the columns whose bit b is its
+  // own), which leave column 32h + lane with lane.  Rows 32..63 go through the
+  // dead decay factors; rows 0..31 add them after the next barrier.
+  if constexpr (kNorm) {
+    if (r < 64) {
+      const float s = sc.eta[r] * __expf(gC - sc.g[r]) * nr;
+      const float* xg = carried_fp32 ? a.x_prev + bh * M + 32 * h : nullptr;  // x_1 = x_prev
+      auto xv = [&](int i) { return carried_fp32 ? xg[i] : xp.at(i); };
+      float y16[16], y8[8], y4[4], y2[2];
+      const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2, b0 = lane & 1;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float lo = xv(i) * s, hi = xv(i + 16) * s;
+        y16[i] = (b4 ? hi : lo) + __shfl_xor_sync(0xffffffffu, b4 ? lo : hi, 16);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        y8[i] = (b3 ? y16[i + 8] : y16[i]) +
+                __shfl_xor_sync(0xffffffffu, b3 ? y16[i] : y16[i + 8], 8);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        y4[i] = (b2 ? y8[i + 4] : y8[i]) + __shfl_xor_sync(0xffffffffu, b2 ? y8[i] : y8[i + 4], 4);
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        y2[i] = (b1 ? y4[i + 2] : y4[i]) + __shfl_xor_sync(0xffffffffu, b1 ? y4[i] : y4[i + 2], 2);
+      ypart = (b0 ? y2[1] : y2[0]) + __shfl_xor_sync(0xffffffffu, b0 ? y2[0] : y2[1], 1);
+      if (warp & 1) sc.cu[32 * h + lane] = ypart;
+    }
+  }
   fence_async_smem();
   tc_fence_before();
   if (__syncthreads_or(sc.fail)) goto teardown;
   tc_fence_after();
+  if constexpr (kNorm) {
+    if (r < 64 && (warp & 1) == 0)
+      a.norm_ws[nl.inc() + mi * 64 + 32 * h + lane] = ypart + sc.cu[32 * h + lane];
+  }
 
   // ---- MMA3 ----
   //   m = 64:  D[0:128) = [Xt^T; 0] [W | U~] + [0; P] [W | U~]
@@ -1342,8 +1403,13 @@ cudaError_t launch_map(const ChunkArgs& a, int nchunks, int c_begin, int n, int*
                        const CUtensorMap& tm_k, const CUtensorMap& tm_q, const CUtensorMap& tm_v,
                        bool pdl, cudaStream_t stream) {
   const size_t smem = map_smem_bytes<M>() + 1024;
-  cudaError_t e = cudaFuncSetAttribute(tc_chunk_map_kernel<M>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  // The variant that also writes the normalised read's per-chunk terms (m = 64).
+  auto kernel = tc_chunk_map_kernel<M, false>;
+  if constexpr (M == 64) {
+    if (a.norm_ws) kernel = tc_chunk_map_kernel<64, true>;
+  }
+  cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n * MapLayout<M>::kHalves, (unsigned)a.BH);
@@ -1355,9 +1421,8 @@ cudaError_t launch_map(const ChunkArgs& a, int nchunks, int c_begin, int n, int*
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, tc_chunk_map_kernel<M>, a, nchunks, c_begin, err,
-                            map_residency<M>(), tm_k, tm_q,
-                            tm_v);
+  return cudaLaunchKernelEx(&cfg, kernel, a, nchunks, c_begin, err, map_residency<M>(), tm_k,
+                            tm_q, tm_v);
 }
 
 // pdl: programmatic dependent launch after the preceding map launch on the

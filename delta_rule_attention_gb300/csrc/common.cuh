@@ -89,6 +89,24 @@ struct ChunkArgs {
   // Tensor-core path, m = 64: the state entering every chunk is also written
   // here when non-null ([B*H, chunks, m, dv] f32; for the backward pass).
   float* S_starts = nullptr;
+  // Tensor-core path, m = 64: the normalised read's per-chunk terms (NormLayout
+  // below) are also written here by the map launch when non-null.
+  float* norm_ws = nullptr;
+};
+
+// Workspace of the normalised read's denominator, in floats, per (head,
+// chunk) mi = bh * chunks + c: z entering the chunk (m), the chunk's increment
+// y_C (m), its decay e^{g_C} (1, padded to 4), and per token e^{g_t}, phi's
+// scale of q_t and the in-chunk read r_t = <phi(q_t), y_t> (C each).
+struct NormLayout {
+  int64_t maps, m, C;
+  __host__ __device__ size_t zin() const { return 0; }
+  __host__ __device__ size_t inc() const { return (size_t)(maps * m); }
+  __host__ __device__ size_t dec() const { return (size_t)(2 * maps * m); }
+  __host__ __device__ size_t eg() const { return dec() + (size_t)(maps * 4); }
+  __host__ __device__ size_t nq() const { return eg() + (size_t)(maps * C); }
+  __host__ __device__ size_t rd() const { return nq() + (size_t)(maps * C); }
+  __host__ __device__ size_t floats() const { return rd() + (size_t)(maps * C); }
 };
 size_t generic_workspace_bytes(int64_t BH, int64_t T, int m, int dv, int C);
 // a.o and a.S_out may be null (not written); S_starts (nullable) receives the
@@ -144,9 +162,12 @@ cudaError_t launch_tc_bwd_scan(const BwdArgs& b, const void* maps, float* dS_end
 // Falcon-1A's normalised read: the denominator z_t^T phi(q_t) + eps_attn
 // (z_t = gamma_t z_{t-1} + eta_t x_t) and the division of o in place, after
 // the Falcon-1A forward has written o.  ws: norm_workspace_bytes bytes.
+// chunk_terms_written: the forward's map launch has already written the
+// per-chunk terms (increment, decays, phi's scales of q, in-chunk reads) to ws
+// (ChunkArgs::norm_ws), so the in-chunk kernel is not launched.
 size_t norm_workspace_bytes(int64_t BH, int64_t T, int m, int C);
 cudaError_t launch_normalizer(const ChunkArgs& a, const float* z0, float* z_out, float eps_attn,
-                              float* ws, cudaStream_t stream);
+                              float* ws, bool chunk_terms_written, cudaStream_t stream);
 
 struct DecodeArgs {
   int rule;

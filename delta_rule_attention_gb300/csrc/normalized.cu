@@ -11,7 +11,9 @@
 // The numerator is the Falcon-1A chunked forward (the tensor-core or generic
 // path).  The denominator runs beside it in three fp32 kernels, the chunk
 // form of the z recurrence (z is the state column a constant unit target
-// would write):
+// would write); on the tensor-core path with m = 64 the forward's map launch
+// writes the terms of kernel 1 (it holds the chunk's features, step sizes,
+// decays and decayed Gram rows already), and only kernels 2 and 3 run:
 //   1. norm_chunk_kernel, one CTA per (head, chunk): the tokens' phi scales,
 //      eta_t and log gamma_t; the in-chunk normaliser y_t (z started from 0
 //      at the chunk), its read r_t = <phi(q_t), y_t>, the prefix decays
@@ -29,20 +31,6 @@ namespace falcon {
 namespace {
 
 constexpr int kNormThreads = 128;
-
-// Workspace of the denominator, per (head, chunk): z entering the chunk (m),
-// the chunk's increment y_C (m), its decay e^{g_C} (1, padded to 4), and per
-// token e^{g_t}, phi's scale of q_t and r_t (C each).
-struct NormLayout {
-  int64_t maps, m, C;
-  __host__ __device__ size_t zin() const { return 0; }
-  __host__ __device__ size_t inc() const { return (size_t)(maps * m); }
-  __host__ __device__ size_t dec() const { return (size_t)(2 * maps * m); }
-  __host__ __device__ size_t eg() const { return dec() + (size_t)(maps * 4); }
-  __host__ __device__ size_t nq() const { return eg() + (size_t)(maps * C); }
-  __host__ __device__ size_t rd() const { return nq() + (size_t)(maps * C); }
-  __host__ __device__ size_t floats() const { return rd() + (size_t)(maps * C); }
-};
 
 // One CTA per (chunk, head), 128 threads.  Shared: the chunk's write features
 // x (C x m, raw, row 0 = the token before the chunk) and raw q rows (C x m),
@@ -385,16 +373,19 @@ size_t norm_workspace_bytes(int64_t BH, int64_t T, int m, int C) {
 }
 
 cudaError_t launch_normalizer(const ChunkArgs& a, const float* z0, float* z_out, float eps_attn,
-                              float* ws, cudaStream_t stream) {
+                              float* ws, bool chunk_terms_written, cudaStream_t stream) {
   const int nchunks = (int)((a.T + a.C - 1) / a.C);
   const NormLayout L{a.BH * nchunks, a.m, a.C};
-  const size_t smem = sizeof(float) * (size_t)(2 * a.C * a.m + 5 * a.C);
-  cudaError_t e = cudaFuncSetAttribute(norm_chunk_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  norm_chunk_kernel<<<dim3(nchunks, (unsigned)a.BH), kNormThreads, smem, stream>>>(a, nchunks, L,
-                                                                                   ws);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  if (!chunk_terms_written) {
+    const size_t smem = sizeof(float) * (size_t)(2 * a.C * a.m + 5 * a.C);
+    e = cudaFuncSetAttribute(norm_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+    norm_chunk_kernel<<<dim3(nchunks, (unsigned)a.BH), kNormThreads, smem, stream>>>(a, nchunks,
+                                                                                     L, ws);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   norm_chain_kernel<<<(unsigned)a.BH, kNormThreads, 0, stream>>>(a.BH, a.m, nchunks, L, ws,
                                                                    ws + L.zin(), z0, z_out);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
