@@ -281,9 +281,14 @@ __global__ void __launch_bounds__(kNormThreads)
 
 // One CTA per (chunk, head): den_t and o_t /= den_t.  A group of G lanes takes
 // one token: 16-byte pieces of its q row (the read of z) and of its o row,
-// loaded before the read is formed.
+// loaded before the read is formed.  own_chain (few chunks, and z_out not
+// overlapping z0): the CTA runs the chain up to its chunk itself, with the
+// chain kernel's operations in its order, and the last chunk's CTA writes z_T.
+constexpr int kOwnChainChunks = 64;
+constexpr int kOwnChainAhead = 8;
 __global__ void __launch_bounds__(kNormThreads)
-    norm_apply_kernel(ChunkArgs a, int nchunks, NormLayout L, const float* ws, float eps_attn) {
+    norm_apply_kernel(ChunkArgs a, int nchunks, NormLayout L, const float* ws, float eps_attn,
+                      bool own_chain, const float* z0, float* z_out) {
   __shared__ float zc[128], fq[64], fr[64];
   const int C = a.C, m = a.m, dv = a.dv;
   const int c = blockIdx.x;
@@ -292,7 +297,28 @@ __global__ void __launch_bounds__(kNormThreads)
   const int64_t t0 = (int64_t)c * C;
   const int n = (int)min((int64_t)C, a.T - t0);
   const size_t mi = (size_t)(bh * nchunks + c);
-  if (tid < m) zc[tid] = ws[L.zin() + mi * m + tid];
+  if (tid < m) {
+    if (own_chain) {
+      const size_t m0 = (size_t)(bh * nchunks);
+      float z = z0 ? z0[bh * m + tid] : 0.f;
+      for (int u0 = 0; u0 < c; u0 += kOwnChainAhead) {
+        float d[kOwnChainAhead], y[kOwnChainAhead];
+#pragma unroll
+        for (int k = 0; k < kOwnChainAhead; ++k) {
+          d[k] = u0 + k < c ? ws[L.dec() + (m0 + u0 + k) * 4] : 0.f;
+          y[k] = u0 + k < c ? ws[L.inc() + (m0 + u0 + k) * m + tid] : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < kOwnChainAhead; ++k)
+          if (u0 + k < c) z = fmaf(d[k], z, y[k]);
+      }
+      zc[tid] = z;
+      if (z_out && c == nchunks - 1)
+        z_out[bh * m + tid] = fmaf(ws[L.dec() + mi * 4], z, ws[L.inc() + mi * m + tid]);
+    } else {
+      zc[tid] = ws[L.zin() + mi * m + tid];
+    }
+  }
   if (tid < C) {
     fq[tid] = ws[L.eg() + mi * C + tid] * ws[L.nq() + mi * C + tid];  // e^{g_t} phi's scale of q_t
     fr[tid] = ws[L.rd() + mi * C + tid] + eps_attn;
@@ -386,11 +412,19 @@ cudaError_t launch_normalizer(const ChunkArgs& a, const float* z0, float* z_out,
                                                                                      L, ws);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  norm_chain_kernel<<<(unsigned)a.BH, kNormThreads, 0, stream>>>(a.BH, a.m, nchunks, L, ws,
-                                                                   ws + L.zin(), z0, z_out);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  norm_apply_kernel<<<dim3(nchunks, (unsigned)a.BH), kNormThreads, 0, stream>>>(a, nchunks, L, ws,
-                                                                                eps_attn);
+  // Few chunks: every apply CTA runs the chain to its chunk (no chain launch),
+  // unless z_out overlaps z0 (the last chunk's CTA would write z_T while
+  // others still read z0).
+  const size_t feat = (size_t)a.BH * a.m;
+  const bool overlap = z0 && z_out && z_out < z0 + feat && z0 < z_out + feat;
+  const bool own_chain = nchunks <= kOwnChainChunks && !overlap;
+  if (!own_chain) {
+    norm_chain_kernel<<<(unsigned)a.BH, kNormThreads, 0, stream>>>(a.BH, a.m, nchunks, L, ws,
+                                                                     ws + L.zin(), z0, z_out);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  norm_apply_kernel<<<dim3(nchunks, (unsigned)a.BH), kNormThreads, 0, stream>>>(
+      a, nchunks, L, ws, eps_attn, own_chain, z0, z_out);
   return cudaGetLastError();
 }
 

@@ -125,3 +125,32 @@ def test_normalized_split_run_equals_full_run():
         assert head_err(torch.cat([o_a, o_b], 2), o_f) < 1e-5
         assert head_err(S_b, S_f) < 1e-5
         assert head_err(z_b, z_f, 1) < 1e-5
+
+
+def test_normalized_read_many_chunks_chain_launch():
+    """71 chunks of two heads (bf16, m = d_v = 64, ragged tail): the
+    normaliser's chain runs as its own launch, and the tensor-core maps (which
+    write the denominator's per-chunk terms) run in chunk ranges."""
+    x = positive_case(1, 2, 70 * 64 + 9, 64, 64, torch.bfloat16, seed=61, carried=True)
+    o, S, z, _ = run(x, 64)
+    ref = ref_of(x)
+    assert head_err(o, ref["o"]) < 2e-2
+    assert head_err(S, ref["S"]) < 2e-2
+    assert head_err(z, ref["z"], 1) < 1e-4
+
+
+def test_normalized_read_z_out_aliases_z0():
+    """z_out given as z0's own buffer (in place) on a few-chunk call: the
+    result equals the call with separate buffers."""
+    import delta_rule_attention_gb300 as falcon
+    x = positive_case(2, 3, 5 * 64 + 11, 64, 64, torch.bfloat16, seed=62, carried=True)
+    o_ref, S_ref, z_ref, _ = run(x, 64)
+    z_buf = x["z0"].clone()
+    o, S, z, _ = falcon.falcon1a_fwd_chunked_normalized(
+        x["q"], x["k"], x["v"], x["beta"], x["lambda"], S0=x["S0"], z0=z_buf,
+        x_prev=x["x_prev"], z_out=z_buf)
+    assert falcon.falcon_sync_check() == 0
+    assert z.data_ptr() == z_buf.data_ptr()
+    assert torch.equal(z.cpu(), z_ref)
+    assert torch.equal(o.float().cpu(), o_ref)
+    assert torch.equal(S.cpu(), S_ref)
