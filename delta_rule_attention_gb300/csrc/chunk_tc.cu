@@ -235,10 +235,14 @@ constexpr int kMapThreads = 256;
 
 // 256 threads per CTA: thread t owns row r = t & 127 (its TMEM lane) and
 // columns 32h .. 32h+31 (h = t >> 7) of the CTA's 64-column half j.
-// kNorm (m = 64): the launch also writes the normalised read's per-chunk terms
-// to a.norm_ws (NormLayout): e^{g_t}, e^{g_C}, phi's scale of q_t, the
-// in-chunk read r_t = sum_{j <= t} P_tj eta_j (P's fp32 rows before they are
-// rounded for MMA3) and the increment y_C = sum_j eta_j e^{g_C - g_j} x_j.
+// kNorm (m = 64, Falcon-1A): the launch also writes the normalised read's
+// per-chunk terms to a.norm_ws (NormLayout): e^{g_t}, e^{g_C}, phi's scale of
+// q_t, the increment y_C = sum_j eta_j e^{g_C - g_j} x_j (fp32, from the raw
+// rows) and the in-chunk read r_t = sum_{j <= t} P_tj eta_j.  Falcon-1A has
+// W = 0, so MMA3's W columns carry no map: column 0 of W is set to eta, and
+// MMA3 returns r_t in column 0 of the output rows (the bf16 P and eta operands
+// of the numerator's own in-chunk term P Diag(eta) V); the Mc staging zeroes
+// that column again.
 template <int M, bool kNorm = false>
 __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
     tc_chunk_map_kernel(ChunkArgs a, int nchunks, int c_begin, int* err, uint32_t pf_ahead,
@@ -552,7 +556,6 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
       for (int cc = 0; cc < 4; ++cc)
         *reinterpret_cast<uint4*>(p_tile + sw_chunk(r - 64, 4 * h + cc)) =
             make_uint4(0u, 0u, 0u, 0u);
-      if constexpr (kNorm) sc.ssp[1][r - 64] = 0.f;  // (the half rows' sums are dead)
     } else if (!above && (r >= 64 || f1)) {
       float d[32];
       tmem_ld32(tlane + 32 * h, d);
@@ -604,21 +607,11 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
           for (int jj = 0; jj < 32; ++jj)
             d[jj] = (32 * h + jj <= i) ? __expf(fminf(gi - sc.g[32 * h + jj], 0.f)) * d[jj] : 0.f;
         }
-        if constexpr (kNorm) {
-          float rs = 0.f;
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj) rs = fmaf(d[jj], sc.eta[32 * h + jj], rs);
-          sc.ssp[h][i] = rs;
-        }
         store_half_sw(p_tile, i, h, d, 1.f);
       }
     }
   }
   if (__syncthreads_or(sc.fail)) goto teardown;  // A and P complete
-  if constexpr (kNorm) {
-    if (r >= 64 && h == 0)
-      a.norm_ws[nl.rd() + mi * kC + (r - 64)] = sc.ssp[0][r - 64] + sc.ssp[1][r - 64];
-  }
 
   // ---- T' = (I + A)^{-1} Diag(eta) into the T tile (Falcon-1A: Diag(eta), written above) ----
   if (f1) solve_unit_lower_sw<true>(a_tile, a_diag, t_tile, base + L::DB, sc.eta);
@@ -638,6 +631,12 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
   {
     float d[32];
     tmem_ld32(tlane + 32 * h, d);
+    if constexpr (kNorm) {  // column 0 of W (zero in Falcon-1A) := eta
+      if (r == 0) {
+#pragma unroll
+        for (int l = 0; l < 32; ++l) d[l] = sc.eta[32 * h + l];
+      }
+    }
     store_half_sw(wu_tile, r, h, d, 1.f);  // [W^T; U~^T] over A and T (MMA2 is complete)
   }
   if (!kWide) {
@@ -654,14 +653,13 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
   // dead decay factors; rows 0..31 add them after the next barrier.
   if constexpr (kNorm) {
     if (r < 64) {
+      // (the carried row x_1 = x_prev, fp32, holds zeros in xp: it is added below)
       const float s = sc.eta[r] * __expf(gC - sc.g[r]) * nr;
-      const float* xg = carried_fp32 ? a.x_prev + bh * M + 32 * h : nullptr;  // x_1 = x_prev
-      auto xv = [&](int i) { return carried_fp32 ? xg[i] : xp.at(i); };
       float y16[16], y8[8], y4[4], y2[2];
       const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2, b0 = lane & 1;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const float lo = xv(i) * s, hi = xv(i + 16) * s;
+        const float lo = xp.at(i) * s, hi = xp.at(i + 16) * s;
         y16[i] = (b4 ? hi : lo) + __shfl_xor_sync(0xffffffffu, b4 ? lo : hi, 16);
       }
 #pragma unroll
@@ -675,6 +673,8 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
       for (int i = 0; i < 2; ++i)
         y2[i] = (b1 ? y4[i + 2] : y4[i]) + __shfl_xor_sync(0xffffffffu, b1 ? y4[i] : y4[i + 2], 2);
       ypart = (b0 ? y2[1] : y2[0]) + __shfl_xor_sync(0xffffffffu, b0 ? y2[0] : y2[1], 1);
+      if (c == 0 && a.x_prev != nullptr && (warp & 1) == 0)
+        ypart = fmaf(sc.eta[0] * __expf(gC - sc.g[0]), a.x_prev[bh * M + 32 * h + lane], ypart);
       if (warp & 1) sc.cu[32 * h + lane] = ypart;
     }
   }
@@ -723,6 +723,12 @@ __global__ void __launch_bounds__(kMapThreads, MapLayout<M>::kMinBlocks)
       const bool lead = tid == 64 * grp;  // thread 0 and thread 64
       const uint32_t half = 8192u * (uint32_t)grp;
       tmem_ld32(tlane + 32 * h, d);
+      if constexpr (kNorm) {  // column 0: y_C (bf16 operands; not used) and r_t
+        if (h == 0) {
+          if (r >= 64) a.norm_ws[nl.rd() + mi * kC + (r - 64)] = d[0];
+          d[0] = 0.f;
+        }
+      }
       // Mc row: rows < 64 -> -Xt^T W ; rows >= 64 -> e^{g_i} phi(q_i) - P W
       const float eq = (r >= 64) ? __expf(sc.g[r - 64]) * nr : 0.f;
 #pragma unroll
@@ -1406,7 +1412,7 @@ cudaError_t launch_map(const ChunkArgs& a, int nchunks, int c_begin, int n, int*
   // The variant that also writes the normalised read's per-chunk terms (m = 64).
   auto kernel = tc_chunk_map_kernel<M, false>;
   if constexpr (M == 64) {
-    if (a.norm_ws) kernel = tc_chunk_map_kernel<64, true>;
+    if (a.norm_ws && a.rule == kFalcon1A) kernel = tc_chunk_map_kernel<64, true>;
   }
   cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
