@@ -208,8 +208,10 @@ int falcon1a_fwd_chunked(const falcon_shape *shape, const void *q,
  *   workspace: at least falcon_normalized_workspace_bytes(shape) bytes.
  * Other arguments, layouts, ownership and errors are those of
  * falcon1a_fwd_chunked (o holds the normalised read).  The call runs the
- * Falcon-1A forward and then three plain kernels for the denominator (ordinary
- * launches: they start after the forward's kernels complete). */
+ * Falcon-1A forward and then one to three plain kernels for the denominator
+ * (ordinary launches: they start after the forward's kernels complete); on the
+ * tensor-core path with m = 64 the forward's map launch also writes the
+ * denominator's per-chunk terms to the workspace. */
 size_t falcon_normalized_workspace_bytes(const falcon_shape *shape);
 int falcon1a_fwd_chunked_normalized(const falcon_shape *shape, const void *q,
                                     const void *k, const void *v,
